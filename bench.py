@@ -1,0 +1,332 @@
+#!/usr/bin/env python
+"""Benchmark of the fused attention forward + split-KV decode on GB300.
+
+One step = the whole hot path over one batch of synthetic input:
+  attn_fwd on the prefill workload (B=4, H=16, N=2048, d=128, bf16) non-causal,
+  attn_fwd on the same inputs causal, and
+  attn_decode on the decode workload (B=16, Hq=32, Hkv=8, KV cache 32768 x 128,
+  valid lengths uniform in [1024, 32768]).
+`value` is forward TFLOPS (algorithmic 4*B*H*N*N*d, halved for causal) over the
+two forward launches; the decode's HBM GB/s is reported beside it.  Inputs are
+resident in HBM; L2 is flushed (a 512 MiB write) between timed steps.
+
+`--impl reference` times the fp64 CPU oracle instead (a bounded sample of the
+same workload on the host cores).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = ("attn fwd TFLOPS & % of GB300 BF16 peak; split-KV decode HBM GB/s & % of peak")
+
+
+def read_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": p["hbm_gbs"], "bf16_tflops": p["bf16_tflops"],
+                "bf16_tflops_sustained": p.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc:
+            self.proc.terminate()
+            self.proc.wait()
+
+    def summary(self):
+        if not self.proc or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax = float(parts[2])
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        os.unlink(self.path)
+        sm.sort()
+        return {"sm_mhz": sm[len(sm) // 2] if sm else None, "sm_max_mhz": smax,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def fwd_flops(B, H, N, d, causal):
+    f = 4.0 * B * H * N * N * d
+    return f / 2 if causal else f
+
+
+def oracle_sample(seconds: float, seed: int = 1):
+    """Time the fp64 oracle on whole heads of the prefill workload (non-causal
+    and causal alternately) until `seconds` of work; returns (TFLOPS, desc, cores)."""
+    import numpy as np
+    import oracle
+    from exact_attention_14_gb300.inputs import PREFILL, make_fwd_inputs
+    cfg = PREFILL
+    q, k, v = make_fwd_inputs(1, 1, 1, cfg.N, cfg.N, cfg.d, seed=seed)
+    oracle.build()
+    flops, t0, heads = 0.0, time.perf_counter(), 0
+    while True:
+        causal = bool(heads % 2)
+        oracle.attention(q, k, v, causal=causal, scale=cfg.scale)
+        flops += fwd_flops(1, 1, cfg.N, cfg.d, causal)
+        heads += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    cores = os.cpu_count() or 1
+    desc = (f"{heads} whole heads of the prefill workload (N={cfg.N}, d={cfg.d}), "
+            f"alternating non-causal/causal, fp64 three-pass oracle, OpenMP on {cores} threads")
+    return flops / el / 1e12, desc, cores, el
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    steps = []
+    for _ in range(args.warmup):
+        oracle_sample(1.0)
+    total_flops = total_t = 0.0
+    cores = os.cpu_count() or 1
+    desc = ""
+    for _ in range(args.steps):
+        tf, desc, cores, el = oracle_sample(3.0)
+        total_flops += tf * el * 1e12
+        total_t += el
+        steps.append(el)
+    value = total_flops / total_t / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOPS",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * total_t / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "prefill fwd B=4 H=16 N=2048 d=128 (oracle sample)"},
+        "cpu_baseline": {"value": value, "unit": "TFLOPS", "cores": cores, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, rank, world, local_rank):
+    import exact_attention_14_gb300 as ea
+    from exact_attention_14_gb300.inputs import DECODE, PREFILL, make_config_inputs, \
+        make_decode_config_inputs
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    ea.load()
+    peaks = read_peaks()
+    cfg = PREFILL
+    q_h, k_h, v_h = make_config_inputs(cfg)
+    q, k, v = q_h.to(dev), k_h.to(dev), v_h.to(dev)
+    o = torch.empty(q.shape, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
+    dq, dk, dv, dsl = make_decode_config_inputs(DECODE)
+    dq, dk, dv, dsl = dq.to(dev), dk.to(dev), dv.to(dev), dsl.to(dev)
+    d_o = torch.empty(dq.shape, dtype=torch.bfloat16, device=dev)
+    d_lse = torch.empty(dq.shape[:3], dtype=torch.float32, device=dev)
+    ws = torch.empty(ea.attn_decode_workspace_size(DECODE.B, DECODE.Hq, DECODE.Hkv, DECODE.Nmax,
+                                                   DECODE.d, 0), dtype=torch.uint8, device=dev)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    sum_len = int(dsl.sum().item())
+    # algorithmic decode bytes: K and V of every valid key, Q read, O (bf16) + LSE written
+    dec_bytes = (2.0 * sum_len * DECODE.Hkv * DECODE.d * 2 + dq.numel() * 2 + d_o.numel() * 2
+                 + d_lse.numel() * 4)
+    f_nc = fwd_flops(cfg.B, cfg.Hq, cfg.N, cfg.d, False)
+    f_c = fwd_flops(cfg.B, cfg.Hq, cfg.N, cfg.d, True)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(ev=None):
+        if ev: ev[0].record(stream)
+        ea.attn_fwd(q, k, v, o, lse, causal=False, stream=stream)
+        if ev: ev[1].record(stream)
+        ea.attn_fwd(q, k, v, o, lse, causal=True, stream=stream)
+        if ev: ev[2].record(stream)
+        ea.attn_decode(dq, dk, dv, dsl, d_o, d_lse, workspace=ws, stream=stream)
+        if ev: ev[3].record(stream)
+
+    args.warmup = max(args.warmup, 3)
+    for _ in range(args.warmup):
+        step()
+        flush.zero_()
+    torch.cuda.synchronize()
+    if ea.attn_last_device_error() != 0:
+        raise RuntimeError("device error during warm-up")
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local_rank) as clk:
+        t0 = time.perf_counter()
+        for i in range(args.steps):
+            step(evs[i])
+            flush.zero_()
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t0
+    if world > 1:
+        torch.distributed.barrier()
+    if ea.attn_last_device_error() != 0:
+        raise RuntimeError("device error during the timed region")
+    t_nc = sum(e[0].elapsed_time(e[1]) for e in evs) / args.steps * 1e-3
+    t_c = sum(e[1].elapsed_time(e[2]) for e in evs) / args.steps * 1e-3
+    t_dec = sum(e[2].elapsed_time(e[3]) for e in evs) / args.steps * 1e-3
+    t_step = t_nc + t_c + t_dec
+    if world > 1:
+        tt = torch.tensor([t_nc, t_c, t_dec], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        t_nc, t_c, t_dec = tt.tolist()
+        t_step = t_nc + t_c + t_dec
+    tflops = world * (f_nc + f_c) / (t_nc + t_c) / 1e12
+    dec_gbs = world * dec_bytes / t_dec / 1e9
+
+    # end to end through the public API: pinned host inputs -> device -> result to host
+    e2e = None
+    if rank == 0 or world > 1:
+        qp, kp, vp = (t.pin_memory() for t in (q_h, k_h, v_h))
+        oh = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+        lh = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+        qd, kd, vd = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+
+        def e2e_step():
+            qd.copy_(qp, non_blocking=True)
+            kd.copy_(kp, non_blocking=True)
+            vd.copy_(vp, non_blocking=True)
+            ea.attn_fwd(qd, kd, vd, o, lse, causal=False, stream=stream)
+            oh.copy_(o, non_blocking=True)
+            lh.copy_(lse, non_blocking=True)
+            ea.attn_fwd(qd, kd, vd, o, lse, causal=True, stream=stream)
+            oh.copy_(o, non_blocking=True)
+            lh.copy_(lse, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        e1.record(stream)
+        e1.synchronize()
+        t_e2e = e0.elapsed_time(e1) / args.steps * 1e-3
+        h2d = sum(t.numel() * t.element_size() for t in (q_h, k_h, v_h))
+        d2h = 2 * (oh.numel() * oh.element_size() + lh.numel() * lh.element_size())
+        e2e = {"value": world * (f_nc + f_c) / t_e2e / 1e12, "unit": "TFLOPS",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        tf, desc, cores, _ = oracle_sample(args.cpu_seconds)
+        cpu = {"value": tf, "unit": "TFLOPS", "cores": cores, "kind": "oracle", "sample": desc}
+
+    if rank != 0:
+        return
+    fwd_time = t_nc + t_c
+    peak_t = peaks["bf16_tflops"]
+    roof = {"bound": "tensor", "kernel": "attn_fwd_kernel (non-causal + causal launches)",
+            "achieved": (f_nc + f_c) / fwd_time / 1e12, "peak": peak_t, "unit": "TFLOP/s",
+            "frac": (f_nc + f_c) / fwd_time / 1e12 / peak_t, "traffic": None,
+            "peak_source": f"{peaks['source']} bf16_tflops (burst)"}
+    roof_dec = {"bound": "hbm", "kernel": "attn_decode_split_kernel + combine",
+                "achieved": dec_bytes / t_dec / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": dec_bytes / t_dec / 1e9 / peaks["hbm_gbs"], "traffic": None,
+                "peak_source": f"{peaks['source']} hbm_gbs"}
+    line = {
+        "metric": METRIC, "value": tflops, "unit": "TFLOPS", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": "prefill fwd B=4 H=16 N=2048 d=128 (non-causal + causal) + "
+                               "decode B=16 Hq=32 Hkv=8 Nmax=32768 d=128",
+                   "global_batch": cfg.B * world, "seq_len": cfg.N,
+                   "parallelism": f"replicas x{world}", "l2": "flushed (512 MiB write) between steps"},
+        "fwd": {"noncausal_tflops": f_nc / t_nc / 1e12, "causal_tflops": f_c / t_c / 1e12,
+                "noncausal_ms": 1e3 * t_nc, "causal_ms": 1e3 * t_c,
+                "frac_of_bf16_peak": (f_nc + f_c) / fwd_time / 1e12 / peak_t},
+        "decode": {"value": dec_gbs, "unit": "GB/s", "ms": 1e3 * t_dec,
+                   "algorithmic_bytes": dec_bytes, "frac_of_hbm": dec_gbs / world / peaks["hbm_gbs"],
+                   "sum_seqlen": sum_len},
+        "roofline": roof, "roofline_decode": roof_dec,
+        "cpu_baseline": cpu, "e2e": e2e,
+        "gpu_launches": 4 * args.steps,
+        "wall_s_timed_region": wall,
+        "clocks": clk.summary(),
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if world > 1:
+        torch.distributed.init_process_group("nccl")
+    try:
+        run_ours(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

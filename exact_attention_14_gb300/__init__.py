@@ -1,1 +1,254 @@
-"""GB300 exact attention: fused forward and split-KV decode (binding filled in below)."""
+"""GB300 (sm_103a) exact attention: fused forward and split-KV decode.
+
+Thin ctypes binding over the C ABI in ``include/attn.h`` (library
+``libgb300_attn.so`` built in-tree by ``_build.build()``).  The functions here
+only marshal arguments -- shapes, data pointers and the CUDA stream -- and turn
+status codes into exceptions; every step of the computation runs in the
+library's CUDA kernels.  PyTorch supplies device memory and streams.
+
+There is no fallback: if the library is missing or was not built for this GPU,
+the first call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+__all__ = [
+    "ATTN_OUT_BF16", "ATTN_OUT_F32", "AttnError", "attn_fwd", "attn_decode",
+    "attn_decode_workspace_size", "attn_status_string", "attn_last_device_error",
+    "attn_decode_num_splits", "attn_list_schedule", "attn_kv_tiles",
+    "attn_fwd_num_units", "attn_fwd_schedule", "forward", "decode", "library_path", "load",
+]
+
+ATTN_OK = 0
+ATTN_ERR_INVALID_ARG = 1
+ATTN_ERR_UNSUPPORTED = 2
+ATTN_ERR_CUDA = 3
+ATTN_ERR_TIMEOUT = 4
+ATTN_ERR_WORKSPACE = 5
+ATTN_OUT_BF16 = 0
+ATTN_OUT_F32 = 1
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libgb300_attn.so")
+_lib = None
+
+# Every symbol the header declares, with its ctypes signature.
+_c_int, _c_ll, _c_sz, _c_f, _vp = (ctypes.c_int, ctypes.c_longlong, ctypes.c_size_t,
+                                   ctypes.c_float, ctypes.c_void_p)
+SIGNATURES = {
+    "attn_fwd": (_c_int, [_vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int,
+                          _c_int, _c_int, _c_f, _c_int, _vp]),
+    "attn_decode_workspace_size": (_c_sz, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_int]),
+    "attn_decode": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int,
+                             _c_int, _c_f, _c_int, _vp, _c_sz, _c_int, _vp]),
+    "attn_status_string": (ctypes.c_char_p, [_c_int]),
+    "attn_last_device_error": (_c_int, [_vp]),
+    "attn_decode_num_splits": (_c_int, [_c_int, _c_int, _c_int]),
+    "attn_list_schedule": (_c_ll, [ctypes.POINTER(ctypes.c_int), _c_int, _c_int, _c_int,
+                                   ctypes.POINTER(ctypes.c_longlong)]),
+    "attn_kv_tiles": (_c_int, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_int]),
+    "attn_fwd_num_units": (_c_ll, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int]),
+    "attn_fwd_schedule": (_c_int, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
+                                   _c_ll, ctypes.POINTER(ctypes.c_int),
+                                   ctypes.POINTER(ctypes.c_int)]),
+}
+
+
+class AttnError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {attn_status_string(code)} ({code})")
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load():
+    """Load the CUDA library (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(
+                f"{_LIB_PATH} is missing: build it with "
+                "`python -c 'import __graft_entry__ as g; g.build()'` "
+                "(there is no CPU fallback)")
+        lib = ctypes.CDLL(_LIB_PATH)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+    return _lib
+
+
+def attn_status_string(code: int) -> str:
+    return load().attn_status_string(int(code)).decode()
+
+
+def _check(code: int, where: str):
+    if code != ATTN_OK:
+        raise AttnError(code, where)
+
+
+def _stream_ptr(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _need(t, dtype, name):
+    import torch
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def attn_fwd(q, k, v, o, lse=None, *, causal: bool = False, scale: float | None = None,
+             stream=None):
+    """Fused forward into caller-provided outputs.
+
+    q [B,Hq,Nq,d] bf16; k, v [B,Hkv,Nk,d] bf16; o [B,Hq,Nq,d] bf16 or fp32;
+    lse [B,Hq,Nq] fp32 or None.  Asynchronous on ``stream`` (default: the
+    current torch stream)."""
+    import torch
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, torch.bfloat16, n)
+    if o.dtype not in (torch.bfloat16, torch.float32):
+        raise TypeError("o must be bfloat16 or float32")
+    _need(o, o.dtype, "o")
+    if lse is not None:
+        _need(lse, torch.float32, "lse")
+    B, Hq, Nq, d = q.shape
+    Hkv, Nk = k.shape[1], k.shape[2]
+    if tuple(k.shape) != (B, Hkv, Nk, d) or tuple(v.shape) != tuple(k.shape):
+        raise ValueError("k/v shape mismatch")
+    if tuple(o.shape) != (B, Hq, Nq, d):
+        raise ValueError("o shape mismatch")
+    if lse is not None and tuple(lse.shape) != (B, Hq, Nq):
+        raise ValueError("lse shape mismatch")
+    if scale is None:
+        scale = d ** -0.5
+    odt = ATTN_OUT_F32 if o.dtype == torch.float32 else ATTN_OUT_BF16
+    rc = load().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, Nq, Nk, d,
+                         int(bool(causal)), float(scale), odt, _stream_ptr(stream))
+    _check(rc, "attn_fwd")
+    return o, lse
+
+
+def forward(q, k, v, *, causal: bool = False, scale: float | None = None,
+            out_dtype=None, return_lse: bool = True, stream=None):
+    """Allocate O (and LSE) with torch and run attn_fwd."""
+    import torch
+    out_dtype = out_dtype or torch.bfloat16
+    o = torch.empty(q.shape, dtype=out_dtype, device=q.device)
+    lse = (torch.empty(q.shape[:3], dtype=torch.float32, device=q.device)
+           if return_lse else None)
+    return attn_fwd(q, k, v, o, lse, causal=causal, scale=scale, stream=stream)
+
+
+def attn_decode_workspace_size(B: int, Hq: int, Hkv: int, Nmax: int, d: int,
+                               num_splits: int = 0) -> int:
+    return int(load().attn_decode_workspace_size(B, Hq, Hkv, Nmax, d, num_splits))
+
+
+def attn_decode(q, k_cache, v_cache, seqlens, o, lse=None, *, scale: float | None = None,
+                num_splits: int = 0, workspace=None, stream=None):
+    """Split-KV decode into caller-provided outputs.
+
+    q [B,Hq,1,d] bf16; caches [B,Hkv,Nmax,d] bf16; seqlens [B] int32 (device);
+    o [B,Hq,1,d] bf16/fp32; lse [B,Hq,1] fp32 or None; workspace: a uint8
+    CUDA tensor of at least attn_decode_workspace_size(...) bytes."""
+    import torch
+    for t, n in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache")):
+        _need(t, torch.bfloat16, n)
+    _need(seqlens, torch.int32, "seqlens")
+    if o.dtype not in (torch.bfloat16, torch.float32):
+        raise TypeError("o must be bfloat16 or float32")
+    _need(o, o.dtype, "o")
+    if lse is not None:
+        _need(lse, torch.float32, "lse")
+    B, Hq, one, d = q.shape
+    Hkv, Nmax = k_cache.shape[1], k_cache.shape[2]
+    if one != 1 or tuple(k_cache.shape) != (B, Hkv, Nmax, d) or v_cache.shape != k_cache.shape:
+        raise ValueError("decode shape mismatch")
+    if tuple(o.shape) != (B, Hq, 1, d) or tuple(seqlens.shape) != (B,):
+        raise ValueError("decode output/seqlens shape mismatch")
+    if scale is None:
+        scale = d ** -0.5
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
+        _need(workspace, workspace.dtype, "workspace")
+        ws_ptr, ws_bytes = _ptr(workspace), workspace.numel() * workspace.element_size()
+    odt = ATTN_OUT_F32 if o.dtype == torch.float32 else ATTN_OUT_BF16
+    rc = load().attn_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(seqlens), _ptr(o),
+                            _ptr(lse), B, Hq, Hkv, Nmax, d, float(scale), int(num_splits),
+                            ws_ptr, ws_bytes, odt, _stream_ptr(stream))
+    _check(rc, "attn_decode")
+    return o, lse
+
+
+def decode(q, k_cache, v_cache, seqlens, *, scale=None, num_splits: int = 0,
+           out_dtype=None, stream=None):
+    """Allocate O, LSE and the workspace with torch and run attn_decode."""
+    import torch
+    out_dtype = out_dtype or torch.bfloat16
+    B, Hq, _, d = q.shape
+    Hkv, Nmax = k_cache.shape[1], k_cache.shape[2]
+    ws = torch.empty(attn_decode_workspace_size(B, Hq, Hkv, Nmax, d, num_splits),
+                     dtype=torch.uint8, device=q.device)
+    o = torch.empty((B, Hq, 1, d), dtype=out_dtype, device=q.device)
+    lse = torch.empty((B, Hq, 1), dtype=torch.float32, device=q.device)
+    return attn_decode(q, k_cache, v_cache, seqlens, o, lse, scale=scale,
+                       num_splits=num_splits, workspace=ws, stream=stream)
+
+
+def attn_last_device_error(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the device error status."""
+    return int(load().attn_last_device_error(_stream_ptr(stream)))
+
+
+# ------------------------- host-side scheduling logic -------------------------
+def attn_decode_num_splits(units: int, num_sms: int, max_splits: int = 128) -> int:
+    return int(load().attn_decode_num_splits(units, num_sms, max_splits))
+
+
+def attn_list_schedule(costs, workers: int, lpt: bool):
+    """Returns (makespan, per-worker loads)."""
+    n = len(costs)
+    arr = (ctypes.c_int * max(n, 1))(*[int(c) for c in costs])
+    loads = (ctypes.c_longlong * workers)()
+    mk = load().attn_list_schedule(arr, n, workers, int(bool(lpt)), loads)
+    if mk < 0:
+        raise ValueError("attn_list_schedule rejected its arguments")
+    return int(mk), [int(x) for x in loads]
+
+
+def attn_kv_tiles(row0: int, rows: int, Nq: int, Nk: int, causal: bool, block: int) -> int:
+    return int(load().attn_kv_tiles(row0, rows, Nq, Nk, int(bool(causal)), block))
+
+
+def attn_fwd_num_units(B, Hq, Hkv, Nq, Nk, d, causal) -> int:
+    return int(load().attn_fwd_num_units(B, Hq, Hkv, Nq, Nk, d, int(bool(causal))))
+
+
+def attn_fwd_schedule(B, Hq, Hkv, Nq, Nk, d, causal):
+    """Returns ([(b, hq, m_block), ...] in walk order, [cost, ...])."""
+    n = attn_fwd_num_units(B, Hq, Hkv, Nq, Nk, d, causal)
+    units = (ctypes.c_int * (3 * n))()
+    costs = (ctypes.c_int * n)()
+    rc = load().attn_fwd_schedule(B, Hq, Hkv, Nq, Nk, d, int(bool(causal)), n, units, costs)
+    if rc != 0:
+        raise ValueError("attn_fwd_schedule rejected its arguments")
+    return [tuple(units[3 * i:3 * i + 3]) for i in range(n)], list(costs)

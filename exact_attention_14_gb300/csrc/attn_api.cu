@@ -1,0 +1,278 @@
+// attn_api.cu -- the C ABI: argument checks, per-device state, tensor-map
+// encoding, dispatch to the kernels, status reporting, and the host-side
+// scheduling exports declared in attn.h.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <numeric>
+#include <vector>
+
+#include "internal.h"
+#include "ptx.cuh"
+#include "fwd_sched.h"
+
+namespace gb300 {
+
+// The library's device error word (one per device/context).  Kernels OR
+// error bits into it; attn_last_device_error() reads and clears it.
+__device__ unsigned int g_attn_error_word;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr long long kMaxLen = 1ll << 24;
+constexpr long long kMaxHeads = 1ll << 24;
+
+struct DevState {
+    bool ready;
+    int num_sms;
+    unsigned int* err_word;
+};
+
+std::mutex g_mu;
+DevState g_dev[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+}  // namespace
+
+attn_status_t current_device_info(DeviceInfo* out) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return ATTN_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lk(g_mu);
+    DevState& s = g_dev[dev];
+    if (!s.ready) {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return ATTN_ERR_CUDA;
+        if (major != 10 || minor != 3) return ATTN_ERR_UNSUPPORTED;  // built for sm_103a only
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_attn_error_word) != cudaSuccess) return ATTN_ERR_CUDA;
+        s.num_sms = sms;
+        s.err_word = static_cast<unsigned int*>(p);
+        s.ready = true;
+    }
+    out->device = dev;
+    out->num_sms = s.num_sms;
+    out->err_word = s.err_word;
+    return ATTN_OK;
+}
+
+attn_status_t encode_tmap_bf16_3d(CUtensorMap* map, const void* base, int d, int rows,
+                                  long long heads, int box_rows) {
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        if (!g_encode) {
+            void* fn = nullptr;
+            cudaDriverEntryPointQueryResult q;
+            if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                 cudaEnableDefault, &q) != cudaSuccess ||
+                q != cudaDriverEntryPointSuccess || !fn)
+                return ATTN_ERR_CUDA;
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+        }
+    }
+    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)rows, (cuuint64_t)heads};
+    cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)d * 2 * (cuuint64_t)rows};
+    cuuint32_t box[3] = {64u, (cuuint32_t)box_rows, 1u};
+    cuuint32_t elem[3] = {1u, 1u, 1u};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+                          strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+}  // namespace gb300
+
+using namespace gb300;
+
+namespace {
+
+attn_status_t check_common(int B, int Hq, int Hkv, int d, float scale, attn_out_dtype_t o_dtype) {
+    if (B < 1 || Hq < 1 || Hkv < 1 || d < 1) return ATTN_ERR_INVALID_ARG;
+    if (Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
+    if ((long long)B * Hq > kMaxHeads || (long long)B * Hkv > kMaxHeads) return ATTN_ERR_INVALID_ARG;
+    if (!(scale >= 0.0f) || !std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+    if (o_dtype != ATTN_OUT_BF16 && o_dtype != ATTN_OUT_F32) return ATTN_ERR_INVALID_ARG;
+    return ATTN_OK;
+}
+
+attn_status_t check_fwd(const void* q, const void* k, const void* v, const void* o,
+                        const float* lse, int B, int Hq, int Hkv, int Nq, int Nk, int d,
+                        int causal, float scale, attn_out_dtype_t o_dtype) {
+    if (!q || !k || !v || !o) return ATTN_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return ATTN_ERR_INVALID_ARG;
+    if (lse && !aligned4(lse)) return ATTN_ERR_INVALID_ARG;
+    attn_status_t st = check_common(B, Hq, Hkv, d, scale, o_dtype);
+    if (st != ATTN_OK) return st;
+    if (Nq < 1 || Nk < 1 || Nq > kMaxLen || Nk > kMaxLen) return ATTN_ERR_INVALID_ARG;
+    if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
+    if (causal && Nq > Nk) return ATTN_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+    return ATTN_OK;
+}
+
+attn_status_t check_decode_shape(int B, int Hq, int Hkv, int Nmax, int d, int num_splits) {
+    if (B < 1 || Hq < 1 || Hkv < 1 || d < 1) return ATTN_ERR_INVALID_ARG;
+    if (Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
+    if ((long long)B * Hq > kMaxHeads || (long long)B * Hkv > kMaxHeads) return ATTN_ERR_INVALID_ARG;
+    if (Nmax < 1 || Nmax > kMaxLen) return ATTN_ERR_INVALID_ARG;
+    if (num_splits < 0) return ATTN_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+    if (Hq / Hkv > 16) return ATTN_ERR_UNSUPPORTED;
+    return ATTN_OK;
+}
+
+// SM count used by the automatic split rule when no device is queried (host
+// exports): the device's own count is used for real launches.
+int decode_sms_or_default(int* sms) {
+    DeviceInfo dev;
+    if (current_device_info(&dev) == ATTN_OK) {
+        *sms = dev.num_sms;
+        return 0;
+    }
+    return -1;
+}
+
+}  // namespace
+
+extern "C" {
+
+attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                       int Hq, int Hkv, int Nq, int Nk, int d, int causal, float scale,
+                       attn_out_dtype_t o_dtype, void* stream) {
+    attn_status_t st = check_fwd(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, d, causal, scale, o_dtype);
+    if (st != ATTN_OK) return st;
+    DeviceInfo dev;
+    if ((st = current_device_info(&dev)) != ATTN_OK) return st;
+    return launch_fwd(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, d, causal, scale, o_dtype,
+                      static_cast<cudaStream_t>(stream), dev);
+}
+
+size_t attn_decode_workspace_size(int B, int Hq, int Hkv, int Nmax, int d, int num_splits) {
+    if (check_decode_shape(B, Hq, Hkv, Nmax, d, num_splits) != ATTN_OK) return 0;
+    int sms = 0;
+    if (decode_sms_or_default(&sms) != 0) return 0;
+    const int chunk = decode_chunk(Nmax, B, Hkv, sms, num_splits);
+    return decode_workspace_bytes(B, Hq, Nmax, d, chunk);
+}
+
+attn_status_t attn_decode(const void* q, const void* k_cache, const void* v_cache,
+                          const int* seqlens, void* o, float* lse, int B, int Hq, int Hkv,
+                          int Nmax, int d, float scale, int num_splits, void* workspace,
+                          size_t workspace_bytes, attn_out_dtype_t o_dtype, void* stream) {
+    if (!q || !k_cache || !v_cache || !seqlens || !o) return ATTN_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o) ||
+        !aligned4(seqlens))
+        return ATTN_ERR_INVALID_ARG;
+    if (lse && !aligned4(lse)) return ATTN_ERR_INVALID_ARG;
+    attn_status_t st = check_common(B, Hq, Hkv, d, scale, o_dtype);
+    if (st != ATTN_OK) return st;
+    if ((st = check_decode_shape(B, Hq, Hkv, Nmax, d, num_splits)) != ATTN_OK) return st;
+    DeviceInfo dev;
+    if ((st = current_device_info(&dev)) != ATTN_OK) return st;
+    const int chunk = decode_chunk(Nmax, B, Hkv, dev.num_sms, num_splits);
+    const size_t need = decode_workspace_bytes(B, Hq, Nmax, d, chunk);
+    if (!workspace || workspace_bytes < need || !aligned16(workspace)) return ATTN_ERR_WORKSPACE;
+    return launch_decode(q, k_cache, v_cache, seqlens, o, lse, B, Hq, Hkv, Nmax, d, scale, chunk,
+                         workspace, o_dtype, static_cast<cudaStream_t>(stream), dev);
+}
+
+const char* attn_status_string(attn_status_t s) {
+    switch (s) {
+        case ATTN_OK: return "ATTN_OK";
+        case ATTN_ERR_INVALID_ARG: return "ATTN_ERR_INVALID_ARG";
+        case ATTN_ERR_UNSUPPORTED: return "ATTN_ERR_UNSUPPORTED";
+        case ATTN_ERR_CUDA: return "ATTN_ERR_CUDA";
+        case ATTN_ERR_TIMEOUT: return "ATTN_ERR_TIMEOUT";
+        case ATTN_ERR_WORKSPACE: return "ATTN_ERR_WORKSPACE";
+    }
+    return "ATTN_ERR_UNKNOWN";
+}
+
+attn_status_t attn_last_device_error(void* stream) {
+    DeviceInfo dev;
+    attn_status_t st = current_device_info(&dev);
+    if (st != ATTN_OK) return st;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return ATTN_ERR_CUDA;
+    unsigned int word = 0;
+    if (cudaMemcpy(&word, dev.err_word, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess)
+        return ATTN_ERR_CUDA;
+    const unsigned int zero = 0;
+    if (word != 0 && cudaMemcpy(dev.err_word, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess)
+        return ATTN_ERR_CUDA;
+    if (word & kErrTimeout) return ATTN_ERR_TIMEOUT;
+    if (word & kErrBadSeqlen) return ATTN_ERR_INVALID_ARG;
+    return ATTN_OK;
+}
+
+int attn_decode_num_splits(int units, int num_sms, int max_splits) {
+    if (units < 1 || num_sms < 1 || max_splits < 1) return 0;
+    std::vector<double> eff((size_t)max_splits + 1, 0.0);
+    double best = 0.0;
+    for (int s = 1; s <= max_splits; ++s) {
+        const double waves = (double)units * s / num_sms;
+        eff[s] = waves / std::ceil(waves);
+        best = std::max(best, eff[s]);
+    }
+    for (int s = 1; s <= max_splits; ++s)
+        if (eff[s] >= 0.85 * best) return s;
+    return 1;
+}
+
+long long attn_list_schedule(const int* costs, int n, int workers, int lpt, long long* loads_out) {
+    if (n < 0 || workers < 1 || (n > 0 && !costs)) return -1;
+    std::vector<int> order((size_t)n);
+    std::iota(order.begin(), order.end(), 0);
+    if (lpt)
+        std::stable_sort(order.begin(), order.end(),
+                         [&](int a, int b) { return costs[a] > costs[b]; });
+    std::vector<long long> load((size_t)workers, 0);
+    for (int idx : order) {
+        if (costs[idx] < 0) return -1;
+        int w = 0;
+        for (int i = 1; i < workers; ++i)
+            if (load[i] < load[w]) w = i;
+        load[w] += costs[idx];
+    }
+    if (loads_out) std::copy(load.begin(), load.end(), loads_out);
+    return workers ? *std::max_element(load.begin(), load.end()) : 0;
+}
+
+int attn_kv_tiles(int row0, int rows, int Nq, int Nk, int causal, int block) {
+    return kv_tiles_for_rows(row0, rows, Nq, Nk, causal, block);
+}
+
+long long attn_fwd_num_units(int B, int Hq, int Hkv, int Nq, int Nk, int d, int causal) {
+    if (B < 1 || Hq < 1 || Hkv < 1 || Nq < 1 || Nk < 1 || d < 1 || Hq % Hkv) return -1;
+    return make_fwd_shape(B, Hq, Hkv, Nq, Nk, d, causal).units;
+}
+
+int attn_fwd_schedule(int B, int Hq, int Hkv, int Nq, int Nk, int d, int causal, long long n,
+                      int* units_out, int* cost_out) {
+    if (B < 1 || Hq < 1 || Hkv < 1 || Nq < 1 || Nk < 1 || d < 1 || Hq % Hkv || !units_out)
+        return -1;
+    const FwdShape s = make_fwd_shape(B, Hq, Hkv, Nq, Nk, d, causal);
+    if (n != s.units) return -1;
+    for (long long i = 0; i < n; ++i) {
+        int bh, mb;
+        unit_of(s, i, bh, mb);
+        units_out[3 * i] = bh / Hq;
+        units_out[3 * i + 1] = bh % Hq;
+        units_out[3 * i + 2] = mb;
+        if (cost_out) cost_out[i] = tile_kv_count(mb, 0, s) + tile_kv_count(mb, 1, s);
+    }
+    return 0;
+}
+
+}  // extern "C"

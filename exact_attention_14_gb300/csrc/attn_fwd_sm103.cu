@@ -1,0 +1,501 @@
+// attn_fwd_sm103.cu -- fused exact attention forward for sm_103a.
+//
+// One persistent CTA per SM walks the unit list of fwd_sched.h.  A unit is two
+// 128-row Q tiles of one (batch, query head); both tiles stream the same K/V
+// tiles.  Roles (12 warps):
+//   warp 0      TMA producer: Q tiles once per unit, then K_j, V_j into a
+//               ring of shared-memory slots (128-byte swizzle, mbarrier
+//               full/empty pairs).
+//   warp 1      MMA issuer (one thread): S_t = Q_t K_j^T and O_t += P_t V_j
+//               on the 5th-generation tensor cores, accumulating in TMEM.
+//   warps 4-7   softmax for Q tile 0, warps 8-11 for Q tile 1: one thread
+//               per query row reads its S row from TMEM, applies the causal
+//               / tail mask, keeps the running max m and sum l (base 2,
+//               conditional rescaling with threshold tau = 8), writes P as
+//               bf16 into TMEM over its S columns, and at the end of the
+//               unit normalises O by 1/l and writes O and the logsumexp.
+//               Two row sums are kept: l over the bf16-rounded P that
+//               multiplies V (so O's weights sum to exactly one) and lx over
+//               the unrounded P (the softmax denominator the LSE needs).
+//   warps 2-3   idle.
+// While one tile's softmax runs, the tensor cores work on the other tile
+// (two-tile ping-pong), so exp and MMA overlap.
+//
+// Method: lecture notes "Optimizing Attention for Modern Hardware:
+// FlashAttention 1-4" -- 2.2 online softmax and rescaling, 2.5 causal block
+// skipping with an in-tile mask from global indices, 2.6 / 3.2 delayed
+// normalisation and the logsumexp output, 4.5 persistent kernel, 5.3
+// conditional rescaling (tau = 8 in base 2, whole-warp decision); "Flash
+// Attention 3/4 notes", FA4 section 1 (two Q tiles per CTA, P through TMEM,
+// 128-row tiles).
+//
+// TMEM columns (512 allocated): S0 [0,128) S1 [128,256) O0 [256,256+D)
+// O1 [256+D, 256+2D).  P_t (bf16 pairs) overwrites S_t columns [0, 64).
+#include <cmath>
+#include <cstdint>
+
+#include "internal.h"
+#include "ptx.cuh"
+#include "fwd_sched.h"
+
+namespace gb300 {
+namespace {
+
+constexpr int kThreads = 384;
+constexpr float kTau = 8.0f;                    // rescale threshold (log2 units)
+constexpr float kLn2 = 0.69314718055994530942f;
+constexpr float kLog2e = 1.44269504088896340736f;
+constexpr uint32_t kNegInfBits = 0xFF800000u;
+
+template <int D>
+struct FwdCfg {
+    static constexpr int kTileBytes = 128 * D * 2;        // one 128-row bf16 tile
+    static constexpr int kStages = (D == 128) ? 4 : 8;     // K/V ring slots
+    static constexpr int kRingOff = 2 * kTileBytes;        // after Q0, Q1
+    static constexpr int kBarOff = kRingOff + kStages * kTileBytes;
+    static constexpr int kSmemBytes = kBarOff + 256 + 1024;  // barriers + alignment slack
+    // TMEM column of S_t and of O_t
+    static __host__ __device__ constexpr uint32_t col_s(int t) { return uint32_t(t) * 128u; }
+    static __host__ __device__ constexpr uint32_t col_o(int t) { return 256u + uint32_t(t) * D; }
+};
+
+struct FwdParams {
+    FwdShape shape;
+    int group;      // Hq / Hkv
+    int off;        // Nk - Nq (causal alignment)
+    float c;        // scale * log2(e)
+};
+
+struct __align__(8) Bars {
+    uint64_t q_full[2], q_empty[2];
+    uint64_t kv_full[8], kv_empty[8];
+    uint64_t s_full[2], p_full[2], o_full[2];
+    uint64_t drain;
+    uint32_t tmem_base;
+    int abort;
+};
+
+__device__ __forceinline__ void raise_abort(Bars* bars, unsigned int* err) {
+    atomicOr(err, kErrTimeout);
+    *((volatile int*)&bars->abort) = 1;
+}
+
+// ---------------------------------------------------------------------------
+// Producer: TMA loads
+// ---------------------------------------------------------------------------
+template <int D>
+__device__ void run_producer(const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv,
+                             uint8_t* smem, Bars* bars, const FwdParams& p, unsigned int* err) {
+    using C = FwdCfg<D>;
+    const volatile int* abort_flag = &bars->abort;
+    const FwdShape& s = p.shape;
+    uint32_t q_issued[2] = {0u, 0u};
+    long long L = 0;  // K/V loads issued
+    int local = 0;
+    bool ok = true;
+    for (long long u = blockIdx.x; u < s.units && ok; u += gridDim.x, ++local) {
+        int bh, mb;
+        unit_of(s, u, bh, mb);
+        const int b = bh / s.Hq;
+        const int hq = bh - b * s.Hq;
+        const int bkv = b * s.Hkv + hq / p.group;
+        const int n0 = tile_kv_count(mb, 0, s), n1 = tile_kv_count(mb, 1, s);
+        const int nmax = n0 > n1 ? n0 : n1;
+        for (int t = 0; t < 2 && ok; ++t) {
+            if (local > 0) ok = mbar_wait(smem_u32(&bars->q_empty[t]), (local - 1) & 1, abort_flag);
+            if (!ok) break;
+            const uint32_t bar = smem_u32(&bars->q_full[t]);
+            mbar_arrive_expect_tx(bar, C::kTileBytes);
+            const uint32_t dst = smem_u32(smem + t * C::kTileBytes);
+#pragma unroll
+            for (int c = 0; c < D / 64; ++c)
+                tma_load_3d(dst + c * 16384, tq, bar, 64 * c, mb * kUnitRows + t * kTileM, bh);
+            ++q_issued[t];
+        }
+        for (int j = 0; j < nmax && ok; ++j) {
+#pragma unroll 1
+            for (int which = 0; which < 2; ++which) {
+                const int slot = (int)(L % C::kStages);
+                const long long round = L / C::kStages;
+                if (round > 0) ok = mbar_wait(smem_u32(&bars->kv_empty[slot]), (uint32_t)((round - 1) & 1), abort_flag);
+                if (!ok) break;
+                const uint32_t bar = smem_u32(&bars->kv_full[slot]);
+                mbar_arrive_expect_tx(bar, C::kTileBytes);
+                const uint32_t dst = smem_u32(smem + C::kRingOff + slot * C::kTileBytes);
+                const CUtensorMap* map = which == 0 ? tk : tv;
+#pragma unroll
+                for (int c = 0; c < D / 64; ++c) tma_load_3d(dst + c * 16384, map, bar, 64 * c, kTileN * j, bkv);
+                ++L;
+            }
+        }
+    }
+    if (!ok) raise_abort(bars, err);
+    // Drain: every issued copy lands before the CTA may exit.
+    for (int t = 0; t < 2; ++t)
+        if (q_issued[t] > 0) mbar_wait(smem_u32(&bars->q_full[t]), (q_issued[t] - 1) & 1, nullptr);
+    for (int slot = 0; slot < C::kStages && slot < L; ++slot) {
+        const long long n_s = (L - slot + C::kStages - 1) / C::kStages;
+        mbar_wait(smem_u32(&bars->kv_full[slot]), (uint32_t)((n_s - 1) & 1), nullptr);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// MMA issuer (single thread)
+// ---------------------------------------------------------------------------
+template <int D>
+__device__ __forceinline__ void issue_qk(uint32_t tmem, int t, uint32_t q_base, uint32_t k_base,
+                                         uint32_t idesc) {
+    using C = FwdCfg<D>;
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+        mma_ss(tmem + C::col_s(t), make_sdesc_sw128(q_base + off, 16, 1024),
+               make_sdesc_sw128(k_base + off, 16, 1024), idesc, kk > 0 ? 1u : 0u);
+    }
+}
+
+template <int D>
+__device__ __forceinline__ void issue_pv(uint32_t tmem, int t, uint32_t v_base, uint32_t idesc,
+                                         bool accumulate) {
+    using C = FwdCfg<D>;
+#pragma unroll
+    for (int kk = 0; kk < kTileN / 16; ++kk) {
+        mma_ts(tmem + C::col_o(t), tmem + C::col_s(t) + kk * 8,
+               make_sdesc_sw128(v_base + kk * 2048, 16384, 1024), idesc,
+               (accumulate || kk > 0) ? 1u : 0u);
+    }
+}
+
+template <int D>
+__device__ void run_mma(uint8_t* smem, Bars* bars, uint32_t tmem, const FwdParams& p,
+                        unsigned int* err) {
+    using C = FwdCfg<D>;
+    const volatile int* abort_flag = &bars->abort;
+    const FwdShape& s = p.shape;
+    const uint32_t idS = make_idesc_bf16(128, kTileN, 0, 0);
+    const uint32_t idO = make_idesc_bf16(128, D, 0, 1);
+    const uint32_t q_base[2] = {smem_u32(smem), smem_u32(smem + C::kTileBytes)};
+    const uint32_t ring = smem_u32(smem + C::kRingOff);
+    long long Cn = 0;  // K/V loads consumed
+    uint32_t cnt_p[2] = {0u, 0u};
+    int local = 0;
+    bool ok = true;
+    for (long long u = blockIdx.x; u < s.units && ok; u += gridDim.x, ++local) {
+        int bh, mb;
+        unit_of(s, u, bh, mb);
+        const int n[2] = {tile_kv_count(mb, 0, s), tile_kv_count(mb, 1, s)};
+        const int nmax = n[0] > n[1] ? n[0] : n[1];
+        for (int t = 0; t < 2 && ok; ++t) ok = mbar_wait(smem_u32(&bars->q_full[t]), local & 1, abort_flag);
+        if (!ok) break;
+        // K_0 -> S_t(0)
+        int slot_k = (int)(Cn % C::kStages);
+        ok = mbar_wait(smem_u32(&bars->kv_full[slot_k]), (uint32_t)((Cn / C::kStages) & 1), abort_flag);
+        ++Cn;
+        if (!ok) break;
+        tc_fence_after();
+        for (int t = 0; t < 2; ++t) {
+            if (n[t] > 0) {
+                issue_qk<D>(tmem, t, q_base[t], ring + slot_k * C::kTileBytes, idS);
+                mma_commit(smem_u32(&bars->s_full[t]));
+            }
+            if (n[t] <= 1) mma_commit(smem_u32(&bars->q_empty[t]));
+        }
+        mma_commit(smem_u32(&bars->kv_empty[slot_k]));
+        for (int j = 0; j < nmax && ok; ++j) {
+            const int slot_v = (int)(Cn % C::kStages);
+            ok = mbar_wait(smem_u32(&bars->kv_full[slot_v]), (uint32_t)((Cn / C::kStages) & 1), abort_flag);
+            ++Cn;
+            const bool more = j + 1 < nmax;
+            if (ok && more) {
+                slot_k = (int)(Cn % C::kStages);
+                ok = mbar_wait(smem_u32(&bars->kv_full[slot_k]), (uint32_t)((Cn / C::kStages) & 1), abort_flag);
+                ++Cn;
+            }
+            if (!ok) break;
+            tc_fence_after();
+            for (int t = 0; t < 2 && ok; ++t) {
+                if (j >= n[t]) continue;
+                ok = mbar_wait(smem_u32(&bars->p_full[t]), cnt_p[t] & 1, abort_flag);
+                ++cnt_p[t];
+                if (!ok) break;
+                tc_fence_after();
+                issue_pv<D>(tmem, t, ring + slot_v * C::kTileBytes, idO, j > 0);
+                if (j + 1 < n[t]) {
+                    // Issued after PV_t(j): the tensor pipe runs this CTA's MMAs in
+                    // order, so S_t(j+1) overwrites P_t(j) only once PV_t(j) has read it.
+                    issue_qk<D>(tmem, t, q_base[t], ring + slot_k * C::kTileBytes, idS);
+                    mma_commit(smem_u32(&bars->s_full[t]));
+                    if (j + 2 == n[t]) mma_commit(smem_u32(&bars->q_empty[t]));
+                } else {
+                    mma_commit(smem_u32(&bars->o_full[t]));
+                }
+            }
+            if (!ok) break;
+            mma_commit(smem_u32(&bars->kv_empty[slot_v]));
+            if (more) mma_commit(smem_u32(&bars->kv_empty[slot_k]));
+        }
+    }
+    if (!ok) raise_abort(bars, err);
+    // Drain: all issued MMAs complete before TMEM is released.
+    mma_commit(smem_u32(&bars->drain));
+    mbar_wait(smem_u32(&bars->drain), 0, nullptr);
+}
+
+// ---------------------------------------------------------------------------
+// Softmax / correction / epilogue warpgroup (one thread per query row)
+// ---------------------------------------------------------------------------
+template <int D, bool OUT_F32>
+__device__ void run_softmax(int t, int wq, int lane, Bars* bars, uint32_t tmem, const FwdParams& p,
+                            void* __restrict__ o_ptr, float* __restrict__ lse_ptr,
+                            unsigned int* err) {
+    using C = FwdCfg<D>;
+    const volatile int* abort_flag = &bars->abort;
+    const FwdShape& s = p.shape;
+    const uint32_t lane_off = uint32_t(wq * 32) << 16;
+    const uint32_t tS = tmem + C::col_s(t) + lane_off;
+    const uint32_t tO = tmem + C::col_o(t) + lane_off;
+    const uint32_t bar_s = smem_u32(&bars->s_full[t]);
+    const uint32_t bar_p = smem_u32(&bars->p_full[t]);
+    const uint32_t bar_o = smem_u32(&bars->o_full[t]);
+    const float c = p.c;
+    uint32_t cnt_s = 0, cnt_o = 0;
+    bool ok = true;
+    for (long long u = blockIdx.x; u < s.units && ok; u += gridDim.x) {
+        int bh, mb;
+        unit_of(s, u, bh, mb);
+        const int n_t = tile_kv_count(mb, t, s);
+        if (n_t == 0) continue;
+        const int row = mb * kUnitRows + t * kTileM + wq * 32 + lane;
+        // last allowed key for this row (global index)
+        int last_key = s.Nk - 1;
+        if (s.causal) {
+            const int lk = row + p.off;
+            last_key = lk < last_key ? lk : last_key;
+        }
+        float m = -INFINITY;  // running max of scaled scores, log2 units
+        float l = 0.f;        // running sum of the bf16-rounded probabilities (normalises O)
+        float lx = 0.f;       // running sum of the unrounded probabilities (gives the LSE)
+        for (int j = 0; j < n_t; ++j) {
+            ok = mbar_wait(bar_s, cnt_s & 1, abort_flag);
+            ++cnt_s;
+            if (!ok) break;
+            tc_fence_after();
+            uint32_t sr[128];
+            tmem_ld32(tS + 0, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+            tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+            tmem_ld32(tS + 64, *reinterpret_cast<uint32_t(*)[32]>(&sr[64]));
+            tmem_ld32(tS + 96, *reinterpret_cast<uint32_t(*)[32]>(&sr[96]));
+            tmem_wait_ld();
+            const int lim = last_key - j * kTileN;  // column c allowed iff c <= lim
+            const bool masked_tile = __any_sync(0xFFFFFFFFu, lim < kTileN - 1);
+            if (masked_tile) {
+#pragma unroll
+                for (int cc = 0; cc < 128; ++cc)
+                    if (cc > lim) sr[cc] = kNegInfBits;
+            }
+            float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+#pragma unroll
+            for (int cc = 0; cc < 128; cc += 4) {
+                mx0 = fmaxf(mx0, __uint_as_float(sr[cc]));
+                mx1 = fmaxf(mx1, __uint_as_float(sr[cc + 1]));
+                mx2 = fmaxf(mx2, __uint_as_float(sr[cc + 2]));
+                mx3 = fmaxf(mx3, __uint_as_float(sr[cc + 3]));
+            }
+            const float mt = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * c;
+            const bool need = mt > m + kTau;
+            if (__any_sync(0xFFFFFFFFu, need)) {
+                const float m_new = fmaxf(m, mt);
+                const float alpha = ex2(m - m_new);
+                l *= alpha;
+                lx *= alpha;
+                if (j > 0) {
+                    // O_t is stable here: S_t(j) completing implies PV_t(j-1) completed.
+#pragma unroll 1
+                    for (int cc = 0; cc < D; cc += 32) {
+                        uint32_t r[32];
+                        tmem_ld32(tO + cc, r);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+                        tmem_st32(tO + cc, r);
+                    }
+                }
+                m = m_new;
+            }
+            const float neg_m = -m;
+            float la = 0.f, lb = 0.f, lc = 0.f, ld = 0.f, xa = 0.f, xb = 0.f;
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) {
+                uint32_t pk[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const int col = cc * 32 + 2 * i;
+                    float p0 = ex2(fmaf(__uint_as_float(sr[col]), c, neg_m));
+                    float p1 = ex2(fmaf(__uint_as_float(sr[col + 1]), c, neg_m));
+                    if (masked_tile) {
+                        p0 = col <= lim ? p0 : 0.f;
+                        p1 = col + 1 <= lim ? p1 : 0.f;
+                    }
+                    pk[i] = pack_bf16x2(p0, p1);
+                    xa += p0;
+                    xb += p1;
+                    if (i & 1) {
+                        lc += bf16lo_to_f32(pk[i]);
+                        ld += bf16hi_to_f32(pk[i]);
+                    } else {
+                        la += bf16lo_to_f32(pk[i]);
+                        lb += bf16hi_to_f32(pk[i]);
+                    }
+                }
+                tmem_st16(tS + cc * 16, pk);
+            }
+            l += (la + lb) + (lc + ld);
+            lx += xa + xb;
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_p);
+        }
+        if (!ok) break;
+        // Epilogue: O = O_acc / l, LSE = ln2 * (m + log2 lx)
+        ok = mbar_wait(bar_o, cnt_o & 1, abort_flag);
+        ++cnt_o;
+        if (!ok) break;
+        tc_fence_after();
+        const bool live = row < s.Nq;
+        const float inv_l = 1.0f / l;
+        const size_t row_idx = (size_t)bh * s.Nq + (size_t)row;
+#pragma unroll 1
+        for (int cc = 0; cc < D; cc += 32) {
+            uint32_t r[32];
+            tmem_ld32(tO + cc, r);
+            tmem_wait_ld();
+            if (live) {
+                if constexpr (OUT_F32) {
+                    float4* dst = reinterpret_cast<float4*>(static_cast<float*>(o_ptr) + row_idx * D + cc);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        dst[i] = make_float4(__uint_as_float(r[4 * i]) * inv_l, __uint_as_float(r[4 * i + 1]) * inv_l,
+                                             __uint_as_float(r[4 * i + 2]) * inv_l, __uint_as_float(r[4 * i + 3]) * inv_l);
+                } else {
+                    uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(o_ptr) + row_idx * D + cc);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        uint4 w;
+                        w.x = pack_bf16x2(__uint_as_float(r[8 * i + 0]) * inv_l, __uint_as_float(r[8 * i + 1]) * inv_l);
+                        w.y = pack_bf16x2(__uint_as_float(r[8 * i + 2]) * inv_l, __uint_as_float(r[8 * i + 3]) * inv_l);
+                        w.z = pack_bf16x2(__uint_as_float(r[8 * i + 4]) * inv_l, __uint_as_float(r[8 * i + 5]) * inv_l);
+                        w.w = pack_bf16x2(__uint_as_float(r[8 * i + 6]) * inv_l, __uint_as_float(r[8 * i + 7]) * inv_l);
+                        dst[i] = w;
+                    }
+                }
+            }
+        }
+        if (live && lse_ptr) lse_ptr[row_idx] = (m + log2f(lx)) * kLn2;
+    }
+    if (!ok) raise_abort(bars, err);
+}
+
+template <int D, bool OUT_F32>
+__global__ void __launch_bounds__(kThreads, 1)
+attn_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                const __grid_constant__ CUtensorMap tv, void* __restrict__ o_ptr,
+                float* __restrict__ lse_ptr, const FwdParams p, unsigned int* err) {
+    using C = FwdCfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~uintptr_t(1023));
+    Bars* bars = reinterpret_cast<Bars*>(smem + C::kBarOff);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(smem_u32(&bars->q_full[t]), 1);
+            mbar_init(smem_u32(&bars->q_empty[t]), 1);
+            mbar_init(smem_u32(&bars->s_full[t]), 1);
+            mbar_init(smem_u32(&bars->p_full[t]), 4);
+            mbar_init(smem_u32(&bars->o_full[t]), 1);
+        }
+        for (int i = 0; i < C::kStages; ++i) {
+            mbar_init(smem_u32(&bars->kv_full[i]), 1);
+            mbar_init(smem_u32(&bars->kv_empty[i]), 1);
+        }
+        mbar_init(smem_u32(&bars->drain), 1);
+        bars->abort = 0;
+        fence_barrier_init();
+        tma_prefetch_desc(&tq);
+        tma_prefetch_desc(&tk);
+        tma_prefetch_desc(&tv);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(&bars->tmem_base), 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = bars->tmem_base;
+
+    if (warp == 0) {
+        if (lane == 0) run_producer<D>(&tq, &tk, &tv, smem, bars, p, err);
+    } else if (warp == 1) {
+        if (lane == 0) run_mma<D>(smem, bars, tmem, p, err);
+    } else if (warp >= 4) {
+        const int t = (warp - 4) >> 2;
+        run_softmax<D, OUT_F32>(t, warp & 3, lane, bars, tmem, p, o_ptr, lse_ptr, err);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+template <int D, bool OUT_F32>
+attn_status_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                           void* o, float* lse, const FwdParams& p, cudaStream_t stream,
+                           const DeviceInfo& dev) {
+    using C = FwdCfg<D>;
+    static int attr_set[64] = {0};
+    if (dev.device < 64 && !attr_set[dev.device]) {
+        if (cudaFuncSetAttribute(attn_fwd_kernel<D, OUT_F32>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 C::kSmemBytes) != cudaSuccess)
+            return ATTN_ERR_CUDA;
+        attr_set[dev.device] = 1;
+    }
+    long long grid = p.shape.units < dev.num_sms ? p.shape.units : dev.num_sms;
+    attn_fwd_kernel<D, OUT_F32><<<(unsigned)grid, kThreads, C::kSmemBytes, stream>>>(
+        tq, tk, tv, o, lse, p, dev.err_word);
+    return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+}  // namespace
+
+attn_status_t launch_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                         int B, int Hq, int Hkv, int Nq, int Nk, int d, int causal, float scale,
+                         attn_out_dtype_t o_dtype, cudaStream_t stream, const DeviceInfo& dev) {
+    FwdParams p;
+    p.shape = make_fwd_shape(B, Hq, Hkv, Nq, Nk, d, causal);
+    p.group = Hq / Hkv;
+    p.off = Nk - Nq;
+    p.c = scale * kLog2e;
+    CUtensorMap tq, tk, tv;
+    attn_status_t st;
+    if ((st = encode_tmap_bf16_3d(&tq, q, d, Nq, (long long)B * Hq, kTileM)) != ATTN_OK) return st;
+    if ((st = encode_tmap_bf16_3d(&tk, k, d, Nk, (long long)B * Hkv, kTileN)) != ATTN_OK) return st;
+    if ((st = encode_tmap_bf16_3d(&tv, v, d, Nk, (long long)B * Hkv, kTileN)) != ATTN_OK) return st;
+    const bool f32 = o_dtype == ATTN_OUT_F32;
+    if (d == 128)
+        return f32 ? launch_fwd_t<128, true>(tq, tk, tv, o, lse, p, stream, dev)
+                   : launch_fwd_t<128, false>(tq, tk, tv, o, lse, p, stream, dev);
+    if (d == 64)
+        return f32 ? launch_fwd_t<64, true>(tq, tk, tv, o, lse, p, stream, dev)
+                   : launch_fwd_t<64, false>(tq, tk, tv, o, lse, p, stream, dev);
+    return ATTN_ERR_UNSUPPORTED;
+}
+
+}  // namespace gb300

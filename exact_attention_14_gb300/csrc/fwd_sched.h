@@ -1,0 +1,95 @@
+// fwd_sched.h -- work decomposition of the fused forward, shared verbatim by the
+// device kernel and the host-side exports (so the tests pin the code the
+// kernel runs).
+//
+// A unit is (batch b, query head hq, m-block mb): 2 Q tiles of 128 rows,
+// rows [256*mb, 256*mb + 256).  Both tiles stream the same K/V tiles, so K/V
+// is loaded once per unit (lecture notes "Optimizing Attention for Modern
+// Hardware", 3.1: Q-outer / KV-inner; "Flash Attention 3/4 notes", FA4
+// section 1: two Q tiles per CTA).
+//
+// Order (lecture notes 4.5; FA4 notes section 3): query heads are grouped into
+// sections whose K/V fit an L2 budget; sections run in order; inside a section
+// the m-blocks run longest-first (causal) and, within one m-block rank, heads
+// run in index order so GQA siblings (consecutive hq sharing a KV head) are
+// adjacent.  The persistent grid walks this list with a static stride.
+#pragma once
+
+#include <cstdint>
+
+#if defined(__CUDACC__)
+#define GB300_HD __host__ __device__ __forceinline__
+#else
+#define GB300_HD inline
+#endif
+
+namespace gb300 {
+
+constexpr int kTileM = 128;           // query rows per Q tile (tcgen05 M)
+constexpr int kTileN = 128;           // keys per K/V tile
+constexpr int kTilesPerUnit = 2;      // Q tiles per unit
+constexpr int kUnitRows = kTileM * kTilesPerUnit;
+constexpr long long kL2SectionBytes = 64ll << 20;  // K/V bytes a section may span
+
+struct FwdShape {
+    int B, Hq, Hkv, Nq, Nk, d, causal;
+    int nmb;                 // m-blocks per head
+    int heads_per_section;   // query heads per section (multiple of Hq/Hkv)
+    long long units;         // B * Hq * nmb
+};
+
+// KV tiles needed by query rows [row0, row0 + rows): causal block skipping.
+GB300_HD int kv_tiles_for_rows(int row0, int rows, int Nq, int Nk, int causal, int block) {
+    if (rows <= 0 || Nk <= 0 || block <= 0) return 0;
+    const int total = (Nk + block - 1) / block;
+    if (!causal) return total;
+    const long long last_key = (long long)row0 + rows - 1 + (long long)(Nk - Nq);
+    if (last_key < 0) return 0;
+    const long long t = last_key / block + 1;
+    return t < total ? (int)t : total;
+}
+
+// Valid rows of Q tile t of m-block mb.
+GB300_HD int tile_rows(int mb, int t, int Nq) {
+    const int r0 = mb * kUnitRows + t * kTileM;
+    const int r = Nq - r0;
+    return r <= 0 ? 0 : (r < kTileM ? r : kTileM);
+}
+
+GB300_HD int tile_kv_count(int mb, int t, const FwdShape& s) {
+    return kv_tiles_for_rows(mb * kUnitRows + t * kTileM, tile_rows(mb, t, s.Nq), s.Nq, s.Nk,
+                             s.causal, kTileN);
+}
+
+inline FwdShape make_fwd_shape(int B, int Hq, int Hkv, int Nq, int Nk, int d, int causal) {
+    FwdShape s;
+    s.B = B; s.Hq = Hq; s.Hkv = Hkv; s.Nq = Nq; s.Nk = Nk; s.d = d; s.causal = causal;
+    s.nmb = (Nq + kUnitRows - 1) / kUnitRows;
+    const int group = Hq / Hkv;
+    const long long kv_head_bytes = 2ll * Nk * d * 2;  // K and V, bf16
+    long long kv_per_sec = kL2SectionBytes / (kv_head_bytes > 0 ? kv_head_bytes : 1);
+    if (kv_per_sec < 1) kv_per_sec = 1;
+    long long hps = kv_per_sec * group;
+    const long long all = (long long)B * Hq;
+    if (hps > all) hps = all;
+    s.heads_per_section = (int)hps;
+    s.units = all * s.nmb;
+    return s;
+}
+
+// Unit index i (0 <= i < units) -> (bh = b * Hq + hq, mb).
+GB300_HD void unit_of(const FwdShape& s, long long i, int& bh, int& mb) {
+    const long long all = (long long)s.B * s.Hq;
+    const long long S = s.heads_per_section;
+    const long long sec_units = S * s.nmb;
+    const long long sec = i / sec_units;
+    const long long r = i - sec * sec_units;
+    const long long rest = all - sec * S;
+    const long long hs = rest < S ? rest : S;
+    const long long rank = r / hs;
+    const long long h_in = r - rank * hs;
+    bh = (int)(sec * S + h_in);
+    mb = s.causal ? (int)(s.nmb - 1 - rank) : (int)rank;
+}
+
+}  // namespace gb300

@@ -1,0 +1,38 @@
+// internal.h -- declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "attn.h"
+
+namespace gb300 {
+
+struct DeviceInfo {
+    int device;
+    int num_sms;
+    unsigned int* err_word;  // device address of the library's error word
+};
+
+// Per-device facts for the current device, initialised once per device.
+attn_status_t current_device_info(DeviceInfo* out);
+
+// 3-D bf16 tensor map over a [heads, rows, d] array with a 128-byte-swizzled
+// box of (64 elements of d) x box_rows x 1.  Out-of-range rows read as zero.
+attn_status_t encode_tmap_bf16_3d(CUtensorMap* map, const void* base, int d, int rows,
+                                  long long heads, int box_rows);
+
+attn_status_t launch_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                         int B, int Hq, int Hkv, int Nq, int Nk, int d, int causal, float scale,
+                         attn_out_dtype_t o_dtype, cudaStream_t stream, const DeviceInfo& dev);
+
+// Decode: chunk size in keys for a request (multiple of 64).
+int decode_chunk(int Nmax, int B, int Hkv, int num_sms, int num_splits);
+size_t decode_workspace_bytes(int B, int Hq, int Nmax, int d, int chunk);
+
+attn_status_t launch_decode(const void* q, const void* k_cache, const void* v_cache,
+                            const int* seqlens, void* o, float* lse, int B, int Hq, int Hkv,
+                            int Nmax, int d, float scale, int chunk, void* workspace,
+                            attn_out_dtype_t o_dtype, cudaStream_t stream, const DeviceInfo& dev);
+
+}  // namespace gb300

@@ -1,0 +1,182 @@
+/*
+ * attn.h -- C ABI of the GB300 (sm_103a) exact-attention library.
+ *
+ * Two operations, both exact scaled-dot-product attention O = softmax(s*QK^T)V
+ * computed tile by tile with the online-softmax running max / sum so that the
+ * N x N score and probability matrices never reach device memory:
+ *
+ *   attn_fwd     fused forward with per-row logsumexp, causal masking and
+ *                grouped-query heads (lecture notes "Optimizing Attention for
+ *                Modern Hardware: FlashAttention 1-4", sections 2.2 tiling and
+ *                rescaling, 2.5 causal block skipping, 2.6 logsumexp, 3.1 loop
+ *                order, 3.2 delayed normalisation, 4.5 persistent kernel and
+ *                LPT schedule, 5.3 conditional rescaling; "Flash Attention 3/4
+ *                notes", FA4 section 1 pipeline and section 3 causal schedule);
+ *   attn_decode  single-query decode over a KV cache with split-KV
+ *                (Flash-Decoding): each split produces a partial (m, l, o) and
+ *                a combine step merges the splits by log-sum-exp (lecture
+ *                notes section 6.1 and exercise 3; "FlashAttention tiling &
+ *                online softmax" section 7.1), with query heads that share a
+ *                KV head packed as rows of one tile (lecture notes 6.2).
+ *
+ * Conventions shared by every entry point
+ *   - Pointers named q/k/v/o/lse/k_cache/v_cache/seqlens/workspace are DEVICE
+ *     pointers.  The caller allocates and owns every buffer; the library never
+ *     allocates device memory.  Tensor data must be 16-byte aligned.
+ *   - Tensors are row-major and contiguous: [B, H, N, d] (d fastest).
+ *   - bf16 means IEEE-style bfloat16 (1-8-7).  Accumulation is fp32.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *     default stream).  Host-side argument checks run before anything is
+ *     enqueued; a rejected call enqueues nothing.  Errors are returned, never
+ *     printed or thrown.
+ *   - Device-side faults of the algorithm itself (a bounded wait that ran
+ *     out, an out-of-range sequence length) are recorded in a per-device error
+ *     word that attn_last_device_error() reads.
+ *   - Head mapping for grouped-query attention: query head hq uses KV head
+ *     hq / (Hq / Hkv) (contiguous groups).
+ *   - Causal masking is aligned bottom-right: query row i may attend key j iff
+ *     j <= i + (Nk - Nq).  With Nq == Nk that is j <= i.
+ *   - LSE is the natural-log logsumexp of the scaled scores of a row:
+ *     LSE_i = log sum_j exp(scale * q_i . k_j).
+ */
+#ifndef GB300_ATTN_H
+#define GB300_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    ATTN_OK = 0,
+    ATTN_ERR_INVALID_ARG = 1,  /* null/misaligned pointer, bad shape or value   */
+    ATTN_ERR_UNSUPPORTED = 2,  /* valid request this build does not implement  */
+    ATTN_ERR_CUDA = 3,         /* a CUDA runtime/driver call failed             */
+    ATTN_ERR_TIMEOUT = 4,      /* a device-side bounded wait ran out            */
+    ATTN_ERR_WORKSPACE = 5     /* decode workspace missing or too small         */
+} attn_status_t;
+
+typedef enum {
+    ATTN_OUT_BF16 = 0,         /* O written as bf16 (round-to-nearest-even)     */
+    ATTN_OUT_F32 = 1           /* O written as fp32                              */
+} attn_out_dtype_t;
+
+/*
+ * attn_fwd -- fused exact attention forward.
+ *
+ *   q    bf16 [B, Hq,  Nq, d]        k, v  bf16 [B, Hkv, Nk, d]
+ *   o    [B, Hq, Nq, d], element type per o_dtype (bf16 or fp32)
+ *   lse  fp32 [B, Hq, Nq] natural-log logsumexp per row, or NULL to skip it
+ *   scale  softmax scale (typically 1/sqrt(d)); finite and >= 0
+ *   causal 0 or 1 (bottom-right aligned; requires Nq <= Nk)
+ *
+ * Supported: d in {64, 128}; Hq % Hkv == 0; 1 <= Nq, Nk <= 2^24;
+ *            B*Hq and B*Hkv <= 2^24.  Other d -> ATTN_ERR_UNSUPPORTED.
+ * Numerics: scores and O accumulate in fp32; the probabilities that multiply V
+ * are rounded to bf16, and the row sum uses those same rounded values.
+ * Returns ATTN_OK once the kernel is enqueued.
+ */
+attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                       int B, int Hq, int Hkv, int Nq, int Nk, int d, int causal,
+                       float scale, attn_out_dtype_t o_dtype, void* stream);
+
+/*
+ * attn_decode_workspace_size -- bytes of device workspace attn_decode needs
+ * for this shape and split request (num_splits as passed to attn_decode).
+ * Returns 0 for arguments attn_decode would reject.
+ */
+size_t attn_decode_workspace_size(int B, int Hq, int Hkv, int Nmax, int d, int num_splits);
+
+/*
+ * attn_decode -- one query token per sequence against a KV cache (split-KV).
+ *
+ *   q        bf16 [B, Hq, 1, d]
+ *   k_cache  bf16 [B, Hkv, Nmax, d]     v_cache  bf16 [B, Hkv, Nmax, d]
+ *   seqlens  int32 [B] (device): valid prefix length of each sequence, in
+ *            [1, Nmax].  Keys at positions >= seqlens[b] are never read into
+ *            the result (they may hold anything, including NaN).  A length
+ *            outside [1, Nmax] is clamped into [0, Nmax] and recorded in the
+ *            device error word (attn_last_device_error -> INVALID_ARG); a
+ *            clamped length of 0 yields O = 0, LSE = -inf.
+ *   o        [B, Hq, 1, d] per o_dtype;  lse  fp32 [B, Hq, 1] or NULL
+ *   num_splits  0 = choose automatically; k > 0 = cut each sequence's KV
+ *            range into chunks of ceil(Nmax / k) keys (rounded up to a multiple
+ *            of 64), so a sequence of length Nmax gets (at most) k splits.
+ *   workspace   device scratch of at least attn_decode_workspace_size(...)
+ *            bytes, 16-byte aligned; contents need no initialisation and are
+ *            garbage afterwards.  Concurrent calls must not share it.
+ *
+ * Supported: d in {64, 128}; Hq % Hkv == 0; Hq / Hkv <= 16; 1 <= Nmax <= 2^24.
+ */
+attn_status_t attn_decode(const void* q, const void* k_cache, const void* v_cache,
+                          const int* seqlens, void* o, float* lse, int B, int Hq, int Hkv,
+                          int Nmax, int d, float scale, int num_splits, void* workspace,
+                          size_t workspace_bytes, attn_out_dtype_t o_dtype, void* stream);
+
+/* Human-readable name of a status code (static string). */
+const char* attn_status_string(attn_status_t status);
+
+/*
+ * attn_last_device_error -- synchronises `stream`, then reads and clears the
+ * current device's error word.  Returns ATTN_OK, ATTN_ERR_TIMEOUT (a kernel's
+ * bounded wait ran out; its outputs are undefined), ATTN_ERR_INVALID_ARG (a
+ * decode sequence length was out of range) or ATTN_ERR_CUDA.
+ */
+attn_status_t attn_last_device_error(void* stream);
+
+/* ---------------------------------------------------------------------------
+ * Host-side scheduling logic, exported so it can be inspected and tested.
+ * These functions touch no GPU.
+ * ------------------------------------------------------------------------- */
+
+/*
+ * Split-count rule for uniform-length decode (lecture notes 6.1, exercise 11):
+ * over s = 1..max_splits, wave efficiency e(s) = w/ceil(w) with
+ * w = units*s/num_sms; return the smallest s with e(s) >= 0.85 * max_s e(s).
+ * units = batch x KV heads.  Returns 0 on a bad argument.
+ */
+int attn_decode_num_splits(int units, int num_sms, int max_splits);
+
+/*
+ * Greedy list scheduling (lecture notes 4.5): jobs are taken in the given
+ * order (lpt = 0) or longest-first (lpt = 1, stable), each to the currently
+ * least-loaded worker, lowest index on ties.  Writes per-worker loads to
+ * loads_out[workers] (may be NULL) and returns the makespan (max load), or
+ * -1 on a bad argument.
+ */
+long long attn_list_schedule(const int* costs, int n, int workers, int lpt, long long* loads_out);
+
+/*
+ * Number of 128-key KV tiles a block of query rows [row0, row0 + rows) must
+ * visit (causal block skipping, lecture notes 2.5): all ceil(Nk / block) tiles
+ * without causal masking, else the tiles up to the one holding key
+ * row0 + rows - 1 + (Nk - Nq).  `block` is the key-tile height.
+ */
+int attn_kv_tiles(int row0, int rows, int Nq, int Nk, int causal, int block);
+
+/*
+ * Number of work units attn_fwd launches for a shape (a unit = one batch,
+ * one query head, one block of 256 query rows = two 128-row Q tiles).
+ */
+long long attn_fwd_num_units(int B, int Hq, int Hkv, int Nq, int Nk, int d, int causal);
+
+/*
+ * The order in which attn_fwd's persistent kernel walks its units: fills
+ * units_out[3*i + {0,1,2}] = (b, hq, m_block) for i < n (n must equal
+ * attn_fwd_num_units) and, if cost_out is non-NULL, cost_out[i] = the number
+ * of (Q tile, KV tile) pairs unit i computes.  Heads are grouped into
+ * sections whose K/V fit a fixed L2 budget, sections run in order, and within
+ * a section the m-blocks run longest-first (lecture notes 4.5; "Flash
+ * Attention 3/4 notes" FA4 section 3).  `num_sms` is the persistent grid size
+ * used for the static stride.  Returns 0, or -1 on a bad argument.
+ */
+int attn_fwd_schedule(int B, int Hq, int Hkv, int Nq, int Nk, int d, int causal,
+                      long long n, int* units_out, int* cost_out);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GB300_ATTN_H */

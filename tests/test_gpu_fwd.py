@@ -1,0 +1,163 @@
+"""GPU parity of attn_fwd against the fp64 oracle, through the C ABI.
+
+Tolerances (fp32 output): max |dO| <= 1e-2, relative L2(O) <= 5e-3,
+max |dLSE| <= 1e-3.  bf16 output is compared with the oracle rounded to bf16
+(round-to-nearest-even) and a bound of 1e-2 plus half a bf16 ulp of the
+reference value.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import exact_attention_14_gb300 as ea
+import oracle
+from exact_attention_14_gb300.inputs import (GQA, LONG, PREFILL, TINY, make_config_inputs,
+                                             make_fwd_inputs)
+
+pytestmark = pytest.mark.gpu
+
+MAX_ABS_O = 1e-2
+REL_L2_O = 5e-3
+MAX_ABS_LSE = 1e-3
+
+
+def gpu_fwd(q, k, v, causal, scale=None, out_dtype=torch.float32, with_lse=True):
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    o, lse = ea.forward(qd, kd, vd, causal=causal, scale=scale, out_dtype=out_dtype,
+                        return_lse=with_lse)
+    torch.cuda.synchronize()
+    assert ea.attn_last_device_error() == 0
+    o = o.float().cpu().double().numpy()
+    lse = None if lse is None else lse.cpu().double().numpy()
+    return o, lse
+
+
+def assert_close(o, lse, o_ref, lse_ref, what=""):
+    d_o = np.abs(o - o_ref)
+    rel = np.linalg.norm(o - o_ref) / max(np.linalg.norm(o_ref), 1e-30)
+    assert np.isfinite(o).all(), f"{what}: non-finite O"
+    assert d_o.max() <= MAX_ABS_O, f"{what}: max|dO| = {d_o.max():.3e}"
+    assert rel <= REL_L2_O, f"{what}: relL2(O) = {rel:.3e}"
+    if lse is not None:
+        d_l = np.abs(lse - lse_ref)
+        assert d_l.max() <= MAX_ABS_LSE, f"{what}: max|dLSE| = {d_l.max():.3e}"
+
+
+def bf16_round(x):
+    return torch.from_numpy(x).to(torch.bfloat16).double().numpy()
+
+
+def assert_close_bf16(o, o_ref, what=""):
+    ref = bf16_round(o_ref)
+    half_ulp = np.exp2(np.floor(np.log2(np.maximum(np.abs(ref), 1e-30))) - 8)
+    err = np.abs(o - ref)
+    assert (err <= MAX_ABS_O + half_ulp).all(), f"{what}: bf16 O off by {err.max():.3e}"
+
+
+# ------------------------------- the configs --------------------------------
+def test_tiny_config_full():
+    q, k, v = make_config_inputs(TINY)
+    o, lse = gpu_fwd(q, k, v, False, TINY.scale)
+    o_ref, lse_ref = oracle.attention(q, k, v, causal=False, scale=TINY.scale)
+    assert_close(o, lse, o_ref, lse_ref, "tiny")
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_prefill_config_full(causal):
+    q, k, v = make_config_inputs(PREFILL)
+    o, lse = gpu_fwd(q, k, v, causal, PREFILL.scale)
+    o_ref, lse_ref = oracle.attention(q, k, v, causal=causal, scale=PREFILL.scale)
+    assert_close(o, lse, o_ref, lse_ref, f"prefill causal={causal}")
+
+
+def sampled_rows(cfg, full_heads, n_random, seed):
+    rng = np.random.default_rng(seed)
+    rows = [(b, h, i) for (b, h) in full_heads for i in range(cfg.N)]
+    rows += [(int(rng.integers(cfg.B)), int(rng.integers(cfg.Hq)), int(rng.integers(cfg.N)))
+             for _ in range(n_random)]
+    # the first and last rows of a few heads (diagonal tiles, longest rows)
+    for h in range(0, cfg.Hq, max(1, cfg.Hq // 4)):
+        rows += [(cfg.B - 1, h, 0), (cfg.B - 1, h, cfg.N - 1), (0, h, 127), (0, h, 128)]
+    return np.array(rows, np.int32)
+
+
+@pytest.mark.parametrize("cfg,full_heads", [
+    (LONG, [(0, 0), (0, 31)]),
+    (GQA, [(0, 0), (7, 31), (3, 13)]),
+])
+def test_large_configs_sampled(cfg, full_heads):
+    """Full-size launch; the oracle computes whole heads plus random rows."""
+    q, k, v = make_config_inputs(cfg)
+    o, lse = gpu_fwd(q, k, v, True, cfg.scale)
+    rows = sampled_rows(cfg, full_heads, 2048, cfg.seed)
+    o_ref, lse_ref = oracle.attention_rows(q, k, v, rows, causal=True, scale=cfg.scale)
+    o_s = o[rows[:, 0], rows[:, 1], rows[:, 2]]
+    lse_s = lse[rows[:, 0], rows[:, 1], rows[:, 2]]
+    assert_close(o_s, lse_s, o_ref, lse_ref, cfg.name)
+    # properties that hold for every row: finite, LSE >= max possible lower bound
+    assert np.isfinite(o).all() and np.isfinite(lse).all()
+
+
+# ------------------------------- edge cases ---------------------------------
+@pytest.mark.parametrize("B,Hq,Hkv,Nq,Nk,d,causal", [
+    (1, 1, 1, 1, 1, 64, False),
+    (1, 1, 1, 1, 1, 128, True),
+    (1, 2, 1, 17, 17, 64, True),
+    (2, 2, 2, 128, 128, 128, True),
+    (1, 1, 1, 129, 129, 128, False),
+    (1, 3, 1, 255, 255, 64, True),
+    (1, 1, 1, 256, 256, 128, True),
+    (1, 2, 2, 257, 257, 128, False),
+    (1, 4, 2, 300, 300, 128, True),
+    (2, 8, 1, 1000, 1000, 64, True),
+    (1, 2, 2, 100, 333, 128, False),   # Nq < Nk
+    (1, 2, 2, 100, 333, 128, True),    # bottom-right causal, mid-tile diagonal
+    (1, 2, 1, 384, 1000, 64, True),
+    (1, 1, 1, 700, 90, 128, False),    # Nq > Nk
+    (3, 16, 2, 520, 520, 128, True),   # GQA 8:1
+])
+def test_edge_shapes(B, Hq, Hkv, Nq, Nk, d, causal):
+    q, k, v = make_fwd_inputs(B, Hq, Hkv, Nq, Nk, d, seed=100 + Nq + Nk + d)
+    scale = 1 / math.sqrt(d)
+    o, lse = gpu_fwd(q, k, v, causal, scale)
+    o_ref, lse_ref = oracle.attention(q, k, v, causal=causal, scale=scale)
+    assert_close(o, lse, o_ref, lse_ref, f"{(B, Hq, Hkv, Nq, Nk, d, causal)}")
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_bf16_output_and_no_lse(d):
+    q, k, v = make_fwd_inputs(2, 4, 2, 333, 333, d, seed=7)
+    o, lse = gpu_fwd(q, k, v, True, None, out_dtype=torch.bfloat16, with_lse=False)
+    assert lse is None
+    o_ref, _ = oracle.attention(q, k, v, causal=True)
+    assert_close_bf16(o, o_ref, "bf16 out")
+
+
+def test_zero_scale_gives_uniform_average():
+    q, k, v = make_fwd_inputs(1, 2, 2, 200, 200, 128, seed=9)
+    o, lse = gpu_fwd(q, k, v, True, 0.0)
+    o_ref, lse_ref = oracle.attention(q, k, v, causal=True, scale=0.0)
+    assert_close(o, lse, o_ref, lse_ref, "scale 0")
+
+
+def test_outlier_channels_large_logits():
+    """Long-context style outliers (|s| up to ~100) on a small shape."""
+    q, k, v = make_fwd_inputs(1, 4, 4, 1024, 1024, 128, seed=21, outlier_channels=4)
+    o, lse = gpu_fwd(q, k, v, True, 1 / math.sqrt(128))
+    o_ref, lse_ref = oracle.attention(q, k, v, causal=True)
+    assert_close(o, lse, o_ref, lse_ref, "outliers")
+
+
+def test_repeatable_and_stream_ordered():
+    """Same inputs twice on a side stream give bit-identical results."""
+    q, k, v = (t.cuda() for t in make_fwd_inputs(2, 4, 4, 640, 640, 128, seed=3))
+    s = torch.cuda.Stream()
+    outs = []
+    with torch.cuda.stream(s):
+        for _ in range(2):
+            o, lse = ea.forward(q, k, v, causal=True, out_dtype=torch.float32, stream=s)
+            outs.append((o.clone(), lse.clone()))
+    s.synchronize()
+    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])

@@ -1,0 +1,193 @@
+"""CPU tests of the C-ABI library: it loads, exports every symbol the header
+declares, rejects bad arguments before touching CUDA, and its host-side
+scheduling logic reproduces the worked examples printed in the lecture notes
+(tests/golden/scheduling.json, each entry cited)."""
+import ctypes
+import json
+import math
+import os
+import re
+
+import pytest
+
+import exact_attention_14_gb300 as ea
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+GOLDEN = json.load(open(os.path.join(ROOT, "tests", "golden", "scheduling.json")))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from exact_attention_14_gb300 import _build
+    _build.build()
+    return ea.load()
+
+
+def header_functions():
+    text = open(os.path.join(ROOT, "include", "attn.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(attn_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_library_exports_every_header_symbol(lib):
+    names = header_functions()
+    assert "attn_fwd" in names and "attn_decode" in names
+    for n in names:
+        assert hasattr(lib, n), n
+        assert n in ea.SIGNATURES, f"binding lacks a signature for {n}"
+
+
+def test_status_strings(lib):
+    assert ea.attn_status_string(0) == "ATTN_OK"
+    assert ea.attn_status_string(4) == "ATTN_ERR_TIMEOUT"
+    assert ea.attn_status_string(99) == "ATTN_ERR_UNKNOWN"
+
+
+FAKE = 0x10000  # aligned, never dereferenced: every case fails validation first
+
+
+def fwd(lib, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=None, B=1, Hq=2, Hkv=1, Nq=8, Nk=8, d=64,
+             causal=0, scale=0.125, odt=0)
+    a.update(kw)
+    return lib.attn_fwd(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["Hq"], a["Hkv"],
+                        a["Nq"], a["Nk"], a["d"], a["causal"], a["scale"], a["odt"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), 1), (dict(o=None), 1), (dict(k=FAKE + 8), 1), (dict(lse=FAKE + 2), 1),
+    (dict(B=0), 1), (dict(Hq=3, Hkv=2), 1), (dict(Nq=0), 1), (dict(Nk=0), 1),
+    (dict(Nq=(1 << 24) + 1), 1), (dict(causal=2), 1), (dict(causal=1, Nq=9, Nk=8), 1),
+    (dict(scale=-1.0), 1), (dict(scale=float("nan")), 1), (dict(scale=float("inf")), 1),
+    (dict(odt=7), 1), (dict(d=96), 2), (dict(d=256), 2), (dict(d=0), 1),
+])
+def test_fwd_argument_checks(lib, kw, code):
+    assert fwd(lib, **kw) == code
+
+
+def dec(lib, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, sl=FAKE, o=FAKE, lse=None, B=2, Hq=8, Hkv=2, Nmax=64, d=128,
+             scale=0.1, ns=0, ws=FAKE, wsb=1 << 20, odt=1)
+    a.update(kw)
+    return lib.attn_decode(a["q"], a["k"], a["v"], a["sl"], a["o"], a["lse"], a["B"], a["Hq"],
+                           a["Hkv"], a["Nmax"], a["d"], a["scale"], a["ns"], a["ws"], a["wsb"],
+                           a["odt"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), 1), (dict(sl=None), 1), (dict(sl=FAKE + 2), 1), (dict(v=FAKE + 4), 1),
+    (dict(Hq=9), 1), (dict(Nmax=0), 1), (dict(ns=-1), 1), (dict(scale=-0.5), 1),
+    (dict(d=80), 2), (dict(Hq=34, Hkv=2), 2),
+])
+def test_decode_argument_checks(lib, kw, code):
+    assert dec(lib, **kw) == code
+
+
+def test_workspace_size_rejects_bad_shapes(lib):
+    assert ea.attn_decode_workspace_size(0, 8, 2, 64, 128) == 0
+    assert ea.attn_decode_workspace_size(1, 8, 3, 64, 128) == 0
+    assert ea.attn_decode_workspace_size(1, 8, 2, 64, 96) == 0
+
+
+# ------------------------------ scheduling pins ------------------------------
+def test_lpt_toy_from_the_notes(lib):
+    g = GOLDEN["lpt_toy"]
+    mk, loads = ea.attn_list_schedule(g["costs"], g["workers"], lpt=False)
+    assert loads == g["natural_loads"] and mk == max(g["natural_loads"])
+    mk, loads = ea.attn_list_schedule(g["costs"], g["workers"], lpt=True)
+    assert loads == g["lpt_loads"] and mk == g["lower_bound"]
+
+
+def test_exercise_10_from_the_notes(lib):
+    g = GOLDEN["exercise_10"]
+    assert ea.attn_list_schedule(g["costs"], g["workers"], lpt=False)[0] == g["natural_makespan"]
+    assert ea.attn_list_schedule(g["costs"], g["workers"], lpt=True)[0] == g["lpt_makespan"]
+    assert math.ceil(sum(g["costs"]) / g["workers"]) == g["lower_bound"]
+
+
+def test_split_heuristic_from_the_notes(lib):
+    for c in GOLDEN["split_heuristic"]["cases"]:
+        s = ea.attn_decode_num_splits(c["units"], c["num_sms"], 128)
+        assert s == c["splits"]
+        w = c["units"] * s / c["num_sms"]
+        assert abs(w / math.ceil(w) - c["efficiency"]) < 0.005
+
+
+def test_split_heuristic_bad_args(lib):
+    assert ea.attn_decode_num_splits(0, 132, 8) == 0
+    assert ea.attn_decode_num_splits(4, 0, 8) == 0
+
+
+def test_causal_block_count_from_the_notes(lib):
+    g = GOLDEN["causal_blocks"]
+    nb = g["N"] // g["block"]
+    full = sum(ea.attn_kv_tiles(i * g["block"], g["block"], g["N"], g["N"], False, g["block"])
+               for i in range(nb))
+    causal = sum(ea.attn_kv_tiles(i * g["block"], g["block"], g["N"], g["N"], True, g["block"])
+                 for i in range(nb))
+    assert full == g["blocks_total"] and causal == g["blocks_causal"]
+    per_block = 4 * g["block"] * g["block"] * g["d"]  # QK^T and PV, 2 flops per MAC
+    assert round(full * per_block / 1e6, 1) == g["mflop_full"]
+    assert round(causal * per_block / 1e6, 1) == g["mflop_causal"]
+
+
+def test_kv_tiles_edge_cases(lib):
+    assert ea.attn_kv_tiles(0, 0, 10, 10, True, 128) == 0          # no rows
+    assert ea.attn_kv_tiles(0, 1, 1, 1, True, 128) == 1
+    assert ea.attn_kv_tiles(0, 128, 128, 300, False, 128) == 3     # ragged Nk
+    # bottom-right causal with Nq < Nk: row 0 sees keys 0..Nk-Nq
+    assert ea.attn_kv_tiles(0, 1, 100, 300, True, 128) == 2
+    assert ea.attn_kv_tiles(0, 128, 128, 128, True, 128) == 1
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,N,d,causal", [
+    (4, 16, 16, 2048, 128, True), (4, 16, 16, 2048, 128, False), (1, 32, 32, 16384, 128, True),
+    (8, 32, 8, 4096, 128, True), (1, 3, 1, 300, 64, True), (2, 4, 2, 129, 64, False),
+])
+def test_forward_schedule_covers_every_unit_once(lib, B, Hq, Hkv, N, d, causal):
+    order, costs = ea.attn_fwd_schedule(B, Hq, Hkv, N, N, d, causal)
+    nmb = -(-N // 256)
+    assert len(order) == B * Hq * nmb == ea.attn_fwd_num_units(B, Hq, Hkv, N, N, d, causal)
+    assert sorted(order) == sorted((b, h, m) for b in range(B) for h in range(Hq)
+                                   for m in range(nmb))
+    # cost = KV tiles of the unit's two Q tiles; totals match the causal count
+    total = sum(costs)
+    nt = -(-N // 128)
+    if causal:
+        assert total == sum(ea.attn_kv_tiles(i * 128, min(128, N - i * 128), N, N, True, 128)
+                            for i in range(nt)) * B * Hq
+    else:
+        assert total == nt * nt * B * Hq
+
+
+def test_forward_schedule_is_longest_first_within_sections(lib):
+    # long-context shape: 8 KB... K/V per head = 8 MiB, so 8 heads per section
+    B, Hq, Hkv, N, d = 1, 32, 32, 16384, 128
+    order, costs = ea.attn_fwd_schedule(B, Hq, Hkv, N, N, d, True)
+    per_sec = 8 * (N // 256)
+    for s in range(0, len(order), per_sec):
+        sec = costs[s:s + per_sec]
+        assert sec == sorted(sec, reverse=True)
+        heads = {h for _, h, _ in order[s:s + per_sec]}
+        assert len(heads) == 8
+
+
+def test_gqa_siblings_are_adjacent(lib):
+    order, _ = ea.attn_fwd_schedule(2, 8, 2, 512, 512, 64, True)
+    # consecutive units of one m-block rank share a KV head in groups of 4
+    for i in range(0, len(order), 4):
+        kv = {(b, h // 4) for b, h, _ in order[i:i + 4]}
+        assert len(kv) == 1
+
+
+def test_wave_quantisation_model_from_the_notes():
+    for c in GOLDEN["wave_quantisation"]["cases"]:
+        waves = math.ceil(c["blocks"] / c["num_sms"])
+        assert waves == c["waves"]
+        assert abs(c["blocks"] / (waves * c["num_sms"]) - c["utilisation"]) < 0.005
+
+
+def test_tau_bound_from_the_notes():
+    g = GOLDEN["tau_bound"]
+    bound = 128 - math.log2(g["N"])
+    assert bound == g["tau_max_exclusive"] and g["tau_used"] < bound
