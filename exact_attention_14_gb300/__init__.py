@@ -16,7 +16,7 @@ import os
 
 __all__ = [
     "ATTN_OUT_BF16", "ATTN_OUT_F32", "AttnError", "attn_fwd", "attn_decode",
-    "attn_decode_workspace_size", "attn_status_string", "attn_last_device_error",
+    "attn_decode_workspace_size", "attn_decode_noalloc", "attn_status_string", "attn_last_device_error",
     "attn_decode_num_splits", "attn_list_schedule", "attn_kv_tiles",
     "attn_fwd_num_units", "attn_fwd_schedule", "forward", "decode", "library_path", "load",
 ]
@@ -42,6 +42,8 @@ SIGNATURES = {
     "attn_decode_workspace_size": (_c_sz, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_int]),
     "attn_decode": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int,
                              _c_int, _c_f, _c_int, _vp, _c_sz, _c_int, _vp]),
+    "attn_decode_noalloc": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int,
+                                     _c_int, _c_int, _c_f, _c_int, _c_int, _vp]),
     "attn_status_string": (ctypes.c_char_p, [_c_int]),
     "attn_last_device_error": (_c_int, [_vp]),
     "attn_decode_num_splits": (_c_int, [_c_int, _c_int, _c_int]),
@@ -212,6 +214,32 @@ def decode(q, k_cache, v_cache, seqlens, *, scale=None, num_splits: int = 0,
     lse = torch.empty((B, Hq, 1), dtype=torch.float32, device=q.device)
     return attn_decode(q, k_cache, v_cache, seqlens, o, lse, scale=scale,
                        num_splits=num_splits, workspace=ws, stream=stream)
+
+
+def attn_decode_noalloc(q, k_cache, v_cache, seqlens, o, lse=None, *,
+                        scale: float | None = None, num_splits: int = 0, stream=None):
+    """attn_decode without a workspace argument, for callers that cannot
+    allocate device memory: the library's fixed 16 MiB per-device scratch array
+    holds the split partials.  Calls that overlap on the GPU share that array
+    and race; calls ordered on one stream do not.  The first call on a device
+    must come before any stream capture."""
+    import torch
+    for t, n in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache")):
+        _need(t, torch.bfloat16, n)
+    _need(seqlens, torch.int32, "seqlens")
+    _need(o, o.dtype, "o")
+    if lse is not None:
+        _need(lse, torch.float32, "lse")
+    B, Hq, _, d = q.shape
+    Hkv, Nmax = k_cache.shape[1], k_cache.shape[2]
+    if scale is None:
+        scale = d ** -0.5
+    odt = ATTN_OUT_F32 if o.dtype == torch.float32 else ATTN_OUT_BF16
+    rc = load().attn_decode_noalloc(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(seqlens), _ptr(o),
+                                    _ptr(lse), B, Hq, Hkv, Nmax, d, float(scale),
+                                    int(num_splits), odt, _stream_ptr(stream))
+    _check(rc, "attn_decode_noalloc")
+    return o, lse
 
 
 def attn_last_device_error(stream=None) -> int:

@@ -464,3 +464,62 @@ attn_status_t launch_decode(const void* q, const void* k_cache, const void* v_ca
 }
 
 }  // namespace gb300
+
+// ---------------------------------------------------------------------------
+// attn_decode_noalloc: the same decode with a scratch buffer the library owns.
+//
+// Some callers cannot call cudaMalloc at all -- for example a plugin inside a
+// host framework that hands all device memory to its own pool and offers no
+// allocator, or a latency-critical loop where an allocation's implicit device
+// synchronisation is not acceptable.  For them the split partials live in one
+// fixed array in device global memory, reserved when the library is loaded on
+// a GPU and held until the process exits.
+// ---------------------------------------------------------------------------
+#include <mutex>
+
+namespace gb300 {
+
+constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;  // 16 MiB per device
+
+static __device__ __align__(256) unsigned char g_decode_scratch[kNoAllocScratchBytes];
+
+namespace {
+std::mutex g_scratch_mu;
+void* g_scratch_addr[64] = {};
+
+// Device address of g_decode_scratch on the current device.  Host code must
+// not pass the symbol itself to a kernel (on the host it is only a stand-in),
+// so the address is looked up once per device, with that device current.
+attn_status_t scratch_address(void** out) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_CUDA;
+    if (dev < 0 || dev >= 64) return ATTN_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lk(g_scratch_mu);
+    if (!g_scratch_addr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess || !p) return ATTN_ERR_CUDA;
+        g_scratch_addr[dev] = p;
+    }
+    *out = g_scratch_addr[dev];
+    return ATTN_OK;
+}
+}  // namespace
+
+}  // namespace gb300
+
+extern "C" attn_status_t attn_decode_noalloc(const void* q, const void* k_cache,
+                                             const void* v_cache, const int* seqlens, void* o,
+                                             float* lse, int B, int Hq, int Hkv, int Nmax, int d,
+                                             float scale, int num_splits,
+                                             attn_out_dtype_t o_dtype, void* stream) {
+    const size_t need = attn_decode_workspace_size(B, Hq, Hkv, Nmax, d, num_splits);
+    if (need == 0)  // a rejected shape, or no usable device: let attn_decode say which
+        return attn_decode(q, k_cache, v_cache, seqlens, o, lse, B, Hq, Hkv, Nmax, d, scale,
+                           num_splits, nullptr, 0, o_dtype, stream);
+    if (need > gb300::kNoAllocScratchBytes) return ATTN_ERR_WORKSPACE;
+    void* ws = nullptr;
+    const attn_status_t st = gb300::scratch_address(&ws);
+    if (st != ATTN_OK) return st;
+    return attn_decode(q, k_cache, v_cache, seqlens, o, lse, B, Hq, Hkv, Nmax, d, scale,
+                       num_splits, ws, gb300::kNoAllocScratchBytes, o_dtype, stream);
+}

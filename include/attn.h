@@ -115,6 +115,32 @@ attn_status_t attn_decode(const void* q, const void* k_cache, const void* v_cach
                           int Nmax, int d, float scale, int num_splits, void* workspace,
                           size_t workspace_bytes, attn_out_dtype_t o_dtype, void* stream);
 
+/*
+ * attn_decode_noalloc -- attn_decode for callers that cannot allocate device
+ * memory.  The pages have no counterpart: it is an addition for callers that
+ * must not call cudaMalloc, such as a plugin inside a host framework that owns
+ * all device memory through its own pool, or a latency-critical loop that
+ * cannot afford an allocation's implicit device synchronisation.
+ *
+ * Same arguments and results as attn_decode, minus the workspace: the split
+ * partials go to a scratch array of 16 MiB that the library reserves in
+ * device global memory on every GPU that loads it, held until the process
+ * exits.  Requests whose attn_decode_workspace_size() exceeds 16 MiB return
+ * ATTN_ERR_WORKSPACE without enqueuing anything (use attn_decode with your own
+ * workspace for those).  No call allocates device memory.
+ *   - The first call on each device looks up the array's device address with
+ *     that device current; make that first call before any stream capture.
+ *   - Every call on a device shares the one array and leaves its contents
+ *     behind.  Nothing in it needs to start at zero: each call writes every
+ *     partial before reading it.  Calls that overlap on the GPU (different
+ *     streams, or different host threads without ordering) race on it; calls
+ *     ordered on one stream do not.
+ */
+attn_status_t attn_decode_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                                  const int* seqlens, void* o, float* lse, int B, int Hq,
+                                  int Hkv, int Nmax, int d, float scale, int num_splits,
+                                  attn_out_dtype_t o_dtype, void* stream);
+
 /* Human-readable name of a status code (static string). */
 const char* attn_status_string(attn_status_t status);
 
