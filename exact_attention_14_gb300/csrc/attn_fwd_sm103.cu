@@ -2,11 +2,11 @@
 //
 // One persistent CTA per SM walks the unit list of fwd_sched.h.  A unit is two
 // 128-row Q tiles of one (batch, query head); both tiles stream the same K/V
-// tiles.  Roles (12 warps):
-//   warp 0      TMA producer: Q tiles once per unit, then K_j, V_j into a
+// tiles.  Roles (12 warps = 3 warpgroups):
+//   warp 0      TMA producer (one elected lane issues): Q tiles once per unit, then K_j, V_j into a
 //               ring of shared-memory slots (128-byte swizzle, mbarrier
 //               full/empty pairs).
-//   warp 1      MMA issuer (one thread): S_t = Q_t K_j^T and O_t += P_t V_j
+//   warp 1      MMA issuer (one elected lane issues): S_t = Q_t K_j^T and O_t += P_t V_j
 //               on the 5th-generation tensor cores, accumulating in TMEM.
 //   warps 4-7   softmax for Q tile 0, warps 8-11 for Q tile 1: one thread
 //               per query row reads its S row from TMEM, applies the causal
@@ -17,7 +17,12 @@
 //               Two row sums are kept: l over the bf16-rounded P that
 //               multiplies V (so O's weights sum to exactly one) and lx over
 //               the unrounded P (the softmax denominator the LSE needs).
+//               A warp reaches TMEM lanes 32*(warp % 4) .. +31, so each
+//               warpgroup covers the tile's 128 rows.
 //   warps 2-3   idle.
+// Registers: launched at 168 per thread; the first warpgroup (producer, MMA
+// issuer) gives back to 104 and the softmax warpgroups take 200 each
+// (128*104 + 256*200 = 384*168, the launch allocation; no spills).
 // While one tile's softmax runs, the tensor cores work on the other tile
 // (two-tile ping-pong), so exp and MMA overlap.
 //
@@ -42,6 +47,9 @@ namespace gb300 {
 namespace {
 
 constexpr int kThreads = 384;
+constexpr int kRegsControl = 104;  // warpgroup 0 after setmaxnreg
+constexpr int kRegsSoftmax = 200;  // warpgroups 1-2 after setmaxnreg
+static_assert(128 * kRegsControl + 256 * kRegsSoftmax <= kThreads * 168, "register split");
 constexpr float kTau = 8.0f;                    // rescale threshold (log2 units)
 constexpr float kLn2 = 0.69314718055994530942f;
 constexpr float kLog2e = 1.44269504088896340736f;
@@ -86,9 +94,12 @@ __device__ __forceinline__ void raise_abort(Bars* bars, unsigned int* err) {
 template <int D>
 __device__ void run_producer(const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv,
                              uint8_t* smem, Bars* bars, const FwdParams& p, unsigned int* err) {
+    // Run by a whole warp so that every loop value is warp-uniform; one elected
+    // lane issues the copies.
     using C = FwdCfg<D>;
     const volatile int* abort_flag = &bars->abort;
     const FwdShape& s = p.shape;
+    const bool leader = elect_one();
     uint32_t q_issued[2] = {0u, 0u};
     long long L = 0;  // K/V loads issued
     int local = 0;
@@ -102,14 +113,18 @@ __device__ void run_producer(const CUtensorMap* tq, const CUtensorMap* tk, const
         const int n0 = tile_kv_count(mb, 0, s), n1 = tile_kv_count(mb, 1, s);
         const int nmax = n0 > n1 ? n0 : n1;
         for (int t = 0; t < 2 && ok; ++t) {
-            if (local > 0) ok = mbar_wait(smem_u32(&bars->q_empty[t]), (local - 1) & 1, abort_flag);
+            if (local > 0)
+                ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&bars->q_empty[t]), (local - 1) & 1, abort_flag));
             if (!ok) break;
-            const uint32_t bar = smem_u32(&bars->q_full[t]);
-            mbar_arrive_expect_tx(bar, C::kTileBytes);
-            const uint32_t dst = smem_u32(smem + t * C::kTileBytes);
+            if (leader) {
+                const uint32_t bar = smem_u32(&bars->q_full[t]);
+                mbar_arrive_expect_tx(bar, C::kTileBytes);
+                const uint32_t dst = smem_u32(smem + t * C::kTileBytes);
 #pragma unroll
-            for (int c = 0; c < D / 64; ++c)
-                tma_load_3d(dst + c * 16384, tq, bar, 64 * c, mb * kUnitRows + t * kTileM, bh);
+                for (int c = 0; c < D / 64; ++c)
+                    tma_load_3d(dst + c * 16384, tq, bar, 64 * c, mb * kUnitRows + t * kTileM, bh);
+            }
+            __syncwarp();
             ++q_issued[t];
         }
         for (int j = 0; j < nmax && ok; ++j) {
@@ -117,19 +132,25 @@ __device__ void run_producer(const CUtensorMap* tq, const CUtensorMap* tk, const
             for (int which = 0; which < 2; ++which) {
                 const int slot = (int)(L % C::kStages);
                 const long long round = L / C::kStages;
-                if (round > 0) ok = mbar_wait(smem_u32(&bars->kv_empty[slot]), (uint32_t)((round - 1) & 1), abort_flag);
+                if (round > 0)
+                    ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&bars->kv_empty[slot]),
+                                                           (uint32_t)((round - 1) & 1), abort_flag));
                 if (!ok) break;
-                const uint32_t bar = smem_u32(&bars->kv_full[slot]);
-                mbar_arrive_expect_tx(bar, C::kTileBytes);
-                const uint32_t dst = smem_u32(smem + C::kRingOff + slot * C::kTileBytes);
-                const CUtensorMap* map = which == 0 ? tk : tv;
+                if (leader) {
+                    const uint32_t bar = smem_u32(&bars->kv_full[slot]);
+                    mbar_arrive_expect_tx(bar, C::kTileBytes);
+                    const uint32_t dst = smem_u32(smem + C::kRingOff + slot * C::kTileBytes);
+                    const CUtensorMap* map = which == 0 ? tk : tv;
 #pragma unroll
-                for (int c = 0; c < D / 64; ++c) tma_load_3d(dst + c * 16384, map, bar, 64 * c, kTileN * j, bkv);
+                    for (int c = 0; c < D / 64; ++c)
+                        tma_load_3d(dst + c * 16384, map, bar, 64 * c, kTileN * j, bkv);
+                }
+                __syncwarp();
                 ++L;
             }
         }
     }
-    if (!ok) raise_abort(bars, err);
+    if (!ok && leader) raise_abort(bars, err);
     // Drain: every issued copy lands before the CTA may exit.
     for (int t = 0; t < 2; ++t)
         if (q_issued[t] > 0) mbar_wait(smem_u32(&bars->q_full[t]), (q_issued[t] - 1) & 1, nullptr);
@@ -137,31 +158,40 @@ __device__ void run_producer(const CUtensorMap* tq, const CUtensorMap* tk, const
         const long long n_s = (L - slot + C::kStages - 1) / C::kStages;
         mbar_wait(smem_u32(&bars->kv_full[slot]), (uint32_t)((n_s - 1) & 1), nullptr);
     }
+    __syncwarp();
 }
 
 // ---------------------------------------------------------------------------
 // MMA issuer (single thread)
 // ---------------------------------------------------------------------------
+// Descriptor low words (start address >> 4, LBO >> 4) of the K-major Q/K tiles
+// and the MN-major V tile; the high word (SBO = 1024 B, version, 128-B swizzle)
+// is the same constant for all three.
+constexpr uint32_t kDescHi = sdesc_hi_sw128(1024);
+
 template <int D>
-__device__ __forceinline__ void issue_qk(uint32_t tmem, int t, uint32_t q_base, uint32_t k_base,
+__device__ __forceinline__ void issue_qk(uint32_t tmem, int t, uint32_t q_lo, uint32_t k_lo,
                                          uint32_t idesc) {
     using C = FwdCfg<D>;
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
-        const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-        mma_ss(tmem + C::col_s(t), make_sdesc_sw128(q_base + off, 16, 1024),
-               make_sdesc_sw128(k_base + off, 16, 1024), idesc, kk > 0 ? 1u : 0u);
+        // +16 K-elements = +32 B inside a 128-B swizzle row; every 4 steps the
+        // next 64-column chunk (16 KiB further)
+        const uint32_t step = (kk >> 2) * (16384 >> 4) + (kk & 3) * (32 >> 4);
+        mma_ss(tmem + C::col_s(t), sdesc_join(q_lo + step, kDescHi),
+               sdesc_join(k_lo + step, kDescHi), idesc, kk > 0 ? 1u : 0u);
     }
 }
 
 template <int D>
-__device__ __forceinline__ void issue_pv(uint32_t tmem, int t, uint32_t v_base, uint32_t idesc,
+__device__ __forceinline__ void issue_pv(uint32_t tmem, int t, uint32_t v_lo, uint32_t idesc,
                                          bool accumulate) {
     using C = FwdCfg<D>;
 #pragma unroll
     for (int kk = 0; kk < kTileN / 16; ++kk) {
+        // +16 keys = +16 rows of 128 B
         mma_ts(tmem + C::col_o(t), tmem + C::col_s(t) + kk * 8,
-               make_sdesc_sw128(v_base + kk * 2048, 16384, 1024), idesc,
+               sdesc_join(v_lo + kk * (2048 >> 4), kDescHi), idesc,
                (accumulate || kk > 0) ? 1u : 0u);
     }
 }
@@ -169,13 +199,23 @@ __device__ __forceinline__ void issue_pv(uint32_t tmem, int t, uint32_t v_base, 
 template <int D>
 __device__ void run_mma(uint8_t* smem, Bars* bars, uint32_t tmem, const FwdParams& p,
                         unsigned int* err) {
+    // Run by a whole warp (warp-uniform descriptors and loop state); one elected
+    // lane issues every MMA and commit, so the commits track all of its MMAs.
     using C = FwdCfg<D>;
     const volatile int* abort_flag = &bars->abort;
     const FwdShape& s = p.shape;
+    const bool leader = elect_one();
     const uint32_t idS = make_idesc_bf16(128, kTileN, 0, 0);
     const uint32_t idO = make_idesc_bf16(128, D, 0, 1);
-    const uint32_t q_base[2] = {smem_u32(smem), smem_u32(smem + C::kTileBytes)};
+    // descriptor low words: Q tiles, and every ring slot as a K (LBO unused) or
+    // a V (LBO = 16 KiB between the two 64-column halves) operand
+    const uint32_t q_lo[2] = {sdesc_lo(smem_u32(smem), 16), sdesc_lo(smem_u32(smem + C::kTileBytes), 16)};
     const uint32_t ring = smem_u32(smem + C::kRingOff);
+    auto k_lo = [&](int slot) { return sdesc_lo(ring + slot * C::kTileBytes, 16); };
+    auto v_lo = [&](int slot) { return sdesc_lo(ring + slot * C::kTileBytes, 16384); };
+    auto wait_all = [&](uint32_t bar, uint32_t parity) {
+        return __all_sync(0xFFFFFFFFu, mbar_wait(bar, parity, abort_flag));
+    };
     long long Cn = 0;  // K/V loads consumed
     uint32_t cnt_p[2] = {0u, 0u};
     int local = 0;
@@ -185,60 +225,77 @@ __device__ void run_mma(uint8_t* smem, Bars* bars, uint32_t tmem, const FwdParam
         unit_of(s, u, bh, mb);
         const int n[2] = {tile_kv_count(mb, 0, s), tile_kv_count(mb, 1, s)};
         const int nmax = n[0] > n[1] ? n[0] : n[1];
-        for (int t = 0; t < 2 && ok; ++t) ok = mbar_wait(smem_u32(&bars->q_full[t]), local & 1, abort_flag);
+        for (int t = 0; t < 2 && ok; ++t) ok = wait_all(smem_u32(&bars->q_full[t]), local & 1);
         if (!ok) break;
         // K_0 -> S_t(0)
         int slot_k = (int)(Cn % C::kStages);
-        ok = mbar_wait(smem_u32(&bars->kv_full[slot_k]), (uint32_t)((Cn / C::kStages) & 1), abort_flag);
+        ok = wait_all(smem_u32(&bars->kv_full[slot_k]), (uint32_t)((Cn / C::kStages) & 1));
         ++Cn;
         if (!ok) break;
         tc_fence_after();
-        for (int t = 0; t < 2; ++t) {
-            if (n[t] > 0) {
-                issue_qk<D>(tmem, t, q_base[t], ring + slot_k * C::kTileBytes, idS);
-                mma_commit(smem_u32(&bars->s_full[t]));
+        if (leader) {
+            for (int t = 0; t < 2; ++t) {
+                if (n[t] > 0) {
+                    issue_qk<D>(tmem, t, q_lo[t], k_lo(slot_k), idS);
+                    mma_commit(smem_u32(&bars->s_full[t]));
+                }
+                if (n[t] <= 1) mma_commit(smem_u32(&bars->q_empty[t]));
             }
-            if (n[t] <= 1) mma_commit(smem_u32(&bars->q_empty[t]));
+            mma_commit(smem_u32(&bars->kv_empty[slot_k]));
         }
-        mma_commit(smem_u32(&bars->kv_empty[slot_k]));
+        __syncwarp();
         for (int j = 0; j < nmax && ok; ++j) {
             const int slot_v = (int)(Cn % C::kStages);
-            ok = mbar_wait(smem_u32(&bars->kv_full[slot_v]), (uint32_t)((Cn / C::kStages) & 1), abort_flag);
+            ok = wait_all(smem_u32(&bars->kv_full[slot_v]), (uint32_t)((Cn / C::kStages) & 1));
             ++Cn;
-            const bool more = j + 1 < nmax;
-            if (ok && more) {
-                slot_k = (int)(Cn % C::kStages);
-                ok = mbar_wait(smem_u32(&bars->kv_full[slot_k]), (uint32_t)((Cn / C::kStages) & 1), abort_flag);
-                ++Cn;
-            }
             if (!ok) break;
             tc_fence_after();
+            // K_{j+1} is awaited only when the first S(j+1) is about to be issued,
+            // so a late K load never holds back the P.V of this step.
+            bool k_ready = false;
             for (int t = 0; t < 2 && ok; ++t) {
                 if (j >= n[t]) continue;
-                ok = mbar_wait(smem_u32(&bars->p_full[t]), cnt_p[t] & 1, abort_flag);
+                ok = wait_all(smem_u32(&bars->p_full[t]), cnt_p[t] & 1);
                 ++cnt_p[t];
                 if (!ok) break;
                 tc_fence_after();
-                issue_pv<D>(tmem, t, ring + slot_v * C::kTileBytes, idO, j > 0);
+                if (leader) issue_pv<D>(tmem, t, v_lo(slot_v), idO, j > 0);
                 if (j + 1 < n[t]) {
+                    if (!k_ready) {
+                        slot_k = (int)(Cn % C::kStages);
+                        ok = wait_all(smem_u32(&bars->kv_full[slot_k]), (uint32_t)((Cn / C::kStages) & 1));
+                        ++Cn;
+                        if (!ok) break;
+                        tc_fence_after();
+                        k_ready = true;
+                    }
                     // Issued after PV_t(j): the tensor pipe runs this CTA's MMAs in
                     // order, so S_t(j+1) overwrites P_t(j) only once PV_t(j) has read it.
-                    issue_qk<D>(tmem, t, q_base[t], ring + slot_k * C::kTileBytes, idS);
-                    mma_commit(smem_u32(&bars->s_full[t]));
-                    if (j + 2 == n[t]) mma_commit(smem_u32(&bars->q_empty[t]));
-                } else {
+                    if (leader) {
+                        issue_qk<D>(tmem, t, q_lo[t], k_lo(slot_k), idS);
+                        mma_commit(smem_u32(&bars->s_full[t]));
+                        if (j + 2 == n[t]) mma_commit(smem_u32(&bars->q_empty[t]));
+                    }
+                } else if (leader) {
                     mma_commit(smem_u32(&bars->o_full[t]));
                 }
+                __syncwarp();
             }
             if (!ok) break;
-            mma_commit(smem_u32(&bars->kv_empty[slot_v]));
-            if (more) mma_commit(smem_u32(&bars->kv_empty[slot_k]));
+            if (leader) {
+                mma_commit(smem_u32(&bars->kv_empty[slot_v]));
+                // k_ready holds exactly when j + 1 < nmax: the producer loaded K_{j+1}
+                if (k_ready) mma_commit(smem_u32(&bars->kv_empty[slot_k]));
+            }
+            __syncwarp();
         }
     }
-    if (!ok) raise_abort(bars, err);
+    if (!ok && leader) raise_abort(bars, err);
     // Drain: all issued MMAs complete before TMEM is released.
-    mma_commit(smem_u32(&bars->drain));
+    if (leader) mma_commit(smem_u32(&bars->drain));
+    __syncwarp();
     mbar_wait(smem_u32(&bars->drain), 0, nullptr);
+    __syncwarp();
 }
 
 // ---------------------------------------------------------------------------
@@ -295,13 +352,13 @@ __device__ void run_softmax(int t, int wq, int lane, Bars* bars, uint32_t tmem, 
             }
             float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
 #pragma unroll
-            for (int cc = 0; cc < 128; cc += 4) {
-                mx0 = fmaxf(mx0, __uint_as_float(sr[cc]));
-                mx1 = fmaxf(mx1, __uint_as_float(sr[cc + 1]));
-                mx2 = fmaxf(mx2, __uint_as_float(sr[cc + 2]));
-                mx3 = fmaxf(mx3, __uint_as_float(sr[cc + 3]));
+            for (int cc = 0; cc < 128; cc += 8) {
+                mx0 = fmax3(mx0, __uint_as_float(sr[cc]), __uint_as_float(sr[cc + 1]));
+                mx1 = fmax3(mx1, __uint_as_float(sr[cc + 2]), __uint_as_float(sr[cc + 3]));
+                mx2 = fmax3(mx2, __uint_as_float(sr[cc + 4]), __uint_as_float(sr[cc + 5]));
+                mx3 = fmax3(mx3, __uint_as_float(sr[cc + 6]), __uint_as_float(sr[cc + 7]));
             }
-            const float mt = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * c;
+            const float mt = fmax3(fmaxf(mx0, mx1), mx2, mx3) * c;
             const bool need = mt > m + kTau;
             if (__any_sync(0xFFFFFFFFu, need)) {
                 const float m_new = fmaxf(m, mt);
@@ -310,47 +367,59 @@ __device__ void run_softmax(int t, int wq, int lane, Bars* bars, uint32_t tmem, 
                 lx *= alpha;
                 if (j > 0) {
                     // O_t is stable here: S_t(j) completing implies PV_t(j-1) completed.
+                    const uint64_t a2 = f2(alpha, alpha);
 #pragma unroll 1
                     for (int cc = 0; cc < D; cc += 32) {
                         uint32_t r[32];
                         tmem_ld32(tO + cc, r);
                         tmem_wait_ld();
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+                        for (int i = 0; i < 32; i += 2) {
+                            float lo, hi;
+                            f2_split(f2_mul(f2(__uint_as_float(r[i]), __uint_as_float(r[i + 1])), a2), lo, hi);
+                            r[i] = __float_as_uint(lo);
+                            r[i + 1] = __float_as_uint(hi);
+                        }
                         tmem_st32(tO + cc, r);
                     }
                 }
                 m = m_new;
             }
-            const float neg_m = -m;
-            float la = 0.f, lb = 0.f, lc = 0.f, ld = 0.f, xa = 0.f, xb = 0.f;
+            // p = 2^(s*c - m) on pairs; P rounded to bf16 into TMEM; two row sums
+            const uint64_t c2 = f2(c, c), nm2 = f2(-m, -m);
+            float acc_r0 = 0.f, acc_r1 = 0.f, acc_r2 = 0.f, acc_r3 = 0.f;
+            uint64_t acc_x0 = 0, acc_x1 = 0;  // (0.f, 0.f) pairs
 #pragma unroll
             for (int cc = 0; cc < 4; ++cc) {
                 uint32_t pk[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
                     const int col = cc * 32 + 2 * i;
-                    float p0 = ex2(fmaf(__uint_as_float(sr[col]), c, neg_m));
-                    float p1 = ex2(fmaf(__uint_as_float(sr[col + 1]), c, neg_m));
+                    float x0, x1;
+                    f2_split(f2_fma(f2(__uint_as_float(sr[col]), __uint_as_float(sr[col + 1])), c2, nm2), x0, x1);
+                    float p0 = ex2(x0), p1 = ex2(x1);
                     if (masked_tile) {
                         p0 = col <= lim ? p0 : 0.f;
                         p1 = col + 1 <= lim ? p1 : 0.f;
                     }
                     pk[i] = pack_bf16x2(p0, p1);
-                    xa += p0;
-                    xb += p1;
-                    if (i & 1) {
-                        lc += bf16lo_to_f32(pk[i]);
-                        ld += bf16hi_to_f32(pk[i]);
-                    } else {
-                        la += bf16lo_to_f32(pk[i]);
-                        lb += bf16hi_to_f32(pk[i]);
+                    switch (i & 3) {
+                        case 0: acc_r0 = add_bf16x2_f32(acc_r0, pk[i]); break;
+                        case 1: acc_r1 = add_bf16x2_f32(acc_r1, pk[i]); break;
+                        case 2: acc_r2 = add_bf16x2_f32(acc_r2, pk[i]); break;
+                        default: acc_r3 = add_bf16x2_f32(acc_r3, pk[i]); break;
                     }
+                    if (i & 1) acc_x1 = f2_add(acc_x1, f2(p0, p1));
+                    else acc_x0 = f2_add(acc_x0, f2(p0, p1));
                 }
                 tmem_st16(tS + cc * 16, pk);
             }
-            l += (la + lb) + (lc + ld);
-            lx += xa + xb;
+            {
+                float a, b;
+                l += (acc_r0 + acc_r1) + (acc_r2 + acc_r3);
+                f2_split(f2_add(acc_x0, acc_x1), a, b);
+                lx += a + b;
+            }
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
@@ -371,23 +440,21 @@ __device__ void run_softmax(int t, int wq, int lane, Bars* bars, uint32_t tmem, 
             tmem_ld32(tO + cc, r);
             tmem_wait_ld();
             if (live) {
+                const uint64_t il2 = f2(inv_l, inv_l);
+                float v[32];
+#pragma unroll
+                for (int i = 0; i < 32; i += 2)
+                    f2_split(f2_mul(f2(__uint_as_float(r[i]), __uint_as_float(r[i + 1])), il2), v[i], v[i + 1]);
                 if constexpr (OUT_F32) {
                     float4* dst = reinterpret_cast<float4*>(static_cast<float*>(o_ptr) + row_idx * D + cc);
 #pragma unroll
-                    for (int i = 0; i < 8; ++i)
-                        dst[i] = make_float4(__uint_as_float(r[4 * i]) * inv_l, __uint_as_float(r[4 * i + 1]) * inv_l,
-                                             __uint_as_float(r[4 * i + 2]) * inv_l, __uint_as_float(r[4 * i + 3]) * inv_l);
+                    for (int i = 0; i < 8; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
                 } else {
                     uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(o_ptr) + row_idx * D + cc);
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        uint4 w;
-                        w.x = pack_bf16x2(__uint_as_float(r[8 * i + 0]) * inv_l, __uint_as_float(r[8 * i + 1]) * inv_l);
-                        w.y = pack_bf16x2(__uint_as_float(r[8 * i + 2]) * inv_l, __uint_as_float(r[8 * i + 3]) * inv_l);
-                        w.z = pack_bf16x2(__uint_as_float(r[8 * i + 4]) * inv_l, __uint_as_float(r[8 * i + 5]) * inv_l);
-                        w.w = pack_bf16x2(__uint_as_float(r[8 * i + 6]) * inv_l, __uint_as_float(r[8 * i + 7]) * inv_l);
-                        dst[i] = w;
-                    }
+                    for (int i = 0; i < 4; ++i)
+                        dst[i] = make_uint4(pack_bf16x2(v[8 * i], v[8 * i + 1]), pack_bf16x2(v[8 * i + 2], v[8 * i + 3]),
+                                            pack_bf16x2(v[8 * i + 4], v[8 * i + 5]), pack_bf16x2(v[8 * i + 6], v[8 * i + 7]));
                 }
             }
         }
@@ -437,11 +504,12 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
     tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
 
-    if (warp == 0) {
-        if (lane == 0) run_producer<D>(&tq, &tk, &tv, smem, bars, p, err);
-    } else if (warp == 1) {
-        if (lane == 0) run_mma<D>(smem, bars, tmem, p, err);
-    } else if (warp >= 4) {
+    if (warp < 4) {
+        reg_dealloc<kRegsControl>();
+        if (warp == 0) run_producer<D>(&tq, &tk, &tv, smem, bars, p, err);
+        if (warp == 1) run_mma<D>(smem, bars, tmem, p, err);
+    } else {
+        reg_alloc<kRegsSoftmax>();
         const int t = (warp - 4) >> 2;
         run_softmax<D, OUT_F32>(t, warp & 3, lane, bars, tmem, p, o_ptr, lse_ptr, err);
     }

@@ -35,6 +35,18 @@ enum : uint32_t {
 // Every spin-wait in the kernels gives up after this many nanoseconds.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 
+// One lane of a fully active warp (elect.sync): the issuing lane of a role
+// that the whole warp runs, so its loop values stay warp-uniform.
+__device__ __forceinline__ bool elect_one() {
+    uint32_t pred;
+    asm volatile(
+        "{\n\t.reg .pred P;\n\t"
+        "elect.sync _|P, 0xffffffff;\n\t"
+        "selp.u32 %0, 1, 0, P;\n\t}"
+        : "=r"(pred));
+    return pred != 0;
+}
+
 // ---------------------------------------------------------------------------
 // mbarrier
 // ---------------------------------------------------------------------------
@@ -71,6 +83,22 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// try_wait that may suspend the thread for up to `hint_ns` (it resumes when the
+// phase completes), so a waiting warp does not take issue slots from others.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
+constexpr uint32_t kSuspendHintNs = 20000;  // 20 us per try
+
 // Bounded wait for the phase of parity `parity` to complete.  Returns false
 // (and leaves the barrier untouched) if the limit ran out or *abort became
 // non-zero; the caller then takes its exit path.
@@ -78,13 +106,10 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
                                           const volatile int* abort_flag) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
-    uint32_t spins = 0;
     while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((++spins & 63u) == 0u) {
-            if (abort_flag && *abort_flag) return false;
-            if (global_timer_ns() - t0 > kWaitLimitNs) return false;
-        }
+        if (mbar_try_wait_sleep(bar, parity, kSuspendHintNs)) return true;
+        if (abort_flag && *abort_flag) return false;
+        if (global_timer_ns() - t0 > kWaitLimitNs) return false;
     }
 }
 
@@ -182,6 +207,21 @@ __device__ __forceinline__ uint64_t make_sdesc_sw128(uint32_t saddr, uint32_t lb
     return d;
 }
 
+// The same descriptor split into its two 32-bit words, so that an MMA loop
+// can step the start address with one 32-bit add on the low word (the start
+// field never carries into LBO within one tile).
+__device__ __forceinline__ uint32_t sdesc_lo(uint32_t saddr, uint32_t lbo_bytes) {
+    return ((saddr & 0x3FFFFu) >> 4) | (((lbo_bytes >> 4) & 0x3FFFu) << 16);
+}
+__host__ __device__ constexpr uint32_t sdesc_hi_sw128(uint32_t sbo_bytes) {
+    return ((sbo_bytes >> 4) & 0x3FFFu) | (1u << 14) | (2u << 29);
+}
+__device__ __forceinline__ uint64_t sdesc_join(uint32_t lo, uint32_t hi) {
+    uint64_t d;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "r"(lo), "r"(hi));
+    return d;
+}
+
 // 32 lanes x 32 columns of 32-bit TMEM cells -> 32 registers per thread.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
     asm volatile(
@@ -252,6 +292,61 @@ __device__ __forceinline__ float bf16lo_to_f32(uint32_t packed) {
 }
 __device__ __forceinline__ float bf16hi_to_f32(uint32_t packed) {
     return __uint_as_float(packed & 0xFFFF0000u);
+}
+
+// Per-warpgroup register budget changes (all 4 warps of a warpgroup execute
+// the same one).  The split must stay within the launch allocation.
+template <int N>
+__device__ __forceinline__ void reg_dealloc() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void reg_alloc() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+// Packed pairs of fp32 (one 64-bit register), operated on two lanes at a time
+// by the f32x2 instructions of sm_100+.
+__device__ __forceinline__ uint64_t f2(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void f2_split(uint64_t v, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+// acc + lo(pk) + hi(pk) where pk holds two bf16 values; each add widens the bf16
+// exactly and rounds to nearest in fp32 (mixed-precision add, sm_100+).
+__device__ __forceinline__ float add_bf16x2_f32(float acc, uint32_t pk) {
+    float r;
+    asm("{\n\t.reg .b16 lo, hi;\n\t"
+        "mov.b32 {lo, hi}, %2;\n\t"
+        "add.rn.f32.bf16 %0, lo, %1;\n\t"
+        "add.rn.f32.bf16 %0, hi, %0;\n\t}"
+        : "=f"(r)
+        : "f"(acc), "r"(pk));
+    return r;
+}
+// max of three fp32 values in one instruction (sm_100+)
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
 }
 
 }  // namespace gb300
