@@ -67,20 +67,38 @@ attn_status_t current_device_info(DeviceInfo* out) {
     return ATTN_OK;
 }
 
+static bool load_encoder() {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_encode) {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                             &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || !fn)
+            return false;
+        g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    return true;
+}
+
+attn_status_t encode_tmap_out_3d(CUtensorMap* map, void* base, bool f32, int d, int rows,
+                                 long long heads, int box_cols, int box_rows) {
+    if (!load_encoder()) return ATTN_ERR_CUDA;
+    const cuuint64_t es = f32 ? 4 : 2;
+    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)rows, (cuuint64_t)heads};
+    cuuint64_t strides[2] = {(cuuint64_t)d * es, (cuuint64_t)d * es * (cuuint64_t)rows};
+    cuuint32_t box[3] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows, 1u};
+    cuuint32_t elem[3] = {1u, 1u, 1u};
+    CUresult r = g_encode(map, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                          3, base, dims, strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
 attn_status_t encode_tmap_bf16_3d(CUtensorMap* map, const void* base, int d, int rows,
                                   long long heads, int box_rows) {
-    {
-        std::lock_guard<std::mutex> lk(g_mu);
-        if (!g_encode) {
-            void* fn = nullptr;
-            cudaDriverEntryPointQueryResult q;
-            if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
-                                                 cudaEnableDefault, &q) != cudaSuccess ||
-                q != cudaDriverEntryPointSuccess || !fn)
-                return ATTN_ERR_CUDA;
-            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-        }
-    }
+    if (!load_encoder()) return ATTN_ERR_CUDA;
     cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)rows, (cuuint64_t)heads};
     cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)d * 2 * (cuuint64_t)rows};
     cuuint32_t box[3] = {64u, (cuuint32_t)box_rows, 1u};

@@ -14,9 +14,10 @@
 //               conditional rescaling with threshold tau = 8), writes P as
 //               bf16 into TMEM over its S columns, and at the end of the
 //               unit normalises O by 1/l and writes O and the logsumexp.
-//               Two row sums are kept: l over the bf16-rounded P that
-//               multiplies V (so O's weights sum to exactly one) and lx over
-//               the unrounded P (the softmax denominator the LSE needs).
+//               Two row sums are kept: lx over the unrounded P (the softmax
+//               denominator the LSE needs) and l = lx plus, per tile, the
+//               rounding error of the tile's largest bf16 P, which normalises
+//               O (a row dominated by one key then gets exactly that V row).
 //               A warp reaches TMEM lanes 32*(warp % 4) .. +31, so each
 //               warpgroup covers the tile's 128 rows.
 //   warps 2-3   idle.
@@ -60,12 +61,19 @@ struct FwdCfg {
     static constexpr int kTileBytes = 128 * D * 2;        // one 128-row bf16 tile
     static constexpr int kStages = (D == 128) ? 4 : 8;     // K/V ring slots
     static constexpr int kRingOff = 2 * kTileBytes;        // after Q0, Q1
-    static constexpr int kBarOff = kRingOff + kStages * kTileBytes;
+    // epilogue staging: per softmax warp, two 2 KiB buffers (32 rows x 64 B)
+    static constexpr int kStgOff = kRingOff + kStages * kTileBytes;
+    static constexpr int kStgBytesPerWarp = 2 * 2048;
+    static constexpr int kBarOff = kStgOff + 8 * kStgBytesPerWarp;
     static constexpr int kSmemBytes = kBarOff + 256 + 1024;  // barriers + alignment slack
+    static_assert(kSmemBytes <= 232448, "shared memory budget");
     // TMEM column of S_t and of O_t
     static __host__ __device__ constexpr uint32_t col_s(int t) { return uint32_t(t) * 128u; }
     static __host__ __device__ constexpr uint32_t col_o(int t) { return 256u + uint32_t(t) * D; }
 };
+
+// Output columns per staged epilogue chunk: 64 bytes per row either way.
+__host__ __device__ constexpr int kEpiCols(bool f32) { return f32 ? 16 : 32; }
 
 struct FwdParams {
     FwdShape shape;
@@ -255,7 +263,7 @@ __device__ void run_mma(uint8_t* smem, Bars* bars, uint32_t tmem, const FwdParam
             bool k_ready = false;
             for (int t = 0; t < 2 && ok; ++t) {
                 if (j >= n[t]) continue;
-                ok = wait_all(smem_u32(&bars->p_full[t]), cnt_p[t] & 1);
+                ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&bars->p_full[t]), cnt_p[t] & 1, abort_flag, 32));
                 ++cnt_p[t];
                 if (!ok) break;
                 tc_fence_after();
@@ -301,9 +309,100 @@ __device__ void run_mma(uint8_t* smem, Bars* bars, uint32_t tmem, const FwdParam
 // ---------------------------------------------------------------------------
 // Softmax / correction / epilogue warpgroup (one thread per query row)
 // ---------------------------------------------------------------------------
+// One KV tile of the online softmax for this thread's query row: the causal /
+// tail mask (MASKED only: with the mask in a separate instantiation, the
+// unmasked tiles carry no per-element compare or select), the tile max, the
+// conditional rescale of O (tau), P = 2^(s*c - m) rounded to bf16 into TMEM
+// over the S columns, and the row sums: lx over the unrounded P (the softmax
+// denominator, for the LSE) and l, which normalises O: lx plus the rounding
+// error of the tile's largest P, so that the weight of the dominant key of a
+// tile in O is exactly its rounded P over the sum.
+template <int D, bool MASKED>
+__device__ __forceinline__ void softmax_tile(uint32_t (&sr)[128], int lim, int j, float c,
+                                             uint32_t tS, uint32_t tO, float& m, float& l,
+                                             float& lx) {
+    if constexpr (MASKED) {
+#pragma unroll
+        for (int cc = 0; cc < 128; ++cc)
+            if (cc > lim) sr[cc] = kNegInfBits;
+    }
+    float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+#pragma unroll
+    for (int cc = 0; cc < 128; cc += 8) {
+        mx0 = fmax3(mx0, __uint_as_float(sr[cc]), __uint_as_float(sr[cc + 1]));
+        mx1 = fmax3(mx1, __uint_as_float(sr[cc + 2]), __uint_as_float(sr[cc + 3]));
+        mx2 = fmax3(mx2, __uint_as_float(sr[cc + 4]), __uint_as_float(sr[cc + 5]));
+        mx3 = fmax3(mx3, __uint_as_float(sr[cc + 6]), __uint_as_float(sr[cc + 7]));
+    }
+    const float mt = fmax3(fmaxf(mx0, mx1), mx2, mx3) * c;
+    const bool need = mt > m + kTau;
+    if (__any_sync(0xFFFFFFFFu, need)) {
+        const float m_new = fmaxf(m, mt);
+        const float alpha = ex2(m - m_new);
+        l *= alpha;
+        lx *= alpha;
+        if (j > 0) {
+            // O_t is stable here: S_t(j) completing implies PV_t(j-1) completed.
+            const uint64_t a2 = f2(alpha, alpha);
+#pragma unroll 1
+            for (int cc = 0; cc < D; cc += 32) {
+                uint32_t r[32];
+                tmem_ld32(tO + cc, r);
+                tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 32; i += 2) {
+                    float lo, hi;
+                    f2_split(f2_mul(f2(__uint_as_float(r[i]), __uint_as_float(r[i + 1])), a2), lo, hi);
+                    r[i] = __float_as_uint(lo);
+                    r[i + 1] = __float_as_uint(hi);
+                }
+                tmem_st32(tO + cc, r);
+            }
+        }
+        m = m_new;
+    }
+    // rounding error of the tile's largest probability (same arithmetic as below)
+    {
+        const float pmax = ex2(fmaf(fmax3(fmaxf(mx0, mx1), mx2, mx3), c, -m));
+        l += bf16lo_to_f32(pack_bf16x2(pmax, 0.f)) - pmax;
+    }
+    // p = 2^(s*c - m) on pairs; P rounded to bf16 into TMEM; unrounded row sum
+    const uint64_t c2 = f2(c, c), nm2 = f2(-m, -m);
+    uint64_t acc_x0 = 0, acc_x1 = 0, acc_x2 = 0, acc_x3 = 0;  // (0.f, 0.f) pairs
+#pragma unroll
+    for (int cc = 0; cc < 4; ++cc) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const int col = cc * 32 + 2 * i;
+            float x0, x1;
+            f2_split(f2_fma(f2(__uint_as_float(sr[col]), __uint_as_float(sr[col + 1])), c2, nm2), x0, x1);
+            float p0 = ex2(x0), p1 = ex2(x1);
+            if constexpr (MASKED) {
+                p0 = col <= lim ? p0 : 0.f;
+                p1 = col + 1 <= lim ? p1 : 0.f;
+            }
+            pk[i] = pack_bf16x2(p0, p1);
+            switch (i & 3) {
+                case 0: acc_x0 = f2_add(acc_x0, f2(p0, p1)); break;
+                case 1: acc_x1 = f2_add(acc_x1, f2(p0, p1)); break;
+                case 2: acc_x2 = f2_add(acc_x2, f2(p0, p1)); break;
+                default: acc_x3 = f2_add(acc_x3, f2(p0, p1)); break;
+            }
+        }
+        tmem_st16(tS + cc * 16, pk);
+    }
+    {
+        float a, b;
+        f2_split(f2_add(f2_add(acc_x0, acc_x1), f2_add(acc_x2, acc_x3)), a, b);
+        lx += a + b;
+        l += a + b;
+    }
+}
+
 template <int D, bool OUT_F32>
-__device__ void run_softmax(int t, int wq, int lane, Bars* bars, uint32_t tmem, const FwdParams& p,
-                            void* __restrict__ o_ptr, float* __restrict__ lse_ptr,
+__device__ void run_softmax(int t, int wq, int lane, uint8_t* smem, Bars* bars, uint32_t tmem,
+                            const FwdParams& p, const CUtensorMap* to, float* __restrict__ lse_ptr,
                             unsigned int* err) {
     using C = FwdCfg<D>;
     const volatile int* abort_flag = &bars->abort;
@@ -315,6 +414,8 @@ __device__ void run_softmax(int t, int wq, int lane, Bars* bars, uint32_t tmem, 
     const uint32_t bar_p = smem_u32(&bars->p_full[t]);
     const uint32_t bar_o = smem_u32(&bars->o_full[t]);
     const float c = p.c;
+    uint8_t* stg = smem + C::kStgOff + (t * 4 + wq) * C::kStgBytesPerWarp;
+    uint32_t epi_buf = 0;
     uint32_t cnt_s = 0, cnt_o = 0;
     bool ok = true;
     for (long long u = blockIdx.x; u < s.units && ok; u += gridDim.x) {
@@ -330,10 +431,10 @@ __device__ void run_softmax(int t, int wq, int lane, Bars* bars, uint32_t tmem, 
             last_key = lk < last_key ? lk : last_key;
         }
         float m = -INFINITY;  // running max of scaled scores, log2 units
-        float l = 0.f;        // running sum of the bf16-rounded probabilities (normalises O)
+        float l = 0.f;        // normaliser of O (see softmax_tile)
         float lx = 0.f;       // running sum of the unrounded probabilities (gives the LSE)
         for (int j = 0; j < n_t; ++j) {
-            ok = mbar_wait(bar_s, cnt_s & 1, abort_flag);
+            ok = mbar_wait(bar_s, cnt_s & 1, abort_flag, 32);
             ++cnt_s;
             if (!ok) break;
             tc_fence_after();
@@ -344,82 +445,10 @@ __device__ void run_softmax(int t, int wq, int lane, Bars* bars, uint32_t tmem, 
             tmem_ld32(tS + 96, *reinterpret_cast<uint32_t(*)[32]>(&sr[96]));
             tmem_wait_ld();
             const int lim = last_key - j * kTileN;  // column c allowed iff c <= lim
-            const bool masked_tile = __any_sync(0xFFFFFFFFu, lim < kTileN - 1);
-            if (masked_tile) {
-#pragma unroll
-                for (int cc = 0; cc < 128; ++cc)
-                    if (cc > lim) sr[cc] = kNegInfBits;
-            }
-            float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
-#pragma unroll
-            for (int cc = 0; cc < 128; cc += 8) {
-                mx0 = fmax3(mx0, __uint_as_float(sr[cc]), __uint_as_float(sr[cc + 1]));
-                mx1 = fmax3(mx1, __uint_as_float(sr[cc + 2]), __uint_as_float(sr[cc + 3]));
-                mx2 = fmax3(mx2, __uint_as_float(sr[cc + 4]), __uint_as_float(sr[cc + 5]));
-                mx3 = fmax3(mx3, __uint_as_float(sr[cc + 6]), __uint_as_float(sr[cc + 7]));
-            }
-            const float mt = fmax3(fmaxf(mx0, mx1), mx2, mx3) * c;
-            const bool need = mt > m + kTau;
-            if (__any_sync(0xFFFFFFFFu, need)) {
-                const float m_new = fmaxf(m, mt);
-                const float alpha = ex2(m - m_new);
-                l *= alpha;
-                lx *= alpha;
-                if (j > 0) {
-                    // O_t is stable here: S_t(j) completing implies PV_t(j-1) completed.
-                    const uint64_t a2 = f2(alpha, alpha);
-#pragma unroll 1
-                    for (int cc = 0; cc < D; cc += 32) {
-                        uint32_t r[32];
-                        tmem_ld32(tO + cc, r);
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int i = 0; i < 32; i += 2) {
-                            float lo, hi;
-                            f2_split(f2_mul(f2(__uint_as_float(r[i]), __uint_as_float(r[i + 1])), a2), lo, hi);
-                            r[i] = __float_as_uint(lo);
-                            r[i + 1] = __float_as_uint(hi);
-                        }
-                        tmem_st32(tO + cc, r);
-                    }
-                }
-                m = m_new;
-            }
-            // p = 2^(s*c - m) on pairs; P rounded to bf16 into TMEM; two row sums
-            const uint64_t c2 = f2(c, c), nm2 = f2(-m, -m);
-            float acc_r0 = 0.f, acc_r1 = 0.f, acc_r2 = 0.f, acc_r3 = 0.f;
-            uint64_t acc_x0 = 0, acc_x1 = 0;  // (0.f, 0.f) pairs
-#pragma unroll
-            for (int cc = 0; cc < 4; ++cc) {
-                uint32_t pk[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const int col = cc * 32 + 2 * i;
-                    float x0, x1;
-                    f2_split(f2_fma(f2(__uint_as_float(sr[col]), __uint_as_float(sr[col + 1])), c2, nm2), x0, x1);
-                    float p0 = ex2(x0), p1 = ex2(x1);
-                    if (masked_tile) {
-                        p0 = col <= lim ? p0 : 0.f;
-                        p1 = col + 1 <= lim ? p1 : 0.f;
-                    }
-                    pk[i] = pack_bf16x2(p0, p1);
-                    switch (i & 3) {
-                        case 0: acc_r0 = add_bf16x2_f32(acc_r0, pk[i]); break;
-                        case 1: acc_r1 = add_bf16x2_f32(acc_r1, pk[i]); break;
-                        case 2: acc_r2 = add_bf16x2_f32(acc_r2, pk[i]); break;
-                        default: acc_r3 = add_bf16x2_f32(acc_r3, pk[i]); break;
-                    }
-                    if (i & 1) acc_x1 = f2_add(acc_x1, f2(p0, p1));
-                    else acc_x0 = f2_add(acc_x0, f2(p0, p1));
-                }
-                tmem_st16(tS + cc * 16, pk);
-            }
-            {
-                float a, b;
-                l += (acc_r0 + acc_r1) + (acc_r2 + acc_r3);
-                f2_split(f2_add(acc_x0, acc_x1), a, b);
-                lx += a + b;
-            }
+            if (__any_sync(0xFFFFFFFFu, lim < kTileN - 1))
+                softmax_tile<D, true>(sr, lim, j, c, tS, tO, m, l, lx);
+            else
+                softmax_tile<D, false>(sr, lim, j, c, tS, tO, m, l, lx);
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
@@ -434,39 +463,58 @@ __device__ void run_softmax(int t, int wq, int lane, Bars* bars, uint32_t tmem, 
         const bool live = row < s.Nq;
         const float inv_l = 1.0f / l;
         const size_t row_idx = (size_t)bh * s.Nq + (size_t)row;
+        // O rows are staged 32 rows x 64 bytes at a time in shared memory and
+        // written by TMA stores (rows past Nq are clipped by the hardware), so
+        // the warp does not wait for the global writes.
+        constexpr int kCols = kEpiCols(OUT_F32);
+        const int row0 = mb * kUnitRows + t * kTileM + wq * 32;
+        const uint64_t il2 = f2(inv_l, inv_l);
 #pragma unroll 1
         for (int cc = 0; cc < D; cc += 32) {
             uint32_t r[32];
             tmem_ld32(tO + cc, r);
             tmem_wait_ld();
-            if (live) {
-                const uint64_t il2 = f2(inv_l, inv_l);
-                float v[32];
+            float v[32];
 #pragma unroll
-                for (int i = 0; i < 32; i += 2)
-                    f2_split(f2_mul(f2(__uint_as_float(r[i]), __uint_as_float(r[i + 1])), il2), v[i], v[i + 1]);
+            for (int i = 0; i < 32; i += 2)
+                f2_split(f2_mul(f2(__uint_as_float(r[i]), __uint_as_float(r[i + 1])), il2), v[i], v[i + 1]);
+#pragma unroll
+            for (int h = 0; h < 32 / kCols; ++h) {
+                uint8_t* buf = stg + (epi_buf & 1) * 2048;
+                if (lane == 0) bulk_wait_group_read<1>();  // this buffer's previous store has read it
+                __syncwarp();
+                uint4* dst = reinterpret_cast<uint4*>(buf + lane * 64);
                 if constexpr (OUT_F32) {
-                    float4* dst = reinterpret_cast<float4*>(static_cast<float*>(o_ptr) + row_idx * D + cc);
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+                    for (int i = 0; i < 4; ++i)
+                        dst[i] = make_uint4(__float_as_uint(v[h * 16 + 4 * i]), __float_as_uint(v[h * 16 + 4 * i + 1]),
+                                            __float_as_uint(v[h * 16 + 4 * i + 2]), __float_as_uint(v[h * 16 + 4 * i + 3]));
                 } else {
-                    uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(o_ptr) + row_idx * D + cc);
 #pragma unroll
                     for (int i = 0; i < 4; ++i)
                         dst[i] = make_uint4(pack_bf16x2(v[8 * i], v[8 * i + 1]), pack_bf16x2(v[8 * i + 2], v[8 * i + 3]),
                                             pack_bf16x2(v[8 * i + 4], v[8 * i + 5]), pack_bf16x2(v[8 * i + 6], v[8 * i + 7]));
                 }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    tma_store_3d(to, smem_u32(buf), cc + h * kCols, row0, bh);
+                    bulk_commit_group();
+                }
+                ++epi_buf;
             }
         }
         if (live && lse_ptr) lse_ptr[row_idx] = (m + log2f(lx)) * kLn2;
     }
+    if (lane == 0) bulk_wait_group_all();  // every staged store has completed
+    __syncwarp();
     if (!ok) raise_abort(bars, err);
 }
 
 template <int D, bool OUT_F32>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
-                const __grid_constant__ CUtensorMap tv, void* __restrict__ o_ptr,
+                const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap to,
                 float* __restrict__ lse_ptr, const FwdParams p, unsigned int* err) {
     using C = FwdCfg<D>;
     extern __shared__ uint8_t smem_raw[];
@@ -494,6 +542,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
         tma_prefetch_desc(&tq);
         tma_prefetch_desc(&tk);
         tma_prefetch_desc(&tv);
+        tma_prefetch_desc(&to);
     }
     if (warp == 1) {
         tmem_alloc(smem_u32(&bars->tmem_base), 512);
@@ -511,7 +560,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
     } else {
         reg_alloc<kRegsSoftmax>();
         const int t = (warp - 4) >> 2;
-        run_softmax<D, OUT_F32>(t, warp & 3, lane, bars, tmem, p, o_ptr, lse_ptr, err);
+        run_softmax<D, OUT_F32>(t, warp & 3, lane, smem, bars, tmem, p, &to, lse_ptr, err);
     }
     tc_fence_before();
     __syncthreads();
@@ -524,8 +573,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
 
 template <int D, bool OUT_F32>
 attn_status_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                           void* o, float* lse, const FwdParams& p, cudaStream_t stream,
-                           const DeviceInfo& dev) {
+                           const CUtensorMap& to, float* lse, const FwdParams& p,
+                           cudaStream_t stream, const DeviceInfo& dev) {
     using C = FwdCfg<D>;
     static int attr_set[64] = {0};
     if (dev.device < 64 && !attr_set[dev.device]) {
@@ -537,7 +586,7 @@ attn_status_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const C
     }
     long long grid = p.shape.units < dev.num_sms ? p.shape.units : dev.num_sms;
     attn_fwd_kernel<D, OUT_F32><<<(unsigned)grid, kThreads, C::kSmemBytes, stream>>>(
-        tq, tk, tv, o, lse, p, dev.err_word);
+        tq, tk, tv, to, lse, p, dev.err_word);
     return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
@@ -551,18 +600,20 @@ attn_status_t launch_fwd(const void* q, const void* k, const void* v, void* o, f
     p.group = Hq / Hkv;
     p.off = Nk - Nq;
     p.c = scale * kLog2e;
-    CUtensorMap tq, tk, tv;
+    CUtensorMap tq, tk, tv, to;
     attn_status_t st;
+    const bool f32 = o_dtype == ATTN_OUT_F32;
     if ((st = encode_tmap_bf16_3d(&tq, q, d, Nq, (long long)B * Hq, kTileM)) != ATTN_OK) return st;
     if ((st = encode_tmap_bf16_3d(&tk, k, d, Nk, (long long)B * Hkv, kTileN)) != ATTN_OK) return st;
     if ((st = encode_tmap_bf16_3d(&tv, v, d, Nk, (long long)B * Hkv, kTileN)) != ATTN_OK) return st;
-    const bool f32 = o_dtype == ATTN_OUT_F32;
+    if ((st = encode_tmap_out_3d(&to, o, f32, d, Nq, (long long)B * Hq, kEpiCols(f32), 32)) != ATTN_OK)
+        return st;
     if (d == 128)
-        return f32 ? launch_fwd_t<128, true>(tq, tk, tv, o, lse, p, stream, dev)
-                   : launch_fwd_t<128, false>(tq, tk, tv, o, lse, p, stream, dev);
+        return f32 ? launch_fwd_t<128, true>(tq, tk, tv, to, lse, p, stream, dev)
+                   : launch_fwd_t<128, false>(tq, tk, tv, to, lse, p, stream, dev);
     if (d == 64)
-        return f32 ? launch_fwd_t<64, true>(tq, tk, tv, o, lse, p, stream, dev)
-                   : launch_fwd_t<64, false>(tq, tk, tv, o, lse, p, stream, dev);
+        return f32 ? launch_fwd_t<64, true>(tq, tk, tv, to, lse, p, stream, dev)
+                   : launch_fwd_t<64, false>(tq, tk, tv, to, lse, p, stream, dev);
     return ATTN_ERR_UNSUPPORTED;
 }
 

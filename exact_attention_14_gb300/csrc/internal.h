@@ -22,6 +22,11 @@ attn_status_t current_device_info(DeviceInfo* out);
 attn_status_t encode_tmap_bf16_3d(CUtensorMap* map, const void* base, int d, int rows,
                                   long long heads, int box_rows);
 
+// 3-D tensor map over an output [heads, rows, d] array (bf16 or fp32), no
+// swizzle, box of box_cols x box_rows x 1, for TMA stores of staged tiles.
+attn_status_t encode_tmap_out_3d(CUtensorMap* map, void* base, bool f32, int d, int rows,
+                                 long long heads, int box_cols, int box_rows);
+
 attn_status_t launch_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
                          int B, int Hq, int Hkv, int Nq, int Nk, int d, int causal, float scale,
                          attn_out_dtype_t o_dtype, cudaStream_t stream, const DeviceInfo& dev);

@@ -103,8 +103,11 @@ constexpr uint32_t kSuspendHintNs = 20000;  // 20 us per try
 // (and leaves the barrier untouched) if the limit ran out or *abort became
 // non-zero; the caller then takes its exit path.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
-                                          const volatile int* abort_flag) {
+                                          const volatile int* abort_flag, int polls = 0) {
     if (mbar_try_wait(bar, parity)) return true;
+    // latency-critical waiters poll a few times before sleeping
+    for (int i = 0; i < polls; ++i)
+        if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     while (true) {
         if (mbar_try_wait_sleep(bar, parity, kSuspendHintNs)) return true;
@@ -127,6 +130,28 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
         " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
         : "memory");
+}
+
+// Shared -> global tensor store (bulk-group completion); rows past the tensor's
+// extent are clipped by the hardware.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int x, int y, int z) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+            reinterpret_cast<uint64_t>(map)),
+        "r"(src), "r"(x), "r"(y), "r"(z)
+        : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() {
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// Wait until at most N committed bulk groups still read their shared source.
+template <int N>
+__device__ __forceinline__ void bulk_wait_group_read() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+// Wait until every committed bulk group has completed.
+__device__ __forceinline__ void bulk_wait_group_all() {
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
 // ---------------------------------------------------------------------------
