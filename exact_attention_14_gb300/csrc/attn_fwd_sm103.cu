@@ -186,8 +186,8 @@ __device__ __forceinline__ void issue_qk(uint32_t tmem, int t, uint32_t q_lo, ui
         // +16 K-elements = +32 B inside a 128-B swizzle row; every 4 steps the
         // next 64-column chunk (16 KiB further)
         const uint32_t step = (kk >> 2) * (16384 >> 4) + (kk & 3) * (32 >> 4);
-        mma_ss(tmem + C::col_s(t), sdesc_join(q_lo + step, kDescHi),
-               sdesc_join(k_lo + step, kDescHi), idesc, kk > 0 ? 1u : 0u);
+        mma_ss_warp(tmem + C::col_s(t), sdesc_join(q_lo + step, kDescHi),
+                    sdesc_join(k_lo + step, kDescHi), idesc, kk > 0 ? 1u : 0u);
     }
 }
 
@@ -198,9 +198,9 @@ __device__ __forceinline__ void issue_pv(uint32_t tmem, int t, uint32_t v_lo, ui
 #pragma unroll
     for (int kk = 0; kk < kTileN / 16; ++kk) {
         // +16 keys = +16 rows of 128 B
-        mma_ts(tmem + C::col_o(t), tmem + C::col_s(t) + kk * 8,
-               sdesc_join(v_lo + kk * (2048 >> 4), kDescHi), idesc,
-               (accumulate || kk > 0) ? 1u : 0u);
+        mma_ts_warp(tmem + C::col_o(t), tmem + C::col_s(t) + kk * 8,
+                    sdesc_join(v_lo + kk * (2048 >> 4), kDescHi), idesc,
+                    (accumulate || kk > 0) ? 1u : 0u);
     }
 }
 
@@ -208,7 +208,9 @@ template <int D>
 __device__ void run_mma(uint8_t* smem, Bars* bars, uint32_t tmem, const FwdParams& p,
                         unsigned int* err) {
     // Run by a whole warp (warp-uniform descriptors and loop state); one elected
-    // lane issues every MMA and commit, so the commits track all of its MMAs.
+    // lane issues every MMA and commit (elect.sync inside each instruction
+    // block), so the commits track all of its MMAs.  A single issuer keeps each
+    // tile's PV and S MMAs contiguous in the tensor pipe's queue.
     using C = FwdCfg<D>;
     const volatile int* abort_flag = &bars->abort;
     const FwdShape& s = p.shape;
@@ -241,17 +243,14 @@ __device__ void run_mma(uint8_t* smem, Bars* bars, uint32_t tmem, const FwdParam
         ++Cn;
         if (!ok) break;
         tc_fence_after();
-        if (leader) {
-            for (int t = 0; t < 2; ++t) {
-                if (n[t] > 0) {
-                    issue_qk<D>(tmem, t, q_lo[t], k_lo(slot_k), idS);
-                    mma_commit(smem_u32(&bars->s_full[t]));
-                }
-                if (n[t] <= 1) mma_commit(smem_u32(&bars->q_empty[t]));
+        for (int t = 0; t < 2; ++t) {
+            if (n[t] > 0) {
+                issue_qk<D>(tmem, t, q_lo[t], k_lo(slot_k), idS);
+                mma_commit_warp(smem_u32(&bars->s_full[t]));
             }
-            mma_commit(smem_u32(&bars->kv_empty[slot_k]));
+            if (n[t] <= 1) mma_commit_warp(smem_u32(&bars->q_empty[t]));
         }
-        __syncwarp();
+        mma_commit_warp(smem_u32(&bars->kv_empty[slot_k]));
         for (int j = 0; j < nmax && ok; ++j) {
             const int slot_v = (int)(Cn % C::kStages);
             ok = wait_all(smem_u32(&bars->kv_full[slot_v]), (uint32_t)((Cn / C::kStages) & 1));
@@ -267,7 +266,7 @@ __device__ void run_mma(uint8_t* smem, Bars* bars, uint32_t tmem, const FwdParam
                 ++cnt_p[t];
                 if (!ok) break;
                 tc_fence_after();
-                if (leader) issue_pv<D>(tmem, t, v_lo(slot_v), idO, j > 0);
+                issue_pv<D>(tmem, t, v_lo(slot_v), idO, j > 0);
                 if (j + 1 < n[t]) {
                     if (!k_ready) {
                         slot_k = (int)(Cn % C::kStages);
@@ -279,29 +278,22 @@ __device__ void run_mma(uint8_t* smem, Bars* bars, uint32_t tmem, const FwdParam
                     }
                     // Issued after PV_t(j): the tensor pipe runs this CTA's MMAs in
                     // order, so S_t(j+1) overwrites P_t(j) only once PV_t(j) has read it.
-                    if (leader) {
-                        issue_qk<D>(tmem, t, q_lo[t], k_lo(slot_k), idS);
-                        mma_commit(smem_u32(&bars->s_full[t]));
-                        if (j + 2 == n[t]) mma_commit(smem_u32(&bars->q_empty[t]));
-                    }
-                } else if (leader) {
-                    mma_commit(smem_u32(&bars->o_full[t]));
+                    issue_qk<D>(tmem, t, q_lo[t], k_lo(slot_k), idS);
+                    mma_commit_warp(smem_u32(&bars->s_full[t]));
+                    if (j + 2 == n[t]) mma_commit_warp(smem_u32(&bars->q_empty[t]));
+                } else {
+                    mma_commit_warp(smem_u32(&bars->o_full[t]));
                 }
-                __syncwarp();
             }
             if (!ok) break;
-            if (leader) {
-                mma_commit(smem_u32(&bars->kv_empty[slot_v]));
-                // k_ready holds exactly when j + 1 < nmax: the producer loaded K_{j+1}
-                if (k_ready) mma_commit(smem_u32(&bars->kv_empty[slot_k]));
-            }
-            __syncwarp();
+            mma_commit_warp(smem_u32(&bars->kv_empty[slot_v]));
+            // k_ready holds exactly when j + 1 < nmax: the producer loaded K_{j+1}
+            if (k_ready) mma_commit_warp(smem_u32(&bars->kv_empty[slot_k]));
         }
     }
     if (!ok && leader) raise_abort(bars, err);
     // Drain: all issued MMAs complete before TMEM is released.
-    if (leader) mma_commit(smem_u32(&bars->drain));
-    __syncwarp();
+    mma_commit_warp(smem_u32(&bars->drain));
     mbar_wait(smem_u32(&bars->drain), 0, nullptr);
     __syncwarp();
 }
