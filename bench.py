@@ -195,9 +195,12 @@ def run_ours(args, rank, world, local_rank):
         if ev: ev[3].record(stream)
 
     args.warmup = max(args.warmup, 3)
+    # The flush comes first in every step: the GPU is still writing it while
+    # the host enqueues the step's launches, so no host gap lands between a
+    # step's events.
     for _ in range(args.warmup):
-        step()
         flush.zero_()
+        step()
     torch.cuda.synchronize()
     if ea.attn_last_device_error() != 0:
         raise RuntimeError("device error during warm-up")
@@ -209,8 +212,8 @@ def run_ours(args, rank, world, local_rank):
     with ClockSampler(local_rank) as clk:
         t0 = time.perf_counter()
         for i in range(args.steps):
-            step(evs[i])
             flush.zero_()
+            step(evs[i])
         torch.cuda.synchronize()
         wall = time.perf_counter() - t0
     if world > 1:

@@ -281,10 +281,10 @@ int attn_fwd_schedule(int B, int Hq, int Hkv, int Nq, int Nk, int d, int causal,
     if (B < 1 || Hq < 1 || Hkv < 1 || Nq < 1 || Nk < 1 || d < 1 || Hq % Hkv || !units_out)
         return -1;
     const FwdShape s = make_fwd_shape(B, Hq, Hkv, Nq, Nk, d, causal);
-    if (n != s.units) return -1;
+    if (n != s.units || s.units >= (1ll << 31)) return -1;
     for (long long i = 0; i < n; ++i) {
         int bh, mb;
-        unit_of(s, i, bh, mb);
+        unit_of(s, (uint32_t)i, bh, mb);
         units_out[3 * i] = bh / Hq;
         units_out[3 * i + 1] = bh % Hq;
         units_out[3 * i + 2] = mb;

@@ -112,7 +112,7 @@ __device__ void run_producer(const CUtensorMap* tq, const CUtensorMap* tk, const
     long long L = 0;  // K/V loads issued
     int local = 0;
     bool ok = true;
-    for (long long u = blockIdx.x; u < s.units && ok; u += gridDim.x, ++local) {
+    for (uint32_t u = blockIdx.x; u < (uint32_t)s.units && ok; u += gridDim.x, ++local) {
         int bh, mb;
         unit_of(s, u, bh, mb);
         const int b = bh / s.Hq;
@@ -230,7 +230,7 @@ __device__ void run_mma(uint8_t* smem, Bars* bars, uint32_t tmem, const FwdParam
     uint32_t cnt_p[2] = {0u, 0u};
     int local = 0;
     bool ok = true;
-    for (long long u = blockIdx.x; u < s.units && ok; u += gridDim.x, ++local) {
+    for (uint32_t u = blockIdx.x; u < (uint32_t)s.units && ok; u += gridDim.x, ++local) {
         int bh, mb;
         unit_of(s, u, bh, mb);
         const int n[2] = {tile_kv_count(mb, 0, s), tile_kv_count(mb, 1, s)};
@@ -410,7 +410,7 @@ __device__ void run_softmax(int t, int wq, int lane, uint8_t* smem, Bars* bars, 
     uint32_t epi_buf = 0;
     uint32_t cnt_s = 0, cnt_o = 0;
     bool ok = true;
-    for (long long u = blockIdx.x; u < s.units && ok; u += gridDim.x) {
+    for (uint32_t u = blockIdx.x; u < (uint32_t)s.units && ok; u += gridDim.x) {
         int bh, mb;
         unit_of(s, u, bh, mb);
         const int n_t = tile_kv_count(mb, t, s);
@@ -589,6 +589,7 @@ attn_status_t launch_fwd(const void* q, const void* k, const void* v, void* o, f
                          attn_out_dtype_t o_dtype, cudaStream_t stream, const DeviceInfo& dev) {
     FwdParams p;
     p.shape = make_fwd_shape(B, Hq, Hkv, Nq, Nk, d, causal);
+    if (p.shape.units >= (1ll << 31)) return ATTN_ERR_UNSUPPORTED;
     p.group = Hq / Hkv;
     p.off = Nk - Nq;
     p.c = scale * kLog2e;

@@ -29,7 +29,12 @@ constexpr int kTileM = 128;           // query rows per Q tile (tcgen05 M)
 constexpr int kTileN = 128;           // keys per K/V tile
 constexpr int kTilesPerUnit = 2;      // Q tiles per unit
 constexpr int kUnitRows = kTileM * kTilesPerUnit;
-constexpr long long kL2SectionBytes = 64ll << 20;  // K/V bytes a section may span
+// K/V bytes a section may span.  Causal sections stay wide so the longest-first
+// order can balance long and short m-blocks across the SMs; non-causal units
+// all cost the same, so a narrow section keeps the ~150 units in flight on few
+// heads and their K/V resident in the near L2 partition.
+constexpr long long kL2SectionBytesCausal = 64ll << 20;
+constexpr long long kL2SectionBytesDense = 16ll << 20;
 
 struct FwdShape {
     int B, Hq, Hkv, Nq, Nk, d, causal;
@@ -67,29 +72,32 @@ inline FwdShape make_fwd_shape(int B, int Hq, int Hkv, int Nq, int Nk, int d, in
     s.nmb = (Nq + kUnitRows - 1) / kUnitRows;
     const int group = Hq / Hkv;
     const long long kv_head_bytes = 2ll * Nk * d * 2;  // K and V, bf16
-    long long kv_per_sec = kL2SectionBytes / (kv_head_bytes > 0 ? kv_head_bytes : 1);
+    const long long budget = causal ? kL2SectionBytesCausal : kL2SectionBytesDense;
+    long long kv_per_sec = budget / (kv_head_bytes > 0 ? kv_head_bytes : 1);
     if (kv_per_sec < 1) kv_per_sec = 1;
     long long hps = kv_per_sec * group;
     const long long all = (long long)B * Hq;
     if (hps > all) hps = all;
     s.heads_per_section = (int)hps;
-    s.units = all * s.nmb;
+    s.units = all * s.nmb;  // the launcher rejects units >= 2^31
     return s;
 }
 
-// Unit index i (0 <= i < units) -> (bh = b * Hq + hq, mb).
-GB300_HD void unit_of(const FwdShape& s, long long i, int& bh, int& mb) {
-    const long long all = (long long)s.B * s.Hq;
-    const long long S = s.heads_per_section;
-    const long long sec_units = S * s.nmb;
-    const long long sec = i / sec_units;
-    const long long r = i - sec * sec_units;
-    const long long rest = all - sec * S;
-    const long long hs = rest < S ? rest : S;
-    const long long rank = r / hs;
-    const long long h_in = r - rank * hs;
+// Unit index i (0 <= i < units < 2^31) -> (bh = b * Hq + hq, mb).  32-bit
+// arithmetic keeps the device-side decode cheap; the host rejects shapes with
+// 2^31 or more units.
+GB300_HD void unit_of(const FwdShape& s, uint32_t i, int& bh, int& mb) {
+    const uint32_t all = (uint32_t)s.B * (uint32_t)s.Hq;
+    const uint32_t S = (uint32_t)s.heads_per_section;
+    const uint32_t sec_units = S * (uint32_t)s.nmb;
+    const uint32_t sec = i / sec_units;
+    const uint32_t r = i - sec * sec_units;
+    const uint32_t rest = all - sec * S;
+    const uint32_t hs = rest < S ? rest : S;
+    const uint32_t rank = r / hs;
+    const uint32_t h_in = r - rank * hs;
     bh = (int)(sec * S + h_in);
-    mb = s.causal ? (int)(s.nmb - 1 - rank) : (int)rank;
+    mb = s.causal ? (int)((uint32_t)s.nmb - 1u - rank) : (int)rank;
 }
 
 }  // namespace gb300

@@ -172,6 +172,19 @@ def test_forward_schedule_is_longest_first_within_sections(lib):
         assert len(heads) == 8
 
 
+def test_dense_schedule_uses_narrow_sections(lib):
+    # non-causal prefill: K/V per head = 1 MiB, 16 MiB sections -> 16 heads each,
+    # walked m-block rank by rank (all units cost the same)
+    B, Hq, Hkv, N, d = 4, 16, 16, 2048, 128
+    order, costs = ea.attn_fwd_schedule(B, Hq, Hkv, N, N, d, False)
+    per_sec = 16 * (N // 256)
+    assert len(set(costs)) == 1
+    for s in range(0, len(order), per_sec):
+        chunk = order[s:s + per_sec]
+        assert len({(b, h) for b, h, _ in chunk}) == 16
+        assert [m for _, _, m in chunk] == sorted(m for _, _, m in chunk)
+
+
 def test_gqa_siblings_are_adjacent(lib):
     order, _ = ea.attn_fwd_schedule(2, 8, 2, 512, 512, 64, True)
     # consecutive units of one m-block rank share a KV head in groups of 4
