@@ -1,9 +1,13 @@
 // attn_fwd_sm103.cu -- fused exact attention forward for sm_103a.
 //
-// One persistent CTA per SM walks the unit list of fwd_sched.h.  A unit is two
-// 128-row Q tiles of one (batch, query head); both tiles stream the same K/V
-// tiles.  Roles (12 warps = 3 warpgroups):
-//   warp 0      TMA producer (one elected lane issues): Q tiles once per unit, then K_j, V_j into a
+// One persistent CTA per SM takes units from the list of fwd_sched.h in list
+// order, each CTA fetching its next unit from a global counter when it is ready
+// for one (greedy list scheduling: with the causal list sorted longest-first
+// this is LPT).  A unit is two 128-row Q tiles of one (batch, query head); both
+// tiles stream the same K/V tiles.  Roles (12 warps = 3 warpgroups):
+//   warp 0      TMA producer (one elected lane issues): fetches the unit and
+//               hands it to the other roles through a two-slot ring in shared
+//               memory, then loads the Q tiles once per unit and K_j, V_j into a
 //               ring of shared-memory slots (128-byte swizzle, mbarrier
 //               full/empty pairs).
 //   warp 1      MMA issuer (one elected lane issues): S_t = Q_t K_j^T and O_t += P_t V_j
@@ -37,6 +41,7 @@
 //
 // TMEM columns (512 allocated): S0 [0,128) S1 [128,256) O0 [256,256+D)
 // O1 [256+D, 256+2D).  P_t (bf16 pairs) overwrites S_t columns [0, 64).
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 
@@ -65,7 +70,8 @@ struct FwdCfg {
     static constexpr int kStgOff = kRingOff + kStages * kTileBytes;
     static constexpr int kStgBytesPerWarp = 2 * 2048;
     static constexpr int kBarOff = kStgOff + 8 * kStgBytesPerWarp;
-    static constexpr int kSmemBytes = kBarOff + 256 + 1024;  // barriers + alignment slack
+    static constexpr int kBarBytes = 512;
+    static constexpr int kSmemBytes = kBarOff + kBarBytes + 1024;  // barriers + alignment slack
     static_assert(kSmemBytes <= 232448, "shared memory budget");
     // TMEM column of S_t and of O_t
     static __host__ __device__ constexpr uint32_t col_s(int t) { return uint32_t(t) * 128u; }
@@ -80,16 +86,50 @@ struct FwdParams {
     int group;      // Hq / Hkv
     int off;        // Nk - Nq (causal alignment)
     float c;        // scale * log2(e)
+    uint32_t slot;  // work-queue slot of this launch
 };
+
+// Work queues: per slot a ticket counter and a count of CTAs that have finished
+// taking tickets.  Each launch uses one slot; the last CTA to finish returns
+// both words to zero, so the next launch (or graph replay) on the slot starts
+// from a clean queue.  Launches rotate through the slots, so up to
+// kQueueSlots launches may run at the same time on different streams.
+constexpr uint32_t kQueueSlots = 1024;
+__device__ unsigned int g_fwd_queue[kQueueSlots][2];
+
+// Roles that take each unit from the producer: the MMA warp and 8 softmax warps.
+constexpr int kUnitConsumers = 9;
 
 struct __align__(8) Bars {
     uint64_t q_full[2], q_empty[2];
     uint64_t kv_full[8], kv_empty[8];
     uint64_t s_full[2], p_full[2], o_full[2];
+    uint64_t unit_full[2], unit_empty[2];
     uint64_t drain;
+    uint32_t unit[2];
     uint32_t tmem_base;
     int abort;
 };
+
+template <int D>
+struct BarsFit {
+    static_assert(sizeof(Bars) <= FwdCfg<D>::kBarBytes, "barrier block");
+};
+template struct BarsFit<64>;
+template struct BarsFit<128>;
+
+// Consumer side of the unit hand-off (whole warp): the k-th unit this warp
+// takes.  Returns false on abort.
+__device__ __forceinline__ bool take_unit(Bars* bars, uint32_t k, uint32_t& u,
+                                          const volatile int* abort_flag) {
+    const uint32_t i = k & 1u;
+    if (!__all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&bars->unit_full[i]), (k >> 1) & 1u, abort_flag)))
+        return false;
+    u = reinterpret_cast<volatile uint32_t*>(bars->unit)[i];
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(smem_u32(&bars->unit_empty[i]));
+    return true;
+}
 
 __device__ __forceinline__ void raise_abort(Bars* bars, unsigned int* err) {
     atomicOr(err, kErrTimeout);
@@ -108,11 +148,28 @@ __device__ void run_producer(const CUtensorMap* tq, const CUtensorMap* tk, const
     const volatile int* abort_flag = &bars->abort;
     const FwdShape& s = p.shape;
     const bool leader = elect_one();
+    const int leader_lane = __ffs(__ballot_sync(0xFFFFFFFFu, leader)) - 1;
+    unsigned int* queue = g_fwd_queue[p.slot];
     uint32_t q_issued[2] = {0u, 0u};
     long long L = 0;  // K/V loads issued
-    int local = 0;
     bool ok = true;
-    for (uint32_t u = blockIdx.x; u < (uint32_t)s.units && ok; u += gridDim.x, ++local) {
+    for (int local = 0; ok; ++local) {
+        // Take the next unit and publish it (a value >= units ends the loop
+        // of every role).
+        const uint32_t hs = (uint32_t)local & 1u;
+        if (local >= 2)
+            ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&bars->unit_empty[hs]),
+                                                   (uint32_t)((local >> 1) - 1) & 1u, abort_flag));
+        if (!ok) break;
+        uint32_t u = 0;
+        if (leader) u = atomicAdd(&queue[0], 1u);
+        u = __shfl_sync(0xFFFFFFFFu, u, leader_lane);
+        if (leader) {
+            reinterpret_cast<volatile uint32_t*>(bars->unit)[hs] = u;
+            mbar_arrive(smem_u32(&bars->unit_full[hs]));
+        }
+        __syncwarp();
+        if (u >= (uint32_t)s.units) break;
         int bh, mb;
         unit_of(s, u, bh, mb);
         const int b = bh / s.Hq;
@@ -159,6 +216,14 @@ __device__ void run_producer(const CUtensorMap* tq, const CUtensorMap* tk, const
         }
     }
     if (!ok && leader) raise_abort(bars, err);
+    // This CTA takes no more tickets; the last CTA to get here resets the queue.
+    if (leader) {
+        __threadfence();
+        if (atomicAdd(&queue[1], 1u) == gridDim.x - 1) {
+            atomicExch(&queue[0], 0u);
+            atomicExch(&queue[1], 0u);
+        }
+    }
     // Drain: every issued copy lands before the CTA may exit.
     for (int t = 0; t < 2; ++t)
         if (q_issued[t] > 0) mbar_wait(smem_u32(&bars->q_full[t]), (q_issued[t] - 1) & 1, nullptr);
@@ -228,9 +293,11 @@ __device__ void run_mma(uint8_t* smem, Bars* bars, uint32_t tmem, const FwdParam
     };
     long long Cn = 0;  // K/V loads consumed
     uint32_t cnt_p[2] = {0u, 0u};
-    int local = 0;
     bool ok = true;
-    for (uint32_t u = blockIdx.x; u < (uint32_t)s.units && ok; u += gridDim.x, ++local) {
+    for (int local = 0; ok; ++local) {
+        uint32_t u;
+        ok = take_unit(bars, (uint32_t)local, u, abort_flag);
+        if (!ok || u >= (uint32_t)s.units) break;
         int bh, mb;
         unit_of(s, u, bh, mb);
         const int n[2] = {tile_kv_count(mb, 0, s), tile_kv_count(mb, 1, s)};
@@ -410,7 +477,10 @@ __device__ void run_softmax(int t, int wq, int lane, uint8_t* smem, Bars* bars, 
     uint32_t epi_buf = 0;
     uint32_t cnt_s = 0, cnt_o = 0;
     bool ok = true;
-    for (uint32_t u = blockIdx.x; u < (uint32_t)s.units && ok; u += gridDim.x) {
+    for (uint32_t k = 0; ok; ++k) {
+        uint32_t u;
+        ok = take_unit(bars, k, u, abort_flag);
+        if (!ok || u >= (uint32_t)s.units) break;
         int bh, mb;
         unit_of(s, u, bh, mb);
         const int n_t = tile_kv_count(mb, t, s);
@@ -528,6 +598,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
             mbar_init(smem_u32(&bars->kv_full[i]), 1);
             mbar_init(smem_u32(&bars->kv_empty[i]), 1);
         }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(smem_u32(&bars->unit_full[i]), 1);
+            mbar_init(smem_u32(&bars->unit_empty[i]), kUnitConsumers);
+        }
         mbar_init(smem_u32(&bars->drain), 1);
         bars->abort = 0;
         fence_barrier_init();
@@ -593,6 +667,8 @@ attn_status_t launch_fwd(const void* q, const void* k, const void* v, void* o, f
     p.group = Hq / Hkv;
     p.off = Nk - Nq;
     p.c = scale * kLog2e;
+    static std::atomic<uint32_t> launches{0};
+    p.slot = launches.fetch_add(1u, std::memory_order_relaxed) % kQueueSlots;
     CUtensorMap tq, tk, tv, to;
     attn_status_t st;
     const bool f32 = o_dtype == ATTN_OUT_F32;

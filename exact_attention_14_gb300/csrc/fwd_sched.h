@@ -12,7 +12,8 @@
 // sections whose K/V fit an L2 budget; sections run in order; inside a section
 // the m-blocks run longest-first (causal) and, within one m-block rank, heads
 // run in index order so GQA siblings (consecutive hq sharing a KV head) are
-// adjacent.  The persistent grid walks this list with a static stride.
+// adjacent.  The persistent CTAs take units from this list in order, each
+// when it is ready for one (a device-side queue).
 #pragma once
 
 #include <cstdint>

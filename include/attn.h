@@ -75,7 +75,13 @@ typedef enum {
  * Supported: d in {64, 128}; Hq % Hkv == 0; 1 <= Nq, Nk <= 2^24;
  *            B*Hq and B*Hkv <= 2^24.  Other d -> ATTN_ERR_UNSUPPORTED.
  * Numerics: scores and O accumulate in fp32; the probabilities that multiply V
- * are rounded to bf16, and the row sum uses those same rounded values.
+ * are rounded to bf16.  The logsumexp uses the sum of the unrounded
+ * probabilities; O is divided by that sum plus, per KV tile, the rounding
+ * error of the tile's largest rounded probability.
+ * Work distribution: the kernel's CTAs take units from the attn_fwd_schedule
+ * list through a device-side queue (one of 1024 slots per launch, rotated by
+ * the library and left zeroed when the kernel ends), so at most 1024 attn_fwd
+ * launches may be in flight at the same time.
  * Returns ATTN_OK once the kernel is enqueued.
  */
 attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
@@ -189,14 +195,16 @@ int attn_kv_tiles(int row0, int rows, int Nq, int Nk, int causal, int block);
 long long attn_fwd_num_units(int B, int Hq, int Hkv, int Nq, int Nk, int d, int causal);
 
 /*
- * The order in which attn_fwd's persistent kernel walks its units: fills
+ * The order in which attn_fwd's persistent kernel takes its units: fills
  * units_out[3*i + {0,1,2}] = (b, hq, m_block) for i < n (n must equal
  * attn_fwd_num_units) and, if cost_out is non-NULL, cost_out[i] = the number
  * of (Q tile, KV tile) pairs unit i computes.  Heads are grouped into
  * sections whose K/V fit a fixed L2 budget, sections run in order, and within
  * a section the m-blocks run longest-first (lecture notes 4.5; "Flash
- * Attention 3/4 notes" FA4 section 3).  `num_sms` is the persistent grid size
- * used for the static stride.  Returns 0, or -1 on a bad argument.
+ * Attention 3/4 notes" FA4 section 3).  Sections span 64 MiB of K/V for
+ * causal launches and 16 MiB otherwise.  Each CTA takes the next unit of this
+ * list when it is ready for one (greedy list scheduling, as
+ * attn_list_schedule models it).  Returns 0, or -1 on a bad argument.
  */
 int attn_fwd_schedule(int B, int Hq, int Hkv, int Nq, int Nk, int d, int causal,
                       long long n, int* units_out, int* cost_out);

@@ -161,3 +161,57 @@ def test_repeatable_and_stream_ordered():
             outs.append((o.clone(), lse.clone()))
     s.synchronize()
     assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
+
+
+# ------------------------------ the work queue -------------------------------
+# The kernel's CTAs take units from a device-side queue that the last CTA
+# returns to zero.  A unit's result does not depend on which CTA computes it,
+# so every launch below must match its eager reference bit for bit.
+
+def test_graph_replays_reuse_the_work_queue():
+    """A captured launch replays on the same queue slot: each replay must see a
+    reset queue and compute every unit."""
+    B, H, N, d = 2, 8, 1024, 128
+    q, k, v = (t.cuda() for t in make_fwd_inputs(B, H, H, N, N, d, seed=21))
+    o = torch.empty(q.shape, dtype=torch.float32, device="cuda")
+    lse = torch.empty(q.shape[:3], dtype=torch.float32, device="cuda")
+    ea.attn_fwd(q, k, v, o, lse, causal=True)  # first call outside capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            ea.attn_fwd(q, k, v, o, lse, causal=True)
+    torch.cuda.current_stream().wait_stream(s)
+    for seed in (22, 23, 24):
+        q2, k2, v2 = (t.cuda() for t in make_fwd_inputs(B, H, H, N, N, d, seed=seed))
+        q.copy_(q2); k.copy_(k2); v.copy_(v2)
+        o.fill_(float("nan"))
+        g.replay()
+        o_ref, l_ref = ea.forward(q, k, v, causal=True, out_dtype=torch.float32)
+        torch.cuda.synchronize()
+        assert ea.attn_last_device_error() == 0
+        assert torch.equal(o, o_ref) and torch.equal(lse, l_ref), f"replay with seed {seed}"
+
+
+def test_concurrent_launches_on_two_streams():
+    """Launches in flight together on two streams use different queue slots."""
+    cases = [make_fwd_inputs(4, 8, 2, 1536, 1536, 128, seed=31),
+             make_fwd_inputs(3, 8, 8, 1000, 1000, 64, seed=32)]
+    cases = [tuple(t.cuda() for t in c) for c in cases]
+    refs = [ea.forward(*c, causal=True, out_dtype=torch.float32) for c in cases]
+    torch.cuda.synchronize()
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    for st in streams:
+        st.wait_stream(torch.cuda.current_stream())
+    outs = [[], []]
+    for _ in range(4):
+        for i, (st, c) in enumerate(zip(streams, cases)):
+            with torch.cuda.stream(st):
+                outs[i].append(ea.forward(*c, causal=True, out_dtype=torch.float32, stream=st))
+    torch.cuda.synchronize()
+    assert ea.attn_last_device_error() == 0
+    for i in range(2):
+        for o, lse in outs[i]:
+            assert torch.equal(o, refs[i][0]) and torch.equal(lse, refs[i][1])
