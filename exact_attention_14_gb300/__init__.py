@@ -18,7 +18,7 @@ __all__ = [
     "ATTN_OUT_BF16", "ATTN_OUT_F32", "AttnError", "attn_fwd", "attn_decode",
     "attn_decode_workspace_size", "attn_decode_noalloc", "attn_status_string", "attn_last_device_error",
     "attn_decode_num_splits", "attn_list_schedule", "attn_kv_tiles",
-    "attn_fwd_num_units", "attn_fwd_schedule", "forward", "decode", "library_path", "load",
+    "attn_fwd_num_units", "attn_fwd_schedule", "attn_fwd_split_plan", "forward", "decode", "library_path", "load",
 ]
 
 ATTN_OK = 0
@@ -54,6 +54,9 @@ SIGNATURES = {
     "attn_fwd_schedule": (_c_int, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
                                    _c_ll, ctypes.POINTER(ctypes.c_int),
                                    ctypes.POINTER(ctypes.c_int)]),
+    "attn_fwd_split_plan": (_c_int, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
+                                     _c_int, ctypes.POINTER(ctypes.c_int),
+                                     ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int)]),
 }
 
 
@@ -280,3 +283,14 @@ def attn_fwd_schedule(B, Hq, Hkv, Nq, Nk, d, causal):
     if rc != 0:
         raise ValueError("attn_fwd_schedule rejected its arguments")
     return [tuple(units[3 * i:3 * i + 3]) for i in range(n)], list(costs)
+
+
+def attn_fwd_split_plan(B, Hq, Hkv, Nq, Nk, d, causal, num_sms):
+    """Returns (n_full, n_split, parts): the tail split attn_fwd applies on a
+    GPU with num_sms SMs."""
+    out = [ctypes.c_int() for _ in range(3)]
+    rc = load().attn_fwd_split_plan(B, Hq, Hkv, Nq, Nk, d, int(bool(causal)), num_sms,
+                                    *(ctypes.byref(o) for o in out))
+    if rc != 0:
+        raise ValueError("attn_fwd_split_plan rejected its arguments")
+    return tuple(o.value for o in out)

@@ -293,4 +293,18 @@ int attn_fwd_schedule(int B, int Hq, int Hkv, int Nq, int Nk, int d, int causal,
     return 0;
 }
 
+int attn_fwd_split_plan(int B, int Hq, int Hkv, int Nq, int Nk, int d, int causal, int num_sms,
+                        int* n_full, int* n_split, int* parts) {
+    if (B < 1 || Hq < 1 || Hkv < 1 || Nq < 1 || Nk < 1 || d < 1 || Hq % Hkv || num_sms < 1 ||
+        !n_full || !n_split || !parts)
+        return -1;
+    const FwdShape s = make_fwd_shape(B, Hq, Hkv, Nq, Nk, d, causal);
+    if (s.units >= (1ll << 31)) return -1;
+    const FwdSplit sp = plan_tail_split(s, num_sms);
+    *n_full = sp.n_full;
+    *n_split = sp.n_split;
+    *parts = sp.parts;
+    return 0;
+}
+
 }  // extern "C"

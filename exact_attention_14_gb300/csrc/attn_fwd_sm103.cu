@@ -1,15 +1,17 @@
 // attn_fwd_sm103.cu -- fused exact attention forward for sm_103a.
 //
-// One persistent CTA per SM takes units from the list of fwd_sched.h in list
-// order, each CTA fetching its next unit from a global counter when it is ready
-// for one (greedy list scheduling: with the causal list sorted longest-first
-// this is LPT).  A unit is two 128-row Q tiles of one (batch, query head); both
-// tiles stream the same K/V tiles.  Roles (12 warps = 3 warpgroups):
-//   warp 0      TMA producer (one elected lane issues): fetches the unit and
-//               hands it to the other roles through a two-slot ring in shared
-//               memory, then loads the Q tiles once per unit and K_j, V_j into a
-//               ring of shared-memory slots (128-byte swizzle, mbarrier
-//               full/empty pairs).
+// One persistent CTA per SM takes work items from the list of fwd_sched.h in
+// list order: CTA i starts with item i, then fetches its next item from a
+// global counter whenever it is ready for one (greedy list scheduling: with the
+// causal list sorted longest-first this is LPT).  An item is a unit -- two
+// 128-row Q tiles of one (batch, query head), both streaming the same K/V
+// tiles -- or, for the tail units of a non-causal launch, a piece of a unit's
+// KV range (fwd_sched.h, tail split).  Roles (12 warps = 3 warpgroups):
+//   warp 0      TMA producer (one elected lane issues): fetches the item,
+//               decodes it and hands it to the other roles through a two-slot
+//               ring in shared memory, then loads the Q tiles once per item
+//               and K_j, V_j into a ring of shared-memory slots (128-byte
+//               swizzle, mbarrier full/empty pairs).
 //   warp 1      MMA issuer (one elected lane issues): S_t = Q_t K_j^T and O_t += P_t V_j
 //               on the 5th-generation tensor cores, accumulating in TMEM.
 //   warps 4-7   softmax for Q tile 0, warps 8-11 for Q tile 1: one thread
@@ -44,6 +46,7 @@
 #include <atomic>
 #include <cmath>
 #include <cstdint>
+#include <mutex>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -87,18 +90,42 @@ struct FwdParams {
     int off;        // Nk - Nq (causal alignment)
     float c;        // scale * log2(e)
     uint32_t slot;  // work-queue slot of this launch
+    FwdSplit split; // tail split (fwd_sched.h)
+    float* partial; // per-piece partial results of split units (NULL if none)
 };
 
-// Work queues: per slot a ticket counter and a count of CTAs that have finished
-// taking tickets.  Each launch uses one slot; the last CTA to finish returns
-// both words to zero, so the next launch (or graph replay) on the slot starts
-// from a clean queue.  Launches rotate through the slots, so up to
-// kQueueSlots launches may run at the same time on different streams.
-constexpr uint32_t kQueueSlots = 1024;
-__device__ unsigned int g_fwd_queue[kQueueSlots][2];
+// Work queues.  Per slot: word 0 the ticket counter (the next work item),
+// word 1 the number of CTAs that have exited, then one arrival counter per
+// (split unit, Q tile, softmax warp) for the merge of split units.  Each
+// launch uses one slot; the last CTA to exit returns the slot's words to zero,
+// so the next launch (or graph replay) on the slot starts from a clean queue.
+// Launches rotate through the slots, so up to kQueueSlots launches may be in
+// flight at the same time on different streams.
+constexpr uint32_t kQueueSlots = 256;
+constexpr int kQueueWords = 2 + 8 * kMaxSplitUnits;
+__device__ unsigned int g_fwd_queue[kQueueSlots][kQueueWords];
 
-// Roles that take each unit from the producer: the MMA warp and 8 softmax warps.
+// Floats of one partial block: one softmax warp's 32 rows of one piece,
+// column-major ([D + 3][32]: the normalised O columns, then m, l, lx) so that
+// a warp's stores and loads of a column are 128 contiguous bytes.
+template <int D>
+__host__ __device__ constexpr int partial_block_floats() { return (D + 3) * 32; }
+
+// Roles that take each work item from the producer: the MMA warp and 8
+// softmax warps.
 constexpr int kUnitConsumers = 9;
+
+// A work item as the producer decodes it for the other roles, so that their
+// unit boundaries carry no index arithmetic.
+struct WorkItem {
+    int bh;         // b * Hq + hq; -1 ends every role's loop
+    int mb;         // m-block: query rows [256 mb, 256 mb + 256)
+    int j0;         // first KV tile of the item
+    int e[2];       // end KV tile (exclusive) of Q tile 0 and 1 (<= j0: no work)
+    int part;       // piece of a split unit, -1 for a whole unit
+    uint32_t cell;  // split units: 8 * (unit - n_full), the unit's first merge cell
+    int pad;
+};
 
 struct __align__(8) Bars {
     uint64_t q_full[2], q_empty[2];
@@ -106,7 +133,7 @@ struct __align__(8) Bars {
     uint64_t s_full[2], p_full[2], o_full[2];
     uint64_t unit_full[2], unit_empty[2];
     uint64_t drain;
-    uint32_t unit[2];
+    WorkItem item[2];
     uint32_t tmem_base;
     int abort;
 };
@@ -118,14 +145,21 @@ struct BarsFit {
 template struct BarsFit<64>;
 template struct BarsFit<128>;
 
-// Consumer side of the unit hand-off (whole warp): the k-th unit this warp
-// takes.  Returns false on abort.
-__device__ __forceinline__ bool take_unit(Bars* bars, uint32_t k, uint32_t& u,
+// Consumer side of the work-item hand-off (whole warp): the k-th item this
+// warp takes.  Returns false on abort.
+__device__ __forceinline__ bool take_item(Bars* bars, uint32_t k, WorkItem& w,
                                           const volatile int* abort_flag) {
     const uint32_t i = k & 1u;
     if (!__all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&bars->unit_full[i]), (k >> 1) & 1u, abort_flag)))
         return false;
-    u = reinterpret_cast<volatile uint32_t*>(bars->unit)[i];
+    const volatile WorkItem* src = &bars->item[i];
+    w.bh = src->bh;
+    w.mb = src->mb;
+    w.j0 = src->j0;
+    w.e[0] = src->e[0];
+    w.e[1] = src->e[1];
+    w.part = src->part;
+    w.cell = src->cell;
     __syncwarp();
     if ((threadIdx.x & 31) == 0) mbar_arrive(smem_u32(&bars->unit_empty[i]));
     return true;
@@ -161,22 +195,39 @@ __device__ void run_producer(const CUtensorMap* tq, const CUtensorMap* tk, const
             ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&bars->unit_empty[hs]),
                                                    (uint32_t)((local >> 1) - 1) & 1u, abort_flag));
         if (!ok) break;
-        uint32_t u = 0;
-        if (leader) u = atomicAdd(&queue[0], 1u);
-        u = __shfl_sync(0xFFFFFFFFu, u, leader_lane);
+        // A CTA's first item is its own index (no atomic on the launch's
+        // critical path); later ones come from the counter, after the grid.
+        uint32_t u = blockIdx.x;
+        if (local > 0) {
+            if (leader) u = gridDim.x + atomicAdd(&queue[0], 1u);
+            u = __shfl_sync(0xFFFFFFFFu, u, leader_lane);
+        }
+        const bool done = u >= split_items(p.split);
+        uint32_t unit = 0;
+        int part = -1, bh = -1, mb = 0, j0 = 0, j1 = 0, n0 = 0, n1 = 0;
+        if (!done) {
+            item_of(p.split, u, unit, part);
+            unit_of(s, unit, bh, mb);
+            n0 = tile_kv_count(mb, 0, s);
+            n1 = tile_kv_count(mb, 1, s);
+            part_range(n0 > n1 ? n0 : n1, p.split.parts, part, j0, j1);
+        }
         if (leader) {
-            reinterpret_cast<volatile uint32_t*>(bars->unit)[hs] = u;
+            volatile WorkItem* dst = &bars->item[hs];
+            dst->bh = bh;
+            dst->mb = mb;
+            dst->j0 = j0;
+            dst->e[0] = n0 < j1 ? n0 : j1;
+            dst->e[1] = n1 < j1 ? n1 : j1;
+            dst->part = part;
+            dst->cell = (unit - (uint32_t)p.split.n_full) * 8u;
             mbar_arrive(smem_u32(&bars->unit_full[hs]));
         }
         __syncwarp();
-        if (u >= (uint32_t)s.units) break;
-        int bh, mb;
-        unit_of(s, u, bh, mb);
+        if (done) break;
         const int b = bh / s.Hq;
         const int hq = bh - b * s.Hq;
         const int bkv = b * s.Hkv + hq / p.group;
-        const int n0 = tile_kv_count(mb, 0, s), n1 = tile_kv_count(mb, 1, s);
-        const int nmax = n0 > n1 ? n0 : n1;
         for (int t = 0; t < 2 && ok; ++t) {
             if (local > 0)
                 ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&bars->q_empty[t]), (local - 1) & 1, abort_flag));
@@ -192,7 +243,7 @@ __device__ void run_producer(const CUtensorMap* tq, const CUtensorMap* tk, const
             __syncwarp();
             ++q_issued[t];
         }
-        for (int j = 0; j < nmax && ok; ++j) {
+        for (int j = j0; j < j1 && ok; ++j) {
 #pragma unroll 1
             for (int which = 0; which < 2; ++which) {
                 const int slot = (int)(L % C::kStages);
@@ -216,12 +267,15 @@ __device__ void run_producer(const CUtensorMap* tq, const CUtensorMap* tk, const
         }
     }
     if (!ok && leader) raise_abort(bars, err);
-    // This CTA takes no more tickets; the last CTA to get here resets the queue.
-    if (leader) {
+    // Without split units the queue holds only the ticket counter, which no
+    // role of this CTA touches any more: count this CTA out now, off the
+    // kernel's tail.  (With split units the count waits for the merges; see
+    // the end of the kernel.)
+    if (p.split.n_split == 0 && leader) {
         __threadfence();
         if (atomicAdd(&queue[1], 1u) == gridDim.x - 1) {
-            atomicExch(&queue[0], 0u);
-            atomicExch(&queue[1], 0u);
+            queue[0] = 0u;
+            queue[1] = 0u;
         }
     }
     // Drain: every issued copy lands before the CTA may exit.
@@ -295,13 +349,13 @@ __device__ void run_mma(uint8_t* smem, Bars* bars, uint32_t tmem, const FwdParam
     uint32_t cnt_p[2] = {0u, 0u};
     bool ok = true;
     for (int local = 0; ok; ++local) {
-        uint32_t u;
-        ok = take_unit(bars, (uint32_t)local, u, abort_flag);
-        if (!ok || u >= (uint32_t)s.units) break;
-        int bh, mb;
-        unit_of(s, u, bh, mb);
-        const int n[2] = {tile_kv_count(mb, 0, s), tile_kv_count(mb, 1, s)};
-        const int nmax = n[0] > n[1] ? n[0] : n[1];
+        WorkItem w;
+        ok = take_item(bars, (uint32_t)local, w, abort_flag);
+        if (!ok || w.bh < 0) break;
+        // this item's KV tiles: [j0, j1) overall, [j0, n[t]) for tile t
+        const int n[2] = {w.e[0], w.e[1]};
+        const int j0 = w.j0;
+        const int j1 = n[0] > n[1] ? n[0] : n[1];
         for (int t = 0; t < 2 && ok; ++t) ok = wait_all(smem_u32(&bars->q_full[t]), local & 1);
         if (!ok) break;
         // K_0 -> S_t(0)
@@ -311,14 +365,14 @@ __device__ void run_mma(uint8_t* smem, Bars* bars, uint32_t tmem, const FwdParam
         if (!ok) break;
         tc_fence_after();
         for (int t = 0; t < 2; ++t) {
-            if (n[t] > 0) {
+            if (n[t] > j0) {
                 issue_qk<D>(tmem, t, q_lo[t], k_lo(slot_k), idS);
                 mma_commit_warp(smem_u32(&bars->s_full[t]));
             }
-            if (n[t] <= 1) mma_commit_warp(smem_u32(&bars->q_empty[t]));
+            if (n[t] - j0 <= 1) mma_commit_warp(smem_u32(&bars->q_empty[t]));
         }
         mma_commit_warp(smem_u32(&bars->kv_empty[slot_k]));
-        for (int j = 0; j < nmax && ok; ++j) {
+        for (int j = j0; j < j1 && ok; ++j) {
             const int slot_v = (int)(Cn % C::kStages);
             ok = wait_all(smem_u32(&bars->kv_full[slot_v]), (uint32_t)((Cn / C::kStages) & 1));
             ++Cn;
@@ -333,7 +387,7 @@ __device__ void run_mma(uint8_t* smem, Bars* bars, uint32_t tmem, const FwdParam
                 ++cnt_p[t];
                 if (!ok) break;
                 tc_fence_after();
-                issue_pv<D>(tmem, t, v_lo(slot_v), idO, j > 0);
+                issue_pv<D>(tmem, t, v_lo(slot_v), idO, j > j0);
                 if (j + 1 < n[t]) {
                     if (!k_ready) {
                         slot_k = (int)(Cn % C::kStages);
@@ -354,7 +408,7 @@ __device__ void run_mma(uint8_t* smem, Bars* bars, uint32_t tmem, const FwdParam
             }
             if (!ok) break;
             mma_commit_warp(smem_u32(&bars->kv_empty[slot_v]));
-            // k_ready holds exactly when j + 1 < nmax: the producer loaded K_{j+1}
+            // k_ready holds exactly when j + 1 < j1: the producer loaded K_{j+1}
             if (k_ready) mma_commit_warp(smem_u32(&bars->kv_empty[slot_k]));
         }
     }
@@ -459,6 +513,152 @@ __device__ __forceinline__ void softmax_tile(uint32_t (&sr)[128], int lim, int j
     }
 }
 
+// Epilogue store of 32 output columns [cc, cc + 32) of this warp's 32 rows:
+// staged 32 rows x 64 bytes at a time in shared memory (two buffers per warp)
+// and written by TMA stores (rows past Nq are clipped by the hardware), so the
+// warp does not wait for the global writes.
+template <bool OUT_F32>
+__device__ __forceinline__ void store_o_cols(const float (&v)[32], int cc, uint8_t* stg,
+                                             uint32_t& epi_buf, int lane, const CUtensorMap* to,
+                                             int row0, int bh) {
+    constexpr int kCols = kEpiCols(OUT_F32);
+#pragma unroll
+    for (int h = 0; h < 32 / kCols; ++h) {
+        uint8_t* buf = stg + (epi_buf & 1) * 2048;
+        if (lane == 0) bulk_wait_group_read<1>();  // this buffer's previous store has read it
+        __syncwarp();
+        uint4* dst = reinterpret_cast<uint4*>(buf + lane * 64);
+        if constexpr (OUT_F32) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                dst[i] = make_uint4(__float_as_uint(v[h * 16 + 4 * i]), __float_as_uint(v[h * 16 + 4 * i + 1]),
+                                    __float_as_uint(v[h * 16 + 4 * i + 2]), __float_as_uint(v[h * 16 + 4 * i + 3]));
+        } else {
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                dst[i] = make_uint4(pack_bf16x2(v[8 * i], v[8 * i + 1]), pack_bf16x2(v[8 * i + 2], v[8 * i + 3]),
+                                    pack_bf16x2(v[8 * i + 4], v[8 * i + 5]), pack_bf16x2(v[8 * i + 6], v[8 * i + 7]));
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+            tma_store_3d(to, smem_u32(buf), cc + h * kCols, row0, bh);
+            bulk_commit_group();
+        }
+        ++epi_buf;
+    }
+}
+
+// End of a piece of a split unit (one softmax warp, its 32 rows of Q tile t):
+// publish this warp's partial block (O / l, m, l, lx), then count the pieces
+// that have arrived; the last one merges all of them (lecture notes 2.2
+// rescaling, 6.1 split-KV): with M = max m_p and w_p = 2^(m_p - M),
+//   O = sum_p w_p l_p (O_p / l_p) / sum_p w_p l_p,
+//   LSE = ln2 * (M + log2 sum_p w_p lx_p).
+// Kept out of line so that its registers do not weigh on the softmax loop.
+template <int D, bool OUT_F32>
+__device__ __noinline__ void split_piece_epilogue(unsigned int* merge_count, float* partial,
+                                                  int parts, uint32_t cell, int part, int lane,
+                                                  uint32_t tO, float m, float l, float lx,
+                                                  uint8_t* stg, uint32_t* epi_buf,
+                                                  const CUtensorMap* to, int row0, int bh,
+                                                  float* lse_out) {
+    const float inv_l = 1.0f / l;
+    float* blocks = partial + (size_t)cell * parts * partial_block_floats<D>();
+    float* mine = blocks + (size_t)part * partial_block_floats<D>();
+#pragma unroll 1
+    for (int cc = 0; cc < D; cc += 32) {
+        uint32_t r[32];
+        tmem_ld32(tO + cc, r);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) mine[(cc + i) * 32 + lane] = __fmul_rn(__uint_as_float(r[i]), inv_l);
+    }
+    mine[D * 32 + lane] = m;
+    mine[(D + 1) * 32 + lane] = l;
+    mine[(D + 2) * 32 + lane] = lx;
+    __threadfence();
+    __syncwarp();
+    uint32_t arrived = 0;
+    if (lane == 0) arrived = atomicAdd(&merge_count[cell], 1u);
+    arrived = __shfl_sync(0xFFFFFFFFu, arrived, 0);
+    if (arrived != (uint32_t)parts - 1) return;
+    // The last piece merges, summing the pieces in piece order with the
+    // same arithmetic whichever piece arrives last (so the result does not
+    // depend on the arrival order).  Its own O / l is recomputed from TMEM
+    // exactly as it was written; the other pieces' blocks come from L2,
+    // the first other piece's next 32-column chunk loaded ahead of use.
+    __threadfence();
+    float mq[kMaxSplitParts], lq[kMaxSplitParts], lxq[kMaxSplitParts];
+#pragma unroll
+    for (int q = 0; q < kMaxSplitParts; ++q) {
+        mq[q] = -INFINITY; lq[q] = 0.f; lxq[q] = 0.f;
+        if (q == part) {
+            mq[q] = m; lq[q] = l; lxq[q] = lx;
+        } else if (q < parts) {
+            const float* bq = blocks + q * partial_block_floats<D>() + D * 32 + lane;
+            mq[q] = __ldcg(bq);
+            lq[q] = __ldcg(bq + 32);
+            lxq[q] = __ldcg(bq + 64);
+        }
+    }
+    float mmax = -INFINITY;
+#pragma unroll
+    for (int q = 0; q < kMaxSplitParts; ++q) mmax = fmaxf(mmax, mq[q]);
+    float wsum = 0.f, wxsum = 0.f;
+    float w[kMaxSplitParts];
+#pragma unroll
+    for (int q = 0; q < kMaxSplitParts; ++q) {
+        const float e = ex2(mq[q] - mmax);  // 0 for absent pieces
+        w[q] = e * lq[q];
+        wsum += w[q];
+        wxsum += e * lxq[q];
+    }
+    const float inv_w = 1.0f / wsum;
+#pragma unroll
+    for (int q = 0; q < kMaxSplitParts; ++q) w[q] *= inv_w;  // weight of piece q's O / l
+    const int q0 = part == 0 ? 1 : 0;
+    const float* b0 = blocks + q0 * partial_block_floats<D>() + lane;
+    float nxt[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) nxt[i] = __ldcg(b0 + i * 32);
+#pragma unroll 1
+    for (int cc = 0; cc < D; cc += 32) {
+        uint32_t r[32];
+        tmem_ld32(tO + cc, r);
+        float cur[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) cur[i] = nxt[i];
+        if (cc + 32 < D) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) nxt[i] = __ldcg(b0 + (cc + 32 + i) * 32);
+        }
+        tmem_wait_ld();
+        float v[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = 0.f;
+#pragma unroll 1
+        for (int q = 0; q < parts; ++q) {
+            float wq_ = 0.f;
+#pragma unroll
+            for (int x = 0; x < kMaxSplitParts; ++x) wq_ = x == q ? w[x] : wq_;
+            if (q == part) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) v[i] = fmaf(wq_, __fmul_rn(__uint_as_float(r[i]), inv_l), v[i]);
+            } else if (q == q0) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) v[i] = fmaf(wq_, cur[i], v[i]);
+            } else {
+                const float* bq = blocks + q * partial_block_floats<D>() + cc * 32 + lane;
+#pragma unroll
+                for (int i = 0; i < 32; ++i) v[i] = fmaf(wq_, __ldcg(bq + i * 32), v[i]);
+            }
+        }
+        store_o_cols<OUT_F32>(v, cc, stg, *epi_buf, lane, to, row0, bh);
+    }
+    if (lse_out) *lse_out = (mmax + log2f(wxsum)) * kLn2;
+}
+
 template <int D, bool OUT_F32>
 __device__ void run_softmax(int t, int wq, int lane, uint8_t* smem, Bars* bars, uint32_t tmem,
                             const FwdParams& p, const CUtensorMap* to, float* __restrict__ lse_ptr,
@@ -478,13 +678,12 @@ __device__ void run_softmax(int t, int wq, int lane, uint8_t* smem, Bars* bars, 
     uint32_t cnt_s = 0, cnt_o = 0;
     bool ok = true;
     for (uint32_t k = 0; ok; ++k) {
-        uint32_t u;
-        ok = take_unit(bars, k, u, abort_flag);
-        if (!ok || u >= (uint32_t)s.units) break;
-        int bh, mb;
-        unit_of(s, u, bh, mb);
-        const int n_t = tile_kv_count(mb, t, s);
-        if (n_t == 0) continue;
+        WorkItem w;
+        ok = take_item(bars, k, w, abort_flag);
+        if (!ok || w.bh < 0) break;
+        const int bh = w.bh, mb = w.mb, j0 = w.j0, part = w.part;
+        const int n_t = t == 0 ? w.e[0] : w.e[1];
+        if (n_t <= j0) continue;
         const int row = mb * kUnitRows + t * kTileM + wq * 32 + lane;
         // last allowed key for this row (global index)
         int last_key = s.Nk - 1;
@@ -495,7 +694,7 @@ __device__ void run_softmax(int t, int wq, int lane, uint8_t* smem, Bars* bars, 
         float m = -INFINITY;  // running max of scaled scores, log2 units
         float l = 0.f;        // normaliser of O (see softmax_tile)
         float lx = 0.f;       // running sum of the unrounded probabilities (gives the LSE)
-        for (int j = 0; j < n_t; ++j) {
+        for (int j = j0; j < n_t; ++j) {
             ok = mbar_wait(bar_s, cnt_s & 1, abort_flag, 32);
             ++cnt_s;
             if (!ok) break;
@@ -508,9 +707,9 @@ __device__ void run_softmax(int t, int wq, int lane, uint8_t* smem, Bars* bars, 
             tmem_wait_ld();
             const int lim = last_key - j * kTileN;  // column c allowed iff c <= lim
             if (__any_sync(0xFFFFFFFFu, lim < kTileN - 1))
-                softmax_tile<D, true>(sr, lim, j, c, tS, tO, m, l, lx);
+                softmax_tile<D, true>(sr, lim, j - j0, c, tS, tO, m, l, lx);
             else
-                softmax_tile<D, false>(sr, lim, j, c, tS, tO, m, l, lx);
+                softmax_tile<D, false>(sr, lim, j - j0, c, tS, tO, m, l, lx);
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
@@ -525,48 +724,28 @@ __device__ void run_softmax(int t, int wq, int lane, uint8_t* smem, Bars* bars, 
         const bool live = row < s.Nq;
         const float inv_l = 1.0f / l;
         const size_t row_idx = (size_t)bh * s.Nq + (size_t)row;
-        // O rows are staged 32 rows x 64 bytes at a time in shared memory and
-        // written by TMA stores (rows past Nq are clipped by the hardware), so
-        // the warp does not wait for the global writes.
-        constexpr int kCols = kEpiCols(OUT_F32);
         const int row0 = mb * kUnitRows + t * kTileM + wq * 32;
         const uint64_t il2 = f2(inv_l, inv_l);
+        if (part < 0) {
 #pragma unroll 1
-        for (int cc = 0; cc < D; cc += 32) {
-            uint32_t r[32];
-            tmem_ld32(tO + cc, r);
-            tmem_wait_ld();
-            float v[32];
+            for (int cc = 0; cc < D; cc += 32) {
+                uint32_t r[32];
+                tmem_ld32(tO + cc, r);
+                tmem_wait_ld();
+                float v[32];
 #pragma unroll
-            for (int i = 0; i < 32; i += 2)
-                f2_split(f2_mul(f2(__uint_as_float(r[i]), __uint_as_float(r[i + 1])), il2), v[i], v[i + 1]);
-#pragma unroll
-            for (int h = 0; h < 32 / kCols; ++h) {
-                uint8_t* buf = stg + (epi_buf & 1) * 2048;
-                if (lane == 0) bulk_wait_group_read<1>();  // this buffer's previous store has read it
-                __syncwarp();
-                uint4* dst = reinterpret_cast<uint4*>(buf + lane * 64);
-                if constexpr (OUT_F32) {
-#pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        dst[i] = make_uint4(__float_as_uint(v[h * 16 + 4 * i]), __float_as_uint(v[h * 16 + 4 * i + 1]),
-                                            __float_as_uint(v[h * 16 + 4 * i + 2]), __float_as_uint(v[h * 16 + 4 * i + 3]));
-                } else {
-#pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        dst[i] = make_uint4(pack_bf16x2(v[8 * i], v[8 * i + 1]), pack_bf16x2(v[8 * i + 2], v[8 * i + 3]),
-                                            pack_bf16x2(v[8 * i + 4], v[8 * i + 5]), pack_bf16x2(v[8 * i + 6], v[8 * i + 7]));
-                }
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-                    tma_store_3d(to, smem_u32(buf), cc + h * kCols, row0, bh);
-                    bulk_commit_group();
-                }
-                ++epi_buf;
+                for (int i = 0; i < 32; i += 2)
+                    f2_split(f2_mul(f2(__uint_as_float(r[i]), __uint_as_float(r[i + 1])), il2), v[i], v[i + 1]);
+                store_o_cols<OUT_F32>(v, cc, stg, epi_buf, lane, to, row0, bh);
             }
+            if (live && lse_ptr) lse_ptr[row_idx] = (m + log2f(lx)) * kLn2;
+            continue;
         }
-        if (live && lse_ptr) lse_ptr[row_idx] = (m + log2f(lx)) * kLn2;
+        // (cell: this warp's slot among the split units' merge counters and blocks)
+        const uint32_t cell = w.cell + (uint32_t)t * 4u + (uint32_t)wq;
+        split_piece_epilogue<D, OUT_F32>(g_fwd_queue[p.slot] + 2, p.partial, p.split.parts, cell, part,
+                                         lane, tO, m, l, lx, stg, &epi_buf, to, row0, bh,
+                                         (live && lse_ptr) ? lse_ptr + row_idx : nullptr);
     }
     if (lane == 0) bulk_wait_group_all();  // every staged store has completed
     __syncwarp();
@@ -635,11 +814,26 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
+    // With split units, the last CTA to exit returns the queue slot to zero:
+    // the ticket counter, the exit count and the merge counters.  Every ticket
+    // and merge-counter atomic of this CTA returned its value before the
+    // barrier above, so they precede the exit count.
+    if (p.split.n_split > 0 && threadIdx.x == 0) {
+        unsigned int* queue = g_fwd_queue[p.slot];
+        __threadfence();
+        if (atomicAdd(&queue[1], 1u) == gridDim.x - 1) {
+            __threadfence();
+            const int words = 8 * p.split.n_split;
+            for (int i = 0; i < words; ++i) queue[2 + i] = 0u;
+            queue[0] = 0u;
+            queue[1] = 0u;
+        }
+    }
 }
 
 template <int D, bool OUT_F32>
 attn_status_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                           const CUtensorMap& to, float* lse, const FwdParams& p,
+                           const CUtensorMap& to, float* lse, const FwdParams& p, int grid,
                            cudaStream_t stream, const DeviceInfo& dev) {
     using C = FwdCfg<D>;
     static int attr_set[64] = {0};
@@ -650,10 +844,58 @@ attn_status_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const C
             return ATTN_ERR_CUDA;
         attr_set[dev.device] = 1;
     }
-    long long grid = p.shape.units < dev.num_sms ? p.shape.units : dev.num_sms;
     attn_fwd_kernel<D, OUT_F32><<<(unsigned)grid, kThreads, C::kSmemBytes, stream>>>(
         tq, tk, tv, to, lse, p, dev.err_word);
     return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+// Stream-ordered memory for the partial results of split units: one pool per
+// device owned by the library, kept (release threshold: never) so that the
+// per-launch allocation is served from the pool after the first one.  The
+// allocation and its free are stream-ordered around the kernel, so launches on
+// different streams, and graph captures, each get their own partials.
+attn_status_t partial_pool(int device, cudaMemPool_t* out) {
+    static std::mutex mu;
+    static cudaMemPool_t pools[64] = {};
+    if (device < 0 || device >= 64) return ATTN_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!pools[device]) {
+        cudaMemPoolProps props = {};
+        props.allocType = cudaMemAllocationTypePinned;
+        props.handleTypes = cudaMemHandleTypeNone;
+        props.location.type = cudaMemLocationTypeDevice;
+        props.location.id = device;
+        cudaMemPool_t pool;
+        if (cudaMemPoolCreate(&pool, &props) != cudaSuccess) return ATTN_ERR_CUDA;
+        uint64_t keep = ~0ull;
+        if (cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep) != cudaSuccess) {
+            cudaMemPoolDestroy(pool);
+            return ATTN_ERR_CUDA;
+        }
+        pools[device] = pool;
+    }
+    *out = pools[device];
+    return ATTN_OK;
+}
+
+template <int D, bool OUT_F32>
+attn_status_t launch_with_partials(const CUtensorMap& tq, const CUtensorMap& tk,
+                                   const CUtensorMap& tv, const CUtensorMap& to, float* lse,
+                                   FwdParams& p, int grid, cudaStream_t stream,
+                                   const DeviceInfo& dev) {
+    const size_t bytes = (size_t)p.split.n_split * p.split.parts * 8 *
+                         partial_block_floats<D>() * sizeof(float);
+    p.partial = nullptr;
+    if (bytes == 0) return launch_fwd_t<D, OUT_F32>(tq, tk, tv, to, lse, p, grid, stream, dev);
+    cudaMemPool_t pool;
+    attn_status_t st = partial_pool(dev.device, &pool);
+    if (st != ATTN_OK) return st;
+    void* buf = nullptr;
+    if (cudaMallocFromPoolAsync(&buf, bytes, pool, stream) != cudaSuccess) return ATTN_ERR_CUDA;
+    p.partial = static_cast<float*>(buf);
+    st = launch_fwd_t<D, OUT_F32>(tq, tk, tv, to, lse, p, grid, stream, dev);
+    if (cudaFreeAsync(buf, stream) != cudaSuccess && st == ATTN_OK) st = ATTN_ERR_CUDA;
+    return st;
 }
 
 }  // namespace
@@ -669,6 +911,10 @@ attn_status_t launch_fwd(const void* q, const void* k, const void* v, void* o, f
     p.c = scale * kLog2e;
     static std::atomic<uint32_t> launches{0};
     p.slot = launches.fetch_add(1u, std::memory_order_relaxed) % kQueueSlots;
+    p.split = plan_tail_split(p.shape, dev.num_sms);
+    const uint32_t items = split_items(p.split);
+    const int grid = (int)(items < (uint32_t)dev.num_sms ? items : (uint32_t)dev.num_sms);
+    p.partial = nullptr;
     CUtensorMap tq, tk, tv, to;
     attn_status_t st;
     const bool f32 = o_dtype == ATTN_OUT_F32;
@@ -678,11 +924,11 @@ attn_status_t launch_fwd(const void* q, const void* k, const void* v, void* o, f
     if ((st = encode_tmap_out_3d(&to, o, f32, d, Nq, (long long)B * Hq, kEpiCols(f32), 32)) != ATTN_OK)
         return st;
     if (d == 128)
-        return f32 ? launch_fwd_t<128, true>(tq, tk, tv, to, lse, p, stream, dev)
-                   : launch_fwd_t<128, false>(tq, tk, tv, to, lse, p, stream, dev);
+        return f32 ? launch_with_partials<128, true>(tq, tk, tv, to, lse, p, grid, stream, dev)
+                   : launch_with_partials<128, false>(tq, tk, tv, to, lse, p, grid, stream, dev);
     if (d == 64)
-        return f32 ? launch_fwd_t<64, true>(tq, tk, tv, to, lse, p, stream, dev)
-                   : launch_fwd_t<64, false>(tq, tk, tv, to, lse, p, stream, dev);
+        return f32 ? launch_with_partials<64, true>(tq, tk, tv, to, lse, p, grid, stream, dev)
+                   : launch_with_partials<64, false>(tq, tk, tv, to, lse, p, grid, stream, dev);
     return ATTN_ERR_UNSUPPORTED;
 }
 

@@ -101,4 +101,59 @@ GB300_HD void unit_of(const FwdShape& s, uint32_t i, int& bh, int& mb) {
     mb = s.causal ? (int)((uint32_t)s.nmb - 1u - rank) : (int)rank;
 }
 
+// Tail split.  Without causal masking every unit costs the same, so a unit
+// count just above a multiple of the SM count leaves most CTAs idle in the
+// last round (512 units on 152 SMs: 56 CTAs run a 4th unit), and fewer units
+// than SMs leave SMs idle throughout.  The units of that last round ("tail"
+// units) are then cut along the KV range into `parts` pieces that run on
+// otherwise idle CTAs; each piece keeps its own (m, l) and
+// O, and the last piece to finish merges them (lecture notes 6.1: split-KV
+// pieces merged by the rescaling rule of 2.2, exact for any number of pieces).  Causal launches are not split: their units differ in
+// cost and the longest-first order already fills the last round.
+constexpr int kMaxSplitParts = 8;
+constexpr int kMaxSplitUnits = 255;
+
+struct FwdSplit {
+    int n_full;   // units run whole: list positions [0, n_full)
+    int n_split;  // tail units run in parts: list positions [n_full, n_full + n_split)
+    int parts;    // pieces per tail unit (1 when nothing is split)
+};
+
+GB300_HD FwdSplit plan_tail_split(const FwdShape& s, int num_sms) {
+    FwdSplit r;
+    r.n_full = (int)s.units; r.n_split = 0; r.parts = 1;
+    if (s.causal || num_sms < 2 || s.units < 1) return r;
+    const long long tail = s.units % num_sms;
+    if (tail == 0 || tail > kMaxSplitUnits) return r;
+    long long parts = num_sms / tail;               // all pieces in one round
+    const int n = kv_tiles_for_rows(0, 1, s.Nq, s.Nk, 0, kTileN);  // KV tiles per unit
+    if (parts > n) parts = n;
+    if (parts > kMaxSplitParts) parts = kMaxSplitParts;
+    if (parts < 2) return r;
+    r.n_full = (int)(s.units - tail);
+    r.n_split = (int)tail;
+    r.parts = (int)parts;
+    return r;
+}
+
+GB300_HD uint32_t split_items(const FwdSplit& sp) {
+    return (uint32_t)sp.n_full + (uint32_t)sp.n_split * (uint32_t)sp.parts;
+}
+
+// Work item -> unit (list position) and piece (-1: the whole unit).
+GB300_HD void item_of(const FwdSplit& sp, uint32_t item, uint32_t& unit, int& part) {
+    if (item < (uint32_t)sp.n_full) { unit = item; part = -1; return; }
+    const uint32_t r = item - (uint32_t)sp.n_full;
+    const uint32_t k = r / (uint32_t)sp.parts;
+    unit = (uint32_t)sp.n_full + k;
+    part = (int)(r - k * (uint32_t)sp.parts);
+}
+
+// KV tiles [j0, j1) of piece `part` of a unit with n KV tiles.
+GB300_HD void part_range(int n, int parts, int part, int& j0, int& j1) {
+    if (part < 0) { j0 = 0; j1 = n; return; }
+    j0 = (int)((long long)part * n / parts);
+    j1 = (int)((long long)(part + 1) * n / parts);
+}
+
 }  // namespace gb300

@@ -6,7 +6,9 @@ profiler captures (ncu) of a single launch configuration.
 
 Workloads: prefill (B=4 H=16 N=2048 d=128), prefill2x (B=8: inputs larger
 than L2), long (B=1 H=32 N=16384), gqa (B=8 Hq=32 Hkv=8 N=4096), decode
-(B=16 Hq=32 Hkv=8 Nmax=32768).  Inputs come from the seeded generators.
+(B=16 Hq=32 Hkv=8 Nmax=32768, lengths 1024..32768) and decode_quarter (the
+same with Nmax=8192, lengths 256..8192: a 512 MiB cache, still larger than
+L2, for multi-pass captures).  Inputs come from the seeded generators.
 """
 from __future__ import annotations
 
@@ -16,7 +18,7 @@ import torch
 
 import exact_attention_14_gb300 as ea
 from exact_attention_14_gb300.inputs import (DECODE, GQA, LONG, PREFILL, make_decode_config_inputs,
-                                             make_fwd_inputs)
+                                             make_decode_inputs, make_fwd_inputs)
 
 FWD = {
     "prefill": PREFILL,
@@ -44,7 +46,13 @@ def main():
         for _ in range(args.iters):
             ea.attn_fwd(q, k, v, o, lse, causal=causal)
     else:
-        q, kc, vc, sl = (t.to(dev) for t in make_decode_config_inputs(DECODE))
+        if args.workload == "decode_quarter":
+            host = make_decode_inputs(DECODE.B, DECODE.Hq, DECODE.Hkv, DECODE.Nmax // 4, DECODE.d,
+                                      seed=DECODE.seed, len_lo=DECODE.len_lo // 4,
+                                      len_hi=DECODE.len_hi // 4)
+        else:
+            host = make_decode_config_inputs(DECODE)
+        q, kc, vc, sl = (t.to(dev) for t in host)
         for _ in range(args.iters):
             ea.decode(q, kc, vc, sl)
     torch.cuda.synchronize()

@@ -79,9 +79,12 @@ typedef enum {
  * probabilities; O is divided by that sum plus, per KV tile, the rounding
  * error of the tile's largest rounded probability.
  * Work distribution: the kernel's CTAs take units from the attn_fwd_schedule
- * list through a device-side queue (one of 1024 slots per launch, rotated by
- * the library and left zeroed when the kernel ends), so at most 1024 attn_fwd
- * launches may be in flight at the same time.
+ * list through a device-side queue (one of 256 slots per launch, rotated by
+ * the library and left zeroed when the kernel ends), so at most 256 attn_fwd
+ * launches may be in flight at the same time.  Tail units may be split along
+ * the KV range (attn_fwd_split_plan); their partial results live in memory
+ * the library takes from its own stream-ordered pool on `stream` for the
+ * launch and returns after it (ATTN_ERR_CUDA if that allocation fails).
  * Returns ATTN_OK once the kernel is enqueued.
  */
 attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
@@ -208,6 +211,25 @@ long long attn_fwd_num_units(int B, int Hq, int Hkv, int Nq, int Nk, int d, int 
  */
 int attn_fwd_schedule(int B, int Hq, int Hkv, int Nq, int Nk, int d, int causal,
                       long long n, int* units_out, int* cost_out);
+
+/*
+ * The tail split attn_fwd applies on a GPU with `num_sms` SMs.  Without
+ * causal masking all units cost the same; when their count is not a multiple
+ * of num_sms, the last units % num_sms units of the schedule (the "tail") are
+ * each cut along the KV range into `parts` pieces of near-equal tile counts
+ * (piece p of n tiles: tiles [p*n/parts, (p+1)*n/parts)), parts =
+ * min(num_sms / tail, KV tiles per unit, 8), so that all pieces run in one
+ * round on CTAs that would otherwise idle.  The persistent grid is
+ * min(n_full + n_split * parts, num_sms) CTAs.  Each piece keeps its own running max and sums;
+ * the last piece of a tail unit to finish merges them by the logsumexp
+ * rescaling (lecture notes 6.1 split-KV, 2.2 rescaling).  No split (n_split =
+ * 0, parts = 1) for causal launches, when units is a multiple of the grid,
+ * when parts < 2 or when the tail exceeds 255 units.  Writes the number of
+ * whole units, of split units and the pieces per split unit; returns 0, or -1
+ * on a bad argument.
+ */
+int attn_fwd_split_plan(int B, int Hq, int Hkv, int Nq, int Nk, int d, int causal, int num_sms,
+                        int* n_full, int* n_split, int* parts);
 
 #ifdef __cplusplus
 }

@@ -150,6 +150,38 @@ def test_outlier_channels_large_logits():
     assert_close(o, lse, o_ref, lse_ref, "outliers")
 
 
+# ------------------------------- tail split ----------------------------------
+# Non-causal launches whose unit count is not a multiple of the SM count cut
+# their last units along the KV range; the last piece to finish merges them.
+
+def _num_sms():
+    return torch.cuda.get_device_properties(0).multi_processor_count
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,Nq,Nk,d,out_f32,outliers", [
+    (1, 1, 1, 256, 4000, 64, True, 0),      # one unit in 8 pieces, ragged last KV tile
+    (1, 8, 8, 100, 2048, 128, True, 0),     # Q tile 1 of every unit is empty
+    (5, 7, 7, 1500, 1500, 128, True, 0),    # whole units, then a split tail
+    (1, 3, 1, 300, 5000, 64, False, 0),     # GQA 3:1, bf16 output
+    (1, 4, 4, 1024, 1024, 128, True, 4),    # outlier channels: piece maxima far apart
+])
+def test_tail_split_parity(B, Hq, Hkv, Nq, Nk, d, out_f32, outliers):
+    n_full, n_split, parts = ea.attn_fwd_split_plan(B, Hq, Hkv, Nq, Nk, d, False, _num_sms())
+    assert n_split > 0 and parts > 1
+    q, k, v = make_fwd_inputs(B, Hq, Hkv, Nq, Nk, d, seed=200 + Nq + d,
+                              outlier_channels=outliers)
+    scale = 1 / math.sqrt(d)
+    o, lse = gpu_fwd(q, k, v, False, scale,
+                     out_dtype=torch.float32 if out_f32 else torch.bfloat16)
+    o_ref, lse_ref = oracle.attention(q, k, v, causal=False, scale=scale)
+    what = f"split {(B, Hq, Hkv, Nq, Nk, d)} into {n_split} x {parts}"
+    if out_f32:
+        assert_close(o, lse, o_ref, lse_ref, what)
+    else:
+        assert_close_bf16(o, o_ref, what)
+        assert np.abs(lse - lse_ref).max() <= MAX_ABS_LSE
+
+
 def test_repeatable_and_stream_ordered():
     """Same inputs twice on a side stream give bit-identical results."""
     q, k, v = (t.cuda() for t in make_fwd_inputs(2, 4, 4, 640, 640, 128, seed=3))
@@ -168,39 +200,44 @@ def test_repeatable_and_stream_ordered():
 # returns to zero.  A unit's result does not depend on which CTA computes it,
 # so every launch below must match its eager reference bit for bit.
 
-def test_graph_replays_reuse_the_work_queue():
+@pytest.mark.parametrize("causal", [True, False])
+def test_graph_replays_reuse_the_work_queue(causal):
     """A captured launch replays on the same queue slot: each replay must see a
-    reset queue and compute every unit."""
+    reset queue and compute every unit.  Non-causal, the shape's 64 units are
+    split in pieces, whose partials come from the library's stream-ordered
+    pool inside the capture."""
     B, H, N, d = 2, 8, 1024, 128
     q, k, v = (t.cuda() for t in make_fwd_inputs(B, H, H, N, N, d, seed=21))
     o = torch.empty(q.shape, dtype=torch.float32, device="cuda")
     lse = torch.empty(q.shape[:3], dtype=torch.float32, device="cuda")
-    ea.attn_fwd(q, k, v, o, lse, causal=True)  # first call outside capture
+    ea.attn_fwd(q, k, v, o, lse, causal=causal)  # first call outside capture
     torch.cuda.synchronize()
     g = torch.cuda.CUDAGraph()
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(s):
         with torch.cuda.graph(g, stream=s):
-            ea.attn_fwd(q, k, v, o, lse, causal=True)
+            ea.attn_fwd(q, k, v, o, lse, causal=causal)
     torch.cuda.current_stream().wait_stream(s)
     for seed in (22, 23, 24):
         q2, k2, v2 = (t.cuda() for t in make_fwd_inputs(B, H, H, N, N, d, seed=seed))
         q.copy_(q2); k.copy_(k2); v.copy_(v2)
         o.fill_(float("nan"))
         g.replay()
-        o_ref, l_ref = ea.forward(q, k, v, causal=True, out_dtype=torch.float32)
+        o_ref, l_ref = ea.forward(q, k, v, causal=causal, out_dtype=torch.float32)
         torch.cuda.synchronize()
         assert ea.attn_last_device_error() == 0
         assert torch.equal(o, o_ref) and torch.equal(lse, l_ref), f"replay with seed {seed}"
 
 
-def test_concurrent_launches_on_two_streams():
-    """Launches in flight together on two streams use different queue slots."""
+@pytest.mark.parametrize("causal", [True, False])
+def test_concurrent_launches_on_two_streams(causal):
+    """Launches in flight together on two streams use different queue slots
+    (and, split, different partial buffers)."""
     cases = [make_fwd_inputs(4, 8, 2, 1536, 1536, 128, seed=31),
              make_fwd_inputs(3, 8, 8, 1000, 1000, 64, seed=32)]
     cases = [tuple(t.cuda() for t in c) for c in cases]
-    refs = [ea.forward(*c, causal=True, out_dtype=torch.float32) for c in cases]
+    refs = [ea.forward(*c, causal=causal, out_dtype=torch.float32) for c in cases]
     torch.cuda.synchronize()
     streams = [torch.cuda.Stream(), torch.cuda.Stream()]
     for st in streams:
@@ -209,7 +246,7 @@ def test_concurrent_launches_on_two_streams():
     for _ in range(4):
         for i, (st, c) in enumerate(zip(streams, cases)):
             with torch.cuda.stream(st):
-                outs[i].append(ea.forward(*c, causal=True, out_dtype=torch.float32, stream=st))
+                outs[i].append(ea.forward(*c, causal=causal, out_dtype=torch.float32, stream=st))
     torch.cuda.synchronize()
     assert ea.attn_last_device_error() == 0
     for i in range(2):

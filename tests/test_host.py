@@ -185,6 +185,49 @@ def test_dense_schedule_uses_narrow_sections(lib):
         assert [m for _, _, m in chunk] == sorted(m for _, _, m in chunk)
 
 
+@pytest.mark.parametrize("shape,causal,sms,expect", [
+    ((4, 16, 16, 2048, 2048, 128), False, 152, (456, 56, 2)),   # prefill: 512 units
+    ((4, 16, 16, 2048, 2048, 128), True, 152, (512, 0, 1)),     # causal: never split
+    ((3, 19, 19, 2048, 2048, 128), False, 152, (456, 0, 1)),    # 3 full rounds
+    ((1, 8, 8, 2048, 2048, 128), False, 152, (0, 64, 2)),       # 64 units, 152 SMs
+    ((1, 2, 2, 4096, 4096, 64), False, 152, (0, 32, 4)),        # 32 units: 4 pieces
+    ((1, 1, 1, 256, 128, 64), False, 152, (1, 0, 1)),           # 1 KV tile: cannot split
+    ((1, 1, 1, 256, 256, 64), False, 152, (0, 1, 2)),
+    ((1, 1, 1, 256, 100000, 64), False, 152, (0, 1, 8)),        # at most 8 pieces
+    ((2, 100, 100, 256, 2048, 128), False, 152, (152, 48, 3)),
+])
+def test_tail_split_plan(lib, shape, causal, sms, expect):
+    assert ea.attn_fwd_split_plan(*shape, causal, sms) == expect
+
+
+def _split_items(shape, causal, sms):
+    """(cost in (Q tile, KV tile) pairs) of every work item in queue order."""
+    B, Hq, Hkv, Nq, Nk, d = shape
+    order, costs = ea.attn_fwd_schedule(B, Hq, Hkv, Nq, Nk, d, causal)
+    n_full, n_split, parts = ea.attn_fwd_split_plan(*shape, causal, sms)
+    items = list(costs[:n_full])
+    for u in range(n_full, n_full + n_split):
+        n = -(-Nk // 128)
+        tiles = 2 if Nq - order[u][2] * 256 > 128 else 1
+        bounds = [p * n // parts for p in range(parts + 1)]
+        assert bounds[0] == 0 and bounds[-1] == n and all(b1 > b0 for b0, b1 in zip(bounds, bounds[1:]))
+        items += [tiles * (b1 - b0) for b0, b1 in zip(bounds, bounds[1:])]
+    return costs, items
+
+
+@pytest.mark.parametrize("B,H,N", [(4, 16, 2048), (1, 8, 2048), (2, 12, 3000), (5, 7, 1500),
+                                   (1, 40, 8192), (8, 16, 1024)])
+def test_tail_split_never_lengthens_the_modelled_makespan(lib, B, H, N):
+    shape = (B, H, H, N, N, 128)
+    costs, items = _split_items(shape, False, 152)
+    assert sum(items) == sum(costs)  # the pieces cover every unit's KV tiles once
+    whole = ea.attn_list_schedule(costs, 152, lpt=False)[0]
+    split = ea.attn_list_schedule(items, 152, lpt=False)[0]
+    assert split <= whole
+    if (B, H, N) == (4, 16, 2048):
+        assert (whole, split) == (4 * 32, 3 * 32 + 16)
+
+
 def test_gqa_siblings_are_adjacent(lib):
     order, _ = ea.attn_fwd_schedule(2, 8, 2, 512, 512, 64, True)
     # consecutive units of one m-block rank share a KV head in groups of 4
