@@ -279,7 +279,7 @@ def run_ours(args, rank, world, local_rank):
             "achieved": (f_nc + f_c) / fwd_time / 1e12, "peak": peak_t, "unit": "TFLOP/s",
             "frac": (f_nc + f_c) / fwd_time / 1e12 / peak_t, "traffic": None,
             "peak_source": f"{peaks['source']} bf16_tflops (burst)"}
-    roof_dec = {"bound": "hbm", "kernel": "attn_decode_split_kernel + combine",
+    roof_dec = {"bound": "hbm", "kernel": "attn_decode_split_kernel (split-KV with in-kernel merge)",
                 "achieved": dec_bytes / t_dec / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": dec_bytes / t_dec / 1e9 / peaks["hbm_gbs"], "traffic": None,
                 "peak_source": f"{peaks['source']} hbm_gbs"}
@@ -300,7 +300,8 @@ def run_ours(args, rank, world, local_rank):
                    "sum_seqlen": sum_len},
         "roofline": roof, "roofline_decode": roof_dec,
         "cpu_baseline": cpu, "e2e": e2e,
-        "gpu_launches": 4 * args.steps,
+        "gpu_launches": (2 + ea.attn_decode_kernel_launches(DECODE.B, DECODE.Hq, DECODE.Hkv,
+                                                            DECODE.Nmax, DECODE.d)) * args.steps,
         "wall_s_timed_region": wall,
         "clocks": clk.summary(),
     }

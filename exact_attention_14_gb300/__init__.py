@@ -18,7 +18,7 @@ __all__ = [
     "ATTN_OUT_BF16", "ATTN_OUT_F32", "AttnError", "attn_fwd", "attn_decode",
     "attn_decode_workspace_size", "attn_decode_noalloc", "attn_status_string", "attn_last_device_error",
     "attn_decode_num_splits", "attn_list_schedule", "attn_kv_tiles",
-    "attn_fwd_num_units", "attn_fwd_schedule", "attn_fwd_split_plan", "forward", "decode", "library_path", "load",
+    "attn_fwd_num_units", "attn_fwd_schedule", "attn_fwd_split_plan", "attn_decode_kernel_launches", "forward", "decode", "library_path", "load",
 ]
 
 ATTN_OK = 0
@@ -54,6 +54,7 @@ SIGNATURES = {
     "attn_fwd_schedule": (_c_int, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
                                    _c_ll, ctypes.POINTER(ctypes.c_int),
                                    ctypes.POINTER(ctypes.c_int)]),
+    "attn_decode_kernel_launches": (_c_int, [_c_int] * 6),
     "attn_fwd_split_plan": (_c_int, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
                                      _c_int, ctypes.POINTER(ctypes.c_int),
                                      ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int)]),
@@ -294,3 +295,12 @@ def attn_fwd_split_plan(B, Hq, Hkv, Nq, Nk, d, causal, num_sms):
     if rc != 0:
         raise ValueError("attn_fwd_split_plan rejected its arguments")
     return tuple(o.value for o in out)
+
+
+def attn_decode_kernel_launches(B, Hq, Hkv, Nmax, d, num_splits=0) -> int:
+    """Kernels attn_decode launches for this shape: 1 (the split kernel merges)
+    or 2 (split + combine)."""
+    n = int(load().attn_decode_kernel_launches(B, Hq, Hkv, Nmax, d, num_splits))
+    if n < 0:
+        raise ValueError("attn_decode_kernel_launches rejected its arguments")
+    return n

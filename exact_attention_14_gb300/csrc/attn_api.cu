@@ -185,6 +185,15 @@ size_t attn_decode_workspace_size(int B, int Hq, int Hkv, int Nmax, int d, int n
     return decode_workspace_bytes(B, Hq, Nmax, d, chunk);
 }
 
+int attn_decode_kernel_launches(int B, int Hq, int Hkv, int Nmax, int d, int num_splits) {
+    if (check_decode_shape(B, Hq, Hkv, Nmax, d, num_splits) != ATTN_OK) return -1;
+    int sms = 0;
+    if (decode_sms_or_default(&sms) != 0) return -1;
+    const int chunk = decode_chunk(Nmax, B, Hkv, sms, num_splits);
+    const int max_splits = (Nmax + chunk - 1) / chunk;
+    return decode_merges_in_kernel(B, Hkv, Hq / Hkv, max_splits, d) ? 1 : 2;
+}
+
 attn_status_t attn_decode(const void* q, const void* k_cache, const void* v_cache,
                           const int* seqlens, void* o, float* lse, int B, int Hq, int Hkv,
                           int Nmax, int d, float scale, int num_splits, void* workspace,

@@ -15,15 +15,22 @@
 // final O / LSE (when the sequence has one split) or a partial (o_s, lse_s)
 // to the workspace.
 //
-// Kernel 2 (combine): per (b, query head) with more than one split, the
+// Merge of the splits: per (b, query head) with more than one split, the
 // partials are merged by log-sum-exp: M = max lse_s, w_s = 2^(lse_s - M),
 // O = sum w_s o_s / sum w_s, LSE = M + log2 sum w_s (lecture notes 6.1 and
-// exercise 3; "FlashAttention tiling & online softmax" 7.1).
+// exercise 3; "FlashAttention tiling & online softmax" 7.1), in split order.
+// Normally the last split CTA of a (b, KV head) to finish does it: each split
+// CTA counts itself in on a per-(b, KV head) counter after writing its
+// partial, and the one that completes the count merges the group's G heads
+// and returns the counter to zero.  Shapes with more (b, KV head) groups than
+// the counter table holds, or more splits than the merge's shared-memory
+// scratch holds, use a second kernel (combine) for the merge.
 //
 // The decode path is memory-bound by design (it must read the KV cache once):
 // it is measured against HBM bandwidth.  Keys at or past L_b are never used:
 // their scores are masked by selection and their V rows are zeroed in shared
 // memory before the P.V product, so NaN there cannot leak.
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 
@@ -58,8 +65,21 @@ struct DecCfg {
 
 struct DecParams {
     int B, Hq, Hkv, G, Nmax, chunk, max_splits;
-    float c;  // scale * log2(e)
+    float c;   // scale * log2(e)
+    int slot;  // arrival-counter slot of this launch; -1: merge in the combine kernel
 };
+
+// Arrival counters of the in-kernel merge: one per (b, KV head) group and
+// launch slot.  Launches rotate through the slots, and every count returns to
+// zero when its group is merged, so up to kDecSlots launches may be in flight
+// at the same time.
+constexpr int kDecSlots = 64;
+constexpr int kDecMaxGroups = 4096;
+__device__ unsigned int g_dec_count[kDecSlots][kDecMaxGroups];
+
+__device__ __forceinline__ void consumers_sync() {
+    asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+}
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
                                         uint32_t& r3) {
@@ -102,7 +122,19 @@ attn_decode_split_kernel(const __grid_constant__ CUtensorMap tk, const __grid_co
         L = L < 0 ? 0 : (L > p.Nmax ? p.Nmax : L);
     }
     const int t0 = split * p.chunk;
-    if (t0 >= L) return;  // uniform across the CTA: nothing started yet
+    if (t0 >= L) {  // uniform across the CTA: nothing started yet
+        if (L == 0 && split == 0 && p.slot >= 0) {
+            // an empty sequence: O = 0 and LSE = -inf for the group's heads
+            for (int e = threadIdx.x; e < p.G * D; e += blockDim.x) {
+                const size_t bh = (size_t)b * p.Hq + (size_t)g * p.G + e / D;
+                const int col = e % D;
+                if constexpr (OUT_F32) static_cast<float*>(o)[bh * D + col] = 0.f;
+                else static_cast<__nv_bfloat16*>(o)[bh * D + col] = __float2bfloat16_rn(0.f);
+                if (col == 0 && lse) lse[bh] = -INFINITY;
+            }
+        }
+        return;
+    }
     const int t1 = min(t0 + p.chunk, L);
     const int n_stages = (t1 - t0 + kStageKeys - 1) / kStageKeys;
     const int nsplit_b = (L + p.chunk - 1) / p.chunk;
@@ -323,9 +355,9 @@ attn_decode_split_kernel(const __grid_constant__ CUtensorMap tk, const __grid_co
         sx[warp * kMaxGroup + qr + 8] = x1;
     }
     __syncthreads();
-    if (!ok || *abort_flag) return;
+    const bool live = ok && !*abort_flag;
     const int tid = threadIdx.x;  // 0..127
-    for (int e = tid; e < G * D; e += kConsumerWarps * 32) {
+    for (int e = tid; e < G * D && live; e += kConsumerWarps * 32) {
         const int h = e / D, col = e - h * D;
         float M = -INFINITY;
 #pragma unroll
@@ -351,6 +383,78 @@ attn_decode_split_kernel(const __grid_constant__ CUtensorMap tk, const __grid_co
             if (col == 0) ws_lse[bh * p.max_splits + split] = lse2;
         }
     }
+    if (nsplit_b == 1 || p.slot < 0) return;
+    // Count this split in (even after an abort, so that the count stays
+    // whole); the CTA that completes the count merges the group.
+    unsigned int* count = &g_dec_count[p.slot][kv_head];
+    volatile int* is_last = abort_flag + 1;
+    __threadfence();
+    consumers_sync();
+    if (tid == 0) *is_last = atomicAdd(count, 1u) == (unsigned int)(nsplit_b - 1);
+    consumers_sync();
+    if (!*is_last) return;
+    __threadfence();
+    // 1. the partials' LSEs of every (head, split) into shared memory, then per
+    //    head (one warp each) M = max lse_s and the weights w_s = 2^(lse_s - M)
+    // (the drained stage ring holds them: the host enables this merge only
+    // when 2 * kMaxGroup + G * max_splits floats fit in it)
+    float* s_head = reinterpret_cast<float*>(smem + C::kScratchO);  // [G][2]: 1/sum w, LSE
+    float* s_w = s_head + 2 * kMaxGroup;                              // [G][nsplit_b]
+    const size_t bh0 = (size_t)b * p.Hq + (size_t)g * G;
+    for (int i = tid; i < G * nsplit_b; i += kConsumerWarps * 32) {
+        const int h = i / nsplit_b, sp = i - h * nsplit_b;
+        s_w[i] = __ldcg(ws_lse + (bh0 + h) * p.max_splits + sp);
+    }
+    consumers_sync();
+    for (int h = warp; h < G; h += kConsumerWarps) {
+        float M = -INFINITY;
+        for (int sp = lane; sp < nsplit_b; sp += 32) M = fmaxf(M, s_w[h * nsplit_b + sp]);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, off));
+        float sum = 0.f;
+        for (int sp = lane; sp < nsplit_b; sp += 32) {
+            const float w = ex2(s_w[h * nsplit_b + sp] - M);
+            s_w[h * nsplit_b + sp] = w;
+            sum += w;
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, off);
+        if (lane == 0) {
+            s_head[2 * h] = 1.0f / sum;
+            s_head[2 * h + 1] = (M + log2f(sum)) * kLn2f;
+        }
+    }
+    consumers_sync();
+    // 2. O = sum_s w_s o_s / sum_s w_s, four columns per thread, several
+    //    splits' loads in flight
+    for (int e = tid; e < G * (D / 4); e += kConsumerWarps * 32) {
+        const int h = e / (D / 4), c4 = e - h * (D / 4);
+        const float* wh = s_w + h * nsplit_b;
+        const float4* src = reinterpret_cast<const float4*>(ws_o + (bh0 + h) * p.max_splits * D) + c4;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
+        for (int sp = 0; sp < nsplit_b; ++sp) {
+            const float4 v = __ldcg(src + (size_t)sp * (D / 4));
+            const float w = wh[sp];
+            acc.x = fmaf(w, v.x, acc.x);
+            acc.y = fmaf(w, v.y, acc.y);
+            acc.z = fmaf(w, v.z, acc.z);
+            acc.w = fmaf(w, v.w, acc.w);
+        }
+        const float inv = s_head[2 * h];
+        const size_t base = (bh0 + h) * D + (size_t)c4 * 4;
+        if constexpr (OUT_F32) {
+            *reinterpret_cast<float4*>(static_cast<float*>(o) + base) =
+                make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+        } else {
+            uint2 pk;
+            pk.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+            pk.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+            *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(o) + base) = pk;
+        }
+        if (c4 == 0 && lse) lse[bh0 + h] = s_head[2 * h + 1];
+    }
+    if (tid == 0) *count = 0u;
 }
 
 template <int D, bool OUT_F32>
@@ -399,17 +503,26 @@ attn_status_t launch_decode_t(const CUtensorMap& tk, const CUtensorMap& tv, cons
             return ATTN_ERR_CUDA;
         attr_set[dev.device] = 1;
     }
+    const DecParams& pk = p;
     dim3 grid((unsigned)p.max_splits, (unsigned)p.Hkv, (unsigned)p.B);
     attn_decode_split_kernel<D, OUT_F32><<<grid, kDecThreads, C::kSmemBytes, stream>>>(
-        tk, tv, static_cast<const __nv_bfloat16*>(q), seqlens, o, lse, ws_o, ws_lse, p,
+        tk, tv, static_cast<const __nv_bfloat16*>(q), seqlens, o, lse, ws_o, ws_lse, pk,
         dev.err_word);
     if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
+    if (pk.slot >= 0) return ATTN_OK;  // merged in the split kernel
     dim3 cgrid((unsigned)p.Hq, (unsigned)p.B);
-    attn_decode_combine_kernel<D, OUT_F32><<<cgrid, D, 0, stream>>>(seqlens, ws_o, ws_lse, o, lse, p);
+    attn_decode_combine_kernel<D, OUT_F32><<<cgrid, D, 0, stream>>>(seqlens, ws_o, ws_lse, o, lse, pk);
     return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
 }  // namespace
+
+bool decode_merges_in_kernel(int B, int Hkv, int G, int max_splits, int d) {
+    // counter table, and the split weights in the drained stage ring
+    const size_t ring_floats = (size_t)(d == 128 ? DecCfg<128>::kBarOff : DecCfg<64>::kBarOff) / 4;
+    return (long long)B * Hkv <= kDecMaxGroups &&
+           (size_t)(2 * kMaxGroup) + (size_t)G * (size_t)max_splits <= ring_floats;
+}
 
 int decode_chunk(int Nmax, int B, int Hkv, int num_sms, int num_splits) {
     int s = num_splits;
@@ -446,6 +559,10 @@ attn_status_t launch_decode(const void* q, const void* k_cache, const void* v_ca
     p.chunk = chunk;
     p.max_splits = (Nmax + chunk - 1) / chunk;
     p.c = scale * kLog2ef;
+    static std::atomic<uint32_t> launches{0};
+    p.slot = decode_merges_in_kernel(B, Hkv, p.G, p.max_splits, d)
+                 ? (int)(launches.fetch_add(1u, std::memory_order_relaxed) % kDecSlots)
+                 : -1;
     const size_t rows = (size_t)B * Hq * p.max_splits;
     float* ws_o = static_cast<float*>(workspace);
     float* ws_lse = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + align16(rows * d * 4));

@@ -34,6 +34,9 @@ attn_status_t launch_fwd(const void* q, const void* k, const void* v, void* o, f
 // Decode: chunk size in keys for a request (multiple of 64).
 int decode_chunk(int Nmax, int B, int Hkv, int num_sms, int num_splits);
 size_t decode_workspace_bytes(int B, int Hq, int Nmax, int d, int chunk);
+// Decode: whether the split kernel merges the splits itself (else a second
+// kernel does); max_splits = ceil(Nmax / chunk).
+bool decode_merges_in_kernel(int B, int Hkv, int G, int max_splits, int d);
 
 attn_status_t launch_decode(const void* q, const void* k_cache, const void* v_cache,
                             const int* seqlens, void* o, float* lse, int B, int Hq, int Hkv,

@@ -99,6 +99,15 @@ attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, flo
 size_t attn_decode_workspace_size(int B, int Hq, int Hkv, int Nmax, int d, int num_splits);
 
 /*
+ * Number of kernels attn_decode launches for this shape and split request:
+ * 1 when the split kernel merges the splits itself (the last split of each
+ * (sequence, KV head) to finish merges them; at most 4096 such groups and
+ * G * ceil(Nmax / chunk) + 32 floats of merge scratch), else 2 (a combine
+ * kernel merges).  Returns -1 for arguments attn_decode would reject.
+ */
+int attn_decode_kernel_launches(int B, int Hq, int Hkv, int Nmax, int d, int num_splits);
+
+/*
  * attn_decode -- one query token per sequence against a KV cache (split-KV).
  *
  *   q        bf16 [B, Hq, 1, d]

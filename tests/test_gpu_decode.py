@@ -115,3 +115,40 @@ def test_workspace_too_small_is_rejected():
     with pytest.raises(ea.AttnError) as ei:
         ea.attn_decode(q, kc, vc, sl, o, None, workspace=ws)
     assert ei.value.code == ea.ATTN_ERR_WORKSPACE
+
+
+def test_empty_sequence_gives_zero_output_and_minus_inf_lse():
+    """A length of 0 is out of range (reported) and clamps to an empty key set:
+    O = 0 and LSE = -inf, the empty-row convention of the oracle."""
+    q, kc, vc, sl = make_decode_inputs(3, 8, 2, 2048, 128, seed=12, len_lo=500, len_hi=2048)
+    sl[1] = 0
+    o, lse = ea.decode(q.cuda(), kc.cuda(), vc.cuda(), sl.cuda(), out_dtype=torch.float32)
+    assert ea.attn_last_device_error() == ea.ATTN_ERR_INVALID_ARG
+    o = o.cpu().double().numpy()
+    lse = lse.cpu().double().numpy()
+    assert (o[1] == 0).all() and np.isneginf(lse[1]).all()
+    o_ref, lse_ref = oracle.decode(q, kc, vc, sl)
+    keep = [0, 2]
+    assert_close(o[keep], lse[keep], o_ref[keep], lse_ref[keep], "other sequences")
+
+
+def test_many_groups_use_the_combine_kernel():
+    """More (sequence, KV head) groups than the in-kernel merge's counter table
+    (4096): the merge runs as a second kernel, with the same results."""
+    B, Hq, Hkv, Nmax, d = 1100, 8, 4, 192, 64
+    assert ea.attn_decode_kernel_launches(B, Hq, Hkv, Nmax, d, 3) == 2
+    assert ea.attn_decode_kernel_launches(DECODE.B, DECODE.Hq, DECODE.Hkv, DECODE.Nmax,
+                                          DECODE.d) == 1
+    q, kc, vc, sl = make_decode_inputs(B, Hq, Hkv, Nmax, d, seed=13, len_lo=1, len_hi=Nmax)
+    o, lse = gpu_decode(q, kc, vc, sl, num_splits=3)
+    o_ref, lse_ref = oracle.decode(q, kc, vc, sl)
+    assert_close(o, lse, o_ref, lse_ref, "combine kernel")
+
+
+def test_split_merge_is_repeatable():
+    q, kc, vc, sl = (t.cuda() for t in make_decode_inputs(4, 32, 8, 8192, 128, seed=14,
+                                                          len_lo=1000, len_hi=8192))
+    outs = [ea.decode(q, kc, vc, sl, out_dtype=torch.float32) for _ in range(3)]
+    torch.cuda.synchronize()
+    for o, lse in outs[1:]:
+        assert torch.equal(o, outs[0][0]) and torch.equal(lse, outs[0][1])
