@@ -45,6 +45,32 @@ def read_peaks():
             "source": "fallback"}
 
 
+def kernel_source_hash() -> str:
+    """sha256 over name + bytes of the kernel sources, in sorted order."""
+    import glob
+    import hashlib
+    csrc = os.path.join(ROOT, "exact_attention_14_gb300", "csrc")
+    files = sorted(glob.glob(os.path.join(csrc, "*.cu")) + glob.glob(os.path.join(csrc, "*.cuh"))
+                   + glob.glob(os.path.join(csrc, "*.h")))
+    h = hashlib.sha256()
+    for path in files:
+        h.update(os.path.basename(path).encode())
+        with open(path, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def read_traffic():
+    """DRAM bytes per launch from the committed ncu summary, or None when the
+    kernel sources changed since it was captured."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        t = json.load(f)
+    return t if t.get("source_sha256") == kernel_source_hash() else None
+
+
 class ClockSampler:
     """nvidia-smi clocks and throttle reasons sampled during the timed region."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -275,13 +301,21 @@ def run_ours(args, rank, world, local_rank):
         return
     fwd_time = t_nc + t_c
     peak_t = peaks["bf16_tflops"]
+    traffic = read_traffic()
     roof = {"bound": "tensor", "kernel": "attn_fwd_kernel (non-causal + causal launches)",
             "achieved": (f_nc + f_c) / fwd_time / 1e12, "peak": peak_t, "unit": "TFLOP/s",
-            "frac": (f_nc + f_c) / fwd_time / 1e12 / peak_t, "traffic": None,
+            "frac": (f_nc + f_c) / fwd_time / 1e12 / peak_t,
+            "traffic": (traffic["attn_fwd_kernel"]["prefill_noncausal"]
+                        + traffic["attn_fwd_kernel"]["prefill_causal"]) if traffic else None,
+            "traffic_note": "DRAM bytes of one non-causal + one causal launch (ncu, profiles/); "
+                            "algorithmic bytes 2 x 134.7 MB",
             "peak_source": f"{peaks['source']} bf16_tflops (burst)"}
     roof_dec = {"bound": "hbm", "kernel": "attn_decode_split_kernel (split-KV with in-kernel merge)",
                 "achieved": dec_bytes / t_dec / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": dec_bytes / t_dec / 1e9 / peaks["hbm_gbs"], "traffic": None,
+                "frac": dec_bytes / t_dec / 1e9 / peaks["hbm_gbs"],
+                "traffic": traffic["attn_decode_split_kernel"]["decode"] if traffic else None,
+                "traffic_note": "DRAM bytes per launch (ncu, profiles/); algorithmic bytes in "
+                                "decode.algorithmic_bytes",
                 "peak_source": f"{peaks['source']} hbm_gbs"}
     line = {
         "metric": METRIC, "value": tflops, "unit": "TFLOPS", "n_gpus": world,
