@@ -61,6 +61,11 @@ def _load():
             lib.oracle_lse_merge.argtypes = [ctypes.c_int, ctypes.c_int, dp, dp,
                                              dp, dp]
             lib.oracle_lse_merge.restype = None
+            lib.oracle_attention_bwd.argtypes = [
+                u16, u16, u16, u16, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double,
+                dp, dp, dp, ctypes.c_int]
+            lib.oracle_attention_bwd.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -165,3 +170,27 @@ def lse_merge(lse_parts, o_parts):
                              _ptr(o_parts, ctypes.c_double),
                              _ptr(lse, ctypes.c_double), _ptr(o, ctypes.c_double))
     return float(lse[0]), o
+
+
+def attention_bwd(q, k, v, dout, *, causal: bool = False, scale: float | None = None,
+                  n_threads: int = 0):
+    """Gradients of O = attention(q, k, v) for the upstream gradient dout
+    (bf16, shaped like q), in fp64.  Returns (dQ, dK, dV) as float64 arrays
+    shaped like q, k, v."""
+    qb, kb, vb, ob = _bits(q), _bits(k), _bits(v), _bits(dout)
+    B, Hq, Hkv, Nq, Nk, d = _shapes(qb, kb, vb)
+    if tuple(ob.shape) != tuple(qb.shape):
+        raise ValueError("dout must be shaped like q")
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    dq = np.empty(qb.shape, np.float64)
+    dk = np.empty(kb.shape, np.float64)
+    dv = np.empty(vb.shape, np.float64)
+    rc = _load().oracle_attention_bwd(
+        _ptr(qb, ctypes.c_uint16), _ptr(kb, ctypes.c_uint16), _ptr(vb, ctypes.c_uint16),
+        _ptr(ob, ctypes.c_uint16), B, Hq, Hkv, Nq, Nk, d, int(bool(causal)), float(scale),
+        _ptr(dq, ctypes.c_double), _ptr(dk, ctypes.c_double), _ptr(dv, ctypes.c_double),
+        int(n_threads))
+    if rc != 0:
+        raise ValueError("oracle_attention_bwd rejected its arguments")
+    return dq, dk, dv

@@ -35,6 +35,18 @@
  * O_s) of disjoint key sets: M = max_s LSE_s, w_s = exp(LSE_s - M),
  * O = sum_s w_s O_s / sum_s w_s, LSE = M + log sum_s w_s.
  *
+ * The gradients (lecture notes section 2.6; "FlashAttention: tiling +
+ * recomputation", section 3.3) for an upstream gradient dO of O, per row i
+ * with P_ij = exp(s_ij - LSE_i) over the allowed keys:
+ *
+ *   dP_ij = dO_i . v_j                 D_i  = sum_j P_ij dP_ij
+ *   dS_ij = P_ij (dP_ij - D_i)         (the softmax Jacobian applied to dP)
+ *   dQ_i  = scale sum_j dS_ij k_j      dK_j = scale sum_i dS_ij q_i
+ *   dV_j  = sum_i P_ij dO_i
+ *
+ * summed over the query heads of a KV head's group for dK and dV.  D is taken
+ * from its definition here (the kernels use the identity D_i = dO_i . O_i).
+ *
  * Inputs are bf16 bit patterns (uint16); widening bf16 to double is exact.
  */
 #include <math.h>
@@ -202,4 +214,99 @@ void oracle_lse_merge(int n, int d, const double *lse_parts, const double *o_par
     }
     for (c = 0; c < d; ++c) o_out[c] /= wsum;
     *lse_out = M + log(wsum);
+}
+
+/*
+ * Gradients of every row (see the header).  dout is bf16 like q, k, v;
+ * dq_out [B, Hq, Nq, d], dk_out and dv_out [B, Hkv, Nk, d].  One task per
+ * (b, KV head), so the sums over a group's query heads need no locks.
+ * Returns 0, or -1 on a bad argument.
+ */
+int oracle_attention_bwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                         const uint16_t *dout, int B, int Hq, int Hkv, int Nq, int Nk,
+                         int d, int causal, double scale, double *dq_out,
+                         double *dk_out, double *dv_out, int n_threads) {
+    if (B < 1 || Hq < 1 || Hkv < 1 || Nq < 1 || Nk < 1 || d < 1) return -1;
+    if (Hq % Hkv != 0) return -1;
+    const int group = Hq / Hkv;
+    const long n_groups = (long)B * Hkv;
+#ifdef _OPENMP
+    if (n_threads > 0) omp_set_num_threads(n_threads);
+#else
+    (void)n_threads;
+#endif
+    memset(dq_out, 0, sizeof(double) * (size_t)B * Hq * Nq * d);
+    memset(dk_out, 0, sizeof(double) * (size_t)B * Hkv * Nk * d);
+    memset(dv_out, 0, sizeof(double) * (size_t)B * Hkv * Nk * d);
+
+#pragma omp parallel
+    {
+        double *p = (double *)malloc(sizeof(double) * (size_t)Nk);
+        double *dp = (double *)malloc(sizeof(double) * (size_t)Nk);
+        double *qi = (double *)malloc(sizeof(double) * (size_t)d);
+        double *doi = (double *)malloc(sizeof(double) * (size_t)d);
+        long t;
+#pragma omp for schedule(dynamic, 1)
+        for (t = 0; t < n_groups; ++t) {
+            const int b = (int)(t / Hkv), g = (int)(t % Hkv);
+            const uint16_t *kh = k + ((size_t)b * Hkv + g) * (size_t)Nk * d;
+            const uint16_t *vh = v + ((size_t)b * Hkv + g) * (size_t)Nk * d;
+            double *dkh = dk_out + ((size_t)b * Hkv + g) * (size_t)Nk * d;
+            double *dvh = dv_out + ((size_t)b * Hkv + g) * (size_t)Nk * d;
+            for (int hq = g * group; hq < (g + 1) * group; ++hq) {
+                for (int i = 0; i < Nq; ++i) {
+                    const size_t row = ((size_t)b * Hq + hq) * Nq + i;
+                    int j_end = Nk;
+                    if (causal) {
+                        long last = (long)i + (long)(Nk - Nq);
+                        if (last + 1 < j_end) j_end = (int)(last + 1 < 0 ? 0 : last + 1);
+                    }
+                    if (j_end <= 0) continue; /* no allowed key: all gradients 0 */
+                    for (int c = 0; c < d; ++c) {
+                        qi[c] = bf16_bits_to_double(q[row * d + c]);
+                        doi[c] = bf16_bits_to_double(dout[row * d + c]);
+                    }
+                    /* P_i: the softmax of the scaled scores over the allowed keys */
+                    double m = -INFINITY;
+                    for (int j = 0; j < j_end; ++j) {
+                        double acc = 0.0;
+                        for (int c = 0; c < d; ++c)
+                            acc += qi[c] * bf16_bits_to_double(kh[(size_t)j * d + c]);
+                        p[j] = scale * acc;
+                        if (p[j] > m) m = p[j];
+                    }
+                    double sum = 0.0;
+                    for (int j = 0; j < j_end; ++j) {
+                        p[j] = exp(p[j] - m);
+                        sum += p[j];
+                    }
+                    for (int j = 0; j < j_end; ++j) p[j] /= sum;
+                    /* dP_i = dO_i V^T and D_i = sum_j P_ij dP_ij */
+                    double D = 0.0;
+                    for (int j = 0; j < j_end; ++j) {
+                        double acc = 0.0;
+                        for (int c = 0; c < d; ++c)
+                            acc += doi[c] * bf16_bits_to_double(vh[(size_t)j * d + c]);
+                        dp[j] = acc;
+                        D += p[j] * acc;
+                    }
+                    /* dS, then the three products */
+                    double *dqi = dq_out + row * d;
+                    for (int j = 0; j < j_end; ++j) {
+                        const double ds = p[j] * (dp[j] - D);
+                        for (int c = 0; c < d; ++c) {
+                            dqi[c] += scale * ds * bf16_bits_to_double(kh[(size_t)j * d + c]);
+                            dkh[(size_t)j * d + c] += scale * ds * qi[c];
+                            dvh[(size_t)j * d + c] += p[j] * doi[c];
+                        }
+                    }
+                }
+            }
+        }
+        free(p);
+        free(dp);
+        free(qi);
+        free(doi);
+    }
+    return 0;
 }
