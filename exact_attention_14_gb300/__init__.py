@@ -18,7 +18,8 @@ __all__ = [
     "ATTN_OUT_BF16", "ATTN_OUT_F32", "AttnError", "attn_fwd", "attn_decode",
     "attn_decode_workspace_size", "attn_decode_noalloc", "attn_status_string", "attn_last_device_error",
     "attn_decode_num_splits", "attn_list_schedule", "attn_kv_tiles",
-    "attn_fwd_num_units", "attn_fwd_schedule", "attn_fwd_split_plan", "attn_decode_kernel_launches", "forward", "decode", "library_path", "load",
+    "attn_fwd_num_units", "attn_fwd_schedule", "attn_fwd_split_plan", "attn_decode_kernel_launches",
+    "attn_bwd", "attn_bwd_workspace_size", "backward", "forward", "decode", "library_path", "load",
 ]
 
 ATTN_OK = 0
@@ -55,6 +56,10 @@ SIGNATURES = {
                                    _c_ll, ctypes.POINTER(ctypes.c_int),
                                    ctypes.POINTER(ctypes.c_int)]),
     "attn_decode_kernel_launches": (_c_int, [_c_int] * 6),
+    "attn_bwd_workspace_size": (ctypes.c_size_t, [_c_int] * 6),
+    "attn_bwd": (_c_int, [ctypes.c_void_p] * 9 + [_c_int] * 7 + [ctypes.c_float, _c_int, _c_int,
+                                                                 ctypes.c_void_p, ctypes.c_size_t,
+                                                                 ctypes.c_void_p]),
     "attn_fwd_split_plan": (_c_int, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
                                      _c_int, ctypes.POINTER(ctypes.c_int),
                                      ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int)]),
@@ -151,6 +156,67 @@ def attn_fwd(q, k, v, o, lse=None, *, causal: bool = False, scale: float | None 
                          int(bool(causal)), float(scale), odt, _stream_ptr(stream))
     _check(rc, "attn_fwd")
     return o, lse
+
+
+def attn_bwd_workspace_size(B: int, Hq: int, Hkv: int, Nq: int, Nk: int, d: int) -> int:
+    return int(load().attn_bwd_workspace_size(B, Hq, Hkv, Nq, Nk, d))
+
+
+def attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, *, causal: bool = False,
+             scale: float | None = None, workspace=None, stream=None):
+    """Backward into caller-provided gradients.
+
+    q, dout [B,Hq,Nq,d] bf16; k, v [B,Hkv,Nk,d] bf16; o [B,Hq,Nq,d] bf16 or
+    fp32 (the forward's output); lse [B,Hq,Nq] fp32 (the forward's natural-log
+    logsumexp); dq [B,Hq,Nq,d] and dk, dv [B,Hkv,Nk,d], all bf16 or all fp32;
+    workspace: uint8 of attn_bwd_workspace_size bytes.  Asynchronous."""
+    import torch
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (dout, "dout")):
+        _need(t, torch.bfloat16, n)
+    if o.dtype not in (torch.bfloat16, torch.float32):
+        raise TypeError("o must be bfloat16 or float32")
+    _need(o, o.dtype, "o")
+    _need(lse, torch.float32, "lse")
+    gdt = dq.dtype
+    if gdt not in (torch.bfloat16, torch.float32) or dk.dtype != gdt or dv.dtype != gdt:
+        raise TypeError("dq, dk, dv must all be bfloat16 or all float32")
+    for t, n in ((dq, "dq"), (dk, "dk"), (dv, "dv")):
+        _need(t, gdt, n)
+    B, Hq, Nq, d = q.shape
+    Hkv, Nk = k.shape[1], k.shape[2]
+    if (tuple(k.shape) != (B, Hkv, Nk, d) or tuple(v.shape) != tuple(k.shape)
+            or tuple(dk.shape) != tuple(k.shape) or tuple(dv.shape) != tuple(k.shape)):
+        raise ValueError("k/v/dk/dv shape mismatch")
+    if tuple(o.shape) != tuple(q.shape) or tuple(dout.shape) != tuple(q.shape) \
+            or tuple(dq.shape) != tuple(q.shape):
+        raise ValueError("o/dout/dq shape mismatch")
+    if tuple(lse.shape) != (B, Hq, Nq):
+        raise ValueError("lse shape mismatch")
+    if scale is None:
+        scale = d ** -0.5
+    need = attn_bwd_workspace_size(B, Hq, Hkv, Nq, Nk, d)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    odt = ATTN_OUT_F32 if o.dtype == torch.float32 else ATTN_OUT_BF16
+    g32 = ATTN_OUT_F32 if gdt == torch.float32 else ATTN_OUT_BF16
+    rc = load().attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq),
+                         _ptr(dk), _ptr(dv), B, Hq, Hkv, Nq, Nk, d, int(bool(causal)),
+                         float(scale), odt, g32, _ptr(workspace), workspace.numel(),
+                         _stream_ptr(stream))
+    _check(rc, "attn_bwd")
+    return dq, dk, dv
+
+
+def backward(q, k, v, o, dout, lse, *, causal: bool = False, scale: float | None = None,
+             grad_dtype=None, stream=None):
+    """Allocate dQ, dK, dV (and the workspace) with torch and run attn_bwd."""
+    import torch
+    grad_dtype = grad_dtype or torch.bfloat16
+    dq = torch.empty(q.shape, dtype=grad_dtype, device=q.device)
+    dk = torch.empty(k.shape, dtype=grad_dtype, device=q.device)
+    dv = torch.empty(v.shape, dtype=grad_dtype, device=q.device)
+    return attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, causal=causal, scale=scale,
+                    stream=stream)
 
 
 def forward(q, k, v, *, causal: bool = False, scale: float | None = None,

@@ -177,6 +177,32 @@ attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, flo
                       static_cast<cudaStream_t>(stream), dev);
 }
 
+size_t attn_bwd_workspace_size(int B, int Hq, int Hkv, int Nq, int Nk, int d) {
+    if (check_common(B, Hq, Hkv, d, 1.0f, ATTN_OUT_BF16) != ATTN_OK) return 0;
+    if (Nq < 1 || Nk < 1 || Nq > kMaxLen || Nk > kMaxLen) return 0;
+    if (d != 64 && d != 128) return 0;
+    return bwd_workspace_bytes(B, Hq, Nq, d);
+}
+
+attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o,
+                       const void* dout, const float* lse, void* dq, void* dk, void* dv, int B,
+                       int Hq, int Hkv, int Nq, int Nk, int d, int causal, float scale,
+                       attn_out_dtype_t o_dtype, attn_out_dtype_t grad_dtype, void* workspace,
+                       size_t workspace_bytes, void* stream) {
+    attn_status_t st = check_fwd(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, d, causal, scale, o_dtype);
+    if (st != ATTN_OK) return st;
+    if (!dout || !lse || !dq || !dk || !dv) return ATTN_ERR_INVALID_ARG;
+    if (!aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+        return ATTN_ERR_INVALID_ARG;
+    if (grad_dtype != ATTN_OUT_BF16 && grad_dtype != ATTN_OUT_F32) return ATTN_ERR_INVALID_ARG;
+    const size_t need = bwd_workspace_bytes(B, Hq, Nq, d);
+    if (!workspace || workspace_bytes < need || !aligned16(workspace)) return ATTN_ERR_WORKSPACE;
+    DeviceInfo dev;
+    if ((st = current_device_info(&dev)) != ATTN_OK) return st;
+    return launch_bwd(q, k, v, o, dout, lse, dq, dk, dv, B, Hq, Hkv, Nq, Nk, d, causal, scale,
+                      o_dtype, grad_dtype, workspace, static_cast<cudaStream_t>(stream), dev);
+}
+
 size_t attn_decode_workspace_size(int B, int Hq, int Hkv, int Nmax, int d, int num_splits) {
     if (check_decode_shape(B, Hq, Hkv, Nmax, d, num_splits) != ATTN_OK) return 0;
     int sms = 0;
@@ -239,6 +265,7 @@ attn_status_t attn_last_device_error(void* stream) {
     if (word != 0 && cudaMemcpy(dev.err_word, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess)
         return ATTN_ERR_CUDA;
     if (word & kErrTimeout) return ATTN_ERR_TIMEOUT;
+    if (word & kErrLayout) return ATTN_ERR_CUDA;
     if (word & kErrBadSeqlen) return ATTN_ERR_INVALID_ARG;
     return ATTN_OK;
 }

@@ -332,7 +332,6 @@ __device__ void run_mma(uint8_t* smem, Bars* bars, uint32_t tmem, const FwdParam
     // tile's PV and S MMAs contiguous in the tensor pipe's queue.
     using C = FwdCfg<D>;
     const volatile int* abort_flag = &bars->abort;
-    const FwdShape& s = p.shape;
     const bool leader = elect_one();
     const uint32_t idS = make_idesc_bf16(128, kTileN, 0, 0);
     const uint32_t idO = make_idesc_bf16(128, D, 0, 1);

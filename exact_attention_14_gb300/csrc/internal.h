@@ -31,6 +31,14 @@ attn_status_t launch_fwd(const void* q, const void* k, const void* v, void* o, f
                          int B, int Hq, int Hkv, int Nq, int Nk, int d, int causal, float scale,
                          attn_out_dtype_t o_dtype, cudaStream_t stream, const DeviceInfo& dev);
 
+// Backward: workspace bytes (fp32 dQ accumulator, lse2, D; padded rows).
+size_t bwd_workspace_bytes(int B, int Hq, int Nq, int d);
+attn_status_t launch_bwd(const void* q, const void* k, const void* v, const void* o,
+                         const void* dout, const float* lse, void* dq, void* dk, void* dv, int B,
+                         int Hq, int Hkv, int Nq, int Nk, int d, int causal, float scale,
+                         attn_out_dtype_t o_dtype, attn_out_dtype_t grad_dtype, void* workspace,
+                         cudaStream_t stream, const DeviceInfo& dev);
+
 // Decode: chunk size in keys for a request (multiple of 64).
 int decode_chunk(int Nmax, int B, int Hkv, int num_sms, int num_splits);
 size_t decode_workspace_bytes(int B, int Hq, int Nmax, int d, int chunk);

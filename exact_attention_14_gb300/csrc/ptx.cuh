@@ -30,6 +30,7 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
 enum : uint32_t {
     kErrTimeout = 1u,      // a bounded wait ran out
     kErrBadSeqlen = 2u,    // decode: a sequence length outside [1, Nmax]
+    kErrLayout = 4u,       // a kernel's shared-memory layout did not fit its allocation
 };
 
 // Every spin-wait in the kernels gives up after this many nanoseconds.
@@ -129,6 +130,16 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
         "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+        : "memory");
+}
+
+// Contiguous bulk copy global -> shared, completing on an mbarrier (both
+// addresses 16-byte aligned, bytes a multiple of 16).
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
         : "memory");
 }
 

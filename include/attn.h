@@ -92,6 +92,50 @@ attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, flo
                        float scale, attn_out_dtype_t o_dtype, void* stream);
 
 /*
+ * attn_bwd_workspace_size -- bytes of device workspace attn_bwd needs: an fp32
+ * dQ accumulator and two fp32 row vectors, over query rows padded to whole
+ * 128-row tiles (4 * B*Hq*ceil(Nq/128)*128 * (d + 2) bytes).  Returns 0 for
+ * shapes attn_bwd would reject.
+ */
+size_t attn_bwd_workspace_size(int B, int Hq, int Hkv, int Nq, int Nk, int d);
+
+/*
+ * attn_bwd -- gradients of attn_fwd (lecture notes "Optimizing Attention for
+ * Modern Hardware: FlashAttention 1-4", 2.6: P recomputed from the stored
+ * logsumexp, D = rowsum(dO o O), dS = P o (dP - D)):
+ *
+ *   dQ = scale dS K,   dK = scale dS^T Q,   dV = P^T dO
+ *
+ * with dK and dV summed over each KV head's query-head group (GQA).
+ *
+ *   q, dout  bf16 [B, Hq, Nq, d]       k, v  bf16 [B, Hkv, Nk, d]
+ *   o        the forward's output [B, Hq, Nq, d], element type per o_dtype
+ *   lse      fp32 [B, Hq, Nq], the forward's natural-log logsumexp
+ *   dq       [B, Hq, Nq, d];  dk, dv  [B, Hkv, Nk, d]; element type per
+ *            grad_dtype (bf16 round-to-nearest-even, or fp32)
+ *   causal, scale  as passed to attn_fwd
+ *   workspace  device memory of at least attn_bwd_workspace_size bytes,
+ *            16-byte aligned; contents need no initialisation; not used after
+ *            the call's kernels finish.
+ *
+ * Supported as for attn_fwd (d in {64, 128}, Hq % Hkv == 0, causal needs
+ * Nq <= Nk).  Pointers 16-byte aligned (lse 4-byte).  The caller owns every
+ * buffer.  Three kernels run in order on `stream`: a per-row pass (D, the LSE
+ * in base 2, the accumulator zeroed), the main pass (one CTA per (b, KV head,
+ * 128-key tile): dK and dV accumulated in tensor memory and written once, dQ
+ * added into the accumulator with atomic adds, so dQ's rounding order can vary
+ * between runs), and the dQ scaling pass.  Numerics: scores and all products
+ * accumulate in fp32; P and dS are rounded to bf16 before the P.dO, dS.Q and
+ * dS.K products.  Returns ATTN_OK once the kernels are enqueued;
+ * ATTN_ERR_WORKSPACE for a missing or short workspace.
+ */
+attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o,
+                       const void* dout, const float* lse, void* dq, void* dk, void* dv, int B,
+                       int Hq, int Hkv, int Nq, int Nk, int d, int causal, float scale,
+                       attn_out_dtype_t o_dtype, attn_out_dtype_t grad_dtype, void* workspace,
+                       size_t workspace_bytes, void* stream);
+
+/*
  * attn_decode_workspace_size -- bytes of device workspace attn_decode needs
  * for this shape and split request (num_splits as passed to attn_decode).
  * Returns 0 for arguments attn_decode would reject.

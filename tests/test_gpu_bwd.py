@@ -1,0 +1,133 @@
+"""GPU parity of attn_bwd against the fp64 oracle, through the C ABI.
+
+The kernel's inputs O and LSE come from the oracle (rounded to fp32), so the
+comparison isolates the backward's own arithmetic; one test chains attn_fwd
+into attn_bwd.
+
+Tolerance, from the arithmetic: scores and every product accumulate in fp32,
+while P and dS are rounded to bf16 (relative error <= 2^-9 each) before the
+P.dO, dS.Q and dS.K products.  Those rounding errors are independent across
+the summed terms, so each gradient's relative L2 error is a small multiple of
+2^-9 ~ 2e-3; the bound is relL2 <= 1e-2 per gradient, and max |error| <=
+2e-2 * max |reference| per gradient (fp32 gradients compared; bf16 gradients
+add half a bf16 ulp of each reference value).
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import exact_attention_14_gb300 as ea
+import oracle
+from exact_attention_14_gb300.inputs import make_fwd_inputs
+
+pytestmark = pytest.mark.gpu
+
+REL_L2 = 1e-2
+MAX_REL_TO_PEAK = 2e-2
+
+
+def _dout(shape, seed):
+    g = torch.Generator().manual_seed(seed)
+    return torch.randn(shape, generator=g, dtype=torch.float32).to(torch.bfloat16)
+
+
+def _errors(got, ref):
+    rel = np.linalg.norm(got - ref) / max(np.linalg.norm(ref), 1e-30)
+    peak = np.abs(got - ref).max() / max(np.abs(ref).max(), 1e-30)
+    return rel, peak
+
+
+def _check(got, ref, what, bf16=False):
+    assert np.isfinite(got).all(), f"{what}: non-finite"
+    rel, peak = _errors(got, ref)
+    if bf16:
+        r = torch.from_numpy(ref).to(torch.bfloat16).double().numpy()
+        half_ulp = np.exp2(np.floor(np.log2(np.maximum(np.abs(r), 1e-30))) - 8)
+        err = np.abs(got - r)
+        assert (err <= MAX_REL_TO_PEAK * np.abs(ref).max() + half_ulp).all(), f"{what}: bf16 bound"
+    else:
+        assert peak <= MAX_REL_TO_PEAK, f"{what}: max|err|/max|ref| = {peak:.3e}"
+    assert rel <= REL_L2, f"{what}: relL2 = {rel:.3e}"
+
+
+def _run(q, k, v, do, causal, scale, grad_dtype=torch.float32, o=None, lse=None):
+    if o is None:
+        o_ref, lse_ref = oracle.attention(q, k, v, causal=causal, scale=scale)
+        o = torch.from_numpy(o_ref).float()
+        lse = torch.from_numpy(lse_ref).float()
+    dq, dk, dv = ea.backward(q.cuda(), k.cuda(), v.cuda(), o.cuda(), do.cuda(), lse.cuda(),
+                             causal=causal, scale=scale, grad_dtype=grad_dtype)
+    torch.cuda.synchronize()
+    assert ea.attn_last_device_error() == 0
+    return tuple(t.float().cpu().double().numpy() for t in (dq, dk, dv))
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,Nq,Nk,d,causal", [
+    (1, 1, 1, 128, 128, 64, False),
+    (1, 2, 2, 256, 256, 128, False),
+    (1, 2, 2, 384, 384, 128, True),
+    (2, 4, 2, 300, 300, 64, True),       # GQA, ragged tails
+    (1, 4, 1, 200, 200, 128, False),     # MQA
+    (1, 2, 2, 100, 333, 128, True),      # bottom-right causal, Nq < Nk
+    (1, 2, 2, 700, 90, 64, False),       # Nq > Nk
+    (2, 8, 2, 1000, 1000, 128, True),
+])
+def test_bwd_parity(B, Hq, Hkv, Nq, Nk, d, causal):
+    q, k, v = make_fwd_inputs(B, Hq, Hkv, Nq, Nk, d, seed=300 + Nq + Nk + d)
+    do = _dout(q.shape, seed=Nq + 1)
+    scale = 1 / math.sqrt(d)
+    dq, dk, dv = _run(q, k, v, do, causal, scale)
+    rq, rk, rv = oracle.attention_bwd(q, k, v, do, causal=causal, scale=scale)
+    what = f"{(B, Hq, Hkv, Nq, Nk, d, causal)}"
+    _check(dq, rq, "dQ " + what)
+    _check(dk, rk, "dK " + what)
+    _check(dv, rv, "dV " + what)
+
+
+def test_bwd_bf16_gradients():
+    q, k, v = make_fwd_inputs(1, 4, 2, 333, 333, 128, seed=77)
+    do = _dout(q.shape, seed=78)
+    dq, dk, dv = _run(q, k, v, do, True, 1 / math.sqrt(128), grad_dtype=torch.bfloat16)
+    rq, rk, rv = oracle.attention_bwd(q, k, v, do, causal=True)
+    for got, ref, n in ((dq, rq, "dQ"), (dk, rk, "dK"), (dv, rv, "dV")):
+        _check(got, ref, n, bf16=True)
+
+
+def test_bwd_prefill_heads_sampled():
+    """The prefill workload's shape (B4 H16 N2048 d128) at full size; the oracle
+    checks two whole heads (MHA heads are independent)."""
+    B, H, N, d = 4, 16, 2048, 128
+    q, k, v = make_fwd_inputs(B, H, H, N, N, d, seed=1)
+    do = _dout(q.shape, seed=2)
+    for causal in (False, True):
+        dq, dk, dv = _run(q, k, v, do, causal, 1 / math.sqrt(d))
+        for (b, h) in ((0, 0), (3, 15)):
+            sl = (slice(b, b + 1), slice(h, h + 1))
+            rq, rk, rv = oracle.attention_bwd(q[sl], k[sl], v[sl], do[sl], causal=causal)
+            _check(dq[sl], rq, f"dQ head {(b, h)} causal={causal}")
+            _check(dk[sl], rk, f"dK head {(b, h)} causal={causal}")
+            _check(dv[sl], rv, f"dV head {(b, h)} causal={causal}")
+
+
+def test_fwd_then_bwd_end_to_end():
+    """attn_fwd's own O (bf16) and LSE feed attn_bwd."""
+    q, k, v = make_fwd_inputs(2, 4, 4, 512, 512, 128, seed=91)
+    do = _dout(q.shape, seed=92)
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    o, lse = ea.forward(qd, kd, vd, causal=True, out_dtype=torch.bfloat16)
+    dq, dk, dv = _run(q, k, v, do, True, 1 / math.sqrt(128), o=o.cpu(), lse=lse.cpu())
+    rq, rk, rv = oracle.attention_bwd(q, k, v, do, causal=True)
+    _check(dq, rq, "dQ")
+    _check(dk, rk, "dK")
+    _check(dv, rv, "dV")
+
+
+def test_bwd_dk_dv_repeatable():
+    """dK and dV are accumulated on chip in a fixed order: bit-identical runs."""
+    q, k, v = make_fwd_inputs(1, 4, 2, 640, 640, 128, seed=93)
+    do = _dout(q.shape, seed=94)
+    a = _run(q, k, v, do, True, 1 / math.sqrt(128))
+    b = _run(q, k, v, do, True, 1 / math.sqrt(128))
+    assert np.array_equal(a[1], b[1]) and np.array_equal(a[2], b[2])

@@ -252,3 +252,17 @@ def test_concurrent_launches_on_two_streams(causal):
     for i in range(2):
         for o, lse in outs[i]:
             assert torch.equal(o, refs[i][0]) and torch.equal(lse, refs[i][1])
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_row_max_jumps_late(causal):
+    """Keys late in each row score far higher than the early ones, so the row
+    max rises by more than tau after the first KV tiles and the softmax must
+    rescale O and redo the tile's exponentials (the rare path)."""
+    q, k, v = make_fwd_inputs(2, 4, 4, 1000, 1000, 128, seed=41)
+    k = k.clone()
+    k[:, :, 600:, :] *= 8.0   # a power of two: exact in bf16
+    k[:, :, 900:, :] *= 4.0
+    o, lse = gpu_fwd(q, k, v, causal, 1 / math.sqrt(128))
+    o_ref, lse_ref = oracle.attention(q, k, v, causal=causal)
+    assert_close(o, lse, o_ref, lse_ref, f"late max, causal={causal}")

@@ -247,3 +247,25 @@ def test_tau_bound_from_the_notes():
     g = GOLDEN["tau_bound"]
     bound = 128 - math.log2(g["N"])
     assert bound == g["tau_max_exclusive"] and g["tau_used"] < bound
+
+
+def test_bwd_workspace_size_and_argument_checks(lib):
+    # fp32 dQ accumulator + two row vectors over rows padded to 128
+    assert ea.attn_bwd_workspace_size(2, 8, 2, 300, 300, 128) == 4 * 2 * 8 * 384 * (128 + 2)
+    assert ea.attn_bwd_workspace_size(1, 4, 3, 128, 128, 64) == 0      # Hq % Hkv
+    assert ea.attn_bwd_workspace_size(1, 4, 4, 128, 128, 96) == 0      # unsupported d
+    fake = ctypes.c_void_p(0x10000)
+    args = [fake] * 9 + [1, 2, 2, 128, 128, 128, 0, ctypes.c_float(0.1), 0, 0, fake, 1 << 30, None]
+    bad = list(args)
+    bad[4] = None                                                      # no dout
+    assert lib.attn_bwd(*bad) == ea.ATTN_ERR_INVALID_ARG
+    bad = list(args)
+    bad[20] = 16                                                       # workspace too small
+    assert lib.attn_bwd(*bad) == ea.ATTN_ERR_WORKSPACE
+    bad = list(args)
+    bad[14] = 96                                                       # d
+    assert lib.attn_bwd(*bad) == ea.ATTN_ERR_UNSUPPORTED
+    bad = list(args)
+    bad[15] = 1
+    bad[12], bad[13] = 256, 128                                        # causal with Nq > Nk
+    assert lib.attn_bwd(*bad) == ea.ATTN_ERR_INVALID_ARG
