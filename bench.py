@@ -292,6 +292,46 @@ def run_ours(args, rank, world, local_rank):
         e2e = {"value": world * (f_nc + f_c) / t_e2e / 1e12, "unit": "TFLOPS",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
+    # Backward (a follow-on row, timed apart from the step): attn_bwd on the
+    # prefill inputs, non-causal then causal, O and LSE from attn_fwd.
+    bwd = None
+    if not args.no_bwd:
+        g = torch.Generator().manual_seed(5)
+        dout = torch.randn(q.shape, generator=g, dtype=torch.float32).to(torch.bfloat16).to(dev)
+        ob = {c: ea.forward(q, k, v, causal=c, out_dtype=torch.bfloat16, stream=stream)
+              for c in (False, True)}
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        bws = torch.empty(ea.attn_bwd_workspace_size(cfg.B, cfg.Hq, cfg.Hkv, cfg.N, cfg.N, cfg.d),
+                          dtype=torch.uint8, device=dev)
+
+        def bwd_step(ev=None):
+            for idx, c in enumerate((False, True)):
+                if ev: ev[idx].record(stream)
+                ea.attn_bwd(q, k, v, ob[c][0], dout, ob[c][1], dq, dk, dv, causal=c,
+                            workspace=bws, stream=stream)
+            if ev: ev[2].record(stream)
+
+        for _ in range(args.warmup):
+            flush.zero_()
+            bwd_step()
+        bev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+        torch.cuda.synchronize()
+        for i in range(args.steps):
+            flush.zero_()
+            bwd_step(bev[i])
+        torch.cuda.synchronize()
+        if ea.attn_last_device_error() != 0:
+            raise RuntimeError("device error in the backward leg")
+        tb_nc = sum(e[0].elapsed_time(e[1]) for e in bev) / args.steps * 1e-3
+        tb_c = sum(e[1].elapsed_time(e[2]) for e in bev) / args.steps * 1e-3
+        fb_nc, fb_c = 2.5 * f_nc, 2.5 * f_c  # five GEMMs per tile against the forward's two
+        bwd = {"kernels": "attn_bwd (prep + main + dQ scaling)",
+               "noncausal_tflops": fb_nc / tb_nc / 1e12, "causal_tflops": fb_c / tb_c / 1e12,
+               "noncausal_ms": 1e3 * tb_nc, "causal_ms": 1e3 * tb_c,
+               "tflops": (fb_nc + fb_c) / (tb_nc + tb_c) / 1e12,
+               "frac_of_bf16_peak": (fb_nc + fb_c) / (tb_nc + tb_c) / 1e12 / peaks["bf16_tflops"],
+               "flops_note": "2.5 x the forward formula (S, dP, dV, dK, dQ products)"}
+
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         tf, desc, cores, _ = oracle_sample(args.cpu_seconds)
@@ -332,7 +372,7 @@ def run_ours(args, rank, world, local_rank):
         "decode": {"value": dec_gbs, "unit": "GB/s", "ms": 1e3 * t_dec,
                    "algorithmic_bytes": dec_bytes, "frac_of_hbm": dec_gbs / world / peaks["hbm_gbs"],
                    "sum_seqlen": sum_len},
-        "roofline": roof, "roofline_decode": roof_dec,
+        "roofline": roof, "roofline_decode": roof_dec, "bwd": bwd,
         "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": (2 + ea.attn_decode_kernel_launches(DECODE.B, DECODE.Hq, DECODE.Hkv,
                                                             DECODE.Nmax, DECODE.d)) * args.steps,
@@ -349,6 +389,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-bwd", action="store_true", help="skip the backward leg")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))

@@ -96,6 +96,19 @@ attn_status_t encode_tmap_out_3d(CUtensorMap* map, void* base, bool f32, int d, 
     return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
+attn_status_t encode_tmap_f32_sw128_3d(CUtensorMap* map, void* base, int d, int rows,
+                                       long long heads, int box_rows) {
+    if (!load_encoder()) return ATTN_ERR_CUDA;
+    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)rows, (cuuint64_t)heads};
+    cuuint64_t strides[2] = {(cuuint64_t)d * 4, (cuuint64_t)d * 4 * (cuuint64_t)rows};
+    cuuint32_t box[3] = {32u, (cuuint32_t)box_rows, 1u};
+    cuuint32_t elem[3] = {1u, 1u, 1u};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, elem,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
 attn_status_t encode_tmap_bf16_3d(CUtensorMap* map, const void* base, int d, int rows,
                                   long long heads, int box_rows) {
     if (!load_encoder()) return ATTN_ERR_CUDA;

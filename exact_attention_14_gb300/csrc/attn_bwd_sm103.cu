@@ -20,8 +20,8 @@
 //                 as bf16 pairs, dS^T also to shared memory as dQ's A operand)
 //          dV  += P^T dO,  dK += dS^T Q      (A from TMEM, B MN-major in smem)
 //          dQ   = dS K                       (A = dS MN-major, B = K MN-major)
-//                 (warps 8-11 read dQ from TMEM and add it into the fp32
-//                 accumulator with 16-byte atomic adds)
+//                 (warps 8-11 load dQ from TMEM into registers, release it,
+//                 and add it into the fp32 accumulator with 16-byte atomics)
 //        After the last tile dK (times scale) and dV are written once.
 //  post  dQ = scale * accumulator, as bf16 or fp32.
 //
@@ -66,6 +66,7 @@ struct BwdCfg {
 
 struct BwdParams {
     int B, Hq, Hkv, Nq, Nk, Nq_pad, group, off, n_kt, causal;
+    int sec_groups;     // (b, KV head) groups per L2 section
     float c;      // scale * log2(e)
     float scale;
     const float* lse2;  // [B*Hq, Nq_pad]
@@ -86,15 +87,28 @@ static_assert(sizeof(BwdBars) <= 256, "barrier block");
 
 // The CTA's work: K/V tile kt of (b, g) and the Q tiles [qt_first, n_qt) of
 // each query head of the group, head-major.
+//
+// Order of the CTAs: the (b, KV head) groups are cut into L2 sections whose
+// dQ accumulator, Q, dO, K and V fit an L2 budget (so the dQ atomic adds of
+// all the section's key tiles meet in L2 instead of DRAM, and each Q / dO
+// tile is read from DRAM once for all of them); sections run in order, and
+// inside a section key tiles are outer (causal tile 0, which sees the most
+// query tiles, first).
 struct BwdWork {
     int b, g, kt, k0, qt_first, n_qt_cta, n_tiles;
 };
 
 __device__ __forceinline__ BwdWork bwd_work(const BwdParams& p) {
     BwdWork w;
-    const int bg_count = p.B * p.Hkv;
-    w.kt = (int)(blockIdx.x / (unsigned)bg_count);  // key tiles outer: causal tile 0 has the most work
-    const int bg = (int)(blockIdx.x - (unsigned)w.kt * (unsigned)bg_count);
+    const unsigned all = (unsigned)(p.B * p.Hkv);
+    const unsigned S = (unsigned)p.sec_groups;
+    const unsigned per_sec = S * (unsigned)p.n_kt;
+    const unsigned sec = blockIdx.x / per_sec;
+    const unsigned r = blockIdx.x - sec * per_sec;
+    const unsigned rest = all - sec * S;
+    const unsigned gs = rest < S ? rest : S;  // groups in this (possibly partial) section
+    w.kt = (int)(r / gs);
+    const int bg = (int)(sec * S + (r - (unsigned)w.kt * gs));
     w.b = bg / p.Hkv;
     w.g = bg - w.b * p.Hkv;
     w.k0 = w.kt * kBT;
@@ -270,22 +284,34 @@ __device__ void bwd_mma(uint8_t* smem, BwdBars* bars, uint32_t tmem, const BwdWo
 // ---------------------------------------------------------------------------
 template <bool MASKED>
 __device__ __forceinline__ void p_ds_chunk(const uint32_t (&s)[32], const uint32_t (&dp)[32],
-                                           const float* lse2s, const float* ds_vec, int qc, float c,
+                                           uint32_t lse2s, uint32_t ds_vec, int qc, float c,
                                            int lim, uint32_t (&pp)[16], uint32_t (&dd)[16]) {
-    // lim: query column qc + x is allowed iff qc + x >= lim (causal), else all
+    // lim: query column qc + x is allowed iff qc + x >= lim (causal), else all.
+    // The tile's lse2 and D come from shared memory 4 at a time (broadcast).
+    const uint64_t c2 = f2(c, c);
 #pragma unroll
-    for (int x = 0; x < 16; ++x) {
-        const int q = qc + 2 * x;
-        float p0 = ex2(fmaf(__uint_as_float(s[2 * x]), c, -lse2s[q]));
-        float p1 = ex2(fmaf(__uint_as_float(s[2 * x + 1]), c, -lse2s[q + 1]));
-        if constexpr (MASKED) {
-            p0 = q >= lim ? p0 : 0.f;
-            p1 = q + 1 >= lim ? p1 : 0.f;
+    for (int x4 = 0; x4 < 8; ++x4) {
+        const float4 l4 = lds128_f32(lse2s + 4u * (qc + 4 * x4));
+        const float4 d4 = lds128_f32(ds_vec + 4u * (qc + 4 * x4));
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int x = 2 * x4 + h;
+            const int q = qc + 2 * x;
+            const uint64_t nl = h == 0 ? f2(-l4.x, -l4.y) : f2(-l4.z, -l4.w);
+            const uint64_t nd = h == 0 ? f2(-d4.x, -d4.y) : f2(-d4.z, -d4.w);
+            float a0, a1;
+            f2_split(f2_fma(f2(__uint_as_float(s[2 * x]), __uint_as_float(s[2 * x + 1])), c2, nl), a0, a1);
+            float p0 = ex2(a0), p1 = ex2(a1);
+            if constexpr (MASKED) {
+                p0 = q >= lim ? p0 : 0.f;
+                p1 = q + 1 >= lim ? p1 : 0.f;
+            }
+            float d0, d1;
+            f2_split(f2_mul(f2(p0, p1), f2_add(f2(__uint_as_float(dp[2 * x]), __uint_as_float(dp[2 * x + 1])), nd)),
+                     d0, d1);
+            pp[x] = pack_bf16x2(p0, p1);
+            dd[x] = pack_bf16x2(d0, d1);
         }
-        const float d0 = p0 * (__uint_as_float(dp[2 * x]) - ds_vec[q]);
-        const float d1 = p1 * (__uint_as_float(dp[2 * x + 1]) - ds_vec[q + 1]);
-        pp[x] = pack_bf16x2(p0, p1);
-        dd[x] = pack_bf16x2(d0, d1);
     }
 }
 
@@ -315,7 +341,7 @@ __device__ void bwd_pds(int wq, int lane, uint8_t* smem, BwdBars* bars, uint32_t
     const uint32_t tS = tmem + lane_off, tdP = tmem + 128 + lane_off;
     const int j = wq * 32 + lane;  // key row of the tile
     const int jg = w.k0 + j;
-    uint8_t* ds_row = smem + C::kDS + j * 128;
+    const uint32_t ds_row = smem_u32(smem + C::kDS) + j * 128;
     bool ok = true;
     for (int i = 0; i < w.n_tiles && ok; ++i) {
         const int st = i & 1;
@@ -323,8 +349,8 @@ __device__ void bwd_pds(int wq, int lane, uint8_t* smem, BwdBars* bars, uint32_t
         if (!ok) break;
         tc_fence_after();
         const int q0 = (w.qt_first + i % w.n_qt_cta) * kBT;
-        const float* lse2s = reinterpret_cast<const float*>(smem + C::kLD + st * 1024);
-        const float* ds_vec = lse2s + kBT;
+        const uint32_t lse2s = smem_u32(smem + C::kLD + st * 1024);
+        const uint32_t ds_vec = lse2s + kBT * 4;
         // causal: query q0 + x sees key jg iff x >= jg - off - q0
         const int lim = jg - p.off - q0;
         const bool masked = p.causal && (q0 + p.off < w.k0 + kBT - 1);
@@ -347,8 +373,7 @@ __device__ void bwd_pds(int wq, int lane, uint8_t* smem, BwdBars* bars, uint32_t
             for (int gq = 0; gq < 4; ++gq) {
                 const int G = cc * 4 + gq;
                 const int off = (G >> 3) * 16384 + ((((G & 7) ^ (j & 7))) << 4);
-                *reinterpret_cast<uint4*>(ds_row + off) =
-                    make_uint4(dd[4 * gq], dd[4 * gq + 1], dd[4 * gq + 2], dd[4 * gq + 3]);
+                sts128(ds_row + off, dd[4 * gq], dd[4 * gq + 1], dd[4 * gq + 2], dd[4 * gq + 3]);
             }
         }
         tmem_wait_st();
@@ -403,7 +428,10 @@ __device__ void bwd_pds(int wq, int lane, uint8_t* smem, BwdBars* bars, uint32_t
 }
 
 // ---------------------------------------------------------------------------
-// dQ read-out (one query row per thread): TMEM -> fp32 accumulator
+// dQ read-out (one query row per thread): TMEM -> fp32 accumulator.  The
+// whole row is loaded into registers first and TMEM released at once (the next
+// tile's S^T waits for that), then added into the accumulator with 16-byte
+// atomic adds, which the warp does not wait for.
 // ---------------------------------------------------------------------------
 template <int D>
 __device__ void bwd_dq(int wq, int lane, BwdBars* bars, uint32_t tmem, const BwdParams& p,
@@ -416,26 +444,23 @@ __device__ void bwd_dq(int wq, int lane, BwdBars* bars, uint32_t tmem, const Bwd
         ok = mbar_wait(smem_u32(&bars->dq_full), i & 1, abort_flag, 32);
         if (!ok) break;
         tc_fence_after();
-        const int hq = w.g * p.group + i / w.n_qt_cta;
-        const int row = (w.qt_first + i % w.n_qt_cta) * kBT + r;
-        float4* dst = reinterpret_cast<float4*>(
-            p.dq_acc + (((size_t)w.b * p.Hq + hq) * p.Nq_pad + (size_t)row) * D);
-#pragma unroll 1
-        for (int cc = 0; cc < D; cc += 32) {
-            uint32_t v[32];
-            tmem_ld32(tmem + cc + lane_off, v);
-            tmem_wait_ld();
-            if (row < p.Nq) {
+        uint32_t v[D];
 #pragma unroll
-                for (int x = 0; x < 8; ++x)
-                    atomicAdd(dst + cc / 4 + x,
-                              make_float4(__uint_as_float(v[4 * x]), __uint_as_float(v[4 * x + 1]),
-                                          __uint_as_float(v[4 * x + 2]), __uint_as_float(v[4 * x + 3])));
-            }
-        }
+        for (int cc = 0; cc < D; cc += 32) tmem_ld32(tmem + cc + lane_off, *reinterpret_cast<uint32_t(*)[32]>(&v[cc]));
+        tmem_wait_ld();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&bars->dq_empty));
+        const int hq = w.g * p.group + i / w.n_qt_cta;
+        const int row = (w.qt_first + i % w.n_qt_cta) * kBT + r;
+        if (row < p.Nq) {
+            float4* dst = reinterpret_cast<float4*>(
+                p.dq_acc + (((size_t)w.b * p.Hq + hq) * p.Nq_pad + (size_t)row) * D);
+#pragma unroll
+            for (int x = 0; x < D / 4; ++x)
+                atomicAdd(dst + x, make_float4(__uint_as_float(v[4 * x]), __uint_as_float(v[4 * x + 1]),
+                                               __uint_as_float(v[4 * x + 2]), __uint_as_float(v[4 * x + 3])));
+        }
     }
     if (!ok) bwd_abort(bars, err);
 }
@@ -444,7 +469,7 @@ template <int D, bool OUT_F32>
 __global__ void __launch_bounds__(kBwdThreads, 1)
 attn_bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                 const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
-                const BwdParams p, unsigned int* err) {
+                const __grid_constant__ CUtensorMap tdq, const BwdParams p, unsigned int* err) {
     using C = BwdCfg<D>;
     extern __shared__ uint8_t smem_raw[];
     const uintptr_t raw = reinterpret_cast<uintptr_t>(smem_raw);
@@ -477,6 +502,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
         tma_prefetch_desc(&tk);
         tma_prefetch_desc(&tv);
         tma_prefetch_desc(&tdo);
+        tma_prefetch_desc(&tdq);
     }
     if (warp == 1) {
         tmem_alloc(smem_u32(&bars->tmem_base), 512);
@@ -560,7 +586,8 @@ attn_bwd_post_kernel(const float* __restrict__ dq_acc, void* __restrict__ dq, lo
 
 template <int D, bool OUT_F32>
 attn_status_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                           const CUtensorMap& tdo, const BwdParams& p, const void* o, int o_f32,
+                           const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdParams& p,
+                           const void* o, int o_f32,
                            const void* dout, const float* lse, float* lse2, float* dvec,
                            void* dq, cudaStream_t stream, const DeviceInfo& dev) {
     using C = BwdCfg<D>;
@@ -578,7 +605,7 @@ attn_status_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const C
     if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
     const long long ctas = (long long)p.B * p.Hkv * p.n_kt;
     attn_bwd_kernel<D, OUT_F32><<<(unsigned)ctas, kBwdThreads, C::kSmemBytes, stream>>>(
-        tq, tk, tv, tdo, p, dev.err_word);
+        tq, tk, tv, tdo, tdq, p, dev.err_word);
     if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
     const long long n4 = (long long)p.B * p.Hq * p.Nq * D / 4;
     attn_bwd_post_kernel<OUT_F32><<<(unsigned)((n4 + 255) / 256), 256, 0, stream>>>(
@@ -610,6 +637,16 @@ attn_status_t launch_bwd(const void* q, const void* k, const void* v, const void
     p.off = Nk - Nq;
     p.n_kt = (Nk + kBT - 1) / kBT;
     p.causal = causal;
+    {
+        // L2 budget per section: a group's fp32 dQ accumulator rows, Q and dO
+        // (bf16) of its query heads, and its K and V
+        const long long per_group = (long long)p.group * p.Nq_pad * d * 4 +
+                                    2ll * p.group * Nq * d * 2 + 2ll * Nk * d * 2;
+        long long sgroups = (64ll << 20) / (per_group > 0 ? per_group : 1);
+        if (sgroups < 1) sgroups = 1;
+        if (sgroups > (long long)B * Hkv) sgroups = (long long)B * Hkv;
+        p.sec_groups = (int)sgroups;
+    }
     p.c = scale * kBwdLog2e;
     p.scale = scale;
     const size_t rows = (size_t)B * Hq * p.Nq_pad;
@@ -621,20 +658,22 @@ attn_status_t launch_bwd(const void* q, const void* k, const void* v, const void
     p.dk = dk;
     p.dv = dv;
     if ((long long)B * Hkv * p.n_kt >= (1ll << 31)) return ATTN_ERR_UNSUPPORTED;
-    CUtensorMap tq, tk, tv, tdo;
+    CUtensorMap tq, tk, tv, tdo, tdq;
     attn_status_t st;
     if ((st = encode_tmap_bf16_3d(&tq, q, d, Nq, (long long)B * Hq, kBT)) != ATTN_OK) return st;
     if ((st = encode_tmap_bf16_3d(&tk, k, d, Nk, (long long)B * Hkv, kBT)) != ATTN_OK) return st;
     if ((st = encode_tmap_bf16_3d(&tv, v, d, Nk, (long long)B * Hkv, kBT)) != ATTN_OK) return st;
     if ((st = encode_tmap_bf16_3d(&tdo, dout, d, Nq, (long long)B * Hq, kBT)) != ATTN_OK) return st;
+    if ((st = encode_tmap_f32_sw128_3d(&tdq, p.dq_acc, d, p.Nq_pad, (long long)B * Hq, 32)) != ATTN_OK)
+        return st;
     const int o_f32 = o_dtype == ATTN_OUT_F32;
     const bool g32 = grad_dtype == ATTN_OUT_F32;
     if (d == 128)
-        return g32 ? launch_bwd_t<128, true>(tq, tk, tv, tdo, p, o, o_f32, dout, lse, lse2, dvec, dq, stream, dev)
-                   : launch_bwd_t<128, false>(tq, tk, tv, tdo, p, o, o_f32, dout, lse, lse2, dvec, dq, stream, dev);
+        return g32 ? launch_bwd_t<128, true>(tq, tk, tv, tdo, tdq, p, o, o_f32, dout, lse, lse2, dvec, dq, stream, dev)
+                   : launch_bwd_t<128, false>(tq, tk, tv, tdo, tdq, p, o, o_f32, dout, lse, lse2, dvec, dq, stream, dev);
     if (d == 64)
-        return g32 ? launch_bwd_t<64, true>(tq, tk, tv, tdo, p, o, o_f32, dout, lse, lse2, dvec, dq, stream, dev)
-                   : launch_bwd_t<64, false>(tq, tk, tv, tdo, p, o, o_f32, dout, lse, lse2, dvec, dq, stream, dev);
+        return g32 ? launch_bwd_t<64, true>(tq, tk, tv, tdo, tdq, p, o, o_f32, dout, lse, lse2, dvec, dq, stream, dev)
+                   : launch_bwd_t<64, false>(tq, tk, tv, tdo, tdq, p, o, o_f32, dout, lse, lse2, dvec, dq, stream, dev);
     return ATTN_ERR_UNSUPPORTED;
 }
 

@@ -526,17 +526,17 @@ __device__ __forceinline__ void store_o_cols(const float (&v)[32], int cc, uint8
         uint8_t* buf = stg + (epi_buf & 1) * 2048;
         if (lane == 0) bulk_wait_group_read<1>();  // this buffer's previous store has read it
         __syncwarp();
-        uint4* dst = reinterpret_cast<uint4*>(buf + lane * 64);
+        const uint32_t dst = smem_u32(buf) + lane * 64;
         if constexpr (OUT_F32) {
 #pragma unroll
             for (int i = 0; i < 4; ++i)
-                dst[i] = make_uint4(__float_as_uint(v[h * 16 + 4 * i]), __float_as_uint(v[h * 16 + 4 * i + 1]),
-                                    __float_as_uint(v[h * 16 + 4 * i + 2]), __float_as_uint(v[h * 16 + 4 * i + 3]));
+                sts128(dst + 16 * i, __float_as_uint(v[h * 16 + 4 * i]), __float_as_uint(v[h * 16 + 4 * i + 1]),
+                       __float_as_uint(v[h * 16 + 4 * i + 2]), __float_as_uint(v[h * 16 + 4 * i + 3]));
         } else {
 #pragma unroll
             for (int i = 0; i < 4; ++i)
-                dst[i] = make_uint4(pack_bf16x2(v[8 * i], v[8 * i + 1]), pack_bf16x2(v[8 * i + 2], v[8 * i + 3]),
-                                    pack_bf16x2(v[8 * i + 4], v[8 * i + 5]), pack_bf16x2(v[8 * i + 6], v[8 * i + 7]));
+                sts128(dst + 16 * i, pack_bf16x2(v[8 * i], v[8 * i + 1]), pack_bf16x2(v[8 * i + 2], v[8 * i + 3]),
+                       pack_bf16x2(v[8 * i + 4], v[8 * i + 5]), pack_bf16x2(v[8 * i + 6], v[8 * i + 7]));
         }
         fence_proxy_async_smem();
         __syncwarp();

@@ -27,6 +27,11 @@ attn_status_t encode_tmap_bf16_3d(CUtensorMap* map, const void* base, int d, int
 attn_status_t encode_tmap_out_3d(CUtensorMap* map, void* base, bool f32, int d, int rows,
                                  long long heads, int box_cols, int box_rows);
 
+// 3-D fp32 tensor map over [heads, rows, d] with a 128-byte-swizzled box of
+// 32 columns x box_rows x 1 (TMA reduce-add of staged fp32 tiles).
+attn_status_t encode_tmap_f32_sw128_3d(CUtensorMap* map, void* base, int d, int rows,
+                                       long long heads, int box_rows);
+
 attn_status_t launch_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
                          int B, int Hq, int Hkv, int Nq, int Nk, int d, int causal, float scale,
                          attn_out_dtype_t o_dtype, cudaStream_t stream, const DeviceInfo& dev);

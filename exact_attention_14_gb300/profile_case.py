@@ -3,6 +3,7 @@ profiler captures (ncu) of a single launch configuration.
 
     python -m exact_attention_14_gb300.profile_case --kernel fwd --workload prefill2x
     python -m exact_attention_14_gb300.profile_case --kernel decode --workload decode
+    python -m exact_attention_14_gb300.profile_case --kernel bwd --workload prefill --causal 0
 
 Workloads: prefill (B=4 H=16 N=2048 d=128), prefill2x (B=8: inputs larger
 than L2), long (B=1 H=32 N=16384), gqa (B=8 Hq=32 Hkv=8 N=4096), decode
@@ -30,13 +31,23 @@ FWD = {
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("--kernel", choices=["fwd", "decode"], required=True)
+    ap.add_argument("--kernel", choices=["fwd", "decode", "bwd"], required=True)
     ap.add_argument("--workload", default="prefill")
     ap.add_argument("--causal", type=int, default=-1, help="-1: the workload's first mode")
     ap.add_argument("--iters", type=int, default=3)
     args = ap.parse_args()
     dev = torch.device("cuda", 0)
-    if args.kernel == "fwd":
+    if args.kernel == "bwd":
+        cfg = FWD[args.workload]
+        causal = cfg.causal[0] if args.causal < 0 else bool(args.causal)
+        q, k, v = (t.to(dev) for t in make_fwd_inputs(cfg.B, cfg.Hq, cfg.Hkv, cfg.N, cfg.N, cfg.d,
+                                                     cfg.seed, cfg.outlier_channels))
+        g = torch.Generator().manual_seed(cfg.seed + 100)
+        dout = torch.randn(q.shape, generator=g, dtype=torch.float32).to(torch.bfloat16).to(dev)
+        o, lse = ea.forward(q, k, v, causal=causal)
+        for _ in range(args.iters):
+            ea.backward(q, k, v, o, dout, lse, causal=causal)
+    elif args.kernel == "fwd":
         cfg = FWD[args.workload]
         causal = cfg.causal[0] if args.causal < 0 else bool(args.causal)
         q, k, v = (t.to(dev) for t in make_fwd_inputs(cfg.B, cfg.Hq, cfg.Hkv, cfg.N, cfg.N, cfg.d,
