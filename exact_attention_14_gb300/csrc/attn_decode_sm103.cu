@@ -223,7 +223,8 @@ attn_decode_split_kernel(const __grid_constant__ CUtensorMap tk, const __grid_co
 
     for (int st = 0; st < n_stages; ++st) {
         const int slot = st % kDecStages;
-        ok = mbar_wait(smem_u32(&full[slot]), (st / kDecStages) & 1, abort_flag);
+        // warp-uniform: ldmatrix and mma.sync below need every lane
+        ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&full[slot]), (st / kDecStages) & 1, abort_flag));
         if (!ok) break;
         const int nvalid = min(kStageKeys, t1 - (t0 + st * kStageKeys));
         const uint32_t sK = smem_u32(smem + slot * C::kStageBytes);

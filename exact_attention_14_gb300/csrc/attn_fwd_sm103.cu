@@ -694,7 +694,7 @@ __device__ void run_softmax(int t, int wq, int lane, uint8_t* smem, Bars* bars, 
         float l = 0.f;        // normaliser of O (see softmax_tile)
         float lx = 0.f;       // running sum of the unrounded probabilities (gives the LSE)
         for (int j = j0; j < n_t; ++j) {
-            ok = mbar_wait(bar_s, cnt_s & 1, abort_flag, 32);
+            ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_s, cnt_s & 1, abort_flag, 32));
             ++cnt_s;
             if (!ok) break;
             tc_fence_after();
@@ -716,7 +716,7 @@ __device__ void run_softmax(int t, int wq, int lane, uint8_t* smem, Bars* bars, 
         }
         if (!ok) break;
         // Epilogue: O = O_acc / l, LSE = ln2 * (m + log2 lx)
-        ok = mbar_wait(bar_o, cnt_o & 1, abort_flag);
+        ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_o, cnt_o & 1, abort_flag));
         ++cnt_o;
         if (!ok) break;
         tc_fence_after();

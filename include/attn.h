@@ -92,9 +92,9 @@ attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, flo
                        float scale, attn_out_dtype_t o_dtype, void* stream);
 
 /*
- * attn_bwd_workspace_size -- bytes of device workspace attn_bwd needs: an fp32
- * dQ accumulator and two fp32 row vectors, over query rows padded to whole
- * 128-row tiles (4 * B*Hq*ceil(Nq/128)*128 * (d + 2) bytes).  Returns 0 for
+ * attn_bwd_workspace_size -- bytes of device workspace attn_bwd needs: two
+ * fp32 row vectors (D and the logsumexp in base 2) over query rows padded to
+ * whole 128-row tiles (8 * B*Hq*ceil(Nq/128)*128 bytes).  Returns 0 for
  * shapes attn_bwd would reject.
  */
 size_t attn_bwd_workspace_size(int B, int Hq, int Hkv, int Nq, int Nk, int d);
@@ -121,12 +121,14 @@ size_t attn_bwd_workspace_size(int B, int Hq, int Hkv, int Nq, int Nk, int d);
  * Supported as for attn_fwd (d in {64, 128}, Hq % Hkv == 0, causal needs
  * Nq <= Nk).  Pointers 16-byte aligned (lse 4-byte).  The caller owns every
  * buffer.  Three kernels run in order on `stream`: a per-row pass (D, the LSE
- * in base 2, the accumulator zeroed), the main pass (one CTA per (b, KV head,
- * 128-key tile): dK and dV accumulated in tensor memory and written once, dQ
- * added into the accumulator with atomic adds, so dQ's rounding order can vary
- * between runs), and the dQ scaling pass.  Numerics: scores and all products
- * accumulate in fp32; P and dS are rounded to bf16 before the P.dO, dS.Q and
- * dS.K products.  Returns ATTN_OK once the kernels are enqueued;
+ * in base 2), a K/V-outer pass (one CTA per (b, KV head, 128-key tile): dK
+ * and dV accumulated in tensor memory over the group's query heads and Q
+ * tiles, written once) and a Q-outer pass (one CTA per (b, query head,
+ * 128-row Q tile): dQ accumulated in tensor memory over the K/V tiles,
+ * written once).  No atomics: every gradient is bit-identical from run to
+ * run.  S and dP are computed in both passes (lecture notes exercise 6).
+ * Numerics: scores and all products accumulate in fp32; P and dS are rounded
+ * to bf16 before the P.dO, dS.Q and dS.K products.  Returns ATTN_OK once the kernels are enqueued;
  * ATTN_ERR_WORKSPACE for a missing or short workspace.
  */
 attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o,

@@ -250,8 +250,8 @@ def test_tau_bound_from_the_notes():
 
 
 def test_bwd_workspace_size_and_argument_checks(lib):
-    # fp32 dQ accumulator + two row vectors over rows padded to 128
-    assert ea.attn_bwd_workspace_size(2, 8, 2, 300, 300, 128) == 4 * 2 * 8 * 384 * (128 + 2)
+    # two fp32 row vectors (D, lse2) over rows padded to 128
+    assert ea.attn_bwd_workspace_size(2, 8, 2, 300, 300, 128) == 8 * 2 * 8 * 384
     assert ea.attn_bwd_workspace_size(1, 4, 3, 128, 128, 64) == 0      # Hq % Hkv
     assert ea.attn_bwd_workspace_size(1, 4, 4, 128, 128, 96) == 0      # unsupported d
     fake = ctypes.c_void_p(0x10000)
