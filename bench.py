@@ -325,7 +325,7 @@ def run_ours(args, rank, world, local_rank):
         tb_nc = sum(e[0].elapsed_time(e[1]) for e in bev) / args.steps * 1e-3
         tb_c = sum(e[1].elapsed_time(e[2]) for e in bev) / args.steps * 1e-3
         fb_nc, fb_c = 2.5 * f_nc, 2.5 * f_c  # five GEMMs per tile against the forward's two
-        bwd = {"kernels": "attn_bwd (prep + main + dQ scaling)",
+        bwd = {"kernels": "attn_bwd (prep + K/V-outer dK/dV pass + Q-outer dQ pass)",
                "noncausal_tflops": fb_nc / tb_nc / 1e12, "causal_tflops": fb_c / tb_c / 1e12,
                "noncausal_ms": 1e3 * tb_nc, "causal_ms": 1e3 * tb_c,
                "tflops": (fb_nc + fb_c) / (tb_nc + tb_c) / 1e12,
