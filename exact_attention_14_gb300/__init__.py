@@ -19,7 +19,7 @@ __all__ = [
     "attn_decode_workspace_size", "attn_decode_noalloc", "attn_status_string", "attn_last_device_error",
     "attn_decode_num_splits", "attn_list_schedule", "attn_kv_tiles",
     "attn_fwd_num_units", "attn_fwd_schedule", "attn_fwd_split_plan", "attn_decode_kernel_launches",
-    "attn_bwd", "attn_bwd_workspace_size", "backward", "forward", "decode", "library_path", "load",
+    "attn_bwd", "attn_bwd_workspace_size", "backward", "attn_decode_paged", "decode_paged", "forward", "decode", "library_path", "load",
 ]
 
 ATTN_OK = 0
@@ -57,6 +57,10 @@ SIGNATURES = {
                                    ctypes.POINTER(ctypes.c_int)]),
     "attn_decode_kernel_launches": (_c_int, [_c_int] * 6),
     "attn_bwd_workspace_size": (ctypes.c_size_t, [_c_int] * 6),
+    "attn_decode_paged": (_c_int, [ctypes.c_void_p] * 7 + [_c_int, _c_int, _c_int, _c_ll, _c_int,
+                                                            _c_int, _c_int, ctypes.c_float, _c_int,
+                                                            ctypes.c_void_p, ctypes.c_size_t, _c_int,
+                                                            ctypes.c_void_p]),
     "attn_bwd": (_c_int, [ctypes.c_void_p] * 9 + [_c_int] * 7 + [ctypes.c_float, _c_int, _c_int,
                                                                  ctypes.c_void_p, ctypes.c_size_t,
                                                                  ctypes.c_void_p]),
@@ -370,3 +374,55 @@ def attn_decode_kernel_launches(B, Hq, Hkv, Nmax, d, num_splits=0) -> int:
     if n < 0:
         raise ValueError("attn_decode_kernel_launches rejected its arguments")
     return n
+
+
+def attn_decode_paged(q, k_pages, v_pages, block_table, seqlens, o, lse=None, *,
+                      scale: float | None = None, num_splits: int = 0, workspace=None,
+                      stream=None):
+    """Decode over a paged KV cache into caller-provided outputs.
+
+    q [B,Hq,1,d] bf16; k_pages, v_pages [num_blocks, page_size, Hkv, d] bf16;
+    block_table [B, max_blocks] int32; seqlens [B] int32; o [B,Hq,1,d] bf16
+    or fp32; lse [B,Hq,1] fp32 or None.  Asynchronous."""
+    import torch
+    _need(q, torch.bfloat16, "q")
+    _need(k_pages, torch.bfloat16, "k_pages")
+    _need(v_pages, torch.bfloat16, "v_pages")
+    _need(block_table, torch.int32, "block_table")
+    _need(seqlens, torch.int32, "seqlens")
+    if o.dtype not in (torch.bfloat16, torch.float32):
+        raise TypeError("o must be bfloat16 or float32")
+    _need(o, o.dtype, "o")
+    if lse is not None:
+        _need(lse, torch.float32, "lse")
+    B, Hq, one, d = q.shape
+    num_blocks, page_size, Hkv, dk = k_pages.shape
+    if one != 1 or dk != d or tuple(v_pages.shape) != tuple(k_pages.shape):
+        raise ValueError("q / page shapes mismatch")
+    if block_table.ndim != 2 or block_table.shape[0] != B or tuple(seqlens.shape) != (B,):
+        raise ValueError("block_table must be [B, max_blocks] and seqlens [B]")
+    max_blocks = block_table.shape[1]
+    if scale is None:
+        scale = d ** -0.5
+    need = attn_decode_workspace_size(B, Hq, Hkv, max_blocks * page_size, d, num_splits)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    odt = ATTN_OUT_F32 if o.dtype == torch.float32 else ATTN_OUT_BF16
+    rc = load().attn_decode_paged(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(block_table),
+                                  _ptr(seqlens), _ptr(o), _ptr(lse), B, Hq, Hkv, num_blocks,
+                                  page_size, max_blocks, d, float(scale), num_splits,
+                                  _ptr(workspace), workspace.numel(), odt, _stream_ptr(stream))
+    _check(rc, "attn_decode_paged")
+    return o, lse
+
+
+def decode_paged(q, k_pages, v_pages, block_table, seqlens, *, scale: float | None = None,
+                 num_splits: int = 0, out_dtype=None, stream=None):
+    """Allocate O and LSE with torch and run attn_decode_paged."""
+    import torch
+    out_dtype = out_dtype or torch.bfloat16
+    B, Hq, _, d = q.shape
+    o = torch.empty((B, Hq, 1, d), dtype=out_dtype, device=q.device)
+    lse = torch.empty((B, Hq, 1), dtype=torch.float32, device=q.device)
+    return attn_decode_paged(q, k_pages, v_pages, block_table, seqlens, o, lse, scale=scale,
+                             num_splits=num_splits, stream=stream)

@@ -96,6 +96,21 @@ attn_status_t encode_tmap_out_3d(CUtensorMap* map, void* base, bool f32, int d, 
     return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
+attn_status_t encode_tmap_paged_kv(CUtensorMap* map, const void* base, int d, int Hkv,
+                                   int page_size, long long num_blocks) {
+    if (!load_encoder()) return ATTN_ERR_CUDA;
+    cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)Hkv, (cuuint64_t)page_size, (cuuint64_t)num_blocks};
+    cuuint64_t strides[3] = {(cuuint64_t)d * 2, (cuuint64_t)Hkv * d * 2,
+                             (cuuint64_t)page_size * Hkv * d * 2};
+    cuuint32_t box[4] = {64u, 1u, 64u, 1u};
+    cuuint32_t elem[4] = {1u, 1u, 1u, 1u};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims,
+                          strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
 attn_status_t encode_tmap_f32_sw128_3d(CUtensorMap* map, void* base, int d, int rows,
                                        long long heads, int box_rows) {
     if (!load_encoder()) return ATTN_ERR_CUDA;
@@ -252,6 +267,34 @@ attn_status_t attn_decode(const void* q, const void* k_cache, const void* v_cach
     if (!workspace || workspace_bytes < need || !aligned16(workspace)) return ATTN_ERR_WORKSPACE;
     return launch_decode(q, k_cache, v_cache, seqlens, o, lse, B, Hq, Hkv, Nmax, d, scale, chunk,
                          workspace, o_dtype, static_cast<cudaStream_t>(stream), dev);
+}
+
+attn_status_t attn_decode_paged(const void* q, const void* k_pages, const void* v_pages,
+                                const int* block_table, const int* seqlens, void* o, float* lse,
+                                int B, int Hq, int Hkv, long long num_blocks, int page_size,
+                                int max_blocks, int d, float scale, int num_splits, void* workspace,
+                                size_t workspace_bytes, attn_out_dtype_t o_dtype, void* stream) {
+    if (!q || !k_pages || !v_pages || !block_table || !seqlens || !o) return ATTN_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages) || !aligned16(o) ||
+        !aligned4(seqlens) || !aligned4(block_table))
+        return ATTN_ERR_INVALID_ARG;
+    if (lse && !aligned4(lse)) return ATTN_ERR_INVALID_ARG;
+    if (num_blocks < 1 || max_blocks < 1 || page_size < 64) return ATTN_ERR_INVALID_ARG;
+    if (page_size % 64 != 0) return ATTN_ERR_UNSUPPORTED;
+    if ((long long)max_blocks * page_size > kMaxLen || num_blocks >= (1ll << 31))
+        return ATTN_ERR_INVALID_ARG;
+    const int Nmax = max_blocks * page_size;
+    attn_status_t st = check_common(B, Hq, Hkv, d, scale, o_dtype);
+    if (st != ATTN_OK) return st;
+    if ((st = check_decode_shape(B, Hq, Hkv, Nmax, d, num_splits)) != ATTN_OK) return st;
+    DeviceInfo dev;
+    if ((st = current_device_info(&dev)) != ATTN_OK) return st;
+    const int chunk = decode_chunk(Nmax, B, Hkv, dev.num_sms, num_splits);
+    const size_t need = decode_workspace_bytes(B, Hq, Nmax, d, chunk);
+    if (!workspace || workspace_bytes < need || !aligned16(workspace)) return ATTN_ERR_WORKSPACE;
+    return launch_decode_paged(q, k_pages, v_pages, block_table, seqlens, o, lse, B, Hq, Hkv,
+                               num_blocks, page_size, max_blocks, d, scale, chunk, workspace,
+                               o_dtype, static_cast<cudaStream_t>(stream), dev);
 }
 
 const char* attn_status_string(attn_status_t s) {

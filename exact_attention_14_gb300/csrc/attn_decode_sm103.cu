@@ -67,6 +67,10 @@ struct DecParams {
     int B, Hq, Hkv, G, Nmax, chunk, max_splits;
     float c;   // scale * log2(e)
     int slot;  // arrival-counter slot of this launch; -1: merge in the combine kernel
+    // paged cache (block_table != nullptr): the 64-key stage starting at key t of
+    // sequence b lives in page block_table[b * max_blocks + t / page_size]
+    const int* block_table;
+    int page_size, max_blocks;
 };
 
 // Arrival counters of the in-kernel merge: one per (b, KV head) group and
@@ -173,10 +177,23 @@ attn_decode_split_kernel(const __grid_constant__ CUtensorMap tk, const __grid_co
                 mbar_arrive_expect_tx(bar, C::kStageBytes);
                 const uint32_t dk = smem_u32(smem + slot * C::kStageBytes);
                 const uint32_t dv = dk + C::kHalfBytes;
+                const int key = t0 + st * kStageKeys;
+                if (p.block_table) {
+                    // a page index out of range only reads zeros (TMA bounds checks)
+                    const int blk = key / p.page_size;
+                    const int page = __ldg(p.block_table + (size_t)b * p.max_blocks + blk);
+                    const int off = key - blk * p.page_size;
 #pragma unroll
-                for (int c = 0; c < D / 64; ++c) {
-                    tma_load_3d(dk + c * (kStageKeys * 128), &tk, bar, 64 * c, t0 + st * kStageKeys, kv_head);
-                    tma_load_3d(dv + c * (kStageKeys * 128), &tv, bar, 64 * c, t0 + st * kStageKeys, kv_head);
+                    for (int c = 0; c < D / 64; ++c) {
+                        tma_load_4d(dk + c * (kStageKeys * 128), &tk, bar, 64 * c, g, off, page);
+                        tma_load_4d(dv + c * (kStageKeys * 128), &tv, bar, 64 * c, g, off, page);
+                    }
+                } else {
+#pragma unroll
+                    for (int c = 0; c < D / 64; ++c) {
+                        tma_load_3d(dk + c * (kStageKeys * 128), &tk, bar, 64 * c, key, kv_head);
+                        tma_load_3d(dv + c * (kStageKeys * 128), &tv, bar, 64 * c, key, kv_head);
+                    }
                 }
                 ++issued;
             }
@@ -547,10 +564,25 @@ size_t decode_workspace_bytes(int B, int Hq, int Nmax, int d, int chunk) {
     return align16(rows * d * 4) + align16(rows * 4);
 }
 
-attn_status_t launch_decode(const void* q, const void* k_cache, const void* v_cache,
-                            const int* seqlens, void* o, float* lse, int B, int Hq, int Hkv,
-                            int Nmax, int d, float scale, int chunk, void* workspace,
-                            attn_out_dtype_t o_dtype, cudaStream_t stream, const DeviceInfo& dev) {
+namespace {
+attn_status_t launch_decode_common(const CUtensorMap& tk, const CUtensorMap& tv, const void* q,
+                                   const int* seqlens, void* o, float* lse, DecParams& p, int d,
+                                   void* workspace, attn_out_dtype_t o_dtype, cudaStream_t stream,
+                                   const DeviceInfo& dev) {
+    const size_t rows = (size_t)p.B * p.Hq * p.max_splits;
+    float* ws_o = static_cast<float*>(workspace);
+    float* ws_lse = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + align16(rows * d * 4));
+    const bool f32 = o_dtype == ATTN_OUT_F32;
+    if (d == 128)
+        return f32 ? launch_decode_t<128, true>(tk, tv, q, seqlens, o, lse, ws_o, ws_lse, p, stream, dev)
+                   : launch_decode_t<128, false>(tk, tv, q, seqlens, o, lse, ws_o, ws_lse, p, stream, dev);
+    if (d == 64)
+        return f32 ? launch_decode_t<64, true>(tk, tv, q, seqlens, o, lse, ws_o, ws_lse, p, stream, dev)
+                   : launch_decode_t<64, false>(tk, tv, q, seqlens, o, lse, ws_o, ws_lse, p, stream, dev);
+    return ATTN_ERR_UNSUPPORTED;
+}
+
+DecParams make_dec_params(int B, int Hq, int Hkv, int Nmax, int d, float scale, int chunk) {
     DecParams p;
     p.B = B;
     p.Hq = Hq;
@@ -564,21 +596,40 @@ attn_status_t launch_decode(const void* q, const void* k_cache, const void* v_ca
     p.slot = decode_merges_in_kernel(B, Hkv, p.G, p.max_splits, d)
                  ? (int)(launches.fetch_add(1u, std::memory_order_relaxed) % kDecSlots)
                  : -1;
-    const size_t rows = (size_t)B * Hq * p.max_splits;
-    float* ws_o = static_cast<float*>(workspace);
-    float* ws_lse = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + align16(rows * d * 4));
+    p.block_table = nullptr;
+    p.page_size = 0;
+    p.max_blocks = 0;
+    return p;
+}
+}  // namespace
+
+attn_status_t launch_decode(const void* q, const void* k_cache, const void* v_cache,
+                            const int* seqlens, void* o, float* lse, int B, int Hq, int Hkv,
+                            int Nmax, int d, float scale, int chunk, void* workspace,
+                            attn_out_dtype_t o_dtype, cudaStream_t stream, const DeviceInfo& dev) {
+    DecParams p = make_dec_params(B, Hq, Hkv, Nmax, d, scale, chunk);
     CUtensorMap tk, tv;
     attn_status_t st;
     if ((st = encode_tmap_bf16_3d(&tk, k_cache, d, Nmax, (long long)B * Hkv, kStageKeys)) != ATTN_OK) return st;
     if ((st = encode_tmap_bf16_3d(&tv, v_cache, d, Nmax, (long long)B * Hkv, kStageKeys)) != ATTN_OK) return st;
-    const bool f32 = o_dtype == ATTN_OUT_F32;
-    if (d == 128)
-        return f32 ? launch_decode_t<128, true>(tk, tv, q, seqlens, o, lse, ws_o, ws_lse, p, stream, dev)
-                   : launch_decode_t<128, false>(tk, tv, q, seqlens, o, lse, ws_o, ws_lse, p, stream, dev);
-    if (d == 64)
-        return f32 ? launch_decode_t<64, true>(tk, tv, q, seqlens, o, lse, ws_o, ws_lse, p, stream, dev)
-                   : launch_decode_t<64, false>(tk, tv, q, seqlens, o, lse, ws_o, ws_lse, p, stream, dev);
-    return ATTN_ERR_UNSUPPORTED;
+    return launch_decode_common(tk, tv, q, seqlens, o, lse, p, d, workspace, o_dtype, stream, dev);
+}
+
+attn_status_t launch_decode_paged(const void* q, const void* k_pages, const void* v_pages,
+                                  const int* block_table, const int* seqlens, void* o, float* lse,
+                                  int B, int Hq, int Hkv, long long num_blocks, int page_size,
+                                  int max_blocks, int d, float scale, int chunk, void* workspace,
+                                  attn_out_dtype_t o_dtype, cudaStream_t stream, const DeviceInfo& dev) {
+    const int Nmax = max_blocks * page_size;
+    DecParams p = make_dec_params(B, Hq, Hkv, Nmax, d, scale, chunk);
+    p.block_table = block_table;
+    p.page_size = page_size;
+    p.max_blocks = max_blocks;
+    CUtensorMap tk, tv;
+    attn_status_t st;
+    if ((st = encode_tmap_paged_kv(&tk, k_pages, d, Hkv, page_size, num_blocks)) != ATTN_OK) return st;
+    if ((st = encode_tmap_paged_kv(&tv, v_pages, d, Hkv, page_size, num_blocks)) != ATTN_OK) return st;
+    return launch_decode_common(tk, tv, q, seqlens, o, lse, p, d, workspace, o_dtype, stream, dev);
 }
 
 }  // namespace gb300

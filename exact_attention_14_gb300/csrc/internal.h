@@ -32,6 +32,11 @@ attn_status_t encode_tmap_out_3d(CUtensorMap* map, void* base, bool f32, int d, 
 attn_status_t encode_tmap_f32_sw128_3d(CUtensorMap* map, void* base, int d, int rows,
                                        long long heads, int box_rows);
 
+// 4-D bf16 tensor map over a paged KV cache [num_blocks, page_size, Hkv, d]
+// with a 128-byte-swizzled box of 64 (d) x 1 (head) x 64 (keys) x 1 (block).
+attn_status_t encode_tmap_paged_kv(CUtensorMap* map, const void* base, int d, int Hkv,
+                                   int page_size, long long num_blocks);
+
 attn_status_t launch_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
                          int B, int Hq, int Hkv, int Nq, int Nk, int d, int causal, float scale,
                          attn_out_dtype_t o_dtype, cudaStream_t stream, const DeviceInfo& dev);
@@ -55,5 +60,13 @@ attn_status_t launch_decode(const void* q, const void* k_cache, const void* v_ca
                             const int* seqlens, void* o, float* lse, int B, int Hq, int Hkv,
                             int Nmax, int d, float scale, int chunk, void* workspace,
                             attn_out_dtype_t o_dtype, cudaStream_t stream, const DeviceInfo& dev);
+// Paged cache: k/v pages [num_blocks, page_size, Hkv, d], block_table
+// [B, max_blocks] (page of logical block i of sequence b); Nmax = max_blocks *
+// page_size, page_size a multiple of 64.
+attn_status_t launch_decode_paged(const void* q, const void* k_pages, const void* v_pages,
+                                  const int* block_table, const int* seqlens, void* o, float* lse,
+                                  int B, int Hq, int Hkv, long long num_blocks, int page_size,
+                                  int max_blocks, int d, float scale, int chunk, void* workspace,
+                                  attn_out_dtype_t o_dtype, cudaStream_t stream, const DeviceInfo& dev);
 
 }  // namespace gb300

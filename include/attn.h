@@ -145,6 +145,31 @@ attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* 
 size_t attn_decode_workspace_size(int B, int Hq, int Hkv, int Nmax, int d, int num_splits);
 
 /*
+ * attn_decode_paged -- attn_decode over a paged KV cache (the block-table
+ * layout decode servers use; lecture notes 6.1 split-KV as in attn_decode).
+ *
+ *   k_pages, v_pages  bf16 [num_blocks, page_size, Hkv, d]: pages of page_size
+ *            consecutive keys, all KV heads of a key together
+ *   block_table  int32 [B, max_blocks] (device): logical block i of sequence
+ *            b (keys [i*page_size, (i+1)*page_size)) is page block_table[b, i]
+ *   seqlens  int32 [B] (device), as for attn_decode, with Nmax = max_blocks *
+ *            page_size; only the blocks that hold keys < seqlens[b] are read
+ *   page_size a multiple of 64 (ATTN_ERR_UNSUPPORTED otherwise)
+ *   workspace  at least attn_decode_workspace_size(B, Hq, Hkv, max_blocks *
+ *            page_size, d, num_splits) bytes
+ *
+ * Everything else (q, o, lse, scale, num_splits, splits and merge, errors) is
+ * as for attn_decode, and for the same keys the result is bit-identical to
+ * attn_decode on the same values stored contiguously.  A block-table entry
+ * outside [0, num_blocks) reads as zeros (it never faults).
+ */
+attn_status_t attn_decode_paged(const void* q, const void* k_pages, const void* v_pages,
+                                const int* block_table, const int* seqlens, void* o, float* lse,
+                                int B, int Hq, int Hkv, long long num_blocks, int page_size,
+                                int max_blocks, int d, float scale, int num_splits, void* workspace,
+                                size_t workspace_bytes, attn_out_dtype_t o_dtype, void* stream);
+
+/*
  * Number of kernels attn_decode launches for this shape and split request:
  * 1 when the split kernel merges the splits itself (the last split of each
  * (sequence, KV head) to finish merges them; at most 4096 such groups and

@@ -269,3 +269,23 @@ def test_bwd_workspace_size_and_argument_checks(lib):
     bad[15] = 1
     bad[12], bad[13] = 256, 128                                        # causal with Nq > Nk
     assert lib.attn_bwd(*bad) == ea.ATTN_ERR_INVALID_ARG
+
+
+def test_decode_paged_argument_checks(lib):
+    fake = ctypes.c_void_p(0x10000)
+    args = [fake] * 7 + [2, 8, 2, 100, 64, 16, 128, ctypes.c_float(0.1), 0, fake, 1 << 30, 0, None]
+    bad = list(args)
+    bad[3] = None                                                      # no block table
+    assert lib.attn_decode_paged(*bad) == ea.ATTN_ERR_INVALID_ARG
+    bad = list(args)
+    bad[11] = 96                                                       # page size not a multiple of 64
+    assert lib.attn_decode_paged(*bad) == ea.ATTN_ERR_UNSUPPORTED
+    bad = list(args)
+    bad[11] = 32                                                       # page size below 64
+    assert lib.attn_decode_paged(*bad) == ea.ATTN_ERR_INVALID_ARG
+    bad = list(args)
+    bad[10] = 0                                                        # no blocks
+    assert lib.attn_decode_paged(*bad) == ea.ATTN_ERR_INVALID_ARG
+    bad = list(args)
+    bad[13] = 96                                                       # d
+    assert lib.attn_decode_paged(*bad) == ea.ATTN_ERR_UNSUPPORTED
