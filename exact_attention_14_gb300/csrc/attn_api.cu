@@ -164,7 +164,7 @@ attn_status_t check_fwd(const void* q, const void* k, const void* v, const void*
     if (Nq < 1 || Nk < 1 || Nq > kMaxLen || Nk > kMaxLen) return ATTN_ERR_INVALID_ARG;
     if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
     if (causal && Nq > Nk) return ATTN_ERR_INVALID_ARG;
-    if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+    if (!head_dim_supported(d)) return ATTN_ERR_UNSUPPORTED;
     return ATTN_OK;
 }
 
@@ -174,7 +174,7 @@ attn_status_t check_decode_shape(int B, int Hq, int Hkv, int Nmax, int d, int nu
     if ((long long)B * Hq > kMaxHeads || (long long)B * Hkv > kMaxHeads) return ATTN_ERR_INVALID_ARG;
     if (Nmax < 1 || Nmax > kMaxLen) return ATTN_ERR_INVALID_ARG;
     if (num_splits < 0) return ATTN_ERR_INVALID_ARG;
-    if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+    if (!head_dim_supported(d)) return ATTN_ERR_UNSUPPORTED;
     if (Hq / Hkv > 16) return ATTN_ERR_UNSUPPORTED;
     return ATTN_OK;
 }
@@ -208,7 +208,7 @@ attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, flo
 size_t attn_bwd_workspace_size(int B, int Hq, int Hkv, int Nq, int Nk, int d) {
     if (check_common(B, Hq, Hkv, d, 1.0f, ATTN_OUT_BF16) != ATTN_OK) return 0;
     if (Nq < 1 || Nk < 1 || Nq > kMaxLen || Nk > kMaxLen) return 0;
-    if (d != 64 && d != 128) return 0;
+    if (!head_dim_supported(d)) return 0;
     return bwd_workspace_bytes(B, Hq, Nq, d);
 }
 
@@ -236,7 +236,7 @@ size_t attn_decode_workspace_size(int B, int Hq, int Hkv, int Nmax, int d, int n
     int sms = 0;
     if (decode_sms_or_default(&sms) != 0) return 0;
     const int chunk = decode_chunk(Nmax, B, Hkv, sms, num_splits);
-    return decode_workspace_bytes(B, Hq, Nmax, d, chunk);
+    return decode_workspace_bytes(B, Hq, Nmax, pad_head_dim(d), chunk);
 }
 
 int attn_decode_kernel_launches(int B, int Hq, int Hkv, int Nmax, int d, int num_splits) {
@@ -245,7 +245,7 @@ int attn_decode_kernel_launches(int B, int Hq, int Hkv, int Nmax, int d, int num
     if (decode_sms_or_default(&sms) != 0) return -1;
     const int chunk = decode_chunk(Nmax, B, Hkv, sms, num_splits);
     const int max_splits = (Nmax + chunk - 1) / chunk;
-    return decode_merges_in_kernel(B, Hkv, Hq / Hkv, max_splits, d) ? 1 : 2;
+    return decode_merges_in_kernel(B, Hkv, Hq / Hkv, max_splits, pad_head_dim(d)) ? 1 : 2;
 }
 
 attn_status_t attn_decode(const void* q, const void* k_cache, const void* v_cache,
@@ -263,7 +263,7 @@ attn_status_t attn_decode(const void* q, const void* k_cache, const void* v_cach
     DeviceInfo dev;
     if ((st = current_device_info(&dev)) != ATTN_OK) return st;
     const int chunk = decode_chunk(Nmax, B, Hkv, dev.num_sms, num_splits);
-    const size_t need = decode_workspace_bytes(B, Hq, Nmax, d, chunk);
+    const size_t need = decode_workspace_bytes(B, Hq, Nmax, pad_head_dim(d), chunk);
     if (!workspace || workspace_bytes < need || !aligned16(workspace)) return ATTN_ERR_WORKSPACE;
     return launch_decode(q, k_cache, v_cache, seqlens, o, lse, B, Hq, Hkv, Nmax, d, scale, chunk,
                          workspace, o_dtype, static_cast<cudaStream_t>(stream), dev);
@@ -290,7 +290,7 @@ attn_status_t attn_decode_paged(const void* q, const void* k_pages, const void* 
     DeviceInfo dev;
     if ((st = current_device_info(&dev)) != ATTN_OK) return st;
     const int chunk = decode_chunk(Nmax, B, Hkv, dev.num_sms, num_splits);
-    const size_t need = decode_workspace_bytes(B, Hq, Nmax, d, chunk);
+    const size_t need = decode_workspace_bytes(B, Hq, Nmax, pad_head_dim(d), chunk);
     if (!workspace || workspace_bytes < need || !aligned16(workspace)) return ATTN_ERR_WORKSPACE;
     return launch_decode_paged(q, k_pages, v_pages, block_table, seqlens, o, lse, B, Hq, Hkv,
                                num_blocks, page_size, max_blocks, d, scale, chunk, workspace,

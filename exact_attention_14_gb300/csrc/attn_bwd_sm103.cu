@@ -71,6 +71,7 @@ struct BwdCfg {
 struct BwdParams {
     int B, Hq, Hkv, Nq, Nk, Nq_pad, group, off, n_kt, causal;
     int sec_groups;     // (b, KV head) groups per L2 section
+    int d_act;          // the tensors' head dim (<= D; the tiles' columns past it are zeros)
     float c;      // scale * log2(e)
     float scale;
     const float* lse2;  // [B*Hq, Nq_pad]
@@ -307,20 +308,25 @@ __device__ __forceinline__ void p_ds_chunk(const uint32_t (&s)[32], const uint32
     }
 }
 
+// 32 values of one output row, columns [0, ncols) of them (ncols <= 32, a
+// multiple of 8): 16-byte stores.
 template <int D, bool OUT_F32>
-__device__ __forceinline__ void store_row32(void* base, size_t elem, const float (&v)[32]) {
+__device__ __forceinline__ void store_row32(void* base, size_t elem, const float (&v)[32],
+                                            int ncols = 32) {
     if constexpr (OUT_F32) {
         uint4* dst = reinterpret_cast<uint4*>(static_cast<float*>(base) + elem);
 #pragma unroll
         for (int i = 0; i < 8; ++i)
-            dst[i] = make_uint4(__float_as_uint(v[4 * i]), __float_as_uint(v[4 * i + 1]),
-                                __float_as_uint(v[4 * i + 2]), __float_as_uint(v[4 * i + 3]));
+            if (4 * i < ncols)
+                dst[i] = make_uint4(__float_as_uint(v[4 * i]), __float_as_uint(v[4 * i + 1]),
+                                    __float_as_uint(v[4 * i + 2]), __float_as_uint(v[4 * i + 3]));
     } else {
         uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(base) + elem);
 #pragma unroll
         for (int i = 0; i < 4; ++i)
-            dst[i] = make_uint4(pack_bf16x2(v[8 * i], v[8 * i + 1]), pack_bf16x2(v[8 * i + 2], v[8 * i + 3]),
-                                pack_bf16x2(v[8 * i + 4], v[8 * i + 5]), pack_bf16x2(v[8 * i + 6], v[8 * i + 7]));
+            if (8 * i < ncols)
+                dst[i] = make_uint4(pack_bf16x2(v[8 * i], v[8 * i + 1]), pack_bf16x2(v[8 * i + 2], v[8 * i + 3]),
+                                    pack_bf16x2(v[8 * i + 4], v[8 * i + 5]), pack_bf16x2(v[8 * i + 6], v[8 * i + 7]));
     }
 }
 
@@ -373,16 +379,17 @@ __device__ void bwd_pds(int wq, int lane, uint8_t* smem, BwdBars* bars, uint32_t
     }
     // dK = scale * dS^T Q, dV = P^T dO: one key row per thread, written once
     const bool live = jg < p.Nk;
-    const size_t elem = (((size_t)w.b * p.Hkv + w.g) * p.Nk + (size_t)(live ? jg : 0)) * D;
+    const size_t elem = (((size_t)w.b * p.Hkv + w.g) * p.Nk + (size_t)(live ? jg : 0)) * p.d_act;
     if (w.n_tiles == 0) {
         float z[32];
 #pragma unroll
         for (int x = 0; x < 32; ++x) z[x] = 0.f;
         if (live)
 #pragma unroll 1
-            for (int cc = 0; cc < D; cc += 32) {
-                store_row32<D, OUT_F32>(p.dk, elem + cc, z);
-                store_row32<D, OUT_F32>(p.dv, elem + cc, z);
+            for (int cc = 0; cc < p.d_act; cc += 32) {
+                const int nc = p.d_act - cc < 32 ? p.d_act - cc : 32;
+                store_row32<D, OUT_F32>(p.dk, elem + cc, z, nc);
+                store_row32<D, OUT_F32>(p.dv, elem + cc, z, nc);
             }
         return;
     }
@@ -398,14 +405,15 @@ __device__ void bwd_pds(int wq, int lane, uint8_t* smem, BwdBars* bars, uint32_t
         float v[32];
         tmem_ld32(tmem + 256 + cc + lane_off, r);
         tmem_wait_ld();
+        const int nc = p.d_act - cc < 32 ? p.d_act - cc : 32;  // <= 0: past the head dim
 #pragma unroll
         for (int x = 0; x < 32; ++x) v[x] = __uint_as_float(r[x]);
-        if (live) store_row32<D, OUT_F32>(p.dv, elem + cc, v);
+        if (live && nc > 0) store_row32<D, OUT_F32>(p.dv, elem + cc, v, nc);
         tmem_ld32(tmem + 256 + D + cc + lane_off, r);
         tmem_wait_ld();
 #pragma unroll
         for (int x = 0; x < 32; ++x) v[x] = __uint_as_float(r[x]) * p.scale;
-        if (live) store_row32<D, OUT_F32>(p.dk, elem + cc, v);
+        if (live && nc > 0) store_row32<D, OUT_F32>(p.dk, elem + cc, v, nc);
     }
 }
 
@@ -701,7 +709,7 @@ __device__ void dq_ds(int wq, int lane, DqBars* bars, uint32_t tmem, const BwdPa
     tc_fence_after();
     // every lane runs the (warp-collective) TMEM loads; rows past Nq store nothing
     const bool live = row < p.Nq;
-    const size_t elem = (bh * p.Nq + (size_t)(live ? row : 0)) * D;
+    const size_t elem = (bh * p.Nq + (size_t)(live ? row : 0)) * p.d_act;
 #pragma unroll 1
     for (int cc = 0; cc < D; cc += 32) {
         float v[32];
@@ -715,7 +723,8 @@ __device__ void dq_ds(int wq, int lane, DqBars* bars, uint32_t tmem, const BwdPa
 #pragma unroll
             for (int x = 0; x < 32; ++x) v[x] = 0.f;
         }
-        if (live) store_row32<D, OUT_F32>(p.dq, elem + cc, v);
+        const int nc = p.d_act - cc < 32 ? p.d_act - cc : 32;
+        if (live && nc > 0) store_row32<D, OUT_F32>(p.dq, elem + cc, v, nc);
     }
 }
 
@@ -782,7 +791,7 @@ template <int D>
 __global__ void __launch_bounds__(256)
 attn_bwd_prep_kernel(const void* __restrict__ o, int o_f32, const __nv_bfloat16* __restrict__ dout,
                      const float* __restrict__ lse, float* __restrict__ lse2, float* __restrict__ dvec,
-                     long long rows_pad, int Nq, int Nq_pad) {
+                     long long rows_pad, int Nq, int Nq_pad, int dh) {
     const long long r = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (r >= rows_pad) return;
@@ -790,8 +799,8 @@ attn_bwd_prep_kernel(const void* __restrict__ o, int o_f32, const __nv_bfloat16*
     const int i = (int)(r - bh * Nq_pad);
     float sum = 0.f;
     if (i < Nq) {
-        const size_t base = ((size_t)bh * Nq + i) * D;
-        for (int c = lane; c < D; c += 32) {
+        const size_t base = ((size_t)bh * Nq + i) * dh;
+        for (int c = lane; c < dh; c += 32) {
             const float ov = o_f32 ? static_cast<const float*>(o)[base + c]
                                    : __bfloat162float(static_cast<const __nv_bfloat16*>(o)[base + c]);
             sum = fmaf(__bfloat162float(dout[base + c]), ov, sum);
@@ -823,7 +832,8 @@ attn_status_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const C
     }
     const long long rows_pad = (long long)p.B * p.Hq * p.Nq_pad;
     attn_bwd_prep_kernel<D><<<(unsigned)((rows_pad + 7) / 8), 256, 0, stream>>>(
-        o, o_f32, static_cast<const __nv_bfloat16*>(dout), lse, lse2, dvec, rows_pad, p.Nq, p.Nq_pad);
+        o, o_f32, static_cast<const __nv_bfloat16*>(dout), lse, lse2, dvec, rows_pad, p.Nq, p.Nq_pad,
+        p.d_act);
     if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
     const long long kv_ctas = (long long)p.B * p.Hkv * p.n_kt;
     attn_bwd_dkdv_kernel<D, OUT_F32><<<(unsigned)kv_ctas, kBwdThreads, BwdCfg<D>::kSmemBytes, stream>>>(
@@ -869,6 +879,7 @@ attn_status_t launch_bwd(const void* q, const void* k, const void* v, const void
     }
     p.c = scale * kBwdLog2e;
     p.scale = scale;
+    p.d_act = d;
     const size_t rows = (size_t)B * Hq * p.Nq_pad;
     float* lse2 = static_cast<float*>(workspace);
     float* dvec = lse2 + rows;
@@ -888,10 +899,10 @@ attn_status_t launch_bwd(const void* q, const void* k, const void* v, const void
     if ((st = encode_tmap_bf16_3d(&tdo, dout, d, Nq, (long long)B * Hq, kBT)) != ATTN_OK) return st;
     const int o_f32 = o_dtype == ATTN_OUT_F32;
     const bool g32 = grad_dtype == ATTN_OUT_F32;
-    if (d == 128)
+    if (pad_head_dim(d) == 128)
         return g32 ? launch_bwd_t<128, true>(tq, tk, tv, tdo, p, o, o_f32, dout, lse, lse2, dvec, stream, dev)
                    : launch_bwd_t<128, false>(tq, tk, tv, tdo, p, o, o_f32, dout, lse, lse2, dvec, stream, dev);
-    if (d == 64)
+    if (pad_head_dim(d) == 64)
         return g32 ? launch_bwd_t<64, true>(tq, tk, tv, tdo, p, o, o_f32, dout, lse, lse2, dvec, stream, dev)
                    : launch_bwd_t<64, false>(tq, tk, tv, tdo, p, o, o_f32, dout, lse, lse2, dvec, stream, dev);
     return ATTN_ERR_UNSUPPORTED;

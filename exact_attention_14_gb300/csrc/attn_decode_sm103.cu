@@ -71,6 +71,7 @@ struct DecParams {
     // sequence b lives in page block_table[b * max_blocks + t / page_size]
     const int* block_table;
     int page_size, max_blocks;
+    int dh;    // the tensors' head dim (<= D: columns past dh are zeros in the tiles)
 };
 
 // Arrival counters of the in-kernel merge: one per (b, KV head) group and
@@ -129,11 +130,11 @@ attn_decode_split_kernel(const __grid_constant__ CUtensorMap tk, const __grid_co
     if (t0 >= L) {  // uniform across the CTA: nothing started yet
         if (L == 0 && split == 0 && p.slot >= 0) {
             // an empty sequence: O = 0 and LSE = -inf for the group's heads
-            for (int e = threadIdx.x; e < p.G * D; e += blockDim.x) {
-                const size_t bh = (size_t)b * p.Hq + (size_t)g * p.G + e / D;
-                const int col = e % D;
-                if constexpr (OUT_F32) static_cast<float*>(o)[bh * D + col] = 0.f;
-                else static_cast<__nv_bfloat16*>(o)[bh * D + col] = __float2bfloat16_rn(0.f);
+            for (int e = threadIdx.x; e < p.G * p.dh; e += blockDim.x) {
+                const size_t bh = (size_t)b * p.Hq + (size_t)g * p.G + e / p.dh;
+                const int col = e % p.dh;
+                if constexpr (OUT_F32) static_cast<float*>(o)[bh * p.dh + col] = 0.f;
+                else static_cast<__nv_bfloat16*>(o)[bh * p.dh + col] = __float2bfloat16_rn(0.f);
                 if (col == 0 && lse) lse[bh] = -INFINITY;
             }
         }
@@ -218,14 +219,17 @@ attn_decode_split_kernel(const __grid_constant__ CUtensorMap tk, const __grid_co
     // Query fragments (A operand, rows = packed heads of this KV group)
     uint32_t qa[D / 16][4];
     {
-        const __nv_bfloat16* qb = q + ((size_t)b * p.Hq + (size_t)g * G) * D;
+        // rows of the group's query heads; columns past dh are zero
+        const int dh = p.dh;
+        const __nv_bfloat16* qb = q + ((size_t)b * p.Hq + (size_t)g * G) * dh;
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
             const int c0 = ks * 16 + 2 * qc;
-            qa[ks][0] = qr < G ? *reinterpret_cast<const uint32_t*>(qb + qr * D + c0) : 0u;
-            qa[ks][1] = qr + 8 < G ? *reinterpret_cast<const uint32_t*>(qb + (qr + 8) * D + c0) : 0u;
-            qa[ks][2] = qr < G ? *reinterpret_cast<const uint32_t*>(qb + qr * D + c0 + 8) : 0u;
-            qa[ks][3] = qr + 8 < G ? *reinterpret_cast<const uint32_t*>(qb + (qr + 8) * D + c0 + 8) : 0u;
+            const bool lo = c0 < dh, hi = c0 + 8 < dh;
+            qa[ks][0] = (qr < G && lo) ? *reinterpret_cast<const uint32_t*>(qb + qr * dh + c0) : 0u;
+            qa[ks][1] = (qr + 8 < G && lo) ? *reinterpret_cast<const uint32_t*>(qb + (qr + 8) * dh + c0) : 0u;
+            qa[ks][2] = (qr < G && hi) ? *reinterpret_cast<const uint32_t*>(qb + qr * dh + c0 + 8) : 0u;
+            qa[ks][3] = (qr + 8 < G && hi) ? *reinterpret_cast<const uint32_t*>(qb + (qr + 8) * dh + c0 + 8) : 0u;
         }
     }
     float oacc[D / 8][4];
@@ -393,8 +397,10 @@ attn_decode_split_kernel(const __grid_constant__ CUtensorMap tk, const __grid_co
         const float lse2 = M + log2f(xsum);
         const size_t bh = (size_t)b * p.Hq + (size_t)g * G + h;
         if (nsplit_b == 1) {
-            if constexpr (OUT_F32) static_cast<float*>(o)[bh * D + col] = val;
-            else static_cast<__nv_bfloat16*>(o)[bh * D + col] = __float2bfloat16_rn(val);
+            if (col < p.dh) {
+                if constexpr (OUT_F32) static_cast<float*>(o)[bh * p.dh + col] = val;
+                else static_cast<__nv_bfloat16*>(o)[bh * p.dh + col] = __float2bfloat16_rn(val);
+            }
             if (col == 0 && lse) lse[bh] = lse2 * kLn2f;
         } else {
             ws_o[(bh * p.max_splits + split) * D + col] = val;
@@ -460,8 +466,10 @@ attn_decode_split_kernel(const __grid_constant__ CUtensorMap tk, const __grid_co
             acc.w = fmaf(w, v.w, acc.w);
         }
         const float inv = s_head[2 * h];
-        const size_t base = (bh0 + h) * D + (size_t)c4 * 4;
-        if constexpr (OUT_F32) {
+        const size_t base = (bh0 + h) * p.dh + (size_t)c4 * 4;
+        if (4 * c4 >= p.dh) {
+            // a column group past the head dim: nothing to write
+        } else if constexpr (OUT_F32) {
             *reinterpret_cast<float4*>(static_cast<float*>(o) + base) =
                 make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
         } else {
@@ -503,8 +511,10 @@ attn_decode_combine_kernel(const int* __restrict__ seqlens, const float* __restr
         val = acc / wsum;
         lse_nat = (M + log2f(wsum)) * kLn2f;
     }
-    if constexpr (OUT_F32) static_cast<float*>(o)[bh * D + col] = val;
-    else static_cast<__nv_bfloat16*>(o)[bh * D + col] = __float2bfloat16_rn(val);
+    if (col < p.dh) {
+        if constexpr (OUT_F32) static_cast<float*>(o)[bh * p.dh + col] = val;
+        else static_cast<__nv_bfloat16*>(o)[bh * p.dh + col] = __float2bfloat16_rn(val);
+    }
     if (col == 0 && lse) lse[bh] = lse_nat;
 }
 
@@ -569,6 +579,7 @@ attn_status_t launch_decode_common(const CUtensorMap& tk, const CUtensorMap& tv,
                                    const int* seqlens, void* o, float* lse, DecParams& p, int d,
                                    void* workspace, attn_out_dtype_t o_dtype, cudaStream_t stream,
                                    const DeviceInfo& dev) {
+    d = pad_head_dim(d);  // the kernel's tile width (columns past p.dh are zeros)
     const size_t rows = (size_t)p.B * p.Hq * p.max_splits;
     float* ws_o = static_cast<float*>(workspace);
     float* ws_lse = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + align16(rows * d * 4));
@@ -579,7 +590,7 @@ attn_status_t launch_decode_common(const CUtensorMap& tk, const CUtensorMap& tv,
     if (d == 64)
         return f32 ? launch_decode_t<64, true>(tk, tv, q, seqlens, o, lse, ws_o, ws_lse, p, stream, dev)
                    : launch_decode_t<64, false>(tk, tv, q, seqlens, o, lse, ws_o, ws_lse, p, stream, dev);
-    return ATTN_ERR_UNSUPPORTED;
+    return ATTN_ERR_UNSUPPORTED;  // d is the padded head dim here
 }
 
 DecParams make_dec_params(int B, int Hq, int Hkv, int Nmax, int d, float scale, int chunk) {
@@ -593,12 +604,13 @@ DecParams make_dec_params(int B, int Hq, int Hkv, int Nmax, int d, float scale, 
     p.max_splits = (Nmax + chunk - 1) / chunk;
     p.c = scale * kLog2ef;
     static std::atomic<uint32_t> launches{0};
-    p.slot = decode_merges_in_kernel(B, Hkv, p.G, p.max_splits, d)
+    p.slot = decode_merges_in_kernel(B, Hkv, p.G, p.max_splits, pad_head_dim(d))
                  ? (int)(launches.fetch_add(1u, std::memory_order_relaxed) % kDecSlots)
                  : -1;
     p.block_table = nullptr;
     p.page_size = 0;
     p.max_blocks = 0;
+    p.dh = d;
     return p;
 }
 }  // namespace

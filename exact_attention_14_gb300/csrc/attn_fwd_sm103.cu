@@ -90,6 +90,7 @@ struct FwdParams {
     int off;        // Nk - Nq (causal alignment)
     float c;        // scale * log2(e)
     uint32_t slot;  // work-queue slot of this launch
+    int d_act;      // the tensors' head dim (<= D; the tiles' columns past it are zeros)
     FwdSplit split; // tail split (fwd_sched.h)
     float* partial; // per-piece partial results of split units (NULL if none)
 };
@@ -519,10 +520,12 @@ __device__ __forceinline__ void softmax_tile(uint32_t (&sr)[128], int lim, int j
 template <bool OUT_F32>
 __device__ __forceinline__ void store_o_cols(const float (&v)[32], int cc, uint8_t* stg,
                                              uint32_t& epi_buf, int lane, const CUtensorMap* to,
-                                             int row0, int bh) {
+                                             int row0, int bh, int d_act) {
     constexpr int kCols = kEpiCols(OUT_F32);
 #pragma unroll
     for (int h = 0; h < 32 / kCols; ++h) {
+        if (cc + h * kCols >= d_act) break;  // columns past the head dim (a box that
+                                             // crosses it is clipped by the hardware)
         uint8_t* buf = stg + (epi_buf & 1) * 2048;
         if (lane == 0) bulk_wait_group_read<1>();  // this buffer's previous store has read it
         __syncwarp();
@@ -561,7 +564,7 @@ __device__ __noinline__ void split_piece_epilogue(unsigned int* merge_count, flo
                                                   uint32_t tO, float m, float l, float lx,
                                                   uint8_t* stg, uint32_t* epi_buf,
                                                   const CUtensorMap* to, int row0, int bh,
-                                                  float* lse_out) {
+                                                  float* lse_out, int d_act) {
     const float inv_l = 1.0f / l;
     float* blocks = partial + (size_t)cell * parts * partial_block_floats<D>();
     float* mine = blocks + (size_t)part * partial_block_floats<D>();
@@ -653,7 +656,7 @@ __device__ __noinline__ void split_piece_epilogue(unsigned int* merge_count, flo
                 for (int i = 0; i < 32; ++i) v[i] = fmaf(wq_, __ldcg(bq + i * 32), v[i]);
             }
         }
-        store_o_cols<OUT_F32>(v, cc, stg, *epi_buf, lane, to, row0, bh);
+        store_o_cols<OUT_F32>(v, cc, stg, *epi_buf, lane, to, row0, bh, d_act);
     }
     if (lse_out) *lse_out = (mmax + log2f(wxsum)) * kLn2;
 }
@@ -735,7 +738,7 @@ __device__ void run_softmax(int t, int wq, int lane, uint8_t* smem, Bars* bars, 
 #pragma unroll
                 for (int i = 0; i < 32; i += 2)
                     f2_split(f2_mul(f2(__uint_as_float(r[i]), __uint_as_float(r[i + 1])), il2), v[i], v[i + 1]);
-                store_o_cols<OUT_F32>(v, cc, stg, epi_buf, lane, to, row0, bh);
+                store_o_cols<OUT_F32>(v, cc, stg, epi_buf, lane, to, row0, bh, p.d_act);
             }
             if (live && lse_ptr) lse_ptr[row_idx] = (m + log2f(lx)) * kLn2;
             continue;
@@ -744,7 +747,7 @@ __device__ void run_softmax(int t, int wq, int lane, uint8_t* smem, Bars* bars, 
         const uint32_t cell = w.cell + (uint32_t)t * 4u + (uint32_t)wq;
         split_piece_epilogue<D, OUT_F32>(g_fwd_queue[p.slot] + 2, p.partial, p.split.parts, cell, part,
                                          lane, tO, m, l, lx, stg, &epi_buf, to, row0, bh,
-                                         (live && lse_ptr) ? lse_ptr + row_idx : nullptr);
+                                         (live && lse_ptr) ? lse_ptr + row_idx : nullptr, p.d_act);
     }
     if (lane == 0) bulk_wait_group_all();  // every staged store has completed
     __syncwarp();
@@ -908,6 +911,7 @@ attn_status_t launch_fwd(const void* q, const void* k, const void* v, void* o, f
     p.group = Hq / Hkv;
     p.off = Nk - Nq;
     p.c = scale * kLog2e;
+    p.d_act = d;
     static std::atomic<uint32_t> launches{0};
     p.slot = launches.fetch_add(1u, std::memory_order_relaxed) % kQueueSlots;
     p.split = plan_tail_split(p.shape, dev.num_sms);
@@ -922,10 +926,11 @@ attn_status_t launch_fwd(const void* q, const void* k, const void* v, void* o, f
     if ((st = encode_tmap_bf16_3d(&tv, v, d, Nk, (long long)B * Hkv, kTileN)) != ATTN_OK) return st;
     if ((st = encode_tmap_out_3d(&to, o, f32, d, Nq, (long long)B * Hq, kEpiCols(f32), 32)) != ATTN_OK)
         return st;
-    if (d == 128)
+    // head dims below 64 / 128 run on those kernels (TMA zero-fills the rest)
+    if (pad_head_dim(d) == 128)
         return f32 ? launch_with_partials<128, true>(tq, tk, tv, to, lse, p, grid, stream, dev)
                    : launch_with_partials<128, false>(tq, tk, tv, to, lse, p, grid, stream, dev);
-    if (d == 64)
+    if (pad_head_dim(d) == 64)
         return f32 ? launch_with_partials<64, true>(tq, tk, tv, to, lse, p, grid, stream, dev)
                    : launch_with_partials<64, false>(tq, tk, tv, to, lse, p, grid, stream, dev);
     return ATTN_ERR_UNSUPPORTED;

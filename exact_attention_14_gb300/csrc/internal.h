@@ -8,6 +8,12 @@
 
 namespace gb300 {
 
+// Head dims d in [8, 128], multiples of 8, run on the kernels built for 64 or
+// 128 columns: TMA fills the columns past d with zeros on load (they add
+// nothing to Q K^T and give zero O columns), and stores skip them.
+inline int pad_head_dim(int d) { return d <= 64 ? 64 : 128; }
+inline bool head_dim_supported(int d) { return d >= 8 && d <= 128 && d % 8 == 0; }
+
 struct DeviceInfo {
     int device;
     int num_sms;

@@ -133,3 +133,15 @@ def test_bwd_repeatable():
     b = _run(q, k, v, do, True, 1 / math.sqrt(128))
     for x, y in zip(a, b):
         assert np.array_equal(x, y)
+
+
+@pytest.mark.parametrize("d,causal", [(48, True), (96, False), (96, True)])
+def test_bwd_head_dims_padded(d, causal):
+    q, k, v = make_fwd_inputs(2, 4, 2, 300, 300, d, seed=700 + d)
+    do = _dout(q.shape, seed=701)
+    scale = 1 / math.sqrt(d)
+    dq, dk, dv = _run(q, k, v, do, causal, scale)
+    rq, rk, rv = oracle.attention_bwd(q, k, v, do, causal=causal, scale=scale)
+    _check(dq, rq, f"dQ d={d}")
+    _check(dk, rk, f"dK d={d}")
+    _check(dv, rv, f"dV d={d}")

@@ -152,3 +152,15 @@ def test_split_merge_is_repeatable():
     torch.cuda.synchronize()
     for o, lse in outs[1:]:
         assert torch.equal(o, outs[0][0]) and torch.equal(lse, outs[0][1])
+
+
+@pytest.mark.parametrize("d", [32, 80, 96])
+def test_decode_head_dims_padded(d):
+    q, kc, vc, sl = make_decode_inputs(3, 8, 2, 2000, d, seed=70 + d, len_lo=1, len_hi=2000)
+    for ns in (0, 5):
+        o, lse = gpu_decode(q, kc, vc, sl, num_splits=ns)
+        o_ref, lse_ref = oracle.decode(q, kc, vc, sl)
+        assert_close(o, lse, o_ref, lse_ref, f"d={d} splits={ns}")
+    pad = 64 if d <= 64 else 128
+    assert ea.attn_decode_workspace_size(3, 8, 2, 2000, d, 5) == \
+        ea.attn_decode_workspace_size(3, 8, 2, 2000, pad, 5)

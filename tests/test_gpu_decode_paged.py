@@ -64,3 +64,16 @@ def test_paged_matches_oracle_and_ignores_nan():
     o_ref, lse_ref = oracle.decode(q, kc, vc, sl)
     assert np.abs(o - o_ref).max() <= MAX_ABS_O
     assert np.abs(lse - lse_ref).max() <= MAX_ABS_LSE
+
+
+def test_paged_head_dim_96():
+    q, kc, vc, sl = make_decode_inputs(2, 8, 2, 1024, 96, seed=55, len_lo=1, len_hi=1024)
+    kp, table = _to_pages(kc, 128, seed=56)
+    vp, _ = _to_pages(vc, 128, seed=56)
+    o1, l1 = ea.decode(q.cuda(), kc.cuda(), vc.cuda(), sl.cuda(), out_dtype=torch.float32)
+    o2, l2 = ea.decode_paged(q.cuda(), kp.cuda(), vp.cuda(), table.cuda(), sl.cuda(),
+                             out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    o_ref, lse_ref = oracle.decode(q, kc, vc, sl)
+    assert np.abs(o2.cpu().double().numpy() - o_ref).max() <= MAX_ABS_O

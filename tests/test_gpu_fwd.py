@@ -266,3 +266,28 @@ def test_row_max_jumps_late(causal):
     o, lse = gpu_fwd(q, k, v, causal, 1 / math.sqrt(128))
     o_ref, lse_ref = oracle.attention(q, k, v, causal=causal)
     assert_close(o, lse, o_ref, lse_ref, f"late max, causal={causal}")
+
+
+# ------------------------------ other head dims ------------------------------
+@pytest.mark.parametrize("d,causal", [(32, True), (48, False), (80, True), (96, False),
+                                      (96, True), (120, True)])
+def test_head_dims_padded(d, causal):
+    """Head dims below 64 / 128 run on those kernels: the loads zero-fill the
+    columns past d and the stores skip them."""
+    q, k, v = make_fwd_inputs(2, 4, 2, 300, 300, d, seed=500 + d)
+    scale = 1 / math.sqrt(d)
+    o, lse = gpu_fwd(q, k, v, causal, scale)
+    o_ref, lse_ref = oracle.attention(q, k, v, causal=causal, scale=scale)
+    assert_close(o, lse, o_ref, lse_ref, f"d={d} causal={causal}")
+    ob, _ = gpu_fwd(q, k, v, causal, scale, out_dtype=torch.bfloat16, with_lse=False)
+    assert_close_bf16(ob, o_ref, f"bf16 out d={d}")
+
+
+def test_head_dim_96_split_tail():
+    """d = 96 through the tail split (the merge's stores also stop at d)."""
+    q, k, v = make_fwd_inputs(1, 8, 8, 100, 2048, 96, seed=601)
+    n_full, n_split, parts = ea.attn_fwd_split_plan(1, 8, 8, 100, 2048, 96, False, _num_sms())
+    assert n_split > 0
+    o, lse = gpu_fwd(q, k, v, False, 1 / math.sqrt(96))
+    o_ref, lse_ref = oracle.attention(q, k, v, causal=False)
+    assert_close(o, lse, o_ref, lse_ref, "d=96 split")

@@ -59,7 +59,7 @@ def fwd(lib, **kw):
     (dict(B=0), 1), (dict(Hq=3, Hkv=2), 1), (dict(Nq=0), 1), (dict(Nk=0), 1),
     (dict(Nq=(1 << 24) + 1), 1), (dict(causal=2), 1), (dict(causal=1, Nq=9, Nk=8), 1),
     (dict(scale=-1.0), 1), (dict(scale=float("nan")), 1), (dict(scale=float("inf")), 1),
-    (dict(odt=7), 1), (dict(d=96), 2), (dict(d=256), 2), (dict(d=0), 1),
+    (dict(odt=7), 1), (dict(d=100), 2), (dict(d=136), 2), (dict(d=256), 2), (dict(d=0), 1),
 ])
 def test_fwd_argument_checks(lib, kw, code):
     assert fwd(lib, **kw) == code
@@ -77,7 +77,7 @@ def dec(lib, **kw):
 @pytest.mark.parametrize("kw,code", [
     (dict(q=None), 1), (dict(sl=None), 1), (dict(sl=FAKE + 2), 1), (dict(v=FAKE + 4), 1),
     (dict(Hq=9), 1), (dict(Nmax=0), 1), (dict(ns=-1), 1), (dict(scale=-0.5), 1),
-    (dict(d=80), 2), (dict(Hq=34, Hkv=2), 2),
+    (dict(d=84), 2), (dict(d=192), 2), (dict(Hq=34, Hkv=2), 2),
 ])
 def test_decode_argument_checks(lib, kw, code):
     assert dec(lib, **kw) == code
@@ -253,7 +253,8 @@ def test_bwd_workspace_size_and_argument_checks(lib):
     # two fp32 row vectors (D, lse2) over rows padded to 128
     assert ea.attn_bwd_workspace_size(2, 8, 2, 300, 300, 128) == 8 * 2 * 8 * 384
     assert ea.attn_bwd_workspace_size(1, 4, 3, 128, 128, 64) == 0      # Hq % Hkv
-    assert ea.attn_bwd_workspace_size(1, 4, 4, 128, 128, 96) == 0      # unsupported d
+    assert ea.attn_bwd_workspace_size(1, 4, 4, 128, 128, 100) == 0     # unsupported d
+    assert ea.attn_bwd_workspace_size(1, 4, 4, 128, 128, 96) > 0       # padded to 128
     fake = ctypes.c_void_p(0x10000)
     args = [fake] * 9 + [1, 2, 2, 128, 128, 128, 0, ctypes.c_float(0.1), 0, 0, fake, 1 << 30, None]
     bad = list(args)
@@ -263,7 +264,7 @@ def test_bwd_workspace_size_and_argument_checks(lib):
     bad[20] = 16                                                       # workspace too small
     assert lib.attn_bwd(*bad) == ea.ATTN_ERR_WORKSPACE
     bad = list(args)
-    bad[14] = 96                                                       # d
+    bad[14] = 100                                                      # d (not a multiple of 8)
     assert lib.attn_bwd(*bad) == ea.ATTN_ERR_UNSUPPORTED
     bad = list(args)
     bad[15] = 1
@@ -287,5 +288,16 @@ def test_decode_paged_argument_checks(lib):
     bad[10] = 0                                                        # no blocks
     assert lib.attn_decode_paged(*bad) == ea.ATTN_ERR_INVALID_ARG
     bad = list(args)
-    bad[13] = 96                                                       # d
+    bad[13] = 192                                                      # d above 128
     assert lib.attn_decode_paged(*bad) == ea.ATTN_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("d,ok", [(8, True), (32, True), (48, True), (80, True), (96, True),
+                                  (120, True), (128, True), (4, False), (100, False), (136, False),
+                                  (192, False), (256, False)])
+def test_supported_head_dims(lib, d, ok):
+    """Head dims in [8, 128] that are multiples of 8 run on the 64- or 128-column
+    kernels (zero-filled columns); others are rejected (size 0)."""
+    assert (ea.attn_bwd_workspace_size(2, 8, 2, 1000, 1000, d) > 0) == ok
+    rc = fwd(lib, d=d)
+    assert rc == (ea.ATTN_ERR_CUDA if ok else ea.ATTN_ERR_UNSUPPORTED) or (ok and rc == ea.ATTN_OK)
