@@ -184,8 +184,8 @@ def run_reference(args, rank, world):
 
 def run_ours(args, rank, world, local_rank):
     import exact_attention_14_gb300 as ea
-    from exact_attention_14_gb300.inputs import DECODE, PREFILL, make_config_inputs, \
-        make_decode_config_inputs
+    from exact_attention_14_gb300.inputs import DECODE, PREFILL, VARLEN, make_config_inputs, \
+        make_decode_config_inputs, make_varlen_inputs, varlen_lengths
 
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
@@ -332,6 +332,44 @@ def run_ours(args, rank, world, local_rank):
                "frac_of_bf16_peak": (fb_nc + fb_c) / (tb_nc + tb_c) / 1e12 / peaks["bf16_tflops"],
                "flops_note": "2.5 x the forward formula (S, dP, dV, dK, dQ products)"}
 
+    # Packed variable-length prefill (a follow-on row, timed apart from the
+    # step): 16 causal sequences of U[256, 4096] tokens in one attn_fwd_varlen.
+    varlen = None
+    if not args.no_varlen:
+        vc = VARLEN
+        lens = varlen_lengths(vc.n_seqs, vc.len_lo, vc.len_hi, vc.seed)
+        vq, vk, vv, vcq, vck = (t.to(dev) for t in make_varlen_inputs(lens, lens, vc.Hq, vc.Hkv,
+                                                                       vc.d, vc.seed))
+        vo = torch.empty(vq.shape, dtype=torch.bfloat16, device=dev)
+        vl = torch.empty((vc.Hq, vq.shape[0]), dtype=torch.float32, device=dev)
+
+        def varlen_step():
+            ea.attn_fwd_varlen(vq, vk, vv, vo, vcq, vck, max(lens), max(lens), vl,
+                               causal=vc.causal, scale=vc.scale, stream=stream)
+
+        for _ in range(args.warmup):
+            flush.zero_()
+            varlen_step()
+        vev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+        torch.cuda.synchronize()
+        for i in range(args.steps):
+            flush.zero_()
+            vev[i][0].record(stream)
+            varlen_step()
+            vev[i][1].record(stream)
+        torch.cuda.synchronize()
+        if ea.attn_last_device_error() != 0:
+            raise RuntimeError("device error in the varlen leg")
+        tv = sum(e[0].elapsed_time(e[1]) for e in vev) / args.steps * 1e-3
+        fv = sum(4.0 * vc.Hq * n * n * vc.d / (2 if vc.causal else 1) for n in lens)
+        varlen = {"kernel": "attn_fwd_kernel (packed, ragged tensor maps)",
+                  "workload": f"{vc.n_seqs} sequences U[{vc.len_lo},{vc.len_hi}] "
+                              f"(total {sum(lens)} tokens, max {max(lens)}) Hq={vc.Hq} "
+                              f"Hkv={vc.Hkv} d={vc.d} causal={vc.causal}",
+                  "tflops": fv / tv / 1e12, "ms": 1e3 * tv,
+                  "frac_of_bf16_peak": fv / tv / 1e12 / peaks["bf16_tflops"],
+                  "flops_note": "sum over sequences of the forward formula 4*H*L^2*d (/2 causal)"}
+
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         tf, desc, cores, _ = oracle_sample(args.cpu_seconds)
@@ -372,7 +410,7 @@ def run_ours(args, rank, world, local_rank):
         "decode": {"value": dec_gbs, "unit": "GB/s", "ms": 1e3 * t_dec,
                    "algorithmic_bytes": dec_bytes, "frac_of_hbm": dec_gbs / world / peaks["hbm_gbs"],
                    "sum_seqlen": sum_len},
-        "roofline": roof, "roofline_decode": roof_dec, "bwd": bwd,
+        "roofline": roof, "roofline_decode": roof_dec, "bwd": bwd, "varlen": varlen,
         "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": (2 + ea.attn_decode_kernel_launches(DECODE.B, DECODE.Hq, DECODE.Hkv,
                                                             DECODE.Nmax, DECODE.d)) * args.steps,
@@ -390,6 +428,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-bwd", action="store_true", help="skip the backward leg")
+    ap.add_argument("--no-varlen", action="store_true", help="skip the packed varlen leg")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))

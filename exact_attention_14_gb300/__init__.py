@@ -1,4 +1,5 @@
-"""GB300 (sm_103a) exact attention: fused forward and split-KV decode.
+"""GB300 (sm_103a) exact attention: fused forward (dense and packed
+variable-length), backward, and split-KV decode (contiguous or paged cache).
 
 Thin ctypes binding over the C ABI in ``include/attn.h`` (library
 ``libgb300_attn.so`` built in-tree by ``_build.build()``).  The functions here
@@ -15,7 +16,8 @@ import ctypes
 import os
 
 __all__ = [
-    "ATTN_OUT_BF16", "ATTN_OUT_F32", "AttnError", "attn_fwd", "attn_decode",
+    "ATTN_OUT_BF16", "ATTN_OUT_F32", "AttnError", "attn_fwd", "attn_fwd_varlen", "forward_varlen",
+    "attn_decode",
     "attn_decode_workspace_size", "attn_decode_noalloc", "attn_status_string", "attn_last_device_error",
     "attn_decode_num_splits", "attn_list_schedule", "attn_kv_tiles",
     "attn_fwd_num_units", "attn_fwd_schedule", "attn_fwd_split_plan", "attn_decode_kernel_launches",
@@ -40,6 +42,7 @@ _c_int, _c_ll, _c_sz, _c_f, _vp = (ctypes.c_int, ctypes.c_longlong, ctypes.c_siz
 SIGNATURES = {
     "attn_fwd": (_c_int, [_vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int,
                           _c_int, _c_int, _c_f, _c_int, _vp]),
+    "attn_fwd_varlen": (_c_int, [_vp] * 7 + [_c_int] * 9 + [_c_f, _c_int, _vp]),
     "attn_decode_workspace_size": (_c_sz, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_int]),
     "attn_decode": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int,
                              _c_int, _c_f, _c_int, _vp, _c_sz, _c_int, _vp]),
@@ -160,6 +163,59 @@ def attn_fwd(q, k, v, o, lse=None, *, causal: bool = False, scale: float | None 
                          int(bool(causal)), float(scale), odt, _stream_ptr(stream))
     _check(rc, "attn_fwd")
     return o, lse
+
+
+def attn_fwd_varlen(q, k, v, o, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int,
+                    max_seqlen_k: int, lse=None, *, causal: bool = False,
+                    scale: float | None = None, stream=None):
+    """Packed variable-length forward into caller-provided outputs.
+
+    q [total_q,Hq,d] bf16; k, v [total_k,Hkv,d] bf16; o [total_q,Hq,d] bf16 or
+    fp32; cu_seqlens_q / cu_seqlens_k int32 [B+1] on the device (sequence b is
+    rows cu[b]..cu[b+1]); lse [Hq,total_q] fp32 or None.  Asynchronous."""
+    import torch
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, torch.bfloat16, n)
+    for t, n in ((cu_seqlens_q, "cu_seqlens_q"), (cu_seqlens_k, "cu_seqlens_k")):
+        _need(t, torch.int32, n)
+    if o.dtype not in (torch.bfloat16, torch.float32):
+        raise TypeError("o must be bfloat16 or float32")
+    _need(o, o.dtype, "o")
+    if lse is not None:
+        _need(lse, torch.float32, "lse")
+    total_q, Hq, d = q.shape
+    total_k, Hkv = k.shape[0], k.shape[1]
+    if tuple(k.shape) != (total_k, Hkv, d) or tuple(v.shape) != tuple(k.shape):
+        raise ValueError("k/v shape mismatch")
+    if tuple(o.shape) != tuple(q.shape):
+        raise ValueError("o shape mismatch")
+    B = cu_seqlens_q.numel() - 1
+    if cu_seqlens_k.numel() != B + 1 or B < 1:
+        raise ValueError("cu_seqlens_q / cu_seqlens_k must both have B + 1 entries")
+    if lse is not None and tuple(lse.shape) != (Hq, total_q):
+        raise ValueError("lse shape mismatch")
+    if scale is None:
+        scale = d ** -0.5
+    odt = ATTN_OUT_F32 if o.dtype == torch.float32 else ATTN_OUT_BF16
+    rc = load().attn_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
+                                _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), B, Hq, Hkv, total_q,
+                                total_k, int(max_seqlen_q), int(max_seqlen_k), d,
+                                int(bool(causal)), float(scale), odt, _stream_ptr(stream))
+    _check(rc, "attn_fwd_varlen")
+    return o, lse
+
+
+def forward_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, max_seqlen_k: int,
+                   *, causal: bool = False, scale: float | None = None, out_dtype=None,
+                   return_lse: bool = True, stream=None):
+    """Allocate O (and LSE [Hq, total_q]) with torch and run attn_fwd_varlen."""
+    import torch
+    out_dtype = out_dtype or torch.bfloat16
+    o = torch.empty(q.shape, dtype=out_dtype, device=q.device)
+    lse = (torch.empty((q.shape[1], q.shape[0]), dtype=torch.float32, device=q.device)
+           if return_lse else None)
+    return attn_fwd_varlen(q, k, v, o, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k,
+                           lse, causal=causal, scale=scale, stream=stream)
 
 
 def attn_bwd_workspace_size(B: int, Hq: int, Hkv: int, Nq: int, Nk: int, d: int) -> int:

@@ -26,6 +26,7 @@ namespace {
 constexpr int kMaxDevices = 64;
 constexpr long long kMaxLen = 1ll << 24;
 constexpr long long kMaxHeads = 1ll << 24;
+constexpr int kMaxPackedRows = 1 << 30;  // rows of a packed batch (ragged maps, fwd_sched.h)
 
 struct DevState {
     bool ready;
@@ -124,6 +125,26 @@ attn_status_t encode_tmap_f32_sw128_3d(CUtensorMap* map, void* base, int d, int 
     return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
+attn_status_t encode_tmap_ragged(CUtensorMap* map, const void* base, bool f32, int d, int heads,
+                                 int box_cols, int box_rows, bool swizzle128) {
+    if (!load_encoder()) return ATTN_ERR_CUDA;
+    const cuuint64_t es = f32 ? 4 : 2;
+    const cuuint64_t rs = (cuuint64_t)heads * d * es;  // row stride (bytes)
+    if (rs >= (1ull << 34)) return ATTN_ERR_UNSUPPORTED;
+    cuuint64_t dims[5] = {(cuuint64_t)d, (cuuint64_t)heads, (cuuint64_t)kRaggedWindow,
+                          (cuuint64_t)kRaggedOuterExtent, (cuuint64_t)kRaggedOuterExtent};
+    cuuint64_t strides[4] = {(cuuint64_t)d * es, rs, rs, (1ull << 34) - rs};
+    cuuint32_t box[5] = {(cuuint32_t)box_cols, 1u, (cuuint32_t)box_rows, 1u, 1u};
+    cuuint32_t elem[5] = {1u, 1u, 1u, 1u, 1u};
+    CUresult r = g_encode(map, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                          5, const_cast<void*>(base), dims, strides, box, elem,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                          swizzle128 ? CU_TENSOR_MAP_L2_PROMOTION_L2_256B : CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
 attn_status_t encode_tmap_bf16_3d(CUtensorMap* map, const void* base, int d, int rows,
                                   long long heads, int box_rows) {
     if (!load_encoder()) return ATTN_ERR_CUDA;
@@ -203,6 +224,28 @@ attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, flo
     if ((st = current_device_info(&dev)) != ATTN_OK) return st;
     return launch_fwd(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, d, causal, scale, o_dtype,
                       static_cast<cudaStream_t>(stream), dev);
+}
+
+attn_status_t attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                              const int* cu_seqlens_q, const int* cu_seqlens_k, int B, int Hq,
+                              int Hkv, int total_q, int total_k, int max_seqlen_q,
+                              int max_seqlen_k, int d, int causal, float scale,
+                              attn_out_dtype_t o_dtype, void* stream) {
+    if (!cu_seqlens_q || !cu_seqlens_k || !aligned4(cu_seqlens_q) || !aligned4(cu_seqlens_k))
+        return ATTN_ERR_INVALID_ARG;
+    if (total_q < 1 || total_k < 1 || total_q > kMaxPackedRows || total_k > kMaxPackedRows)
+        return ATTN_ERR_INVALID_ARG;
+    if (max_seqlen_q > total_q || max_seqlen_k > total_k) return ATTN_ERR_INVALID_ARG;
+    // (the per-sequence causal condition is checked on the device)
+    attn_status_t st = check_fwd(q, k, v, o, lse, B, Hq, Hkv, max_seqlen_q, max_seqlen_k, d, 0,
+                                 scale, o_dtype);
+    if (st != ATTN_OK) return st;
+    if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
+    DeviceInfo dev;
+    if ((st = current_device_info(&dev)) != ATTN_OK) return st;
+    return launch_fwd_varlen(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, B, Hq, Hkv, total_q,
+                             total_k, max_seqlen_q, max_seqlen_k, d, causal, scale, o_dtype,
+                             static_cast<cudaStream_t>(stream), dev);
 }
 
 size_t attn_bwd_workspace_size(int B, int Hq, int Hkv, int Nq, int Nk, int d) {

@@ -93,6 +93,10 @@ struct FwdParams {
     int d_act;      // the tensors' head dim (<= D; the tiles' columns past it are zeros)
     FwdSplit split; // tail split (fwd_sched.h)
     float* partial; // per-piece partial results of split units (NULL if none)
+    // packed variable-length batches (shape.Nq / Nk are then the maximum lengths)
+    const int* cu_q;  // [B + 1] row offsets of the sequences in the packed Q / O
+    const int* cu_k;  // [B + 1] row offsets in the packed K / V
+    int total_q, total_k;
 };
 
 // Work queues.  Per slot: word 0 the ticket counter (the next work item),
@@ -125,7 +129,9 @@ struct WorkItem {
     int e[2];       // end KV tile (exclusive) of Q tile 0 and 1 (<= j0: no work)
     int part;       // piece of a split unit, -1 for a whole unit
     uint32_t cell;  // split units: 8 * (unit - n_full), the unit's first merge cell
-    int pad;
+    int q0, k0;     // packed batches: first Q / K row of the sequence
+    int nq, nk;     // packed batches: the sequence's query and key counts
+    int pad[2];
 };
 
 struct __align__(8) Bars {
@@ -148,6 +154,7 @@ template struct BarsFit<128>;
 
 // Consumer side of the work-item hand-off (whole warp): the k-th item this
 // warp takes.  Returns false on abort.
+template <bool VARLEN>
 __device__ __forceinline__ bool take_item(Bars* bars, uint32_t k, WorkItem& w,
                                           const volatile int* abort_flag) {
     const uint32_t i = k & 1u;
@@ -161,6 +168,11 @@ __device__ __forceinline__ bool take_item(Bars* bars, uint32_t k, WorkItem& w,
     w.e[1] = src->e[1];
     w.part = src->part;
     w.cell = src->cell;
+    if constexpr (VARLEN) {
+        w.q0 = src->q0;
+        w.nq = src->nq;
+        w.nk = src->nk;
+    }
     __syncwarp();
     if ((threadIdx.x & 31) == 0) mbar_arrive(smem_u32(&bars->unit_empty[i]));
     return true;
@@ -174,7 +186,24 @@ __device__ __forceinline__ void raise_abort(Bars* bars, unsigned int* err) {
 // ---------------------------------------------------------------------------
 // Producer: TMA loads
 // ---------------------------------------------------------------------------
-template <int D>
+// Sequence b of a packed batch: its first rows and lengths.  False (and the
+// error bit, from the leader) when its offsets leave the arrays, decrease, or
+// give a length above the launch's maximum, a query row without keys (nk = 0),
+// or, causal, more queries than keys; such a sequence is not computed.  Every
+// copy of a valid sequence stays inside [q0, q0 + nq) and [k0, k0 + nk).
+__device__ __forceinline__ bool varlen_seq(const FwdParams& p, int b, bool leader, int& q0,
+                                           int& nq, int& k0, int& nk, unsigned int* err) {
+    const int qs = __ldg(p.cu_q + b), qe = __ldg(p.cu_q + b + 1);
+    const int ks = __ldg(p.cu_k + b), ke = __ldg(p.cu_k + b + 1);
+    const bool good = 0 <= qs && qs <= qe && qe <= p.total_q && qe - qs <= p.shape.Nq &&
+                      0 <= ks && ks <= ke && ke <= p.total_k && ke - ks <= p.shape.Nk &&
+                      (qe == qs || ke > ks) && (!p.shape.causal || qe - qs <= ke - ks);
+    q0 = qs; nq = qe - qs; k0 = ks; nk = ke - ks;
+    if (!good && leader) atomicOr(err, kErrBadSeqlen);
+    return good;
+}
+
+template <int D, bool VARLEN>
 __device__ void run_producer(const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv,
                              uint8_t* smem, Bars* bars, const FwdParams& p, unsigned int* err) {
     // Run by a whole warp so that every loop value is warp-uniform; one elected
@@ -188,6 +217,7 @@ __device__ void run_producer(const CUtensorMap* tq, const CUtensorMap* tk, const
     uint32_t q_issued[2] = {0u, 0u};
     long long L = 0;  // K/V loads issued
     bool ok = true;
+    bool first = true;
     for (int local = 0; ok; ++local) {
         // Take the next unit and publish it (a value >= units ends the loop
         // of every role).
@@ -198,19 +228,34 @@ __device__ void run_producer(const CUtensorMap* tq, const CUtensorMap* tk, const
         if (!ok) break;
         // A CTA's first item is its own index (no atomic on the launch's
         // critical path); later ones come from the counter, after the grid.
-        uint32_t u = blockIdx.x;
-        if (local > 0) {
-            if (leader) u = gridDim.x + atomicAdd(&queue[0], 1u);
-            u = __shfl_sync(0xFFFFFFFFu, u, leader_lane);
-        }
-        const bool done = u >= split_items(p.split);
+        // Packed batches skip the items past their sequence's last query row.
         uint32_t unit = 0;
         int part = -1, bh = -1, mb = 0, j0 = 0, j1 = 0, n0 = 0, n1 = 0;
-        if (!done) {
+        int q0 = 0, k0 = 0, nq = s.Nq, nk = s.Nk;
+        bool done = false;
+        while (true) {
+            uint32_t u = blockIdx.x;
+            if (!first) {
+                if (leader) u = gridDim.x + atomicAdd(&queue[0], 1u);
+                u = __shfl_sync(0xFFFFFFFFu, u, leader_lane);
+            }
+            first = false;
+            done = u >= split_items(p.split);
+            if (done) {
+                bh = -1;  // the end marker (a skipped item may have set bh)
+                break;
+            }
             item_of(p.split, u, unit, part);
             unit_of(s, unit, bh, mb);
-            n0 = tile_kv_count(mb, 0, s);
-            n1 = tile_kv_count(mb, 1, s);
+            if constexpr (VARLEN) {
+                if (!varlen_seq(p, bh / s.Hq, leader, q0, nq, k0, nk, err)) continue;
+                if (mb * kUnitRows >= nq) continue;
+            }
+            break;
+        }
+        if (!done) {
+            n0 = tile_kv_count_len(mb, 0, nq, nk, s.causal);
+            n1 = tile_kv_count_len(mb, 1, nq, nk, s.causal);
             part_range(n0 > n1 ? n0 : n1, p.split.parts, part, j0, j1);
         }
         if (leader) {
@@ -222,6 +267,10 @@ __device__ void run_producer(const CUtensorMap* tq, const CUtensorMap* tk, const
             dst->e[1] = n1 < j1 ? n1 : j1;
             dst->part = part;
             dst->cell = (unit - (uint32_t)p.split.n_full) * 8u;
+            dst->q0 = q0;
+            dst->k0 = k0;
+            dst->nq = nq;
+            dst->nk = nk;
             mbar_arrive(smem_u32(&bars->unit_full[hs]));
         }
         __syncwarp();
@@ -237,9 +286,15 @@ __device__ void run_producer(const CUtensorMap* tq, const CUtensorMap* tk, const
                 const uint32_t bar = smem_u32(&bars->q_full[t]);
                 mbar_arrive_expect_tx(bar, C::kTileBytes);
                 const uint32_t dst = smem_u32(smem + t * C::kTileBytes);
+                const int row = mb * kUnitRows + t * kTileM;
 #pragma unroll
-                for (int c = 0; c < D / 64; ++c)
-                    tma_load_3d(dst + c * 16384, tq, bar, 64 * c, mb * kUnitRows + t * kTileM, bh);
+                for (int c = 0; c < D / 64; ++c) {
+                    if constexpr (VARLEN)
+                        tma_load_5d(dst + c * 16384, tq, bar, 64 * c, hq, kRaggedWindow - nq + row,
+                                    q0 + nq, kRaggedWindow);
+                    else
+                        tma_load_3d(dst + c * 16384, tq, bar, 64 * c, row, bh);
+                }
             }
             __syncwarp();
             ++q_issued[t];
@@ -259,8 +314,13 @@ __device__ void run_producer(const CUtensorMap* tq, const CUtensorMap* tk, const
                     const uint32_t dst = smem_u32(smem + C::kRingOff + slot * C::kTileBytes);
                     const CUtensorMap* map = which == 0 ? tk : tv;
 #pragma unroll
-                    for (int c = 0; c < D / 64; ++c)
-                        tma_load_3d(dst + c * 16384, map, bar, 64 * c, kTileN * j, bkv);
+                    for (int c = 0; c < D / 64; ++c) {
+                        if constexpr (VARLEN)
+                            tma_load_5d(dst + c * 16384, map, bar, 64 * c, hq / p.group,
+                                        kRaggedWindow - nk + kTileN * j, k0 + nk, kRaggedWindow);
+                        else
+                            tma_load_3d(dst + c * 16384, map, bar, 64 * c, kTileN * j, bkv);
+                    }
                 }
                 __syncwarp();
                 ++L;
@@ -350,7 +410,7 @@ __device__ void run_mma(uint8_t* smem, Bars* bars, uint32_t tmem, const FwdParam
     bool ok = true;
     for (int local = 0; ok; ++local) {
         WorkItem w;
-        ok = take_item(bars, (uint32_t)local, w, abort_flag);
+        ok = take_item<false>(bars, (uint32_t)local, w, abort_flag);
         if (!ok || w.bh < 0) break;
         // this item's KV tiles: [j0, j1) overall, [j0, n[t]) for tile t
         const int n[2] = {w.e[0], w.e[1]};
@@ -517,10 +577,12 @@ __device__ __forceinline__ void softmax_tile(uint32_t (&sr)[128], int lim, int j
 // staged 32 rows x 64 bytes at a time in shared memory (two buffers per warp)
 // and written by TMA stores (rows past Nq are clipped by the hardware), so the
 // warp does not wait for the global writes.
-template <bool OUT_F32>
+// Coordinates: dense (row0, bh); packed batches (row0 = the ragged r of the
+// warp's first row, bh = the query head, e = the ragged e; fwd_sched.h).
+template <bool OUT_F32, bool VARLEN>
 __device__ __forceinline__ void store_o_cols(const float (&v)[32], int cc, uint8_t* stg,
                                              uint32_t& epi_buf, int lane, const CUtensorMap* to,
-                                             int row0, int bh, int d_act) {
+                                             int row0, int bh, int e, int d_act) {
     constexpr int kCols = kEpiCols(OUT_F32);
 #pragma unroll
     for (int h = 0; h < 32 / kCols; ++h) {
@@ -544,7 +606,10 @@ __device__ __forceinline__ void store_o_cols(const float (&v)[32], int cc, uint8
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-            tma_store_3d(to, smem_u32(buf), cc + h * kCols, row0, bh);
+            if constexpr (VARLEN)
+                tma_store_5d(to, smem_u32(buf), cc + h * kCols, bh, row0, e, kRaggedWindow);
+            else
+                tma_store_3d(to, smem_u32(buf), cc + h * kCols, row0, bh);
             bulk_commit_group();
         }
         ++epi_buf;
@@ -656,12 +721,12 @@ __device__ __noinline__ void split_piece_epilogue(unsigned int* merge_count, flo
                 for (int i = 0; i < 32; ++i) v[i] = fmaf(wq_, __ldcg(bq + i * 32), v[i]);
             }
         }
-        store_o_cols<OUT_F32>(v, cc, stg, *epi_buf, lane, to, row0, bh, d_act);
+        store_o_cols<OUT_F32, false>(v, cc, stg, *epi_buf, lane, to, row0, bh, 0, d_act);
     }
     if (lse_out) *lse_out = (mmax + log2f(wxsum)) * kLn2;
 }
 
-template <int D, bool OUT_F32>
+template <int D, bool OUT_F32, bool VARLEN>
 __device__ void run_softmax(int t, int wq, int lane, uint8_t* smem, Bars* bars, uint32_t tmem,
                             const FwdParams& p, const CUtensorMap* to, float* __restrict__ lse_ptr,
                             unsigned int* err) {
@@ -681,16 +746,18 @@ __device__ void run_softmax(int t, int wq, int lane, uint8_t* smem, Bars* bars, 
     bool ok = true;
     for (uint32_t k = 0; ok; ++k) {
         WorkItem w;
-        ok = take_item(bars, k, w, abort_flag);
+        ok = take_item<VARLEN>(bars, k, w, abort_flag);
         if (!ok || w.bh < 0) break;
         const int bh = w.bh, mb = w.mb, j0 = w.j0, part = w.part;
         const int n_t = t == 0 ? w.e[0] : w.e[1];
         if (n_t <= j0) continue;
+        const int nq = VARLEN ? w.nq : s.Nq;
+        const int nk = VARLEN ? w.nk : s.Nk;
         const int row = mb * kUnitRows + t * kTileM + wq * 32 + lane;
-        // last allowed key for this row (global index)
-        int last_key = s.Nk - 1;
+        // last allowed key for this row (index within the sequence)
+        int last_key = nk - 1;
         if (s.causal) {
-            const int lk = row + p.off;
+            const int lk = row + (VARLEN ? nk - nq : p.off);
             last_key = lk < last_key ? lk : last_key;
         }
         float m = -INFINITY;  // running max of scaled scores, log2 units
@@ -723,10 +790,19 @@ __device__ void run_softmax(int t, int wq, int lane, uint8_t* smem, Bars* bars, 
         ++cnt_o;
         if (!ok) break;
         tc_fence_after();
-        const bool live = row < s.Nq;
+        const bool live = row < nq;
         const float inv_l = 1.0f / l;
-        const size_t row_idx = (size_t)bh * s.Nq + (size_t)row;
-        const int row0 = mb * kUnitRows + t * kTileM + wq * 32;
+        const int hq = bh - (bh / s.Hq) * s.Hq;
+        // LSE: [B, Hq, Nq], or [Hq, total_q] for packed batches
+        const size_t row_idx = VARLEN ? (size_t)hq * p.total_q + (size_t)(w.q0 + row)
+                                      : (size_t)bh * s.Nq + (size_t)row;
+        int row0 = mb * kUnitRows + t * kTileM + wq * 32;
+        int oz = bh, oe = 0;
+        if constexpr (VARLEN) {
+            row0 += kRaggedWindow - nq;
+            oz = hq;
+            oe = w.q0 + nq;
+        }
         const uint64_t il2 = f2(inv_l, inv_l);
         if (part < 0) {
 #pragma unroll 1
@@ -738,23 +814,25 @@ __device__ void run_softmax(int t, int wq, int lane, uint8_t* smem, Bars* bars, 
 #pragma unroll
                 for (int i = 0; i < 32; i += 2)
                     f2_split(f2_mul(f2(__uint_as_float(r[i]), __uint_as_float(r[i + 1])), il2), v[i], v[i + 1]);
-                store_o_cols<OUT_F32>(v, cc, stg, epi_buf, lane, to, row0, bh, p.d_act);
+                store_o_cols<OUT_F32, VARLEN>(v, cc, stg, epi_buf, lane, to, row0, oz, oe, p.d_act);
             }
             if (live && lse_ptr) lse_ptr[row_idx] = (m + log2f(lx)) * kLn2;
             continue;
         }
-        // (cell: this warp's slot among the split units' merge counters and blocks)
-        const uint32_t cell = w.cell + (uint32_t)t * 4u + (uint32_t)wq;
-        split_piece_epilogue<D, OUT_F32>(g_fwd_queue[p.slot] + 2, p.partial, p.split.parts, cell, part,
-                                         lane, tO, m, l, lx, stg, &epi_buf, to, row0, bh,
-                                         (live && lse_ptr) ? lse_ptr + row_idx : nullptr, p.d_act);
+        if constexpr (!VARLEN) {  // packed batches are never split
+            // (cell: this warp's slot among the split units' merge counters and blocks)
+            const uint32_t cell = w.cell + (uint32_t)t * 4u + (uint32_t)wq;
+            split_piece_epilogue<D, OUT_F32>(g_fwd_queue[p.slot] + 2, p.partial, p.split.parts, cell,
+                                             part, lane, tO, m, l, lx, stg, &epi_buf, to, row0, bh,
+                                             (live && lse_ptr) ? lse_ptr + row_idx : nullptr, p.d_act);
+        }
     }
     if (lane == 0) bulk_wait_group_all();  // every staged store has completed
     __syncwarp();
     if (!ok) raise_abort(bars, err);
 }
 
-template <int D, bool OUT_F32>
+template <int D, bool OUT_F32, bool VARLEN>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                 const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap to,
@@ -802,12 +880,12 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
 
     if (warp < 4) {
         reg_dealloc<kRegsControl>();
-        if (warp == 0) run_producer<D>(&tq, &tk, &tv, smem, bars, p, err);
+        if (warp == 0) run_producer<D, VARLEN>(&tq, &tk, &tv, smem, bars, p, err);
         if (warp == 1) run_mma<D>(smem, bars, tmem, p, err);
     } else {
         reg_alloc<kRegsSoftmax>();
         const int t = (warp - 4) >> 2;
-        run_softmax<D, OUT_F32>(t, warp & 3, lane, smem, bars, tmem, p, &to, lse_ptr, err);
+        run_softmax<D, OUT_F32, VARLEN>(t, warp & 3, lane, smem, bars, tmem, p, &to, lse_ptr, err);
     }
     tc_fence_before();
     __syncthreads();
@@ -833,20 +911,20 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
     }
 }
 
-template <int D, bool OUT_F32>
+template <int D, bool OUT_F32, bool VARLEN = false>
 attn_status_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                            const CUtensorMap& to, float* lse, const FwdParams& p, int grid,
                            cudaStream_t stream, const DeviceInfo& dev) {
     using C = FwdCfg<D>;
     static int attr_set[64] = {0};
     if (dev.device < 64 && !attr_set[dev.device]) {
-        if (cudaFuncSetAttribute(attn_fwd_kernel<D, OUT_F32>,
+        if (cudaFuncSetAttribute(attn_fwd_kernel<D, OUT_F32, VARLEN>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  C::kSmemBytes) != cudaSuccess)
             return ATTN_ERR_CUDA;
         attr_set[dev.device] = 1;
     }
-    attn_fwd_kernel<D, OUT_F32><<<(unsigned)grid, kThreads, C::kSmemBytes, stream>>>(
+    attn_fwd_kernel<D, OUT_F32, VARLEN><<<(unsigned)grid, kThreads, C::kSmemBytes, stream>>>(
         tq, tk, tv, to, lse, p, dev.err_word);
     return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
@@ -900,6 +978,11 @@ attn_status_t launch_with_partials(const CUtensorMap& tq, const CUtensorMap& tk,
     return st;
 }
 
+uint32_t next_queue_slot() {
+    static std::atomic<uint32_t> launches{0};
+    return launches.fetch_add(1u, std::memory_order_relaxed) % kQueueSlots;
+}
+
 }  // namespace
 
 attn_status_t launch_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
@@ -912,9 +995,10 @@ attn_status_t launch_fwd(const void* q, const void* k, const void* v, void* o, f
     p.off = Nk - Nq;
     p.c = scale * kLog2e;
     p.d_act = d;
-    static std::atomic<uint32_t> launches{0};
-    p.slot = launches.fetch_add(1u, std::memory_order_relaxed) % kQueueSlots;
+    p.slot = next_queue_slot();
     p.split = plan_tail_split(p.shape, dev.num_sms);
+    p.cu_q = p.cu_k = nullptr;
+    p.total_q = p.total_k = 0;
     const uint32_t items = split_items(p.split);
     const int grid = (int)(items < (uint32_t)dev.num_sms ? items : (uint32_t)dev.num_sms);
     p.partial = nullptr;
@@ -933,6 +1017,51 @@ attn_status_t launch_fwd(const void* q, const void* k, const void* v, void* o, f
     if (pad_head_dim(d) == 64)
         return f32 ? launch_with_partials<64, true>(tq, tk, tv, to, lse, p, grid, stream, dev)
                    : launch_with_partials<64, false>(tq, tk, tv, to, lse, p, grid, stream, dev);
+    return ATTN_ERR_UNSUPPORTED;
+}
+
+}  // namespace gb300
+
+namespace gb300 {
+
+attn_status_t launch_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                                const int* cu_q, const int* cu_k, int B, int Hq, int Hkv,
+                                int total_q, int total_k, int max_q, int max_k, int d, int causal,
+                                float scale, attn_out_dtype_t o_dtype, cudaStream_t stream,
+                                const DeviceInfo& dev) {
+    FwdParams p;
+    // units cover every sequence at the maximum lengths; the producer skips
+    // the m-blocks past each sequence's own length
+    p.shape = make_fwd_shape(B, Hq, Hkv, max_q, max_k, d, causal);
+    if (p.shape.units >= (1ll << 31)) return ATTN_ERR_UNSUPPORTED;
+    p.group = Hq / Hkv;
+    p.off = 0;
+    p.c = scale * kLog2e;
+    p.d_act = d;
+    p.slot = next_queue_slot();
+    p.split.n_full = (int)p.shape.units;  // sequences differ in cost: no tail split
+    p.split.n_split = 0;
+    p.split.parts = 1;
+    p.partial = nullptr;
+    p.cu_q = cu_q;
+    p.cu_k = cu_k;
+    p.total_q = total_q;
+    p.total_k = total_k;
+    const long long items = p.shape.units;
+    const int grid = (int)(items < dev.num_sms ? items : dev.num_sms);
+    CUtensorMap tq, tk, tv, to;
+    attn_status_t st;
+    const bool f32 = o_dtype == ATTN_OUT_F32;
+    if ((st = encode_tmap_ragged(&tq, q, false, d, Hq, 64, kTileM, true)) != ATTN_OK) return st;
+    if ((st = encode_tmap_ragged(&tk, k, false, d, Hkv, 64, kTileN, true)) != ATTN_OK) return st;
+    if ((st = encode_tmap_ragged(&tv, v, false, d, Hkv, 64, kTileN, true)) != ATTN_OK) return st;
+    if ((st = encode_tmap_ragged(&to, o, f32, d, Hq, kEpiCols(f32), 32, false)) != ATTN_OK) return st;
+    if (pad_head_dim(d) == 128)
+        return f32 ? launch_fwd_t<128, true, true>(tq, tk, tv, to, lse, p, grid, stream, dev)
+                   : launch_fwd_t<128, false, true>(tq, tk, tv, to, lse, p, grid, stream, dev);
+    if (pad_head_dim(d) == 64)
+        return f32 ? launch_fwd_t<64, true, true>(tq, tk, tv, to, lse, p, grid, stream, dev)
+                   : launch_fwd_t<64, false, true>(tq, tk, tv, to, lse, p, grid, stream, dev);
     return ATTN_ERR_UNSUPPORTED;
 }
 

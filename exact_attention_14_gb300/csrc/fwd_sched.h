@@ -62,9 +62,14 @@ GB300_HD int tile_rows(int mb, int t, int Nq) {
     return r <= 0 ? 0 : (r < kTileM ? r : kTileM);
 }
 
+// KV tiles of Q tile t of m-block mb, for Nq query rows and Nk keys.
+GB300_HD int tile_kv_count_len(int mb, int t, int Nq, int Nk, int causal) {
+    return kv_tiles_for_rows(mb * kUnitRows + t * kTileM, tile_rows(mb, t, Nq), Nq, Nk, causal,
+                             kTileN);
+}
+
 GB300_HD int tile_kv_count(int mb, int t, const FwdShape& s) {
-    return kv_tiles_for_rows(mb * kUnitRows + t * kTileM, tile_rows(mb, t, s.Nq), s.Nq, s.Nk,
-                             s.causal, kTileN);
+    return tile_kv_count_len(mb, t, s.Nq, s.Nk, s.causal);
 }
 
 inline FwdShape make_fwd_shape(int B, int Hq, int Hkv, int Nq, int Nk, int d, int causal) {
@@ -100,6 +105,18 @@ GB300_HD void unit_of(const FwdShape& s, uint32_t i, int& bh, int& mb) {
     bh = (int)(sec * S + h_in);
     mb = s.causal ? (int)((uint32_t)s.nmb - 1u - rank) : (int)rank;
 }
+
+// Packed variable-length batches.  Sequence b holds rows [cu[b], cu[b+1]) of a
+// packed [total, H, d] array.  Its tensor maps add two dimensions so that the
+// hardware's bounds check stops exactly at each sequence's end (loads past it
+// read zeros, stores past it are dropped): element (c, h, r, e, f) lies at
+//   base + c*es + h*d*es + (r + e)*rs + f*(2^34 - rs)        (mod 2^64),
+// rs the row stride.  Row `row` of a sequence starting at s with length L uses
+// r = W - L + row, e = s + L, f = W with W = 2^30: the f term is
+// W*2^34 - W*rs = 2^64 - W*rs, so the address is base + (s + row)*rs, and
+// r < W (the extent of r) holds exactly when row < L.
+constexpr int kRaggedWindow = 1 << 30;     // W: extent of r, and the f coordinate
+constexpr unsigned kRaggedOuterExtent = 0x7FFFFFFFu;  // extents of e and f (> W)
 
 // Tail split.  Without causal masking every unit costs the same, so a unit
 // count just above a multiple of the SM count leaves most CTAs idle in the

@@ -43,9 +43,24 @@ attn_status_t encode_tmap_f32_sw128_3d(CUtensorMap* map, void* base, int d, int 
 attn_status_t encode_tmap_paged_kv(CUtensorMap* map, const void* base, int d, int Hkv,
                                    int page_size, long long num_blocks);
 
+// 5-D tensor map over a packed [total, heads, d] array (bf16, or fp32 for
+// outputs) addressed per sequence: see the ragged layout in fwd_sched.h.  Box of
+// box_cols x 1 head x box_rows rows; 128-byte swizzle for the operand loads,
+// none for the staged output stores.
+attn_status_t encode_tmap_ragged(CUtensorMap* map, const void* base, bool f32, int d, int heads,
+                                 int box_cols, int box_rows, bool swizzle128);
+
 attn_status_t launch_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
                          int B, int Hq, int Hkv, int Nq, int Nk, int d, int causal, float scale,
                          attn_out_dtype_t o_dtype, cudaStream_t stream, const DeviceInfo& dev);
+
+// Packed variable-length forward: q/o [total_q, Hq, d], k/v [total_k, Hkv, d],
+// lse [Hq, total_q]; cu_q / cu_k device int32 [B + 1].
+attn_status_t launch_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                                const int* cu_q, const int* cu_k, int B, int Hq, int Hkv,
+                                int total_q, int total_k, int max_q, int max_k, int d, int causal,
+                                float scale, attn_out_dtype_t o_dtype, cudaStream_t stream,
+                                const DeviceInfo& dev);
 
 // Backward: workspace bytes (fp32 dQ accumulator, lse2, D; padded rows).
 size_t bwd_workspace_bytes(int B, int Hq, int Nq, int d);

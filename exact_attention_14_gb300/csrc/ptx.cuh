@@ -29,7 +29,7 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
 // Error bits written to the library's device error word.
 enum : uint32_t {
     kErrTimeout = 1u,      // a bounded wait ran out
-    kErrBadSeqlen = 2u,    // decode: a sequence length outside [1, Nmax]
+    kErrBadSeqlen = 2u,    // a sequence length or offset outside its documented range
     kErrLayout = 4u,       // a kernel's shared-memory layout did not fit its allocation
 };
 
@@ -164,6 +164,24 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map
         "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int x, int y, int z, int w, int v) {
+    asm volatile(
+        "cp.async.bulk.tensor.5d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(v), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_store_5d(const CUtensorMap* map, uint32_t src, int x, int y, int z,
+                                             int w, int v) {
+    asm volatile(
+        "cp.async.bulk.tensor.5d.global.shared::cta.bulk_group [%0, {%2, %3, %4, %5, %6}], [%1];" ::"l"(
+            reinterpret_cast<uint64_t>(map)),
+        "r"(src), "r"(x), "r"(y), "r"(z), "r"(w), "r"(v)
         : "memory");
 }
 

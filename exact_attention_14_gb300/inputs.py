@@ -11,7 +11,8 @@ the long-context case scales 4 head-dim channels per head by 8 in Q and K (the
 same channels in both -- the reading that keeps the outliers aligned in QK^T);
 decode draws each sequence's valid length uniformly from an inclusive integer
 range and fills the cache tail (positions >= length) with N(0, 1) or, for the
-leak test, with NaN.
+leak test, with NaN.  Packed variable-length batches draw each sequence's
+length uniformly from an inclusive range and lay the sequences end to end.
 """
 from __future__ import annotations
 
@@ -72,6 +73,29 @@ DECODE = DecodeConfig("decode split-KV", 16, 32, 8, 32768, 128, 1024, 32768, see
 FWD_CONFIGS = (TINY, PREFILL, LONG, GQA)
 
 
+@dataclass(frozen=True)
+class VarlenConfig:
+    """A packed batch of n_seqs sequences, each of length U[len_lo, len_hi]
+    (the same length for its queries and keys)."""
+    name: str
+    n_seqs: int
+    Hq: int
+    Hkv: int
+    d: int
+    len_lo: int
+    len_hi: int
+    causal: bool
+    seed: int
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.d)
+
+
+# A prefill batch of mixed lengths, 16 sequences of 256..4096 tokens.
+VARLEN = VarlenConfig("varlen causal prefill", 16, 16, 16, 128, 256, 4096, True, seed=5)
+
+
 def _gen(seed: int) -> torch.Generator:
     g = torch.Generator(device="cpu")
     g.manual_seed(int(seed))
@@ -127,3 +151,34 @@ def make_decode_inputs(B: int, Hq: int, Hkv: int, Nmax: int, d: int, seed: int,
 def make_decode_config_inputs(cfg: DecodeConfig, tail: str = "normal"):
     return make_decode_inputs(cfg.B, cfg.Hq, cfg.Hkv, cfg.Nmax, cfg.d, cfg.seed,
                               cfg.len_lo, cfg.len_hi, tail=tail)
+
+
+def varlen_lengths(n_seqs: int, len_lo: int, len_hi: int, seed: int) -> list:
+    """n_seqs lengths drawn uniformly from [len_lo, len_hi] (inclusive)."""
+    g = _gen(seed)
+    return torch.randint(len_lo, len_hi + 1, (n_seqs,), generator=g).tolist()
+
+
+def make_varlen_inputs(lens_q, lens_k, Hq: int, Hkv: int, d: int, seed: int,
+                       extra_rows: int = 0, extra_value: float = float("nan")):
+    """Packed q [total_q, Hq, d], k, v [total_k, Hkv, d] (bf16, CPU) for
+    sequences of lengths lens_q / lens_k laid end to end, and the row offsets
+    cu_q, cu_k (int32 [B + 1]).  extra_rows rows past the last sequence hold
+    extra_value (they belong to no sequence)."""
+    g = _gen(seed)
+    cu_q = [0]
+    for n in lens_q:
+        cu_q.append(cu_q[-1] + int(n))
+    cu_k = [0]
+    for n in lens_k:
+        cu_k.append(cu_k[-1] + int(n))
+    tq, tk = cu_q[-1] + extra_rows, cu_k[-1] + extra_rows
+    q = torch.randn((tq, Hq, d), generator=g, dtype=torch.float32)
+    k = torch.randn((tk, Hkv, d), generator=g, dtype=torch.float32)
+    v = torch.randn((tk, Hkv, d), generator=g, dtype=torch.float32)
+    if extra_rows:
+        q[cu_q[-1]:] = extra_value
+        k[cu_k[-1]:] = extra_value
+        v[cu_k[-1]:] = extra_value
+    return (q.to(torch.bfloat16), k.to(torch.bfloat16), v.to(torch.bfloat16),
+            torch.tensor(cu_q, dtype=torch.int32), torch.tensor(cu_k, dtype=torch.int32))

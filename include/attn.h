@@ -1,9 +1,9 @@
 /*
  * attn.h -- C ABI of the GB300 (sm_103a) exact-attention library.
  *
- * Two operations, both exact scaled-dot-product attention O = softmax(s*QK^T)V
- * computed tile by tile with the online-softmax running max / sum so that the
- * N x N score and probability matrices never reach device memory:
+ * Exact scaled-dot-product attention O = softmax(s*QK^T)V computed tile by
+ * tile with the online-softmax running max / sum so that the N x N score and
+ * probability matrices never reach device memory.  Operations:
  *
  *   attn_fwd     fused forward with per-row logsumexp, causal masking and
  *                grouped-query heads (lecture notes "Optimizing Attention for
@@ -12,12 +12,16 @@
  *                order, 3.2 delayed normalisation, 4.5 persistent kernel and
  *                LPT schedule, 5.3 conditional rescaling; "Flash Attention 3/4
  *                notes", FA4 section 1 pipeline and section 3 causal schedule);
+ *   attn_fwd_varlen  the same forward over a packed batch of sequences of
+ *                different lengths (row offsets per sequence);
+ *   attn_bwd     the gradients dQ, dK, dV from the forward's logsumexp;
  *   attn_decode  single-query decode over a KV cache with split-KV
  *                (Flash-Decoding): each split produces a partial (m, l, o) and
  *                a combine step merges the splits by log-sum-exp (lecture
  *                notes section 6.1 and exercise 3; "FlashAttention tiling &
  *                online softmax" section 7.1), with query heads that share a
- *                KV head packed as rows of one tile (lecture notes 6.2).
+ *                KV head packed as rows of one tile (lecture notes 6.2);
+ *                attn_decode_paged reads the cache through a block table.
  *
  * Conventions shared by every entry point
  *   - Pointers named q/k/v/o/lse/k_cache/v_cache/seqlens/workspace are DEVICE
@@ -72,7 +76,9 @@ typedef enum {
  *   scale  softmax scale (typically 1/sqrt(d)); finite and >= 0
  *   causal 0 or 1 (bottom-right aligned; requires Nq <= Nk)
  *
- * Supported: d in {64, 128}; Hq % Hkv == 0; 1 <= Nq, Nk <= 2^24;
+ * Supported: 8 <= d <= 128 with d % 8 == 0 (d other than 64 and 128 runs on
+ *            the 64- or 128-column kernel with the columns past d read as
+ *            zero and never written); Hq % Hkv == 0; 1 <= Nq, Nk <= 2^24;
  *            B*Hq and B*Hkv <= 2^24.  Other d -> ATTN_ERR_UNSUPPORTED.
  * Numerics: scores and O accumulate in fp32; the probabilities that multiply V
  * are rounded to bf16.  The logsumexp uses the sum of the unrounded
@@ -90,6 +96,36 @@ typedef enum {
 attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
                        int B, int Hq, int Hkv, int Nq, int Nk, int d, int causal,
                        float scale, attn_out_dtype_t o_dtype, void* stream);
+
+/*
+ * attn_fwd_varlen -- attn_fwd over a packed batch of B sequences of different
+ * lengths.  Sequence b is query rows [cu_seqlens_q[b], cu_seqlens_q[b+1]) and
+ * key rows [cu_seqlens_k[b], cu_seqlens_k[b+1]); it attends only to its own
+ * keys (causal: bottom-right aligned within the sequence).
+ *
+ *   q    bf16 [total_q, Hq,  d]      k, v  bf16 [total_k, Hkv, d]
+ *   o    [total_q, Hq, d], element type per o_dtype
+ *   lse  fp32 [Hq, total_q], or NULL
+ *   cu_seqlens_q, cu_seqlens_k  DEVICE int32 [B + 1], non-decreasing, from 0
+ *        or more up to total_q / total_k (rows outside every sequence are
+ *        neither read nor written)
+ *   max_seqlen_q, max_seqlen_k  upper bounds of the lengths (host ints)
+ *
+ * Supported as attn_fwd; 1 <= total_q, total_k <= 2^30; max lengths in
+ * [1, 2^24].  The lengths live on the device, so their checks run there: a
+ * sequence whose offsets leave [0, total], decrease, exceed the maximum
+ * length, give query rows without keys, or (causal) more queries than keys
+ * is not computed (its O and LSE rows are left as they were) and
+ * attn_last_device_error() then reports ATTN_ERR_INVALID_ARG.  A sequence of
+ * length 0 is skipped.  Numerics as attn_fwd; no KV tail split.  Loads stop
+ * at each sequence's last row (no value of another sequence, NaN included,
+ * reaches a result).  Uses a work-queue slot as attn_fwd.
+ */
+attn_status_t attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                              const int* cu_seqlens_q, const int* cu_seqlens_k, int B, int Hq,
+                              int Hkv, int total_q, int total_k, int max_seqlen_q,
+                              int max_seqlen_k, int d, int causal, float scale,
+                              attn_out_dtype_t o_dtype, void* stream);
 
 /*
  * attn_bwd_workspace_size -- bytes of device workspace attn_bwd needs: two
@@ -118,7 +154,7 @@ size_t attn_bwd_workspace_size(int B, int Hq, int Hkv, int Nq, int Nk, int d);
  *            16-byte aligned; contents need no initialisation; not used after
  *            the call's kernels finish.
  *
- * Supported as for attn_fwd (d in {64, 128}, Hq % Hkv == 0, causal needs
+ * Supported as for attn_fwd (8 <= d <= 128, d % 8 == 0, Hq % Hkv == 0, causal needs
  * Nq <= Nk).  Pointers 16-byte aligned (lse 4-byte).  The caller owns every
  * buffer.  Three kernels run in order on `stream`: a per-row pass (D, the LSE
  * in base 2), a K/V-outer pass (one CTA per (b, KV head, 128-key tile): dK
@@ -197,7 +233,8 @@ int attn_decode_kernel_launches(int B, int Hq, int Hkv, int Nmax, int d, int num
  *            bytes, 16-byte aligned; contents need no initialisation and are
  *            garbage afterwards.  Concurrent calls must not share it.
  *
- * Supported: d in {64, 128}; Hq % Hkv == 0; Hq / Hkv <= 16; 1 <= Nmax <= 2^24.
+ * Supported: 8 <= d <= 128 with d % 8 == 0; Hq % Hkv == 0; Hq / Hkv <= 16;
+ * 1 <= Nmax <= 2^24.
  */
 attn_status_t attn_decode(const void* q, const void* k_cache, const void* v_cache,
                           const int* seqlens, void* o, float* lse, int B, int Hq, int Hkv,

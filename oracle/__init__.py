@@ -147,6 +147,33 @@ def attention_rows(q, k, v, rows, *, causal: bool = False, scale: float | None =
     return o, lse
 
 
+def attention_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, *, causal: bool = False,
+                     scale: float | None = None, n_threads: int = 0):
+    """Packed batch of independent sequences: sequence b is query rows
+    cu_q[b]..cu_q[b+1] of q [total_q, Hq, d] and key rows cu_k[b]..cu_k[b+1]
+    of k, v [total_k, Hkv, d]; it is its own attention problem (causal
+    bottom-right aligned within it), computed by attention() above.
+
+    Returns (O [total_q, Hq, d], LSE [Hq, total_q]) float64; rows that belong
+    to no sequence are NaN."""
+    cu_q = [int(x) for x in np.asarray(cu_seqlens_q).reshape(-1)]
+    cu_k = [int(x) for x in np.asarray(cu_seqlens_k).reshape(-1)]
+    total_q, Hq, d = q.shape
+    o = np.full((total_q, Hq, d), np.nan)
+    lse = np.full((Hq, total_q), np.nan)
+    for b in range(len(cu_q) - 1):
+        qs, qe, ks, ke = cu_q[b], cu_q[b + 1], cu_k[b], cu_k[b + 1]
+        if qe == qs:
+            continue
+        qb = q[qs:qe].permute(1, 0, 2).unsqueeze(0)
+        kb = k[ks:ke].permute(1, 0, 2).unsqueeze(0)
+        vb = v[ks:ke].permute(1, 0, 2).unsqueeze(0)
+        ob, lb = attention(qb, kb, vb, causal=causal, scale=scale, n_threads=n_threads)
+        o[qs:qe] = ob[0].transpose(1, 0, 2)
+        lse[:, qs:qe] = lb[0]
+    return o, lse
+
+
 def decode(q, k_cache, v_cache, seqlens, *, scale: float | None = None,
            n_threads: int = 0):
     """Single-query decode over the valid prefix of each sequence's KV cache.

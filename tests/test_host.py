@@ -301,3 +301,23 @@ def test_supported_head_dims(lib, d, ok):
     assert (ea.attn_bwd_workspace_size(2, 8, 2, 1000, 1000, d) > 0) == ok
     rc = fwd(lib, d=d)
     assert rc == (ea.ATTN_ERR_CUDA if ok else ea.ATTN_ERR_UNSUPPORTED) or (ok and rc == ea.ATTN_OK)
+
+
+def fwd_varlen(lib, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=None, cq=FAKE, ck=FAKE, B=2, Hq=2, Hkv=1,
+             tq=300, tk=300, mq=200, mk=200, d=128, causal=1, scale=0.1, odt=1)
+    a.update(kw)
+    return lib.attn_fwd_varlen(a["q"], a["k"], a["v"], a["o"], a["lse"], a["cq"], a["ck"],
+                               a["B"], a["Hq"], a["Hkv"], a["tq"], a["tk"], a["mq"], a["mk"],
+                               a["d"], a["causal"], a["scale"], a["odt"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), 1), (dict(cq=None), 1), (dict(ck=FAKE + 2), 1), (dict(o=FAKE + 4), 1),
+    (dict(tq=0), 1), (dict(tk=0), 1), (dict(tq=(1 << 30) + 1), 1), (dict(mq=301), 1),
+    (dict(mk=301), 1), (dict(mq=0), 1), (dict(B=0), 1), (dict(Hq=3, Hkv=2), 1),
+    (dict(causal=2), 1), (dict(scale=-1.0), 1), (dict(odt=5), 1), (dict(d=100), 2),
+    (dict(d=256), 2),
+])
+def test_fwd_varlen_argument_checks(lib, kw, code):
+    assert fwd_varlen(lib, **kw) == code
