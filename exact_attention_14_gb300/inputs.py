@@ -182,3 +182,25 @@ def make_varlen_inputs(lens_q, lens_k, Hq: int, Hkv: int, d: int, seed: int,
         v[cu_k[-1]:] = extra_value
     return (q.to(torch.bfloat16), k.to(torch.bfloat16), v.to(torch.bfloat16),
             torch.tensor(cu_q, dtype=torch.int32), torch.tensor(cu_k, dtype=torch.int32))
+
+
+def make_outlier_inputs(B: int, Hq: int, Hkv: int, N: int, d: int, seed: int,
+                        frac: float = 1e-3, magnitude: float = 25.0):
+    """q [B,Hq,N,d], k, v [B,Hkv,N,d] bf16: N(0, 1) values with a fraction
+    `frac` of the entries of q and k (random positions) replaced by
+    +-magnitude (random signs) -- normal data with rare large values."""
+    g = _gen(seed)
+    q = torch.randn((B, Hq, N, d), generator=g, dtype=torch.float32)
+    k = torch.randn((B, Hkv, N, d), generator=g, dtype=torch.float32)
+    v = torch.randn((B, Hkv, N, d), generator=g, dtype=torch.float32)
+    for t in (q, k):
+        hit = torch.rand(t.shape, generator=g) < frac
+        sgn = torch.where(torch.rand(t.shape, generator=g) < 0.5, -1.0, 1.0)
+        t[hit] = (magnitude * sgn)[hit]
+    return q.to(torch.bfloat16), k.to(torch.bfloat16), v.to(torch.bfloat16)
+
+
+def hadamard_signs(d: int, seed: int) -> torch.Tensor:
+    """d random signs (int8, +-1) for the rotation of Q and K."""
+    g = _gen(seed)
+    return torch.where(torch.rand(d, generator=g) < 0.5, -1, 1).to(torch.int8)
