@@ -184,8 +184,8 @@ def run_reference(args, rank, world):
 
 def run_ours(args, rank, world, local_rank):
     import exact_attention_14_gb300 as ea
-    from exact_attention_14_gb300.inputs import DECODE, PREFILL, VARLEN, make_config_inputs, \
-        make_decode_config_inputs, make_varlen_inputs, varlen_lengths
+    from exact_attention_14_gb300.inputs import DECODE, LONG, PREFILL, VARLEN, hadamard_signs, \
+        make_config_inputs, make_decode_config_inputs, make_varlen_inputs, varlen_lengths
 
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
@@ -370,6 +370,61 @@ def run_ours(args, rank, world, local_rank):
                   "frac_of_bf16_peak": fv / tv / 1e12 / peaks["bf16_tflops"],
                   "flops_note": "sum over sequences of the forward formula 4*H*L^2*d (/2 causal)"}
 
+    # FP8 forward (a follow-on row, timed apart from the step): the long-context
+    # causal workload (B1 H32 N16384 d128, 4 outlier channels in Q and K),
+    # quantized with the random-sign Hadamard rotation; the three quantize
+    # launches and the attention launch are timed separately.
+    fp8 = None
+    if not args.no_fp8:
+        lq, lk, lv = (t.to(dev) for t in make_config_inputs(LONG))
+        signs = hadamard_signs(LONG.d, seed=LONG.seed).to(dev)
+        q8, qd = ea.fp8_quantize(lq, signs, stream=stream)
+        k8, kd = ea.fp8_quantize(lk, signs, stream=stream)
+        vt8, vd = ea.fp8_quantize(lv, None, transpose=True, stream=stream)
+        o8 = torch.empty(lq.shape, dtype=torch.bfloat16, device=dev)
+        l8 = torch.empty(lq.shape[:3], dtype=torch.float32, device=dev)
+        eff = LONG.scale / LONG.d
+
+        def quant_step():
+            ea.attn_fp8_quantize(lq, q8, qd, signs, stream=stream)
+            ea.attn_fp8_quantize(lk, k8, kd, signs, stream=stream)
+            ea.attn_fp8_quantize(lv, vt8, vd, None, transpose=True, stream=stream)
+
+        def fp8_step():
+            ea.attn_fwd_fp8(q8, k8, vt8, qd, kd, vd, o8, l8, causal=True, scale=eff, stream=stream)
+
+        for _ in range(args.warmup):
+            flush.zero_()
+            quant_step()
+            fp8_step()
+        fev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+        torch.cuda.synchronize()
+        for i in range(args.steps):
+            flush.zero_()
+            fev[i][0].record(stream)
+            quant_step()
+            fev[i][1].record(stream)
+            fp8_step()
+            fev[i][2].record(stream)
+        torch.cuda.synchronize()
+        if ea.attn_last_device_error() != 0:
+            raise RuntimeError("device error in the fp8 leg")
+        tq_ = sum(e[0].elapsed_time(e[1]) for e in fev) / args.steps * 1e-3
+        ta_ = sum(e[1].elapsed_time(e[2]) for e in fev) / args.steps * 1e-3
+        f8 = LONG.flops(True)
+        n_el = lq.numel() + lk.numel() + lv.numel()
+        qbytes = 3 * n_el + 4 * (qd.numel() + kd.numel() + vd.numel())   # bf16 in, E4M3 out
+        peak8 = 2 * peaks["bf16_tflops"]
+        fp8 = {"kernels": "attn_fp8_quantize (x3: Q, K rotated; V transposed) + attn_fwd_fp8_kernel",
+               "workload": "long-context causal B=1 H=32 N=16384 d=128, 4 outlier channels",
+               "attn_tflops": f8 / ta_ / 1e12, "attn_ms": 1e3 * ta_,
+               "attn_frac_of_fp8_peak": f8 / ta_ / 1e12 / peak8,
+               "fp8_peak_tflops": peak8,
+               "fp8_peak_source": "measured bf16_tflops x 2 (nominal fp8/bf16 ratio)",
+               "quantize_gbs": qbytes / tq_ / 1e9, "quantize_ms": 1e3 * tq_,
+               "quantize_frac_of_hbm": qbytes / tq_ / 1e9 / peaks["hbm_gbs"],
+               "with_quantize_tflops": f8 / (ta_ + tq_) / 1e12}
+
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         tf, desc, cores, _ = oracle_sample(args.cpu_seconds)
@@ -410,7 +465,7 @@ def run_ours(args, rank, world, local_rank):
         "decode": {"value": dec_gbs, "unit": "GB/s", "ms": 1e3 * t_dec,
                    "algorithmic_bytes": dec_bytes, "frac_of_hbm": dec_gbs / world / peaks["hbm_gbs"],
                    "sum_seqlen": sum_len},
-        "roofline": roof, "roofline_decode": roof_dec, "bwd": bwd, "varlen": varlen,
+        "roofline": roof, "roofline_decode": roof_dec, "bwd": bwd, "varlen": varlen, "fp8": fp8,
         "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": (2 + ea.attn_decode_kernel_launches(DECODE.B, DECODE.Hq, DECODE.Hkv,
                                                             DECODE.Nmax, DECODE.d)) * args.steps,
@@ -429,6 +484,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-bwd", action="store_true", help="skip the backward leg")
     ap.add_argument("--no-varlen", action="store_true", help="skip the packed varlen leg")
+    ap.add_argument("--no-fp8", action="store_true", help="skip the FP8 leg")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))

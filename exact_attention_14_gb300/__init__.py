@@ -17,6 +17,8 @@ import os
 
 __all__ = [
     "ATTN_OUT_BF16", "ATTN_OUT_F32", "AttnError", "attn_fwd", "attn_fwd_varlen", "forward_varlen",
+    "attn_fp8_quantize", "fp8_quantize", "attn_fwd_fp8", "forward_fp8", "attn_fp8_codes_bytes",
+    "attn_fp8_descale_count",
     "attn_decode",
     "attn_decode_workspace_size", "attn_decode_noalloc", "attn_status_string", "attn_last_device_error",
     "attn_decode_num_splits", "attn_list_schedule", "attn_kv_tiles",
@@ -43,6 +45,10 @@ SIGNATURES = {
     "attn_fwd": (_c_int, [_vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int,
                           _c_int, _c_int, _c_f, _c_int, _vp]),
     "attn_fwd_varlen": (_c_int, [_vp] * 7 + [_c_int] * 9 + [_c_f, _c_int, _vp]),
+    "attn_fp8_codes_bytes": (_c_sz, [_c_int] * 5),
+    "attn_fp8_descale_count": (_c_sz, [_c_int] * 3),
+    "attn_fp8_quantize": (_c_int, [_vp] * 4 + [_c_int] * 5 + [_vp]),
+    "attn_fwd_fp8": (_c_int, [_vp] * 8 + [_c_int] * 7 + [_c_f, _c_int, _vp]),
     "attn_decode_workspace_size": (_c_sz, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_int]),
     "attn_decode": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int,
                              _c_int, _c_f, _c_int, _vp, _c_sz, _c_int, _vp]),
@@ -216,6 +222,101 @@ def forward_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, max_s
            if return_lse else None)
     return attn_fwd_varlen(q, k, v, o, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k,
                            lse, causal=causal, scale=scale, stream=stream)
+
+
+def attn_fp8_codes_bytes(B: int, H: int, N: int, d: int, transpose: bool = False) -> int:
+    return int(load().attn_fp8_codes_bytes(B, H, N, d, int(bool(transpose))))
+
+
+def attn_fp8_descale_count(B: int, H: int, N: int) -> int:
+    return int(load().attn_fp8_descale_count(B, H, N))
+
+
+def attn_fp8_quantize(x, codes, descale, signs=None, *, transpose: bool = False, stream=None):
+    """Block-quantize x [B,H,N,d] bf16 into caller-provided E4M3 codes (uint8
+    [B,H,N,d], or [B,H,d,Np] when transpose) and descale [B,H,ceil(N/128)]
+    fp32; signs: None or an int8 tensor of d values +-1 (rotate first)."""
+    import torch
+    _need(x, torch.bfloat16, "x")
+    _need(codes, torch.uint8, "codes")
+    _need(descale, torch.float32, "descale")
+    if signs is not None:
+        _need(signs, torch.int8, "signs")
+    B, H, N, d = x.shape
+    if signs is not None and signs.numel() != d:
+        raise ValueError("signs must hold d values")
+    npad = (N + 15) // 16 * 16
+    want = (B, H, d, npad) if transpose else (B, H, N, d)
+    if tuple(codes.shape) != want:
+        raise ValueError(f"codes must be {want}")
+    if tuple(descale.shape) != (B, H, (N + 127) // 128):
+        raise ValueError("descale shape mismatch")
+    rc = load().attn_fp8_quantize(_ptr(x), _ptr(codes), _ptr(descale), _ptr(signs), B, H, N, d,
+                                  int(bool(transpose)), _stream_ptr(stream))
+    _check(rc, "attn_fp8_quantize")
+    return codes, descale
+
+
+def fp8_quantize(x, signs=None, *, transpose: bool = False, stream=None):
+    """Allocate the codes and scales with torch and run attn_fp8_quantize."""
+    import torch
+    B, H, N, d = x.shape
+    npad = (N + 15) // 16 * 16
+    shape = (B, H, d, npad) if transpose else (B, H, N, d)
+    codes = (torch.zeros if transpose else torch.empty)(shape, dtype=torch.uint8, device=x.device)
+    descale = torch.empty((B, H, (N + 127) // 128), dtype=torch.float32, device=x.device)
+    return attn_fp8_quantize(x, codes, descale, signs, transpose=transpose, stream=stream)
+
+
+def attn_fwd_fp8(q8, k8, vt8, q_descale, k_descale, v_descale, o, lse=None, *,
+                 causal: bool = False, scale: float | None = None, stream=None):
+    """Forward on E4M3 operands into caller-provided outputs: q8 [B,Hq,Nq,128],
+    k8 [B,Hkv,Nk,128], vt8 [B,Hkv,128,Np] (uint8 codes), descales fp32
+    [B,H,ceil(N/128)]; o [B,Hq,Nq,128] bf16/fp32; lse [B,Hq,Nq] or None."""
+    import torch
+    for t, n in ((q8, "q8"), (k8, "k8"), (vt8, "vt8")):
+        _need(t, torch.uint8, n)
+    for t, n in ((q_descale, "q_descale"), (k_descale, "k_descale"), (v_descale, "v_descale")):
+        _need(t, torch.float32, n)
+    if o.dtype not in (torch.bfloat16, torch.float32):
+        raise TypeError("o must be bfloat16 or float32")
+    _need(o, o.dtype, "o")
+    if lse is not None:
+        _need(lse, torch.float32, "lse")
+    B, Hq, Nq, d = q8.shape
+    Hkv, Nk = k8.shape[1], k8.shape[2]
+    if tuple(k8.shape) != (B, Hkv, Nk, d) or tuple(vt8.shape) != (B, Hkv, d, (Nk + 15) // 16 * 16):
+        raise ValueError("k8 / vt8 shape mismatch")
+    if tuple(o.shape) != (B, Hq, Nq, d):
+        raise ValueError("o shape mismatch")
+    if scale is None:
+        scale = d ** -0.5
+    odt = ATTN_OUT_F32 if o.dtype == torch.float32 else ATTN_OUT_BF16
+    rc = load().attn_fwd_fp8(_ptr(q8), _ptr(k8), _ptr(vt8), _ptr(q_descale), _ptr(k_descale),
+                             _ptr(v_descale), _ptr(o), _ptr(lse), B, Hq, Hkv, Nq, Nk, d,
+                             int(bool(causal)), float(scale), odt, _stream_ptr(stream))
+    _check(rc, "attn_fwd_fp8")
+    return o, lse
+
+
+def forward_fp8(q, k, v, *, causal: bool = False, scale: float | None = None, signs=None,
+                out_dtype=None, return_lse: bool = True, stream=None):
+    """bf16 q, k, v -> E4M3 (Q and K rotated by diag(signs) H when signs is
+    given: an int8 tensor of d values +-1) -> attn_fwd_fp8.  Returns (O, LSE)."""
+    import torch
+    d = q.shape[-1]
+    if scale is None:
+        scale = d ** -0.5
+    q8, qd = fp8_quantize(q, signs, stream=stream)
+    k8, kd = fp8_quantize(k, signs, stream=stream)
+    vt8, vd = fp8_quantize(v, None, transpose=True, stream=stream)
+    eff = scale / d if signs is not None else scale   # (Q D H)(K D H)^T = d Q K^T
+    out_dtype = out_dtype or torch.bfloat16
+    o = torch.empty(q.shape, dtype=out_dtype, device=q.device)
+    lse = (torch.empty(q.shape[:3], dtype=torch.float32, device=q.device)
+           if return_lse else None)
+    return attn_fwd_fp8(q8, k8, vt8, qd, kd, vd, o, lse, causal=causal, scale=eff,
+                        stream=stream)
 
 
 def attn_bwd_workspace_size(B: int, Hq: int, Hkv: int, Nq: int, Nk: int, d: int) -> int:

@@ -145,6 +145,20 @@ attn_status_t encode_tmap_ragged(CUtensorMap* map, const void* base, bool f32, i
     return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
+attn_status_t encode_tmap_u8_3d(CUtensorMap* map, const void* base, int inner, long long pitch,
+                                int rows, long long heads, int box_inner, int box_rows) {
+    if (!load_encoder()) return ATTN_ERR_CUDA;
+    cuuint64_t dims[3] = {(cuuint64_t)inner, (cuuint64_t)rows, (cuuint64_t)heads};
+    cuuint64_t strides[2] = {(cuuint64_t)pitch, (cuuint64_t)pitch * (cuuint64_t)rows};
+    cuuint32_t box[3] = {(cuuint32_t)box_inner, (cuuint32_t)box_rows, 1u};
+    cuuint32_t elem[3] = {1u, 1u, 1u};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims,
+                          strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
 attn_status_t encode_tmap_bf16_3d(CUtensorMap* map, const void* base, int d, int rows,
                                   long long heads, int box_rows) {
     if (!load_encoder()) return ATTN_ERR_CUDA;
@@ -224,6 +238,50 @@ attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, flo
     if ((st = current_device_info(&dev)) != ATTN_OK) return st;
     return launch_fwd(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, d, causal, scale, o_dtype,
                       static_cast<cudaStream_t>(stream), dev);
+}
+
+size_t attn_fp8_codes_bytes(int B, int H, int N, int d, int transpose) {
+    if (B < 1 || H < 1 || N < 1 || d != 128 || (transpose != 0 && transpose != 1)) return 0;
+    if ((long long)B * H > kMaxHeads || N > kMaxLen) return 0;
+    const long long n = transpose ? (long long)(N + 15) / 16 * 16 : (long long)N;
+    return (size_t)((long long)B * H * n * d);
+}
+
+size_t attn_fp8_descale_count(int B, int H, int N) {
+    if (B < 1 || H < 1 || N < 1 || (long long)B * H > kMaxHeads || N > kMaxLen) return 0;
+    return (size_t)((long long)B * H * ((N + 127) / 128));
+}
+
+attn_status_t attn_fp8_quantize(const void* x, void* codes, float* descale, const int8_t* signs,
+                                int B, int H, int N, int d, int transpose, void* stream) {
+    if (!x || !codes || !descale || !aligned16(x) || !aligned16(codes) || !aligned4(descale))
+        return ATTN_ERR_INVALID_ARG;
+    if (B < 1 || H < 1 || N < 1 || N > kMaxLen || (long long)B * H > kMaxHeads)
+        return ATTN_ERR_INVALID_ARG;
+    if (transpose != 0 && transpose != 1) return ATTN_ERR_INVALID_ARG;
+    if ((long long)B * H > 65535) return ATTN_ERR_UNSUPPORTED;  // grid.y
+    if (d != 128) return ATTN_ERR_UNSUPPORTED;
+    DeviceInfo dev;
+    attn_status_t st = current_device_info(&dev);
+    if (st != ATTN_OK) return st;
+    return launch_fp8_quantize(x, codes, descale, signs, B * H, N, transpose,
+                               static_cast<cudaStream_t>(stream), dev);
+}
+
+attn_status_t attn_fwd_fp8(const void* q8, const void* k8, const void* vt8, const float* q_descale,
+                           const float* k_descale, const float* v_descale, void* o, float* lse,
+                           int B, int Hq, int Hkv, int Nq, int Nk, int d, int causal, float scale,
+                           attn_out_dtype_t o_dtype, void* stream) {
+    if (!q_descale || !k_descale || !v_descale || !aligned4(q_descale) || !aligned4(k_descale) ||
+        !aligned4(v_descale))
+        return ATTN_ERR_INVALID_ARG;
+    attn_status_t st = check_fwd(q8, k8, vt8, o, lse, B, Hq, Hkv, Nq, Nk, d, causal, scale, o_dtype);
+    if (st != ATTN_OK) return st;
+    if (d != 128) return ATTN_ERR_UNSUPPORTED;
+    DeviceInfo dev;
+    if ((st = current_device_info(&dev)) != ATTN_OK) return st;
+    return launch_fwd_fp8(q8, k8, vt8, q_descale, k_descale, v_descale, o, lse, B, Hq, Hkv, Nq, Nk,
+                          causal, scale, o_dtype, static_cast<cudaStream_t>(stream), dev);
 }
 
 attn_status_t attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,

@@ -50,6 +50,22 @@ attn_status_t encode_tmap_paged_kv(CUtensorMap* map, const void* base, int d, in
 attn_status_t encode_tmap_ragged(CUtensorMap* map, const void* base, bool f32, int d, int heads,
                                  int box_cols, int box_rows, bool swizzle128);
 
+// 3-D uint8 tensor map over [heads, rows, inner] with a row pitch in bytes
+// (a multiple of 16), 128-byte-swizzled box of box_inner x box_rows x 1.
+attn_status_t encode_tmap_u8_3d(CUtensorMap* map, const void* base, int inner, long long pitch,
+                                int rows, long long heads, int box_inner, int box_rows);
+
+// FP8: block quantization of bf16 [BH, N, 128] (optionally rotated by the
+// sign-flipped Hadamard transform; transposed to [BH, 128, Np] on request), and
+// the forward on E4M3 operands (d = 128).
+attn_status_t launch_fp8_quantize(const void* x, void* out, float* descale, const int8_t* signs,
+                                  int BH, int N, int transpose, cudaStream_t stream,
+                                  const DeviceInfo& dev);
+attn_status_t launch_fwd_fp8(const void* q8, const void* k8, const void* vt8, const float* q_descale,
+                             const float* k_descale, const float* v_descale, void* o, float* lse,
+                             int B, int Hq, int Hkv, int Nq, int Nk, int causal, float scale,
+                             attn_out_dtype_t o_dtype, cudaStream_t stream, const DeviceInfo& dev);
+
 attn_status_t launch_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
                          int B, int Hq, int Hkv, int Nq, int Nk, int d, int causal, float scale,
                          attn_out_dtype_t o_dtype, cudaStream_t stream, const DeviceInfo& dev);

@@ -305,6 +305,55 @@ __device__ __forceinline__ void mma_commit_warp(uint32_t bar) {
         : "memory");
 }
 
+// The same two MMA forms for 8-bit operands (kind::f8f6f4; both operands E4M3
+// here, K = 32 per instruction).  With A in TMEM a 32-bit column holds four
+// consecutive K elements of the row (lane).
+__device__ __forceinline__ void mma_ss_f8_warp(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                               uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred e, p;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void mma_ts_f8_warp(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                               uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred e, p;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Instruction descriptor for kind::f8f6f4 with E4M3 x E4M3 -> fp32, dense,
+// both operands K-major (A/B format code 0 = E4M3).
+__host__ __device__ constexpr uint32_t make_idesc_e4m3(int M, int N) {
+    return (1u << 4) | (uint32_t(N >> 3) << 17) | (uint32_t(M >> 4) << 24);
+}
+
+// Two fp32 values rounded to E4M3 (nearest even, saturating at +-448), packed
+// into 16 bits with `lo` in bits 0-7.
+__device__ __forceinline__ uint32_t pack_e4m3x2(float lo, float hi) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+// The E4M3 value (as fp32) that a non-negative fp32 value rounds to.
+__device__ __forceinline__ float e4m3_round_f32(float x) {
+    uint16_t c, h2;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(c) : "f"(0.0f), "f"(x));
+    uint32_t hh;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(hh) : "h"(c));
+    h2 = (uint16_t)(hh & 0xFFFFu);
+    float f;
+    asm("cvt.f32.f16 %0, %1;" : "=f"(f) : "h"(h2));
+    return f;
+}
+
 // Instruction descriptor for kind::f16: bf16 x bf16 -> fp32, dense.
 //   bits 4-5 D format (1 = f32), 7-9 A format (1 = bf16), 10-12 B format,
 //   15 A major (0 = K), 16 B major (0 = K, 1 = MN), 17-22 N>>3, 24-28 M>>4.

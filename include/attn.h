@@ -14,6 +14,9 @@
  *                notes", FA4 section 1 pipeline and section 3 causal schedule);
  *   attn_fwd_varlen  the same forward over a packed batch of sequences of
  *                different lengths (row offsets per sequence);
+ *   attn_fwd_fp8 the forward on E4M3 operands with one scale per 128-row
+ *                block, after attn_fp8_quantize (optionally rotating Q and K
+ *                by a random-sign Hadamard matrix);
  *   attn_bwd     the gradients dQ, dK, dV from the forward's logsumexp;
  *   attn_decode  single-query decode over a KV cache with split-KV
  *                (Flash-Decoding): each split produces a partial (m, l, o) and
@@ -126,6 +129,55 @@ attn_status_t attn_fwd_varlen(const void* q, const void* k, const void* v, void*
                               int Hkv, int total_q, int total_k, int max_seqlen_q,
                               int max_seqlen_k, int d, int causal, float scale,
                               attn_out_dtype_t o_dtype, void* stream);
+
+/*
+ * attn_fp8_quantize -- block quantization to E4M3 (lecture notes "Optimizing
+ * Attention for Modern Hardware: FlashAttention 1-4", 4.4; "Flash Attention
+ * 3/4 notes", FA3 section 2: one scale per block, incoherent processing).
+ *
+ *   x        bf16 [B, H, N, d] (device)
+ *   signs    NULL, or d int8 values +-1 (device): each row x is first replaced
+ *            by H (s o x), H the unnormalised Sylvester-Hadamard matrix
+ *            (entries +-1), computed in fp32 by the fast Walsh-Hadamard
+ *            transform (stages h = 1, 2, ..., d/2; pairs (i, i+h) become
+ *            (a+b, a-b)).  Rotating Q and K with the same signs multiplies
+ *            their scores by d (pass scale / d to attn_fwd_fp8).
+ *   codes    E4M3 codes (device), [B, H, N, d] when transpose = 0, or
+ *            [B, H, d, Np] with Np = ceil(N/16)*16 when transpose = 1 (the
+ *            layout attn_fwd_fp8 wants for V; the padding keys hold 0);
+ *            attn_fp8_codes_bytes() bytes
+ *   descale  fp32 [B, H, ceil(N/128)]: for each block of 128 rows,
+ *            amax / 448 with amax the block's largest |value| (1 for an
+ *            all-zero block); codes are E4M3(fp32(x * (448 / amax))) rounded to
+ *            nearest even, so code * descale approximates x.
+ * Supported: d = 128; B*H <= 65535.  Asynchronous on `stream`.
+ */
+size_t attn_fp8_codes_bytes(int B, int H, int N, int d, int transpose);
+size_t attn_fp8_descale_count(int B, int H, int N);
+attn_status_t attn_fp8_quantize(const void* x, void* codes, float* descale, const int8_t* signs,
+                                int B, int H, int N, int d, int transpose, void* stream);
+
+/*
+ * attn_fwd_fp8 -- attn_fwd on E4M3 operands from attn_fp8_quantize:
+ *
+ *   q8  [B, Hq, Nq, 128] codes, q_descale [B, Hq, ceil(Nq/128)]
+ *   k8  [B, Hkv, Nk, 128] codes, k_descale [B, Hkv, ceil(Nk/128)]
+ *   vt8 [B, Hkv, 128, Np] transposed codes, v_descale [B, Hkv, ceil(Nk/128)]
+ *   o, lse, causal, o_dtype as attn_fwd; scale as attn_fwd (divide by d when
+ *   Q and K were rotated).
+ *
+ * Computes softmax(scale * Q^ K^^T) V^ over the dequantized operands (code *
+ * block descale) with fp32 accumulation; the probabilities are rounded to
+ * E4M3 before the P.V product (in a frame that carries V's block scale and a
+ * factor 2^4, so they stay within E4M3's range), and the row sums follow the
+ * unrounded ones as in attn_fwd.  LSE is the natural-log logsumexp of the
+ * scaled scores.  Supported: d = 128, other limits as attn_fwd.  Uses one of
+ * 256 queue slots per launch, as attn_fwd.
+ */
+attn_status_t attn_fwd_fp8(const void* q8, const void* k8, const void* vt8, const float* q_descale,
+                           const float* k_descale, const float* v_descale, void* o, float* lse,
+                           int B, int Hq, int Hkv, int Nq, int Nk, int d, int causal, float scale,
+                           attn_out_dtype_t o_dtype, void* stream);
 
 /*
  * attn_bwd_workspace_size -- bytes of device workspace attn_bwd needs: two

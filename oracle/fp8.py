@@ -39,7 +39,7 @@ Readings taken where the pages leave a step open:
 5. The attention over the quantized operands is exact attention over the
    dequantized values (computed here in fp64).  The FP8 kernel additionally
    rounds the probabilities to E4M3 before the P.V product; that rounding is
-   the kernel's, and the tests bound its effect (fp8_p_rounding_bound).
+   the kernel's, and attention_fp8 returns the bound the tests hold it to.
 """
 from __future__ import annotations
 
@@ -209,5 +209,37 @@ def attention_fp8(q8, k8, vt8, q_descale, k_descale, v_descale, Nk: int, *, caus
     grp = q.shape[1] // k.shape[1]
     va = np.abs(np.repeat(v, grp, axis=1))
     bound = 2.0 ** -3 * np.einsum("bhij,bhjd->bhid", p, va) + \
-        2.0 ** -9 * va.max(axis=(2, 3), keepdims=True)
+        2.0 ** -8 * va.max(axis=(2, 3), keepdims=True)
     return o, lse, bound
+
+
+def attention_fp8_rows(q8, k8, vt8, q_descale, k_descale, v_descale, Nk: int, rows, *,
+                       causal: bool, scale: float):
+    """Selected rows (b, hq, i) of attention_fp8, for shapes whose full score
+    matrix is too large.  Returns (O [n, d], LSE [n], bound [n, d])."""
+    q8, k8, vt8 = np.asarray(q8), np.asarray(k8), np.asarray(vt8)
+    Nq = q8.shape[2]
+    grp = q8.shape[1] // k8.shape[1]
+    rows = np.asarray(rows).reshape(-1, 3)
+    heads = {}
+    out_o, out_l, out_b = [], [], []
+    for b, h, i in rows:
+        hk = h // grp
+        if (b, hk) not in heads:
+            kk = dequantize(k8[b:b + 1, hk:hk + 1], np.asarray(k_descale)[b:b + 1, hk:hk + 1], Nk)
+            vv = dequantize(vt8[b:b + 1, hk:hk + 1], np.asarray(v_descale)[b:b + 1, hk:hk + 1], Nk,
+                            transposed=True)
+            heads[(b, hk)] = (kk[0, 0], vv[0, 0])
+        kk, vv = heads[(b, hk)]
+        blk = i // BLOCK
+        qrow = e4m3_decode(q8[b, h, i]) * float(np.asarray(q_descale)[b, h, blk])
+        n_allowed = min(Nk, i + 1 + (Nk - Nq)) if causal else Nk
+        s = scale * (kk[:n_allowed] @ qrow)
+        mx = s.max()
+        e = np.exp(s - mx)
+        p = e / e.sum()
+        out_o.append(p @ vv[:n_allowed])
+        out_l.append(mx + np.log(e.sum()))
+        va = np.abs(vv[:n_allowed])
+        out_b.append(2.0 ** -3 * (p @ va) + 2.0 ** -8 * np.abs(vv).max())
+    return np.array(out_o), np.array(out_l), np.array(out_b)

@@ -321,3 +321,25 @@ def fwd_varlen(lib, **kw):
 ])
 def test_fwd_varlen_argument_checks(lib, kw, code):
     assert fwd_varlen(lib, **kw) == code
+
+
+def test_fp8_sizes_and_argument_checks(lib):
+    assert ea.attn_fp8_codes_bytes(2, 3, 300, 128) == 2 * 3 * 300 * 128
+    assert ea.attn_fp8_codes_bytes(2, 3, 300, 128, transpose=True) == 2 * 3 * 128 * 304
+    assert ea.attn_fp8_codes_bytes(1, 1, 10, 64) == 0
+    assert ea.attn_fp8_descale_count(2, 3, 300) == 18
+    q = lib.attn_fp8_quantize
+    assert q(None, FAKE, FAKE, None, 1, 1, 8, 128, 0, None) == 1
+    assert q(FAKE, FAKE + 8, FAKE, None, 1, 1, 8, 128, 0, None) == 1
+    assert q(FAKE, FAKE, FAKE + 2, None, 1, 1, 8, 128, 0, None) == 1
+    assert q(FAKE, FAKE, FAKE, None, 1, 1, 0, 128, 0, None) == 1
+    assert q(FAKE, FAKE, FAKE, None, 1, 1, 8, 128, 2, None) == 1
+    assert q(FAKE, FAKE, FAKE, None, 1, 1, 8, 64, 0, None) == 2
+    f = lib.attn_fwd_fp8
+    args = [FAKE] * 6 + [FAKE, None, 1, 2, 1, 8, 8, 128, 0, 0.1, 0, None]
+    bad_d = list(args); bad_d[13] = 64
+    assert f(*bad_d) == 2
+    bad_s = list(args); bad_s[3] = None
+    assert f(*bad_s) == 1
+    bad_c = list(args); bad_c[14] = 1; bad_c[11] = 9
+    assert f(*bad_c) == 1
