@@ -45,30 +45,39 @@ def read_peaks():
             "source": "fallback"}
 
 
-def kernel_source_hash() -> str:
-    """sha256 over name + bytes of the kernel sources, in sorted order."""
-    import glob
+# The sources each profiled kernel is built from (its own translation unit and
+# the headers it includes); a kernel's DRAM figures stay valid while these hash
+# to the value stored beside them.
+KERNEL_SOURCES = {
+    "attn_fwd_kernel": ["attn_fwd_sm103.cu", "fwd_sched.h", "ptx.cuh", "internal.h"],
+    "attn_decode_split_kernel": ["attn_decode_sm103.cu", "ptx.cuh", "internal.h"],
+    "attn_bwd": ["attn_bwd_sm103.cu", "ptx.cuh", "internal.h"],
+    "attn_fp8": ["attn_fp8_sm103.cu", "fwd_sched.h", "ptx.cuh", "internal.h"],
+}
+
+
+def kernel_source_hash(kernel: str) -> str:
+    """sha256 over name + bytes of one kernel's sources, in the listed order."""
     import hashlib
     csrc = os.path.join(ROOT, "exact_attention_14_gb300", "csrc")
-    files = sorted(glob.glob(os.path.join(csrc, "*.cu")) + glob.glob(os.path.join(csrc, "*.cuh"))
-                   + glob.glob(os.path.join(csrc, "*.h")))
     h = hashlib.sha256()
-    for path in files:
-        h.update(os.path.basename(path).encode())
-        with open(path, "rb") as fh:
+    for name in KERNEL_SOURCES[kernel]:
+        h.update(name.encode())
+        with open(os.path.join(csrc, name), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()
 
 
 def read_traffic():
-    """DRAM bytes per launch from the committed ncu summary, or None when the
-    kernel sources changed since it was captured."""
+    """DRAM bytes per launch from the committed ncu summaries, for the kernels
+    whose sources have not changed since the capture."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
-        return None
+        return {}
     with open(path) as f:
         t = json.load(f)
-    return t if t.get("source_sha256") == kernel_source_hash() else None
+    return {k: v for k, v in t.get("kernels", {}).items()
+            if k in KERNEL_SOURCES and v.get("sources_sha256") == kernel_source_hash(k)}
 
 
 class ClockSampler:
@@ -439,14 +448,16 @@ def run_ours(args, rank, world, local_rank):
             "achieved": (f_nc + f_c) / fwd_time / 1e12, "peak": peak_t, "unit": "TFLOP/s",
             "frac": (f_nc + f_c) / fwd_time / 1e12 / peak_t,
             "traffic": (traffic["attn_fwd_kernel"]["prefill_noncausal"]
-                        + traffic["attn_fwd_kernel"]["prefill_causal"]) if traffic else None,
+                        + traffic["attn_fwd_kernel"]["prefill_causal"])
+                       if "attn_fwd_kernel" in traffic else None,
             "traffic_note": "DRAM bytes of one non-causal + one causal launch (ncu, profiles/); "
                             "algorithmic bytes 2 x 134.7 MB",
             "peak_source": f"{peaks['source']} bf16_tflops (burst)"}
     roof_dec = {"bound": "hbm", "kernel": "attn_decode_split_kernel (split-KV with in-kernel merge)",
                 "achieved": dec_bytes / t_dec / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": dec_bytes / t_dec / 1e9 / peaks["hbm_gbs"],
-                "traffic": traffic["attn_decode_split_kernel"]["decode"] if traffic else None,
+                "traffic": traffic["attn_decode_split_kernel"]["decode"]
+                           if "attn_decode_split_kernel" in traffic else None,
                 "traffic_note": "DRAM bytes per launch (ncu, profiles/); algorithmic bytes in "
                                 "decode.algorithmic_bytes",
                 "peak_source": f"{peaks['source']} hbm_gbs"}

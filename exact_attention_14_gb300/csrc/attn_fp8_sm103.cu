@@ -8,15 +8,17 @@
 // MMA); "Flash Attention 3/4 notes", FA3 section 2 (one scale per block,
 // (QM)(KM)^T = QK^T).
 //
-// attn_fp8_quantize_kernel (HBM-bound): one CTA per (batch * head, block of
-//   128 rows).  Each warp takes 32 rows; a lane holds 4 consecutive entries of
-//   a row.  With signs given, a row x becomes H (s o x) (H the unnormalised
-//   Sylvester-Hadamard matrix) by the fast Walsh-Hadamard transform in fp32:
-//   stages h = 1, 2 inside a lane, h = 4 .. 64 between lanes (shuffles); each
-//   pair (i, i + h) becomes (a + b, a - b).  The block's amax gives
+// attn_fp8_quantize_rows_kernel / attn_fp8_quantize_kernel (HBM-bound): one
+//   CTA per (batch * head, block of 128 rows).  With signs given, a row x
+//   becomes H (s o x) (H the unnormalised Sylvester-Hadamard matrix) by the
+//   fast Walsh-Hadamard transform in fp32: stages h = 1, 2, ..., 64; each pair
+//   (i, i + h) becomes (a + b, a - b); the stages inside a lane's slice of the
+//   row run in registers, the others through shuffles.  The block's amax gives
 //   inv = 448 / amax and descale = amax / 448; codes are E4M3(x * inv), written
-//   row-major [B, H, N, 128] or, for V, transposed [B, H, 128, Np] so that the
-//   P.V product reads V K-major.
+//   row-major [B, H, N, 128] by the rows kernel (16 entries per lane, values
+//   kept in registers) or, for V, transposed [B, H, 128, Np] by the other
+//   (the block staged in shared memory) so that the P.V product reads V
+//   K-major.
 //
 // attn_fwd_fp8_kernel (tensor-bound): the bf16 forward's persistent design
 //   (one CTA per SM, device-side queue over the units of fwd_sched.h, warp 0
@@ -82,17 +84,22 @@ attn_fp8_quantize_kernel(const __nv_bfloat16* __restrict__ x, uint8_t* __restric
         for (int e = 0; e < 4; ++e) sg[e] = (float)__ldg(signs + 4 * lane + e);
     }
     float amax = 0.f;
+    // all 32 rows' loads first (8 KiB in flight per warp), then the arithmetic
+    uint2 raw[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        const int row = blk * 128 + warp * 32 + i;
+        raw[i] = row < N ? __ldg(reinterpret_cast<const uint2*>(x + (bh * N + row) * kD) + lane)
+                         : make_uint2(0u, 0u);
+    }
+#pragma unroll
     for (int i = 0; i < 32; ++i) {
         const int r = warp * 32 + i;
-        const int row = blk * 128 + r;
-        float v[4] = {0.f, 0.f, 0.f, 0.f};
-        if (row < N) {
-            const uint2 raw = __ldg(reinterpret_cast<const uint2*>(x + (bh * N + row) * kD) + lane);
-            v[0] = __uint_as_float(raw.x << 16);
-            v[1] = __uint_as_float(raw.x & 0xFFFF0000u);
-            v[2] = __uint_as_float(raw.y << 16);
-            v[3] = __uint_as_float(raw.y & 0xFFFF0000u);
-        }
+        float v[4];
+        v[0] = __uint_as_float(raw[i].x << 16);
+        v[1] = __uint_as_float(raw[i].x & 0xFFFF0000u);
+        v[2] = __uint_as_float(raw[i].y << 16);
+        v[3] = __uint_as_float(raw[i].y & 0xFFFF0000u);
         if constexpr (ROTATE) {
 #pragma unroll
             for (int e = 0; e < 4; ++e) v[e] = __fmul_rn(v[e], sg[e]);
@@ -147,6 +154,90 @@ attn_fp8_quantize_kernel(const __nv_bfloat16* __restrict__ x, uint8_t* __restric
             }
             *reinterpret_cast<uint4*>(dst + k0) = make_uint4(w[0], w[1], w[2], w[3]);
         }
+    }
+}
+
+// Row-major output (Q, K): 256 threads, a warp takes 16 rows, four at a time
+// (8 lanes per row, 16 consecutive entries per lane), so the butterfly stages
+// h = 1 .. 8 stay inside a lane and only h = 16, 32, 64 cross lanes; the values
+// stay in registers between the amax and the codes.
+constexpr int kRThreads = 256;
+
+template <bool ROTATE>
+__global__ void __launch_bounds__(kRThreads)
+attn_fp8_quantize_rows_kernel(const __nv_bfloat16* __restrict__ x, uint8_t* __restrict__ out,
+                              float* __restrict__ descale, const int8_t* __restrict__ signs,
+                              int N, int nblk) {
+    __shared__ float warp_max[8];
+    const int blk = blockIdx.x;
+    const long long bh = blockIdx.y;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 3, pos = lane & 7;   // row within a group of 4, 16-entry slice
+    uint4 raw[4][2];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int row = blk * 128 + warp * 16 + 4 * i + g;
+        const uint4* src = reinterpret_cast<const uint4*>(x + (bh * N + row) * kD + 16 * pos);
+        raw[i][0] = row < N ? __ldg(src) : make_uint4(0u, 0u, 0u, 0u);
+        raw[i][1] = row < N ? __ldg(src + 1) : make_uint4(0u, 0u, 0u, 0u);
+    }
+    float sg[16];
+    if constexpr (ROTATE) {
+#pragma unroll
+        for (int e = 0; e < 16; ++e) sg[e] = (float)__ldg(signs + 16 * pos + e);
+    }
+    float v[4][16];
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t w[8] = {raw[i][0].x, raw[i][0].y, raw[i][0].z, raw[i][0].w,
+                               raw[i][1].x, raw[i][1].y, raw[i][1].z, raw[i][1].w};
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            v[i][2 * e] = __uint_as_float(w[e] << 16);
+            v[i][2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
+        }
+        if constexpr (ROTATE) {
+#pragma unroll
+            for (int e = 0; e < 16; ++e) v[i][e] = __fmul_rn(v[i][e], sg[e]);
+#pragma unroll
+            for (int h = 1; h < 16; h <<= 1) {
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    if (e & h) continue;
+                    const float a = v[i][e], b = v[i][e + h];
+                    v[i][e] = __fadd_rn(a, b);
+                    v[i][e + h] = __fsub_rn(a, b);
+                }
+            }
+#pragma unroll
+            for (int bit = 1; bit < 8; bit <<= 1) {   // h = 16 * bit
+#pragma unroll
+                for (int e = 0; e < 16; ++e) v[i][e] = fwht_xlane(v[i][e], lane, bit);
+            }
+        }
+#pragma unroll
+        for (int e = 0; e < 16; ++e) amax = fmaxf(amax, fabsf(v[i][e]));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+    if (lane == 0) warp_max[warp] = amax;
+    __syncthreads();
+    amax = warp_max[0];
+#pragma unroll
+    for (int k = 1; k < 8; ++k) amax = fmaxf(amax, warp_max[k]);
+    const float inv = amax > 0.f ? __fdiv_rn(kE4m3Max, amax) : 0.f;
+    if (threadIdx.x == 0) descale[bh * nblk + blk] = amax > 0.f ? __fdiv_rn(amax, kE4m3Max) : 1.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int row = blk * 128 + warp * 16 + 4 * i + g;
+        if (row >= N) continue;
+        uint32_t c[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            c[q] = pack_e4m3x2(__fmul_rn(v[i][4 * q], inv), __fmul_rn(v[i][4 * q + 1], inv)) |
+                   (pack_e4m3x2(__fmul_rn(v[i][4 * q + 2], inv), __fmul_rn(v[i][4 * q + 3], inv)) << 16);
+        *reinterpret_cast<uint4*>(out + (bh * N + row) * kD + 16 * pos) = make_uint4(c[0], c[1], c[2], c[3]);
     }
 }
 
@@ -735,11 +826,18 @@ attn_status_t launch_fp8_quantize(const void* x, void* out, float* descale, cons
                                   const DeviceInfo& dev) {
     const int nblk = (N + 127) / 128;
     const int npad = (N + 15) / 16 * 16;
-    if (signs)
-        return transpose ? launch_quant_t<true, true>(x, out, descale, signs, BH, N, npad, nblk, stream, dev)
-                         : launch_quant_t<true, false>(x, out, descale, signs, BH, N, npad, nblk, stream, dev);
-    return transpose ? launch_quant_t<false, true>(x, out, descale, signs, BH, N, npad, nblk, stream, dev)
-                     : launch_quant_t<false, false>(x, out, descale, signs, BH, N, npad, nblk, stream, dev);
+    if (!transpose) {
+        dim3 grid((unsigned)nblk, (unsigned)BH);
+        const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
+        uint8_t* ob = static_cast<uint8_t*>(out);
+        if (signs)
+            attn_fp8_quantize_rows_kernel<true><<<grid, kRThreads, 0, stream>>>(xb, ob, descale, signs, N, nblk);
+        else
+            attn_fp8_quantize_rows_kernel<false><<<grid, kRThreads, 0, stream>>>(xb, ob, descale, signs, N, nblk);
+        return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+    }
+    return signs ? launch_quant_t<true, true>(x, out, descale, signs, BH, N, npad, nblk, stream, dev)
+                 : launch_quant_t<false, true>(x, out, descale, signs, BH, N, npad, nblk, stream, dev);
 }
 
 attn_status_t launch_fwd_fp8(const void* q8, const void* k8, const void* vt8, const float* q_descale,

@@ -4,12 +4,18 @@ profiler captures (ncu) of a single launch configuration.
     python -m exact_attention_14_gb300.profile_case --kernel fwd --workload prefill2x
     python -m exact_attention_14_gb300.profile_case --kernel decode --workload decode
     python -m exact_attention_14_gb300.profile_case --kernel bwd --workload prefill --causal 0
+    python -m exact_attention_14_gb300.profile_case --kernel fp8 --workload long
+    python -m exact_attention_14_gb300.profile_case --kernel fp8quant --workload long
+    python -m exact_attention_14_gb300.profile_case --kernel varlen
 
 Workloads: prefill (B=4 H=16 N=2048 d=128), prefill2x (B=8: inputs larger
 than L2), long (B=1 H=32 N=16384), gqa (B=8 Hq=32 Hkv=8 N=4096), decode
 (B=16 Hq=32 Hkv=8 Nmax=32768, lengths 1024..32768) and decode_quarter (the
 same with Nmax=8192, lengths 256..8192: a 512 MiB cache, still larger than
-L2, for multi-pass captures).  Inputs come from the seeded generators.
+L2, for multi-pass captures); varlen is the packed causal prefill batch (16
+sequences of 256..4096 tokens).  fp8 runs attn_fwd_fp8 on E4M3 operands of the
+workload (Q and K rotated by the random-sign Hadamard matrix), fp8quant the
+rotating quantization of its Q.  Inputs come from the seeded generators.
 """
 from __future__ import annotations
 
@@ -18,8 +24,9 @@ import argparse
 import torch
 
 import exact_attention_14_gb300 as ea
-from exact_attention_14_gb300.inputs import (DECODE, GQA, LONG, PREFILL, make_decode_config_inputs,
-                                             make_decode_inputs, make_fwd_inputs)
+from exact_attention_14_gb300.inputs import (DECODE, GQA, LONG, PREFILL, VARLEN, hadamard_signs,
+                                             make_decode_config_inputs, make_decode_inputs,
+                                             make_fwd_inputs, make_varlen_inputs, varlen_lengths)
 
 FWD = {
     "prefill": PREFILL,
@@ -31,13 +38,39 @@ FWD = {
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("--kernel", choices=["fwd", "decode", "bwd"], required=True)
+    ap.add_argument("--kernel", choices=["fwd", "decode", "bwd", "fp8", "fp8quant", "varlen"],
+                    required=True)
     ap.add_argument("--workload", default="prefill")
     ap.add_argument("--causal", type=int, default=-1, help="-1: the workload's first mode")
     ap.add_argument("--iters", type=int, default=3)
     args = ap.parse_args()
     dev = torch.device("cuda", 0)
-    if args.kernel == "bwd":
+    if args.kernel in ("fp8", "fp8quant"):
+        cfg = FWD[args.workload]
+        causal = cfg.causal[0] if args.causal < 0 else bool(args.causal)
+        q, k, v = (t.to(dev) for t in make_fwd_inputs(cfg.B, cfg.Hq, cfg.Hkv, cfg.N, cfg.N, cfg.d,
+                                                     cfg.seed, cfg.outlier_channels))
+        signs = hadamard_signs(cfg.d, seed=cfg.seed).to(dev)
+        q8, qd = ea.fp8_quantize(q, signs)
+        k8, kd = ea.fp8_quantize(k, signs)
+        vt8, vd = ea.fp8_quantize(v, None, transpose=True)
+        o = torch.empty(q.shape, dtype=torch.bfloat16, device=dev)
+        lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
+        for _ in range(args.iters):
+            if args.kernel == "fp8":
+                ea.attn_fwd_fp8(q8, k8, vt8, qd, kd, vd, o, lse, causal=causal,
+                                scale=cfg.scale / cfg.d)
+            else:
+                ea.attn_fp8_quantize(q, q8, qd, signs)
+    elif args.kernel == "varlen":
+        lens = varlen_lengths(VARLEN.n_seqs, VARLEN.len_lo, VARLEN.len_hi, VARLEN.seed)
+        q, k, v, cq, ck = (t.to(dev) for t in make_varlen_inputs(lens, lens, VARLEN.Hq, VARLEN.Hkv,
+                                                                 VARLEN.d, VARLEN.seed))
+        o = torch.empty(q.shape, dtype=torch.bfloat16, device=dev)
+        lse = torch.empty((VARLEN.Hq, q.shape[0]), dtype=torch.float32, device=dev)
+        for _ in range(args.iters):
+            ea.attn_fwd_varlen(q, k, v, o, cq, ck, max(lens), max(lens), lse, causal=VARLEN.causal)
+    elif args.kernel == "bwd":
         cfg = FWD[args.workload]
         causal = cfg.causal[0] if args.causal < 0 else bool(args.causal)
         q, k, v = (t.to(dev) for t in make_fwd_inputs(cfg.B, cfg.Hq, cfg.Hkv, cfg.N, cfg.N, cfg.d,
