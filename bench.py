@@ -162,6 +162,22 @@ def oracle_sample(seconds: float, seed: int = 1):
     return flops / el / 1e12, desc, cores, el
 
 
+def ranks_barrier(world: int) -> None:
+    """Barrier over the launched ranks (no-op for one process)."""
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def ranks_max(values, world: int, device) -> list:
+    """Element-wise maximum of per-rank timings over all ranks (the job's time
+    is its slowest rank's)."""
+    if world == 1:
+        return [float(v) for v in values]
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return t.tolist()
+
+
 def run_reference(args, rank, world):
     if rank != 0:
         return
@@ -241,8 +257,7 @@ def run_ours(args, rank, world, local_rank):
         raise RuntimeError("device error during warm-up")
 
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
-    if world > 1:
-        torch.distributed.barrier()
+    ranks_barrier(world)
     torch.cuda.synchronize()
     with ClockSampler(local_rank) as clk:
         t0 = time.perf_counter()
@@ -251,19 +266,14 @@ def run_ours(args, rank, world, local_rank):
             step(evs[i])
         torch.cuda.synchronize()
         wall = time.perf_counter() - t0
-    if world > 1:
-        torch.distributed.barrier()
+    ranks_barrier(world)
     if ea.attn_last_device_error() != 0:
         raise RuntimeError("device error during the timed region")
     t_nc = sum(e[0].elapsed_time(e[1]) for e in evs) / args.steps * 1e-3
     t_c = sum(e[1].elapsed_time(e[2]) for e in evs) / args.steps * 1e-3
     t_dec = sum(e[2].elapsed_time(e[3]) for e in evs) / args.steps * 1e-3
+    t_nc, t_c, t_dec = ranks_max([t_nc, t_c, t_dec], world, dev)
     t_step = t_nc + t_c + t_dec
-    if world > 1:
-        tt = torch.tensor([t_nc, t_c, t_dec], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        t_nc, t_c, t_dec = tt.tolist()
-        t_step = t_nc + t_c + t_dec
     tflops = world * (f_nc + f_c) / (t_nc + t_c) / 1e12
     dec_gbs = world * dec_bytes / t_dec / 1e9
 
@@ -311,6 +321,7 @@ def run_ours(args, rank, world, local_rank):
         for _ in range(3):
             e2e_step()
         torch.cuda.synchronize()
+        ranks_barrier(world)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(s_in)
         for _ in range(args.steps):
@@ -318,7 +329,7 @@ def run_ours(args, rank, world, local_rank):
         e1.record(s_out)
         e1.synchronize()
         torch.cuda.synchronize()
-        t_e2e = e0.elapsed_time(e1) / args.steps * 1e-3
+        t_e2e = ranks_max([e0.elapsed_time(e1) / args.steps * 1e-3], world, dev)[0]
         # the last step's causal result, read back through the pipeline, equals
         # the headline step's (same inputs, deterministic kernel)
         if not (torch.equal(oh[1], o.cpu()) and torch.equal(lh[1], lse.cpu())):
