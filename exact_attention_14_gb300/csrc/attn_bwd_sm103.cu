@@ -35,10 +35,17 @@
 // warps 2-3 idle, warps 4-7 the elementwise work (one TMEM lane quarter each).
 //
 // TMEM, dkdv (512 columns): [0,128) S^T, then P^T in [0,64); [128,256) dP^T,
-// then dS^T in [128,192); dV [256,256+d); dK [256+d,256+2d).  S^T and dP^T
-// of the next tile are issued right after dV and dK have read P^T and dS^T
-// (one CTA's MMAs run in issue order).
-// TMEM, dq: [0,128) S, then dS in [0,64); [128,256) dP; dQ [256,256+d).
+// then dS^T in [128,192); dV [256,256+d); dK [256+d,256+2d).  The P^T / dS^T
+// warps work in two phases per Q tile (P^T from S^T, then dS^T from dP^T), and
+// the MMAs interleave with them: dV(i) and S^T(i+1) run during phase 2 of tile
+// i, dK(i) and dP^T(i+1) during phase 1 of tile i+1 (each next-tile product is
+// issued after the one that reads its columns: one CTA's MMAs run in issue
+// order).
+// TMEM, dq: S in [0,128) for even K/V tiles and [384,512) for odd ones (dS over
+// its first 64 columns), dP [128,256), dQ [256,256+d).  K streams through a
+// 3-stage ring and V through a 2-stage one; S_{j+2} is issued as soon as dQ_j
+// has read tile j's S buffer, so the dS warps' exponentials for tile j+1
+// (phase 1) overlap dQ_j and dP_{j+1}.
 #include <cmath>
 #include <cstdint>
 
@@ -84,7 +91,7 @@ struct BwdParams {
 struct __align__(8) BwdBars {
     uint64_t kv_full;
     uint64_t qd_full[2], qd_empty[2];
-    uint64_t s_full, p_full, acc_full, drain;
+    uint64_t s_full, dp_full, p_full, ds_full, acc_full, drain;
     uint32_t tmem_base;
     int abort;
 };
@@ -242,25 +249,38 @@ __device__ void bwd_mma(uint8_t* smem, BwdBars* bars, uint32_t tmem, const BwdWo
         if (ok) {
             tc_fence_after();
             issue_kmajor<D>(tS, k_kmaj, q_kmaj(0), idS);
-            issue_kmajor<D>(tdP, v_kmaj, do_kmaj(0), idS);
             mma_commit_warp(smem_u32(&bars->s_full));
+            issue_kmajor<D>(tdP, v_kmaj, do_kmaj(0), idS);
+            mma_commit_warp(smem_u32(&bars->dp_full));
         }
+        // Per Q tile i: dV(i) once P^T(i) is in TMEM, then S^T(i+1) into the
+        // columns dV(i) has read; dK(i) once dS^T(i) is in TMEM, then dP^T(i+1)
+        // into the columns dK(i) has read (one CTA's MMAs run in issue order).
+        // The P^T / dS^T warps work on tile i while the tensor cores run
+        // dV(i), S^T(i+1) and then dK(i), dP^T(i+1).
         for (int i = 0; i < w.n_tiles && ok; ++i) {
             const int st = i & 1;
+            const int st1 = (i + 1) & 1;
+            const bool more = i + 1 < w.n_tiles;
             ok = wait_all(smem_u32(&bars->p_full), i & 1, 32);
             if (!ok) break;
             tc_fence_after();
-            issue_tmem_a(tdV, tS, do_mn(st), idKV, i > 0);
-            issue_tmem_a(tdK, tdP, q_mn(st), idKV, i > 0);
-            mma_commit_warp(smem_u32(&bars->qd_empty[st]));  // Q and dO of this tile are read
-            if (i + 1 < w.n_tiles) {
-                const int st1 = (i + 1) & 1;
+            issue_tmem_a(tdV, tS, do_mn(st), idKV, i > 0);          // dV += P^T dO
+            if (more) {
                 ok = wait_all(smem_u32(&bars->qd_full[st1]), ((i + 1) >> 1) & 1, 0);
                 if (!ok) break;
                 tc_fence_after();
-                issue_kmajor<D>(tS, k_kmaj, q_kmaj(st1), idS);
-                issue_kmajor<D>(tdP, v_kmaj, do_kmaj(st1), idS);
+                issue_kmajor<D>(tS, k_kmaj, q_kmaj(st1), idS);       // S^T(i+1)
                 mma_commit_warp(smem_u32(&bars->s_full));
+            }
+            ok = wait_all(smem_u32(&bars->ds_full), i & 1, 32);
+            if (!ok) break;
+            tc_fence_after();
+            issue_tmem_a(tdK, tdP, q_mn(st), idKV, i > 0);          // dK += dS^T Q
+            mma_commit_warp(smem_u32(&bars->qd_empty[st]));         // Q and dO of tile i are read
+            if (more) {
+                issue_kmajor<D>(tdP, v_kmaj, do_kmaj(st1), idS);     // dP^T(i+1)
+                mma_commit_warp(smem_u32(&bars->dp_full));
             }
         }
         if (ok) mma_commit_warp(smem_u32(&bars->acc_full));
@@ -275,23 +295,22 @@ __device__ void bwd_mma(uint8_t* smem, BwdBars* bars, uint32_t tmem, const BwdWo
 // ---------------------------------------------------------------------------
 // P / dS warpgroup (one key row per thread) and the dK / dV epilogue
 // ---------------------------------------------------------------------------
+// P^T = 2^(S^T c - lse2) for 32 query columns [qc, qc + 32) of this thread's
+// key row, kept in fp32 (pf) and packed to bf16 pairs (pp).  lim: query column
+// qc + x is allowed iff qc + x >= lim (causal), else all.  The tile's lse2
+// comes from shared memory 4 at a time (broadcast).
 template <bool MASKED>
-__device__ __forceinline__ void p_ds_chunk(const uint32_t (&s)[32], const uint32_t (&dp)[32],
-                                           uint32_t lse2s, uint32_t ds_vec, int qc, float c,
-                                           int lim, uint32_t (&pp)[16], uint32_t (&dd)[16]) {
-    // lim: query column qc + x is allowed iff qc + x >= lim (causal), else all.
-    // The tile's lse2 and D come from shared memory 4 at a time (broadcast).
+__device__ __forceinline__ void p_chunk(const uint32_t (&s)[32], uint32_t lse2s, int qc, float c,
+                                        int lim, float (&pf)[32], uint32_t (&pp)[16]) {
     const uint64_t c2 = f2(c, c);
 #pragma unroll
     for (int x4 = 0; x4 < 8; ++x4) {
         const float4 l4 = lds128_f32(lse2s + 4u * (qc + 4 * x4));
-        const float4 d4 = lds128_f32(ds_vec + 4u * (qc + 4 * x4));
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
             const int x = 2 * x4 + h;
             const int q = qc + 2 * x;
             const uint64_t nl = h == 0 ? f2(-l4.x, -l4.y) : f2(-l4.z, -l4.w);
-            const uint64_t nd = h == 0 ? f2(-d4.x, -d4.y) : f2(-d4.z, -d4.w);
             float a0, a1;
             f2_split(f2_fma(f2(__uint_as_float(s[2 * x]), __uint_as_float(s[2 * x + 1])), c2, nl), a0, a1);
             float p0 = ex2(a0), p1 = ex2(a1);
@@ -299,10 +318,27 @@ __device__ __forceinline__ void p_ds_chunk(const uint32_t (&s)[32], const uint32
                 p0 = q >= lim ? p0 : 0.f;
                 p1 = q + 1 >= lim ? p1 : 0.f;
             }
-            float d0, d1;
-            f2_split(f2_mul(f2(p0, p1), f2_add(f2(__uint_as_float(dp[2 * x]), __uint_as_float(dp[2 * x + 1])), nd)),
-                     d0, d1);
+            pf[2 * x] = p0;
+            pf[2 * x + 1] = p1;
             pp[x] = pack_bf16x2(p0, p1);
+        }
+    }
+}
+
+// dS^T = P^T o (dP^T - D) for the same 32 query columns, packed to bf16 pairs.
+__device__ __forceinline__ void ds_chunk_t(const float (&pf)[32], const uint32_t (&dp)[32],
+                                           uint32_t ds_vec, int qc, uint32_t (&dd)[16]) {
+#pragma unroll
+    for (int x4 = 0; x4 < 8; ++x4) {
+        const float4 d4 = lds128_f32(ds_vec + 4u * (qc + 4 * x4));
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int x = 2 * x4 + h;
+            const uint64_t nd = h == 0 ? f2(-d4.x, -d4.y) : f2(-d4.z, -d4.w);
+            float d0, d1;
+            f2_split(f2_mul(f2(pf[2 * x], pf[2 * x + 1]),
+                            f2_add(f2(__uint_as_float(dp[2 * x]), __uint_as_float(dp[2 * x + 1])), nd)),
+                     d0, d1);
             dd[x] = pack_bf16x2(d0, d1);
         }
     }
@@ -351,25 +387,48 @@ __device__ void bwd_pds(int wq, int lane, uint8_t* smem, BwdBars* bars, uint32_t
         // causal: query q0 + x sees key jg iff x >= jg - off - q0
         const int lim = jg - p.off - q0;
         const bool masked = p.causal && (q0 + p.off < w.k0 + kBT - 1);
-#pragma unroll 1
-        for (int cc = 0; cc < 4; ++cc) {
-            uint32_t s[32], dp[32];
-            tmem_ld32(tS + cc * 32, s);
+        // Phase 1: P^T from S^T, kept in registers and written as bf16 over the
+        // S^T columns already read; releases dV(i) and S^T(i+1).
+        float pf0[32], pf1[32], pf2[32], pf3[32];
+        auto phase1 = [&](int cc, float (&pf)[32]) {
+            uint32_t sv[32], pp[16];
+            tmem_ld32(tS + cc * 32, sv);
+            tmem_wait_ld();
+            if (masked)
+                p_chunk<true>(sv, lse2s, cc * 32, p.c, lim, pf, pp);
+            else
+                p_chunk<false>(sv, lse2s, cc * 32, p.c, lim, pf, pp);
+            tmem_st16(tS + cc * 16, pp);
+        };
+        phase1(0, pf0);
+        phase1(1, pf1);
+        phase1(2, pf2);
+        phase1(3, pf3);
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&bars->p_full));
+        // Phase 2: dS^T from P^T and dP^T, written as bf16 over the dP^T
+        // columns already read; releases dK(i) and dP^T(i+1).
+        ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&bars->dp_full), i & 1, abort_flag, 32));
+        if (!ok) break;
+        tc_fence_after();
+        auto phase2 = [&](int cc, const float (&pf)[32]) {
+            uint32_t dp[32], dd[16];
             tmem_ld32(tdP + cc * 32, dp);
             tmem_wait_ld();
-            uint32_t pp[16], dd[16];
-            if (masked)
-                p_ds_chunk<true>(s, dp, lse2s, ds_vec, cc * 32, p.c, lim, pp, dd);
-            else
-                p_ds_chunk<false>(s, dp, lse2s, ds_vec, cc * 32, p.c, lim, pp, dd);
-            tmem_st16(tS + cc * 16, pp);   // P^T over S^T columns already read
-            tmem_st16(tdP + cc * 16, dd);  // dS^T over dP^T columns already read
-        }
+            ds_chunk_t(pf, dp, ds_vec, cc * 32, dd);
+            tmem_st16(tdP + cc * 16, dd);
+        };
+        phase2(0, pf0);
+        phase2(1, pf1);
+        phase2(2, pf2);
+        phase2(3, pf3);
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) {
-            mbar_arrive(smem_u32(&bars->p_full));
+            mbar_arrive(smem_u32(&bars->ds_full));
             mbar_arrive(smem_u32(&bars->qd_empty[st]));
         }
     }
@@ -443,7 +502,9 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tq, const __grid_consta
             mbar_init(smem_u32(&bars->qd_empty[s]), 1 + 4);  // dK commit + 4 P/dS warps
         }
         mbar_init(smem_u32(&bars->s_full), 1);
+        mbar_init(smem_u32(&bars->dp_full), 1);
         mbar_init(smem_u32(&bars->p_full), 4);
+        mbar_init(smem_u32(&bars->ds_full), 4);
         mbar_init(smem_u32(&bars->acc_full), 1);
         mbar_init(smem_u32(&bars->drain), 1);
         bars->abort = 0;
@@ -483,8 +544,9 @@ struct DqCfg {
     static constexpr int kTile = kBT * D * 2;
     static constexpr int kQ = 0;
     static constexpr int kDO = kTile;
-    static constexpr int kRing = 2 * kTile;     // 2 stages of (K, V)
-    static constexpr int kBar = kRing + 4 * kTile;
+    static constexpr int kKRing = 2 * kTile;    // 3 stages of K
+    static constexpr int kVRing = 5 * kTile;    // 2 stages of V
+    static constexpr int kBar = 7 * kTile;
     static constexpr int kLayout = kBar + 256;
     static constexpr int kSmemBytes =
         kLayout + 1024 < kMaxSmemPerBlock ? kLayout + 1024 : kMaxSmemPerBlock;
@@ -493,8 +555,8 @@ struct DqCfg {
 
 struct __align__(8) DqBars {
     uint64_t q_full;
-    uint64_t kv_full[2], kv_empty[2];
-    uint64_t s_full, p_full, dq_full, drain;
+    uint64_t k_full[3], k_empty[3], v_full[2], v_empty[2];
+    uint64_t s_full[2], dp_full, ds_full, dq_full, drain;  // s_full[b]: the S in buffer b
     uint32_t tmem_base;
     int abort;
 };
@@ -559,32 +621,49 @@ __device__ void dq_producer(const CUtensorMap* tq, const CUtensorMap* tk, const 
         }
     }
     __syncwarp();
+    // K_j into stage j % 3 (free once dQ(j-3) has read it), V_j into stage
+    // j % 2 (free once dP(j-2) has read it).
     bool ok = true;
-    int issued = 0;
+    int nk = 0, nv = 0;  // K and V loads issued
     for (int j = 0; j < w.n_kv && ok; ++j) {
-        const int st = j & 1;
-        if (j >= 2)
-            ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&bars->kv_empty[st]), ((j >> 1) - 1) & 1,
+        const int sk = j % 3, sv = j & 1;
+        if (j >= 3)
+            ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&bars->k_empty[sk]), ((j / 3) - 1) & 1,
                                                    abort_flag));
         if (!ok) break;
         if (leader) {
-            const uint32_t bar = smem_u32(&bars->kv_full[st]);
-            mbar_arrive_expect_tx(bar, 2 * C::kTile);
-            const uint32_t dk = smem_u32(smem + C::kRing + st * 2 * C::kTile);
+            const uint32_t bar = smem_u32(&bars->k_full[sk]);
+            mbar_arrive_expect_tx(bar, C::kTile);
+            const uint32_t dst = smem_u32(smem + C::kKRing + sk * C::kTile);
 #pragma unroll
-            for (int c = 0; c < D / 64; ++c) {
-                tma_load_3d(dk + c * 16384, tk, bar, 64 * c, j * kBT, kvh);
-                tma_load_3d(dk + C::kTile + c * 16384, tv, bar, 64 * c, j * kBT, kvh);
-            }
+            for (int c = 0; c < D / 64; ++c) tma_load_3d(dst + c * 16384, tk, bar, 64 * c, j * kBT, kvh);
         }
         __syncwarp();
-        ++issued;
+        ++nk;
+        if (j >= 2)
+            ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&bars->v_empty[sv]), ((j >> 1) - 1) & 1,
+                                                   abort_flag));
+        if (!ok) break;
+        if (leader) {
+            const uint32_t bar = smem_u32(&bars->v_full[sv]);
+            mbar_arrive_expect_tx(bar, C::kTile);
+            const uint32_t dst = smem_u32(smem + C::kVRing + sv * C::kTile);
+#pragma unroll
+            for (int c = 0; c < D / 64; ++c) tma_load_3d(dst + c * 16384, tv, bar, 64 * c, j * kBT, kvh);
+        }
+        __syncwarp();
+        ++nv;
     }
     if (!ok && leader) atomicOr(err, kErrTimeout), *((volatile int*)&bars->abort) = 1;
+    // Drain: every issued copy lands before the CTA may exit.
     mbar_wait(smem_u32(&bars->q_full), 0, nullptr);
-    for (int st = 0; st < 2 && st < issued; ++st) {
-        const int uses = (issued - st + 1) / 2;
-        mbar_wait(smem_u32(&bars->kv_full[st]), (uses - 1) & 1, nullptr);
+    for (int sk = 0; sk < 3 && sk < nk; ++sk) {
+        const int uses = (nk - sk + 2) / 3;
+        mbar_wait(smem_u32(&bars->k_full[sk]), (uses - 1) & 1, nullptr);
+    }
+    for (int sv = 0; sv < 2 && sv < nv; ++sv) {
+        const int uses = (nv - sv + 1) / 2;
+        mbar_wait(smem_u32(&bars->v_full[sv]), (uses - 1) & 1, nullptr);
     }
     __syncwarp();
 }
@@ -597,40 +676,49 @@ __device__ void dq_mma(uint8_t* smem, DqBars* bars, uint32_t tmem, const DqWork&
     const bool leader = elect_one();
     const uint32_t idS = make_idesc_bf16(128, 128, 0, 0);
     const uint32_t idQ = make_idesc_bf16(128, D, 0, 1);
-    const uint32_t tS = tmem, tdP = tmem + 128, tdQ = tmem + 256;
+    const uint32_t tdP = tmem + 128, tdQ = tmem + 256;
+    auto tS = [&](int j) { return tmem + ((j & 1) ? 384u : 0u); };  // S buffer of tile j
     const uint32_t q_k = sdesc_lo(smem_u32(smem + C::kQ), 16);
     const uint32_t do_k = sdesc_lo(smem_u32(smem + C::kDO), 16);
-    auto k_k = [&](int st) { return sdesc_lo(smem_u32(smem + C::kRing + st * 2 * C::kTile), 16); };
-    auto v_k = [&](int st) { return sdesc_lo(smem_u32(smem + C::kRing + st * 2 * C::kTile + C::kTile), 16); };
-    auto k_mn = [&](int st) { return sdesc_lo(smem_u32(smem + C::kRing + st * 2 * C::kTile), 16384); };
+    auto k_k = [&](int sk) { return sdesc_lo(smem_u32(smem + C::kKRing + sk * C::kTile), 16); };
+    auto k_mn = [&](int sk) { return sdesc_lo(smem_u32(smem + C::kKRing + sk * C::kTile), 16384); };
+    auto v_k = [&](int sv) { return sdesc_lo(smem_u32(smem + C::kVRing + sv * C::kTile), 16); };
     auto wait_all = [&](uint32_t bar, uint32_t parity, int polls) {
         return __all_sync(0xFFFFFFFFu, mbar_wait(bar, parity, abort_flag, polls));
     };
+    auto issue_s = [&](int j) {  // S_j = Q K_j^T into buffer j & 1
+        if (!wait_all(smem_u32(&bars->k_full[j % 3]), (uint32_t)((j / 3) & 1), 0)) return false;
+        tc_fence_after();
+        issue_kmajor<D>(tS(j), q_k, k_k(j % 3), idS);
+        mma_commit_warp(smem_u32(&bars->s_full[j & 1]));
+        return true;
+    };
+    auto issue_dp = [&](int j) {  // dP_j = dO V_j^T
+        if (!wait_all(smem_u32(&bars->v_full[j & 1]), (uint32_t)((j >> 1) & 1), 0)) return false;
+        tc_fence_after();
+        issue_kmajor<D>(tdP, do_k, v_k(j & 1), idS);
+        mma_commit_warp(smem_u32(&bars->v_empty[j & 1]));  // V_j is read
+        mma_commit_warp(smem_u32(&bars->dp_full));
+        return true;
+    };
+    // Order: S_0, dP_0, S_1; then per tile j, once dS_j is in TMEM: dQ += dS_j
+    // K_j, dP_{j+1} (into the dP columns the dS warps have read), S_{j+2} (into
+    // the buffer dQ_j has read; one CTA's MMAs run in issue order).  The dS
+    // warps' exponentials for tile j+1 overlap dQ_j and dP_{j+1}.
     bool ok = true;
     if (w.n_kv > 0) {
-        ok = wait_all(smem_u32(&bars->q_full), 0, 0) && wait_all(smem_u32(&bars->kv_full[0]), 0, 0);
-        if (ok) {
-            tc_fence_after();
-            issue_kmajor<D>(tS, q_k, k_k(0), idS);
-            issue_kmajor<D>(tdP, do_k, v_k(0), idS);
-            mma_commit_warp(smem_u32(&bars->s_full));
-        }
+        ok = wait_all(smem_u32(&bars->q_full), 0, 0);
+        if (ok) ok = issue_s(0);
+        if (ok) ok = issue_dp(0);
+        if (ok && w.n_kv > 1) ok = issue_s(1);
         for (int j = 0; j < w.n_kv && ok; ++j) {
-            const int st = j & 1;
-            ok = wait_all(smem_u32(&bars->p_full), j & 1, 32);
+            ok = wait_all(smem_u32(&bars->ds_full), j & 1, 32);
             if (!ok) break;
             tc_fence_after();
-            issue_tmem_a(tdQ, tS, k_mn(st), idQ, j > 0);      // dQ += dS K_j
-            mma_commit_warp(smem_u32(&bars->kv_empty[st]));  // K_j, V_j are read
-            if (j + 1 < w.n_kv) {
-                const int st1 = (j + 1) & 1;
-                ok = wait_all(smem_u32(&bars->kv_full[st1]), ((j + 1) >> 1) & 1, 0);
-                if (!ok) break;
-                tc_fence_after();
-                issue_kmajor<D>(tS, q_k, k_k(st1), idS);
-                issue_kmajor<D>(tdP, do_k, v_k(st1), idS);
-                mma_commit_warp(smem_u32(&bars->s_full));
-            }
+            issue_tmem_a(tdQ, tS(j), k_mn(j % 3), idQ, j > 0);  // dQ += dS_j K_j
+            mma_commit_warp(smem_u32(&bars->k_empty[j % 3]));   // K_j is read (S_j, dQ_j)
+            if (j + 1 < w.n_kv && !(ok = issue_dp(j + 1))) break;
+            if (j + 2 < w.n_kv && !(ok = issue_s(j + 2))) break;
         }
         if (ok) mma_commit_warp(smem_u32(&bars->dq_full));
     }
@@ -640,12 +728,11 @@ __device__ void dq_mma(uint8_t* smem, DqBars* bars, uint32_t tmem, const DqWork&
     __syncwarp();
 }
 
-// dS = 2^(S c - lse2) o (dP - D) for 32 key columns of this thread's query row.
-// lim: key column kc + x is allowed iff kc + x <= lim (causal), else all.
+// P = 2^(S c - lse2) for 32 key columns [kc, kc + 32) of this thread's query
+// row (fp32).  lim: key column kc + x is allowed iff kc + x <= lim (causal).
 template <bool MASKED>
-__device__ __forceinline__ void ds_chunk(const uint32_t (&s)[32], const uint32_t (&dp)[32],
-                                         uint64_t c2, uint64_t nl2, uint64_t nd2, int kc, int lim,
-                                         uint32_t (&dd)[16]) {
+__device__ __forceinline__ void p_row_chunk(const uint32_t (&s)[32], uint64_t c2, uint64_t nl2,
+                                            int kc, int lim, float (&pf)[32]) {
 #pragma unroll
     for (int x = 0; x < 16; ++x) {
         const int col = kc + 2 * x;
@@ -656,8 +743,19 @@ __device__ __forceinline__ void ds_chunk(const uint32_t (&s)[32], const uint32_t
             p0 = col <= lim ? p0 : 0.f;
             p1 = col + 1 <= lim ? p1 : 0.f;
         }
+        pf[2 * x] = p0;
+        pf[2 * x + 1] = p1;
+    }
+}
+
+// dS = P o (dP - D) for the same 32 columns, packed to bf16 pairs.
+__device__ __forceinline__ void ds_row_chunk(const float (&pf)[32], const uint32_t (&dp)[32],
+                                             uint64_t nd2, uint32_t (&dd)[16]) {
+#pragma unroll
+    for (int x = 0; x < 16; ++x) {
         float d0, d1;
-        f2_split(f2_mul(f2(p0, p1), f2_add(f2(__uint_as_float(dp[2 * x]), __uint_as_float(dp[2 * x + 1])), nd2)),
+        f2_split(f2_mul(f2(pf[2 * x], pf[2 * x + 1]),
+                        f2_add(f2(__uint_as_float(dp[2 * x]), __uint_as_float(dp[2 * x + 1])), nd2)),
                  d0, d1);
         dd[x] = pack_bf16x2(d0, d1);
     }
@@ -668,7 +766,7 @@ __device__ void dq_ds(int wq, int lane, DqBars* bars, uint32_t tmem, const BwdPa
                       const DqWork& w, unsigned int* err) {
     const volatile int* abort_flag = &bars->abort;
     const uint32_t lane_off = uint32_t(wq * 32) << 16;
-    const uint32_t tS = tmem + lane_off, tdP = tmem + 128 + lane_off;
+    const uint32_t tdP = tmem + 128 + lane_off;
     const int row = w.q0 + wq * 32 + lane;
     const size_t bh = (size_t)w.b * p.Hq + w.hq;
     const float lse2 = p.lse2[bh * p.Nq_pad + row];  // +inf past Nq: P = 0
@@ -676,28 +774,46 @@ __device__ void dq_ds(int wq, int lane, DqBars* bars, uint32_t tmem, const BwdPa
     const uint64_t c2 = f2(p.c, p.c), nl2 = f2(-lse2, -lse2), nd2 = f2(-dval, -dval);
     bool ok = true;
     for (int j = 0; j < w.n_kv && ok; ++j) {
-        ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&bars->s_full), j & 1, abort_flag, 32));
+        const uint32_t tS = tmem + ((j & 1) ? 384u : 0u) + lane_off;
+        ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&bars->s_full[j & 1]), (j >> 1) & 1, abort_flag, 32));
         if (!ok) break;
         tc_fence_after();
         const int lim = row + p.off - j * kBT;  // causal: key column c allowed iff c <= lim
         const bool masked = __any_sync(0xFFFFFFFFu, p.causal && lim < kBT - 1);
-#pragma unroll 1
-        for (int cc = 0; cc < 4; ++cc) {
-            uint32_t sv[32], dp[32];
+        // Phase 1: P from S (needs S_j only; runs while dQ_{j-1} and dP_j compute)
+        float pf0[32], pf1[32], pf2[32], pf3[32];
+        auto phase1 = [&](int cc, float (&pf)[32]) {
+            uint32_t sv[32];
             tmem_ld32(tS + cc * 32, sv);
+            tmem_wait_ld();
+            if (masked)
+                p_row_chunk<true>(sv, c2, nl2, cc * 32, p.causal ? lim : kBT, pf);
+            else
+                p_row_chunk<false>(sv, c2, nl2, cc * 32, kBT, pf);
+        };
+        phase1(0, pf0);
+        phase1(1, pf1);
+        phase1(2, pf2);
+        phase1(3, pf3);
+        // Phase 2: dS from P and dP, as bf16 over the S columns (all read)
+        ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&bars->dp_full), j & 1, abort_flag, 32));
+        if (!ok) break;
+        tc_fence_after();
+        auto phase2 = [&](int cc, const float (&pf)[32]) {
+            uint32_t dp[32], dd[16];
             tmem_ld32(tdP + cc * 32, dp);
             tmem_wait_ld();
-            uint32_t dd[16];
-            if (masked)
-                ds_chunk<true>(sv, dp, c2, nl2, nd2, cc * 32, p.causal ? lim : kBT, dd);
-            else
-                ds_chunk<false>(sv, dp, c2, nl2, nd2, cc * 32, kBT, dd);
-            tmem_st16(tS + cc * 16, dd);  // dS over S columns already read
-        }
+            ds_row_chunk(pf, dp, nd2, dd);
+            tmem_st16(tS + cc * 16, dd);
+        };
+        phase2(0, pf0);
+        phase2(1, pf1);
+        phase2(2, pf2);
+        phase2(3, pf3);
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&bars->p_full));
+        if (lane == 0) mbar_arrive(smem_u32(&bars->ds_full));
     }
     if (ok && w.n_kv > 0)
         ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&bars->dq_full), 0, abort_flag));
@@ -747,12 +863,17 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
     const DqWork w = dq_work(p);
     if (threadIdx.x == 0) {
         mbar_init(smem_u32(&bars->q_full), 1);
-        for (int s = 0; s < 2; ++s) {
-            mbar_init(smem_u32(&bars->kv_full[s]), 1);
-            mbar_init(smem_u32(&bars->kv_empty[s]), 1);
+        for (int s = 0; s < 3; ++s) {
+            mbar_init(smem_u32(&bars->k_full[s]), 1);
+            mbar_init(smem_u32(&bars->k_empty[s]), 1);
         }
-        mbar_init(smem_u32(&bars->s_full), 1);
-        mbar_init(smem_u32(&bars->p_full), 4);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(smem_u32(&bars->v_full[s]), 1);
+            mbar_init(smem_u32(&bars->v_empty[s]), 1);
+            mbar_init(smem_u32(&bars->s_full[s]), 1);
+        }
+        mbar_init(smem_u32(&bars->dp_full), 1);
+        mbar_init(smem_u32(&bars->ds_full), 4);
         mbar_init(smem_u32(&bars->dq_full), 1);
         mbar_init(smem_u32(&bars->drain), 1);
         bars->abort = 0;
