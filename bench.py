@@ -210,7 +210,8 @@ def run_reference(args, rank, world):
 def run_ours(args, rank, world, local_rank):
     import exact_attention_14_gb300 as ea
     from exact_attention_14_gb300.inputs import DECODE, LONG, PREFILL, VARLEN, hadamard_signs, \
-        make_config_inputs, make_decode_config_inputs, make_varlen_inputs, varlen_lengths
+        make_config_inputs, make_decode_config_inputs, make_fwd_inputs, make_varlen_inputs, \
+        varlen_lengths
 
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
@@ -475,6 +476,37 @@ def run_ours(args, rank, world, local_rank):
                "quantize_frac_of_hbm": qbytes / tq_ / 1e9 / peaks["hbm_gbs"],
                "with_quantize_tflops": f8 / (ta_ + tq_) / 1e12}
 
+    # Head dim 256 (a follow-on row, timed apart from the step): the prefill
+    # shape B4 H16 N2048 at d = 256 on the one-Q-tile-per-CTA kernel.
+    wide = None
+    if not args.no_wide:
+        wq_, wk_, wv_ = (t.to(dev) for t in make_fwd_inputs(cfg.B, cfg.Hq, cfg.Hkv, cfg.N, cfg.N,
+                                                             256, seed=6))
+        wo = torch.empty(wq_.shape, dtype=torch.bfloat16, device=dev)
+        wl = torch.empty(wq_.shape[:3], dtype=torch.float32, device=dev)
+        for _ in range(args.warmup):
+            for c in (False, True):
+                flush.zero_()
+                ea.attn_fwd(wq_, wk_, wv_, wo, wl, causal=c, stream=stream)
+        wev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+        torch.cuda.synchronize()
+        for i in range(args.steps):
+            for m, c in enumerate((False, True)):
+                flush.zero_()
+                wev[i][2 * m].record(stream)
+                ea.attn_fwd(wq_, wk_, wv_, wo, wl, causal=c, stream=stream)
+                wev[i][2 * m + 1].record(stream)
+        torch.cuda.synchronize()
+        if ea.attn_last_device_error() != 0:
+            raise RuntimeError("device error in the d=256 leg")
+        tw = [sum(e[2 * m].elapsed_time(e[2 * m + 1]) for e in wev) / args.steps * 1e-3 for m in range(2)]
+        fw = [fwd_flops(cfg.B, cfg.Hq, cfg.N, 256, c) for c in (False, True)]
+        wide = {"kernel": "attn_fwd_wide_kernel<256> (one Q tile per CTA, 64-key tiles, two S buffers)",
+                "workload": f"prefill B={cfg.B} H={cfg.Hq} N={cfg.N} d=256",
+                "noncausal_tflops": fw[0] / tw[0] / 1e12, "causal_tflops": fw[1] / tw[1] / 1e12,
+                "noncausal_ms": 1e3 * tw[0], "causal_ms": 1e3 * tw[1],
+                "frac_of_bf16_peak": sum(fw) / sum(tw) / 1e12 / peaks["bf16_tflops"]}
+
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         tf, desc, cores, _ = oracle_sample(args.cpu_seconds)
@@ -518,6 +550,7 @@ def run_ours(args, rank, world, local_rank):
                    "algorithmic_bytes": dec_bytes, "frac_of_hbm": dec_gbs / world / peaks["hbm_gbs"],
                    "sum_seqlen": sum_len},
         "roofline": roof, "roofline_decode": roof_dec, "bwd": bwd, "varlen": varlen, "fp8": fp8,
+        "wide": wide,
         "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": (2 + ea.attn_decode_kernel_launches(DECODE.B, DECODE.Hq, DECODE.Hkv,
                                                             DECODE.Nmax, DECODE.d)) * args.steps,
@@ -537,6 +570,7 @@ def main():
     ap.add_argument("--no-bwd", action="store_true", help="skip the backward leg")
     ap.add_argument("--no-varlen", action="store_true", help="skip the packed varlen leg")
     ap.add_argument("--no-fp8", action="store_true", help="skip the FP8 leg")
+    ap.add_argument("--no-wide", action="store_true", help="skip the d=256 leg")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))

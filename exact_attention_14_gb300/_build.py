@@ -15,8 +15,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libgb300_attn.so")
 
-SOURCES = ["attn_api.cu", "attn_fwd_sm103.cu", "attn_decode_sm103.cu", "attn_bwd_sm103.cu",
-           "attn_fp8_sm103.cu"]
+SOURCES = ["attn_api.cu", "attn_fwd_sm103.cu", "attn_fwd_wide_sm103.cu", "attn_decode_sm103.cu",
+           "attn_bwd_sm103.cu", "attn_fp8_sm103.cu"]
 HEADERS = ["ptx.cuh", "fwd_sched.h", "internal.h"]
 
 NVCC = os.environ.get("NVCC", "nvcc")

@@ -199,7 +199,7 @@ attn_status_t check_fwd(const void* q, const void* k, const void* v, const void*
     if (Nq < 1 || Nk < 1 || Nq > kMaxLen || Nk > kMaxLen) return ATTN_ERR_INVALID_ARG;
     if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
     if (causal && Nq > Nk) return ATTN_ERR_INVALID_ARG;
-    if (!head_dim_supported(d)) return ATTN_ERR_UNSUPPORTED;
+    if (!fwd_head_dim_supported(d)) return ATTN_ERR_UNSUPPORTED;
     return ATTN_OK;
 }
 
@@ -299,6 +299,7 @@ attn_status_t attn_fwd_varlen(const void* q, const void* k, const void* v, void*
                                  scale, o_dtype);
     if (st != ATTN_OK) return st;
     if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
+    if (!head_dim_supported(d)) return ATTN_ERR_UNSUPPORTED;
     DeviceInfo dev;
     if ((st = current_device_info(&dev)) != ATTN_OK) return st;
     return launch_fwd_varlen(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, B, Hq, Hkv, total_q,
@@ -320,6 +321,7 @@ attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* 
                        size_t workspace_bytes, void* stream) {
     attn_status_t st = check_fwd(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, d, causal, scale, o_dtype);
     if (st != ATTN_OK) return st;
+    if (!head_dim_supported(d)) return ATTN_ERR_UNSUPPORTED;  // the backward stops at d = 128
     if (!dout || !lse || !dq || !dk || !dv) return ATTN_ERR_INVALID_ARG;
     if (!aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
         return ATTN_ERR_INVALID_ARG;

@@ -988,6 +988,9 @@ uint32_t next_queue_slot() {
 attn_status_t launch_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
                          int B, int Hq, int Hkv, int Nq, int Nk, int d, int causal, float scale,
                          attn_out_dtype_t o_dtype, cudaStream_t stream, const DeviceInfo& dev) {
+    if (d > 128)
+        return launch_fwd_wide(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, d, causal, scale, o_dtype, stream,
+                               dev);
     FwdParams p;
     p.shape = make_fwd_shape(B, Hq, Hkv, Nq, Nk, d, causal);
     if (p.shape.units >= (1ll << 31)) return ATTN_ERR_UNSUPPORTED;

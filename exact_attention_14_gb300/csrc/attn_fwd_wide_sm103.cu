@@ -1,0 +1,613 @@
+// attn_fwd_wide_sm103.cu -- fused attention forward for head dims above 128
+// (d in (128, 256], run on kernels built for D = 192 and D = 256).
+//
+// The 128-column forward keeps two 128-row Q tiles in flight per CTA, each with
+// a 128-column S and a d-column O in tensor memory; at d > 128 two O
+// accumulators no longer fit next to their S tiles in the 512 TMEM columns.
+// This kernel keeps one Q tile per CTA and overlaps the other way: K/V tiles
+// of 64 keys, and two S buffers of 64 columns, so S(j+1) is computed while the
+// softmax warps work on S(j) (TMEM: S0 [0,64), S1 [64,128), O [128, 128+D)).
+// Per 64-key tile the tensor cores do 2 * 128 * 64 * D * 2 FLOPs, which at
+// D = 256 outweighs the softmax work of the tile.
+//
+// Roles (8 warps): warp 0 TMA producer (Q once per unit, K and V through
+// 2-slot rings of their own), warp 1 MMA issuer and TMEM owner, warps 2-3 idle,
+// warps 4-7 softmax (one query row per thread) and epilogue.  Persistent CTAs
+// take units (b, query head, 128-row Q tile) from a device-side queue in the
+// order of fwd_sched.h (L2 sections; causal longest-first).
+//
+// MMA order per unit of n tiles: S(0), S(1), then for each tile j once P(j) is
+// in TMEM: PV(j), S(j + 2) into the buffer PV(j) has read (one CTA's MMAs run
+// in issue order).  Because S(j + 1) may finish before PV(j - 1), the softmax
+// rescales O (lecture notes 5.3, tau = 8) only after waiting for the P.V
+// product of the previous tile (a barrier committed after every PV).
+//
+// Method: lecture notes "Optimizing Attention for Modern Hardware:
+// FlashAttention 1-4", 2.2 online softmax, 2.5 causal block skipping, 2.6 / 3.2
+// delayed normalisation and the logsumexp, 4.5 persistent kernel, 5.3
+// conditional rescaling; the head dims the pages list for the FlashAttention
+// kernels (64, 96, 128, 192, 256) and their warning about other head dims
+// ("FlashAttention: tiling + recomputation", 6, pitfall 1).
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+
+#include "internal.h"
+#include "ptx.cuh"
+#include "fwd_sched.h"
+
+namespace gb300 {
+namespace {
+
+constexpr int kWThreads = 256;
+constexpr int kWM = 128;   // query rows per Q tile
+constexpr int kWN = 64;    // keys per K/V tile
+constexpr float kWTau = 8.0f;
+constexpr float kWLn2 = 0.69314718055994530942f;
+constexpr float kWLog2e = 1.44269504088896340736f;
+constexpr uint32_t kWNegInf = 0xFF800000u;
+
+template <int D>
+struct WideCfg {
+    static constexpr int kQBytes = kWM * D * 2;     // D / 64 chunks of 128 rows x 128 B
+    static constexpr int kKVBytes = kWN * D * 2;    // D / 64 chunks of 64 rows x 128 B
+    static constexpr int kKRing = kQBytes;          // 2 slots
+    static constexpr int kVRing = kKRing + 2 * kKVBytes;  // 2 slots
+    static constexpr int kStg = kVRing + 2 * kKVBytes;    // 4 warps x 2 x 2 KiB
+    static constexpr int kBar = kStg + 4 * 4096;
+    static constexpr int kSmemBytes = kBar + 512 + 1024;
+    static_assert(kSmemBytes <= 232448, "shared memory budget");
+    static constexpr uint32_t kColO = 128;
+};
+
+__host__ __device__ constexpr int wide_epi_cols(bool f32) { return f32 ? 16 : 32; }
+
+struct WideParams {
+    FwdShape shape;   // nmb counts 128-row Q tiles here
+    int group, off, d_act;
+    float c;          // scale * log2(e)
+    uint32_t slot;
+};
+
+constexpr uint32_t kWideQueueSlots = 256;
+__device__ unsigned int g_wide_queue[kWideQueueSlots][2];  // ticket counter, exit count
+
+struct WItem {
+    int bh, mt, n;
+};
+
+struct __align__(8) WideBars {
+    uint64_t q_full, q_empty;
+    uint64_t k_full[2], k_empty[2], v_full[2], v_empty[2];
+    uint64_t s_full[2], p_full[2], pv_done, o_full;
+    uint64_t unit_full[2], unit_empty[2];
+    uint64_t drain;
+    WItem item[2];
+    uint32_t tmem_base;
+    int abort;
+};
+static_assert(sizeof(WideBars) <= 512, "barrier block");
+
+constexpr int kWConsumers = 5;  // MMA warp + 4 softmax warps
+
+// KV tiles of 64 keys that Q tile mt (rows [128 mt, 128 mt + 128)) needs.
+__device__ __forceinline__ int wide_kv_tiles(const FwdShape& s, int mt) {
+    const int r0 = mt * kWM;
+    int rows = s.Nq - r0;
+    rows = rows < kWM ? rows : kWM;
+    return kv_tiles_for_rows(r0, rows, s.Nq, s.Nk, s.causal, kWN);
+}
+
+__device__ __forceinline__ bool take_witem(WideBars* bars, uint32_t k, WItem& w,
+                                           const volatile int* abort_flag) {
+    const uint32_t i = k & 1u;
+    if (!__all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&bars->unit_full[i]), (k >> 1) & 1u, abort_flag)))
+        return false;
+    const volatile WItem* src = &bars->item[i];
+    w.bh = src->bh;
+    w.mt = src->mt;
+    w.n = src->n;
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(smem_u32(&bars->unit_empty[i]));
+    return true;
+}
+
+__device__ __forceinline__ void wide_abort(WideBars* bars, unsigned int* err) {
+    atomicOr(err, kErrTimeout);
+    *((volatile int*)&bars->abort) = 1;
+}
+
+template <int D>
+__device__ void wide_producer(const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv,
+                              uint8_t* smem, WideBars* bars, const WideParams& p, unsigned int* err) {
+    using C = WideCfg<D>;
+    const volatile int* abort_flag = &bars->abort;
+    const FwdShape& s = p.shape;
+    const bool leader = elect_one();
+    const int leader_lane = __ffs(__ballot_sync(0xFFFFFFFFu, leader)) - 1;
+    unsigned int* queue = g_wide_queue[p.slot];
+    int nq = 0;           // Q loads issued
+    long long nk = 0, nv = 0;  // K and V loads issued
+    bool ok = true;
+    for (int local = 0; ok; ++local) {
+        const uint32_t hs = (uint32_t)local & 1u;
+        if (local >= 2)
+            ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&bars->unit_empty[hs]),
+                                                   (uint32_t)((local >> 1) - 1) & 1u, abort_flag));
+        if (!ok) break;
+        uint32_t u = blockIdx.x;
+        if (local > 0) {
+            if (leader) u = gridDim.x + atomicAdd(&queue[0], 1u);
+            u = __shfl_sync(0xFFFFFFFFu, u, leader_lane);
+        }
+        const bool done = u >= (uint32_t)s.units;
+        int bh = -1, mt = 0, n = 0;
+        if (!done) {
+            unit_of(s, u, bh, mt);
+            n = wide_kv_tiles(s, mt);
+        }
+        if (leader) {
+            volatile WItem* dst = &bars->item[hs];
+            dst->bh = bh;
+            dst->mt = mt;
+            dst->n = n;
+            mbar_arrive(smem_u32(&bars->unit_full[hs]));
+        }
+        __syncwarp();
+        if (done) break;
+        const int b = bh / s.Hq;
+        const int hq = bh - b * s.Hq;
+        const int kvh = b * s.Hkv + hq / p.group;
+        if (nq > 0)
+            ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&bars->q_empty), (uint32_t)(nq - 1) & 1u,
+                                                   abort_flag));
+        if (!ok) break;
+        if (leader) {
+            const uint32_t bar = smem_u32(&bars->q_full);
+            mbar_arrive_expect_tx(bar, C::kQBytes);
+#pragma unroll
+            for (int c = 0; c < D / 64; ++c)
+                tma_load_3d(smem_u32(smem) + c * (kWM * 128), tq, bar, 64 * c, mt * kWM, bh);
+        }
+        __syncwarp();
+        ++nq;
+        for (int j = 0; j < n && ok; ++j) {
+            const int sk = (int)(nk & 1);
+            if (nk >= 2)
+                ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&bars->k_empty[sk]),
+                                                       (uint32_t)(((nk >> 1) - 1) & 1), abort_flag));
+            if (!ok) break;
+            if (leader) {
+                const uint32_t bar = smem_u32(&bars->k_full[sk]);
+                mbar_arrive_expect_tx(bar, C::kKVBytes);
+                const uint32_t dst = smem_u32(smem + C::kKRing + sk * C::kKVBytes);
+#pragma unroll
+                for (int c = 0; c < D / 64; ++c)
+                    tma_load_3d(dst + c * (kWN * 128), tk, bar, 64 * c, j * kWN, kvh);
+            }
+            __syncwarp();
+            ++nk;
+            const int sv = (int)(nv & 1);
+            if (nv >= 2)
+                ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&bars->v_empty[sv]),
+                                                       (uint32_t)(((nv >> 1) - 1) & 1), abort_flag));
+            if (!ok) break;
+            if (leader) {
+                const uint32_t bar = smem_u32(&bars->v_full[sv]);
+                mbar_arrive_expect_tx(bar, C::kKVBytes);
+                const uint32_t dst = smem_u32(smem + C::kVRing + sv * C::kKVBytes);
+#pragma unroll
+                for (int c = 0; c < D / 64; ++c)
+                    tma_load_3d(dst + c * (kWN * 128), tv, bar, 64 * c, j * kWN, kvh);
+            }
+            __syncwarp();
+            ++nv;
+        }
+    }
+    if (!ok && leader) wide_abort(bars, err);
+    if (leader) {
+        __threadfence();
+        if (atomicAdd(&queue[1], 1u) == gridDim.x - 1) {
+            queue[0] = 0u;
+            queue[1] = 0u;
+        }
+    }
+    // Drain: every issued copy lands before the CTA may exit.
+    if (nq > 0) mbar_wait(smem_u32(&bars->q_full), (uint32_t)(nq - 1) & 1u, nullptr);
+    for (int st = 0; st < 2 && st < nk; ++st)
+        mbar_wait(smem_u32(&bars->k_full[st]), (uint32_t)(((nk - st + 1) / 2 - 1) & 1), nullptr);
+    for (int st = 0; st < 2 && st < nv; ++st)
+        mbar_wait(smem_u32(&bars->v_full[st]), (uint32_t)(((nv - st + 1) / 2 - 1) & 1), nullptr);
+    __syncwarp();
+}
+
+constexpr uint32_t kWDescHi = sdesc_hi_sw128(1024);
+
+// S = Q K_j^T: M = 128, N = 64, K = D (16 per instruction; 64-column chunks
+// 16 KiB apart in Q, 8 KiB apart in K).
+template <int D>
+__device__ __forceinline__ void wide_issue_s(uint32_t d_tmem, uint32_t q_lo, uint32_t k_lo,
+                                             uint32_t idesc) {
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t in = (kk & 3) * (32 >> 4);
+        mma_ss_warp(d_tmem, sdesc_join(q_lo + (kk >> 2) * ((kWM * 128) >> 4) + in, kWDescHi),
+                    sdesc_join(k_lo + (kk >> 2) * ((kWN * 128) >> 4) + in, kWDescHi), idesc,
+                    kk > 0 ? 1u : 0u);
+    }
+}
+
+// O += P V_j: A = P (bf16 pairs in TMEM, 8 columns per 16 keys), B = V_j
+// MN-major (LBO 8 KiB between 64-column chunks, 16 keys = 16 rows of 128 B).
+__device__ __forceinline__ void wide_issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_lo,
+                                              uint32_t idesc, bool accumulate) {
+#pragma unroll
+    for (int kk = 0; kk < kWN / 16; ++kk)
+        mma_ts_warp(d_tmem, p_tmem + kk * 8, sdesc_join(v_lo + kk * (2048 >> 4), kWDescHi), idesc,
+                    (accumulate || kk > 0) ? 1u : 0u);
+}
+
+template <int D>
+__device__ void wide_mma(uint8_t* smem, WideBars* bars, uint32_t tmem, unsigned int* err) {
+    using C = WideCfg<D>;
+    const volatile int* abort_flag = &bars->abort;
+    const bool leader = elect_one();
+    const uint32_t idS = make_idesc_bf16(kWM, kWN, 0, 0);
+    const uint32_t idO = make_idesc_bf16(kWM, D, 0, 1);
+    const uint32_t q_lo = sdesc_lo(smem_u32(smem), 16);
+    auto k_lo = [&](int st) { return sdesc_lo(smem_u32(smem + C::kKRing + st * C::kKVBytes), 16); };
+    auto v_lo = [&](int st) {
+        return sdesc_lo(smem_u32(smem + C::kVRing + st * C::kKVBytes), kWN * 128);
+    };
+    auto wait_all = [&](uint32_t bar, uint32_t parity, int polls) {
+        return __all_sync(0xFFFFFFFFu, mbar_wait(bar, parity, abort_flag, polls));
+    };
+    long long g = 0;           // tiles of all units so far: tile g uses S buffer g & 1
+    long long nk = 0, nv = 0;  // K and V tiles consumed
+    bool ok = true;
+    // S for global tile gg into buffer gg & 1 (K from the K ring).
+    auto issue_s = [&](long long gg, bool last_s) {
+        const int sk = (int)(nk & 1);
+        if (!wait_all(smem_u32(&bars->k_full[sk]), (uint32_t)((nk >> 1) & 1), 0)) return false;
+        tc_fence_after();
+        wide_issue_s<D>(tmem + (uint32_t)(gg & 1) * kWN, q_lo, k_lo(sk), idS);
+        mma_commit_warp(smem_u32(&bars->s_full[gg & 1]));
+        mma_commit_warp(smem_u32(&bars->k_empty[sk]));
+        if (last_s) mma_commit_warp(smem_u32(&bars->q_empty));
+        ++nk;
+        return true;
+    };
+    for (int local = 0; ok; ++local) {
+        WItem w;
+        ok = take_witem(bars, (uint32_t)local, w, abort_flag);
+        if (!ok || w.bh < 0) break;
+        const int n = w.n;
+        ok = wait_all(smem_u32(&bars->q_full), (uint32_t)local & 1u, 0);
+        if (!ok) break;
+        ok = issue_s(g, n == 1);
+        if (ok && n > 1) ok = issue_s(g + 1, n == 2);
+        for (int j = 0; j < n && ok; ++j, ++g) {
+            const int b = (int)(g & 1);
+            ok = wait_all(smem_u32(&bars->p_full[b]), (uint32_t)((g >> 1) & 1), 32);
+            if (!ok) break;
+            const int sv = (int)(nv & 1);
+            ok = wait_all(smem_u32(&bars->v_full[sv]), (uint32_t)((nv >> 1) & 1), 0);
+            if (!ok) break;
+            tc_fence_after();
+            wide_issue_pv(tmem + C::kColO, tmem + (uint32_t)b * kWN, v_lo(sv), idO, j > 0);
+            mma_commit_warp(smem_u32(&bars->pv_done));
+            mma_commit_warp(smem_u32(&bars->v_empty[sv]));
+            ++nv;
+            if (j + 2 < n) {
+                ok = issue_s(g + 2, j + 3 == n);
+                if (!ok) break;
+            }
+            if (j + 1 == n) mma_commit_warp(smem_u32(&bars->o_full));
+        }
+    }
+    if (!ok && leader) wide_abort(bars, err);
+    mma_commit_warp(smem_u32(&bars->drain));
+    mbar_wait(smem_u32(&bars->drain), 0, nullptr);
+    __syncwarp();
+}
+
+// One 64-key tile of the online softmax for this thread's row (see the 128-
+// column forward): mask, tile max, conditional rescale of O (after the
+// previous P.V product has completed), P = 2^(s c - m) to TMEM as bf16 pairs,
+// and the two row sums.
+template <int D, bool MASKED>
+__device__ __forceinline__ void wide_softmax_tile(uint32_t (&sr)[64], int lim, bool first, float c,
+                                                  uint32_t tP, uint32_t tO, float& m, float& l,
+                                                  float& lx, WideBars* bars, long long g,
+                                                  const volatile int* abort_flag, bool& ok) {
+    if constexpr (MASKED) {
+#pragma unroll
+        for (int cc = 0; cc < 64; ++cc)
+            if (cc > lim) sr[cc] = kWNegInf;
+    }
+    float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+#pragma unroll
+    for (int cc = 0; cc < 64; cc += 8) {
+        mx0 = fmax3(mx0, __uint_as_float(sr[cc]), __uint_as_float(sr[cc + 1]));
+        mx1 = fmax3(mx1, __uint_as_float(sr[cc + 2]), __uint_as_float(sr[cc + 3]));
+        mx2 = fmax3(mx2, __uint_as_float(sr[cc + 4]), __uint_as_float(sr[cc + 5]));
+        mx3 = fmax3(mx3, __uint_as_float(sr[cc + 6]), __uint_as_float(sr[cc + 7]));
+    }
+    const float smax = fmax3(fmaxf(mx0, mx1), mx2, mx3);
+    const float mt = smax * c;
+    const bool need = mt > m + kWTau;
+    if (__any_sync(0xFFFFFFFFu, need)) {
+        const float m_new = fmaxf(m, mt);
+        const float alpha = ex2(m - m_new);
+        l *= alpha;
+        lx *= alpha;
+        if (!first) {
+            // O must hold the previous tile's product before it is rescaled
+            ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&bars->pv_done), (uint32_t)((g - 1) & 1),
+                                                   abort_flag));
+            if (!ok) return;
+            tc_fence_after();
+            const uint64_t a2 = f2(alpha, alpha);
+#pragma unroll 1
+            for (int cc = 0; cc < D; cc += 32) {
+                uint32_t r[32];
+                tmem_ld32(tO + cc, r);
+                tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 32; i += 2) {
+                    float lo, hi;
+                    f2_split(f2_mul(f2(__uint_as_float(r[i]), __uint_as_float(r[i + 1])), a2), lo, hi);
+                    r[i] = __float_as_uint(lo);
+                    r[i + 1] = __float_as_uint(hi);
+                }
+                tmem_st32(tO + cc, r);
+            }
+        }
+        m = m_new;
+    }
+    {
+        const float pmax = ex2(fmaf(smax, c, -m));
+        l += bf16lo_to_f32(pack_bf16x2(pmax, 0.f)) - pmax;
+    }
+    const uint64_t c2 = f2(c, c), nm2 = f2(-m, -m);
+    uint64_t acc0 = 0, acc1 = 0;
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const int col = half * 32 + 2 * i;
+            float x0, x1;
+            f2_split(f2_fma(f2(__uint_as_float(sr[col]), __uint_as_float(sr[col + 1])), c2, nm2), x0, x1);
+            float p0 = ex2(x0), p1 = ex2(x1);
+            if constexpr (MASKED) {
+                p0 = col <= lim ? p0 : 0.f;
+                p1 = col + 1 <= lim ? p1 : 0.f;
+            }
+            pk[i] = pack_bf16x2(p0, p1);
+            if (i & 1)
+                acc1 = f2_add(acc1, f2(p0, p1));
+            else
+                acc0 = f2_add(acc0, f2(p0, p1));
+        }
+        tmem_st16(tP + half * 16, pk);
+    }
+    float a, bb;
+    f2_split(f2_add(acc0, acc1), a, bb);
+    lx += a + bb;
+    l += a + bb;
+}
+
+template <bool OUT_F32>
+__device__ __forceinline__ void wide_store_cols(const float (&v)[32], int cc, uint8_t* stg,
+                                                uint32_t& epi_buf, int lane, const CUtensorMap* to,
+                                                int row0, int bh, int d_act) {
+    constexpr int kCols = wide_epi_cols(OUT_F32);
+#pragma unroll
+    for (int h = 0; h < 32 / kCols; ++h) {
+        if (cc + h * kCols >= d_act) break;
+        uint8_t* buf = stg + (epi_buf & 1) * 2048;
+        if (lane == 0) bulk_wait_group_read<1>();
+        __syncwarp();
+        const uint32_t dst = smem_u32(buf) + lane * 64;
+        if constexpr (OUT_F32) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                sts128(dst + 16 * i, __float_as_uint(v[h * 16 + 4 * i]), __float_as_uint(v[h * 16 + 4 * i + 1]),
+                       __float_as_uint(v[h * 16 + 4 * i + 2]), __float_as_uint(v[h * 16 + 4 * i + 3]));
+        } else {
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                sts128(dst + 16 * i, pack_bf16x2(v[8 * i], v[8 * i + 1]), pack_bf16x2(v[8 * i + 2], v[8 * i + 3]),
+                       pack_bf16x2(v[8 * i + 4], v[8 * i + 5]), pack_bf16x2(v[8 * i + 6], v[8 * i + 7]));
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+            tma_store_3d(to, smem_u32(buf), cc + h * kCols, row0, bh);
+            bulk_commit_group();
+        }
+        ++epi_buf;
+    }
+}
+
+template <int D, bool OUT_F32>
+__device__ void wide_softmax(int wq, int lane, uint8_t* smem, WideBars* bars, uint32_t tmem,
+                             const WideParams& p, const CUtensorMap* to, float* __restrict__ lse_ptr,
+                             unsigned int* err) {
+    using C = WideCfg<D>;
+    const volatile int* abort_flag = &bars->abort;
+    const FwdShape& s = p.shape;
+    const uint32_t lane_off = uint32_t(wq * 32) << 16;
+    const uint32_t tO = tmem + C::kColO + lane_off;
+    uint8_t* stg = smem + C::kStg + wq * 4096;
+    uint32_t epi_buf = 0;
+    long long g = 0;
+    bool ok = true;
+    for (uint32_t k = 0; ok; ++k) {
+        WItem w;
+        ok = take_witem(bars, k, w, abort_flag);
+        if (!ok || w.bh < 0) break;
+        const int row = w.mt * kWM + wq * 32 + lane;
+        int last_key = s.Nk - 1;
+        if (s.causal) {
+            const int lk = row + p.off;
+            last_key = lk < last_key ? lk : last_key;
+        }
+        float m = -INFINITY, l = 0.f, lx = 0.f;
+        for (int j = 0; j < w.n && ok; ++j, ++g) {
+            const int b = (int)(g & 1);
+            const uint32_t tS = tmem + (uint32_t)b * kWN + lane_off;
+            ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&bars->s_full[b]), (uint32_t)((g >> 1) & 1),
+                                                   abort_flag, 32));
+            if (!ok) break;
+            tc_fence_after();
+            uint32_t sr[64];
+            tmem_ld32(tS, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+            tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+            tmem_wait_ld();
+            const int lim = last_key - j * kWN;
+            if (__any_sync(0xFFFFFFFFu, lim < kWN - 1))
+                wide_softmax_tile<D, true>(sr, lim, j == 0, p.c, tS, tO, m, l, lx, bars, g, abort_flag, ok);
+            else
+                wide_softmax_tile<D, false>(sr, lim, j == 0, p.c, tS, tO, m, l, lx, bars, g, abort_flag, ok);
+            if (!ok) break;
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&bars->p_full[b]));
+        }
+        if (!ok) break;
+        ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&bars->o_full), k & 1u, abort_flag));
+        if (!ok) break;
+        tc_fence_after();
+        const float inv_l = 1.0f / l;
+        const uint64_t il2 = f2(inv_l, inv_l);
+        const int row0 = w.mt * kWM + wq * 32;
+#pragma unroll 1
+        for (int cc = 0; cc < D; cc += 32) {
+            uint32_t r[32];
+            tmem_ld32(tO + cc, r);
+            tmem_wait_ld();
+            float v[32];
+#pragma unroll
+            for (int i = 0; i < 32; i += 2)
+                f2_split(f2_mul(f2(__uint_as_float(r[i]), __uint_as_float(r[i + 1])), il2), v[i], v[i + 1]);
+            wide_store_cols<OUT_F32>(v, cc, stg, epi_buf, lane, to, row0, w.bh, p.d_act);
+        }
+        if (row < s.Nq && lse_ptr)
+            lse_ptr[(size_t)w.bh * s.Nq + (size_t)row] = (m + log2f(lx)) * kWLn2;
+        // (the next unit's P.V overwrites O only after this warpgroup's next
+        // P is in TMEM, which follows these loads)
+    }
+    if (lane == 0) bulk_wait_group_all();
+    __syncwarp();
+    if (!ok) wide_abort(bars, err);
+}
+
+template <int D, bool OUT_F32>
+__global__ void __launch_bounds__(kWThreads, 1)
+attn_fwd_wide_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                     const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap to,
+                     float* __restrict__ lse_ptr, const WideParams p, unsigned int* err) {
+    using C = WideCfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~uintptr_t(1023));
+    WideBars* bars = reinterpret_cast<WideBars*>(smem + C::kBar);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bars->q_full), 1);
+        mbar_init(smem_u32(&bars->q_empty), 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(smem_u32(&bars->k_full[i]), 1);
+            mbar_init(smem_u32(&bars->k_empty[i]), 1);
+            mbar_init(smem_u32(&bars->v_full[i]), 1);
+            mbar_init(smem_u32(&bars->v_empty[i]), 1);
+            mbar_init(smem_u32(&bars->s_full[i]), 1);
+            mbar_init(smem_u32(&bars->p_full[i]), 4);
+            mbar_init(smem_u32(&bars->unit_full[i]), 1);
+            mbar_init(smem_u32(&bars->unit_empty[i]), kWConsumers);
+        }
+        mbar_init(smem_u32(&bars->pv_done), 1);
+        mbar_init(smem_u32(&bars->o_full), 1);
+        mbar_init(smem_u32(&bars->drain), 1);
+        bars->abort = 0;
+        fence_barrier_init();
+        tma_prefetch_desc(&tq);
+        tma_prefetch_desc(&tk);
+        tma_prefetch_desc(&tv);
+        tma_prefetch_desc(&to);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(&bars->tmem_base), 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = bars->tmem_base;
+    if (warp == 0) wide_producer<D>(&tq, &tk, &tv, smem, bars, p, err);
+    else if (warp == 1) wide_mma<D>(smem, bars, tmem, err);
+    else if (warp >= 4) wide_softmax<D, OUT_F32>(warp & 3, lane, smem, bars, tmem, p, &to, lse_ptr, err);
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+template <int D, bool OUT_F32>
+attn_status_t launch_wide_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                            const CUtensorMap& to, float* lse, const WideParams& p, int grid,
+                            cudaStream_t stream, const DeviceInfo& dev) {
+    using C = WideCfg<D>;
+    static int attr_set[64] = {0};
+    if (dev.device < 64 && !attr_set[dev.device]) {
+        if (cudaFuncSetAttribute(attn_fwd_wide_kernel<D, OUT_F32>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) != cudaSuccess)
+            return ATTN_ERR_CUDA;
+        attr_set[dev.device] = 1;
+    }
+    attn_fwd_wide_kernel<D, OUT_F32><<<(unsigned)grid, kWThreads, C::kSmemBytes, stream>>>(
+        tq, tk, tv, to, lse, p, dev.err_word);
+    return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+}  // namespace
+
+attn_status_t launch_fwd_wide(const void* q, const void* k, const void* v, void* o, float* lse,
+                              int B, int Hq, int Hkv, int Nq, int Nk, int d, int causal, float scale,
+                              attn_out_dtype_t o_dtype, cudaStream_t stream, const DeviceInfo& dev) {
+    WideParams p;
+    p.shape = make_fwd_shape(B, Hq, Hkv, Nq, Nk, d, causal);
+    p.shape.nmb = (Nq + kWM - 1) / kWM;  // units are single 128-row Q tiles
+    p.shape.units = (long long)B * Hq * p.shape.nmb;
+    if (p.shape.units >= (1ll << 31)) return ATTN_ERR_UNSUPPORTED;
+    p.group = Hq / Hkv;
+    p.off = Nk - Nq;
+    p.d_act = d;
+    p.c = scale * kWLog2e;
+    static std::atomic<uint32_t> launches{0};
+    p.slot = launches.fetch_add(1u, std::memory_order_relaxed) % kWideQueueSlots;
+    const long long units = p.shape.units;
+    const int grid = (int)(units < dev.num_sms ? units : dev.num_sms);
+    CUtensorMap tq, tk, tv, to;
+    attn_status_t st;
+    const bool f32 = o_dtype == ATTN_OUT_F32;
+    if ((st = encode_tmap_bf16_3d(&tq, q, d, Nq, (long long)B * Hq, kWM)) != ATTN_OK) return st;
+    if ((st = encode_tmap_bf16_3d(&tk, k, d, Nk, (long long)B * Hkv, kWN)) != ATTN_OK) return st;
+    if ((st = encode_tmap_bf16_3d(&tv, v, d, Nk, (long long)B * Hkv, kWN)) != ATTN_OK) return st;
+    if ((st = encode_tmap_out_3d(&to, o, f32, d, Nq, (long long)B * Hq, wide_epi_cols(f32), 32)) != ATTN_OK)
+        return st;
+    if (d <= 192)
+        return f32 ? launch_wide_t<192, true>(tq, tk, tv, to, lse, p, grid, stream, dev)
+                   : launch_wide_t<192, false>(tq, tk, tv, to, lse, p, grid, stream, dev);
+    return f32 ? launch_wide_t<256, true>(tq, tk, tv, to, lse, p, grid, stream, dev)
+               : launch_wide_t<256, false>(tq, tk, tv, to, lse, p, grid, stream, dev);
+}
+
+}  // namespace gb300

@@ -13,6 +13,9 @@ namespace gb300 {
 // nothing to Q K^T and give zero O columns), and stores skip them.
 inline int pad_head_dim(int d) { return d <= 64 ? 64 : 128; }
 inline bool head_dim_supported(int d) { return d >= 8 && d <= 128 && d % 8 == 0; }
+// The dense forward also takes 128 < d <= 256 (multiples of 8) on the kernels
+// built for 192 and 256 columns (one Q tile per CTA; attn_fwd_wide_sm103.cu).
+inline bool fwd_head_dim_supported(int d) { return d >= 8 && d <= 256 && d % 8 == 0; }
 
 struct DeviceInfo {
     int device;
@@ -69,6 +72,11 @@ attn_status_t launch_fwd_fp8(const void* q8, const void* k8, const void* vt8, co
 attn_status_t launch_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
                          int B, int Hq, int Hkv, int Nq, int Nk, int d, int causal, float scale,
                          attn_out_dtype_t o_dtype, cudaStream_t stream, const DeviceInfo& dev);
+
+// Dense forward for 128 < d <= 256.
+attn_status_t launch_fwd_wide(const void* q, const void* k, const void* v, void* o, float* lse,
+                              int B, int Hq, int Hkv, int Nq, int Nk, int d, int causal, float scale,
+                              attn_out_dtype_t o_dtype, cudaStream_t stream, const DeviceInfo& dev);
 
 // Packed variable-length forward: q/o [total_q, Hq, d], k/v [total_k, Hkv, d],
 // lse [Hq, total_q]; cu_q / cu_k device int32 [B + 1].

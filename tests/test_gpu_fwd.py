@@ -291,3 +291,57 @@ def test_head_dim_96_split_tail():
     o, lse = gpu_fwd(q, k, v, False, 1 / math.sqrt(96))
     o_ref, lse_ref = oracle.attention(q, k, v, causal=False)
     assert_close(o, lse, o_ref, lse_ref, "d=96 split")
+
+
+# ---------------------- head dims above 128 (wide kernel) --------------------
+@pytest.mark.parametrize("B,Hq,Hkv,Nq,Nk,d,causal", [
+    (1, 1, 1, 128, 128, 256, False),
+    (2, 4, 2, 300, 300, 256, True),      # GQA, ragged tails
+    (2, 4, 2, 300, 300, 192, False),
+    (1, 4, 1, 200, 520, 192, True),      # MQA, bottom-right causal, Nq < Nk
+    (1, 2, 2, 700, 90, 256, False),      # Nq > Nk
+    (1, 2, 2, 257, 257, 136, True),      # padded to 192
+    (1, 2, 2, 333, 333, 160, False),
+    (1, 2, 2, 129, 400, 248, True),      # padded to 256
+])
+def test_wide_head_dims(B, Hq, Hkv, Nq, Nk, d, causal):
+    q, k, v = make_fwd_inputs(B, Hq, Hkv, Nq, Nk, d, seed=1000 + d + Nq)
+    scale = 1 / math.sqrt(d)
+    o, lse = gpu_fwd(q, k, v, causal, scale)
+    o_ref, lse_ref = oracle.attention(q, k, v, causal=causal, scale=scale)
+    assert_close(o, lse, o_ref, lse_ref, f"{(B, Hq, Hkv, Nq, Nk, d, causal)}")
+    ob, _ = gpu_fwd(q, k, v, causal, scale, out_dtype=torch.bfloat16, with_lse=False)
+    assert_close_bf16(ob, o_ref, f"bf16 out d={d}")
+
+
+def test_wide_sampled_heads_long():
+    """B2 H8 N4096 d256, causal and not; the oracle checks two whole heads."""
+    q, k, v = make_fwd_inputs(2, 8, 8, 4096, 4096, 256, seed=1100)
+    for causal in (False, True):
+        o, lse = gpu_fwd(q, k, v, causal, 1 / 16)
+        for (b, h) in ((0, 0), (1, 7)):
+            sl = (slice(b, b + 1), slice(h, h + 1))
+            o_ref, lse_ref = oracle.attention(q[sl], k[sl], v[sl], causal=causal, scale=1 / 16)
+            assert_close(o[sl], lse[sl], o_ref, lse_ref, f"head {(b, h)} causal={causal}")
+
+
+def test_wide_repeatable_and_graph():
+    q, k, v = make_fwd_inputs(2, 4, 2, 640, 640, 256, seed=1200)
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    o = torch.empty(q.shape, dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty(q.shape[:3], dtype=torch.float32, device="cuda")
+    ea.attn_fwd(qd, kd, vd, o, lse, causal=True)
+    torch.cuda.synchronize()
+    ref_o, ref_l = o.clone(), lse.clone()
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, stream=s):
+            ea.attn_fwd(qd, kd, vd, o, lse, causal=True, stream=s)
+    for _ in range(3):
+        o.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(o, ref_o) and torch.equal(lse, ref_l)
+    assert ea.attn_last_device_error() == 0

@@ -59,7 +59,7 @@ def fwd(lib, **kw):
     (dict(B=0), 1), (dict(Hq=3, Hkv=2), 1), (dict(Nq=0), 1), (dict(Nk=0), 1),
     (dict(Nq=(1 << 24) + 1), 1), (dict(causal=2), 1), (dict(causal=1, Nq=9, Nk=8), 1),
     (dict(scale=-1.0), 1), (dict(scale=float("nan")), 1), (dict(scale=float("inf")), 1),
-    (dict(odt=7), 1), (dict(d=100), 2), (dict(d=136), 2), (dict(d=256), 2), (dict(d=0), 1),
+    (dict(odt=7), 1), (dict(d=100), 2), (dict(d=264), 2), (dict(d=4), 2), (dict(d=0), 1),
 ])
 def test_fwd_argument_checks(lib, kw, code):
     assert fwd(lib, **kw) == code
@@ -292,15 +292,22 @@ def test_decode_paged_argument_checks(lib):
     assert lib.attn_decode_paged(*bad) == ea.ATTN_ERR_UNSUPPORTED
 
 
-@pytest.mark.parametrize("d,ok", [(8, True), (32, True), (48, True), (80, True), (96, True),
-                                  (120, True), (128, True), (4, False), (100, False), (136, False),
-                                  (192, False), (256, False)])
-def test_supported_head_dims(lib, d, ok):
-    """Head dims in [8, 128] that are multiples of 8 run on the 64- or 128-column
-    kernels (zero-filled columns); others are rejected (size 0)."""
-    assert (ea.attn_bwd_workspace_size(2, 8, 2, 1000, 1000, d) > 0) == ok
+@pytest.mark.parametrize("d,fwd_ok,bwd_ok", [
+    (8, True, True), (32, True, True), (48, True, True), (80, True, True), (96, True, True),
+    (120, True, True), (128, True, True), (4, False, False), (100, False, False),
+    (130, False, False), (136, True, False), (192, True, False), (200, True, False),
+    (256, True, False), (264, False, False)])
+def test_supported_head_dims(lib, d, fwd_ok, bwd_ok):
+    """The forward takes d in [8, 256] (multiples of 8): up to 128 on the 64- or
+    128-column kernels, above on the 192- or 256-column ones (zero-filled
+    columns); the backward (workspace size 0 when unsupported) and decode stop
+    at 128."""
+    assert (ea.attn_bwd_workspace_size(2, 8, 2, 1000, 1000, d) > 0) == bwd_ok
     rc = fwd(lib, d=d)
-    assert rc == (ea.ATTN_ERR_CUDA if ok else ea.ATTN_ERR_UNSUPPORTED) or (ok and rc == ea.ATTN_OK)
+    assert rc == (ea.ATTN_ERR_CUDA if fwd_ok else ea.ATTN_ERR_UNSUPPORTED) or (fwd_ok and rc == ea.ATTN_OK)
+    bwd_rc = lib.attn_bwd(*([FAKE] * 9), 1, 2, 1, 8, 8, d, 0, 0.125, 0, 0, FAKE, 1 << 30, None)
+    if not bwd_ok:
+        assert bwd_rc == ea.ATTN_ERR_UNSUPPORTED
 
 
 def fwd_varlen(lib, **kw):
