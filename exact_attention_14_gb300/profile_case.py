@@ -9,7 +9,7 @@ profiler captures (ncu) of a single launch configuration.
     python -m exact_attention_14_gb300.profile_case --kernel varlen
 
 Workloads: prefill (B=4 H=16 N=2048 d=128), prefill2x (B=8: inputs larger
-than L2), long (B=1 H=32 N=16384), gqa (B=8 Hq=32 Hkv=8 N=4096), decode
+than L2), prefill256 (the prefill shape at d=256), long (B=1 H=32 N=16384), gqa (B=8 Hq=32 Hkv=8 N=4096), decode
 (B=16 Hq=32 Hkv=8 Nmax=32768, lengths 1024..32768) and decode_quarter (the
 same with Nmax=8192, lengths 256..8192: a 512 MiB cache, still larger than
 L2, for multi-pass captures); varlen is the packed causal prefill batch (16
@@ -31,6 +31,8 @@ from exact_attention_14_gb300.inputs import (DECODE, GQA, LONG, PREFILL, VARLEN,
 FWD = {
     "prefill": PREFILL,
     "prefill2x": PREFILL.__class__(**{**PREFILL.__dict__, "name": "prefill x2", "B": 8}),
+    "prefill256": PREFILL.__class__(**{**PREFILL.__dict__, "name": "prefill d256", "d": 256,
+                                       "seed": 6}),
     "long": LONG,
     "gqa": GQA,
 }
