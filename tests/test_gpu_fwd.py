@@ -345,3 +345,30 @@ def test_wide_repeatable_and_graph():
         torch.cuda.synchronize()
         assert torch.equal(o, ref_o) and torch.equal(lse, ref_l)
     assert ea.attn_last_device_error() == 0
+
+
+# ------------------------------- edge shapes ---------------------------------
+@pytest.mark.parametrize("B,Hq,Hkv,Nq,Nk,d,causal", [
+    (1, 1, 1, 1, 1, 128, False),        # one query, one key
+    (1, 2, 1, 1, 1, 64, True),
+    (2, 2, 2, 5, 7, 64, False),         # fewer keys than a row of 8
+    (1, 4, 4, 1, 2049, 128, True),      # a single query row over a ragged key range
+    (1, 2, 2, 2, 129, 128, False),
+    (64, 32, 8, 128, 128, 64, True),    # 2048 heads, one unit each
+    (2, 32, 1, 200, 300, 128, False),   # MQA group of 32
+    (3, 19, 19, 2048, 2048, 64, False), # tail split at d = 64
+])
+def test_edge_shapes(B, Hq, Hkv, Nq, Nk, d, causal):
+    q, k, v = make_fwd_inputs(B, Hq, Hkv, Nq, Nk, d, seed=1300 + Nq + Nk)
+    scale = 1 / math.sqrt(d)
+    o, lse = gpu_fwd(q, k, v, causal, scale)
+    if B * Hq * Nq > 4096:
+        rng = np.random.default_rng(Nq + Nk)
+        rows = np.stack([rng.integers(0, B, 256), rng.integers(0, Hq, 256), rng.integers(0, Nq, 256)], 1)
+        ro, rl = oracle.attention_rows(q, k, v, rows, causal=causal, scale=scale)
+        got = np.stack([o[b, h, i] for b, h, i in rows])
+        gl = np.array([lse[b, h, i] for b, h, i in rows])
+        assert_close(got, gl, ro, rl, f"{(B, Hq, Hkv, Nq, Nk, d, causal)} sampled")
+    else:
+        o_ref, lse_ref = oracle.attention(q, k, v, causal=causal, scale=scale)
+        assert_close(o, lse, o_ref, lse_ref, f"{(B, Hq, Hkv, Nq, Nk, d, causal)}")
