@@ -358,7 +358,7 @@ def test_wide_repeatable_and_graph():
     (2, 32, 1, 200, 300, 128, False),   # MQA group of 32
     (3, 19, 19, 2048, 2048, 64, False), # tail split at d = 64
 ])
-def test_edge_shapes(B, Hq, Hkv, Nq, Nk, d, causal):
+def test_small_and_many_head_shapes(B, Hq, Hkv, Nq, Nk, d, causal):
     q, k, v = make_fwd_inputs(B, Hq, Hkv, Nq, Nk, d, seed=1300 + Nq + Nk)
     scale = 1 / math.sqrt(d)
     o, lse = gpu_fwd(q, k, v, causal, scale)

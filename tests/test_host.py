@@ -350,3 +350,15 @@ def test_fp8_sizes_and_argument_checks(lib):
     assert f(*bad_s) == 1
     bad_c = list(args); bad_c[14] = 1; bad_c[11] = 9
     assert f(*bad_c) == 1
+
+
+def test_no_test_function_defined_twice():
+    """A second definition of a test function would silently replace the first
+    (and its parametrised cases) when pytest collects the module."""
+    import ast
+    import glob
+    for path in glob.glob(os.path.join(ROOT, "tests", "test_*.py")):
+        tree = ast.parse(open(path).read())
+        names = [n.name for n in tree.body if isinstance(n, ast.FunctionDef) and n.name.startswith("test_")]
+        dup = {n for n in names if names.count(n) > 1}
+        assert not dup, f"{os.path.basename(path)} defines {sorted(dup)} more than once"
