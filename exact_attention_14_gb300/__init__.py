@@ -49,6 +49,7 @@ SIGNATURES = {
     "attn_fp8_descale_count": (_c_sz, [_c_int] * 3),
     "attn_fp8_quantize": (_c_int, [_vp] * 4 + [_c_int] * 5 + [_vp]),
     "attn_fwd_fp8": (_c_int, [_vp] * 8 + [_c_int] * 7 + [_c_f, _c_int, _vp]),
+    "attn_selftest_bounded_wait": (_c_int, [_c_int, _vp, _vp]),
     "attn_decode_workspace_size": (_c_sz, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_int]),
     "attn_decode": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int,
                              _c_int, _c_f, _c_int, _vp, _c_sz, _c_int, _vp]),
@@ -471,6 +472,15 @@ def attn_decode_noalloc(q, k_cache, v_cache, seqlens, o, lse=None, *,
                                     int(num_splits), odt, _stream_ptr(stream))
     _check(rc, "attn_decode_noalloc")
     return o, lse
+
+
+def attn_selftest_bounded_wait(mode: int, result, stream=None) -> None:
+    """Run the bounded-wait diagnostic (mode 0: time out; mode 1: abort flag)
+    writing its outcome into `result` (an int32 CUDA tensor of one element)."""
+    import torch
+    _need(result, torch.int32, "result")
+    _check(load().attn_selftest_bounded_wait(int(mode), _ptr(result), _stream_ptr(stream)),
+           "attn_selftest_bounded_wait")
 
 
 def attn_last_device_error(stream=None) -> int:

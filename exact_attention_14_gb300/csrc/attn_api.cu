@@ -173,6 +173,45 @@ attn_status_t encode_tmap_bf16_3d(CUtensorMap* map, const void* base, int d, int
     return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
+// Diagnostic of the kernels' bounded waits: warp 0 waits, with the same
+// mbar_wait every kernel uses, on an mbarrier that nothing ever arrives on.
+// mode 0: the wait runs out its time limit; the kernel then ORs kErrTimeout
+// into the error word as the real kernels do.  mode 1: warp 1 raises the CTA's
+// abort flag after about a millisecond and the wait must return early.
+// result: 1 = left through the abort flag, 2 = ran out of time, 3 = the phase
+// completed (impossible).
+__global__ void attn_selftest_wait_kernel(int mode, int* result, unsigned int* err) {
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bar), 1);
+        abort_flag = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+    const int warp = threadIdx.x >> 5;
+    if (warp == 0) {
+        const uint64_t t0 = global_timer_ns();
+        const bool ok = mbar_wait(smem_u32(&bar), 0, (const volatile int*)&abort_flag);
+        const uint64_t waited = global_timer_ns() - t0;
+        if (threadIdx.x == 0) {
+            if (ok) {
+                *result = 3;
+            } else if (waited > kWaitLimitNs) {
+                *result = 2;
+                atomicOr(err, kErrTimeout);
+            } else {
+                *result = 1;
+            }
+        }
+    } else if (warp == 1 && mode == 1 && threadIdx.x == 32) {
+        const uint64_t t0 = global_timer_ns();
+        while (global_timer_ns() - t0 < 1000000ull) {
+        }
+        *((volatile int*)&abort_flag) = 1;
+    }
+}
+
 }  // namespace gb300
 
 using namespace gb300;
@@ -410,6 +449,15 @@ const char* attn_status_string(attn_status_t s) {
         case ATTN_ERR_WORKSPACE: return "ATTN_ERR_WORKSPACE";
     }
     return "ATTN_ERR_UNKNOWN";
+}
+
+attn_status_t attn_selftest_bounded_wait(int mode, int* result, void* stream) {
+    if ((mode != 0 && mode != 1) || !result || !aligned4(result)) return ATTN_ERR_INVALID_ARG;
+    DeviceInfo dev;
+    attn_status_t st = current_device_info(&dev);
+    if (st != ATTN_OK) return st;
+    attn_selftest_wait_kernel<<<1, 64, 0, static_cast<cudaStream_t>(stream)>>>(mode, result, dev.err_word);
+    return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
 attn_status_t attn_last_device_error(void* stream) {

@@ -400,6 +400,21 @@ int attn_fwd_schedule(int B, int Hq, int Hkv, int Nq, int Nk, int d, int causal,
 int attn_fwd_split_plan(int B, int Hq, int Hkv, int Nq, int Nk, int d, int causal, int num_sms,
                         int* n_full, int* n_split, int* parts);
 
+/*
+ * attn_selftest_bounded_wait -- diagnostic of the kernels' bounded waits (every
+ * spin in the library's kernels gives up after 2 s, records ATTN_ERR_TIMEOUT in
+ * the device error word, and lets the context carry on).  One CTA waits, with
+ * the kernels' own wait, on an mbarrier that nothing ever arrives on:
+ *   mode 0  the wait runs out (about 2 s); attn_last_device_error() then
+ *           reports ATTN_ERR_TIMEOUT;
+ *   mode 1  another warp raises the CTA's abort flag after about 1 ms and the
+ *           wait returns at once (no error recorded).
+ *   result  DEVICE int: 1 = left through the abort flag, 2 = ran out of time,
+ *           3 = the phase completed (never expected).
+ * Asynchronous on `stream`.
+ */
+attn_status_t attn_selftest_bounded_wait(int mode, int* result, void* stream);
+
 #ifdef __cplusplus
 }
 #endif
