@@ -93,6 +93,7 @@ struct FwdParams {
     int d_act;      // the tensors' head dim (<= D; the tiles' columns past it are zeros)
     FwdSplit split; // tail split (fwd_sched.h)
     float* partial; // per-piece partial results of split units (NULL if none)
+    void* o;        // O: [B, Hq, Nq, d_act], or [total_q, Hq, d_act] for packed batches
     // packed variable-length batches (shape.Nq / Nk are then the maximum lengths)
     const int* cu_q;  // [B + 1] row offsets of the sequences in the packed Q / O
     const int* cu_k;  // [B + 1] row offsets in the packed K / V
@@ -416,21 +417,23 @@ __device__ void run_mma(uint8_t* smem, Bars* bars, uint32_t tmem, const FwdParam
         const int n[2] = {w.e[0], w.e[1]};
         const int j0 = w.j0;
         const int j1 = n[0] > n[1] ? n[0] : n[1];
-        for (int t = 0; t < 2 && ok; ++t) ok = wait_all(smem_u32(&bars->q_full[t]), local & 1);
-        if (!ok) break;
-        // K_0 -> S_t(0)
+        // K_0 -> S_t(0).  Each tile's first S waits only for its own Q tile:
+        // with causal masking the previous unit frees Q_1 only at its last
+        // step, so the next unit's Q_1 lands later than its Q_0.
         int slot_k = (int)(Cn % C::kStages);
         ok = wait_all(smem_u32(&bars->kv_full[slot_k]), (uint32_t)((Cn / C::kStages) & 1));
         ++Cn;
-        if (!ok) break;
-        tc_fence_after();
-        for (int t = 0; t < 2; ++t) {
+        for (int t = 0; t < 2 && ok; ++t) {
+            ok = wait_all(smem_u32(&bars->q_full[t]), local & 1);
+            if (!ok) break;
+            tc_fence_after();
             if (n[t] > j0) {
                 issue_qk<D>(tmem, t, q_lo[t], k_lo(slot_k), idS);
                 mma_commit_warp(smem_u32(&bars->s_full[t]));
             }
             if (n[t] - j0 <= 1) mma_commit_warp(smem_u32(&bars->q_empty[t]));
         }
+        if (!ok) break;
         mma_commit_warp(smem_u32(&bars->kv_empty[slot_k]));
         for (int j = j0; j < j1 && ok; ++j) {
             const int slot_v = (int)(Cn % C::kStages);
@@ -613,6 +616,56 @@ __device__ __forceinline__ void store_o_cols(const float (&v)[32], int cc, uint8
             bulk_commit_group();
         }
         ++epi_buf;
+    }
+}
+
+// Epilogue store of 32 output columns [cc, cc + 32) of this warp's 32 rows
+// of O straight from registers, whole 32-byte sectors per store: lanes 2k and
+// 2k+1 (rows 2k and 2k+1) swap one 16-byte piece of each sector, then both
+// write row 2k's sector (first 16 bytes from lane 2k, second from lane 2k+1)
+// and, in the next store, row 2k+1's.  No shared memory is involved (the
+// tensor cores' operand reads keep it busy), and nothing waits for the
+// stores to complete.
+//   o_warp      address of the warp's first row of O
+//   row_stride  bytes from one row of O to the next
+//   rows_live   rows of the warp inside the sequence (may be <= 0)
+template <bool OUT_F32>
+__device__ __forceinline__ void store_o_pairs(const float (&v)[32], int cc, int lane, uint8_t* o_warp,
+                                              size_t row_stride, int rows_live, int d_act) {
+    constexpr int kEs = OUT_F32 ? 4 : 2;
+    constexpr int kPieces = 32 * kEs / 16;  // 16-byte pieces of the row's 32 columns
+    constexpr int kColsPerPiece = 16 / kEs;
+    uint32_t w[kPieces * 4];
+    if constexpr (OUT_F32) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(v[i]);
+    } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
+    }
+    const bool odd = lane & 1;
+    const int row_a = lane & ~1, row_b = lane | 1;
+    uint8_t* pa = o_warp + (size_t)row_a * row_stride + (odd ? 16 : 0);
+    uint8_t* pb = o_warp + (size_t)row_b * row_stride + (odd ? 16 : 0);
+    const bool live_a = row_a < rows_live, live_b = row_b < rows_live;
+#pragma unroll
+    for (int sct = 0; sct < kPieces / 2; ++sct) {
+        if (cc + 2 * sct * kColsPerPiece >= d_act) break;  // columns past the head dim
+        const int pe = 2 * sct, po = 2 * sct + 1;  // the sector's two pieces
+        // (d_act % 8 == 0: a piece is wholly inside or outside the row; the
+        // odd lane's piece may be outside when the even lane's is not)
+        const bool col_ok = cc + (odd ? po : pe) * kColsPerPiece < d_act;
+        uint32_t x[4], y[4], da[4], db[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            x[i] = odd ? w[pe * 4 + i] : w[po * 4 + i];  // the piece the partner writes
+            y[i] = __shfl_xor_sync(0xFFFFFFFFu, x[i], 1);
+            da[i] = odd ? y[i] : w[pe * 4 + i];          // row 2k: piece pe (even lane), po (odd lane)
+            db[i] = odd ? w[po * 4 + i] : y[i];          // row 2k+1
+        }
+        const size_t off = (size_t)(cc * kEs + sct * 32);
+        if (live_a && col_ok) *reinterpret_cast<uint4*>(pa + off) = make_uint4(da[0], da[1], da[2], da[3]);
+        if (live_b && col_ok) *reinterpret_cast<uint4*>(pb + off) = make_uint4(db[0], db[1], db[2], db[3]);
     }
 }
 
@@ -805,6 +858,13 @@ __device__ void run_softmax(int t, int wq, int lane, uint8_t* smem, Bars* bars, 
         }
         const uint64_t il2 = f2(inv_l, inv_l);
         if (part < 0) {
+            // this warp's first row of O and the stride between rows
+            constexpr int kEs = OUT_F32 ? 4 : 2;
+            const int wrow = mb * kUnitRows + t * kTileM + wq * 32;
+            const size_t first = VARLEN ? (size_t)(w.q0 + wrow) * s.Hq + (size_t)hq
+                                        : (size_t)bh * s.Nq + (size_t)wrow;
+            uint8_t* o_warp = static_cast<uint8_t*>(p.o) + first * (size_t)p.d_act * kEs;
+            const size_t row_stride = (VARLEN ? (size_t)s.Hq : 1u) * (size_t)p.d_act * kEs;
 #pragma unroll 1
             for (int cc = 0; cc < D; cc += 32) {
                 uint32_t r[32];
@@ -814,7 +874,7 @@ __device__ void run_softmax(int t, int wq, int lane, uint8_t* smem, Bars* bars, 
 #pragma unroll
                 for (int i = 0; i < 32; i += 2)
                     f2_split(f2_mul(f2(__uint_as_float(r[i]), __uint_as_float(r[i + 1])), il2), v[i], v[i + 1]);
-                store_o_cols<OUT_F32, VARLEN>(v, cc, stg, epi_buf, lane, to, row0, oz, oe, p.d_act);
+                store_o_pairs<OUT_F32>(v, cc, lane, o_warp, row_stride, nq - wrow, p.d_act);
             }
             if (live && lse_ptr) lse_ptr[row_idx] = (m + log2f(lx)) * kLn2;
             continue;
@@ -1005,6 +1065,7 @@ attn_status_t launch_fwd(const void* q, const void* k, const void* v, void* o, f
     const uint32_t items = split_items(p.split);
     const int grid = (int)(items < (uint32_t)dev.num_sms ? items : (uint32_t)dev.num_sms);
     p.partial = nullptr;
+    p.o = o;
     CUtensorMap tq, tk, tv, to;
     attn_status_t st;
     const bool f32 = o_dtype == ATTN_OUT_F32;
@@ -1046,6 +1107,7 @@ attn_status_t launch_fwd_varlen(const void* q, const void* k, const void* v, voi
     p.split.n_split = 0;
     p.split.parts = 1;
     p.partial = nullptr;
+    p.o = o;
     p.cu_q = cu_q;
     p.cu_k = cu_k;
     p.total_q = total_q;
