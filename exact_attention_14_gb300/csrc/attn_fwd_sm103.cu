@@ -576,16 +576,15 @@ __device__ __forceinline__ void softmax_tile(uint32_t (&sr)[128], int lim, int j
     }
 }
 
-// Epilogue store of 32 output columns [cc, cc + 32) of this warp's 32 rows:
-// staged 32 rows x 64 bytes at a time in shared memory (two buffers per warp)
-// and written by TMA stores (rows past Nq are clipped by the hardware), so the
-// warp does not wait for the global writes.
-// Coordinates: dense (row0, bh); packed batches (row0 = the ragged r of the
-// warp's first row, bh = the query head, e = the ragged e; fwd_sched.h).
-template <bool OUT_F32, bool VARLEN>
+// Store of 32 output columns [cc, cc + 32) of this warp's 32 rows by the
+// piece of a split unit that merges (whole units write O from registers, see
+// store_o_pairs): staged 32 rows x 64 bytes at a time in shared memory (two
+// buffers per warp) and written by TMA stores (rows past Nq are clipped by the
+// hardware).  Packed batches are never split, so the rows are (row0, bh).
+template <bool OUT_F32>
 __device__ __forceinline__ void store_o_cols(const float (&v)[32], int cc, uint8_t* stg,
                                              uint32_t& epi_buf, int lane, const CUtensorMap* to,
-                                             int row0, int bh, int e, int d_act) {
+                                             int row0, int bh, int d_act) {
     constexpr int kCols = kEpiCols(OUT_F32);
 #pragma unroll
     for (int h = 0; h < 32 / kCols; ++h) {
@@ -609,10 +608,7 @@ __device__ __forceinline__ void store_o_cols(const float (&v)[32], int cc, uint8
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-            if constexpr (VARLEN)
-                tma_store_5d(to, smem_u32(buf), cc + h * kCols, bh, row0, e, kRaggedWindow);
-            else
-                tma_store_3d(to, smem_u32(buf), cc + h * kCols, row0, bh);
+            tma_store_3d(to, smem_u32(buf), cc + h * kCols, row0, bh);
             bulk_commit_group();
         }
         ++epi_buf;
@@ -774,7 +770,7 @@ __device__ __noinline__ void split_piece_epilogue(unsigned int* merge_count, flo
                 for (int i = 0; i < 32; ++i) v[i] = fmaf(wq_, __ldcg(bq + i * 32), v[i]);
             }
         }
-        store_o_cols<OUT_F32, false>(v, cc, stg, *epi_buf, lane, to, row0, bh, 0, d_act);
+        store_o_cols<OUT_F32>(v, cc, stg, *epi_buf, lane, to, row0, bh, d_act);
     }
     if (lse_out) *lse_out = (mmax + log2f(wxsum)) * kLn2;
 }
@@ -849,13 +845,6 @@ __device__ void run_softmax(int t, int wq, int lane, uint8_t* smem, Bars* bars, 
         // LSE: [B, Hq, Nq], or [Hq, total_q] for packed batches
         const size_t row_idx = VARLEN ? (size_t)hq * p.total_q + (size_t)(w.q0 + row)
                                       : (size_t)bh * s.Nq + (size_t)row;
-        int row0 = mb * kUnitRows + t * kTileM + wq * 32;
-        int oz = bh, oe = 0;
-        if constexpr (VARLEN) {
-            row0 += kRaggedWindow - nq;
-            oz = hq;
-            oe = w.q0 + nq;
-        }
         const uint64_t il2 = f2(inv_l, inv_l);
         if (part < 0) {
             // this warp's first row of O and the stride between rows
@@ -882,6 +871,7 @@ __device__ void run_softmax(int t, int wq, int lane, uint8_t* smem, Bars* bars, 
         if constexpr (!VARLEN) {  // packed batches are never split
             // (cell: this warp's slot among the split units' merge counters and blocks)
             const uint32_t cell = w.cell + (uint32_t)t * 4u + (uint32_t)wq;
+            const int row0 = mb * kUnitRows + t * kTileM + wq * 32;
             split_piece_epilogue<D, OUT_F32>(g_fwd_queue[p.slot] + 2, p.partial, p.split.parts, cell,
                                              part, lane, tO, m, l, lx, stg, &epi_buf, to, row0, bh,
                                              (live && lse_ptr) ? lse_ptr + row_idx : nullptr, p.d_act);
@@ -1120,6 +1110,8 @@ attn_status_t launch_fwd_varlen(const void* q, const void* k, const void* v, voi
     if ((st = encode_tmap_ragged(&tq, q, false, d, Hq, 64, kTileM, true)) != ATTN_OK) return st;
     if ((st = encode_tmap_ragged(&tk, k, false, d, Hkv, 64, kTileN, true)) != ATTN_OK) return st;
     if ((st = encode_tmap_ragged(&tv, v, false, d, Hkv, 64, kTileN, true)) != ATTN_OK) return st;
+    // (O of a packed batch is written from registers, never by this map; it
+    // is still encoded, which checks O's alignment like the other maps)
     if ((st = encode_tmap_ragged(&to, o, f32, d, Hq, kEpiCols(f32), 32, false)) != ATTN_OK) return st;
     if (pad_head_dim(d) == 128)
         return f32 ? launch_fwd_t<128, true, true>(tq, tk, tv, to, lse, p, grid, stream, dev)
