@@ -57,21 +57,33 @@ KERNEL_SOURCES = {
 }
 
 
+def _code_only(text: str) -> str:
+    """C/C++ source with comments removed and trailing blanks stripped: what a
+    DRAM-traffic record depends on (string literals in these sources hold no
+    comment markers)."""
+    import re
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
+
+
 def kernel_source_hash(kernel: str) -> str:
-    """sha256 over name + bytes of one kernel's sources, in the listed order."""
+    """sha256 over name + code (comments removed) of one kernel's sources, in
+    the listed order: a comment edit keeps a traffic record valid, a code edit
+    does not."""
     import hashlib
     csrc = os.path.join(ROOT, "exact_attention_14_gb300", "csrc")
     h = hashlib.sha256()
     for name in KERNEL_SOURCES[kernel]:
         h.update(name.encode())
-        with open(os.path.join(csrc, name), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(csrc, name), encoding="utf-8") as fh:
+            h.update(_code_only(fh.read()).encode())
     return h.hexdigest()
 
 
 def read_traffic():
     """DRAM bytes per launch from the committed ncu summaries, for the kernels
-    whose sources have not changed since the capture."""
+    whose code (comments aside) has not changed since the capture."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return {}

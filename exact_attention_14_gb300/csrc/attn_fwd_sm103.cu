@@ -69,7 +69,9 @@ struct FwdCfg {
     static constexpr int kTileBytes = 128 * D * 2;        // one 128-row bf16 tile
     static constexpr int kStages = (D == 128) ? 4 : 8;     // K/V ring slots
     static constexpr int kRingOff = 2 * kTileBytes;        // after Q0, Q1
-    // epilogue staging: per softmax warp, two 2 KiB buffers (32 rows x 64 B)
+    // per softmax warp, two 2 KiB buffers (32 rows x 64 B) in which the merging
+    // piece of a split unit stages O for TMA stores (whole units write O from
+    // registers)
     static constexpr int kStgOff = kRingOff + kStages * kTileBytes;
     static constexpr int kStgBytesPerWarp = 2 * 2048;
     static constexpr int kBarOff = kStgOff + 8 * kStgBytesPerWarp;
