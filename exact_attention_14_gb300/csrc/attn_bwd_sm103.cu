@@ -344,25 +344,49 @@ __device__ __forceinline__ void ds_chunk_t(const float (&pf)[32], const uint32_t
     }
 }
 
-// 32 values of one output row, columns [0, ncols) of them (ncols <= 32, a
-// multiple of 8): 16-byte stores.
-template <int D, bool OUT_F32>
-__device__ __forceinline__ void store_row32(void* base, size_t elem, const float (&v)[32],
-                                            int ncols = 32) {
+// Store of 32 columns [cc, cc + 32) of this warp's 32 rows of an output
+// (rows row0 .. row0 + 31 of a row-major array with `row_elems` elements per
+// row), whole 32-byte sectors per store: lanes 2k and 2k+1 swap one 16-byte
+// piece of each sector, then both write row 2k's sector and, in the next
+// store, row 2k+1's.  Run by the whole warp (shuffles); rows at or past
+// rows_live and columns at or past ncols (uniform, a multiple of 8) are not
+// written.
+template <bool OUT_F32>
+__device__ __forceinline__ void store_rows32_pairs(void* base, size_t row0, size_t row_elems, int cc,
+                                                   const float (&v)[32], int ncols, int rows_live,
+                                                   int lane) {
+    constexpr int kEs = OUT_F32 ? 4 : 2;
+    constexpr int kPieces = 32 * kEs / 16;
+    constexpr int kColsPerPiece = 16 / kEs;
+    uint32_t wd[kPieces * 4];
     if constexpr (OUT_F32) {
-        uint4* dst = reinterpret_cast<uint4*>(static_cast<float*>(base) + elem);
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-            if (4 * i < ncols)
-                dst[i] = make_uint4(__float_as_uint(v[4 * i]), __float_as_uint(v[4 * i + 1]),
-                                    __float_as_uint(v[4 * i + 2]), __float_as_uint(v[4 * i + 3]));
+        for (int i = 0; i < 32; ++i) wd[i] = __float_as_uint(v[i]);
     } else {
-        uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(base) + elem);
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-            if (8 * i < ncols)
-                dst[i] = make_uint4(pack_bf16x2(v[8 * i], v[8 * i + 1]), pack_bf16x2(v[8 * i + 2], v[8 * i + 3]),
-                                    pack_bf16x2(v[8 * i + 4], v[8 * i + 5]), pack_bf16x2(v[8 * i + 6], v[8 * i + 7]));
+        for (int i = 0; i < 16; ++i) wd[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
+    }
+    const bool odd = lane & 1;
+    const int ra = lane & ~1, rb = lane | 1;
+    uint8_t* b8 = static_cast<uint8_t*>(base);
+    uint8_t* pa = b8 + ((row0 + (size_t)ra) * row_elems + (size_t)cc) * kEs + (odd ? 16 : 0);
+    uint8_t* pb = b8 + ((row0 + (size_t)rb) * row_elems + (size_t)cc) * kEs + (odd ? 16 : 0);
+    const bool live_a = ra < rows_live, live_b = rb < rows_live;
+#pragma unroll
+    for (int sct = 0; sct < kPieces / 2; ++sct) {
+        if (2 * sct * kColsPerPiece >= ncols) break;
+        const int pe = 2 * sct, po = 2 * sct + 1;
+        const bool col_ok = (odd ? po : pe) * kColsPerPiece < ncols;
+        uint32_t da[4], db[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t x = odd ? wd[pe * 4 + i] : wd[po * 4 + i];
+            const uint32_t y = __shfl_xor_sync(0xFFFFFFFFu, x, 1);
+            da[i] = odd ? y : wd[pe * 4 + i];
+            db[i] = odd ? wd[po * 4 + i] : y;
+        }
+        if (live_a && col_ok) *reinterpret_cast<uint4*>(pa + sct * 32) = make_uint4(da[0], da[1], da[2], da[3]);
+        if (live_b && col_ok) *reinterpret_cast<uint4*>(pb + sct * 32) = make_uint4(db[0], db[1], db[2], db[3]);
     }
 }
 
@@ -437,19 +461,19 @@ __device__ void bwd_pds(int wq, int lane, uint8_t* smem, BwdBars* bars, uint32_t
         return;
     }
     // dK = scale * dS^T Q, dV = P^T dO: one key row per thread, written once
-    const bool live = jg < p.Nk;
-    const size_t elem = (((size_t)w.b * p.Hkv + w.g) * p.Nk + (size_t)(live ? jg : 0)) * p.d_act;
+    // this warp's first key row and how many of its rows are inside Nk
+    const size_t wrow0 = ((size_t)w.b * p.Hkv + w.g) * p.Nk + (size_t)(w.k0 + wq * 32);
+    const int rows_live = p.Nk - (w.k0 + wq * 32);
     if (w.n_tiles == 0) {
         float z[32];
 #pragma unroll
         for (int x = 0; x < 32; ++x) z[x] = 0.f;
-        if (live)
 #pragma unroll 1
-            for (int cc = 0; cc < p.d_act; cc += 32) {
-                const int nc = p.d_act - cc < 32 ? p.d_act - cc : 32;
-                store_row32<D, OUT_F32>(p.dk, elem + cc, z, nc);
-                store_row32<D, OUT_F32>(p.dv, elem + cc, z, nc);
-            }
+        for (int cc = 0; cc < p.d_act; cc += 32) {
+            const int nc = p.d_act - cc < 32 ? p.d_act - cc : 32;
+            store_rows32_pairs<OUT_F32>(p.dk, wrow0, p.d_act, cc, z, nc, rows_live, lane);
+            store_rows32_pairs<OUT_F32>(p.dv, wrow0, p.d_act, cc, z, nc, rows_live, lane);
+        }
         return;
     }
     ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&bars->acc_full), 0, abort_flag));
@@ -467,12 +491,12 @@ __device__ void bwd_pds(int wq, int lane, uint8_t* smem, BwdBars* bars, uint32_t
         const int nc = p.d_act - cc < 32 ? p.d_act - cc : 32;  // <= 0: past the head dim
 #pragma unroll
         for (int x = 0; x < 32; ++x) v[x] = __uint_as_float(r[x]);
-        if (live && nc > 0) store_row32<D, OUT_F32>(p.dv, elem + cc, v, nc);
+        if (nc > 0) store_rows32_pairs<OUT_F32>(p.dv, wrow0, p.d_act, cc, v, nc, rows_live, lane);
         tmem_ld32(tmem + 256 + D + cc + lane_off, r);
         tmem_wait_ld();
 #pragma unroll
         for (int x = 0; x < 32; ++x) v[x] = __uint_as_float(r[x]) * p.scale;
-        if (live && nc > 0) store_row32<D, OUT_F32>(p.dk, elem + cc, v, nc);
+        if (nc > 0) store_rows32_pairs<OUT_F32>(p.dk, wrow0, p.d_act, cc, v, nc, rows_live, lane);
     }
 }
 
@@ -824,8 +848,9 @@ __device__ void dq_ds(int wq, int lane, DqBars* bars, uint32_t tmem, const BwdPa
     }
     tc_fence_after();
     // every lane runs the (warp-collective) TMEM loads; rows past Nq store nothing
-    const bool live = row < p.Nq;
-    const size_t elem = (bh * p.Nq + (size_t)(live ? row : 0)) * p.d_act;
+    // this warp's first query row and how many of its rows are inside Nq
+    const size_t wrow0 = bh * p.Nq + (size_t)(w.q0 + wq * 32);
+    const int rows_live = p.Nq - (w.q0 + wq * 32);
 #pragma unroll 1
     for (int cc = 0; cc < D; cc += 32) {
         float v[32];
@@ -840,7 +865,7 @@ __device__ void dq_ds(int wq, int lane, DqBars* bars, uint32_t tmem, const BwdPa
             for (int x = 0; x < 32; ++x) v[x] = 0.f;
         }
         const int nc = p.d_act - cc < 32 ? p.d_act - cc : 32;
-        if (live && nc > 0) store_row32<D, OUT_F32>(p.dq, elem + cc, v, nc);
+        if (nc > 0) store_rows32_pairs<OUT_F32>(p.dq, wrow0, p.d_act, cc, v, nc, rows_live, lane);
     }
 }
 
