@@ -53,8 +53,7 @@ struct WideCfg {
     static constexpr int kKVBytes = kWN * D * 2;    // D / 64 chunks of 64 rows x 128 B
     static constexpr int kKRing = kQBytes;          // 2 slots
     static constexpr int kVRing = kKRing + 2 * kKVBytes;  // 2 slots
-    static constexpr int kStg = kVRing + 2 * kKVBytes;    // 4 warps x 2 x 2 KiB
-    static constexpr int kBar = kStg + 4 * 4096;
+    static constexpr int kBar = kVRing + 2 * kKVBytes;
     static constexpr int kSmemBytes = kBar + 512 + 1024;
     static_assert(kSmemBytes <= 232448, "shared memory budget");
     static constexpr uint32_t kColO = 128;
@@ -67,6 +66,7 @@ struct WideParams {
     int group, off, d_act;
     float c;          // scale * log2(e)
     uint32_t slot;
+    void* o;          // O: [B, Hq, Nq, d_act]
 };
 
 constexpr uint32_t kWideQueueSlots = 256;
@@ -398,36 +398,46 @@ __device__ __forceinline__ void wide_softmax_tile(uint32_t (&sr)[64], int lim, b
     l += a + bb;
 }
 
+// Epilogue store of 32 columns [cc, cc + 32) of this warp's 32 rows of O
+// straight from registers, whole 32-byte sectors per store: lanes 2k and 2k+1
+// swap one 16-byte piece of each sector, then both write row 2k's sector and,
+// in the next store, row 2k+1's (no shared memory, which the S MMAs' operand
+// reads keep busy).  Run by the whole warp; rows at or past rows_live and
+// 16-byte pieces at or past d_act (a multiple of 8) are not written.
 template <bool OUT_F32>
-__device__ __forceinline__ void wide_store_cols(const float (&v)[32], int cc, uint8_t* stg,
-                                                uint32_t& epi_buf, int lane, const CUtensorMap* to,
-                                                int row0, int bh, int d_act) {
-    constexpr int kCols = wide_epi_cols(OUT_F32);
+__device__ __forceinline__ void wide_store_pairs(const float (&v)[32], int cc, int lane, uint8_t* o_warp,
+                                                 size_t row_stride, int rows_live, int d_act) {
+    constexpr int kEs = OUT_F32 ? 4 : 2;
+    constexpr int kPieces = 32 * kEs / 16;
+    constexpr int kColsPerPiece = 16 / kEs;
+    uint32_t wd[kPieces * 4];
+    if constexpr (OUT_F32) {
 #pragma unroll
-    for (int h = 0; h < 32 / kCols; ++h) {
-        if (cc + h * kCols >= d_act) break;
-        uint8_t* buf = stg + (epi_buf & 1) * 2048;
-        if (lane == 0) bulk_wait_group_read<1>();
-        __syncwarp();
-        const uint32_t dst = smem_u32(buf) + lane * 64;
-        if constexpr (OUT_F32) {
+        for (int i = 0; i < 32; ++i) wd[i] = __float_as_uint(v[i]);
+    } else {
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-                sts128(dst + 16 * i, __float_as_uint(v[h * 16 + 4 * i]), __float_as_uint(v[h * 16 + 4 * i + 1]),
-                       __float_as_uint(v[h * 16 + 4 * i + 2]), __float_as_uint(v[h * 16 + 4 * i + 3]));
-        } else {
+        for (int i = 0; i < 16; ++i) wd[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
+    }
+    const bool odd = lane & 1;
+    const int ra = lane & ~1, rb = lane | 1;
+    uint8_t* pa = o_warp + (size_t)ra * row_stride + (size_t)cc * kEs + (odd ? 16 : 0);
+    uint8_t* pb = o_warp + (size_t)rb * row_stride + (size_t)cc * kEs + (odd ? 16 : 0);
+    const bool live_a = ra < rows_live, live_b = rb < rows_live;
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-                sts128(dst + 16 * i, pack_bf16x2(v[8 * i], v[8 * i + 1]), pack_bf16x2(v[8 * i + 2], v[8 * i + 3]),
-                       pack_bf16x2(v[8 * i + 4], v[8 * i + 5]), pack_bf16x2(v[8 * i + 6], v[8 * i + 7]));
+    for (int sct = 0; sct < kPieces / 2; ++sct) {
+        if (cc + 2 * sct * kColsPerPiece >= d_act) break;
+        const int pe = 2 * sct, po = 2 * sct + 1;
+        const bool col_ok = cc + (odd ? po : pe) * kColsPerPiece < d_act;
+        uint32_t da[4], db[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t x = odd ? wd[pe * 4 + i] : wd[po * 4 + i];
+            const uint32_t y = __shfl_xor_sync(0xFFFFFFFFu, x, 1);
+            da[i] = odd ? y : wd[pe * 4 + i];
+            db[i] = odd ? wd[po * 4 + i] : y;
         }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-            tma_store_3d(to, smem_u32(buf), cc + h * kCols, row0, bh);
-            bulk_commit_group();
-        }
-        ++epi_buf;
+        if (live_a && col_ok) *reinterpret_cast<uint4*>(pa + sct * 32) = make_uint4(da[0], da[1], da[2], da[3]);
+        if (live_b && col_ok) *reinterpret_cast<uint4*>(pb + sct * 32) = make_uint4(db[0], db[1], db[2], db[3]);
     }
 }
 
@@ -440,8 +450,6 @@ __device__ void wide_softmax(int wq, int lane, uint8_t* smem, WideBars* bars, ui
     const FwdShape& s = p.shape;
     const uint32_t lane_off = uint32_t(wq * 32) << 16;
     const uint32_t tO = tmem + C::kColO + lane_off;
-    uint8_t* stg = smem + C::kStg + wq * 4096;
-    uint32_t epi_buf = 0;
     long long g = 0;
     bool ok = true;
     for (uint32_t k = 0; ok; ++k) {
@@ -484,6 +492,8 @@ __device__ void wide_softmax(int wq, int lane, uint8_t* smem, WideBars* bars, ui
         const float inv_l = 1.0f / l;
         const uint64_t il2 = f2(inv_l, inv_l);
         const int row0 = w.mt * kWM + wq * 32;
+        constexpr int kEs = OUT_F32 ? 4 : 2;
+        uint8_t* o_warp = static_cast<uint8_t*>(p.o) + ((size_t)w.bh * s.Nq + (size_t)row0) * p.d_act * kEs;
 #pragma unroll 1
         for (int cc = 0; cc < D; cc += 32) {
             uint32_t r[32];
@@ -493,15 +503,13 @@ __device__ void wide_softmax(int wq, int lane, uint8_t* smem, WideBars* bars, ui
 #pragma unroll
             for (int i = 0; i < 32; i += 2)
                 f2_split(f2_mul(f2(__uint_as_float(r[i]), __uint_as_float(r[i + 1])), il2), v[i], v[i + 1]);
-            wide_store_cols<OUT_F32>(v, cc, stg, epi_buf, lane, to, row0, w.bh, p.d_act);
+            wide_store_pairs<OUT_F32>(v, cc, lane, o_warp, (size_t)p.d_act * kEs, s.Nq - row0, p.d_act);
         }
         if (row < s.Nq && lse_ptr)
             lse_ptr[(size_t)w.bh * s.Nq + (size_t)row] = (m + log2f(lx)) * kWLn2;
         // (the next unit's P.V overwrites O only after this warpgroup's next
         // P is in TMEM, which follows these loads)
     }
-    if (lane == 0) bulk_wait_group_all();
-    __syncwarp();
     if (!ok) wide_abort(bars, err);
 }
 
@@ -591,6 +599,7 @@ attn_status_t launch_fwd_wide(const void* q, const void* k, const void* v, void*
     p.off = Nk - Nq;
     p.d_act = d;
     p.c = scale * kWLog2e;
+    p.o = o;
     static std::atomic<uint32_t> launches{0};
     p.slot = launches.fetch_add(1u, std::memory_order_relaxed) % kWideQueueSlots;
     const long long units = p.shape.units;
