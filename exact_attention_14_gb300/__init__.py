@@ -140,6 +140,26 @@ def _need(t, dtype, name):
         raise ValueError(f"{name} must be contiguous")
 
 
+def _one_device(*tensors):
+    """The device of the given tensors (None entries skipped): the library
+    launches on the current CUDA device, so every operand must live on one
+    device, which the call then makes current."""
+    dev = None
+    for t in tensors:
+        if t is None:
+            continue
+        if dev is None:
+            dev = t.device
+        elif t.device != dev:
+            raise ValueError(f"operands on different devices: {dev} and {t.device}")
+    return dev
+
+
+def _on(dev):
+    import torch
+    return torch.cuda.device(dev)
+
+
 def attn_fwd(q, k, v, o, lse=None, *, causal: bool = False, scale: float | None = None,
              stream=None):
     """Fused forward into caller-provided outputs.
@@ -166,8 +186,9 @@ def attn_fwd(q, k, v, o, lse=None, *, causal: bool = False, scale: float | None 
     if scale is None:
         scale = d ** -0.5
     odt = ATTN_OUT_F32 if o.dtype == torch.float32 else ATTN_OUT_BF16
-    rc = load().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, Nq, Nk, d,
-                         int(bool(causal)), float(scale), odt, _stream_ptr(stream))
+    with _on(_one_device(q, k, v, o, lse)):
+        rc = load().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, Nq, Nk, d,
+                             int(bool(causal)), float(scale), odt, _stream_ptr(stream))
     _check(rc, "attn_fwd")
     return o, lse
 
@@ -204,10 +225,11 @@ def attn_fwd_varlen(q, k, v, o, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int,
     if scale is None:
         scale = d ** -0.5
     odt = ATTN_OUT_F32 if o.dtype == torch.float32 else ATTN_OUT_BF16
-    rc = load().attn_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
-                                _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), B, Hq, Hkv, total_q,
-                                total_k, int(max_seqlen_q), int(max_seqlen_k), d,
-                                int(bool(causal)), float(scale), odt, _stream_ptr(stream))
+    with _on(_one_device(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k)):
+        rc = load().attn_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
+                                    _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), B, Hq, Hkv, total_q,
+                                    total_k, int(max_seqlen_q), int(max_seqlen_k), d,
+                                    int(bool(causal)), float(scale), odt, _stream_ptr(stream))
     _check(rc, "attn_fwd_varlen")
     return o, lse
 
@@ -252,8 +274,9 @@ def attn_fp8_quantize(x, codes, descale, signs=None, *, transpose: bool = False,
         raise ValueError(f"codes must be {want}")
     if tuple(descale.shape) != (B, H, (N + 127) // 128):
         raise ValueError("descale shape mismatch")
-    rc = load().attn_fp8_quantize(_ptr(x), _ptr(codes), _ptr(descale), _ptr(signs), B, H, N, d,
-                                  int(bool(transpose)), _stream_ptr(stream))
+    with _on(_one_device(x, codes, descale, signs)):
+        rc = load().attn_fp8_quantize(_ptr(x), _ptr(codes), _ptr(descale), _ptr(signs), B, H, N, d,
+                                      int(bool(transpose)), _stream_ptr(stream))
     _check(rc, "attn_fp8_quantize")
     return codes, descale
 
@@ -293,9 +316,10 @@ def attn_fwd_fp8(q8, k8, vt8, q_descale, k_descale, v_descale, o, lse=None, *,
     if scale is None:
         scale = d ** -0.5
     odt = ATTN_OUT_F32 if o.dtype == torch.float32 else ATTN_OUT_BF16
-    rc = load().attn_fwd_fp8(_ptr(q8), _ptr(k8), _ptr(vt8), _ptr(q_descale), _ptr(k_descale),
-                             _ptr(v_descale), _ptr(o), _ptr(lse), B, Hq, Hkv, Nq, Nk, d,
-                             int(bool(causal)), float(scale), odt, _stream_ptr(stream))
+    with _on(_one_device(q8, k8, vt8, q_descale, k_descale, v_descale, o, lse)):
+        rc = load().attn_fwd_fp8(_ptr(q8), _ptr(k8), _ptr(vt8), _ptr(q_descale), _ptr(k_descale),
+                                 _ptr(v_descale), _ptr(o), _ptr(lse), B, Hq, Hkv, Nq, Nk, d,
+                                 int(bool(causal)), float(scale), odt, _stream_ptr(stream))
     _check(rc, "attn_fwd_fp8")
     return o, lse
 
@@ -361,10 +385,11 @@ def attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, *, causal: bool = False,
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     odt = ATTN_OUT_F32 if o.dtype == torch.float32 else ATTN_OUT_BF16
     g32 = ATTN_OUT_F32 if gdt == torch.float32 else ATTN_OUT_BF16
-    rc = load().attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq),
-                         _ptr(dk), _ptr(dv), B, Hq, Hkv, Nq, Nk, d, int(bool(causal)),
-                         float(scale), odt, g32, _ptr(workspace), workspace.numel(),
-                         _stream_ptr(stream))
+    with _on(_one_device(q, k, v, o, dout, lse, dq, dk, dv, workspace)):
+        rc = load().attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq),
+                             _ptr(dk), _ptr(dv), B, Hq, Hkv, Nq, Nk, d, int(bool(causal)),
+                             float(scale), odt, g32, _ptr(workspace), workspace.numel(),
+                             _stream_ptr(stream))
     _check(rc, "attn_bwd")
     return dq, dk, dv
 
@@ -426,9 +451,10 @@ def attn_decode(q, k_cache, v_cache, seqlens, o, lse=None, *, scale: float | Non
         _need(workspace, workspace.dtype, "workspace")
         ws_ptr, ws_bytes = _ptr(workspace), workspace.numel() * workspace.element_size()
     odt = ATTN_OUT_F32 if o.dtype == torch.float32 else ATTN_OUT_BF16
-    rc = load().attn_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(seqlens), _ptr(o),
-                            _ptr(lse), B, Hq, Hkv, Nmax, d, float(scale), int(num_splits),
-                            ws_ptr, ws_bytes, odt, _stream_ptr(stream))
+    with _on(_one_device(q, k_cache, v_cache, seqlens, o, lse)):
+        rc = load().attn_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(seqlens), _ptr(o),
+                                _ptr(lse), B, Hq, Hkv, Nmax, d, float(scale), int(num_splits),
+                                ws_ptr, ws_bytes, odt, _stream_ptr(stream))
     _check(rc, "attn_decode")
     return o, lse
 
@@ -467,9 +493,10 @@ def attn_decode_noalloc(q, k_cache, v_cache, seqlens, o, lse=None, *,
     if scale is None:
         scale = d ** -0.5
     odt = ATTN_OUT_F32 if o.dtype == torch.float32 else ATTN_OUT_BF16
-    rc = load().attn_decode_noalloc(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(seqlens), _ptr(o),
-                                    _ptr(lse), B, Hq, Hkv, Nmax, d, float(scale),
-                                    int(num_splits), odt, _stream_ptr(stream))
+    with _on(_one_device(q, k_cache, v_cache, seqlens, o, lse)):
+        rc = load().attn_decode_noalloc(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(seqlens), _ptr(o),
+                                        _ptr(lse), B, Hq, Hkv, Nmax, d, float(scale),
+                                        int(num_splits), odt, _stream_ptr(stream))
     _check(rc, "attn_decode_noalloc")
     return o, lse
 
@@ -479,8 +506,9 @@ def attn_selftest_bounded_wait(mode: int, result, stream=None) -> None:
     writing its outcome into `result` (an int32 CUDA tensor of one element)."""
     import torch
     _need(result, torch.int32, "result")
-    _check(load().attn_selftest_bounded_wait(int(mode), _ptr(result), _stream_ptr(stream)),
-           "attn_selftest_bounded_wait")
+    with _on(_one_device(result)):
+        _check(load().attn_selftest_bounded_wait(int(mode), _ptr(result), _stream_ptr(stream)),
+               "attn_selftest_bounded_wait")
 
 
 def attn_last_device_error(stream=None) -> int:
@@ -575,10 +603,11 @@ def attn_decode_paged(q, k_pages, v_pages, block_table, seqlens, o, lse=None, *,
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
     odt = ATTN_OUT_F32 if o.dtype == torch.float32 else ATTN_OUT_BF16
-    rc = load().attn_decode_paged(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(block_table),
-                                  _ptr(seqlens), _ptr(o), _ptr(lse), B, Hq, Hkv, num_blocks,
-                                  page_size, max_blocks, d, float(scale), num_splits,
-                                  _ptr(workspace), workspace.numel(), odt, _stream_ptr(stream))
+    with _on(_one_device(q, k_pages, v_pages, block_table, seqlens, o, lse, workspace)):
+        rc = load().attn_decode_paged(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(block_table),
+                                      _ptr(seqlens), _ptr(o), _ptr(lse), B, Hq, Hkv, num_blocks,
+                                      page_size, max_blocks, d, float(scale), num_splits,
+                                      _ptr(workspace), workspace.numel(), odt, _stream_ptr(stream))
     _check(rc, "attn_decode_paged")
     return o, lse
 
