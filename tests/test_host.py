@@ -362,3 +362,14 @@ def test_no_test_function_defined_twice():
         names = [n.name for n in tree.body if isinstance(n, ast.FunctionDef) and n.name.startswith("test_")]
         dup = {n for n in names if names.count(n) > 1}
         assert not dup, f"{os.path.basename(path)} defines {sorted(dup)} more than once"
+
+
+def test_operands_must_share_one_device():
+    """The binding makes the operands' device current for each call and
+    refuses operands spread over devices (checked here with host and meta
+    tensors, no GPU needed)."""
+    import torch
+    a, b = torch.empty(2), torch.empty(2)
+    assert ea._one_device(a, None, b) == a.device
+    with pytest.raises(ValueError, match="different devices"):
+        ea._one_device(a, torch.empty(2, device="meta"))
