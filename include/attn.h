@@ -79,10 +79,13 @@ typedef enum {
  *   scale  softmax scale (typically 1/sqrt(d)); finite and >= 0
  *   causal 0 or 1 (bottom-right aligned; requires Nq <= Nk)
  *
- * Supported: 8 <= d <= 128 with d % 8 == 0 (d other than 64 and 128 runs on
- *            the 64- or 128-column kernel with the columns past d read as
- *            zero and never written); Hq % Hkv == 0; 1 <= Nq, Nk <= 2^24;
- *            B*Hq and B*Hkv <= 2^24.  Other d -> ATTN_ERR_UNSUPPORTED.
+ * Supported: 8 <= d <= 256 with d % 8 == 0: d <= 128 runs on the 64- or
+ *            128-column kernel (two 128-row Q tiles per CTA), 128 < d <= 256
+ *            on the 192- or 256-column kernel (one Q tile per CTA, 64-key
+ *            K/V tiles, no tail split); other d are padded to the next of
+ *            these with the columns past d read as zero and never written.
+ *            Hq % Hkv == 0; 1 <= Nq, Nk <= 2^24; B*Hq and B*Hkv <= 2^24.
+ *            Other d -> ATTN_ERR_UNSUPPORTED.
  * Numerics: scores and O accumulate in fp32; the probabilities that multiply V
  * are rounded to bf16.  The logsumexp uses the sum of the unrounded
  * probabilities; O is divided by that sum plus, per KV tile, the rounding
@@ -114,8 +117,8 @@ attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, flo
  *        neither read nor written)
  *   max_seqlen_q, max_seqlen_k  upper bounds of the lengths (host ints)
  *
- * Supported as attn_fwd; 1 <= total_q, total_k <= 2^30; max lengths in
- * [1, 2^24].  The lengths live on the device, so their checks run there: a
+ * Supported as attn_fwd but with 8 <= d <= 128 (d % 8 == 0); 1 <= total_q,
+ * total_k <= 2^30; max lengths in [1, 2^24].  The lengths live on the device, so their checks run there: a
  * sequence whose offsets leave [0, total], decrease, exceed the maximum
  * length, give query rows without keys, or (causal) more queries than keys
  * is not computed (its O and LSE rows are left as they were) and
@@ -206,8 +209,8 @@ size_t attn_bwd_workspace_size(int B, int Hq, int Hkv, int Nq, int Nk, int d);
  *            16-byte aligned; contents need no initialisation; not used after
  *            the call's kernels finish.
  *
- * Supported as for attn_fwd (8 <= d <= 128, d % 8 == 0, Hq % Hkv == 0, causal needs
- * Nq <= Nk).  Pointers 16-byte aligned (lse 4-byte).  The caller owns every
+ * Supported: 8 <= d <= 128 with d % 8 == 0 (attn_fwd's limits otherwise:
+ * Hq % Hkv == 0, causal needs Nq <= Nk).  Pointers 16-byte aligned (lse 4-byte).  The caller owns every
  * buffer.  Three kernels run in order on `stream`: a per-row pass (D, the LSE
  * in base 2), a K/V-outer pass (one CTA per (b, KV head, 128-key tile): dK
  * and dV accumulated in tensor memory over the group's query heads and Q
