@@ -28,9 +28,15 @@
  *
  * Conventions shared by every entry point
  *   - Pointers named q/k/v/o/lse/k_cache/v_cache/seqlens/workspace are DEVICE
- *     pointers.  The caller allocates and owns every buffer; the library never
- *     allocates device memory.  Tensor data must be 16-byte aligned.
- *   - Tensors are row-major and contiguous: [B, H, N, d] (d fastest).
+ *     pointers.  The caller allocates and owns every buffer it passes.  The
+ *     library's own device memory is static tables loaded with it (work
+ *     queues, merge counters, the error word, attn_decode_noalloc's scratch)
+ *     and, for attn_fwd's split tail units only, per-launch partial results
+ *     taken from a library-owned stream-ordered pool.  Tensor data must be
+ *     16-byte aligned.
+ *   - Tensors are row-major and contiguous: [B, H, N, d] (d fastest) unless
+ *     an entry point states another layout (packed batches, paged caches,
+ *     transposed FP8 codes).
  *   - bf16 means IEEE-style bfloat16 (1-8-7).  Accumulation is fp32.
  *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy
  *     default stream).  Host-side argument checks run before anything is
