@@ -46,8 +46,8 @@ def read_peaks():
 
 
 # The sources each profiled kernel is built from (its own translation unit and
-# the headers it includes); a kernel's DRAM figures stay valid while these hash
-# to the value stored beside them.
+# the headers it includes); a kernel's DRAM figures stay valid while their code
+# (comments removed) hashes to the value stored beside them.
 KERNEL_SOURCES = {
     "attn_fwd_kernel": ["attn_fwd_sm103.cu", "fwd_sched.h", "ptx.cuh", "internal.h"],
     "attn_decode_split_kernel": ["attn_decode_sm103.cu", "ptx.cuh", "internal.h"],
@@ -484,7 +484,7 @@ def run_ours(args, rank, world, local_rank):
                "attn_tflops": f8 / ta_ / 1e12, "attn_ms": 1e3 * ta_,
                "attn_frac_of_fp8_peak": f8 / ta_ / 1e12 / peak8,
                "fp8_peak_tflops": peak8,
-               "fp8_peak_source": "measured bf16_tflops x 2 (nominal fp8/bf16 ratio)",
+               "fp8_peak_source": f"{peaks['source']} bf16_tflops x 2 (nominal fp8/bf16 ratio)",
                "quantize_gbs": qbytes / tq_ / 1e9, "quantize_ms": 1e3 * tq_,
                "quantize_frac_of_hbm": qbytes / tq_ / 1e9 / peaks["hbm_gbs"],
                "with_quantize_tflops": f8 / (ta_ + tq_) / 1e12}
