@@ -8,7 +8,17 @@ One step = the whole hot path over one batch of synthetic input:
   valid lengths uniform in [1024, 32768]).
 `value` is forward TFLOPS (algorithmic 4*B*H*N*N*d, halved for causal) over the
 two forward launches; the decode's HBM GB/s is reported beside it.  Inputs are
-resident in HBM; L2 is flushed (a 512 MiB write) between timed steps.
+resident in HBM; L2 is flushed (a 512 MiB write) between timed steps.  Each
+launch of the step is then timed again over --stat-iters iterations for its
+median, min and max.
+
+Beside the step: the long-context (B=1 H=32 N=16384, outlier channels) and GQA
+(B=8 Hq=32 Hkv=8 N=4096) causal forwards (`configs`), the backward, the packed
+variable-length forward, the FP8 forward and the d=256 forward, each timed
+alone; `e2e` runs the whole step through the public API from pinned host
+buffers.  The oracle leg (`cpu_baseline`) times the fp64 CPU oracle on whole
+heads of the prefill inputs and checks the bench's own last outputs for those
+heads against it.
 
 `--impl reference` times the fp64 CPU oracle instead (a bounded sample of the
 same workload on the host cores).
@@ -151,28 +161,62 @@ def fwd_flops(B, H, N, d, causal):
     return f / 2 if causal else f
 
 
-def oracle_sample(seconds: float, seed: int = 1):
-    """Time the fp64 oracle on whole heads of the prefill workload (non-causal
-    and causal alternately) until `seconds` of work; returns (TFLOPS, desc, cores)."""
-    import numpy as np
+def oracle_sample(seconds: float, q, k, v, scale, heads=None):
+    """Time the fp64 oracle on whole heads of the prefill workload (the same
+    inputs the GPU legs use), non-causal and causal alternately, until
+    `seconds` of work (or over the given (b, h, causal) heads).  Returns
+    (TFLOPS, desc, cores, elapsed, [(b, h, causal, O, LSE), ...])."""
     import oracle
-    from exact_attention_14_gb300.inputs import PREFILL, make_fwd_inputs
-    cfg = PREFILL
-    q, k, v = make_fwd_inputs(1, 1, 1, cfg.N, cfg.N, cfg.d, seed=seed)
     oracle.build()
-    flops, t0, heads = 0.0, time.perf_counter(), 0
+    B, H, N, d = q.shape
+    flops, t0, done, out = 0.0, time.perf_counter(), 0, []
     while True:
-        causal = bool(heads % 2)
-        oracle.attention(q, k, v, causal=causal, scale=cfg.scale)
-        flops += fwd_flops(1, 1, cfg.N, cfg.d, causal)
-        heads += 1
+        if heads is not None:
+            if done >= len(heads):
+                break
+            b, h, causal = heads[done]
+        else:
+            b, h, causal = (done // 2) % B, ((done // 2) // B) % H, bool(done % 2)
+        sl = (slice(b, b + 1), slice(h, h + 1))
+        o_ref, l_ref = oracle.attention(q[sl], k[sl], v[sl], causal=causal, scale=scale)
+        out.append((b, h, causal, o_ref[0, 0], l_ref[0, 0]))
+        flops += fwd_flops(1, 1, N, d, causal)
+        done += 1
         el = time.perf_counter() - t0
-        if el >= seconds:
+        if heads is None and el >= seconds:
             break
+    el = time.perf_counter() - t0
     cores = os.cpu_count() or 1
-    desc = (f"{heads} whole heads of the prefill workload (N={cfg.N}, d={cfg.d}), "
+    desc = (f"{done} whole heads of the prefill workload (N={N}, d={d}), "
             f"alternating non-causal/causal, fp64 three-pass oracle, OpenMP on {cores} threads")
-    return flops / el / 1e12, desc, cores, el
+    return flops / el / 1e12, desc, cores, el, out
+
+
+def stats_ms(times_s):
+    """Median, min and max (ms) of per-iteration device times."""
+    t = sorted(times_s)
+    n = len(t)
+    med = t[n // 2] if n % 2 else 0.5 * (t[n // 2 - 1] + t[n // 2])
+    return {"median_ms": 1e3 * med, "min_ms": 1e3 * t[0], "max_ms": 1e3 * t[-1], "iters": n}
+
+
+def time_legs(stream, fns, iters, flush, flush_each=False):
+    """Per-launch device times (s) of each callable in `fns`, over `iters`
+    iterations after an L2 flush (before every callable if flush_each), CUDA
+    events on `stream`.  Returns one list of times per callable."""
+    evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in fns] for _ in range(iters)]
+    for i in range(iters):
+        flush.zero_()
+        for j, fn in enumerate(fns):
+            if flush_each and j > 0:
+                flush.zero_()
+            evs[i][j][0].record(stream)
+            fn()
+            evs[i][j][1].record(stream)
+    torch.cuda.synchronize()
+    return [[evs[i][j][0].elapsed_time(evs[i][j][1]) * 1e-3 for i in range(iters)]
+            for j in range(len(fns))]
 
 
 def ranks_barrier(world: int) -> None:
@@ -194,17 +238,17 @@ def ranks_max(values, world: int, device) -> list:
 def run_reference(args, rank, world):
     if rank != 0:
         return
-    steps = []
+    from exact_attention_14_gb300.inputs import PREFILL, make_config_inputs
+    q, k, v = make_config_inputs(PREFILL)
     for _ in range(args.warmup):
-        oracle_sample(1.0)
+        oracle_sample(1.0, q, k, v, PREFILL.scale)
     total_flops = total_t = 0.0
     cores = os.cpu_count() or 1
     desc = ""
     for _ in range(args.steps):
-        tf, desc, cores, el = oracle_sample(3.0)
+        tf, desc, cores, el, _ = oracle_sample(3.0, q, k, v, PREFILL.scale)
         total_flops += tf * el * 1e12
         total_t += el
-        steps.append(el)
     value = total_flops / total_t / 1e12
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOPS",
@@ -222,21 +266,27 @@ def run_reference(args, rank, world):
 
 def run_ours(args, rank, world, local_rank):
     import exact_attention_14_gb300 as ea
-    from exact_attention_14_gb300.inputs import DECODE, LONG, PREFILL, VARLEN, hadamard_signs, \
-        make_config_inputs, make_decode_config_inputs, make_fwd_inputs, make_varlen_inputs, \
-        varlen_lengths
+    from exact_attention_14_gb300.inputs import DECODE, GQA, LONG, PREFILL, VARLEN, \
+        hadamard_signs, make_config_inputs, make_decode_config_inputs, make_fwd_inputs, \
+        make_varlen_inputs, varlen_lengths
 
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
     ea.load()
     peaks = read_peaks()
+    peak_t = peaks["bf16_tflops"]
+    traffic = read_traffic()
     cfg = PREFILL
     q_h, k_h, v_h = make_config_inputs(cfg)
     q, k, v = q_h.to(dev), k_h.to(dev), v_h.to(dev)
-    o = torch.empty(q.shape, dtype=torch.bfloat16, device=dev)
-    lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
-    dq, dk, dv, dsl = make_decode_config_inputs(DECODE)
-    dq, dk, dv, dsl = dq.to(dev), dk.to(dev), dv.to(dev), dsl.to(dev)
+    # one output buffer per mask, so both results stay for the parity check
+    o = {c: torch.empty(q.shape, dtype=torch.bfloat16, device=dev) for c in (False, True)}
+    lse = {c: torch.empty(q.shape[:3], dtype=torch.float32, device=dev) for c in (False, True)}
+    fws = {c: torch.empty(max(16, ea.attn_fwd_workspace_size(cfg.B, cfg.Hq, cfg.Hkv, cfg.N, cfg.N,
+                                                             cfg.d, c)),
+                          dtype=torch.uint8, device=dev) for c in (False, True)}
+    dq_h, dk_h, dv_h, dsl_h = make_decode_config_inputs(DECODE)
+    dq, dk, dv, dsl = dq_h.to(dev), dk_h.to(dev), dv_h.to(dev), dsl_h.to(dev)
     d_o = torch.empty(dq.shape, dtype=torch.bfloat16, device=dev)
     d_lse = torch.empty(dq.shape[:3], dtype=torch.float32, device=dev)
     ws = torch.empty(ea.attn_decode_workspace_size(DECODE.B, DECODE.Hq, DECODE.Hkv, DECODE.Nmax,
@@ -250,14 +300,20 @@ def run_ours(args, rank, world, local_rank):
     f_c = fwd_flops(cfg.B, cfg.Hq, cfg.N, cfg.d, True)
     stream = torch.cuda.current_stream(dev)
 
-    def step(ev=None):
-        if ev: ev[0].record(stream)
-        ea.attn_fwd(q, k, v, o, lse, causal=False, stream=stream)
-        if ev: ev[1].record(stream)
-        ea.attn_fwd(q, k, v, o, lse, causal=True, stream=stream)
-        if ev: ev[2].record(stream)
+    def fwd_launch(c):
+        return lambda: ea.attn_fwd(q, k, v, o[c], lse[c], causal=c, workspace=fws[c],
+                                   stream=stream)
+
+    def dec_launch():
         ea.attn_decode(dq, dk, dv, dsl, d_o, d_lse, workspace=ws, stream=stream)
-        if ev: ev[3].record(stream)
+
+    step_fns = [fwd_launch(False), fwd_launch(True), dec_launch]
+
+    def step(ev=None):
+        for j, fn in enumerate(step_fns):
+            if ev: ev[j].record(stream)
+            fn()
+        if ev: ev[len(step_fns)].record(stream)
 
     args.warmup = max(args.warmup, 3)
     # The flush comes first in every step: the GPU is still writing it while
@@ -280,273 +336,72 @@ def run_ours(args, rank, world, local_rank):
             step(evs[i])
         torch.cuda.synchronize()
         wall = time.perf_counter() - t0
+        # per-launch statistics over more iterations (same launches, L2 flushed
+        # before each step), still under the clock sampler
+        n_stat = max(args.stat_iters, args.steps)
+        st_nc, st_c, st_dec = time_legs(stream, step_fns, n_stat, flush)
     ranks_barrier(world)
     if ea.attn_last_device_error() != 0:
         raise RuntimeError("device error during the timed region")
-    t_nc = sum(e[0].elapsed_time(e[1]) for e in evs) / args.steps * 1e-3
-    t_c = sum(e[1].elapsed_time(e[2]) for e in evs) / args.steps * 1e-3
-    t_dec = sum(e[2].elapsed_time(e[3]) for e in evs) / args.steps * 1e-3
+    per = [[e[j].elapsed_time(e[j + 1]) * 1e-3 for e in evs] for j in range(3)]
+    t_nc, t_c, t_dec = (sum(x) / args.steps for x in per)
     t_nc, t_c, t_dec = ranks_max([t_nc, t_c, t_dec], world, dev)
     t_step = t_nc + t_c + t_dec
     tflops = world * (f_nc + f_c) / (t_nc + t_c) / 1e12
     dec_gbs = world * dec_bytes / t_dec / 1e9
 
-    # end to end through the public API: pinned host inputs -> device -> result to host
+    # end to end through the public API: pinned host inputs -> device -> result
+    # to host, for the whole step (both forwards and the decode; the decode's
+    # KV cache is resident state, its query and lengths come from the host)
     e2e = None
     if rank == 0 or world > 1:
-        qp, kp, vp = (t.pin_memory() for t in (q_h, k_h, v_h))
-        oh = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for _ in range(2)]
-        lh = [torch.empty(lse.shape, dtype=lse.dtype).pin_memory() for _ in range(2)]
-        # Steps stream through three CUDA streams: step i's host->device copies
-        # (s_in) overlap step i-1's kernels and step i-2's device->host copies
-        # (s_out); device buffers alternate between two sets, and events keep
-        # each set from being overwritten before its readers are done.
-        s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-        ins = [tuple(torch.empty_like(t) for t in (q, k, v)) for _ in range(2)]
-        outs = [[(torch.empty_like(o), torch.empty_like(lse)) for _ in range(2)] for _ in range(2)]
-        ev_in, ev_comp, ev_out = ([torch.cuda.Event() for _ in range(2)] for _ in range(3))
-        count = [0]
+        e2e = run_e2e(ea, args, world, dev, stream, (q_h, k_h, v_h), (dq_h, dsl_h), (dk, dv),
+                      o, lse, d_o, d_lse, ws, fws, f_nc + f_c)
 
-        def e2e_step():
-            i = count[0]
-            count[0] += 1
-            b = i % 2
-            qd, kd, vd = ins[b]
-            with torch.cuda.stream(s_in):
-                if i >= 2:
-                    s_in.wait_event(ev_comp[b])       # step i-2's kernels have read ins[b]
-                qd.copy_(qp, non_blocking=True)
-                kd.copy_(kp, non_blocking=True)
-                vd.copy_(vp, non_blocking=True)
-                ev_in[b].record(s_in)
-            stream.wait_event(ev_in[b])
-            if i >= 2:
-                stream.wait_event(ev_out[b])          # step i-2's results have left outs[b]
-            for m, c in enumerate((False, True)):
-                ea.attn_fwd(qd, kd, vd, outs[b][m][0], outs[b][m][1], causal=c, stream=stream)
-            ev_comp[b].record(stream)
-            with torch.cuda.stream(s_out):
-                s_out.wait_event(ev_comp[b])
-                for m in range(2):
-                    oh[m].copy_(outs[b][m][0], non_blocking=True)
-                    lh[m].copy_(outs[b][m][1], non_blocking=True)
-                ev_out[b].record(s_out)
-
-        for _ in range(3):
-            e2e_step()
-        torch.cuda.synchronize()
-        ranks_barrier(world)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(s_in)
-        for _ in range(args.steps):
-            e2e_step()
-        e1.record(s_out)
-        e1.synchronize()
-        torch.cuda.synchronize()
-        t_e2e = ranks_max([e0.elapsed_time(e1) / args.steps * 1e-3], world, dev)[0]
-        # the last step's causal result, read back through the pipeline, equals
-        # the headline step's (same inputs, deterministic kernel)
-        if not (torch.equal(oh[1], o.cpu()) and torch.equal(lh[1], lse.cpu())):
-            raise RuntimeError("end-to-end leg returned a different result")
-        h2d = sum(t.numel() * t.element_size() for t in (q_h, k_h, v_h))
-        d2h = sum(t.numel() * t.element_size() for t in oh + lh)
-        e2e = {"value": world * (f_nc + f_c) / t_e2e / 1e12, "unit": "TFLOPS",
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "ms_per_step": 1e3 * t_e2e,
-               "pipeline": "pinned host buffers; step i's H2D, step i-1's two attn_fwd calls and "
-                           "step i-2's D2H on three streams, device buffers double-buffered"}
-
-    # Backward (a follow-on row, timed apart from the step): attn_bwd on the
-    # prefill inputs, non-causal then causal, O and LSE from attn_fwd.
-    bwd = None
+    extra = {}
+    if not args.no_configs:
+        extra["configs"] = run_configs(ea, args, dev, stream, flush, peaks, traffic)
     if not args.no_bwd:
-        g = torch.Generator().manual_seed(5)
-        dout = torch.randn(q.shape, generator=g, dtype=torch.float32).to(torch.bfloat16).to(dev)
-        ob = {c: ea.forward(q, k, v, causal=c, out_dtype=torch.bfloat16, stream=stream)
-              for c in (False, True)}
-        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-        bws = torch.empty(ea.attn_bwd_workspace_size(cfg.B, cfg.Hq, cfg.Hkv, cfg.N, cfg.N, cfg.d),
-                          dtype=torch.uint8, device=dev)
-
-        def bwd_step(ev=None):
-            for idx, c in enumerate((False, True)):
-                if ev: ev[idx].record(stream)
-                ea.attn_bwd(q, k, v, ob[c][0], dout, ob[c][1], dq, dk, dv, causal=c,
-                            workspace=bws, stream=stream)
-            if ev: ev[2].record(stream)
-
-        for _ in range(args.warmup):
-            flush.zero_()
-            bwd_step()
-        bev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
-        torch.cuda.synchronize()
-        for i in range(args.steps):
-            flush.zero_()
-            bwd_step(bev[i])
-        torch.cuda.synchronize()
-        if ea.attn_last_device_error() != 0:
-            raise RuntimeError("device error in the backward leg")
-        tb_nc = sum(e[0].elapsed_time(e[1]) for e in bev) / args.steps * 1e-3
-        tb_c = sum(e[1].elapsed_time(e[2]) for e in bev) / args.steps * 1e-3
-        fb_nc, fb_c = 2.5 * f_nc, 2.5 * f_c  # five GEMMs per tile against the forward's two
-        bwd = {"kernels": "attn_bwd (prep + K/V-outer dK/dV pass + Q-outer dQ pass)",
-               "noncausal_tflops": fb_nc / tb_nc / 1e12, "causal_tflops": fb_c / tb_c / 1e12,
-               "noncausal_ms": 1e3 * tb_nc, "causal_ms": 1e3 * tb_c,
-               "tflops": (fb_nc + fb_c) / (tb_nc + tb_c) / 1e12,
-               "frac_of_bf16_peak": (fb_nc + fb_c) / (tb_nc + tb_c) / 1e12 / peaks["bf16_tflops"],
-               "flops_note": "2.5 x the forward formula (S, dP, dV, dK, dQ products)"}
-
-    # Packed variable-length prefill (a follow-on row, timed apart from the
-    # step): 16 causal sequences of U[256, 4096] tokens in one attn_fwd_varlen.
-    varlen = None
+        extra["bwd"] = run_bwd(ea, args, dev, stream, flush, peaks, q, k, v)
     if not args.no_varlen:
-        vc = VARLEN
-        lens = varlen_lengths(vc.n_seqs, vc.len_lo, vc.len_hi, vc.seed)
-        vq, vk, vv, vcq, vck = (t.to(dev) for t in make_varlen_inputs(lens, lens, vc.Hq, vc.Hkv,
-                                                                       vc.d, vc.seed))
-        vo = torch.empty(vq.shape, dtype=torch.bfloat16, device=dev)
-        vl = torch.empty((vc.Hq, vq.shape[0]), dtype=torch.float32, device=dev)
-
-        def varlen_step():
-            ea.attn_fwd_varlen(vq, vk, vv, vo, vcq, vck, max(lens), max(lens), vl,
-                               causal=vc.causal, scale=vc.scale, stream=stream)
-
-        for _ in range(args.warmup):
-            flush.zero_()
-            varlen_step()
-        vev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
-        torch.cuda.synchronize()
-        for i in range(args.steps):
-            flush.zero_()
-            vev[i][0].record(stream)
-            varlen_step()
-            vev[i][1].record(stream)
-        torch.cuda.synchronize()
-        if ea.attn_last_device_error() != 0:
-            raise RuntimeError("device error in the varlen leg")
-        tv = sum(e[0].elapsed_time(e[1]) for e in vev) / args.steps * 1e-3
-        fv = sum(4.0 * vc.Hq * n * n * vc.d / (2 if vc.causal else 1) for n in lens)
-        varlen = {"kernel": "attn_fwd_kernel (packed, ragged tensor maps)",
-                  "workload": f"{vc.n_seqs} sequences U[{vc.len_lo},{vc.len_hi}] "
-                              f"(total {sum(lens)} tokens, max {max(lens)}) Hq={vc.Hq} "
-                              f"Hkv={vc.Hkv} d={vc.d} causal={vc.causal}",
-                  "tflops": fv / tv / 1e12, "ms": 1e3 * tv,
-                  "frac_of_bf16_peak": fv / tv / 1e12 / peaks["bf16_tflops"],
-                  "flops_note": "sum over sequences of the forward formula 4*H*L^2*d (/2 causal)"}
-
-    # FP8 forward (a follow-on row, timed apart from the step): the long-context
-    # causal workload (B1 H32 N16384 d128, 4 outlier channels in Q and K),
-    # quantized with the random-sign Hadamard rotation; the three quantize
-    # launches and the attention launch are timed separately.
-    fp8 = None
+        extra["varlen"] = run_varlen(ea, args, dev, stream, flush, peaks)
     if not args.no_fp8:
-        lq, lk, lv = (t.to(dev) for t in make_config_inputs(LONG))
-        signs = hadamard_signs(LONG.d, seed=LONG.seed).to(dev)
-        q8, qd = ea.fp8_quantize(lq, signs, stream=stream)
-        k8, kd = ea.fp8_quantize(lk, signs, stream=stream)
-        vt8, vd = ea.fp8_quantize(lv, None, transpose=True, stream=stream)
-        o8 = torch.empty(lq.shape, dtype=torch.bfloat16, device=dev)
-        l8 = torch.empty(lq.shape[:3], dtype=torch.float32, device=dev)
-        eff = LONG.scale / LONG.d
-
-        def quant_step():
-            ea.attn_fp8_quantize(lq, q8, qd, signs, stream=stream)
-            ea.attn_fp8_quantize(lk, k8, kd, signs, stream=stream)
-            ea.attn_fp8_quantize(lv, vt8, vd, None, transpose=True, stream=stream)
-
-        def fp8_step():
-            ea.attn_fwd_fp8(q8, k8, vt8, qd, kd, vd, o8, l8, causal=True, scale=eff, stream=stream)
-
-        for _ in range(args.warmup):
-            flush.zero_()
-            quant_step()
-            fp8_step()
-        fev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
-        torch.cuda.synchronize()
-        for i in range(args.steps):
-            flush.zero_()
-            fev[i][0].record(stream)
-            quant_step()
-            fev[i][1].record(stream)
-            fp8_step()
-            fev[i][2].record(stream)
-        torch.cuda.synchronize()
-        if ea.attn_last_device_error() != 0:
-            raise RuntimeError("device error in the fp8 leg")
-        tq_ = sum(e[0].elapsed_time(e[1]) for e in fev) / args.steps * 1e-3
-        ta_ = sum(e[1].elapsed_time(e[2]) for e in fev) / args.steps * 1e-3
-        f8 = LONG.flops(True)
-        n_el = lq.numel() + lk.numel() + lv.numel()
-        qbytes = 3 * n_el + 4 * (qd.numel() + kd.numel() + vd.numel())   # bf16 in, E4M3 out
-        peak8 = 2 * peaks["bf16_tflops"]
-        fp8 = {"kernels": "attn_fp8_quantize (x3: Q, K rotated; V transposed) + attn_fwd_fp8_kernel",
-               "workload": "long-context causal B=1 H=32 N=16384 d=128, 4 outlier channels",
-               "attn_tflops": f8 / ta_ / 1e12, "attn_ms": 1e3 * ta_,
-               "attn_frac_of_fp8_peak": f8 / ta_ / 1e12 / peak8,
-               "fp8_peak_tflops": peak8,
-               "fp8_peak_source": f"{peaks['source']} bf16_tflops x 2 (nominal fp8/bf16 ratio)",
-               "quantize_gbs": qbytes / tq_ / 1e9, "quantize_ms": 1e3 * tq_,
-               "quantize_frac_of_hbm": qbytes / tq_ / 1e9 / peaks["hbm_gbs"],
-               "with_quantize_tflops": f8 / (ta_ + tq_) / 1e12}
-
-    # Head dim 256 (a follow-on row, timed apart from the step): the prefill
-    # shape B4 H16 N2048 at d = 256 on the one-Q-tile-per-CTA kernel.
-    wide = None
+        extra["fp8"] = run_fp8(ea, args, dev, stream, flush, peaks)
     if not args.no_wide:
-        wq_, wk_, wv_ = (t.to(dev) for t in make_fwd_inputs(cfg.B, cfg.Hq, cfg.Hkv, cfg.N, cfg.N,
-                                                             256, seed=6))
-        wo = torch.empty(wq_.shape, dtype=torch.bfloat16, device=dev)
-        wl = torch.empty(wq_.shape[:3], dtype=torch.float32, device=dev)
-        for _ in range(args.warmup):
-            for c in (False, True):
-                flush.zero_()
-                ea.attn_fwd(wq_, wk_, wv_, wo, wl, causal=c, stream=stream)
-        wev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
-        torch.cuda.synchronize()
-        for i in range(args.steps):
-            for m, c in enumerate((False, True)):
-                flush.zero_()
-                wev[i][2 * m].record(stream)
-                ea.attn_fwd(wq_, wk_, wv_, wo, wl, causal=c, stream=stream)
-                wev[i][2 * m + 1].record(stream)
-        torch.cuda.synchronize()
-        if ea.attn_last_device_error() != 0:
-            raise RuntimeError("device error in the d=256 leg")
-        tw = [sum(e[2 * m].elapsed_time(e[2 * m + 1]) for e in wev) / args.steps * 1e-3 for m in range(2)]
-        fw = [fwd_flops(cfg.B, cfg.Hq, cfg.N, 256, c) for c in (False, True)]
-        wide = {"kernel": "attn_fwd_wide_kernel<256> (one Q tile per CTA, 64-key tiles, two S buffers)",
-                "workload": f"prefill B={cfg.B} H={cfg.Hq} N={cfg.N} d=256",
-                "noncausal_tflops": fw[0] / tw[0] / 1e12, "causal_tflops": fw[1] / tw[1] / 1e12,
-                "noncausal_ms": 1e3 * tw[0], "causal_ms": 1e3 * tw[1],
-                "frac_of_bf16_peak": sum(fw) / sum(tw) / 1e12 / peaks["bf16_tflops"]}
+        extra["wide"] = run_wide(ea, args, dev, stream, flush, peaks)
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        tf, desc, cores, _ = oracle_sample(args.cpu_seconds)
-        cpu = {"value": tf, "unit": "TFLOPS", "cores": cores, "kind": "oracle", "sample": desc}
+        tf, desc, cores, _, heads = oracle_sample(args.cpu_seconds, q_h, k_h, v_h, cfg.scale)
+        cpu = {"value": tf, "unit": "TFLOPS", "cores": cores, "kind": "oracle", "sample": desc,
+               "parity_check": parity_of_heads(heads, o, lse)}
+        if not cpu["parity_check"]["pass"]:
+            raise RuntimeError(f"bench outputs differ from the oracle: {cpu['parity_check']}")
 
     if rank != 0:
         return
     fwd_time = t_nc + t_c
-    peak_t = peaks["bf16_tflops"]
-    traffic = read_traffic()
+    tr = traffic.get("attn_fwd_kernel", {})
     roof = {"bound": "tensor", "kernel": "attn_fwd_kernel (non-causal + causal launches)",
             "achieved": (f_nc + f_c) / fwd_time / 1e12, "peak": peak_t, "unit": "TFLOP/s",
             "frac": (f_nc + f_c) / fwd_time / 1e12 / peak_t,
-            "traffic": (traffic["attn_fwd_kernel"]["prefill_noncausal"]
-                        + traffic["attn_fwd_kernel"]["prefill_causal"])
-                       if "attn_fwd_kernel" in traffic else None,
+            "traffic": (tr["prefill_noncausal"] + tr["prefill_causal"])
+                       if "prefill_noncausal" in tr and "prefill_causal" in tr else None,
             "traffic_note": "DRAM bytes of one non-causal + one causal launch (ncu, profiles/); "
                             "algorithmic bytes 2 x 134.7 MB",
-            "peak_source": f"{peaks['source']} bf16_tflops (burst)"}
+            "peak_source": f"{peaks['source']} bf16_tflops (burst)",
+            "noncausal": {"achieved": f_nc / t_nc / 1e12, "frac": f_nc / t_nc / 1e12 / peak_t,
+                          "traffic": tr.get("prefill_noncausal"), **stats_ms(st_nc)},
+            "causal": {"achieved": f_c / t_c / 1e12, "frac": f_c / t_c / 1e12 / peak_t,
+                       "traffic": tr.get("prefill_causal"), **stats_ms(st_c)}}
+    trd = traffic.get("attn_decode_split_kernel", {})
     roof_dec = {"bound": "hbm", "kernel": "attn_decode_split_kernel (split-KV with in-kernel merge)",
                 "achieved": dec_bytes / t_dec / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": dec_bytes / t_dec / 1e9 / peaks["hbm_gbs"],
-                "traffic": traffic["attn_decode_split_kernel"]["decode"]
-                           if "attn_decode_split_kernel" in traffic else None,
+                "traffic": trd.get("decode"),
                 "traffic_note": "DRAM bytes per launch (ncu, profiles/); algorithmic bytes in "
                                 "decode.algorithmic_bytes",
-                "peak_source": f"{peaks['source']} hbm_gbs"}
+                "peak_source": f"{peaks['source']} hbm_gbs", **stats_ms(st_dec)}
     line = {
         "metric": METRIC, "value": tflops, "unit": "TFLOPS", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t_step,
@@ -562,8 +417,7 @@ def run_ours(args, rank, world, local_rank):
         "decode": {"value": dec_gbs, "unit": "GB/s", "ms": 1e3 * t_dec,
                    "algorithmic_bytes": dec_bytes, "frac_of_hbm": dec_gbs / world / peaks["hbm_gbs"],
                    "sum_seqlen": sum_len},
-        "roofline": roof, "roofline_decode": roof_dec, "bwd": bwd, "varlen": varlen, "fp8": fp8,
-        "wide": wide,
+        "roofline": roof, "roofline_decode": roof_dec, **extra,
         "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": (2 + ea.attn_decode_kernel_launches(DECODE.B, DECODE.Hq, DECODE.Hkv,
                                                             DECODE.Nmax, DECODE.d)) * args.steps,
@@ -573,6 +427,265 @@ def run_ours(args, rank, world, local_rank):
     print(json.dumps(line), flush=True)
 
 
+def parity_of_heads(heads, o, lse):
+    """The bench's last outputs (bf16 O, fp32 LSE) on the heads the oracle leg
+    computed, against the oracle within the parity tolerances (O compared with
+    the oracle rounded to bf16, plus half a bf16 ulp)."""
+    import numpy as np
+    worst_o = worst_l = 0.0
+    ok = True
+    for b, h, causal, o_ref, l_ref in heads:
+        got = o[causal][b, h].float().cpu().double().numpy()
+        ref = torch.from_numpy(o_ref).to(torch.bfloat16).double().numpy()
+        half_ulp = np.exp2(np.floor(np.log2(np.maximum(np.abs(ref), 1e-30))) - 8)
+        err = np.abs(got - ref)
+        ok &= bool((err <= 1e-2 + half_ulp).all())
+        worst_o = max(worst_o, float(err.max()))
+        dl = float(np.abs(lse[causal][b, h].cpu().double().numpy() - l_ref).max())
+        ok &= dl <= 1e-3
+        worst_l = max(worst_l, dl)
+    return {"heads": len(heads), "rows": sum(x[3].shape[0] for x in heads),
+            "max_abs_o": worst_o, "max_abs_lse": worst_l, "pass": ok,
+            "tolerance": "|dO| <= 1e-2 + half a bf16 ulp of the bf16-rounded oracle, |dLSE| <= 1e-3"}
+
+
+def run_e2e(ea, args, world, dev, stream, fwd_host, dec_host, dec_cache, o, lse, d_o, d_lse, ws,
+            fws, fwd_flops_total):
+    """The whole step through the public API with host buffers: each step
+    copies its inputs from pinned host memory (prefill Q, K, V; the decode
+    query and lengths) and reads its results back (both forwards' O and LSE,
+    the decode's O and LSE).  Steps are pipelined over three streams: step i's
+    host-to-device copies overlap step i-1's kernels and step i-2's copies
+    back; device buffers alternate between two sets."""
+    q_h, k_h, v_h = fwd_host
+    dq_h, dsl_h = dec_host
+    dk, dv = dec_cache
+    inp_h = [t.pin_memory() for t in (q_h, k_h, v_h, dq_h, dsl_h)]
+    res_shapes = [(o[False], lse[False]), (o[True], lse[True]), (d_o, d_lse)]
+    outs_h = [torch.empty(t.shape, dtype=t.dtype).pin_memory()
+              for pair in res_shapes for t in pair]
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ins = [[torch.empty_like(t, device=dev) for t in inp_h] for _ in range(2)]
+    outs = [[torch.empty_like(t) for pair in res_shapes for t in pair] for _ in range(2)]
+    dws = [torch.empty_like(ws) for _ in range(2)]
+    ev_in, ev_comp, ev_out = ([torch.cuda.Event() for _ in range(2)] for _ in range(3))
+    count = [0]
+
+    def e2e_step():
+        i = count[0]
+        count[0] += 1
+        b = i % 2
+        qd, kd, vd, dqd, dsld = ins[b]
+        with torch.cuda.stream(s_in):
+            if i >= 2:
+                s_in.wait_event(ev_comp[b])       # step i-2's kernels have read ins[b]
+            for dst, src in zip(ins[b], inp_h):
+                dst.copy_(src, non_blocking=True)
+            ev_in[b].record(s_in)
+        stream.wait_event(ev_in[b])
+        if i >= 2:
+            stream.wait_event(ev_out[b])          # step i-2's results have left outs[b]
+        ob = outs[b]
+        for m, c in enumerate((False, True)):
+            ea.attn_fwd(qd, kd, vd, ob[2 * m], ob[2 * m + 1], causal=c, workspace=fws[c],
+                        stream=stream)
+        ea.attn_decode(dqd, dk, dv, dsld, ob[4], ob[5], workspace=dws[b], stream=stream)
+        ev_comp[b].record(stream)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(ev_comp[b])
+            for dst, src in zip(outs_h, ob):
+                dst.copy_(src, non_blocking=True)
+            ev_out[b].record(s_out)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    ranks_barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s_in)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(s_out)
+    e1.synchronize()
+    torch.cuda.synchronize()
+    t_e2e = ranks_max([e0.elapsed_time(e1) / args.steps * 1e-3], world, dev)[0]
+    # the last step's results, read back through the pipeline, equal the
+    # headline step's (same inputs, deterministic kernels)
+    dev_res = [t for pair in res_shapes for t in pair]
+    if not all(torch.equal(h, d.cpu()) for h, d in zip(outs_h, dev_res)):
+        raise RuntimeError("end-to-end leg returned a different result")
+    h2d = sum(t.numel() * t.element_size() for t in inp_h)
+    d2h = sum(t.numel() * t.element_size() for t in outs_h)
+    return {"value": world * fwd_flops_total / t_e2e / 1e12, "unit": "TFLOPS",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": 1e3 * t_e2e,
+            "covers": "both prefill forwards and the decode of a step (forward FLOPs over the "
+                      "whole step's time)",
+            "pipeline": "pinned host buffers; step i's H2D, step i-1's kernels and step i-2's "
+                        "D2H on three streams, device buffers double-buffered"}
+
+
+def run_configs(ea, args, dev, stream, flush, peaks, traffic):
+    """The long-context (B1 H32 N16384, outlier channels) and GQA (B8 Hq32
+    Hkv8 N4096) causal forwards, each timed alone after an L2 flush."""
+    from exact_attention_14_gb300.inputs import GQA, LONG, make_config_inputs
+    out = {}
+    tr = traffic.get("attn_fwd_kernel", {})
+    for cfg, key in ((LONG, "long"), (GQA, "gqa")):
+        q, k, v = (t.to(dev) for t in make_config_inputs(cfg))
+        o = torch.empty(q.shape, dtype=torch.bfloat16, device=dev)
+        lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
+        wsz = ea.attn_fwd_workspace_size(cfg.B, cfg.Hq, cfg.Hkv, cfg.N, cfg.N, cfg.d, True)
+        w = torch.empty(max(16, wsz), dtype=torch.uint8, device=dev)
+        fn = lambda: ea.attn_fwd(q, k, v, o, lse, causal=True, workspace=w, stream=stream)  # noqa
+        for _ in range(args.warmup):
+            flush.zero_()
+            fn()
+        t = time_legs(stream, [fn], max(args.stat_iters, args.steps), flush)[0]
+        if ea.attn_last_device_error() != 0:
+            raise RuntimeError(f"device error in the {key} leg")
+        st = stats_ms(t)
+        f = cfg.flops(True)
+        tf = f / (st["median_ms"] * 1e-3) / 1e12
+        out[key] = {"kernel": "attn_fwd_kernel", "workload":
+                    f"{cfg.name}: B={cfg.B} Hq={cfg.Hq} Hkv={cfg.Hkv} N={cfg.N} d={cfg.d}",
+                    "tflops": tf, "frac_of_bf16_peak": tf / peaks["bf16_tflops"],
+                    "flops": f, "traffic": tr.get(f"{key}_causal"), **st}
+        del q, k, v, o, lse, w
+    return out
+
+
+def run_bwd(ea, args, dev, stream, flush, peaks, q, k, v):
+    """attn_bwd on the prefill inputs, non-causal then causal, O and LSE from
+    attn_fwd."""
+    from exact_attention_14_gb300.inputs import PREFILL as cfg
+    g = torch.Generator().manual_seed(5)
+    dout = torch.randn(q.shape, generator=g, dtype=torch.float32).to(torch.bfloat16).to(dev)
+    ob = {c: ea.forward(q, k, v, causal=c, out_dtype=torch.bfloat16, stream=stream)
+          for c in (False, True)}
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    bws = torch.empty(ea.attn_bwd_workspace_size(cfg.B, cfg.Hq, cfg.Hkv, cfg.N, cfg.N, cfg.d),
+                      dtype=torch.uint8, device=dev)
+    fns = [lambda c=c: ea.attn_bwd(q, k, v, ob[c][0], dout, ob[c][1], dq, dk, dv, causal=c,
+                                   workspace=bws, stream=stream) for c in (False, True)]
+    for _ in range(args.warmup):
+        flush.zero_()
+        for fn in fns:
+            fn()
+    t_nc, t_c = time_legs(stream, fns, max(args.stat_iters, args.steps), flush, flush_each=True)
+    if ea.attn_last_device_error() != 0:
+        raise RuntimeError("device error in the backward leg")
+    s_nc, s_c = stats_ms(t_nc), stats_ms(t_c)
+    f_nc = 2.5 * fwd_flops(cfg.B, cfg.Hq, cfg.N, cfg.d, False)  # five GEMMs per tile
+    f_c = 2.5 * fwd_flops(cfg.B, cfg.Hq, cfg.N, cfg.d, True)
+    tb_nc, tb_c = s_nc["median_ms"] * 1e-3, s_c["median_ms"] * 1e-3
+    return {"kernels": "attn_bwd (prep + K/V-outer dK/dV pass + Q-outer dQ pass)",
+            "noncausal_tflops": f_nc / tb_nc / 1e12, "causal_tflops": f_c / tb_c / 1e12,
+            "noncausal": s_nc, "causal": s_c,
+            "tflops": (f_nc + f_c) / (tb_nc + tb_c) / 1e12,
+            "frac_of_bf16_peak": (f_nc + f_c) / (tb_nc + tb_c) / 1e12 / peaks["bf16_tflops"],
+            "flops_note": "2.5 x the forward formula (S, dP, dV, dK, dQ products); medians"}
+
+
+def run_varlen(ea, args, dev, stream, flush, peaks):
+    """16 causal sequences of U[256, 4096] tokens in one attn_fwd_varlen."""
+    from exact_attention_14_gb300.inputs import VARLEN as vc, make_varlen_inputs, varlen_lengths
+    lens = varlen_lengths(vc.n_seqs, vc.len_lo, vc.len_hi, vc.seed)
+    vq, vk, vv, vcq, vck = (t.to(dev) for t in make_varlen_inputs(lens, lens, vc.Hq, vc.Hkv,
+                                                                   vc.d, vc.seed))
+    vo = torch.empty(vq.shape, dtype=torch.bfloat16, device=dev)
+    vl = torch.empty((vc.Hq, vq.shape[0]), dtype=torch.float32, device=dev)
+    fn = lambda: ea.attn_fwd_varlen(vq, vk, vv, vo, vcq, vck, max(lens), max(lens), vl,  # noqa
+                                    causal=vc.causal, scale=vc.scale, stream=stream)
+    for _ in range(args.warmup):
+        flush.zero_()
+        fn()
+    st = stats_ms(time_legs(stream, [fn], max(args.stat_iters, args.steps), flush)[0])
+    if ea.attn_last_device_error() != 0:
+        raise RuntimeError("device error in the varlen leg")
+    fv = sum(4.0 * vc.Hq * n * n * vc.d / (2 if vc.causal else 1) for n in lens)
+    tv = st["median_ms"] * 1e-3
+    return {"kernel": "attn_fwd_kernel (packed, ragged tensor maps)",
+            "workload": f"{vc.n_seqs} sequences U[{vc.len_lo},{vc.len_hi}] "
+                        f"(total {sum(lens)} tokens, max {max(lens)}) Hq={vc.Hq} "
+                        f"Hkv={vc.Hkv} d={vc.d} causal={vc.causal}",
+            "tflops": fv / tv / 1e12, "frac_of_bf16_peak": fv / tv / 1e12 / peaks["bf16_tflops"],
+            **st, "flops_note": "sum over sequences of the forward formula 4*H*L^2*d (/2 causal)"}
+
+
+def run_fp8(ea, args, dev, stream, flush, peaks):
+    """The long-context causal workload quantized with the random-sign
+    Hadamard rotation; the three quantize launches and the attention launch
+    are timed separately."""
+    from exact_attention_14_gb300.inputs import LONG, hadamard_signs, make_config_inputs
+    lq, lk, lv = (t.to(dev) for t in make_config_inputs(LONG))
+    signs = hadamard_signs(LONG.d, seed=LONG.seed).to(dev)
+    q8, qd = ea.fp8_quantize(lq, signs, stream=stream)
+    k8, kd = ea.fp8_quantize(lk, signs, stream=stream)
+    vt8, vd = ea.fp8_quantize(lv, None, transpose=True, stream=stream)
+    o8 = torch.empty(lq.shape, dtype=torch.bfloat16, device=dev)
+    l8 = torch.empty(lq.shape[:3], dtype=torch.float32, device=dev)
+
+    def quant():
+        ea.attn_fp8_quantize(lq, q8, qd, signs, stream=stream)
+        ea.attn_fp8_quantize(lk, k8, kd, signs, stream=stream)
+        ea.attn_fp8_quantize(lv, vt8, vd, None, transpose=True, stream=stream)
+
+    def attn():
+        ea.attn_fwd_fp8(q8, k8, vt8, qd, kd, vd, o8, l8, causal=True, scale=LONG.scale,
+                        rotated=True, stream=stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        quant()
+        attn()
+    tq_, ta_ = time_legs(stream, [quant, attn], max(args.stat_iters, args.steps), flush)
+    if ea.attn_last_device_error() != 0:
+        raise RuntimeError("device error in the fp8 leg")
+    sq, sa = stats_ms(tq_), stats_ms(ta_)
+    tq_, ta_ = sq["median_ms"] * 1e-3, sa["median_ms"] * 1e-3
+    f8 = LONG.flops(True)
+    n_el = lq.numel() + lk.numel() + lv.numel()
+    qbytes = 3 * n_el + 4 * (qd.numel() + kd.numel() + vd.numel())   # bf16 in, E4M3 out
+    peak8 = 2 * peaks["bf16_tflops"]
+    return {"kernels": "attn_fp8_quantize (x3: Q, K rotated; V transposed) + attn_fwd_fp8_kernel",
+            "workload": "long-context causal B=1 H=32 N=16384 d=128, 4 outlier channels",
+            "attn_tflops": f8 / ta_ / 1e12, "attn": sa,
+            "attn_frac_of_fp8_peak": f8 / ta_ / 1e12 / peak8,
+            "fp8_peak_tflops": peak8,
+            "fp8_peak_source": f"nominal: 2 x {peaks['source']} bf16_tflops (the fp8/bf16 "
+                               "dense ratio; no measured fp8 peak)",
+            "quantize_gbs": qbytes / tq_ / 1e9, "quantize": sq,
+            "quantize_frac_of_hbm": qbytes / tq_ / 1e9 / peaks["hbm_gbs"],
+            "with_quantize_tflops": f8 / (ta_ + tq_) / 1e12}
+
+
+def run_wide(ea, args, dev, stream, flush, peaks):
+    """The prefill shape B4 H16 N2048 at d = 256 on the one-Q-tile-per-CTA
+    kernel, non-causal and causal, each after an L2 flush."""
+    from exact_attention_14_gb300.inputs import PREFILL as cfg, make_fwd_inputs
+    wq_, wk_, wv_ = (t.to(dev) for t in make_fwd_inputs(cfg.B, cfg.Hq, cfg.Hkv, cfg.N, cfg.N,
+                                                         256, seed=6))
+    wo = torch.empty(wq_.shape, dtype=torch.bfloat16, device=dev)
+    wl = torch.empty(wq_.shape[:3], dtype=torch.float32, device=dev)
+    fns = [lambda c=c: ea.attn_fwd(wq_, wk_, wv_, wo, wl, causal=c, stream=stream)
+           for c in (False, True)]
+    for _ in range(args.warmup):
+        for fn in fns:
+            flush.zero_()
+            fn()
+    t_nc, t_c = time_legs(stream, fns, max(args.stat_iters, args.steps), flush, flush_each=True)
+    if ea.attn_last_device_error() != 0:
+        raise RuntimeError("device error in the d=256 leg")
+    s_nc, s_c = stats_ms(t_nc), stats_ms(t_c)
+    fw = [fwd_flops(cfg.B, cfg.Hq, cfg.N, 256, c) for c in (False, True)]
+    tw = [s_nc["median_ms"] * 1e-3, s_c["median_ms"] * 1e-3]
+    return {"kernel": "attn_fwd_wide_kernel<256> (one Q tile per CTA, 64-key tiles, two S buffers)",
+            "workload": f"prefill B={cfg.B} H={cfg.Hq} N={cfg.N} d=256",
+            "noncausal_tflops": fw[0] / tw[0] / 1e12, "causal_tflops": fw[1] / tw[1] / 1e12,
+            "noncausal": s_nc, "causal": s_c,
+            "frac_of_bf16_peak": sum(fw) / sum(tw) / 1e12 / peaks["bf16_tflops"]}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -580,6 +693,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--stat-iters", type=int, default=50,
+                    help="iterations per leg for the median/min/max statistics")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the long-context and GQA legs")
     ap.add_argument("--no-bwd", action="store_true", help="skip the backward leg")
     ap.add_argument("--no-varlen", action="store_true", help="skip the packed varlen leg")
     ap.add_argument("--no-fp8", action="store_true", help="skip the FP8 leg")

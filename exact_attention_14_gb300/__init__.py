@@ -16,7 +16,8 @@ import ctypes
 import os
 
 __all__ = [
-    "ATTN_OUT_BF16", "ATTN_OUT_F32", "AttnError", "attn_fwd", "attn_fwd_varlen", "forward_varlen",
+    "ATTN_OUT_BF16", "ATTN_OUT_F32", "AttnError", "attn_fwd", "attn_fwd_workspace_size",
+    "attn_fwd_varlen", "forward_varlen",
     "attn_fp8_quantize", "fp8_quantize", "attn_fwd_fp8", "forward_fp8", "attn_fp8_codes_bytes",
     "attn_fp8_descale_count",
     "attn_decode",
@@ -43,12 +44,13 @@ _c_int, _c_ll, _c_sz, _c_f, _vp = (ctypes.c_int, ctypes.c_longlong, ctypes.c_siz
                                    ctypes.c_float, ctypes.c_void_p)
 SIGNATURES = {
     "attn_fwd": (_c_int, [_vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int,
-                          _c_int, _c_int, _c_f, _c_int, _vp]),
+                          _c_int, _c_int, _c_f, _c_int, _vp, _c_sz, _vp]),
+    "attn_fwd_workspace_size": (_c_sz, [_c_int] * 7),
     "attn_fwd_varlen": (_c_int, [_vp] * 7 + [_c_int] * 9 + [_c_f, _c_int, _vp]),
     "attn_fp8_codes_bytes": (_c_sz, [_c_int] * 5),
     "attn_fp8_descale_count": (_c_sz, [_c_int] * 3),
     "attn_fp8_quantize": (_c_int, [_vp] * 4 + [_c_int] * 5 + [_vp]),
-    "attn_fwd_fp8": (_c_int, [_vp] * 8 + [_c_int] * 7 + [_c_f, _c_int, _vp]),
+    "attn_fwd_fp8": (_c_int, [_vp] * 8 + [_c_int] * 7 + [_c_f, _c_int, _c_int, _vp]),
     "attn_selftest_bounded_wait": (_c_int, [_c_int, _vp, _vp]),
     "attn_decode_workspace_size": (_c_sz, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_int]),
     "attn_decode": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int,
@@ -140,6 +142,14 @@ def _need(t, dtype, name):
         raise ValueError(f"{name} must be contiguous")
 
 
+def _workspace(ws):
+    """(pointer, bytes) of an optional workspace tensor."""
+    if ws is None:
+        return None, 0
+    _need(ws, ws.dtype, "workspace")
+    return _ptr(ws), ws.numel() * ws.element_size()
+
+
 def _one_device(*tensors):
     """The device of the given tensors (None entries skipped): the library
     launches on the current CUDA device, so every operand must live on one
@@ -160,12 +170,21 @@ def _on(dev):
     return torch.cuda.device(dev)
 
 
+def attn_fwd_workspace_size(B: int, Hq: int, Hkv: int, Nq: int, Nk: int, d: int,
+                            causal: bool) -> int:
+    """Bytes of workspace attn_fwd needs for this shape on the current device
+    (0 when it splits no unit)."""
+    return int(load().attn_fwd_workspace_size(B, Hq, Hkv, Nq, Nk, d, int(bool(causal))))
+
+
 def attn_fwd(q, k, v, o, lse=None, *, causal: bool = False, scale: float | None = None,
-             stream=None):
+             workspace=None, stream=None):
     """Fused forward into caller-provided outputs.
 
     q [B,Hq,Nq,d] bf16; k, v [B,Hkv,Nk,d] bf16; o [B,Hq,Nq,d] bf16 or fp32;
-    lse [B,Hq,Nq] fp32 or None.  Asynchronous on ``stream`` (default: the
+    lse [B,Hq,Nq] fp32 or None; workspace: a CUDA tensor of at least
+    attn_fwd_workspace_size(...) bytes, or None (then one is allocated with
+    torch when the shape needs it).  Asynchronous on ``stream`` (default: the
     current torch stream)."""
     import torch
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
@@ -186,9 +205,18 @@ def attn_fwd(q, k, v, o, lse=None, *, causal: bool = False, scale: float | None 
     if scale is None:
         scale = d ** -0.5
     odt = ATTN_OUT_F32 if o.dtype == torch.float32 else ATTN_OUT_BF16
-    with _on(_one_device(q, k, v, o, lse)):
+    dev = _one_device(q, k, v, o, lse, workspace)
+    with _on(dev):
+        if workspace is None:
+            need = attn_fwd_workspace_size(B, Hq, Hkv, Nq, Nk, d, causal)
+            if need > 0:
+                workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+                if isinstance(stream, torch.cuda.Stream):
+                    workspace.record_stream(stream)   # freed only after that stream's use
+        ws_ptr, ws_bytes = _workspace(workspace)
         rc = load().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, Nq, Nk, d,
-                             int(bool(causal)), float(scale), odt, _stream_ptr(stream))
+                             int(bool(causal)), float(scale), odt, ws_ptr, ws_bytes,
+                             _stream_ptr(stream))
     _check(rc, "attn_fwd")
     return o, lse
 
@@ -293,10 +321,14 @@ def fp8_quantize(x, signs=None, *, transpose: bool = False, stream=None):
 
 
 def attn_fwd_fp8(q8, k8, vt8, q_descale, k_descale, v_descale, o, lse=None, *,
-                 causal: bool = False, scale: float | None = None, stream=None):
+                 causal: bool = False, scale: float | None = None, rotated: bool = False,
+                 stream=None):
     """Forward on E4M3 operands into caller-provided outputs: q8 [B,Hq,Nq,128],
     k8 [B,Hkv,Nk,128], vt8 [B,Hkv,128,Np] (uint8 codes), descales fp32
-    [B,H,ceil(N/128)]; o [B,Hq,Nq,128] bf16/fp32; lse [B,Hq,Nq] or None."""
+    [B,H,ceil(N/128)]; o [B,Hq,Nq,128] bf16/fp32; lse [B,Hq,Nq] or None.
+    scale is the original problem's softmax scale; rotated: Q and K were
+    quantized with the same Hadamard signs (the library then divides the
+    scale by d)."""
     import torch
     for t, n in ((q8, "q8"), (k8, "k8"), (vt8, "vt8")):
         _need(t, torch.uint8, n)
@@ -313,13 +345,20 @@ def attn_fwd_fp8(q8, k8, vt8, q_descale, k_descale, v_descale, o, lse=None, *,
         raise ValueError("k8 / vt8 shape mismatch")
     if tuple(o.shape) != (B, Hq, Nq, d):
         raise ValueError("o shape mismatch")
+    if lse is not None and tuple(lse.shape) != (B, Hq, Nq):
+        raise ValueError("lse shape mismatch")
+    nbq, nbk = (Nq + 127) // 128, (Nk + 127) // 128
+    if (tuple(q_descale.shape) != (B, Hq, nbq) or tuple(k_descale.shape) != (B, Hkv, nbk)
+            or tuple(v_descale.shape) != (B, Hkv, nbk)):
+        raise ValueError("descale shape mismatch")
     if scale is None:
         scale = d ** -0.5
     odt = ATTN_OUT_F32 if o.dtype == torch.float32 else ATTN_OUT_BF16
     with _on(_one_device(q8, k8, vt8, q_descale, k_descale, v_descale, o, lse)):
         rc = load().attn_fwd_fp8(_ptr(q8), _ptr(k8), _ptr(vt8), _ptr(q_descale), _ptr(k_descale),
                                  _ptr(v_descale), _ptr(o), _ptr(lse), B, Hq, Hkv, Nq, Nk, d,
-                                 int(bool(causal)), float(scale), odt, _stream_ptr(stream))
+                                 int(bool(causal)), float(scale), int(bool(rotated)), odt,
+                                 _stream_ptr(stream))
     _check(rc, "attn_fwd_fp8")
     return o, lse
 
@@ -335,13 +374,12 @@ def forward_fp8(q, k, v, *, causal: bool = False, scale: float | None = None, si
     q8, qd = fp8_quantize(q, signs, stream=stream)
     k8, kd = fp8_quantize(k, signs, stream=stream)
     vt8, vd = fp8_quantize(v, None, transpose=True, stream=stream)
-    eff = scale / d if signs is not None else scale   # (Q D H)(K D H)^T = d Q K^T
     out_dtype = out_dtype or torch.bfloat16
     o = torch.empty(q.shape, dtype=out_dtype, device=q.device)
     lse = (torch.empty(q.shape[:3], dtype=torch.float32, device=q.device)
            if return_lse else None)
-    return attn_fwd_fp8(q8, k8, vt8, qd, kd, vd, o, lse, causal=causal, scale=eff,
-                        stream=stream)
+    return attn_fwd_fp8(q8, k8, vt8, qd, kd, vd, o, lse, causal=causal, scale=scale,
+                        rotated=signs is not None, stream=stream)
 
 
 def attn_bwd_workspace_size(B: int, Hq: int, Hkv: int, Nq: int, Nk: int, d: int) -> int:
@@ -422,6 +460,38 @@ def attn_decode_workspace_size(B: int, Hq: int, Hkv: int, Nmax: int, d: int,
     return int(load().attn_decode_workspace_size(B, Hq, Hkv, Nmax, d, num_splits))
 
 
+def _check_decode_args(q, k_cache, v_cache, seqlens, o, lse):
+    """Types and shapes of a contiguous-cache decode call (everything the
+    kernels index by): q [B,Hq,1,d] bf16, caches [B,Hkv,Nmax,d] bf16, seqlens
+    [B] int32, o [B,Hq,1,d] bf16/fp32, lse [B,Hq,1] fp32 or None.  Returns
+    (B, Hq, Hkv, Nmax, d)."""
+    import torch
+    named = [(q, "q", torch.bfloat16), (k_cache, "k_cache", torch.bfloat16),
+             (v_cache, "v_cache", torch.bfloat16), (seqlens, "seqlens", torch.int32)]
+    if lse is not None:
+        named.append((lse, "lse", torch.float32))
+    # types, then shapes, then placement: each is checked before any pointer
+    # reaches the library
+    for t, n, dt in named:
+        if not isinstance(t, torch.Tensor) or t.dtype != dt:
+            raise TypeError(f"{n} must be a {dt} tensor")
+    if not isinstance(o, torch.Tensor) or o.dtype not in (torch.bfloat16, torch.float32):
+        raise TypeError("o must be a bfloat16 or float32 tensor")
+    if q.ndim != 4 or k_cache.ndim != 4:
+        raise ValueError("q and the caches must be 4-D")
+    B, Hq, one, d = q.shape
+    Hkv, Nmax = k_cache.shape[1], k_cache.shape[2]
+    if one != 1 or tuple(k_cache.shape) != (B, Hkv, Nmax, d) or v_cache.shape != k_cache.shape:
+        raise ValueError("decode shape mismatch")
+    if tuple(o.shape) != (B, Hq, 1, d) or tuple(seqlens.shape) != (B,):
+        raise ValueError("decode output/seqlens shape mismatch")
+    if lse is not None and tuple(lse.shape) != (B, Hq, 1):
+        raise ValueError("lse shape mismatch")
+    for t, n, dt in named + [(o, "o", o.dtype)]:
+        _need(t, dt, n)
+    return B, Hq, Hkv, Nmax, d
+
+
 def attn_decode(q, k_cache, v_cache, seqlens, o, lse=None, *, scale: float | None = None,
                 num_splits: int = 0, workspace=None, stream=None):
     """Split-KV decode into caller-provided outputs.
@@ -430,26 +500,10 @@ def attn_decode(q, k_cache, v_cache, seqlens, o, lse=None, *, scale: float | Non
     o [B,Hq,1,d] bf16/fp32; lse [B,Hq,1] fp32 or None; workspace: a uint8
     CUDA tensor of at least attn_decode_workspace_size(...) bytes."""
     import torch
-    for t, n in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache")):
-        _need(t, torch.bfloat16, n)
-    _need(seqlens, torch.int32, "seqlens")
-    if o.dtype not in (torch.bfloat16, torch.float32):
-        raise TypeError("o must be bfloat16 or float32")
-    _need(o, o.dtype, "o")
-    if lse is not None:
-        _need(lse, torch.float32, "lse")
-    B, Hq, one, d = q.shape
-    Hkv, Nmax = k_cache.shape[1], k_cache.shape[2]
-    if one != 1 or tuple(k_cache.shape) != (B, Hkv, Nmax, d) or v_cache.shape != k_cache.shape:
-        raise ValueError("decode shape mismatch")
-    if tuple(o.shape) != (B, Hq, 1, d) or tuple(seqlens.shape) != (B,):
-        raise ValueError("decode output/seqlens shape mismatch")
+    B, Hq, Hkv, Nmax, d = _check_decode_args(q, k_cache, v_cache, seqlens, o, lse)
     if scale is None:
         scale = d ** -0.5
-    ws_ptr, ws_bytes = None, 0
-    if workspace is not None:
-        _need(workspace, workspace.dtype, "workspace")
-        ws_ptr, ws_bytes = _ptr(workspace), workspace.numel() * workspace.element_size()
+    ws_ptr, ws_bytes = _workspace(workspace)
     odt = ATTN_OUT_F32 if o.dtype == torch.float32 else ATTN_OUT_BF16
     with _on(_one_device(q, k_cache, v_cache, seqlens, o, lse)):
         rc = load().attn_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(seqlens), _ptr(o),
@@ -482,14 +536,7 @@ def attn_decode_noalloc(q, k_cache, v_cache, seqlens, o, lse=None, *,
     and race; calls ordered on one stream do not.  The first call on a device
     must come before any stream capture."""
     import torch
-    for t, n in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache")):
-        _need(t, torch.bfloat16, n)
-    _need(seqlens, torch.int32, "seqlens")
-    _need(o, o.dtype, "o")
-    if lse is not None:
-        _need(lse, torch.float32, "lse")
-    B, Hq, _, d = q.shape
-    Hkv, Nmax = k_cache.shape[1], k_cache.shape[2]
+    B, Hq, Hkv, Nmax, d = _check_decode_args(q, k_cache, v_cache, seqlens, o, lse)
     if scale is None:
         scale = d ** -0.5
     odt = ATTN_OUT_F32 if o.dtype == torch.float32 else ATTN_OUT_BF16
@@ -580,22 +627,30 @@ def attn_decode_paged(q, k_pages, v_pages, block_table, seqlens, o, lse=None, *,
     block_table [B, max_blocks] int32; seqlens [B] int32; o [B,Hq,1,d] bf16
     or fp32; lse [B,Hq,1] fp32 or None.  Asynchronous."""
     import torch
-    _need(q, torch.bfloat16, "q")
-    _need(k_pages, torch.bfloat16, "k_pages")
-    _need(v_pages, torch.bfloat16, "v_pages")
-    _need(block_table, torch.int32, "block_table")
-    _need(seqlens, torch.int32, "seqlens")
-    if o.dtype not in (torch.bfloat16, torch.float32):
-        raise TypeError("o must be bfloat16 or float32")
-    _need(o, o.dtype, "o")
+    named = [(q, "q", torch.bfloat16), (k_pages, "k_pages", torch.bfloat16),
+             (v_pages, "v_pages", torch.bfloat16), (block_table, "block_table", torch.int32),
+             (seqlens, "seqlens", torch.int32)]
     if lse is not None:
-        _need(lse, torch.float32, "lse")
+        named.append((lse, "lse", torch.float32))
+    for t, n, dt in named:   # types, then shapes, then placement
+        if not isinstance(t, torch.Tensor) or t.dtype != dt:
+            raise TypeError(f"{n} must be a {dt} tensor")
+    if not isinstance(o, torch.Tensor) or o.dtype not in (torch.bfloat16, torch.float32):
+        raise TypeError("o must be a bfloat16 or float32 tensor")
+    if q.ndim != 4 or k_pages.ndim != 4:
+        raise ValueError("q and the pages must be 4-D")
     B, Hq, one, d = q.shape
     num_blocks, page_size, Hkv, dk = k_pages.shape
     if one != 1 or dk != d or tuple(v_pages.shape) != tuple(k_pages.shape):
         raise ValueError("q / page shapes mismatch")
     if block_table.ndim != 2 or block_table.shape[0] != B or tuple(seqlens.shape) != (B,):
         raise ValueError("block_table must be [B, max_blocks] and seqlens [B]")
+    if tuple(o.shape) != (B, Hq, 1, d):
+        raise ValueError("o shape mismatch")
+    if lse is not None and tuple(lse.shape) != (B, Hq, 1):
+        raise ValueError("lse shape mismatch")
+    for t, n, dt in named + [(o, "o", o.dtype)]:
+        _need(t, dt, n)
     max_blocks = block_table.shape[1]
     if scale is None:
         scale = d ** -0.5

@@ -253,9 +253,29 @@ attn_status_t check_decode_shape(int B, int Hq, int Hkv, int Nmax, int d, int nu
     return ATTN_OK;
 }
 
-// SM count used by the automatic split rule when no device is queried (host
-// exports): the device's own count is used for real launches.
-int decode_sms_or_default(int* sms) {
+}  // namespace
+
+// Pointer, shape and value checks of a contiguous-cache decode call (no device
+// is touched), shared by attn_decode and attn_decode_noalloc.
+attn_status_t gb300::check_decode_call(const void* q, const void* k_cache, const void* v_cache,
+                                       const int* seqlens, const void* o, const float* lse, int B,
+                                       int Hq, int Hkv, int Nmax, int d, float scale,
+                                       int num_splits, attn_out_dtype_t o_dtype) {
+    if (!q || !k_cache || !v_cache || !seqlens || !o) return ATTN_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o) ||
+        !aligned4(seqlens))
+        return ATTN_ERR_INVALID_ARG;
+    if (lse && !aligned4(lse)) return ATTN_ERR_INVALID_ARG;
+    attn_status_t st = check_common(B, Hq, Hkv, d, scale, o_dtype);
+    if (st != ATTN_OK) return st;
+    return check_decode_shape(B, Hq, Hkv, Nmax, d, num_splits);
+}
+
+namespace {
+
+// SM count of the current device, for the size queries (the launches read the
+// same per-device value).  -1 when no device can be queried.
+int current_num_sms(int* sms) {
     DeviceInfo dev;
     if (current_device_info(&dev) == ATTN_OK) {
         *sms = dev.num_sms;
@@ -268,14 +288,28 @@ int decode_sms_or_default(int* sms) {
 
 extern "C" {
 
+size_t attn_fwd_workspace_size(int B, int Hq, int Hkv, int Nq, int Nk, int d, int causal) {
+    if (check_common(B, Hq, Hkv, d, 1.0f, ATTN_OUT_BF16) != ATTN_OK) return 0;
+    if (Nq < 1 || Nk < 1 || Nq > kMaxLen || Nk > kMaxLen) return 0;
+    if ((causal != 0 && causal != 1) || (causal && Nq > Nk)) return 0;
+    if (!fwd_head_dim_supported(d)) return 0;
+    int sms = 0;
+    if (current_num_sms(&sms) != 0) return 0;
+    return fwd_workspace_bytes(B, Hq, Hkv, Nq, Nk, d, causal, sms);
+}
+
 attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                        int Hq, int Hkv, int Nq, int Nk, int d, int causal, float scale,
-                       attn_out_dtype_t o_dtype, void* stream) {
+                       attn_out_dtype_t o_dtype, void* workspace, size_t workspace_bytes,
+                       void* stream) {
     attn_status_t st = check_fwd(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, d, causal, scale, o_dtype);
     if (st != ATTN_OK) return st;
     DeviceInfo dev;
     if ((st = current_device_info(&dev)) != ATTN_OK) return st;
-    return launch_fwd(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, d, causal, scale, o_dtype,
+    const size_t need = fwd_workspace_bytes(B, Hq, Hkv, Nq, Nk, d, causal, dev.num_sms);
+    if (need > 0 && (!workspace || workspace_bytes < need || !aligned16(workspace)))
+        return ATTN_ERR_WORKSPACE;
+    return launch_fwd(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, d, causal, scale, o_dtype, workspace,
                       static_cast<cudaStream_t>(stream), dev);
 }
 
@@ -310,17 +344,22 @@ attn_status_t attn_fp8_quantize(const void* x, void* codes, float* descale, cons
 attn_status_t attn_fwd_fp8(const void* q8, const void* k8, const void* vt8, const float* q_descale,
                            const float* k_descale, const float* v_descale, void* o, float* lse,
                            int B, int Hq, int Hkv, int Nq, int Nk, int d, int causal, float scale,
-                           attn_out_dtype_t o_dtype, void* stream) {
+                           int rotated, attn_out_dtype_t o_dtype, void* stream) {
     if (!q_descale || !k_descale || !v_descale || !aligned4(q_descale) || !aligned4(k_descale) ||
         !aligned4(v_descale))
         return ATTN_ERR_INVALID_ARG;
+    if (rotated != 0 && rotated != 1) return ATTN_ERR_INVALID_ARG;
     attn_status_t st = check_fwd(q8, k8, vt8, o, lse, B, Hq, Hkv, Nq, Nk, d, causal, scale, o_dtype);
     if (st != ATTN_OK) return st;
     if (d != 128) return ATTN_ERR_UNSUPPORTED;
     DeviceInfo dev;
     if ((st = current_device_info(&dev)) != ATTN_OK) return st;
+    // Q and K rotated by the same signed Hadamard matrix H (entries +-1, H H^T
+    // = d I): (Q D H)(K D H)^T = d Q K^T, so the scores carry a factor d that
+    // the scale takes back (exact: d = 128 is a power of two).
+    const float eff = rotated ? scale / (float)d : scale;
     return launch_fwd_fp8(q8, k8, vt8, q_descale, k_descale, v_descale, o, lse, B, Hq, Hkv, Nq, Nk,
-                          causal, scale, o_dtype, static_cast<cudaStream_t>(stream), dev);
+                          causal, eff, o_dtype, static_cast<cudaStream_t>(stream), dev);
 }
 
 attn_status_t attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
@@ -376,7 +415,7 @@ attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* 
 size_t attn_decode_workspace_size(int B, int Hq, int Hkv, int Nmax, int d, int num_splits) {
     if (check_decode_shape(B, Hq, Hkv, Nmax, d, num_splits) != ATTN_OK) return 0;
     int sms = 0;
-    if (decode_sms_or_default(&sms) != 0) return 0;
+    if (current_num_sms(&sms) != 0) return 0;
     const int chunk = decode_chunk(Nmax, B, Hkv, sms, num_splits);
     return decode_workspace_bytes(B, Hq, Nmax, pad_head_dim(d), chunk);
 }
@@ -384,7 +423,7 @@ size_t attn_decode_workspace_size(int B, int Hq, int Hkv, int Nmax, int d, int n
 int attn_decode_kernel_launches(int B, int Hq, int Hkv, int Nmax, int d, int num_splits) {
     if (check_decode_shape(B, Hq, Hkv, Nmax, d, num_splits) != ATTN_OK) return -1;
     int sms = 0;
-    if (decode_sms_or_default(&sms) != 0) return -1;
+    if (current_num_sms(&sms) != 0) return -1;
     const int chunk = decode_chunk(Nmax, B, Hkv, sms, num_splits);
     const int max_splits = (Nmax + chunk - 1) / chunk;
     return decode_merges_in_kernel(B, Hkv, Hq / Hkv, max_splits, pad_head_dim(d)) ? 1 : 2;
@@ -394,14 +433,9 @@ attn_status_t attn_decode(const void* q, const void* k_cache, const void* v_cach
                           const int* seqlens, void* o, float* lse, int B, int Hq, int Hkv,
                           int Nmax, int d, float scale, int num_splits, void* workspace,
                           size_t workspace_bytes, attn_out_dtype_t o_dtype, void* stream) {
-    if (!q || !k_cache || !v_cache || !seqlens || !o) return ATTN_ERR_INVALID_ARG;
-    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o) ||
-        !aligned4(seqlens))
-        return ATTN_ERR_INVALID_ARG;
-    if (lse && !aligned4(lse)) return ATTN_ERR_INVALID_ARG;
-    attn_status_t st = check_common(B, Hq, Hkv, d, scale, o_dtype);
+    attn_status_t st = check_decode_call(q, k_cache, v_cache, seqlens, o, lse, B, Hq, Hkv, Nmax,
+                                         d, scale, num_splits, o_dtype);
     if (st != ATTN_OK) return st;
-    if ((st = check_decode_shape(B, Hq, Hkv, Nmax, d, num_splits)) != ATTN_OK) return st;
     DeviceInfo dev;
     if ((st = current_device_info(&dev)) != ATTN_OK) return st;
     const int chunk = decode_chunk(Nmax, B, Hkv, dev.num_sms, num_splits);

@@ -693,8 +693,13 @@ extern "C" attn_status_t attn_decode_noalloc(const void* q, const void* k_cache,
                                              float* lse, int B, int Hq, int Hkv, int Nmax, int d,
                                              float scale, int num_splits,
                                              attn_out_dtype_t o_dtype, void* stream) {
+    // attn_decode's own argument checks first, so both entry points reject a
+    // bad call with the same status
+    const attn_status_t chk = gb300::check_decode_call(q, k_cache, v_cache, seqlens, o, lse, B, Hq,
+                                                       Hkv, Nmax, d, scale, num_splits, o_dtype);
+    if (chk != ATTN_OK) return chk;
     const size_t need = attn_decode_workspace_size(B, Hq, Hkv, Nmax, d, num_splits);
-    if (need == 0)  // a rejected shape, or no usable device: let attn_decode say which
+    if (need == 0)  // no usable device: let attn_decode report it
         return attn_decode(q, k_cache, v_cache, seqlens, o, lse, B, Hq, Hkv, Nmax, d, scale,
                            num_splits, nullptr, 0, o_dtype, stream);
     if (need > gb300::kNoAllocScratchBytes) return ATTN_ERR_WORKSPACE;

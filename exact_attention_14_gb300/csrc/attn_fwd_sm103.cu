@@ -46,7 +46,6 @@
 #include <atomic>
 #include <cmath>
 #include <cstdint>
-#include <mutex>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -981,53 +980,15 @@ attn_status_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const C
     return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
-// Stream-ordered memory for the partial results of split units: one pool per
-// device owned by the library, kept (release threshold: never) so that the
-// per-launch allocation is served from the pool after the first one.  The
-// allocation and its free are stream-ordered around the kernel, so launches on
-// different streams, and graph captures, each get their own partials.
-attn_status_t partial_pool(int device, cudaMemPool_t* out) {
-    static std::mutex mu;
-    static cudaMemPool_t pools[64] = {};
-    if (device < 0 || device >= 64) return ATTN_ERR_UNSUPPORTED;
-    std::lock_guard<std::mutex> lock(mu);
-    if (!pools[device]) {
-        cudaMemPoolProps props = {};
-        props.allocType = cudaMemAllocationTypePinned;
-        props.handleTypes = cudaMemHandleTypeNone;
-        props.location.type = cudaMemLocationTypeDevice;
-        props.location.id = device;
-        cudaMemPool_t pool;
-        if (cudaMemPoolCreate(&pool, &props) != cudaSuccess) return ATTN_ERR_CUDA;
-        uint64_t keep = ~0ull;
-        if (cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep) != cudaSuccess) {
-            cudaMemPoolDestroy(pool);
-            return ATTN_ERR_CUDA;
-        }
-        pools[device] = pool;
-    }
-    *out = pools[device];
-    return ATTN_OK;
-}
-
 template <int D, bool OUT_F32>
 attn_status_t launch_with_partials(const CUtensorMap& tq, const CUtensorMap& tk,
                                    const CUtensorMap& tv, const CUtensorMap& to, float* lse,
-                                   FwdParams& p, int grid, cudaStream_t stream,
+                                   FwdParams& p, int grid, void* workspace, cudaStream_t stream,
                                    const DeviceInfo& dev) {
-    const size_t bytes = (size_t)p.split.n_split * p.split.parts * 8 *
-                         partial_block_floats<D>() * sizeof(float);
-    p.partial = nullptr;
-    if (bytes == 0) return launch_fwd_t<D, OUT_F32>(tq, tk, tv, to, lse, p, grid, stream, dev);
-    cudaMemPool_t pool;
-    attn_status_t st = partial_pool(dev.device, &pool);
-    if (st != ATTN_OK) return st;
-    void* buf = nullptr;
-    if (cudaMallocFromPoolAsync(&buf, bytes, pool, stream) != cudaSuccess) return ATTN_ERR_CUDA;
-    p.partial = static_cast<float*>(buf);
-    st = launch_fwd_t<D, OUT_F32>(tq, tk, tv, to, lse, p, grid, stream, dev);
-    if (cudaFreeAsync(buf, stream) != cudaSuccess && st == ATTN_OK) st = ATTN_ERR_CUDA;
-    return st;
+    // the split units' partial results live in the caller's workspace
+    // (fwd_workspace_bytes of it, checked by the caller of launch_fwd)
+    p.partial = p.split.n_split > 0 ? static_cast<float*>(workspace) : nullptr;
+    return launch_fwd_t<D, OUT_F32>(tq, tk, tv, to, lse, p, grid, stream, dev);
 }
 
 uint32_t next_queue_slot() {
@@ -1037,9 +998,18 @@ uint32_t next_queue_slot() {
 
 }  // namespace
 
+size_t fwd_workspace_bytes(int B, int Hq, int Hkv, int Nq, int Nk, int d, int causal, int num_sms) {
+    if (d > 128) return 0;  // the d > 128 kernel splits no unit
+    const FwdShape s = make_fwd_shape(B, Hq, Hkv, Nq, Nk, d, causal);
+    const FwdSplit sp = plan_tail_split(s, num_sms);
+    const size_t block = pad_head_dim(d) == 128 ? partial_block_floats<128>() : partial_block_floats<64>();
+    return (size_t)sp.n_split * sp.parts * 8 * block * sizeof(float);
+}
+
 attn_status_t launch_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
                          int B, int Hq, int Hkv, int Nq, int Nk, int d, int causal, float scale,
-                         attn_out_dtype_t o_dtype, cudaStream_t stream, const DeviceInfo& dev) {
+                         attn_out_dtype_t o_dtype, void* workspace, cudaStream_t stream,
+                         const DeviceInfo& dev) {
     if (d > 128)
         return launch_fwd_wide(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, d, causal, scale, o_dtype, stream,
                                dev);
@@ -1068,11 +1038,11 @@ attn_status_t launch_fwd(const void* q, const void* k, const void* v, void* o, f
         return st;
     // head dims below 64 / 128 run on those kernels (TMA zero-fills the rest)
     if (pad_head_dim(d) == 128)
-        return f32 ? launch_with_partials<128, true>(tq, tk, tv, to, lse, p, grid, stream, dev)
-                   : launch_with_partials<128, false>(tq, tk, tv, to, lse, p, grid, stream, dev);
+        return f32 ? launch_with_partials<128, true>(tq, tk, tv, to, lse, p, grid, workspace, stream, dev)
+                   : launch_with_partials<128, false>(tq, tk, tv, to, lse, p, grid, workspace, stream, dev);
     if (pad_head_dim(d) == 64)
-        return f32 ? launch_with_partials<64, true>(tq, tk, tv, to, lse, p, grid, stream, dev)
-                   : launch_with_partials<64, false>(tq, tk, tv, to, lse, p, grid, stream, dev);
+        return f32 ? launch_with_partials<64, true>(tq, tk, tv, to, lse, p, grid, workspace, stream, dev)
+                   : launch_with_partials<64, false>(tq, tk, tv, to, lse, p, grid, workspace, stream, dev);
     return ATTN_ERR_UNSUPPORTED;
 }
 

@@ -69,9 +69,14 @@ attn_status_t launch_fwd_fp8(const void* q8, const void* k8, const void* vt8, co
                              int B, int Hq, int Hkv, int Nq, int Nk, int causal, float scale,
                              attn_out_dtype_t o_dtype, cudaStream_t stream, const DeviceInfo& dev);
 
+// Dense forward.  Bytes of workspace it needs for the partial results of the
+// units its tail split cuts into pieces (0 when nothing is split) on a GPU
+// with num_sms SMs; launch_fwd takes a workspace of at least that size.
+size_t fwd_workspace_bytes(int B, int Hq, int Hkv, int Nq, int Nk, int d, int causal, int num_sms);
 attn_status_t launch_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
                          int B, int Hq, int Hkv, int Nq, int Nk, int d, int causal, float scale,
-                         attn_out_dtype_t o_dtype, cudaStream_t stream, const DeviceInfo& dev);
+                         attn_out_dtype_t o_dtype, void* workspace, cudaStream_t stream,
+                         const DeviceInfo& dev);
 
 // Dense forward for 128 < d <= 256.
 attn_status_t launch_fwd_wide(const void* q, const void* k, const void* v, void* o, float* lse,
@@ -94,6 +99,12 @@ attn_status_t launch_bwd(const void* q, const void* k, const void* v, const void
                          attn_out_dtype_t o_dtype, attn_out_dtype_t grad_dtype, void* workspace,
                          cudaStream_t stream, const DeviceInfo& dev);
 
+// Decode: the argument checks of attn_decode (pointers, alignment, shape,
+// scale, split request, output type); touches no device.
+attn_status_t check_decode_call(const void* q, const void* k_cache, const void* v_cache,
+                                const int* seqlens, const void* o, const float* lse, int B, int Hq,
+                                int Hkv, int Nmax, int d, float scale, int num_splits,
+                                attn_out_dtype_t o_dtype);
 // Decode: chunk size in keys for a request (multiple of 64).
 int decode_chunk(int Nmax, int B, int Hkv, int num_sms, int num_splits);
 size_t decode_workspace_bytes(int B, int Hq, int Nmax, int d, int chunk);

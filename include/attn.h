@@ -28,12 +28,15 @@
  *
  * Conventions shared by every entry point
  *   - Pointers named q/k/v/o/lse/k_cache/v_cache/seqlens/workspace are DEVICE
- *     pointers.  The caller allocates and owns every buffer it passes.  The
+ *     pointers.  The caller allocates and owns every buffer it passes,
+ *     workspaces included; no entry point allocates device memory.  The
  *     library's own device memory is static tables loaded with it (work
- *     queues, merge counters, the error word, attn_decode_noalloc's scratch)
- *     and, for attn_fwd's split tail units only, per-launch partial results
- *     taken from a library-owned stream-ordered pool.  Tensor data must be
- *     16-byte aligned.
+ *     queues, merge counters, the error word, attn_decode_noalloc's scratch).
+ *     Tensor data must be 16-byte aligned.
+ *   - Per-device state (SM count, the error word's address, the scratch
+ *     address) is looked up on the first call on each device and kept for the
+ *     life of the process: resetting a device (cudaDeviceReset) after the
+ *     library has used it is not supported.
  *   - Tensors are row-major and contiguous: [B, H, N, d] (d fastest) unless
  *     an entry point states another layout (packed batches, paged caches,
  *     transposed FP8 codes).
@@ -68,7 +71,7 @@ typedef enum {
     ATTN_ERR_UNSUPPORTED = 2,  /* valid request this build does not implement  */
     ATTN_ERR_CUDA = 3,         /* a CUDA runtime/driver call failed             */
     ATTN_ERR_TIMEOUT = 4,      /* a device-side bounded wait ran out            */
-    ATTN_ERR_WORKSPACE = 5     /* decode workspace missing or too small         */
+    ATTN_ERR_WORKSPACE = 5     /* workspace missing, too small or misaligned    */
 } attn_status_t;
 
 typedef enum {
@@ -100,14 +103,30 @@ typedef enum {
  * list through a device-side queue (one of 256 slots per launch, rotated by
  * the library and left zeroed when the kernel ends), so at most 256 attn_fwd
  * launches may be in flight at the same time.  Tail units may be split along
- * the KV range (attn_fwd_split_plan); their partial results live in memory
- * the library takes from its own stream-ordered pool on `stream` for the
- * launch and returns after it (ATTN_ERR_CUDA if that allocation fails).
- * Returns ATTN_OK once the kernel is enqueued.
+ * the KV range (attn_fwd_split_plan); their partial results go to the
+ * caller's workspace.
+ *   workspace  device memory of at least attn_fwd_workspace_size(...) bytes,
+ *            16-byte aligned, or NULL when that size is 0; contents need no
+ *            initialisation and are garbage afterwards.  Launches that may
+ *            overlap on the GPU (different streams) need separate workspaces.
+ * Returns ATTN_OK once the kernel is enqueued; ATTN_ERR_WORKSPACE for a
+ * missing, short or misaligned workspace (checked after the arguments).
  */
 attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
                        int B, int Hq, int Hkv, int Nq, int Nk, int d, int causal,
-                       float scale, attn_out_dtype_t o_dtype, void* stream);
+                       float scale, attn_out_dtype_t o_dtype, void* workspace,
+                       size_t workspace_bytes, void* stream);
+
+/*
+ * attn_fwd_workspace_size -- bytes of device workspace attn_fwd needs for
+ * this shape on the current device: the partial results of the tail units it
+ * splits (per piece and per 32 query rows, (d' + 3) x 32 fp32 values with
+ * d' = 64 or 128: O / l, m, l, lx), 0 when it splits none (causal launches,
+ * unit counts that fill the SMs' last round, d > 128).  The split depends on
+ * the device's SM count, so query on the device that will run the launch.
+ * Returns 0 for arguments attn_fwd would reject, or when no device answers.
+ */
+size_t attn_fwd_workspace_size(int B, int Hq, int Hkv, int Nq, int Nk, int d, int causal);
 
 /*
  * attn_fwd_varlen -- attn_fwd over a packed batch of B sequences of different
@@ -150,7 +169,7 @@ attn_status_t attn_fwd_varlen(const void* q, const void* k, const void* v, void*
  *            (entries +-1), computed in fp32 by the fast Walsh-Hadamard
  *            transform (stages h = 1, 2, ..., d/2; pairs (i, i+h) become
  *            (a+b, a-b)).  Rotating Q and K with the same signs multiplies
- *            their scores by d (pass scale / d to attn_fwd_fp8).
+ *            their scores by d (pass rotated = 1 to attn_fwd_fp8).
  *   codes    E4M3 codes (device), [B, H, N, d] when transpose = 0, or
  *            [B, H, d, Np] with Np = ceil(N/16)*16 when transpose = 1 (the
  *            layout attn_fwd_fp8 wants for V; the padding keys hold 0);
@@ -172,8 +191,11 @@ attn_status_t attn_fp8_quantize(const void* x, void* codes, float* descale, cons
  *   q8  [B, Hq, Nq, 128] codes, q_descale [B, Hq, ceil(Nq/128)]
  *   k8  [B, Hkv, Nk, 128] codes, k_descale [B, Hkv, ceil(Nk/128)]
  *   vt8 [B, Hkv, 128, Np] transposed codes, v_descale [B, Hkv, ceil(Nk/128)]
- *   o, lse, causal, o_dtype as attn_fwd; scale as attn_fwd (divide by d when
- *   Q and K were rotated).
+ *   o, lse, causal, o_dtype as attn_fwd; scale as attn_fwd: the softmax
+ *   scale of the original (unrotated) problem
+ *   rotated  1 when q8 and k8 were made by attn_fp8_quantize with the same
+ *            signs (rotated Q and K): their scores are then d times the
+ *            original ones and the library applies scale / d; 0 otherwise.
  *
  * Computes softmax(scale * Q^ K^^T) V^ over the dequantized operands (code *
  * block descale) with fp32 accumulation; the probabilities are rounded to
@@ -186,7 +208,7 @@ attn_status_t attn_fp8_quantize(const void* x, void* codes, float* descale, cons
 attn_status_t attn_fwd_fp8(const void* q8, const void* k8, const void* vt8, const float* q_descale,
                            const float* k_descale, const float* v_descale, void* o, float* lse,
                            int B, int Hq, int Hkv, int Nq, int Nk, int d, int causal, float scale,
-                           attn_out_dtype_t o_dtype, void* stream);
+                           int rotated, attn_out_dtype_t o_dtype, void* stream);
 
 /*
  * attn_bwd_workspace_size -- bytes of device workspace attn_bwd needs: two

@@ -1,12 +1,12 @@
 """Runs one kernel of the library on a named workload a few times, for
 profiler captures (ncu) of a single launch configuration.
 
-    python -m exact_attention_14_gb300.profile_case --kernel fwd --workload prefill2x
-    python -m exact_attention_14_gb300.profile_case --kernel decode --workload decode
-    python -m exact_attention_14_gb300.profile_case --kernel bwd --workload prefill --causal 0
-    python -m exact_attention_14_gb300.profile_case --kernel fp8 --workload long
-    python -m exact_attention_14_gb300.profile_case --kernel fp8quant --workload long
-    python -m exact_attention_14_gb300.profile_case --kernel varlen
+    python profile_case.py --kernel fwd --workload prefill2x
+    python profile_case.py --kernel decode --workload decode
+    python profile_case.py --kernel bwd --workload prefill --causal 0
+    python profile_case.py --kernel fp8 --workload long
+    python profile_case.py --kernel fp8quant --workload long
+    python profile_case.py --kernel varlen
 
 Workloads: prefill (B=4 H=16 N=2048 d=128), prefill2x (B=8: inputs larger
 than L2), prefill256 (the prefill shape at d=256), long (B=1 H=32 N=16384), gqa (B=8 Hq=32 Hkv=8 N=4096), decode
@@ -61,7 +61,7 @@ def main():
         for _ in range(args.iters):
             if args.kernel == "fp8":
                 ea.attn_fwd_fp8(q8, k8, vt8, qd, kd, vd, o, lse, causal=causal,
-                                scale=cfg.scale / cfg.d)
+                                scale=cfg.scale, rotated=True)
             else:
                 ea.attn_fp8_quantize(q, q8, qd, signs)
     elif args.kernel == "varlen":

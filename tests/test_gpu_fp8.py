@@ -64,12 +64,14 @@ def _oracle_operands(q, k, v, signs):
     return q8, k8, vt8, qd, kd, vd
 
 
-def _run_fp8(ops, causal, scale, out_dtype=torch.float32):
+def _run_fp8(ops, causal, scale, out_dtype=torch.float32, rotated=False):
+    """The kernel on the oracle's codes; `scale` is the original problem's
+    (the kernel divides it by d when rotated)."""
     q8, k8, vt8, qd, kd, vd = (torch.from_numpy(np.ascontiguousarray(a)).cuda() for a in ops)
     B, Hq, Nq, d = q8.shape
     o = torch.empty((B, Hq, Nq, d), dtype=out_dtype, device="cuda")
     lse = torch.empty((B, Hq, Nq), dtype=torch.float32, device="cuda")
-    ea.attn_fwd_fp8(q8, k8, vt8, qd, kd, vd, o, lse, causal=causal, scale=scale)
+    ea.attn_fwd_fp8(q8, k8, vt8, qd, kd, vd, o, lse, causal=causal, scale=scale, rotated=rotated)
     torch.cuda.synchronize()
     assert ea.attn_last_device_error() == 0
     return o.float().cpu().double().numpy(), lse.cpu().double().numpy()
@@ -94,10 +96,11 @@ def _check(o, lse, ro, rl, bound, what):
 def test_fwd_fp8_parity(B, Hq, Hkv, Nq, Nk, causal, rotate):
     q, k, v = make_fwd_inputs(B, Hq, Hkv, Nq, Nk, 128, seed=910 + Nq + Nk)
     s = hadamard_signs(128, seed=911) if rotate else None
-    scale = 1 / math.sqrt(128) / (128 if rotate else 1)
+    scale = 1 / math.sqrt(128)
+    eff = scale / 128 if rotate else scale   # rotated operands' scores carry a factor d
     ops = _oracle_operands(q, k, v, s)
-    o, lse = _run_fp8(ops, causal, scale)
-    ro, rl, bound = fp8.attention_fp8(*ops[:3], *ops[3:], Nk, causal=causal, scale=scale)
+    o, lse = _run_fp8(ops, causal, scale, rotated=rotate)
+    ro, rl, bound = fp8.attention_fp8(*ops[:3], *ops[3:], Nk, causal=causal, scale=eff)
     _check(o, lse, ro, rl, bound, f"{(B, Hq, Hkv, Nq, Nk, causal, rotate)}")
 
 
@@ -129,9 +132,9 @@ def test_fwd_fp8_long_context_sampled():
     4 outlier channels), rotated; the oracle checks sampled rows."""
     q, k, v = make_config_inputs(LONG)
     s = hadamard_signs(128, seed=LONG.seed)
-    scale = LONG.scale / 128
+    scale = LONG.scale / 128    # over the rotated operands
     ops = _oracle_operands(q, k, v, s)
-    o, lse = _run_fp8(ops, True, scale, out_dtype=torch.bfloat16)
+    o, lse = _run_fp8(ops, True, LONG.scale, out_dtype=torch.bfloat16, rotated=True)
     rng = np.random.default_rng(5)
     rows = np.stack([np.zeros(48, int), rng.integers(0, 32, 48),
                      np.concatenate([rng.integers(0, 16384, 40), np.arange(8) * 2047])], 1)

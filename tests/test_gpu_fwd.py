@@ -5,6 +5,7 @@ max |dLSE| <= 1e-3.  bf16 output is compared with the oracle rounded to bf16
 (round-to-nearest-even) and a bound of 1e-2 plus half a bf16 ulp of the
 reference value.
 """
+import ctypes
 import math
 
 import numpy as np
@@ -98,6 +99,17 @@ def test_large_configs_sampled(cfg, full_heads):
     assert_close(o_s, lse_s, o_ref, lse_ref, cfg.name)
     # properties that hold for every row: finite, LSE >= max possible lower bound
     assert np.isfinite(o).all() and np.isfinite(lse).all()
+
+
+@pytest.mark.parametrize("cfg", [LONG, GQA], ids=["long", "gqa"])
+def test_large_configs_full(cfg):
+    """Full-size launch of the long-context (B1 H32 N16384, outlier channels)
+    and GQA (B8 Hq32 Hkv8 N4096) causal workloads, every row of O and LSE
+    against the fp64 oracle (about a minute of oracle time on 16 cores)."""
+    q, k, v = make_config_inputs(cfg)
+    o, lse = gpu_fwd(q, k, v, True, cfg.scale)
+    o_ref, lse_ref = oracle.attention(q, k, v, causal=True, scale=cfg.scale)
+    assert_close(o, lse, o_ref, lse_ref, f"{cfg.name} (all rows)")
 
 
 # ------------------------------- edge cases ---------------------------------
@@ -204,20 +216,22 @@ def test_repeatable_and_stream_ordered():
 def test_graph_replays_reuse_the_work_queue(causal):
     """A captured launch replays on the same queue slot: each replay must see a
     reset queue and compute every unit.  Non-causal, the shape's 64 units are
-    split in pieces, whose partials come from the library's stream-ordered
-    pool inside the capture."""
+    split in pieces, whose partials go to the caller's workspace."""
     B, H, N, d = 2, 8, 1024, 128
     q, k, v = (t.cuda() for t in make_fwd_inputs(B, H, H, N, N, d, seed=21))
     o = torch.empty(q.shape, dtype=torch.float32, device="cuda")
     lse = torch.empty(q.shape[:3], dtype=torch.float32, device="cuda")
-    ea.attn_fwd(q, k, v, o, lse, causal=causal)  # first call outside capture
+    need = ea.attn_fwd_workspace_size(B, H, H, N, N, d, causal)
+    assert (need > 0) == (not causal)
+    ws = torch.empty(max(need, 16), dtype=torch.uint8, device="cuda")
+    ea.attn_fwd(q, k, v, o, lse, causal=causal, workspace=ws)  # first call outside capture
     torch.cuda.synchronize()
     g = torch.cuda.CUDAGraph()
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(s):
         with torch.cuda.graph(g, stream=s):
-            ea.attn_fwd(q, k, v, o, lse, causal=causal)
+            ea.attn_fwd(q, k, v, o, lse, causal=causal, workspace=ws)
     torch.cuda.current_stream().wait_stream(s)
     for seed in (22, 23, 24):
         q2, k2, v2 = (t.cuda() for t in make_fwd_inputs(B, H, H, N, N, d, seed=seed))
@@ -228,6 +242,39 @@ def test_graph_replays_reuse_the_work_queue(causal):
         torch.cuda.synchronize()
         assert ea.attn_last_device_error() == 0
         assert torch.equal(o, o_ref) and torch.equal(lse, l_ref), f"replay with seed {seed}"
+
+
+def test_workspace_size_and_checks():
+    """The workspace holds the split tail units' partials: (d' + 3) x 32 fp32
+    values per piece and per 32 query rows (d' = 64 or 128).  A missing,
+    short or misaligned workspace is refused with ATTN_ERR_WORKSPACE before
+    anything is enqueued; shapes without a split need none."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    lib = ea.load()
+    for (B, H, N, d) in ((4, 16, 2048, 128), (3, 19, 2048, 64), (2, 8, 1024, 128)):
+        n_full, n_split, parts = ea.attn_fwd_split_plan(B, H, H, N, N, d, False, sms)
+        want = n_split * parts * 8 * ((64 if d <= 64 else 128) + 3) * 32 * 4
+        assert ea.attn_fwd_workspace_size(B, H, H, N, N, d, False) == want
+        assert ea.attn_fwd_workspace_size(B, H, H, N, N, d, True) == 0
+    B, H, N, d = 4, 16, 2048, 128
+    need = ea.attn_fwd_workspace_size(B, H, H, N, N, d, False)
+    assert need > 0
+    q, k, v = (t.cuda() for t in make_fwd_inputs(B, H, H, N, N, d, seed=1))
+    o = torch.empty(q.shape, dtype=torch.float32, device="cuda")
+    ws = torch.empty(need + 16, dtype=torch.uint8, device="cuda")
+    p = lambda t: ctypes.c_void_p(t.data_ptr())
+    call = lambda c, w, nb: lib.attn_fwd(p(q), p(k), p(v), p(o), None, B, H, H, N, N, d, c,
+                                         ctypes.c_float(d ** -0.5), ea.ATTN_OUT_F32, w, nb, None)
+    assert call(0, None, 0) == ea.ATTN_ERR_WORKSPACE
+    assert call(0, p(ws), need - 1) == ea.ATTN_ERR_WORKSPACE
+    assert call(0, ctypes.c_void_p(ws.data_ptr() + 8), need) == ea.ATTN_ERR_WORKSPACE
+    assert call(1, None, 0) == ea.ATTN_OK          # causal: nothing is split
+    assert call(0, p(ws), need) == ea.ATTN_OK
+    torch.cuda.synchronize()
+    assert ea.attn_last_device_error() == 0
+    o_ref, _ = ea.forward(q, k, v, causal=False, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert torch.equal(o, o_ref)
 
 
 @pytest.mark.parametrize("causal", [True, False])

@@ -48,10 +48,11 @@ FAKE = 0x10000  # aligned, never dereferenced: every case fails validation first
 
 def fwd(lib, **kw):
     a = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=None, B=1, Hq=2, Hkv=1, Nq=8, Nk=8, d=64,
-             causal=0, scale=0.125, odt=0)
+             causal=0, scale=0.125, odt=0, ws=None, wsb=0)
     a.update(kw)
     return lib.attn_fwd(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["Hq"], a["Hkv"],
-                        a["Nq"], a["Nk"], a["d"], a["causal"], a["scale"], a["odt"], None)
+                        a["Nq"], a["Nk"], a["d"], a["causal"], a["scale"], a["odt"], a["ws"],
+                        a["wsb"], None)
 
 
 @pytest.mark.parametrize("kw,code", [
@@ -87,6 +88,19 @@ def test_workspace_size_rejects_bad_shapes(lib):
     assert ea.attn_decode_workspace_size(0, 8, 2, 64, 128) == 0
     assert ea.attn_decode_workspace_size(1, 8, 3, 64, 128) == 0
     assert ea.attn_decode_workspace_size(1, 8, 2, 64, 96) == 0
+    for args in [(0, 8, 8, 64, 64, 128, 0), (1, 8, 3, 64, 64, 128, 0), (1, 8, 8, 64, 64, 100, 0),
+                 (1, 8, 8, 64, 32, 128, 1), (1, 8, 8, 64, 64, 128, 2), (1, 8, 8, 0, 64, 128, 0)]:
+        assert ea.attn_fwd_workspace_size(*args) == 0, args
+
+
+def test_fwd_workspace_size_without_a_device(lib):
+    """The size depends on the device's SM count: with no device to ask, the
+    query returns 0 and attn_fwd stops at the device query."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a device answers here (the GPU tests check the size)")
+    assert ea.attn_fwd_workspace_size(4, 16, 16, 2048, 2048, 128, 0) == 0
+    assert fwd(lib, B=4, Hq=16, Hkv=16, Nq=2048, Nk=2048, d=128) == ea.ATTN_ERR_CUDA
 
 
 # ------------------------------ scheduling pins ------------------------------
@@ -302,11 +316,16 @@ def test_supported_head_dims(lib, d, fwd_ok, bwd_ok):
     128-column kernels, above on the 192- or 256-column ones (zero-filled
     columns); the backward (workspace size 0 when unsupported) and decode stop
     at 128."""
+    import torch
     assert (ea.attn_bwd_workspace_size(2, 8, 2, 1000, 1000, d) > 0) == bwd_ok
-    rc = fwd(lib, d=d)
-    assert rc == (ea.ATTN_ERR_CUDA if fwd_ok else ea.ATTN_ERR_UNSUPPORTED) or (fwd_ok and rc == ea.ATTN_OK)
-    bwd_rc = lib.attn_bwd(*([FAKE] * 9), 1, 2, 1, 8, 8, d, 0, 0.125, 0, 0, FAKE, 1 << 30, None)
+    # FAKE is not device memory: a call whose arguments pass every check is
+    # made only where no device can run it (it then stops at the device query)
+    if not fwd_ok:
+        assert fwd(lib, d=d) == ea.ATTN_ERR_UNSUPPORTED
+    elif not torch.cuda.is_available():
+        assert fwd(lib, d=d) == ea.ATTN_ERR_CUDA
     if not bwd_ok:
+        bwd_rc = lib.attn_bwd(*([FAKE] * 9), 1, 2, 1, 8, 8, d, 0, 0.125, 0, 0, FAKE, 1 << 30, None)
         assert bwd_rc == ea.ATTN_ERR_UNSUPPORTED
 
 
@@ -343,13 +362,15 @@ def test_fp8_sizes_and_argument_checks(lib):
     assert q(FAKE, FAKE, FAKE, None, 1, 1, 8, 128, 2, None) == 1
     assert q(FAKE, FAKE, FAKE, None, 1, 1, 8, 64, 0, None) == 2
     f = lib.attn_fwd_fp8
-    args = [FAKE] * 6 + [FAKE, None, 1, 2, 1, 8, 8, 128, 0, 0.1, 0, None]
+    args = [FAKE] * 6 + [FAKE, None, 1, 2, 1, 8, 8, 128, 0, 0.1, 0, 0, None]
     bad_d = list(args); bad_d[13] = 64
     assert f(*bad_d) == 2
     bad_s = list(args); bad_s[3] = None
     assert f(*bad_s) == 1
     bad_c = list(args); bad_c[14] = 1; bad_c[11] = 9
     assert f(*bad_c) == 1
+    bad_r = list(args); bad_r[16] = 2       # rotated is 0 or 1
+    assert f(*bad_r) == 1
 
 
 def test_no_test_function_defined_twice():
@@ -373,3 +394,54 @@ def test_operands_must_share_one_device():
     assert ea._one_device(a, None, b) == a.device
     with pytest.raises(ValueError, match="different devices"):
         ea._one_device(a, torch.empty(2, device="meta"))
+
+
+@pytest.mark.parametrize("fn", ["attn_decode", "attn_decode_noalloc"])
+def test_decode_binding_checks_shapes_before_the_library(fn):
+    """The decode wrappers reject wrong types and shapes (an o, lse, cache or
+    length vector the kernels would index out of bounds) before any pointer
+    reaches the library; host tensors are refused as well."""
+    import torch
+    call = getattr(ea, fn)
+    B, Hq, Hkv, N, d = 2, 8, 2, 64, 128
+    q = torch.zeros(B, Hq, 1, d, dtype=torch.bfloat16)
+    kc = torch.zeros(B, Hkv, N, d, dtype=torch.bfloat16)
+    sl = torch.full((B,), N, dtype=torch.int32)
+    o = torch.zeros(B, Hq, 1, d, dtype=torch.float32)
+    lse = torch.zeros(B, Hq, 1, dtype=torch.float32)
+    bad = [
+        (dict(o=torch.zeros(B, Hq - 1, 1, d)), ValueError),
+        (dict(o=torch.zeros(B, Hq, 1, d, dtype=torch.float64)), TypeError),
+        (dict(o=torch.zeros(B, Hq, 1, d, dtype=torch.float16)), TypeError),
+        (dict(lse=torch.zeros(B, Hq - 2, 1)), ValueError),
+        (dict(lse=torch.zeros(B, Hq, 1, dtype=torch.float64)), TypeError),
+        (dict(v_cache=torch.zeros(B, Hkv, N - 1, d, dtype=torch.bfloat16)), ValueError),
+        (dict(k_cache=torch.zeros(B, Hkv, N, d, dtype=torch.float32)), TypeError),
+        (dict(seqlens=torch.zeros(B + 1, dtype=torch.int32)), ValueError),
+        (dict(seqlens=torch.zeros(B, dtype=torch.int64)), TypeError),
+        (dict(q=torch.zeros(B, Hq, 2, d, dtype=torch.bfloat16)), ValueError),
+        (dict(), ValueError),   # all well formed, but host tensors: "must be a CUDA tensor"
+    ]
+    for kw, exc in bad:
+        a = dict(q=q, k_cache=kc, v_cache=kc.clone(), seqlens=sl, o=o, lse=lse)
+        a.update(kw)
+        with pytest.raises(exc, match="CUDA" if not kw else "tensor|mismatch|4-D"):
+            call(a["q"], a["k_cache"], a["v_cache"], a["seqlens"], a["o"], a["lse"])
+
+
+def test_decode_paged_binding_checks_output_shapes():
+    import torch
+    B, Hq, Hkv, d = 2, 8, 2, 128
+    q = torch.zeros(B, Hq, 1, d, dtype=torch.bfloat16)
+    pages = torch.zeros(4, 64, Hkv, d, dtype=torch.bfloat16)
+    bt = torch.zeros(B, 2, dtype=torch.int32)
+    sl = torch.full((B,), 128, dtype=torch.int32)
+    with pytest.raises(ValueError, match="o shape"):
+        ea.attn_decode_paged(q, pages, pages, bt, sl, torch.zeros(B, Hq, 1, d - 8),
+                             torch.zeros(B, Hq, 1))
+    with pytest.raises(ValueError, match="lse shape"):
+        ea.attn_decode_paged(q, pages, pages, bt, sl, torch.zeros(B, Hq, 1, d),
+                             torch.zeros(B, Hq))
+    with pytest.raises(ValueError, match="CUDA"):
+        ea.attn_decode_paged(q, pages, pages, bt, sl, torch.zeros(B, Hq, 1, d),
+                             torch.zeros(B, Hq, 1))

@@ -181,3 +181,62 @@ def test_rotation_gains_nothing_for_isolated_outliers():
     q, k, _ = make_outlier_inputs(1, 1, 1, 1024, 128, seed=10)
     plain, rotated = _score_error(q, k, None), _score_error(q, k, hadamard_signs(128, seed=11))
     assert 1 / 1.5 < plain / rotated < 1.5, (plain, rotated)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("B,Hq,Hkv,Nq,Nk", [
+    (1, 2, 2, 130, 130),     # a ragged second 128-row block on both sides
+    (2, 4, 1, 200, 333),     # MQA, Nq < Nk: bottom-right causal alignment
+    (1, 6, 3, 257, 300),     # GQA, three Q blocks
+])
+def test_attention_fp8_rows_equals_attention_fp8(B, Hq, Hkv, Nq, Nk, causal):
+    """The per-row variant (which checks the full-size long-context launch)
+    gives, row for row, what attention_fp8 gives over the whole matrices: the
+    same dequantization and block descales (row i uses block i // 128), the
+    same causal cut (keys j <= i + Nk - Nq), the same GQA head, the same
+    bound.  An off-by-one in any of these fails here."""
+    q, k, v = make_fwd_inputs(B, Hq, Hkv, Nq, Nk, 128, seed=77 + Nq)
+    s = hadamard_signs(128, seed=78)
+    q8, qd = fp8.quantize(q, signs=s)
+    k8, kd = fp8.quantize(k, signs=s)
+    vt8, vd = fp8.quantize(v, transpose=True)
+    # distinct descales per block, so a wrong block index shows
+    qd = qd * (1.0 + np.arange(qd.size, dtype=np.float32).reshape(qd.shape) / 16)
+    kd = kd * (1.0 + np.arange(kd.size, dtype=np.float32).reshape(kd.shape) / 32)
+    scale = 0.5 / 128
+    o, lse, bound = fp8.attention_fp8(q8, k8, vt8, qd, kd, vd, Nk, causal=causal, scale=scale)
+    rows = np.array([(b, h, i) for b in range(B) for h in range(Hq) for i in range(Nq)])
+    ro, rl, rb = fp8.attention_fp8_rows(q8, k8, vt8, qd, kd, vd, Nk, rows, causal=causal,
+                                        scale=scale)
+    assert np.abs(ro - o.reshape(-1, 128)).max() <= 1e-12
+    assert np.abs(rl - lse.reshape(-1)).max() <= 1e-12
+    assert np.abs(rb - bound.reshape(-1, 128)).max() <= 1e-12
+
+
+def test_attention_fp8_bound_covers_rounded_probabilities():
+    """The bound attention_fp8 returns covers the error of O when the
+    probabilities are rounded to E4M3 before the P.V product, as the kernel
+    does: P~ = 2^(s*c - m + 4) in the frame of a running max m, rounded,
+    with the row sum of the unrounded P~ as the normaliser.  Emulated here in
+    fp64 with the oracle's E4M3 rounding on rows of mixed sharpness; the
+    bound must hold and must not be loose by orders of magnitude."""
+    rng = np.random.default_rng(11)
+    Nq, Nk, d = 64, 512, 128
+    q8 = fp8.e4m3_encode(rng.standard_normal((1, 1, Nq, d)) * 4)
+    k8 = fp8.e4m3_encode(rng.standard_normal((1, 1, Nk, d)) * 4)
+    v = rng.standard_normal((1, 1, Nk, d))
+    vt8, vd = fp8.quantize(torch.from_numpy(v).to(torch.bfloat16), transpose=True)
+    ones = lambda n: np.ones((1, 1, n), np.float32)  # noqa: E731
+    for scale in (0.002, 0.01, 0.05):
+        o, _, bound = fp8.attention_fp8(q8, k8, vt8, ones(1), ones(4), vd, Nk, causal=False,
+                                        scale=scale)
+        qv = fp8.e4m3_decode(q8)[0, 0]
+        kv = fp8.e4m3_decode(k8)[0, 0]
+        vv = fp8.dequantize(vt8, vd, Nk, transposed=True)[0, 0]
+        s = scale * qv @ kv.T / math.log(2)                   # base-2 scores
+        m = s.max(axis=1, keepdims=True)
+        pt = np.exp2(s - m + 4)                               # frame with the factor 2^4
+        o_emul = (fp8.e4m3_round(pt) @ vv) / pt.sum(axis=1, keepdims=True)
+        err = np.abs(o_emul - o[0, 0])
+        assert (err <= bound[0, 0]).all(), scale
+        assert err.max() > 1e-3 * bound[0, 0].max(), scale   # the case has real error
