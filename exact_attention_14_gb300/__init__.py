@@ -65,7 +65,7 @@ SIGNATURES = {
     "attn_kv_tiles": (_c_int, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_int]),
     "attn_fwd_num_units": (_c_ll, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int]),
     "attn_fwd_schedule": (_c_int, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
-                                   _c_ll, ctypes.POINTER(ctypes.c_int),
+                                   _c_int, _c_ll, ctypes.POINTER(ctypes.c_int),
                                    ctypes.POINTER(ctypes.c_int)]),
     "attn_decode_kernel_launches": (_c_int, [_c_int] * 6),
     "attn_bwd_workspace_size": (ctypes.c_size_t, [_c_int] * 6),
@@ -587,12 +587,14 @@ def attn_fwd_num_units(B, Hq, Hkv, Nq, Nk, d, causal) -> int:
     return int(load().attn_fwd_num_units(B, Hq, Hkv, Nq, Nk, d, int(bool(causal))))
 
 
-def attn_fwd_schedule(B, Hq, Hkv, Nq, Nk, d, causal):
-    """Returns ([(b, hq, m_block), ...] in walk order, [cost, ...])."""
+def attn_fwd_schedule(B, Hq, Hkv, Nq, Nk, d, causal, num_sms: int = 0):
+    """Returns ([(b, hq, m_block), ...] in walk order, [cost, ...]) for a GPU
+    with num_sms SMs (0: the fixed section widths)."""
     n = attn_fwd_num_units(B, Hq, Hkv, Nq, Nk, d, causal)
     units = (ctypes.c_int * (3 * n))()
     costs = (ctypes.c_int * n)()
-    rc = load().attn_fwd_schedule(B, Hq, Hkv, Nq, Nk, d, int(bool(causal)), n, units, costs)
+    rc = load().attn_fwd_schedule(B, Hq, Hkv, Nq, Nk, d, int(bool(causal)), int(num_sms), n,
+                                  units, costs)
     if rc != 0:
         raise ValueError("attn_fwd_schedule rejected its arguments")
     return [tuple(units[3 * i:3 * i + 3]) for i in range(n)], list(costs)

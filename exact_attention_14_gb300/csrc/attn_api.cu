@@ -553,11 +553,12 @@ long long attn_fwd_num_units(int B, int Hq, int Hkv, int Nq, int Nk, int d, int 
     return make_fwd_shape(B, Hq, Hkv, Nq, Nk, d, causal).units;
 }
 
-int attn_fwd_schedule(int B, int Hq, int Hkv, int Nq, int Nk, int d, int causal, long long n,
-                      int* units_out, int* cost_out) {
-    if (B < 1 || Hq < 1 || Hkv < 1 || Nq < 1 || Nk < 1 || d < 1 || Hq % Hkv || !units_out)
+int attn_fwd_schedule(int B, int Hq, int Hkv, int Nq, int Nk, int d, int causal, int num_sms,
+                      long long n, int* units_out, int* cost_out) {
+    if (B < 1 || Hq < 1 || Hkv < 1 || Nq < 1 || Nk < 1 || d < 1 || Hq % Hkv || !units_out ||
+        num_sms < 0)
         return -1;
-    const FwdShape s = make_fwd_shape(B, Hq, Hkv, Nq, Nk, d, causal);
+    const FwdShape s = make_fwd_shape(B, Hq, Hkv, Nq, Nk, d, causal, num_sms);
     if (n != s.units || s.units >= (1ll << 31)) return -1;
     for (long long i = 0; i < n; ++i) {
         int bh, mb;

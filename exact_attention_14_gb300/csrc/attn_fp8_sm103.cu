@@ -845,7 +845,7 @@ attn_status_t launch_fwd_fp8(const void* q8, const void* k8, const void* vt8, co
                              int B, int Hq, int Hkv, int Nq, int Nk, int causal, float scale,
                              attn_out_dtype_t o_dtype, cudaStream_t stream, const DeviceInfo& dev) {
     Fp8Params p;
-    p.shape = make_fwd_shape(B, Hq, Hkv, Nq, Nk, kD, causal);
+    p.shape = make_fwd_shape(B, Hq, Hkv, Nq, Nk, kD, causal, dev.num_sms);
     if (p.shape.units >= (1ll << 31)) return ATTN_ERR_UNSUPPORTED;
     p.group = Hq / Hkv;
     p.off = Nk - Nq;

@@ -1014,7 +1014,7 @@ attn_status_t launch_fwd(const void* q, const void* k, const void* v, void* o, f
         return launch_fwd_wide(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, d, causal, scale, o_dtype, stream,
                                dev);
     FwdParams p;
-    p.shape = make_fwd_shape(B, Hq, Hkv, Nq, Nk, d, causal);
+    p.shape = make_fwd_shape(B, Hq, Hkv, Nq, Nk, d, causal, dev.num_sms);
     if (p.shape.units >= (1ll << 31)) return ATTN_ERR_UNSUPPORTED;
     p.group = Hq / Hkv;
     p.off = Nk - Nq;

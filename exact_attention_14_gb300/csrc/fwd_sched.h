@@ -16,7 +16,13 @@
 // when it is ready for one (a device-side queue).
 #pragma once
 
+#include <algorithm>
 #include <cstdint>
+#include <functional>
+#include <map>
+#include <mutex>
+#include <tuple>
+#include <vector>
 
 #if defined(__CUDACC__)
 #define GB300_HD __host__ __device__ __forceinline__
@@ -30,12 +36,22 @@ constexpr int kTileM = 128;           // query rows per Q tile (tcgen05 M)
 constexpr int kTileN = 128;           // keys per K/V tile
 constexpr int kTilesPerUnit = 2;      // Q tiles per unit
 constexpr int kUnitRows = kTileM * kTilesPerUnit;
-// K/V bytes a section may span.  Causal sections stay wide so the longest-first
-// order can balance long and short m-blocks across the SMs; non-causal units
-// all cost the same, so a narrow section keeps the ~150 units in flight on few
-// heads and their K/V resident in the near L2 partition.
+// K/V bytes a section may span.  Non-causal units all cost the same, so a
+// narrow section keeps the ~150 units in flight on few heads and their K/V
+// resident in the near L2 partition.  Causal units differ in cost, and how
+// well the longest-first order inside each section balances them depends on
+// the section's width: a causal launch takes the narrowest of the candidate
+// widths whose modelled makespan (causal_section_heads below) is within 1 %
+// of the best; kL2SectionBytesCausal is the width used when no SM count is
+// given.
 constexpr long long kL2SectionBytesCausal = 64ll << 20;
 constexpr long long kL2SectionBytesDense = 16ll << 20;
+constexpr long long kCausalSectionCandidates[] = {8ll << 20, 16ll << 20, 32ll << 20, 64ll << 20,
+                                                  128ll << 20};
+// Fixed cost of a unit in the model, in KV steps (the epilogue and the next
+// unit's first softmax, while the tensor cores idle; about 2.6 us against
+// 1.4 us per step, measured).
+constexpr double kUnitOverheadSteps = 2.0;
 
 struct FwdShape {
     int B, Hq, Hkv, Nq, Nk, d, causal;
@@ -72,21 +88,93 @@ GB300_HD int tile_kv_count(int mb, int t, const FwdShape& s) {
     return tile_kv_count_len(mb, t, s.Nq, s.Nk, s.causal);
 }
 
-inline FwdShape make_fwd_shape(int B, int Hq, int Hkv, int Nq, int Nk, int d, int causal) {
-    FwdShape s;
-    s.B = B; s.Hq = Hq; s.Hkv = Hkv; s.Nq = Nq; s.Nk = Nk; s.d = d; s.causal = causal;
-    s.nmb = (Nq + kUnitRows - 1) / kUnitRows;
+// Query heads per section for a K/V byte budget (a multiple of the GQA group).
+inline int section_heads_for(int B, int Hq, int Hkv, int Nk, int d, long long budget) {
     const int group = Hq / Hkv;
     const long long kv_head_bytes = 2ll * Nk * d * 2;  // K and V, bf16
-    const long long budget = causal ? kL2SectionBytesCausal : kL2SectionBytesDense;
     long long kv_per_sec = budget / (kv_head_bytes > 0 ? kv_head_bytes : 1);
     if (kv_per_sec < 1) kv_per_sec = 1;
     long long hps = kv_per_sec * group;
     const long long all = (long long)B * Hq;
     if (hps > all) hps = all;
-    s.heads_per_section = (int)hps;
-    s.units = all * s.nmb;  // the launcher rejects units >= 2^31
+    return (int)hps;
+}
+
+inline FwdShape make_fwd_shape_sections(int B, int Hq, int Hkv, int Nq, int Nk, int d, int causal,
+                                        int heads_per_section) {
+    FwdShape s;
+    s.B = B; s.Hq = Hq; s.Hkv = Hkv; s.Nq = Nq; s.Nk = Nk; s.d = d; s.causal = causal;
+    s.nmb = (Nq + kUnitRows - 1) / kUnitRows;
+    s.heads_per_section = heads_per_section;
+    s.units = (long long)B * Hq * s.nmb;  // the launcher rejects units >= 2^31
     return s;
+}
+
+GB300_HD void unit_of(const FwdShape& s, uint32_t i, int& bh, int& mb);
+
+// Makespan, in KV steps, of the greedy list schedule of the units (lecture
+// notes 4.5: each of num_sms workers takes the next unit of the list when it
+// is free), a unit costing its KV steps (the longer of its two Q tiles) plus
+// kUnitOverheadSteps.
+inline double list_makespan(const FwdShape& s, int num_sms) {
+    std::vector<double> load((size_t)num_sms, 0.0);  // a min-heap of worker loads
+    for (long long i = 0; i < s.units; ++i) {
+        int bh, mb;
+        unit_of(s, (uint32_t)i, bh, mb);
+        const int n0 = tile_kv_count(mb, 0, s), n1 = tile_kv_count(mb, 1, s);
+        std::pop_heap(load.begin(), load.end(), std::greater<double>());
+        load.back() += (n0 > n1 ? n0 : n1) + kUnitOverheadSteps;
+        std::push_heap(load.begin(), load.end(), std::greater<double>());
+    }
+    return *std::max_element(load.begin(), load.end());
+}
+
+// Heads per section of a causal launch on num_sms SMs: of the candidate K/V
+// budgets, the narrowest whose modelled makespan is within 1 % of the best
+// (narrower sections keep more of the K/V they stream in L2).  Cached per
+// shape; shapes of more than 2^22 units keep the default width (the model's
+// cost grows with the unit count).
+inline int causal_section_heads(int B, int Hq, int Hkv, int Nq, int Nk, int d, int num_sms) {
+    const long long units = (long long)B * Hq * ((Nq + kUnitRows - 1) / kUnitRows);
+    const int fallback = section_heads_for(B, Hq, Hkv, Nk, d, kL2SectionBytesCausal);
+    if (num_sms < 1 || units > (1ll << 22)) return fallback;
+    using Key = std::tuple<int, int, int, int, int, int, int>;
+    static std::mutex mu;
+    static std::map<Key, int> cache;
+    const Key key{B, Hq, Hkv, Nq, Nk, d, num_sms};
+    {
+        std::lock_guard<std::mutex> lk(mu);
+        auto it = cache.find(key);
+        if (it != cache.end()) return it->second;
+    }
+    int heads[sizeof(kCausalSectionCandidates) / sizeof(kCausalSectionCandidates[0])];
+    double span[sizeof(heads) / sizeof(heads[0])];
+    double best = 0.0;
+    int n = 0;
+    for (long long budget : kCausalSectionCandidates) {
+        const int h = section_heads_for(B, Hq, Hkv, Nk, d, budget);
+        if (n > 0 && h == heads[n - 1]) continue;  // same list as the narrower budget
+        heads[n] = h;
+        span[n] = list_makespan(make_fwd_shape_sections(B, Hq, Hkv, Nq, Nk, d, 1, h), num_sms);
+        best = (n == 0 || span[n] < best) ? span[n] : best;
+        ++n;
+    }
+    int choice = heads[n - 1];
+    for (int i = 0; i < n; ++i)
+        if (span[i] <= best * 1.01) { choice = heads[i]; break; }
+    std::lock_guard<std::mutex> lk(mu);
+    if (cache.size() > 256) cache.clear();
+    cache[key] = choice;
+    return choice;
+}
+
+// The launch shape.  num_sms > 0 lets causal launches choose their section
+// width by the makespan model; 0 keeps the fixed budgets.
+inline FwdShape make_fwd_shape(int B, int Hq, int Hkv, int Nq, int Nk, int d, int causal,
+                               int num_sms = 0) {
+    const int hps = causal ? causal_section_heads(B, Hq, Hkv, Nq, Nk, d, num_sms)
+                           : section_heads_for(B, Hq, Hkv, Nk, d, kL2SectionBytesDense);
+    return make_fwd_shape_sections(B, Hq, Hkv, Nq, Nk, d, causal, hps);
 }
 
 // Unit index i (0 <= i < units < 2^31) -> (bh = b * Hq + hq, mb).  32-bit

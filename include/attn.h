@@ -398,18 +398,21 @@ int attn_kv_tiles(int row0, int rows, int Nq, int Nk, int causal, int block);
 long long attn_fwd_num_units(int B, int Hq, int Hkv, int Nq, int Nk, int d, int causal);
 
 /*
- * The order in which attn_fwd's persistent kernel takes its units: fills
- * units_out[3*i + {0,1,2}] = (b, hq, m_block) for i < n (n must equal
- * attn_fwd_num_units) and, if cost_out is non-NULL, cost_out[i] = the number
- * of (Q tile, KV tile) pairs unit i computes.  Heads are grouped into
- * sections whose K/V fit a fixed L2 budget, sections run in order, and within
- * a section the m-blocks run longest-first (lecture notes 4.5; "Flash
- * Attention 3/4 notes" FA4 section 3).  Sections span 64 MiB of K/V for
- * causal launches and 16 MiB otherwise.  Each CTA takes the next unit of this
- * list when it is ready for one (greedy list scheduling, as
+ * The order in which attn_fwd's persistent kernel takes its units on a GPU
+ * with num_sms SMs: fills units_out[3*i + {0,1,2}] = (b, hq, m_block) for
+ * i < n (n must equal attn_fwd_num_units) and, if cost_out is non-NULL,
+ * cost_out[i] = the number of (Q tile, KV tile) pairs unit i computes.  Heads
+ * are grouped into sections of K/V, sections run in order, and within a
+ * section the m-blocks run longest-first (lecture notes 4.5; "Flash Attention
+ * 3/4 notes" FA4 section 3).  Non-causal sections span 16 MiB of K/V.  A
+ * causal launch takes, of the widths 8, 16, 32, 64 and 128 MiB, the narrowest
+ * whose makespan under greedy list scheduling on num_sms workers (each unit
+ * costing its KV steps plus 2 for its fixed cost) is within 1 % of the best;
+ * num_sms = 0 gives the fixed width of 64 MiB.  Each CTA takes the next unit
+ * of this list when it is ready for one (greedy list scheduling, as
  * attn_list_schedule models it).  Returns 0, or -1 on a bad argument.
  */
-int attn_fwd_schedule(int B, int Hq, int Hkv, int Nq, int Nk, int d, int causal,
+int attn_fwd_schedule(int B, int Hq, int Hkv, int Nq, int Nk, int d, int causal, int num_sms,
                       long long n, int* units_out, int* cost_out);
 
 /*

@@ -158,8 +158,9 @@ def test_kv_tiles_edge_cases(lib):
     (4, 16, 16, 2048, 128, True), (4, 16, 16, 2048, 128, False), (1, 32, 32, 16384, 128, True),
     (8, 32, 8, 4096, 128, True), (1, 3, 1, 300, 64, True), (2, 4, 2, 129, 64, False),
 ])
-def test_forward_schedule_covers_every_unit_once(lib, B, Hq, Hkv, N, d, causal):
-    order, costs = ea.attn_fwd_schedule(B, Hq, Hkv, N, N, d, causal)
+@pytest.mark.parametrize("sms", [0, 152])
+def test_forward_schedule_covers_every_unit_once(lib, B, Hq, Hkv, N, d, causal, sms):
+    order, costs = ea.attn_fwd_schedule(B, Hq, Hkv, N, N, d, causal, num_sms=sms)
     nmb = -(-N // 256)
     assert len(order) == B * Hq * nmb == ea.attn_fwd_num_units(B, Hq, Hkv, N, N, d, causal)
     assert sorted(order) == sorted((b, h, m) for b in range(B) for h in range(Hq)
@@ -240,6 +241,52 @@ def test_tail_split_never_lengthens_the_modelled_makespan(lib, B, H, N):
     assert split <= whole
     if (B, H, N) == (4, 16, 2048):
         assert (whole, split) == (4 * 32, 3 * 32 + 16)
+
+
+def _section_order(B, Hq, Hkv, N, hps, causal):
+    """The unit list for sections of hps query heads: sections in order; in a
+    section, m-block ranks longest-first (causal), heads in index order."""
+    nmb = -(-N // 256)
+    order = []
+    for h0 in range(0, B * Hq, hps):
+        heads = range(h0, min(h0 + hps, B * Hq))
+        for rank in range(nmb):
+            mb = nmb - 1 - rank if causal else rank
+            order += [(bh // Hq, bh % Hq, mb) for bh in heads]
+    return order
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,N", [(4, 16, 16, 2048), (1, 32, 32, 16384), (8, 32, 8, 4096),
+                                        (3, 19, 19, 2048), (1, 16, 16, 8192), (8, 8, 8, 1024)])
+def test_causal_section_width_minimises_the_modelled_makespan(lib, B, Hq, Hkv, N):
+    """With the SM count given, a causal launch takes the narrowest candidate
+    section width (8..128 MiB of K/V) whose greedy-list makespan, each unit
+    costing the KV steps of its longer Q tile plus 2, is within 1 % of the
+    best candidate's (lecture notes 4.5).  The lists are rebuilt here."""
+    d, sms = 128, 152
+    kv_head = 2 * N * d * 2
+    nt = -(-N // 128)
+
+    def steps(order):
+        return [max(min(2 * m + 1, nt), min(2 * m + 2, nt)) + 2 for _, _, m in order]
+
+    cands = []
+    for mib in (8, 16, 32, 64, 128):
+        hps = min(max(1, (mib << 20) // kv_head) * (Hq // Hkv), B * Hq)
+        if cands and cands[-1][0] == hps:
+            continue
+        order = _section_order(B, Hq, Hkv, N, hps, True)
+        cands.append((hps, order, ea.attn_list_schedule(steps(order), sms, lpt=False)[0]))
+    best = min(c[2] for c in cands)
+    want = next(c for c in cands if c[2] <= best * 1.01)
+    got, _ = ea.attn_fwd_schedule(B, Hq, Hkv, N, N, d, True, num_sms=sms)
+    assert got == want[1], [(c[0], c[2]) for c in cands]
+    if (B, Hq, N) == (4, 16, 2048):
+        assert want[0] == 16          # prefill: 16 MiB sections (64 MiB models no better)
+    # without an SM count the fixed 64 MiB width stays
+    fixed, _ = ea.attn_fwd_schedule(B, Hq, Hkv, N, N, d, True)
+    hps64 = min(max(1, (64 << 20) // kv_head) * (Hq // Hkv), B * Hq)
+    assert fixed == _section_order(B, Hq, Hkv, N, hps64, True)
 
 
 def test_gqa_siblings_are_adjacent(lib):
