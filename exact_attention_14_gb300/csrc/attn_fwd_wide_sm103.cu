@@ -591,9 +591,8 @@ attn_status_t launch_fwd_wide(const void* q, const void* k, const void* v, void*
                               int B, int Hq, int Hkv, int Nq, int Nk, int d, int causal, float scale,
                               attn_out_dtype_t o_dtype, cudaStream_t stream, const DeviceInfo& dev) {
     WideParams p;
-    p.shape = make_fwd_shape(B, Hq, Hkv, Nq, Nk, d, causal);
-    p.shape.nmb = (Nq + kWM - 1) / kWM;  // units are single 128-row Q tiles
-    p.shape.units = (long long)B * Hq * p.shape.nmb;
+    // units are single 128-row Q tiles
+    p.shape = make_fwd_shape(B, Hq, Hkv, Nq, Nk, d, causal, dev.num_sms, kWM);
     if (p.shape.units >= (1ll << 31)) return ATTN_ERR_UNSUPPORTED;
     p.group = Hq / Hkv;
     p.off = Nk - Nq;

@@ -100,11 +100,13 @@ inline int section_heads_for(int B, int Hq, int Hkv, int Nk, int d, long long bu
     return (int)hps;
 }
 
+// A unit covers unit_rows query rows: kUnitRows (two 128-row Q tiles, the
+// d <= 128 kernels) or 128 (one Q tile, the d > 128 kernel).
 inline FwdShape make_fwd_shape_sections(int B, int Hq, int Hkv, int Nq, int Nk, int d, int causal,
-                                        int heads_per_section) {
+                                        int heads_per_section, int unit_rows = kUnitRows) {
     FwdShape s;
     s.B = B; s.Hq = Hq; s.Hkv = Hkv; s.Nq = Nq; s.Nk = Nk; s.d = d; s.causal = causal;
-    s.nmb = (Nq + kUnitRows - 1) / kUnitRows;
+    s.nmb = (Nq + unit_rows - 1) / unit_rows;
     s.heads_per_section = heads_per_section;
     s.units = (long long)B * Hq * s.nmb;  // the launcher rejects units >= 2^31
     return s;
@@ -114,16 +116,25 @@ GB300_HD void unit_of(const FwdShape& s, uint32_t i, int& bh, int& mb);
 
 // Makespan, in KV steps, of the greedy list schedule of the units (lecture
 // notes 4.5: each of num_sms workers takes the next unit of the list when it
-// is free), a unit costing its KV steps (the longer of its two Q tiles) plus
-// kUnitOverheadSteps.
-inline double list_makespan(const FwdShape& s, int num_sms) {
+// is free), a unit costing its KV steps plus kUnitOverheadSteps: for
+// two-tile units the steps of the longer Q tile (128-key steps), for
+// single-tile units (unit_rows 128) the 64-key steps of the d > 128 kernel.
+inline double list_makespan(const FwdShape& s, int num_sms, int unit_rows) {
     std::vector<double> load((size_t)num_sms, 0.0);  // a min-heap of worker loads
     for (long long i = 0; i < s.units; ++i) {
         int bh, mb;
         unit_of(s, (uint32_t)i, bh, mb);
-        const int n0 = tile_kv_count(mb, 0, s), n1 = tile_kv_count(mb, 1, s);
+        int steps;
+        if (unit_rows == kUnitRows) {
+            const int n0 = tile_kv_count(mb, 0, s), n1 = tile_kv_count(mb, 1, s);
+            steps = n0 > n1 ? n0 : n1;
+        } else {
+            const int r0 = mb * kTileM;
+            const int rows = s.Nq - r0 < kTileM ? s.Nq - r0 : kTileM;
+            steps = kv_tiles_for_rows(r0, rows, s.Nq, s.Nk, s.causal, 64);
+        }
         std::pop_heap(load.begin(), load.end(), std::greater<double>());
-        load.back() += (n0 > n1 ? n0 : n1) + kUnitOverheadSteps;
+        load.back() += steps + kUnitOverheadSteps;
         std::push_heap(load.begin(), load.end(), std::greater<double>());
     }
     return *std::max_element(load.begin(), load.end());
@@ -134,14 +145,15 @@ inline double list_makespan(const FwdShape& s, int num_sms) {
 // (narrower sections keep more of the K/V they stream in L2).  Cached per
 // shape; shapes of more than 2^22 units keep the default width (the model's
 // cost grows with the unit count).
-inline int causal_section_heads(int B, int Hq, int Hkv, int Nq, int Nk, int d, int num_sms) {
-    const long long units = (long long)B * Hq * ((Nq + kUnitRows - 1) / kUnitRows);
+inline int causal_section_heads(int B, int Hq, int Hkv, int Nq, int Nk, int d, int num_sms,
+                                int unit_rows = kUnitRows) {
+    const long long units = (long long)B * Hq * ((Nq + unit_rows - 1) / unit_rows);
     const int fallback = section_heads_for(B, Hq, Hkv, Nk, d, kL2SectionBytesCausal);
     if (num_sms < 1 || units > (1ll << 22)) return fallback;
-    using Key = std::tuple<int, int, int, int, int, int, int>;
+    using Key = std::tuple<int, int, int, int, int, int, int, int>;
     static std::mutex mu;
     static std::map<Key, int> cache;
-    const Key key{B, Hq, Hkv, Nq, Nk, d, num_sms};
+    const Key key{B, Hq, Hkv, Nq, Nk, d, num_sms, unit_rows};
     {
         std::lock_guard<std::mutex> lk(mu);
         auto it = cache.find(key);
@@ -155,7 +167,8 @@ inline int causal_section_heads(int B, int Hq, int Hkv, int Nq, int Nk, int d, i
         const int h = section_heads_for(B, Hq, Hkv, Nk, d, budget);
         if (n > 0 && h == heads[n - 1]) continue;  // same list as the narrower budget
         heads[n] = h;
-        span[n] = list_makespan(make_fwd_shape_sections(B, Hq, Hkv, Nq, Nk, d, 1, h), num_sms);
+        span[n] = list_makespan(make_fwd_shape_sections(B, Hq, Hkv, Nq, Nk, d, 1, h, unit_rows),
+                                num_sms, unit_rows);
         best = (n == 0 || span[n] < best) ? span[n] : best;
         ++n;
     }
@@ -171,10 +184,10 @@ inline int causal_section_heads(int B, int Hq, int Hkv, int Nq, int Nk, int d, i
 // The launch shape.  num_sms > 0 lets causal launches choose their section
 // width by the makespan model; 0 keeps the fixed budgets.
 inline FwdShape make_fwd_shape(int B, int Hq, int Hkv, int Nq, int Nk, int d, int causal,
-                               int num_sms = 0) {
-    const int hps = causal ? causal_section_heads(B, Hq, Hkv, Nq, Nk, d, num_sms)
+                               int num_sms = 0, int unit_rows = kUnitRows) {
+    const int hps = causal ? causal_section_heads(B, Hq, Hkv, Nq, Nk, d, num_sms, unit_rows)
                            : section_heads_for(B, Hq, Hkv, Nk, d, kL2SectionBytesDense);
-    return make_fwd_shape_sections(B, Hq, Hkv, Nq, Nk, d, causal, hps);
+    return make_fwd_shape_sections(B, Hq, Hkv, Nq, Nk, d, causal, hps, unit_rows);
 }
 
 // Unit index i (0 <= i < units < 2^31) -> (bh = b * Hq + hq, mb).  32-bit
