@@ -369,6 +369,7 @@ def run_ours(args, rank, world, local_rank):
         extra["fp8"] = run_fp8(ea, args, dev, stream, flush, peaks)
     if not args.no_wide:
         extra["wide"] = run_wide(ea, args, dev, stream, flush, peaks)
+        extra["decode_d256"] = run_decode_wide(ea, args, dev, stream, flush, peaks)
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -657,6 +658,39 @@ def run_fp8(ea, args, dev, stream, flush, peaks):
             "quantize_gbs": qbytes / tq_ / 1e9, "quantize": sq,
             "quantize_frac_of_hbm": qbytes / tq_ / 1e9 / peaks["hbm_gbs"],
             "with_quantize_tflops": f8 / (ta_ + tq_) / 1e12}
+
+
+def run_decode_wide(ea, args, dev, stream, flush, peaks):
+    """Split-KV decode at d = 256 (the 256-column kernel): B=16 Hq=32 Hkv=8,
+    KV cache [16, 8, 16384, 256] bf16 (the d = 128 workload's cache bytes),
+    lengths uniform in [512, 16384].  Timing only (parity is in the tests), so
+    the cache is drawn on the GPU from a seeded generator."""
+    B, Hq, Hkv, Nmax, d = 16, 32, 8, 16384, 256
+    g = torch.Generator(device=dev).manual_seed(7)
+    q = torch.randn(B, Hq, 1, d, device=dev, generator=g).to(torch.bfloat16)
+    kc = torch.randn(B, Hkv, Nmax, d, device=dev, generator=g).to(torch.bfloat16)
+    vc = torch.randn(B, Hkv, Nmax, d, device=dev, generator=g).to(torch.bfloat16)
+    sl = torch.randint(512, Nmax + 1, (B,), generator=torch.Generator().manual_seed(7),
+                       dtype=torch.int64).to(torch.int32).to(dev)
+    o = torch.empty(B, Hq, 1, d, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(B, Hq, 1, dtype=torch.float32, device=dev)
+    ws = torch.empty(ea.attn_decode_workspace_size(B, Hq, Hkv, Nmax, d, 0), dtype=torch.uint8,
+                     device=dev)
+    fn = lambda: ea.attn_decode(q, kc, vc, sl, o, lse, workspace=ws, stream=stream)  # noqa
+    for _ in range(args.warmup):
+        flush.zero_()
+        fn()
+    st = stats_ms(time_legs(stream, [fn], max(args.stat_iters, args.steps), flush)[0])
+    if ea.attn_last_device_error() != 0:
+        raise RuntimeError("device error in the d=256 decode leg")
+    sum_len = int(sl.sum().item())
+    nbytes = 2.0 * sum_len * Hkv * d * 2 + q.numel() * 2 + o.numel() * 2 + lse.numel() * 4
+    t = st["median_ms"] * 1e-3
+    del kc, vc
+    return {"kernel": "attn_decode_split_kernel<256> (split-KV, in-kernel merge)",
+            "workload": f"decode B={B} Hq={Hq} Hkv={Hkv} Nmax={Nmax} d={d}, lengths U[512,{Nmax}]",
+            "gbs": nbytes / t / 1e9, "frac_of_hbm": nbytes / t / 1e9 / peaks["hbm_gbs"],
+            "algorithmic_bytes": nbytes, "sum_seqlen": sum_len, **st}
 
 
 def run_wide(ea, args, dev, stream, flush, peaks):

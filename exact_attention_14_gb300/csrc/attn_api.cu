@@ -248,7 +248,7 @@ attn_status_t check_decode_shape(int B, int Hq, int Hkv, int Nmax, int d, int nu
     if ((long long)B * Hq > kMaxHeads || (long long)B * Hkv > kMaxHeads) return ATTN_ERR_INVALID_ARG;
     if (Nmax < 1 || Nmax > kMaxLen) return ATTN_ERR_INVALID_ARG;
     if (num_splits < 0) return ATTN_ERR_INVALID_ARG;
-    if (!head_dim_supported(d)) return ATTN_ERR_UNSUPPORTED;
+    if (!decode_head_dim_supported(d)) return ATTN_ERR_UNSUPPORTED;
     if (Hq / Hkv > 16) return ATTN_ERR_UNSUPPORTED;
     return ATTN_OK;
 }
@@ -417,7 +417,7 @@ size_t attn_decode_workspace_size(int B, int Hq, int Hkv, int Nmax, int d, int n
     int sms = 0;
     if (current_num_sms(&sms) != 0) return 0;
     const int chunk = decode_chunk(Nmax, B, Hkv, sms, num_splits);
-    return decode_workspace_bytes(B, Hq, Nmax, pad_head_dim(d), chunk);
+    return decode_workspace_bytes(B, Hq, Nmax, decode_pad_head_dim(d), chunk);
 }
 
 int attn_decode_kernel_launches(int B, int Hq, int Hkv, int Nmax, int d, int num_splits) {
@@ -426,7 +426,7 @@ int attn_decode_kernel_launches(int B, int Hq, int Hkv, int Nmax, int d, int num
     if (current_num_sms(&sms) != 0) return -1;
     const int chunk = decode_chunk(Nmax, B, Hkv, sms, num_splits);
     const int max_splits = (Nmax + chunk - 1) / chunk;
-    return decode_merges_in_kernel(B, Hkv, Hq / Hkv, max_splits, pad_head_dim(d)) ? 1 : 2;
+    return decode_merges_in_kernel(B, Hkv, Hq / Hkv, max_splits, decode_pad_head_dim(d)) ? 1 : 2;
 }
 
 attn_status_t attn_decode(const void* q, const void* k_cache, const void* v_cache,
@@ -439,7 +439,7 @@ attn_status_t attn_decode(const void* q, const void* k_cache, const void* v_cach
     DeviceInfo dev;
     if ((st = current_device_info(&dev)) != ATTN_OK) return st;
     const int chunk = decode_chunk(Nmax, B, Hkv, dev.num_sms, num_splits);
-    const size_t need = decode_workspace_bytes(B, Hq, Nmax, pad_head_dim(d), chunk);
+    const size_t need = decode_workspace_bytes(B, Hq, Nmax, decode_pad_head_dim(d), chunk);
     if (!workspace || workspace_bytes < need || !aligned16(workspace)) return ATTN_ERR_WORKSPACE;
     return launch_decode(q, k_cache, v_cache, seqlens, o, lse, B, Hq, Hkv, Nmax, d, scale, chunk,
                          workspace, o_dtype, static_cast<cudaStream_t>(stream), dev);
@@ -466,7 +466,7 @@ attn_status_t attn_decode_paged(const void* q, const void* k_pages, const void* 
     DeviceInfo dev;
     if ((st = current_device_info(&dev)) != ATTN_OK) return st;
     const int chunk = decode_chunk(Nmax, B, Hkv, dev.num_sms, num_splits);
-    const size_t need = decode_workspace_bytes(B, Hq, Nmax, pad_head_dim(d), chunk);
+    const size_t need = decode_workspace_bytes(B, Hq, Nmax, decode_pad_head_dim(d), chunk);
     if (!workspace || workspace_bytes < need || !aligned16(workspace)) return ATTN_ERR_WORKSPACE;
     return launch_decode_paged(q, k_pages, v_pages, block_table, seqlens, o, lse, B, Hq, Hkv,
                                num_blocks, page_size, max_blocks, d, scale, chunk, workspace,

@@ -547,7 +547,8 @@ attn_status_t launch_decode_t(const CUtensorMap& tk, const CUtensorMap& tv, cons
 
 bool decode_merges_in_kernel(int B, int Hkv, int G, int max_splits, int d) {
     // counter table, and the split weights in the drained stage ring
-    const size_t ring_floats = (size_t)(d == 128 ? DecCfg<128>::kBarOff : DecCfg<64>::kBarOff) / 4;
+    const size_t ring_floats =
+        (size_t)(d == 256 ? DecCfg<256>::kBarOff : d == 128 ? DecCfg<128>::kBarOff : DecCfg<64>::kBarOff) / 4;
     return (long long)B * Hkv <= kDecMaxGroups &&
            (size_t)(2 * kMaxGroup) + (size_t)G * (size_t)max_splits <= ring_floats;
 }
@@ -579,11 +580,14 @@ attn_status_t launch_decode_common(const CUtensorMap& tk, const CUtensorMap& tv,
                                    const int* seqlens, void* o, float* lse, DecParams& p, int d,
                                    void* workspace, attn_out_dtype_t o_dtype, cudaStream_t stream,
                                    const DeviceInfo& dev) {
-    d = pad_head_dim(d);  // the kernel's tile width (columns past p.dh are zeros)
+    d = decode_pad_head_dim(d);  // the kernel's tile width (columns past p.dh are zeros)
     const size_t rows = (size_t)p.B * p.Hq * p.max_splits;
     float* ws_o = static_cast<float*>(workspace);
     float* ws_lse = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + align16(rows * d * 4));
     const bool f32 = o_dtype == ATTN_OUT_F32;
+    if (d == 256)
+        return f32 ? launch_decode_t<256, true>(tk, tv, q, seqlens, o, lse, ws_o, ws_lse, p, stream, dev)
+                   : launch_decode_t<256, false>(tk, tv, q, seqlens, o, lse, ws_o, ws_lse, p, stream, dev);
     if (d == 128)
         return f32 ? launch_decode_t<128, true>(tk, tv, q, seqlens, o, lse, ws_o, ws_lse, p, stream, dev)
                    : launch_decode_t<128, false>(tk, tv, q, seqlens, o, lse, ws_o, ws_lse, p, stream, dev);
@@ -604,7 +608,7 @@ DecParams make_dec_params(int B, int Hq, int Hkv, int Nmax, int d, float scale, 
     p.max_splits = (Nmax + chunk - 1) / chunk;
     p.c = scale * kLog2ef;
     static std::atomic<uint32_t> launches{0};
-    p.slot = decode_merges_in_kernel(B, Hkv, p.G, p.max_splits, pad_head_dim(d))
+    p.slot = decode_merges_in_kernel(B, Hkv, p.G, p.max_splits, decode_pad_head_dim(d))
                  ? (int)(launches.fetch_add(1u, std::memory_order_relaxed) % kDecSlots)
                  : -1;
     p.block_table = nullptr;

@@ -142,9 +142,12 @@ inline double list_makespan(const FwdShape& s, int num_sms, int unit_rows) {
 
 // Heads per section of a causal launch on num_sms SMs: of the candidate K/V
 // budgets, the narrowest whose modelled makespan is within 1 % of the best
-// (narrower sections keep more of the K/V they stream in L2).  Cached per
-// shape; shapes of more than 2^22 units keep the default width (the model's
-// cost grows with the unit count).
+// (narrower sections keep more of the K/V they stream in L2).  For the
+// single-tile units of the d > 128 kernel the candidates start at 32 MiB:
+// measured there (prefill shape at d = 256, causal) 16 MiB sections took
+// 141.6 us against 135.8 us at 32 MiB and 137.2 us at 64 MiB, although the
+// model ties them.  Cached per shape; shapes of more than 2^22 units keep the
+// default width (the model's cost grows with the unit count).
 inline int causal_section_heads(int B, int Hq, int Hkv, int Nq, int Nk, int d, int num_sms,
                                 int unit_rows = kUnitRows) {
     const long long units = (long long)B * Hq * ((Nq + unit_rows - 1) / unit_rows);
@@ -164,6 +167,7 @@ inline int causal_section_heads(int B, int Hq, int Hkv, int Nq, int Nk, int d, i
     double best = 0.0;
     int n = 0;
     for (long long budget : kCausalSectionCandidates) {
+        if (unit_rows != kUnitRows && budget < (32ll << 20)) continue;
         const int h = section_heads_for(B, Hq, Hkv, Nk, d, budget);
         if (n > 0 && h == heads[n - 1]) continue;  // same list as the narrower budget
         heads[n] = h;

@@ -16,6 +16,10 @@ inline bool head_dim_supported(int d) { return d >= 8 && d <= 128 && d % 8 == 0;
 // The dense forward also takes 128 < d <= 256 (multiples of 8) on the kernels
 // built for 192 and 256 columns (one Q tile per CTA; attn_fwd_wide_sm103.cu).
 inline bool fwd_head_dim_supported(int d) { return d >= 8 && d <= 256 && d % 8 == 0; }
+// Decode takes the same range: d <= 128 on the 64- or 128-column kernel,
+// 128 < d <= 256 on the 256-column one.
+inline int decode_pad_head_dim(int d) { return d <= 64 ? 64 : (d <= 128 ? 128 : 256); }
+inline bool decode_head_dim_supported(int d) { return fwd_head_dim_supported(d); }
 
 struct DeviceInfo {
     int device;

@@ -316,7 +316,9 @@ int attn_decode_kernel_launches(int B, int Hq, int Hkv, int Nmax, int d, int num
  *            bytes, 16-byte aligned; contents need no initialisation and are
  *            garbage afterwards.  Concurrent calls must not share it.
  *
- * Supported: 8 <= d <= 128 with d % 8 == 0; Hq % Hkv == 0; Hq / Hkv <= 16;
+ * Supported: 8 <= d <= 256 with d % 8 == 0 (d <= 128 on the 64- or
+ * 128-column kernel, 128 < d <= 256 on the 256-column one; the columns past d
+ * are read as zero and never written); Hq % Hkv == 0; Hq / Hkv <= 16;
  * 1 <= Nmax <= 2^24.
  */
 attn_status_t attn_decode(const void* q, const void* k_cache, const void* v_cache,

@@ -83,6 +83,19 @@ def test_decode_shapes(B, Hq, Hkv, Nmax, d, lo, hi):
     assert_close(o, lse, o_ref, lse_ref, f"{(B, Hq, Hkv, Nmax, d)}")
 
 
+@pytest.mark.parametrize("d", [192, 256])
+def test_decode_wide_head_dims_gqa_and_many_splits(d):
+    """The 256-column kernel on a GQA group of 8 heads with lengths up to 8192,
+    with the in-kernel merge (automatic splits) and with the combine kernel
+    (more groups than its counter table), against the oracle."""
+    q, kc, vc, sl = make_decode_inputs(4, 32, 4, 8192, d, seed=90 + d, len_lo=1, len_hi=8192,
+                                       tail="nan")
+    o_ref, lse_ref = oracle.decode(q, kc, vc, sl)
+    for ns in (0, 1, 16):
+        o, lse = gpu_decode(q, kc, vc, sl, num_splits=ns)
+        assert_close(o, lse, o_ref, lse_ref, f"d={d} splits={ns}")
+
+
 def test_decode_bf16_output():
     q, kc, vc, sl = make_decode_inputs(2, 8, 2, 1500, 128, seed=5, len_lo=700, len_hi=1500)
     o_ref, _ = oracle.decode(q, kc, vc, sl)
@@ -154,13 +167,15 @@ def test_split_merge_is_repeatable():
         assert torch.equal(o, outs[0][0]) and torch.equal(lse, outs[0][1])
 
 
-@pytest.mark.parametrize("d", [32, 80, 96])
+@pytest.mark.parametrize("d", [32, 80, 96, 136, 192, 256])
 def test_decode_head_dims_padded(d):
+    """Head dims up to 256: d <= 128 on the 64- or 128-column kernel, above on
+    the 256-column one (the columns past d read as zeros and are not written)."""
     q, kc, vc, sl = make_decode_inputs(3, 8, 2, 2000, d, seed=70 + d, len_lo=1, len_hi=2000)
     for ns in (0, 5):
         o, lse = gpu_decode(q, kc, vc, sl, num_splits=ns)
         o_ref, lse_ref = oracle.decode(q, kc, vc, sl)
         assert_close(o, lse, o_ref, lse_ref, f"d={d} splits={ns}")
-    pad = 64 if d <= 64 else 128
+    pad = 64 if d <= 64 else (128 if d <= 128 else 256)
     assert ea.attn_decode_workspace_size(3, 8, 2, 2000, d, 5) == \
         ea.attn_decode_workspace_size(3, 8, 2, 2000, pad, 5)

@@ -34,7 +34,7 @@ def _to_pages(cache, page_size, seed, extra_pages=3):
 
 
 @pytest.mark.parametrize("page_size,d,num_splits", [(64, 128, 0), (256, 128, 0), (64, 64, 3),
-                                                    (128, 128, 7)])
+                                                    (128, 128, 7), (64, 256, 0), (128, 192, 5)])
 def test_paged_equals_contiguous_bit_for_bit(page_size, d, num_splits):
     q, kc, vc, sl = make_decode_inputs(4, 16, 4, 2048, d, seed=51, len_lo=1, len_hi=2048)
     kp, table = _to_pages(kc, page_size, seed=52)
@@ -66,8 +66,9 @@ def test_paged_matches_oracle_and_ignores_nan():
     assert np.abs(lse - lse_ref).max() <= MAX_ABS_LSE
 
 
-def test_paged_head_dim_96():
-    q, kc, vc, sl = make_decode_inputs(2, 8, 2, 1024, 96, seed=55, len_lo=1, len_hi=1024)
+@pytest.mark.parametrize("d", [96, 256])
+def test_paged_head_dims(d):
+    q, kc, vc, sl = make_decode_inputs(2, 8, 2, 1024, d, seed=55, len_lo=1, len_hi=1024)
     kp, table = _to_pages(kc, 128, seed=56)
     vp, _ = _to_pages(vc, 128, seed=56)
     o1, l1 = ea.decode(q.cuda(), kc.cuda(), vc.cuda(), sl.cuda(), out_dtype=torch.float32)

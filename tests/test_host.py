@@ -78,7 +78,7 @@ def dec(lib, **kw):
 @pytest.mark.parametrize("kw,code", [
     (dict(q=None), 1), (dict(sl=None), 1), (dict(sl=FAKE + 2), 1), (dict(v=FAKE + 4), 1),
     (dict(Hq=9), 1), (dict(Nmax=0), 1), (dict(ns=-1), 1), (dict(scale=-0.5), 1),
-    (dict(d=84), 2), (dict(d=192), 2), (dict(Hq=34, Hkv=2), 2),
+    (dict(d=84), 2), (dict(d=264), 2), (dict(d=4), 2), (dict(Hq=34, Hkv=2), 2),
 ])
 def test_decode_argument_checks(lib, kw, code):
     assert dec(lib, **kw) == code
@@ -349,7 +349,7 @@ def test_decode_paged_argument_checks(lib):
     bad[10] = 0                                                        # no blocks
     assert lib.attn_decode_paged(*bad) == ea.ATTN_ERR_INVALID_ARG
     bad = list(args)
-    bad[13] = 192                                                      # d above 128
+    bad[13] = 264                                                      # d above 256
     assert lib.attn_decode_paged(*bad) == ea.ATTN_ERR_UNSUPPORTED
 
 
@@ -365,6 +365,11 @@ def test_supported_head_dims(lib, d, fwd_ok, bwd_ok):
     at 128."""
     import torch
     assert (ea.attn_bwd_workspace_size(2, 8, 2, 1000, 1000, d) > 0) == bwd_ok
+    # decode takes the forward's head dims (its size query needs a device)
+    if not torch.cuda.is_available():
+        rc = lib.attn_decode(FAKE, FAKE, FAKE, FAKE, FAKE, None, 2, 8, 2, 64, d, 0.1, 0, FAKE,
+                             1 << 20, 1, None)
+        assert rc == (ea.ATTN_ERR_CUDA if fwd_ok else ea.ATTN_ERR_UNSUPPORTED)
     # FAKE is not device memory: a call whose arguments pass every check is
     # made only where no device can run it (it then stops at the device query)
     if not fwd_ok:
