@@ -388,7 +388,7 @@ attn_status_t attn_fwd_varlen(const void* q, const void* k, const void* v, void*
 size_t attn_bwd_workspace_size(int B, int Hq, int Hkv, int Nq, int Nk, int d) {
     if (check_common(B, Hq, Hkv, d, 1.0f, ATTN_OUT_BF16) != ATTN_OK) return 0;
     if (Nq < 1 || Nk < 1 || Nq > kMaxLen || Nk > kMaxLen) return 0;
-    if (!head_dim_supported(d)) return 0;
+    if (!fwd_head_dim_supported(d)) return 0;
     return bwd_workspace_bytes(B, Hq, Nq, d);
 }
 
@@ -399,7 +399,7 @@ attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* 
                        size_t workspace_bytes, void* stream) {
     attn_status_t st = check_fwd(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, d, causal, scale, o_dtype);
     if (st != ATTN_OK) return st;
-    if (!head_dim_supported(d)) return ATTN_ERR_UNSUPPORTED;  // the backward stops at d = 128
+    // (check_fwd has limited d to the forward's head dims, which the backward takes too)
     if (!dout || !lse || !dq || !dk || !dv) return ATTN_ERR_INVALID_ARG;
     if (!aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
         return ATTN_ERR_INVALID_ARG;

@@ -991,6 +991,608 @@ attn_status_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const C
     return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
+// ---------------------------------------------------------------------------
+// Head dims 128 < d <= 256 (kernels built for 256 columns; columns past d are
+// zeros in every tile and are not written).
+//
+// At d = 256 the dK/dV pass's accumulators alone (dV and dK, 256 columns
+// each) fill TMEM, and a 128-row Q or dO tile is 64 KiB, so these kernels use
+// other tile shapes, each product a shape the d > 128 forward also runs:
+//  dkdv  one CTA per (b, KV head g, 128-key tile, column half h of d).  K and
+//        V of the tile stay in shared memory (64 KiB each); Q, dO, lse2 and D
+//        stream in 64-row tiles through one stage.  Per Q tile:
+//          S^T = K Q^T, dP^T = V dO^T           (M=128, N=64, K=256)
+//          P^T, dS^T as in the d <= 128 pass    (64 query columns per key row)
+//          dV_h += P^T dO_h, dK_h += dS^T Q_h   (M=128, N=128, K=64: columns
+//                                                 [128h, 128h + 128) of d)
+//        S^T and dP^T are computed by both CTAs of a key tile (the two
+//        halves), so the pass does 3 of its 4 products' work twice.
+//        TMEM: S^T [0,64) (P^T over [0,32)), dP^T [64,128) (dS^T over
+//        [64,96)), dV_h [128,256), dK_h [256,384).
+//  dq    one CTA per (b, query head, 128-row Q tile).  Q and dO stay in
+//        shared memory; K and V stream in 64-key tiles through one stage.
+//        Per K/V tile: S = Q K^T, dP = dO V^T (M=128, N=64, K=256), dS as in
+//        the d <= 128 pass, dQ += dS K (M=128, N=256, K=64).
+//        TMEM: S [0,64) (dS over [0,32)), dP [64,128), dQ [128,384).
+// Both passes run their steps in order (one stage: the next tile's loads wait
+// for the products that read the current one).
+// ---------------------------------------------------------------------------
+constexpr int kWD = 256;    // tile columns
+constexpr int kWQ = 64;     // query rows per dkdv Q tile, keys per dq K/V tile
+constexpr uint32_t kWBwdDescHi = sdesc_hi_sw128(1024);
+
+struct WideBwdCfg {
+    static constexpr int kBig = kBT * kWD * 2;     // 128 rows x 256: 4 chunks of 16 KiB
+    static constexpr int kSmall = kWQ * kWD * 2;   // 64 rows x 256: 4 chunks of 8 KiB
+    // dkdv: K, V | Q, dO | lse2[64], D[64];  dq: Q, dO | K, V
+    static constexpr int kA0 = 0;
+    static constexpr int kA1 = kBig;
+    static constexpr int kB0 = 2 * kBig;
+    static constexpr int kB1 = 2 * kBig + kSmall;
+    static constexpr int kLD = 2 * kBig + 2 * kSmall;
+    static constexpr int kBar = kLD + 1024;
+    static constexpr int kLayout = kBar + 256;
+    static constexpr int kSmemBytes = kLayout + 1024;
+    static_assert(kSmemBytes <= kMaxSmemPerBlock, "shared memory budget");
+};
+
+struct __align__(8) WideBwdBars {
+    uint64_t res_full;            // the resident tiles (dkdv: K, V; dq: Q, dO)
+    uint64_t ld_full, ld_empty;   // the streamed stage
+    uint64_t s_full, dp_full, p_full, ds_full, acc_full, drain;
+    uint32_t tmem_base;
+    int abort;
+};
+static_assert(sizeof(WideBwdBars) <= 256, "barrier block");
+
+// S = A B^T with M = 128, N = 64, K = 256: A 128 rows K-major (chunks of 64
+// columns 16 KiB apart), B 64 rows K-major (chunks 8 KiB apart).
+__device__ __forceinline__ void wbwd_issue_s(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo,
+                                             uint32_t idesc) {
+#pragma unroll
+    for (int kk = 0; kk < kWD / 16; ++kk) {
+        const uint32_t in = (kk & 3) * (32 >> 4);
+        mma_ss_warp(d_tmem, sdesc_join(a_lo + (kk >> 2) * ((kBT * 128) >> 4) + in, kWBwdDescHi),
+                    sdesc_join(b_lo + (kk >> 2) * ((kWQ * 128) >> 4) + in, kWBwdDescHi), idesc,
+                    kk > 0 ? 1u : 0u);
+    }
+}
+
+// D += A B with A from TMEM (bf16 pairs, 8 columns per 16 rows of K, K = 64)
+// and B a 64-row tile MN-major (LBO 8 KiB between 64-column chunks, 16 rows =
+// 2 KiB per K step); N per idesc.
+__device__ __forceinline__ void wbwd_issue_ta(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo,
+                                              uint32_t idesc, bool accumulate) {
+#pragma unroll
+    for (int kk = 0; kk < kWQ / 16; ++kk)
+        mma_ts_warp(d_tmem, a_tmem + kk * 8, sdesc_join(b_lo + kk * (2048 >> 4), kWBwdDescHi), idesc,
+                    (accumulate || kk > 0) ? 1u : 0u);
+}
+
+struct WideDkdvWork {
+    int b, g, kt, k0, half, qt_first, n_qt_cta, n_tiles;
+};
+
+// CTA index -> (column half, then the dkdv pass's section order of key tiles).
+__device__ __forceinline__ WideDkdvWork wide_dkdv_work(const BwdParams& p) {
+    WideDkdvWork w;
+    const unsigned idx = blockIdx.x >> 1;
+    w.half = (int)(blockIdx.x & 1u);
+    const unsigned all = (unsigned)(p.B * p.Hkv);
+    const unsigned S = (unsigned)p.sec_groups;
+    const unsigned per_sec = S * (unsigned)p.n_kt;
+    const unsigned sec = idx / per_sec;
+    const unsigned r = idx - sec * per_sec;
+    const unsigned rest = all - sec * S;
+    const unsigned gs = rest < S ? rest : S;
+    w.kt = (int)(r / gs);
+    const int bg = (int)(sec * S + (r - (unsigned)w.kt * gs));
+    w.b = bg / p.Hkv;
+    w.g = bg - w.b * p.Hkv;
+    w.k0 = w.kt * kBT;
+    const int n_qt = (p.Nq + kWQ - 1) / kWQ;
+    int first = 0;
+    if (p.causal) {
+        const int lo = w.k0 - p.off;  // the first query that sees key k0
+        first = lo <= 0 ? 0 : lo / kWQ;
+    }
+    w.qt_first = first;
+    w.n_qt_cta = n_qt - first > 0 ? n_qt - first : 0;
+    w.n_tiles = w.n_qt_cta * p.group;
+    return w;
+}
+
+__device__ __forceinline__ void wbwd_abort(WideBwdBars* bars, unsigned int* err) {
+    atomicOr(err, kErrTimeout);
+    *((volatile int*)&bars->abort) = 1;
+}
+
+template <bool OUT_F32>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+attn_bwd_wide_dkdv_kernel(const __grid_constant__ CUtensorMap tq64, const __grid_constant__ CUtensorMap tdo64,
+                          const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
+                          const BwdParams p, unsigned int* err) {
+    using C = WideBwdCfg;
+    extern __shared__ uint8_t smem_raw[];
+    const uintptr_t raw = reinterpret_cast<uintptr_t>(smem_raw);
+    uint8_t* smem = reinterpret_cast<uint8_t*>((raw + 1023) & ~uintptr_t(1023));
+    if ((uintptr_t)(smem - smem_raw) + C::kLayout > (uintptr_t)C::kSmemBytes) {
+        if (threadIdx.x == 0) atomicOr(err, kErrLayout);
+        return;
+    }
+    WideBwdBars* bars = reinterpret_cast<WideBwdBars*>(smem + C::kBar);
+    const volatile int* abort_flag = &bars->abort;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const WideDkdvWork w = wide_dkdv_work(p);
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bars->res_full), 1);
+        mbar_init(smem_u32(&bars->ld_full), 1);
+        mbar_init(smem_u32(&bars->ld_empty), 1 + 4);  // the dK commit + 4 P/dS warps
+        mbar_init(smem_u32(&bars->s_full), 1);
+        mbar_init(smem_u32(&bars->dp_full), 1);
+        mbar_init(smem_u32(&bars->p_full), 4);
+        mbar_init(smem_u32(&bars->ds_full), 4);
+        mbar_init(smem_u32(&bars->acc_full), 1);
+        mbar_init(smem_u32(&bars->drain), 1);
+        bars->abort = 0;
+        fence_barrier_init();
+        tma_prefetch_desc(&tq64);
+        tma_prefetch_desc(&tdo64);
+        tma_prefetch_desc(&tk);
+        tma_prefetch_desc(&tv);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(&bars->tmem_base), 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = bars->tmem_base;
+
+    if (warp == 0) {
+        // ---- producer: K, V once; then Q, dO, lse2, D per 64-row tile
+        const bool leader = elect_one();
+        const int kvh = w.b * p.Hkv + w.g;
+        if (leader) {
+            const uint32_t bar = smem_u32(&bars->res_full);
+            mbar_arrive_expect_tx(bar, 2 * C::kBig);
+#pragma unroll
+            for (int c = 0; c < kWD / 64; ++c) {
+                tma_load_3d(smem_u32(smem + C::kA0) + c * 16384, &tk, bar, 64 * c, w.k0, kvh);
+                tma_load_3d(smem_u32(smem + C::kA1) + c * 16384, &tv, bar, 64 * c, w.k0, kvh);
+            }
+        }
+        __syncwarp();
+        bool ok = true;
+        int issued = 0;
+        for (int i = 0; i < w.n_tiles && ok; ++i) {
+            if (i > 0)
+                ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&bars->ld_empty), (i - 1) & 1, abort_flag));
+            if (!ok) break;
+            const int hq = w.g * p.group + i / w.n_qt_cta;
+            const int q0 = (w.qt_first + i % w.n_qt_cta) * kWQ;
+            const int bh = w.b * p.Hq + hq;
+            if (leader) {
+                const uint32_t bar = smem_u32(&bars->ld_full);
+                mbar_arrive_expect_tx(bar, 2 * C::kSmall + 2 * kWQ * 4);
+#pragma unroll
+                for (int c = 0; c < kWD / 64; ++c) {
+                    tma_load_3d(smem_u32(smem + C::kB0) + c * 8192, &tq64, bar, 64 * c, q0, bh);
+                    tma_load_3d(smem_u32(smem + C::kB1) + c * 8192, &tdo64, bar, 64 * c, q0, bh);
+                }
+                const size_t row = (size_t)bh * p.Nq_pad + q0;
+                bulk_load(smem_u32(smem + C::kLD), p.lse2 + row, kWQ * 4, bar);
+                bulk_load(smem_u32(smem + C::kLD + kWQ * 4), p.dvec + row, kWQ * 4, bar);
+            }
+            __syncwarp();
+            ++issued;
+        }
+        if (!ok && leader) wbwd_abort(bars, err);
+        mbar_wait(smem_u32(&bars->res_full), 0, nullptr);
+        if (issued > 0) mbar_wait(smem_u32(&bars->ld_full), (issued - 1) & 1, nullptr);
+        __syncwarp();
+    } else if (warp == 1) {
+        // ---- MMA issuer: per tile S^T, dP^T, then dV_h (after P^T), dK_h (after dS^T)
+        const bool leader = elect_one();
+        const uint32_t idS = make_idesc_bf16(128, kWQ, 0, 0);
+        const uint32_t idH = make_idesc_bf16(128, 128, 0, 1);
+        const uint32_t tS = tmem, tdP = tmem + 64, tdV = tmem + 128, tdK = tmem + 256;
+        const uint32_t k_lo = sdesc_lo(smem_u32(smem + C::kA0), 16);
+        const uint32_t v_lo = sdesc_lo(smem_u32(smem + C::kA1), 16);
+        const uint32_t q_lo = sdesc_lo(smem_u32(smem + C::kB0), 16);
+        const uint32_t do_lo = sdesc_lo(smem_u32(smem + C::kB1), 16);
+        // this CTA's column half of Q and dO as MN-major B operands
+        const uint32_t q_mn = sdesc_lo(smem_u32(smem + C::kB0) + w.half * 2 * 8192, 8192);
+        const uint32_t do_mn = sdesc_lo(smem_u32(smem + C::kB1) + w.half * 2 * 8192, 8192);
+        auto wait_all = [&](uint32_t bar, uint32_t parity) {
+            return __all_sync(0xFFFFFFFFu, mbar_wait(bar, parity, abort_flag, 32));
+        };
+        bool ok = true;
+        if (w.n_tiles > 0) ok = wait_all(smem_u32(&bars->res_full), 0);
+        for (int i = 0; i < w.n_tiles && ok; ++i) {
+            ok = wait_all(smem_u32(&bars->ld_full), i & 1);
+            if (!ok) break;
+            tc_fence_after();
+            wbwd_issue_s(tS, k_lo, q_lo, idS);                     // S^T = K Q^T
+            mma_commit_warp(smem_u32(&bars->s_full));
+            wbwd_issue_s(tdP, v_lo, do_lo, idS);                   // dP^T = V dO^T
+            mma_commit_warp(smem_u32(&bars->dp_full));
+            ok = wait_all(smem_u32(&bars->p_full), i & 1);
+            if (!ok) break;
+            tc_fence_after();
+            wbwd_issue_ta(tdV, tS, do_mn, idH, i > 0);             // dV_h += P^T dO_h
+            ok = wait_all(smem_u32(&bars->ds_full), i & 1);
+            if (!ok) break;
+            tc_fence_after();
+            wbwd_issue_ta(tdK, tdP, q_mn, idH, i > 0);             // dK_h += dS^T Q_h
+            mma_commit_warp(smem_u32(&bars->ld_empty));            // the stage is read
+        }
+        if (ok && w.n_tiles > 0) mma_commit_warp(smem_u32(&bars->acc_full));
+        if (!ok && leader) wbwd_abort(bars, err);
+        mma_commit_warp(smem_u32(&bars->drain));
+        mbar_wait(smem_u32(&bars->drain), 0, nullptr);
+        __syncwarp();
+    } else if (warp >= 4) {
+        // ---- P^T / dS^T (one key row per thread), then the dK_h / dV_h epilogue
+        const int wq = warp & 3;
+        const uint32_t lane_off = uint32_t(wq * 32) << 16;
+        const uint32_t tS = tmem + lane_off, tdP = tmem + 64 + lane_off;
+        const int jg = w.k0 + wq * 32 + lane;
+        const uint32_t lse2s = smem_u32(smem + C::kLD);
+        const uint32_t ds_vec = lse2s + kWQ * 4;
+        bool ok = true;
+        for (int i = 0; i < w.n_tiles && ok; ++i) {
+            ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&bars->s_full), i & 1, abort_flag, 32));
+            if (!ok) break;
+            tc_fence_after();
+            const int q0 = (w.qt_first + i % w.n_qt_cta) * kWQ;
+            const int lim = jg - p.off - q0;  // causal: column x allowed iff x >= lim
+            const bool masked = p.causal && (q0 + p.off < w.k0 + kBT - 1);
+            float pf0[32], pf1[32];
+            {
+                uint32_t sv[32], pp[16];
+                tmem_ld32(tS, sv);
+                tmem_wait_ld();
+                if (masked) p_chunk<true>(sv, lse2s, 0, p.c, lim, pf0, pp);
+                else p_chunk<false>(sv, lse2s, 0, p.c, lim, pf0, pp);
+                tmem_st16(tS, pp);
+                tmem_ld32(tS + 32, sv);
+                tmem_wait_ld();
+                if (masked) p_chunk<true>(sv, lse2s, 32, p.c, lim, pf1, pp);
+                else p_chunk<false>(sv, lse2s, 32, p.c, lim, pf1, pp);
+                tmem_st16(tS + 16, pp);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&bars->p_full));
+            ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&bars->dp_full), i & 1, abort_flag, 32));
+            if (!ok) break;
+            tc_fence_after();
+            {
+                uint32_t dp[32], dd[16];
+                tmem_ld32(tdP, dp);
+                tmem_wait_ld();
+                ds_chunk_t(pf0, dp, ds_vec, 0, dd);
+                tmem_st16(tdP, dd);
+                tmem_ld32(tdP + 32, dp);
+                tmem_wait_ld();
+                ds_chunk_t(pf1, dp, ds_vec, 32, dd);
+                tmem_st16(tdP + 16, dd);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(smem_u32(&bars->ds_full));
+                mbar_arrive(smem_u32(&bars->ld_empty));  // lse2 and D of the tile are read
+            }
+        }
+        if (!ok) {
+            wbwd_abort(bars, err);
+        } else {
+            // dK_h = scale dS^T Q_h, dV_h = P^T dO_h: columns [128h, 128h + 128)
+            const size_t wrow0 = ((size_t)w.b * p.Hkv + w.g) * p.Nk + (size_t)(w.k0 + wq * 32);
+            const int rows_live = p.Nk - (w.k0 + wq * 32);
+            const int c0 = w.half * 128;
+            bool have = w.n_tiles > 0;
+            if (have) {
+                ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&bars->acc_full), 0, abort_flag));
+                if (!ok) wbwd_abort(bars, err);
+                else tc_fence_after();
+            }
+            if (ok) {
+#pragma unroll 1
+                for (int cc = 0; cc < 128; cc += 32) {
+                    const int nc = p.d_act - (c0 + cc) < 32 ? p.d_act - (c0 + cc) : 32;
+                    float v[32];
+                    uint32_t r[32];
+                    if (have) {
+                        tmem_ld32(tmem + 128 + cc + lane_off, r);
+                        tmem_wait_ld();
+                    }
+#pragma unroll
+                    for (int x = 0; x < 32; ++x) v[x] = have ? __uint_as_float(r[x]) : 0.f;
+                    if (nc > 0) store_rows32_pairs<OUT_F32>(p.dv, wrow0, p.d_act, c0 + cc, v, nc, rows_live, lane);
+                    if (have) {
+                        tmem_ld32(tmem + 256 + cc + lane_off, r);
+                        tmem_wait_ld();
+                    }
+#pragma unroll
+                    for (int x = 0; x < 32; ++x) v[x] = have ? __uint_as_float(r[x]) * p.scale : 0.f;
+                    if (nc > 0) store_rows32_pairs<OUT_F32>(p.dk, wrow0, p.d_act, c0 + cc, v, nc, rows_live, lane);
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+struct WideDqWork {
+    int b, g, hq, q0, n_kv;
+};
+
+// CTA index -> (b, query head, 128-row Q tile) in the dq pass's section order;
+// n_kv counts 64-key tiles.
+__device__ __forceinline__ WideDqWork wide_dq_work(const BwdParams& p) {
+    const DqWork d = dq_work(p);
+    WideDqWork w;
+    w.b = d.b;
+    w.g = d.g;
+    w.hq = d.hq;
+    w.q0 = d.q0;
+    const int n_t64 = (p.Nk + kWQ - 1) / kWQ;
+    if (p.causal) {
+        const int last_row = (w.q0 + kBT - 1 < p.Nq - 1 ? w.q0 + kBT - 1 : p.Nq - 1);
+        const int last_key = last_row + p.off;
+        const int n = last_key < 0 ? 0 : last_key / kWQ + 1;
+        w.n_kv = n < n_t64 ? n : n_t64;
+    } else {
+        w.n_kv = n_t64;
+    }
+    return w;
+}
+
+template <bool OUT_F32>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+attn_bwd_wide_dq_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tdo,
+                        const __grid_constant__ CUtensorMap tk64, const __grid_constant__ CUtensorMap tv64,
+                        const BwdParams p, unsigned int* err) {
+    using C = WideBwdCfg;
+    extern __shared__ uint8_t smem_raw[];
+    const uintptr_t raw = reinterpret_cast<uintptr_t>(smem_raw);
+    uint8_t* smem = reinterpret_cast<uint8_t*>((raw + 1023) & ~uintptr_t(1023));
+    if ((uintptr_t)(smem - smem_raw) + C::kLayout > (uintptr_t)C::kSmemBytes) {
+        if (threadIdx.x == 0) atomicOr(err, kErrLayout);
+        return;
+    }
+    WideBwdBars* bars = reinterpret_cast<WideBwdBars*>(smem + C::kBar);
+    const volatile int* abort_flag = &bars->abort;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const WideDqWork w = wide_dq_work(p);
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bars->res_full), 1);
+        mbar_init(smem_u32(&bars->ld_full), 1);
+        mbar_init(smem_u32(&bars->ld_empty), 1);  // the dQ commit
+        mbar_init(smem_u32(&bars->s_full), 1);
+        mbar_init(smem_u32(&bars->dp_full), 1);
+        mbar_init(smem_u32(&bars->ds_full), 4);
+        mbar_init(smem_u32(&bars->acc_full), 1);
+        mbar_init(smem_u32(&bars->drain), 1);
+        bars->abort = 0;
+        fence_barrier_init();
+        tma_prefetch_desc(&tq);
+        tma_prefetch_desc(&tdo);
+        tma_prefetch_desc(&tk64);
+        tma_prefetch_desc(&tv64);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(&bars->tmem_base), 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = bars->tmem_base;
+    const size_t bh = (size_t)w.b * p.Hq + w.hq;
+
+    if (warp == 0) {
+        // ---- producer: Q, dO once; then K_j, V_j per 64-key tile
+        const bool leader = elect_one();
+        const int kvh = w.b * p.Hkv + w.g;
+        if (leader) {
+            const uint32_t bar = smem_u32(&bars->res_full);
+            mbar_arrive_expect_tx(bar, 2 * C::kBig);
+#pragma unroll
+            for (int c = 0; c < kWD / 64; ++c) {
+                tma_load_3d(smem_u32(smem + C::kA0) + c * 16384, &tq, bar, 64 * c, w.q0, (int)bh);
+                tma_load_3d(smem_u32(smem + C::kA1) + c * 16384, &tdo, bar, 64 * c, w.q0, (int)bh);
+            }
+        }
+        __syncwarp();
+        bool ok = true;
+        int issued = 0;
+        for (int j = 0; j < w.n_kv && ok; ++j) {
+            if (j > 0)
+                ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&bars->ld_empty), (j - 1) & 1, abort_flag));
+            if (!ok) break;
+            if (leader) {
+                const uint32_t bar = smem_u32(&bars->ld_full);
+                mbar_arrive_expect_tx(bar, 2 * C::kSmall);
+#pragma unroll
+                for (int c = 0; c < kWD / 64; ++c) {
+                    tma_load_3d(smem_u32(smem + C::kB0) + c * 8192, &tk64, bar, 64 * c, j * kWQ, kvh);
+                    tma_load_3d(smem_u32(smem + C::kB1) + c * 8192, &tv64, bar, 64 * c, j * kWQ, kvh);
+                }
+            }
+            __syncwarp();
+            ++issued;
+        }
+        if (!ok && leader) wbwd_abort(bars, err);
+        mbar_wait(smem_u32(&bars->res_full), 0, nullptr);
+        if (issued > 0) mbar_wait(smem_u32(&bars->ld_full), (issued - 1) & 1, nullptr);
+        __syncwarp();
+    } else if (warp == 1) {
+        // ---- MMA issuer: per K/V tile S, dP, then dQ (after dS)
+        const bool leader = elect_one();
+        const uint32_t idS = make_idesc_bf16(128, kWQ, 0, 0);
+        const uint32_t idQ = make_idesc_bf16(128, kWD, 0, 1);
+        const uint32_t tS = tmem, tdP = tmem + 64, tdQ = tmem + 128;
+        const uint32_t q_lo = sdesc_lo(smem_u32(smem + C::kA0), 16);
+        const uint32_t do_lo = sdesc_lo(smem_u32(smem + C::kA1), 16);
+        const uint32_t k_lo = sdesc_lo(smem_u32(smem + C::kB0), 16);
+        const uint32_t v_lo = sdesc_lo(smem_u32(smem + C::kB1), 16);
+        const uint32_t k_mn = sdesc_lo(smem_u32(smem + C::kB0), 8192);
+        auto wait_all = [&](uint32_t bar, uint32_t parity) {
+            return __all_sync(0xFFFFFFFFu, mbar_wait(bar, parity, abort_flag, 32));
+        };
+        bool ok = true;
+        if (w.n_kv > 0) ok = wait_all(smem_u32(&bars->res_full), 0);
+        for (int j = 0; j < w.n_kv && ok; ++j) {
+            ok = wait_all(smem_u32(&bars->ld_full), j & 1);
+            if (!ok) break;
+            tc_fence_after();
+            wbwd_issue_s(tS, q_lo, k_lo, idS);                     // S = Q K_j^T
+            mma_commit_warp(smem_u32(&bars->s_full));
+            wbwd_issue_s(tdP, do_lo, v_lo, idS);                   // dP = dO V_j^T
+            mma_commit_warp(smem_u32(&bars->dp_full));
+            ok = wait_all(smem_u32(&bars->ds_full), j & 1);
+            if (!ok) break;
+            tc_fence_after();
+            wbwd_issue_ta(tdQ, tS, k_mn, idQ, j > 0);              // dQ += dS K_j
+            mma_commit_warp(smem_u32(&bars->ld_empty));            // K_j, V_j are read
+        }
+        if (ok && w.n_kv > 0) mma_commit_warp(smem_u32(&bars->acc_full));
+        if (!ok && leader) wbwd_abort(bars, err);
+        mma_commit_warp(smem_u32(&bars->drain));
+        mbar_wait(smem_u32(&bars->drain), 0, nullptr);
+        __syncwarp();
+    } else if (warp >= 4) {
+        // ---- dS (one query row per thread), then the dQ epilogue
+        const int wq = warp & 3;
+        const uint32_t lane_off = uint32_t(wq * 32) << 16;
+        const uint32_t tS = tmem + lane_off, tdP = tmem + 64 + lane_off;
+        const int row = w.q0 + wq * 32 + lane;
+        const float lse2 = p.lse2[bh * p.Nq_pad + row];  // +inf past Nq: P = 0
+        const float dval = p.dvec[bh * p.Nq_pad + row];
+        const uint64_t c2 = f2(p.c, p.c), nl2 = f2(-lse2, -lse2), nd2 = f2(-dval, -dval);
+        bool ok = true;
+        for (int j = 0; j < w.n_kv && ok; ++j) {
+            ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&bars->s_full), j & 1, abort_flag, 32));
+            if (!ok) break;
+            tc_fence_after();
+            const int lim = row + p.off - j * kWQ;  // causal: key column c allowed iff c <= lim
+            const bool masked = __any_sync(0xFFFFFFFFu, p.causal && lim < kWQ - 1);
+            float pf0[32], pf1[32];
+            {
+                uint32_t sv[32];
+                tmem_ld32(tS, sv);
+                tmem_wait_ld();
+                if (masked) p_row_chunk<true>(sv, c2, nl2, 0, p.causal ? lim : kWQ, pf0);
+                else p_row_chunk<false>(sv, c2, nl2, 0, kWQ, pf0);
+                tmem_ld32(tS + 32, sv);
+                tmem_wait_ld();
+                if (masked) p_row_chunk<true>(sv, c2, nl2, 32, p.causal ? lim : kWQ, pf1);
+                else p_row_chunk<false>(sv, c2, nl2, 32, kWQ, pf1);
+            }
+            ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&bars->dp_full), j & 1, abort_flag, 32));
+            if (!ok) break;
+            tc_fence_after();
+            {
+                uint32_t dp[32], dd[16];
+                tmem_ld32(tdP, dp);
+                tmem_wait_ld();
+                ds_row_chunk(pf0, dp, nd2, dd);
+                tmem_st16(tS, dd);
+                tmem_ld32(tdP + 32, dp);
+                tmem_wait_ld();
+                ds_row_chunk(pf1, dp, nd2, dd);
+                tmem_st16(tS + 16, dd);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&bars->ds_full));
+        }
+        if (ok && w.n_kv > 0) {
+            ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&bars->acc_full), 0, abort_flag));
+            if (ok) tc_fence_after();
+        }
+        if (!ok) {
+            wbwd_abort(bars, err);
+        } else {
+            // every lane runs the (warp-collective) TMEM loads; rows past Nq store nothing
+            const size_t wrow0 = bh * p.Nq + (size_t)(w.q0 + wq * 32);
+            const int rows_live = p.Nq - (w.q0 + wq * 32);
+#pragma unroll 1
+            for (int cc = 0; cc < kWD; cc += 32) {
+                float v[32];
+                if (w.n_kv > 0) {
+                    uint32_t r[32];
+                    tmem_ld32(tmem + 128 + cc + lane_off, r);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int x = 0; x < 32; ++x) v[x] = __uint_as_float(r[x]) * p.scale;
+                } else {
+#pragma unroll
+                    for (int x = 0; x < 32; ++x) v[x] = 0.f;
+                }
+                const int nc = p.d_act - cc < 32 ? p.d_act - cc : 32;
+                if (nc > 0) store_rows32_pairs<OUT_F32>(p.dq, wrow0, p.d_act, cc, v, nc, rows_live, lane);
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+template <bool OUT_F32>
+attn_status_t launch_bwd_wide_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                                const CUtensorMap& tdo, const CUtensorMap& tq64,
+                                const CUtensorMap& tk64, const CUtensorMap& tv64,
+                                const CUtensorMap& tdo64, const BwdParams& p, const void* o,
+                                int o_f32, const void* dout, const float* lse, float* lse2,
+                                float* dvec, cudaStream_t stream, const DeviceInfo& dev) {
+    static int attr_set[64] = {0};
+    if (dev.device < 64 && !attr_set[dev.device]) {
+        if (cudaFuncSetAttribute(attn_bwd_wide_dkdv_kernel<OUT_F32>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 WideBwdCfg::kSmemBytes) != cudaSuccess ||
+            cudaFuncSetAttribute(attn_bwd_wide_dq_kernel<OUT_F32>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 WideBwdCfg::kSmemBytes) != cudaSuccess)
+            return ATTN_ERR_CUDA;
+        attr_set[dev.device] = 1;
+    }
+    const long long rows_pad = (long long)p.B * p.Hq * p.Nq_pad;
+    attn_bwd_prep_kernel<kWD><<<(unsigned)((rows_pad + 7) / 8), 256, 0, stream>>>(
+        o, o_f32, static_cast<const __nv_bfloat16*>(dout), lse, lse2, dvec, rows_pad, p.Nq, p.Nq_pad,
+        p.d_act);
+    if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
+    const long long kv_ctas = 2ll * p.B * p.Hkv * p.n_kt;  // two column halves per key tile
+    attn_bwd_wide_dkdv_kernel<OUT_F32><<<(unsigned)kv_ctas, kBwdThreads, WideBwdCfg::kSmemBytes, stream>>>(
+        tq64, tdo64, tk, tv, p, dev.err_word);
+    if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
+    const long long q_ctas = (long long)p.B * p.Hq * ((p.Nq + kBT - 1) / kBT);
+    attn_bwd_wide_dq_kernel<OUT_F32><<<(unsigned)q_ctas, kBwdThreads, WideBwdCfg::kSmemBytes, stream>>>(
+        tq, tdo, tk64, tv64, p, dev.err_word);
+    return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
 }  // namespace
 
 size_t bwd_workspace_bytes(int B, int Hq, int Nq, int d) {
@@ -1045,6 +1647,19 @@ attn_status_t launch_bwd(const void* q, const void* k, const void* v, const void
     if ((st = encode_tmap_bf16_3d(&tdo, dout, d, Nq, (long long)B * Hq, kBT)) != ATTN_OK) return st;
     const int o_f32 = o_dtype == ATTN_OUT_F32;
     const bool g32 = grad_dtype == ATTN_OUT_F32;
+    if (d > 128) {
+        // 64-row boxes for the streamed tiles of the wide passes
+        if ((long long)B * Hkv * p.n_kt * 2 >= (1ll << 31)) return ATTN_ERR_UNSUPPORTED;
+        CUtensorMap tq64, tk64, tv64, tdo64;
+        if ((st = encode_tmap_bf16_3d(&tq64, q, d, Nq, (long long)B * Hq, kWQ)) != ATTN_OK) return st;
+        if ((st = encode_tmap_bf16_3d(&tk64, k, d, Nk, (long long)B * Hkv, kWQ)) != ATTN_OK) return st;
+        if ((st = encode_tmap_bf16_3d(&tv64, v, d, Nk, (long long)B * Hkv, kWQ)) != ATTN_OK) return st;
+        if ((st = encode_tmap_bf16_3d(&tdo64, dout, d, Nq, (long long)B * Hq, kWQ)) != ATTN_OK) return st;
+        return g32 ? launch_bwd_wide_t<true>(tq, tk, tv, tdo, tq64, tk64, tv64, tdo64, p, o, o_f32,
+                                             dout, lse, lse2, dvec, stream, dev)
+                   : launch_bwd_wide_t<false>(tq, tk, tv, tdo, tq64, tk64, tv64, tdo64, p, o, o_f32,
+                                              dout, lse, lse2, dvec, stream, dev);
+    }
     if (pad_head_dim(d) == 128)
         return g32 ? launch_bwd_t<128, true>(tq, tk, tv, tdo, p, o, o_f32, dout, lse, lse2, dvec, stream, dev)
                    : launch_bwd_t<128, false>(tq, tk, tv, tdo, p, o, o_f32, dout, lse, lse2, dvec, stream, dev);

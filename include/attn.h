@@ -237,8 +237,12 @@ size_t attn_bwd_workspace_size(int B, int Hq, int Hkv, int Nq, int Nk, int d);
  *            16-byte aligned; contents need no initialisation; not used after
  *            the call's kernels finish.
  *
- * Supported: 8 <= d <= 128 with d % 8 == 0 (attn_fwd's limits otherwise:
- * Hq % Hkv == 0, causal needs Nq <= Nk).  Pointers 16-byte aligned (lse 4-byte).  The caller owns every
+ * Supported: 8 <= d <= 256 with d % 8 == 0 (attn_fwd's limits otherwise:
+ * Hq % Hkv == 0, causal needs Nq <= Nk).  d <= 128 runs on the kernels
+ * described below; 128 < d <= 256 on kernels built for 256 columns with other
+ * tile shapes (the dK/dV pass per 128 keys and per 128-column half of d over
+ * 64-row Q tiles, the dQ pass per 128 query rows over 64-key tiles, each with
+ * one shared-memory stage).  Pointers 16-byte aligned (lse 4-byte).  The caller owns every
  * buffer.  Three kernels run in order on `stream`: a per-row pass (D, the LSE
  * in base 2), a K/V-outer pass (one CTA per (b, KV head, 128-key tile): dK
  * and dV accumulated in tensor memory over the group's query heads and Q

@@ -145,3 +145,40 @@ def test_bwd_head_dims_padded(d, causal):
     _check(dq, rq, f"dQ d={d}")
     _check(dk, rk, f"dK d={d}")
     _check(dv, rv, f"dV d={d}")
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,Nq,Nk,d,causal", [
+    (1, 2, 2, 128, 128, 256, False),
+    (1, 2, 1, 300, 300, 256, True),      # MQA, ragged 64-row Q tiles and 64-key tiles
+    (2, 4, 2, 200, 200, 192, False),     # the 256-column kernels with zero columns past d
+    (1, 2, 2, 100, 333, 136, True),      # bottom-right causal, Nq < Nk
+    (1, 2, 2, 450, 130, 256, False),     # Nq > Nk, a ragged key tile
+    (1, 8, 2, 700, 700, 256, True),      # GQA group of 4, several key tiles per CTA half
+])
+def test_bwd_wide_head_dims(B, Hq, Hkv, Nq, Nk, d, causal):
+    """Head dims above 128 (the 256-column kernels: the dK/dV pass per column
+    half of d over 64-row Q tiles, the dQ pass over 64-key tiles)."""
+    q, k, v = make_fwd_inputs(B, Hq, Hkv, Nq, Nk, d, seed=1400 + Nq + Nk + d)
+    do = _dout(q.shape, seed=1401 + d)
+    scale = 1 / math.sqrt(d)
+    dq, dk, dv = _run(q, k, v, do, causal, scale)
+    rq, rk, rv = oracle.attention_bwd(q, k, v, do, causal=causal, scale=scale)
+    what = f"{(B, Hq, Hkv, Nq, Nk, d, causal)}"
+    _check(dq, rq, "dQ " + what)
+    _check(dk, rk, "dK " + what)
+    _check(dv, rv, "dV " + what)
+
+
+def test_bwd_wide_chained_bf16_and_repeatable():
+    """d = 256: attn_fwd's own O and LSE into attn_bwd with bf16 gradients,
+    twice, bit-identical."""
+    q, k, v = make_fwd_inputs(1, 4, 2, 512, 512, 256, seed=1500)
+    do = _dout(q.shape, seed=1501)
+    o, lse = ea.forward(q.cuda(), k.cuda(), v.cuda(), causal=True, out_dtype=torch.bfloat16)
+    a = _run(q, k, v, do, True, 1 / 16, grad_dtype=torch.bfloat16, o=o.cpu(), lse=lse.cpu())
+    b = _run(q, k, v, do, True, 1 / 16, grad_dtype=torch.bfloat16, o=o.cpu(), lse=lse.cpu())
+    for x, y in zip(a, b):
+        assert np.array_equal(x, y)
+    rq, rk, rv = oracle.attention_bwd(q, k, v, do, causal=True, scale=1 / 16)
+    for got, ref, n in zip(a, (rq, rk, rv), ("dQ", "dK", "dV")):
+        _check(got, ref, n, bf16=True)

@@ -356,13 +356,12 @@ def test_decode_paged_argument_checks(lib):
 @pytest.mark.parametrize("d,fwd_ok,bwd_ok", [
     (8, True, True), (32, True, True), (48, True, True), (80, True, True), (96, True, True),
     (120, True, True), (128, True, True), (4, False, False), (100, False, False),
-    (130, False, False), (136, True, False), (192, True, False), (200, True, False),
-    (256, True, False), (264, False, False)])
+    (130, False, False), (136, True, True), (192, True, True), (200, True, True),
+    (256, True, True), (264, False, False)])
 def test_supported_head_dims(lib, d, fwd_ok, bwd_ok):
-    """The forward takes d in [8, 256] (multiples of 8): up to 128 on the 64- or
-    128-column kernels, above on the 192- or 256-column ones (zero-filled
-    columns); the backward (workspace size 0 when unsupported) and decode stop
-    at 128."""
+    """The forward, the backward (workspace size 0 when unsupported) and decode
+    take d in [8, 256] (multiples of 8): up to 128 on the 64- or 128-column
+    kernels, above on the wider ones (zero-filled columns)."""
     import torch
     assert (ea.attn_bwd_workspace_size(2, 8, 2, 1000, 1000, d) > 0) == bwd_ok
     # decode takes the forward's head dims (its size query needs a device)
