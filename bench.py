@@ -369,7 +369,7 @@ def run_ours(args, rank, world, local_rank):
         extra["fp8"] = run_fp8(ea, args, dev, stream, flush, peaks)
     if not args.no_wide:
         extra["wide"] = run_wide(ea, args, dev, stream, flush, peaks)
-        extra["decode_d256"] = run_decode_wide(ea, args, dev, stream, flush, peaks)
+        extra["decode_d256"] = run_decode_wide(ea, args, dev, stream, flush, peaks, traffic)
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -660,7 +660,7 @@ def run_fp8(ea, args, dev, stream, flush, peaks):
             "with_quantize_tflops": f8 / (ta_ + tq_) / 1e12}
 
 
-def run_decode_wide(ea, args, dev, stream, flush, peaks):
+def run_decode_wide(ea, args, dev, stream, flush, peaks, traffic):
     """Split-KV decode at d = 256 (the 256-column kernel): B=16 Hq=32 Hkv=8,
     KV cache [16, 8, 16384, 256] bf16 (the d = 128 workload's cache bytes),
     lengths uniform in [512, 16384].  Timing only (parity is in the tests), so
@@ -690,7 +690,8 @@ def run_decode_wide(ea, args, dev, stream, flush, peaks):
     return {"kernel": "attn_decode_split_kernel<256> (split-KV, in-kernel merge)",
             "workload": f"decode B={B} Hq={Hq} Hkv={Hkv} Nmax={Nmax} d={d}, lengths U[512,{Nmax}]",
             "gbs": nbytes / t / 1e9, "frac_of_hbm": nbytes / t / 1e9 / peaks["hbm_gbs"],
-            "algorithmic_bytes": nbytes, "sum_seqlen": sum_len, **st}
+            "algorithmic_bytes": nbytes, "sum_seqlen": sum_len,
+            "traffic": traffic.get("attn_decode_split_kernel", {}).get("decode_d256"), **st}
 
 
 def run_wide(ea, args, dev, stream, flush, peaks):
@@ -713,11 +714,38 @@ def run_wide(ea, args, dev, stream, flush, peaks):
     s_nc, s_c = stats_ms(t_nc), stats_ms(t_c)
     fw = [fwd_flops(cfg.B, cfg.Hq, cfg.N, 256, c) for c in (False, True)]
     tw = [s_nc["median_ms"] * 1e-3, s_c["median_ms"] * 1e-3]
+    # the backward at d = 256 on the same inputs (O and LSE from the forward)
+    g = torch.Generator().manual_seed(8)
+    dout = torch.randn(wq_.shape, generator=g, dtype=torch.float32).to(torch.bfloat16).to(dev)
+    ob = {c: ea.forward(wq_, wk_, wv_, causal=c, out_dtype=torch.bfloat16, stream=stream)
+          for c in (False, True)}
+    gq, gk, gv = torch.empty_like(wq_), torch.empty_like(wk_), torch.empty_like(wv_)
+    bws = torch.empty(ea.attn_bwd_workspace_size(cfg.B, cfg.Hq, cfg.Hkv, cfg.N, cfg.N, 256),
+                      dtype=torch.uint8, device=dev)
+    bfns = [lambda c=c: ea.attn_bwd(wq_, wk_, wv_, ob[c][0], dout, ob[c][1], gq, gk, gv, causal=c,
+                                    workspace=bws, stream=stream) for c in (False, True)]
+    for _ in range(args.warmup):
+        for fn in bfns:
+            flush.zero_()
+            fn()
+    tb_nc, tb_c = time_legs(stream, bfns, max(args.stat_iters, args.steps), flush, flush_each=True)
+    if ea.attn_last_device_error() != 0:
+        raise RuntimeError("device error in the d=256 backward leg")
+    sb_nc, sb_c = stats_ms(tb_nc), stats_ms(tb_c)
+    fb = [2.5 * f for f in fw]
+    tb = [sb_nc["median_ms"] * 1e-3, sb_c["median_ms"] * 1e-3]
     return {"kernel": "attn_fwd_wide_kernel<256> (one Q tile per CTA, 64-key tiles, two S buffers)",
             "workload": f"prefill B={cfg.B} H={cfg.Hq} N={cfg.N} d=256",
             "noncausal_tflops": fw[0] / tw[0] / 1e12, "causal_tflops": fw[1] / tw[1] / 1e12,
             "noncausal": s_nc, "causal": s_c,
-            "frac_of_bf16_peak": sum(fw) / sum(tw) / 1e12 / peaks["bf16_tflops"]}
+            "frac_of_bf16_peak": sum(fw) / sum(tw) / 1e12 / peaks["bf16_tflops"],
+            "bwd": {"kernels": "attn_bwd at d = 256 (prep + dK/dV pass per column half over "
+                               "64-row Q tiles + dQ pass over 64-key tiles)",
+                    "noncausal_tflops": fb[0] / tb[0] / 1e12, "causal_tflops": fb[1] / tb[1] / 1e12,
+                    "noncausal": sb_nc, "causal": sb_c,
+                    "frac_of_bf16_peak": sum(fb) / sum(tb) / 1e12 / peaks["bf16_tflops"],
+                    "flops_note": "2.5 x the forward formula (S, dP, dV, dK, dQ products); the "
+                                  "dK/dV pass computes S and dP once per column half"}}
 
 
 def main():

@@ -12,7 +12,8 @@ Workloads: prefill (B=4 H=16 N=2048 d=128), prefill2x (B=8: inputs larger
 than L2), prefill256 (the prefill shape at d=256), long (B=1 H=32 N=16384), gqa (B=8 Hq=32 Hkv=8 N=4096), decode
 (B=16 Hq=32 Hkv=8 Nmax=32768, lengths 1024..32768) and decode_quarter (the
 same with Nmax=8192, lengths 256..8192: a 512 MiB cache, still larger than
-L2, for multi-pass captures); varlen is the packed causal prefill batch (16
+L2, for multi-pass captures), decode256 (d = 256: B=16 Hq=32 Hkv=8 Nmax=16384,
+lengths 512..16384); varlen is the packed causal prefill batch (16
 sequences of 256..4096 tokens).  fp8 runs attn_fwd_fp8 on E4M3 operands of the
 workload (Q and K rotated by the random-sign Hadamard matrix), fp8quant the
 rotating quantization of its Q.  Inputs come from the seeded generators.
@@ -91,6 +92,17 @@ def main():
         lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
         for _ in range(args.iters):
             ea.attn_fwd(q, k, v, o, lse, causal=causal)
+    elif args.workload == "decode256":
+        # decode at d = 256: B16 Hq32 Hkv8, cache [16, 8, 16384, 256], lengths U[512, 16384]
+        # (the bench's d = 256 decode leg; drawn on the GPU from seeded generators)
+        g = torch.Generator(device=dev).manual_seed(7)
+        q = torch.randn(16, 32, 1, 256, device=dev, generator=g).to(torch.bfloat16)
+        kc = torch.randn(16, 8, 16384, 256, device=dev, generator=g).to(torch.bfloat16)
+        vc = torch.randn(16, 8, 16384, 256, device=dev, generator=g).to(torch.bfloat16)
+        sl = torch.randint(512, 16385, (16,), generator=torch.Generator().manual_seed(7),
+                           dtype=torch.int64).to(torch.int32).to(dev)
+        for _ in range(args.iters):
+            ea.decode(q, kc, vc, sl)
     else:
         if args.workload == "decode_quarter":
             host = make_decode_inputs(DECODE.B, DECODE.Hq, DECODE.Hkv, DECODE.Nmax // 4, DECODE.d,
