@@ -1021,29 +1021,55 @@ constexpr int kWD = 256;    // tile columns
 constexpr int kWQ = 64;     // query rows per dkdv Q tile, keys per dq K/V tile
 constexpr uint32_t kWBwdDescHi = sdesc_hi_sw128(1024);
 
-struct WideBwdCfg {
+// dkdv: K, V resident | Q in two buffers (with lse2[64], D[64] each) | dO
+struct WideDkdvCfg {
     static constexpr int kBig = kBT * kWD * 2;     // 128 rows x 256: 4 chunks of 16 KiB
     static constexpr int kSmall = kWQ * kWD * 2;   // 64 rows x 256: 4 chunks of 8 KiB
-    // dkdv: K, V | Q, dO | lse2[64], D[64];  dq: Q, dO | K, V
-    static constexpr int kA0 = 0;
-    static constexpr int kA1 = kBig;
-    static constexpr int kB0 = 2 * kBig;
-    static constexpr int kB1 = 2 * kBig + kSmall;
-    static constexpr int kLD = 2 * kBig + 2 * kSmall;
+    static constexpr int kK = 0;
+    static constexpr int kV = kBig;
+    static constexpr int kQ = 2 * kBig;                 // 2 buffers
+    static constexpr int kDO = 2 * kBig + 2 * kSmall;   // 1 buffer
+    static constexpr int kLD = 2 * kBig + 3 * kSmall;   // 2 x (lse2[64], D[64])
     static constexpr int kBar = kLD + 1024;
     static constexpr int kLayout = kBar + 256;
     static constexpr int kSmemBytes = kLayout + 1024;
     static_assert(kSmemBytes <= kMaxSmemPerBlock, "shared memory budget");
 };
 
-struct __align__(8) WideBwdBars {
-    uint64_t res_full;            // the resident tiles (dkdv: K, V; dq: Q, dO)
-    uint64_t ld_full, ld_empty;   // the streamed stage
+struct __align__(8) WideDkdvBars {
+    uint64_t kv_full;
+    uint64_t q_full[2], q_empty[2];  // Q_i and its lse2 / D rows, buffer i & 1
+    uint64_t do_full, do_empty;      // dO_i
     uint64_t s_full, dp_full, p_full, ds_full, acc_full, drain;
     uint32_t tmem_base;
     int abort;
 };
-static_assert(sizeof(WideBwdBars) <= 256, "barrier block");
+static_assert(sizeof(WideDkdvBars) <= 256, "barrier block");
+
+// dq: Q, dO resident | K in two buffers | V
+struct WideDqCfg {
+    static constexpr int kBig = kBT * kWD * 2;     // 128 rows x 256: 4 chunks of 16 KiB
+    static constexpr int kSmall = kWQ * kWD * 2;   // 64 rows x 256: 4 chunks of 8 KiB
+    static constexpr int kQ = 0;
+    static constexpr int kDO = kBig;
+    static constexpr int kK = 2 * kBig;                 // 2 buffers
+    static constexpr int kV = 2 * kBig + 2 * kSmall;    // 1 buffer
+    static constexpr int kBar = 2 * kBig + 3 * kSmall;
+    static constexpr int kLayout = kBar + 256;
+    static constexpr int kSmemBytes = kLayout + 1024;
+    static_assert(kSmemBytes <= kMaxSmemPerBlock, "shared memory budget");
+};
+
+struct __align__(8) WideDqBars {
+    uint64_t res_full;                 // Q, dO
+    uint64_t k_full[2], k_empty[2];    // K_j, buffer j & 1
+    uint64_t v_full, v_empty;          // V_j
+    uint64_t s_full[2];                // S_j, TMEM buffer j & 1
+    uint64_t dp_full, ds_full, acc_full, drain;
+    uint32_t tmem_base;
+    int abort;
+};
+static_assert(sizeof(WideDqBars) <= 256, "barrier block");
 
 // S = A B^T with M = 128, N = 64, K = 256: A 128 rows K-major (chunks of 64
 // columns 16 KiB apart), B 64 rows K-major (chunks 8 KiB apart).
@@ -1102,17 +1128,12 @@ __device__ __forceinline__ WideDkdvWork wide_dkdv_work(const BwdParams& p) {
     return w;
 }
 
-__device__ __forceinline__ void wbwd_abort(WideBwdBars* bars, unsigned int* err) {
-    atomicOr(err, kErrTimeout);
-    *((volatile int*)&bars->abort) = 1;
-}
-
 template <bool OUT_F32>
 __global__ void __launch_bounds__(kBwdThreads, 1)
 attn_bwd_wide_dkdv_kernel(const __grid_constant__ CUtensorMap tq64, const __grid_constant__ CUtensorMap tdo64,
                           const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
                           const BwdParams p, unsigned int* err) {
-    using C = WideBwdCfg;
+    using C = WideDkdvCfg;
     extern __shared__ uint8_t smem_raw[];
     const uintptr_t raw = reinterpret_cast<uintptr_t>(smem_raw);
     uint8_t* smem = reinterpret_cast<uint8_t*>((raw + 1023) & ~uintptr_t(1023));
@@ -1120,15 +1141,23 @@ attn_bwd_wide_dkdv_kernel(const __grid_constant__ CUtensorMap tq64, const __grid
         if (threadIdx.x == 0) atomicOr(err, kErrLayout);
         return;
     }
-    WideBwdBars* bars = reinterpret_cast<WideBwdBars*>(smem + C::kBar);
+    WideDkdvBars* bars = reinterpret_cast<WideDkdvBars*>(smem + C::kBar);
     const volatile int* abort_flag = &bars->abort;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const WideDkdvWork w = wide_dkdv_work(p);
+    auto raise_abort = [&]() {
+        atomicOr(err, kErrTimeout);
+        *((volatile int*)&bars->abort) = 1;
+    };
     if (threadIdx.x == 0) {
-        mbar_init(smem_u32(&bars->res_full), 1);
-        mbar_init(smem_u32(&bars->ld_full), 1);
-        mbar_init(smem_u32(&bars->ld_empty), 1 + 4);  // the dK commit + 4 P/dS warps
+        mbar_init(smem_u32(&bars->kv_full), 1);
+        for (int b2 = 0; b2 < 2; ++b2) {
+            mbar_init(smem_u32(&bars->q_full[b2]), 1);
+            mbar_init(smem_u32(&bars->q_empty[b2]), 1 + 4);  // the dK commit + 4 P/dS warps
+        }
+        mbar_init(smem_u32(&bars->do_full), 1);
+        mbar_init(smem_u32(&bars->do_empty), 1);  // the dV commit (dP^T has read dO before it)
         mbar_init(smem_u32(&bars->s_full), 1);
         mbar_init(smem_u32(&bars->dp_full), 1);
         mbar_init(smem_u32(&bars->p_full), 4);
@@ -1152,85 +1181,144 @@ attn_bwd_wide_dkdv_kernel(const __grid_constant__ CUtensorMap tq64, const __grid
     const uint32_t tmem = bars->tmem_base;
 
     if (warp == 0) {
-        // ---- producer: K, V once; then Q, dO, lse2, D per 64-row tile
+        // ---- producer: K, V once; per 64-row tile Q (+ lse2, D) into buffer i & 1
+        // and dO into its one buffer.  Order Q_0, dO_0, Q_1, then dO_i once dV(i-1)
+        // has read dO_{i-1}, and Q_{i+1} once dK(i-1) and the P/dS warps are done
+        // with buffer (i+1) & 1.
         const bool leader = elect_one();
         const int kvh = w.b * p.Hkv + w.g;
         if (leader) {
-            const uint32_t bar = smem_u32(&bars->res_full);
+            const uint32_t bar = smem_u32(&bars->kv_full);
             mbar_arrive_expect_tx(bar, 2 * C::kBig);
 #pragma unroll
             for (int c = 0; c < kWD / 64; ++c) {
-                tma_load_3d(smem_u32(smem + C::kA0) + c * 16384, &tk, bar, 64 * c, w.k0, kvh);
-                tma_load_3d(smem_u32(smem + C::kA1) + c * 16384, &tv, bar, 64 * c, w.k0, kvh);
+                tma_load_3d(smem_u32(smem + C::kK) + c * 16384, &tk, bar, 64 * c, w.k0, kvh);
+                tma_load_3d(smem_u32(smem + C::kV) + c * 16384, &tv, bar, 64 * c, w.k0, kvh);
             }
         }
         __syncwarp();
-        bool ok = true;
-        int issued = 0;
-        for (int i = 0; i < w.n_tiles && ok; ++i) {
-            if (i > 0)
-                ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&bars->ld_empty), (i - 1) & 1, abort_flag));
-            if (!ok) break;
+        auto tile_rows = [&](int i, int& q0, int& bh) {
             const int hq = w.g * p.group + i / w.n_qt_cta;
-            const int q0 = (w.qt_first + i % w.n_qt_cta) * kWQ;
-            const int bh = w.b * p.Hq + hq;
+            q0 = (w.qt_first + i % w.n_qt_cta) * kWQ;
+            bh = w.b * p.Hq + hq;
+        };
+        bool ok = true;
+        int nq = 0, ndo = 0;  // Q and dO tiles issued
+        auto load_q = [&](int i) {
+            const int qb = i & 1;
+            if (i >= 2)
+                ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&bars->q_empty[qb]), ((i >> 1) - 1) & 1,
+                                                       abort_flag));
+            if (!ok) return;
+            int q0, bh;
+            tile_rows(i, q0, bh);
             if (leader) {
-                const uint32_t bar = smem_u32(&bars->ld_full);
-                mbar_arrive_expect_tx(bar, 2 * C::kSmall + 2 * kWQ * 4);
+                const uint32_t bar = smem_u32(&bars->q_full[qb]);
+                mbar_arrive_expect_tx(bar, C::kSmall + 2 * kWQ * 4);
 #pragma unroll
-                for (int c = 0; c < kWD / 64; ++c) {
-                    tma_load_3d(smem_u32(smem + C::kB0) + c * 8192, &tq64, bar, 64 * c, q0, bh);
-                    tma_load_3d(smem_u32(smem + C::kB1) + c * 8192, &tdo64, bar, 64 * c, q0, bh);
-                }
+                for (int c = 0; c < kWD / 64; ++c)
+                    tma_load_3d(smem_u32(smem + C::kQ + qb * C::kSmall) + c * 8192, &tq64, bar, 64 * c, q0, bh);
                 const size_t row = (size_t)bh * p.Nq_pad + q0;
-                bulk_load(smem_u32(smem + C::kLD), p.lse2 + row, kWQ * 4, bar);
-                bulk_load(smem_u32(smem + C::kLD + kWQ * 4), p.dvec + row, kWQ * 4, bar);
+                const uint32_t ld = smem_u32(smem + C::kLD + qb * 512);
+                bulk_load(ld, p.lse2 + row, kWQ * 4, bar);
+                bulk_load(ld + kWQ * 4, p.dvec + row, kWQ * 4, bar);
             }
             __syncwarp();
-            ++issued;
+            ++nq;
+        };
+        auto load_do = [&](int i) {
+            if (i >= 1)
+                ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&bars->do_empty), (i - 1) & 1, abort_flag));
+            if (!ok) return;
+            int q0, bh;
+            tile_rows(i, q0, bh);
+            if (leader) {
+                const uint32_t bar = smem_u32(&bars->do_full);
+                mbar_arrive_expect_tx(bar, C::kSmall);
+#pragma unroll
+                for (int c = 0; c < kWD / 64; ++c)
+                    tma_load_3d(smem_u32(smem + C::kDO) + c * 8192, &tdo64, bar, 64 * c, q0, bh);
+            }
+            __syncwarp();
+            ++ndo;
+        };
+        if (w.n_tiles > 0) {
+            load_q(0);
+            if (ok) load_do(0);
+            if (ok && w.n_tiles > 1) load_q(1);
+            for (int i = 1; i < w.n_tiles && ok; ++i) {
+                load_do(i);
+                if (ok && i + 1 < w.n_tiles) load_q(i + 1);
+            }
         }
-        if (!ok && leader) wbwd_abort(bars, err);
-        mbar_wait(smem_u32(&bars->res_full), 0, nullptr);
-        if (issued > 0) mbar_wait(smem_u32(&bars->ld_full), (issued - 1) & 1, nullptr);
+        if (!ok && leader) raise_abort();
+        // Drain: every issued copy lands before the CTA may exit.
+        mbar_wait(smem_u32(&bars->kv_full), 0, nullptr);
+        for (int qb = 0; qb < 2 && qb < nq; ++qb) {
+            const int uses = (nq - qb + 1) / 2;
+            mbar_wait(smem_u32(&bars->q_full[qb]), (uses - 1) & 1, nullptr);
+        }
+        if (ndo > 0) mbar_wait(smem_u32(&bars->do_full), (ndo - 1) & 1, nullptr);
         __syncwarp();
     } else if (warp == 1) {
-        // ---- MMA issuer: per tile S^T, dP^T, then dV_h (after P^T), dK_h (after dS^T)
+        // ---- MMA issuer.  S^T(0), dP^T(0); per tile i: dV(i) once P^T(i) is in
+        // TMEM, then S^T(i+1) into the columns dV(i) has read; dK(i) once dS^T(i)
+        // is in TMEM, then dP^T(i+1) into the columns dK(i) has read (one CTA's
+        // MMAs run in issue order).  The P/dS warps work on tile i+1's P^T while
+        // dK(i) and the load of dO_{i+1} proceed.
         const bool leader = elect_one();
         const uint32_t idS = make_idesc_bf16(128, kWQ, 0, 0);
         const uint32_t idH = make_idesc_bf16(128, 128, 0, 1);
         const uint32_t tS = tmem, tdP = tmem + 64, tdV = tmem + 128, tdK = tmem + 256;
-        const uint32_t k_lo = sdesc_lo(smem_u32(smem + C::kA0), 16);
-        const uint32_t v_lo = sdesc_lo(smem_u32(smem + C::kA1), 16);
-        const uint32_t q_lo = sdesc_lo(smem_u32(smem + C::kB0), 16);
-        const uint32_t do_lo = sdesc_lo(smem_u32(smem + C::kB1), 16);
+        const uint32_t k_lo = sdesc_lo(smem_u32(smem + C::kK), 16);
+        const uint32_t v_lo = sdesc_lo(smem_u32(smem + C::kV), 16);
+        const uint32_t do_lo = sdesc_lo(smem_u32(smem + C::kDO), 16);
         // this CTA's column half of Q and dO as MN-major B operands
-        const uint32_t q_mn = sdesc_lo(smem_u32(smem + C::kB0) + w.half * 2 * 8192, 8192);
-        const uint32_t do_mn = sdesc_lo(smem_u32(smem + C::kB1) + w.half * 2 * 8192, 8192);
+        const uint32_t do_mn = sdesc_lo(smem_u32(smem + C::kDO) + w.half * 2 * 8192, 8192);
+        auto q_lo = [&](int qb) { return sdesc_lo(smem_u32(smem + C::kQ + qb * C::kSmall), 16); };
+        auto q_mn = [&](int qb) {
+            return sdesc_lo(smem_u32(smem + C::kQ + qb * C::kSmall) + w.half * 2 * 8192, 8192);
+        };
         auto wait_all = [&](uint32_t bar, uint32_t parity) {
             return __all_sync(0xFFFFFFFFu, mbar_wait(bar, parity, abort_flag, 32));
         };
-        bool ok = true;
-        if (w.n_tiles > 0) ok = wait_all(smem_u32(&bars->res_full), 0);
-        for (int i = 0; i < w.n_tiles && ok; ++i) {
-            ok = wait_all(smem_u32(&bars->ld_full), i & 1);
-            if (!ok) break;
+        auto issue_st = [&](int i) {  // S^T(i) = K Q_i^T
+            if (!wait_all(smem_u32(&bars->q_full[i & 1]), (i >> 1) & 1)) return false;
             tc_fence_after();
-            wbwd_issue_s(tS, k_lo, q_lo, idS);                     // S^T = K Q^T
+            wbwd_issue_s(tS, k_lo, q_lo(i & 1), idS);
             mma_commit_warp(smem_u32(&bars->s_full));
-            wbwd_issue_s(tdP, v_lo, do_lo, idS);                   // dP^T = V dO^T
+            return true;
+        };
+        auto issue_dpt = [&](int i) {  // dP^T(i) = V dO_i^T
+            if (!wait_all(smem_u32(&bars->do_full), i & 1)) return false;
+            tc_fence_after();
+            wbwd_issue_s(tdP, v_lo, do_lo, idS);
             mma_commit_warp(smem_u32(&bars->dp_full));
+            return true;
+        };
+        bool ok = true;
+        if (w.n_tiles > 0) {
+            ok = wait_all(smem_u32(&bars->kv_full), 0);
+            if (ok) ok = issue_st(0);
+            if (ok) ok = issue_dpt(0);
+        }
+        for (int i = 0; i < w.n_tiles && ok; ++i) {
+            const bool more = i + 1 < w.n_tiles;
             ok = wait_all(smem_u32(&bars->p_full), i & 1);
             if (!ok) break;
             tc_fence_after();
             wbwd_issue_ta(tdV, tS, do_mn, idH, i > 0);             // dV_h += P^T dO_h
+            mma_commit_warp(smem_u32(&bars->do_empty));            // dO_i is read
+            if (more && !(ok = issue_st(i + 1))) break;
             ok = wait_all(smem_u32(&bars->ds_full), i & 1);
             if (!ok) break;
             tc_fence_after();
-            wbwd_issue_ta(tdK, tdP, q_mn, idH, i > 0);             // dK_h += dS^T Q_h
-            mma_commit_warp(smem_u32(&bars->ld_empty));            // the stage is read
+            wbwd_issue_ta(tdK, tdP, q_mn(i & 1), idH, i > 0);      // dK_h += dS^T Q_h
+            mma_commit_warp(smem_u32(&bars->q_empty[i & 1]));      // Q_i is read
+            if (more && !(ok = issue_dpt(i + 1))) break;
         }
         if (ok && w.n_tiles > 0) mma_commit_warp(smem_u32(&bars->acc_full));
-        if (!ok && leader) wbwd_abort(bars, err);
+        if (!ok && leader) raise_abort();
         mma_commit_warp(smem_u32(&bars->drain));
         mbar_wait(smem_u32(&bars->drain), 0, nullptr);
         __syncwarp();
@@ -1240,8 +1328,6 @@ attn_bwd_wide_dkdv_kernel(const __grid_constant__ CUtensorMap tq64, const __grid
         const uint32_t lane_off = uint32_t(wq * 32) << 16;
         const uint32_t tS = tmem + lane_off, tdP = tmem + 64 + lane_off;
         const int jg = w.k0 + wq * 32 + lane;
-        const uint32_t lse2s = smem_u32(smem + C::kLD);
-        const uint32_t ds_vec = lse2s + kWQ * 4;
         bool ok = true;
         for (int i = 0; i < w.n_tiles && ok; ++i) {
             ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&bars->s_full), i & 1, abort_flag, 32));
@@ -1250,6 +1336,8 @@ attn_bwd_wide_dkdv_kernel(const __grid_constant__ CUtensorMap tq64, const __grid
             const int q0 = (w.qt_first + i % w.n_qt_cta) * kWQ;
             const int lim = jg - p.off - q0;  // causal: column x allowed iff x >= lim
             const bool masked = p.causal && (q0 + p.off < w.k0 + kBT - 1);
+            const uint32_t lse2s = smem_u32(smem + C::kLD + (i & 1) * 512);
+            const uint32_t ds_vec = lse2s + kWQ * 4;
             float pf0[32], pf1[32];
             {
                 uint32_t sv[32], pp[16];
@@ -1287,20 +1375,20 @@ attn_bwd_wide_dkdv_kernel(const __grid_constant__ CUtensorMap tq64, const __grid
             __syncwarp();
             if (lane == 0) {
                 mbar_arrive(smem_u32(&bars->ds_full));
-                mbar_arrive(smem_u32(&bars->ld_empty));  // lse2 and D of the tile are read
+                mbar_arrive(smem_u32(&bars->q_empty[i & 1]));  // lse2 and D of the tile are read
             }
         }
         if (!ok) {
-            wbwd_abort(bars, err);
+            raise_abort();
         } else {
             // dK_h = scale dS^T Q_h, dV_h = P^T dO_h: columns [128h, 128h + 128)
             const size_t wrow0 = ((size_t)w.b * p.Hkv + w.g) * p.Nk + (size_t)(w.k0 + wq * 32);
             const int rows_live = p.Nk - (w.k0 + wq * 32);
             const int c0 = w.half * 128;
-            bool have = w.n_tiles > 0;
+            const bool have = w.n_tiles > 0;
             if (have) {
                 ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&bars->acc_full), 0, abort_flag));
-                if (!ok) wbwd_abort(bars, err);
+                if (!ok) raise_abort();
                 else tc_fence_after();
             }
             if (ok) {
@@ -1366,7 +1454,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 attn_bwd_wide_dq_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tdo,
                         const __grid_constant__ CUtensorMap tk64, const __grid_constant__ CUtensorMap tv64,
                         const BwdParams p, unsigned int* err) {
-    using C = WideBwdCfg;
+    using C = WideDqCfg;
     extern __shared__ uint8_t smem_raw[];
     const uintptr_t raw = reinterpret_cast<uintptr_t>(smem_raw);
     uint8_t* smem = reinterpret_cast<uint8_t*>((raw + 1023) & ~uintptr_t(1023));
@@ -1374,16 +1462,24 @@ attn_bwd_wide_dq_kernel(const __grid_constant__ CUtensorMap tq, const __grid_con
         if (threadIdx.x == 0) atomicOr(err, kErrLayout);
         return;
     }
-    WideBwdBars* bars = reinterpret_cast<WideBwdBars*>(smem + C::kBar);
+    WideDqBars* bars = reinterpret_cast<WideDqBars*>(smem + C::kBar);
     const volatile int* abort_flag = &bars->abort;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const WideDqWork w = wide_dq_work(p);
+    auto raise_abort = [&]() {
+        atomicOr(err, kErrTimeout);
+        *((volatile int*)&bars->abort) = 1;
+    };
     if (threadIdx.x == 0) {
         mbar_init(smem_u32(&bars->res_full), 1);
-        mbar_init(smem_u32(&bars->ld_full), 1);
-        mbar_init(smem_u32(&bars->ld_empty), 1);  // the dQ commit
-        mbar_init(smem_u32(&bars->s_full), 1);
+        for (int b2 = 0; b2 < 2; ++b2) {
+            mbar_init(smem_u32(&bars->k_full[b2]), 1);
+            mbar_init(smem_u32(&bars->k_empty[b2]), 1);  // the dQ commit (S has read K before it)
+            mbar_init(smem_u32(&bars->s_full[b2]), 1);
+        }
+        mbar_init(smem_u32(&bars->v_full), 1);
+        mbar_init(smem_u32(&bars->v_empty), 1);  // the dP commit
         mbar_init(smem_u32(&bars->dp_full), 1);
         mbar_init(smem_u32(&bars->ds_full), 4);
         mbar_init(smem_u32(&bars->acc_full), 1);
@@ -1406,7 +1502,8 @@ attn_bwd_wide_dq_kernel(const __grid_constant__ CUtensorMap tq, const __grid_con
     const size_t bh = (size_t)w.b * p.Hq + w.hq;
 
     if (warp == 0) {
-        // ---- producer: Q, dO once; then K_j, V_j per 64-key tile
+        // ---- producer: Q, dO once; K_j into buffer j & 1 once dQ(j-2) has read
+        // it; V_j into its one buffer once dP(j-1) has read it.
         const bool leader = elect_one();
         const int kvh = w.b * p.Hkv + w.g;
         if (leader) {
@@ -1414,65 +1511,112 @@ attn_bwd_wide_dq_kernel(const __grid_constant__ CUtensorMap tq, const __grid_con
             mbar_arrive_expect_tx(bar, 2 * C::kBig);
 #pragma unroll
             for (int c = 0; c < kWD / 64; ++c) {
-                tma_load_3d(smem_u32(smem + C::kA0) + c * 16384, &tq, bar, 64 * c, w.q0, (int)bh);
-                tma_load_3d(smem_u32(smem + C::kA1) + c * 16384, &tdo, bar, 64 * c, w.q0, (int)bh);
+                tma_load_3d(smem_u32(smem + C::kQ) + c * 16384, &tq, bar, 64 * c, w.q0, (int)bh);
+                tma_load_3d(smem_u32(smem + C::kDO) + c * 16384, &tdo, bar, 64 * c, w.q0, (int)bh);
             }
         }
         __syncwarp();
         bool ok = true;
-        int issued = 0;
-        for (int j = 0; j < w.n_kv && ok; ++j) {
-            if (j > 0)
-                ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&bars->ld_empty), (j - 1) & 1, abort_flag));
-            if (!ok) break;
+        int nk = 0, nv = 0;  // K and V tiles issued
+        auto load_k = [&](int j) {
+            const int kb = j & 1;
+            if (j >= 2)
+                ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&bars->k_empty[kb]), ((j >> 1) - 1) & 1,
+                                                       abort_flag));
+            if (!ok) return;
             if (leader) {
-                const uint32_t bar = smem_u32(&bars->ld_full);
-                mbar_arrive_expect_tx(bar, 2 * C::kSmall);
+                const uint32_t bar = smem_u32(&bars->k_full[kb]);
+                mbar_arrive_expect_tx(bar, C::kSmall);
 #pragma unroll
-                for (int c = 0; c < kWD / 64; ++c) {
-                    tma_load_3d(smem_u32(smem + C::kB0) + c * 8192, &tk64, bar, 64 * c, j * kWQ, kvh);
-                    tma_load_3d(smem_u32(smem + C::kB1) + c * 8192, &tv64, bar, 64 * c, j * kWQ, kvh);
-                }
+                for (int c = 0; c < kWD / 64; ++c)
+                    tma_load_3d(smem_u32(smem + C::kK + kb * C::kSmall) + c * 8192, &tk64, bar, 64 * c,
+                                j * kWQ, kvh);
             }
             __syncwarp();
-            ++issued;
+            ++nk;
+        };
+        auto load_v = [&](int j) {
+            if (j >= 1)
+                ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&bars->v_empty), (j - 1) & 1, abort_flag));
+            if (!ok) return;
+            if (leader) {
+                const uint32_t bar = smem_u32(&bars->v_full);
+                mbar_arrive_expect_tx(bar, C::kSmall);
+#pragma unroll
+                for (int c = 0; c < kWD / 64; ++c)
+                    tma_load_3d(smem_u32(smem + C::kV) + c * 8192, &tv64, bar, 64 * c, j * kWQ, kvh);
+            }
+            __syncwarp();
+            ++nv;
+        };
+        // K_0, V_0, K_1, then V_j and K_{j+1} as their buffers free up
+        if (w.n_kv > 0) {
+            load_k(0);
+            if (ok) load_v(0);
+            if (ok && w.n_kv > 1) load_k(1);
+            for (int j = 1; j < w.n_kv && ok; ++j) {
+                load_v(j);
+                if (ok && j + 1 < w.n_kv) load_k(j + 1);
+            }
         }
-        if (!ok && leader) wbwd_abort(bars, err);
+        if (!ok && leader) raise_abort();
         mbar_wait(smem_u32(&bars->res_full), 0, nullptr);
-        if (issued > 0) mbar_wait(smem_u32(&bars->ld_full), (issued - 1) & 1, nullptr);
+        for (int kb = 0; kb < 2 && kb < nk; ++kb) {
+            const int uses = (nk - kb + 1) / 2;
+            mbar_wait(smem_u32(&bars->k_full[kb]), (uses - 1) & 1, nullptr);
+        }
+        if (nv > 0) mbar_wait(smem_u32(&bars->v_full), (nv - 1) & 1, nullptr);
         __syncwarp();
     } else if (warp == 1) {
-        // ---- MMA issuer: per K/V tile S, dP, then dQ (after dS)
+        // ---- MMA issuer: S_0, dP_0, S_1; per tile j, once dS_j is in TMEM: dQ +=
+        // dS_j K_j, dP_{j+1} (into the dP columns the dS warps have read), S_{j+2}
+        // into the buffer dQ_j has read (one CTA's MMAs run in issue order).
         const bool leader = elect_one();
         const uint32_t idS = make_idesc_bf16(128, kWQ, 0, 0);
         const uint32_t idQ = make_idesc_bf16(128, kWD, 0, 1);
-        const uint32_t tS = tmem, tdP = tmem + 64, tdQ = tmem + 128;
-        const uint32_t q_lo = sdesc_lo(smem_u32(smem + C::kA0), 16);
-        const uint32_t do_lo = sdesc_lo(smem_u32(smem + C::kA1), 16);
-        const uint32_t k_lo = sdesc_lo(smem_u32(smem + C::kB0), 16);
-        const uint32_t v_lo = sdesc_lo(smem_u32(smem + C::kB1), 16);
-        const uint32_t k_mn = sdesc_lo(smem_u32(smem + C::kB0), 8192);
+        const uint32_t tdP = tmem + 128, tdQ = tmem + 192;
+        auto tS = [&](int j) { return tmem + (uint32_t)(j & 1) * 64u; };
+        const uint32_t q_lo = sdesc_lo(smem_u32(smem + C::kQ), 16);
+        const uint32_t do_lo = sdesc_lo(smem_u32(smem + C::kDO), 16);
+        const uint32_t v_lo = sdesc_lo(smem_u32(smem + C::kV), 16);
+        auto k_lo = [&](int kb) { return sdesc_lo(smem_u32(smem + C::kK + kb * C::kSmall), 16); };
+        auto k_mn = [&](int kb) { return sdesc_lo(smem_u32(smem + C::kK + kb * C::kSmall), 8192); };
         auto wait_all = [&](uint32_t bar, uint32_t parity) {
             return __all_sync(0xFFFFFFFFu, mbar_wait(bar, parity, abort_flag, 32));
         };
-        bool ok = true;
-        if (w.n_kv > 0) ok = wait_all(smem_u32(&bars->res_full), 0);
-        for (int j = 0; j < w.n_kv && ok; ++j) {
-            ok = wait_all(smem_u32(&bars->ld_full), j & 1);
-            if (!ok) break;
+        auto issue_s = [&](int j) {  // S_j = Q K_j^T into buffer j & 1
+            if (!wait_all(smem_u32(&bars->k_full[j & 1]), (j >> 1) & 1)) return false;
             tc_fence_after();
-            wbwd_issue_s(tS, q_lo, k_lo, idS);                     // S = Q K_j^T
-            mma_commit_warp(smem_u32(&bars->s_full));
-            wbwd_issue_s(tdP, do_lo, v_lo, idS);                   // dP = dO V_j^T
+            wbwd_issue_s(tS(j), q_lo, k_lo(j & 1), idS);
+            mma_commit_warp(smem_u32(&bars->s_full[j & 1]));
+            return true;
+        };
+        auto issue_dp = [&](int j) {  // dP_j = dO V_j^T
+            if (!wait_all(smem_u32(&bars->v_full), j & 1)) return false;
+            tc_fence_after();
+            wbwd_issue_s(tdP, do_lo, v_lo, idS);
+            mma_commit_warp(smem_u32(&bars->v_empty));  // V_j is read
             mma_commit_warp(smem_u32(&bars->dp_full));
+            return true;
+        };
+        bool ok = true;
+        if (w.n_kv > 0) {
+            ok = wait_all(smem_u32(&bars->res_full), 0);
+            if (ok) ok = issue_s(0);
+            if (ok) ok = issue_dp(0);
+            if (ok && w.n_kv > 1) ok = issue_s(1);
+        }
+        for (int j = 0; j < w.n_kv && ok; ++j) {
             ok = wait_all(smem_u32(&bars->ds_full), j & 1);
             if (!ok) break;
             tc_fence_after();
-            wbwd_issue_ta(tdQ, tS, k_mn, idQ, j > 0);              // dQ += dS K_j
-            mma_commit_warp(smem_u32(&bars->ld_empty));            // K_j, V_j are read
+            wbwd_issue_ta(tdQ, tS(j), k_mn(j & 1), idQ, j > 0);    // dQ += dS_j K_j
+            mma_commit_warp(smem_u32(&bars->k_empty[j & 1]));     // K_j is read (S_j, dQ_j)
+            if (j + 1 < w.n_kv && !(ok = issue_dp(j + 1))) break;
+            if (j + 2 < w.n_kv && !(ok = issue_s(j + 2))) break;
         }
         if (ok && w.n_kv > 0) mma_commit_warp(smem_u32(&bars->acc_full));
-        if (!ok && leader) wbwd_abort(bars, err);
+        if (!ok && leader) raise_abort();
         mma_commit_warp(smem_u32(&bars->drain));
         mbar_wait(smem_u32(&bars->drain), 0, nullptr);
         __syncwarp();
@@ -1480,14 +1624,16 @@ attn_bwd_wide_dq_kernel(const __grid_constant__ CUtensorMap tq, const __grid_con
         // ---- dS (one query row per thread), then the dQ epilogue
         const int wq = warp & 3;
         const uint32_t lane_off = uint32_t(wq * 32) << 16;
-        const uint32_t tS = tmem + lane_off, tdP = tmem + 64 + lane_off;
+        const uint32_t tdP = tmem + 128 + lane_off;
         const int row = w.q0 + wq * 32 + lane;
         const float lse2 = p.lse2[bh * p.Nq_pad + row];  // +inf past Nq: P = 0
         const float dval = p.dvec[bh * p.Nq_pad + row];
         const uint64_t c2 = f2(p.c, p.c), nl2 = f2(-lse2, -lse2), nd2 = f2(-dval, -dval);
         bool ok = true;
         for (int j = 0; j < w.n_kv && ok; ++j) {
-            ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&bars->s_full), j & 1, abort_flag, 32));
+            const uint32_t tS = tmem + (uint32_t)(j & 1) * 64u + lane_off;
+            ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&bars->s_full[j & 1]), (j >> 1) & 1,
+                                                   abort_flag, 32));
             if (!ok) break;
             tc_fence_after();
             const int lim = row + p.off - j * kWQ;  // causal: key column c allowed iff c <= lim
@@ -1528,7 +1674,7 @@ attn_bwd_wide_dq_kernel(const __grid_constant__ CUtensorMap tq, const __grid_con
             if (ok) tc_fence_after();
         }
         if (!ok) {
-            wbwd_abort(bars, err);
+            raise_abort();
         } else {
             // every lane runs the (warp-collective) TMEM loads; rows past Nq store nothing
             const size_t wrow0 = bh * p.Nq + (size_t)(w.q0 + wq * 32);
@@ -1538,7 +1684,7 @@ attn_bwd_wide_dq_kernel(const __grid_constant__ CUtensorMap tq, const __grid_con
                 float v[32];
                 if (w.n_kv > 0) {
                     uint32_t r[32];
-                    tmem_ld32(tmem + 128 + cc + lane_off, r);
+                    tmem_ld32(tmem + 192 + cc + lane_off, r);
                     tmem_wait_ld();
 #pragma unroll
                     for (int x = 0; x < 32; ++x) v[x] = __uint_as_float(r[x]) * p.scale;
@@ -1571,10 +1717,10 @@ attn_status_t launch_bwd_wide_t(const CUtensorMap& tq, const CUtensorMap& tk, co
     if (dev.device < 64 && !attr_set[dev.device]) {
         if (cudaFuncSetAttribute(attn_bwd_wide_dkdv_kernel<OUT_F32>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 WideBwdCfg::kSmemBytes) != cudaSuccess ||
+                                 WideDkdvCfg::kSmemBytes) != cudaSuccess ||
             cudaFuncSetAttribute(attn_bwd_wide_dq_kernel<OUT_F32>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 WideBwdCfg::kSmemBytes) != cudaSuccess)
+                                 WideDqCfg::kSmemBytes) != cudaSuccess)
             return ATTN_ERR_CUDA;
         attr_set[dev.device] = 1;
     }
@@ -1584,11 +1730,11 @@ attn_status_t launch_bwd_wide_t(const CUtensorMap& tq, const CUtensorMap& tk, co
         p.d_act);
     if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
     const long long kv_ctas = 2ll * p.B * p.Hkv * p.n_kt;  // two column halves per key tile
-    attn_bwd_wide_dkdv_kernel<OUT_F32><<<(unsigned)kv_ctas, kBwdThreads, WideBwdCfg::kSmemBytes, stream>>>(
+    attn_bwd_wide_dkdv_kernel<OUT_F32><<<(unsigned)kv_ctas, kBwdThreads, WideDkdvCfg::kSmemBytes, stream>>>(
         tq64, tdo64, tk, tv, p, dev.err_word);
     if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
     const long long q_ctas = (long long)p.B * p.Hq * ((p.Nq + kBT - 1) / kBT);
-    attn_bwd_wide_dq_kernel<OUT_F32><<<(unsigned)q_ctas, kBwdThreads, WideBwdCfg::kSmemBytes, stream>>>(
+    attn_bwd_wide_dq_kernel<OUT_F32><<<(unsigned)q_ctas, kBwdThreads, WideDqCfg::kSmemBytes, stream>>>(
         tq, tdo, tk64, tv64, p, dev.err_word);
     return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
