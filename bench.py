@@ -648,7 +648,13 @@ def run_fp8(ea, args, dev, stream, flush, peaks):
     n_el = lq.numel() + lk.numel() + lv.numel()
     qbytes = 3 * n_el + 4 * (qd.numel() + kd.numel() + vd.numel())   # bf16 in, E4M3 out
     peak8 = 2 * peaks["bf16_tflops"]
+    gemm8 = fp8_gemm_tflops(dev)
     return {"kernels": "attn_fp8_quantize (x3: Q, K rotated; V transposed) + attn_fwd_fp8_kernel",
+            "fp8_gemm_measured_tflops": gemm8,
+            "attn_frac_of_measured_fp8_gemm": (f8 / ta_ / 1e12 / gemm8) if gemm8 else None,
+            "fp8_gemm_note": "context: best of 10 library E4M3 GEMMs (torch._scaled_mm, 8192^3, "
+                             "bf16 out) on this GPU in the same run; the roofline peak above "
+                             "follows the rule for a dtype without a driver-measured peak",
             "workload": "long-context causal B=1 H=32 N=16384 d=128, 4 outlier channels",
             "attn_tflops": f8 / ta_ / 1e12, "attn": sa,
             "attn_frac_of_fp8_peak": f8 / ta_ / 1e12 / peak8,
@@ -692,6 +698,30 @@ def run_decode_wide(ea, args, dev, stream, flush, peaks, traffic):
             "gbs": nbytes / t / 1e9, "frac_of_hbm": nbytes / t / 1e9 / peaks["hbm_gbs"],
             "algorithmic_bytes": nbytes, "sum_seqlen": sum_len,
             "traffic": traffic.get("attn_decode_split_kernel", {}).get("decode_d256"), **st}
+
+
+def fp8_gemm_tflops(dev):
+    """A measured E4M3 GEMM rate on this GPU (torch._scaled_mm, 8192^3, best of
+    10 CUDA-event timings), reported beside the FP8 leg's nominal peak; None if
+    the library path is unavailable."""
+    try:
+        n = 8192
+        a = torch.randn(n, n, device=dev).to(torch.float8_e4m3fn)
+        b = torch.randn(n, n, device=dev).to(torch.float8_e4m3fn).t()
+        one = torch.ones((), device=dev)
+        torch._scaled_mm(a, b, scale_a=one, scale_b=one, out_dtype=torch.bfloat16)
+        best = None
+        for _ in range(10):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            torch._scaled_mm(a, b, scale_a=one, scale_b=one, out_dtype=torch.bfloat16)
+            e1.record()
+            e1.synchronize()
+            t = e0.elapsed_time(e1) * 1e-3
+            best = t if best is None else min(best, t)
+        return 2.0 * n ** 3 / best / 1e12
+    except Exception:  # noqa: BLE001 -- context only
+        return None
 
 
 def run_wide(ea, args, dev, stream, flush, peaks):
