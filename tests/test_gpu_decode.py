@@ -85,15 +85,26 @@ def test_decode_shapes(B, Hq, Hkv, Nmax, d, lo, hi):
 
 @pytest.mark.parametrize("d", [192, 256])
 def test_decode_wide_head_dims_gqa_and_many_splits(d):
-    """The 256-column kernel on a GQA group of 8 heads with lengths up to 8192,
-    with the in-kernel merge (automatic splits) and with the combine kernel
-    (more groups than its counter table), against the oracle."""
+    """The 256-column kernel on a GQA group of 8 heads with lengths up to 8192
+    (NaN past each length), one split and many, merged inside the split
+    kernel, against the oracle."""
     q, kc, vc, sl = make_decode_inputs(4, 32, 4, 8192, d, seed=90 + d, len_lo=1, len_hi=8192,
                                        tail="nan")
     o_ref, lse_ref = oracle.decode(q, kc, vc, sl)
     for ns in (0, 1, 16):
         o, lse = gpu_decode(q, kc, vc, sl, num_splits=ns)
         assert_close(o, lse, o_ref, lse_ref, f"d={d} splits={ns}")
+
+
+def test_decode_wide_head_dim_combine_kernel():
+    """d = 256 with more (sequence, KV head) groups than the in-kernel merge's
+    counter table holds: the splits are merged by the combine kernel."""
+    B, Hq, Hkv, Nmax, d = 520, 8, 8, 192, 256
+    assert ea.attn_decode_kernel_launches(B, Hq, Hkv, Nmax, d, 3) == 2
+    q, kc, vc, sl = make_decode_inputs(B, Hq, Hkv, Nmax, d, seed=97, len_lo=1, len_hi=Nmax)
+    o, lse = gpu_decode(q, kc, vc, sl, num_splits=3)
+    o_ref, lse_ref = oracle.decode(q, kc, vc, sl)
+    assert_close(o, lse, o_ref, lse_ref, "d=256 combine kernel")
 
 
 def test_decode_bf16_output():
