@@ -931,33 +931,74 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
 // ---------------------------------------------------------------------------
 // prep
 // ---------------------------------------------------------------------------
-// One warp per padded query row: D = dO . O and lse2 = LSE log2(e)
-// (padding: 0 and +inf).
-template <int D>
+// D = dO . O and lse2 = LSE log2(e) for every padded query row (padding: 0
+// and +inf).  LPR lanes share a row, each reading 8 consecutive elements of
+// dO and of O per 16-byte load (rows start on 16-byte boundaries: d % 8 == 0
+// and both arrays 16-byte aligned), so a warp covers 32 / LPR rows with
+// whole-sector loads; their partial sums meet by shuffles inside the group.
+template <int LPR>
 __global__ void __launch_bounds__(256)
 attn_bwd_prep_kernel(const void* __restrict__ o, int o_f32, const __nv_bfloat16* __restrict__ dout,
                      const float* __restrict__ lse, float* __restrict__ lse2, float* __restrict__ dvec,
                      long long rows_pad, int Nq, int Nq_pad, int dh) {
-    const long long r = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+    constexpr int kRowsPerWarp = 32 / LPR;
     const int lane = threadIdx.x & 31;
-    if (r >= rows_pad) return;
-    const long long bh = r / Nq_pad;
-    const int i = (int)(r - bh * Nq_pad);
+    const int sub = lane % LPR;
+    const long long r = ((long long)blockIdx.x * 8 + (threadIdx.x >> 5)) * kRowsPerWarp + lane / LPR;
+    const bool live_row = r < rows_pad;
+    const long long bh = live_row ? r / Nq_pad : 0;
+    const int i = live_row ? (int)(r - bh * Nq_pad) : Nq;
     float sum = 0.f;
     if (i < Nq) {
         const size_t base = ((size_t)bh * Nq + i) * dh;
-        for (int c = lane; c < dh; c += 32) {
-            const float ov = o_f32 ? static_cast<const float*>(o)[base + c]
-                                   : __bfloat162float(static_cast<const __nv_bfloat16*>(o)[base + c]);
-            sum = fmaf(__bfloat162float(dout[base + c]), ov, sum);
+        for (int c = sub * 8; c < dh; c += LPR * 8) {
+            const uint4 g = *reinterpret_cast<const uint4*>(dout + base + c);
+            const uint32_t gw[4] = {g.x, g.y, g.z, g.w};
+            float ov[8];
+            if (o_f32) {
+                const float4 a = *reinterpret_cast<const float4*>(static_cast<const float*>(o) + base + c);
+                const float4 b = *reinterpret_cast<const float4*>(static_cast<const float*>(o) + base + c + 4);
+                ov[0] = a.x; ov[1] = a.y; ov[2] = a.z; ov[3] = a.w;
+                ov[4] = b.x; ov[5] = b.y; ov[6] = b.z; ov[7] = b.w;
+            } else {
+                const uint4 h = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(o) + base + c);
+                const uint32_t hw[4] = {h.x, h.y, h.z, h.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    ov[2 * e] = __uint_as_float(hw[e] << 16);
+                    ov[2 * e + 1] = __uint_as_float(hw[e] & 0xFFFF0000u);
+                }
+            }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                sum = fmaf(__uint_as_float(gw[e] << 16), ov[2 * e], sum);
+                sum = fmaf(__uint_as_float(gw[e] & 0xFFFF0000u), ov[2 * e + 1], sum);
+            }
         }
     }
 #pragma unroll
-    for (int s = 16; s > 0; s >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, s);
-    if (lane == 0) {
+    for (int s = LPR / 2; s > 0; s >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, s);
+    if (live_row && sub == 0) {
         dvec[r] = i < Nq ? sum : 0.f;
         lse2[r] = i < Nq ? lse[(size_t)bh * Nq + i] * kBwdLog2e : INFINITY;
     }
+}
+
+// The prep launch for head dim dh (<= 256): 8, 16 or 32 lanes per row.
+attn_status_t launch_bwd_prep(const void* o, int o_f32, const void* dout, const float* lse,
+                              float* lse2, float* dvec, long long rows_pad, int Nq, int Nq_pad,
+                              int dh, cudaStream_t stream) {
+    const auto* g = static_cast<const __nv_bfloat16*>(dout);
+    const int lpr = dh <= 64 ? 8 : dh <= 128 ? 16 : 32;
+    const long long rows_per_block = 8ll * (32 / lpr);
+    const unsigned grid = (unsigned)((rows_pad + rows_per_block - 1) / rows_per_block);
+    if (lpr == 8)
+        attn_bwd_prep_kernel<8><<<grid, 256, 0, stream>>>(o, o_f32, g, lse, lse2, dvec, rows_pad, Nq, Nq_pad, dh);
+    else if (lpr == 16)
+        attn_bwd_prep_kernel<16><<<grid, 256, 0, stream>>>(o, o_f32, g, lse, lse2, dvec, rows_pad, Nq, Nq_pad, dh);
+    else
+        attn_bwd_prep_kernel<32><<<grid, 256, 0, stream>>>(o, o_f32, g, lse, lse2, dvec, rows_pad, Nq, Nq_pad, dh);
+    return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
 template <int D, bool OUT_F32>
@@ -977,10 +1018,9 @@ attn_status_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const C
         attr_set[dev.device] = 1;
     }
     const long long rows_pad = (long long)p.B * p.Hq * p.Nq_pad;
-    attn_bwd_prep_kernel<D><<<(unsigned)((rows_pad + 7) / 8), 256, 0, stream>>>(
-        o, o_f32, static_cast<const __nv_bfloat16*>(dout), lse, lse2, dvec, rows_pad, p.Nq, p.Nq_pad,
-        p.d_act);
-    if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
+    attn_status_t st = launch_bwd_prep(o, o_f32, dout, lse, lse2, dvec, rows_pad, p.Nq, p.Nq_pad,
+                                       p.d_act, stream);
+    if (st != ATTN_OK) return st;
     const long long kv_ctas = (long long)p.B * p.Hkv * p.n_kt;
     attn_bwd_dkdv_kernel<D, OUT_F32><<<(unsigned)kv_ctas, kBwdThreads, BwdCfg<D>::kSmemBytes, stream>>>(
         tq, tk, tv, tdo, p, dev.err_word);
@@ -1725,10 +1765,9 @@ attn_status_t launch_bwd_wide_t(const CUtensorMap& tq, const CUtensorMap& tk, co
         attr_set[dev.device] = 1;
     }
     const long long rows_pad = (long long)p.B * p.Hq * p.Nq_pad;
-    attn_bwd_prep_kernel<kWD><<<(unsigned)((rows_pad + 7) / 8), 256, 0, stream>>>(
-        o, o_f32, static_cast<const __nv_bfloat16*>(dout), lse, lse2, dvec, rows_pad, p.Nq, p.Nq_pad,
-        p.d_act);
-    if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
+    attn_status_t st = launch_bwd_prep(o, o_f32, dout, lse, lse2, dvec, rows_pad, p.Nq, p.Nq_pad,
+                                       p.d_act, stream);
+    if (st != ATTN_OK) return st;
     const long long kv_ctas = 2ll * p.B * p.Hkv * p.n_kt;  // two column halves per key tile
     attn_bwd_wide_dkdv_kernel<OUT_F32><<<(unsigned)kv_ctas, kBwdThreads, WideDkdvCfg::kSmemBytes, stream>>>(
         tq64, tdo64, tk, tv, p, dev.err_word);
