@@ -4,14 +4,19 @@
 // The 128-column forward keeps two 128-row Q tiles in flight per CTA, each with
 // a 128-column S and a d-column O in tensor memory; at d > 128 two O
 // accumulators no longer fit next to their S tiles in the 512 TMEM columns.
-// This kernel keeps one Q tile per CTA and overlaps the other way: K/V tiles
-// of 64 keys, and two S buffers of 64 columns, so S(j+1) is computed while the
-// softmax warps work on S(j) (TMEM: S0 [0,64), S1 [64,128), O [128, 128+D)).
-// Per 64-key tile the tensor cores do 2 * 128 * 64 * D * 2 FLOPs, which at
-// D = 256 outweighs the softmax work of the tile.
+// This kernel keeps one Q tile per CTA and overlaps the other way: two S
+// buffers of 128 keys, so S(j+1) is computed while the softmax warps work on
+// S(j) (TMEM: O [0, D), S0 [256, 384), S1 [384, 512)).  Per 128-key tile the
+// tensor cores do 2 * 128 * 128 * D * 2 FLOPs, which at D = 256 outweighs the
+// softmax work of the tile; with N = 128 keys the S product reads its operands
+// from shared memory at the tensor cores' full rate (N = 64 would not).
+// K and V reach shared memory through one ring of 32 KiB slots, filled in the
+// order the MMAs consume them: K_j as two column chunks (d 0-127 and 128-D,
+// 128 keys each) and V_j as two 64-key halves.  A K/V tile pair of 128 keys at
+// D = 256 is 128 KiB, so whole tiles could not be double-buffered next to Q.
 //
-// Roles (8 warps): warp 0 TMA producer (Q once per unit, K and V through
-// 2-slot rings of their own), warp 1 MMA issuer and TMEM owner, warps 2-3 idle,
+// Roles (8 warps): warp 0 TMA producer (Q once per unit, K and V chunks
+// through the ring), warp 1 MMA issuer and TMEM owner, warps 2-3 idle,
 // warps 4-7 softmax (one query row per thread) and epilogue.  Persistent CTAs
 // take units (b, query head, 128-row Q tile) from a device-side queue in the
 // order of fwd_sched.h (L2 sections; causal longest-first).
@@ -41,7 +46,10 @@ namespace {
 
 constexpr int kWThreads = 256;
 constexpr int kWM = 128;   // query rows per Q tile
-constexpr int kWN = 64;    // keys per K/V tile
+constexpr int kWN = 128;   // keys per K/V tile (and S buffer)
+constexpr int kWV = 64;    // keys per V chunk
+constexpr int kWSlots = 5;                // ring slots
+constexpr int kWSlotBytes = 32768;
 constexpr float kWTau = 8.0f;
 constexpr float kWLn2 = 0.69314718055994530942f;
 constexpr float kWLog2e = 1.44269504088896340736f;
@@ -50,13 +58,20 @@ constexpr uint32_t kWNegInf = 0xFF800000u;
 template <int D>
 struct WideCfg {
     static constexpr int kQBytes = kWM * D * 2;     // D / 64 chunks of 128 rows x 128 B
-    static constexpr int kKVBytes = kWN * D * 2;    // D / 64 chunks of 64 rows x 128 B
-    static constexpr int kKRing = kQBytes;          // 2 slots
-    static constexpr int kVRing = kKRing + 2 * kKVBytes;  // 2 slots
-    static constexpr int kBar = kVRing + 2 * kKVBytes;
+    // ring entries: K chunk c (128 keys x columns [128 c, min(128 c + 128, D)),
+    // 64-column pieces of 128 rows x 128 B) and V half h (64 keys x D, 64-column
+    // pieces of 64 rows x 128 B)
+    static __host__ __device__ constexpr int kKChunkBytes(int c) { return kWN * (D - 128 * c < 128 ? D - 128 * c : 128) * 2; }
+    static constexpr int kVHalfBytes = kWV * D * 2;
+    static constexpr int kRing = kQBytes;
+    static constexpr int kBar = kRing + kWSlots * kWSlotBytes;
     static constexpr int kSmemBytes = kBar + 512 + 1024;
     static_assert(kSmemBytes <= 232448, "shared memory budget");
-    static constexpr uint32_t kColO = 128;
+    static_assert(kKChunkBytes(0) <= kWSlotBytes && kKChunkBytes(1) <= kWSlotBytes &&
+                  kVHalfBytes <= kWSlotBytes, "ring slot size");
+    static_assert(D > 128 && D <= 256, "two K column chunks");
+    static constexpr uint32_t kColO = 0;
+    static __host__ __device__ constexpr uint32_t col_s(int b) { return 256u + 128u * (uint32_t)b; }
 };
 
 __host__ __device__ constexpr int wide_epi_cols(bool f32) { return f32 ? 16 : 32; }
@@ -78,7 +93,7 @@ struct WItem {
 
 struct __align__(8) WideBars {
     uint64_t q_full, q_empty;
-    uint64_t k_full[2], k_empty[2], v_full[2], v_empty[2];
+    uint64_t ring_full[kWSlots], ring_empty[kWSlots];
     uint64_t s_full[2], p_full[2], pv_done, o_full;
     uint64_t unit_full[2], unit_empty[2];
     uint64_t drain;
@@ -90,7 +105,7 @@ static_assert(sizeof(WideBars) <= 512, "barrier block");
 
 constexpr int kWConsumers = 5;  // MMA warp + 4 softmax warps
 
-// KV tiles of 64 keys that Q tile mt (rows [128 mt, 128 mt + 128)) needs.
+// KV tiles of 128 keys that Q tile mt (rows [128 mt, 128 mt + 128)) needs.
 __device__ __forceinline__ int wide_kv_tiles(const FwdShape& s, int mt) {
     const int r0 = mt * kWM;
     int rows = s.Nq - r0;
@@ -126,8 +141,8 @@ __device__ void wide_producer(const CUtensorMap* tq, const CUtensorMap* tk, cons
     const bool leader = elect_one();
     const int leader_lane = __ffs(__ballot_sync(0xFFFFFFFFu, leader)) - 1;
     unsigned int* queue = g_wide_queue[p.slot];
-    int nq = 0;           // Q loads issued
-    long long nk = 0, nv = 0;  // K and V loads issued
+    int nq = 0;         // Q loads issued
+    long long L = 0;    // ring entries issued
     bool ok = true;
     for (int local = 0; ok; ++local) {
         const uint32_t hs = (uint32_t)local & 1u;
@@ -171,37 +186,51 @@ __device__ void wide_producer(const CUtensorMap* tq, const CUtensorMap* tk, cons
         }
         __syncwarp();
         ++nq;
+        // ring entries in the MMA warp's order: K_0, K_1, then per tile j
+        // V_j and K_{j+2}
+        auto emit_k = [&](int j) {
+            for (int c = 0; c < 2 && ok; ++c) {
+                const int slot = (int)(L % kWSlots);
+                if (L >= kWSlots)
+                    ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&bars->ring_empty[slot]),
+                                                           (uint32_t)((L / kWSlots - 1) & 1), abort_flag));
+                if (!ok) return;
+                if (leader) {
+                    const uint32_t bar = smem_u32(&bars->ring_full[slot]);
+                    mbar_arrive_expect_tx(bar, C::kKChunkBytes(c));
+                    const uint32_t dst = smem_u32(smem + C::kRing + slot * kWSlotBytes);
+                    const int pieces = C::kKChunkBytes(c) / (kWN * 128);
+                    for (int pc = 0; pc < pieces; ++pc)
+                        tma_load_3d(dst + pc * (kWN * 128), tk, bar, 128 * c + 64 * pc, j * kWN, kvh);
+                }
+                __syncwarp();
+                ++L;
+            }
+        };
+        auto emit_v = [&](int j) {
+            for (int h = 0; h < 2 && ok; ++h) {
+                const int slot = (int)(L % kWSlots);
+                if (L >= kWSlots)
+                    ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&bars->ring_empty[slot]),
+                                                           (uint32_t)((L / kWSlots - 1) & 1), abort_flag));
+                if (!ok) return;
+                if (leader) {
+                    const uint32_t bar = smem_u32(&bars->ring_full[slot]);
+                    mbar_arrive_expect_tx(bar, C::kVHalfBytes);
+                    const uint32_t dst = smem_u32(smem + C::kRing + slot * kWSlotBytes);
+#pragma unroll
+                    for (int pc = 0; pc < D / 64; ++pc)
+                        tma_load_3d(dst + pc * (kWV * 128), tv, bar, 64 * pc, j * kWN + kWV * h, kvh);
+                }
+                __syncwarp();
+                ++L;
+            }
+        };
+        emit_k(0);
+        if (n > 1) emit_k(1);
         for (int j = 0; j < n && ok; ++j) {
-            const int sk = (int)(nk & 1);
-            if (nk >= 2)
-                ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&bars->k_empty[sk]),
-                                                       (uint32_t)(((nk >> 1) - 1) & 1), abort_flag));
-            if (!ok) break;
-            if (leader) {
-                const uint32_t bar = smem_u32(&bars->k_full[sk]);
-                mbar_arrive_expect_tx(bar, C::kKVBytes);
-                const uint32_t dst = smem_u32(smem + C::kKRing + sk * C::kKVBytes);
-#pragma unroll
-                for (int c = 0; c < D / 64; ++c)
-                    tma_load_3d(dst + c * (kWN * 128), tk, bar, 64 * c, j * kWN, kvh);
-            }
-            __syncwarp();
-            ++nk;
-            const int sv = (int)(nv & 1);
-            if (nv >= 2)
-                ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&bars->v_empty[sv]),
-                                                       (uint32_t)(((nv >> 1) - 1) & 1), abort_flag));
-            if (!ok) break;
-            if (leader) {
-                const uint32_t bar = smem_u32(&bars->v_full[sv]);
-                mbar_arrive_expect_tx(bar, C::kKVBytes);
-                const uint32_t dst = smem_u32(smem + C::kVRing + sv * C::kKVBytes);
-#pragma unroll
-                for (int c = 0; c < D / 64; ++c)
-                    tma_load_3d(dst + c * (kWN * 128), tv, bar, 64 * c, j * kWN, kvh);
-            }
-            __syncwarp();
-            ++nv;
+            emit_v(j);
+            if (j + 2 < n) emit_k(j + 2);
         }
     }
     if (!ok && leader) wide_abort(bars, err);
@@ -214,35 +243,37 @@ __device__ void wide_producer(const CUtensorMap* tq, const CUtensorMap* tk, cons
     }
     // Drain: every issued copy lands before the CTA may exit.
     if (nq > 0) mbar_wait(smem_u32(&bars->q_full), (uint32_t)(nq - 1) & 1u, nullptr);
-    for (int st = 0; st < 2 && st < nk; ++st)
-        mbar_wait(smem_u32(&bars->k_full[st]), (uint32_t)(((nk - st + 1) / 2 - 1) & 1), nullptr);
-    for (int st = 0; st < 2 && st < nv; ++st)
-        mbar_wait(smem_u32(&bars->v_full[st]), (uint32_t)(((nv - st + 1) / 2 - 1) & 1), nullptr);
+    for (int st = 0; st < kWSlots && st < L; ++st) {
+        const long long uses = (L - st + kWSlots - 1) / kWSlots;
+        mbar_wait(smem_u32(&bars->ring_full[st]), (uint32_t)((uses - 1) & 1), nullptr);
+    }
     __syncwarp();
 }
 
 constexpr uint32_t kWDescHi = sdesc_hi_sw128(1024);
 
-// S = Q K_j^T: M = 128, N = 64, K = D (16 per instruction; 64-column chunks
-// 16 KiB apart in Q, 8 KiB apart in K).
+// S = Q K_j^T, k-steps [kk0, kk1) of 16 columns: M = 128, N = 128.  Q is
+// D / 64 pieces of 128 rows x 128 B (16 KiB apart); the K chunk holding
+// columns [128 c, 128 c + 128) is two such pieces of its own.
 template <int D>
-__device__ __forceinline__ void wide_issue_s(uint32_t d_tmem, uint32_t q_lo, uint32_t k_lo,
-                                             uint32_t idesc) {
+__device__ __forceinline__ void wide_issue_s(uint32_t d_tmem, uint32_t q_lo, uint32_t k_lo, int kk0,
+                                             int kk1, uint32_t idesc) {
 #pragma unroll
-    for (int kk = 0; kk < D / 16; ++kk) {
+    for (int kk = kk0; kk < kk1; ++kk) {
         const uint32_t in = (kk & 3) * (32 >> 4);
         mma_ss_warp(d_tmem, sdesc_join(q_lo + (kk >> 2) * ((kWM * 128) >> 4) + in, kWDescHi),
-                    sdesc_join(k_lo + (kk >> 2) * ((kWN * 128) >> 4) + in, kWDescHi), idesc,
+                    sdesc_join(k_lo + ((kk >> 2) & 1) * ((kWN * 128) >> 4) + in, kWDescHi), idesc,
                     kk > 0 ? 1u : 0u);
     }
 }
 
-// O += P V_j: A = P (bf16 pairs in TMEM, 8 columns per 16 keys), B = V_j
-// MN-major (LBO 8 KiB between 64-column chunks, 16 keys = 16 rows of 128 B).
+// O += P V for one 64-key half of V_j: A = P (bf16 pairs in TMEM, 8 columns
+// per 16 keys), B = the half MN-major (LBO 8 KiB between 64-column pieces,
+// 16 keys = 16 rows of 128 B).
 __device__ __forceinline__ void wide_issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_lo,
                                               uint32_t idesc, bool accumulate) {
 #pragma unroll
-    for (int kk = 0; kk < kWN / 16; ++kk)
+    for (int kk = 0; kk < kWV / 16; ++kk)
         mma_ts_warp(d_tmem, p_tmem + kk * 8, sdesc_join(v_lo + kk * (2048 >> 4), kWDescHi), idesc,
                     (accumulate || kk > 0) ? 1u : 0u);
 }
@@ -255,26 +286,36 @@ __device__ void wide_mma(uint8_t* smem, WideBars* bars, uint32_t tmem, unsigned 
     const uint32_t idS = make_idesc_bf16(kWM, kWN, 0, 0);
     const uint32_t idO = make_idesc_bf16(kWM, D, 0, 1);
     const uint32_t q_lo = sdesc_lo(smem_u32(smem), 16);
-    auto k_lo = [&](int st) { return sdesc_lo(smem_u32(smem + C::kKRing + st * C::kKVBytes), 16); };
+    auto k_lo = [&](int st) { return sdesc_lo(smem_u32(smem + C::kRing + st * kWSlotBytes), 16); };
     auto v_lo = [&](int st) {
-        return sdesc_lo(smem_u32(smem + C::kVRing + st * C::kKVBytes), kWN * 128);
+        return sdesc_lo(smem_u32(smem + C::kRing + st * kWSlotBytes), kWV * 128);
     };
     auto wait_all = [&](uint32_t bar, uint32_t parity, int polls) {
         return __all_sync(0xFFFFFFFFu, mbar_wait(bar, parity, abort_flag, polls));
     };
-    long long g = 0;           // tiles of all units so far: tile g uses S buffer g & 1
-    long long nk = 0, nv = 0;  // K and V tiles consumed
+    long long g = 0;   // tiles of all units so far: tile g uses S buffer g & 1
+    long long L = 0;   // ring entries consumed
     bool ok = true;
-    // S for global tile gg into buffer gg & 1 (K from the K ring).
-    auto issue_s = [&](long long gg, bool last_s) {
-        const int sk = (int)(nk & 1);
-        if (!wait_all(smem_u32(&bars->k_full[sk]), (uint32_t)((nk >> 1) & 1), 0)) return false;
+    // The next ring entry, once it has landed.
+    auto take = [&](int& slot) {
+        slot = (int)(L % kWSlots);
+        if (!wait_all(smem_u32(&bars->ring_full[slot]), (uint32_t)((L / kWSlots) & 1), 0)) return false;
         tc_fence_after();
-        wide_issue_s<D>(tmem + (uint32_t)(gg & 1) * kWN, q_lo, k_lo(sk), idS);
+        ++L;
+        return true;
+    };
+    // S for global tile gg into buffer gg & 1 (K_j's two column chunks).
+    auto issue_s = [&](long long gg, bool last_s) {
+        const uint32_t dS = tmem + C::col_s((int)(gg & 1));
+        int slot;
+        if (!take(slot)) return false;
+        wide_issue_s<D>(dS, q_lo, k_lo(slot), 0, 8, idS);
+        mma_commit_warp(smem_u32(&bars->ring_empty[slot]));
+        if (!take(slot)) return false;
+        wide_issue_s<D>(dS, q_lo, k_lo(slot), 8, D / 16, idS);
+        mma_commit_warp(smem_u32(&bars->ring_empty[slot]));
         mma_commit_warp(smem_u32(&bars->s_full[gg & 1]));
-        mma_commit_warp(smem_u32(&bars->k_empty[sk]));
         if (last_s) mma_commit_warp(smem_u32(&bars->q_empty));
-        ++nk;
         return true;
     };
     for (int local = 0; ok; ++local) {
@@ -290,14 +331,16 @@ __device__ void wide_mma(uint8_t* smem, WideBars* bars, uint32_t tmem, unsigned 
             const int b = (int)(g & 1);
             ok = wait_all(smem_u32(&bars->p_full[b]), (uint32_t)((g >> 1) & 1), 32);
             if (!ok) break;
-            const int sv = (int)(nv & 1);
-            ok = wait_all(smem_u32(&bars->v_full[sv]), (uint32_t)((nv >> 1) & 1), 0);
+            for (int h = 0; h < 2 && ok; ++h) {
+                int slot;
+                ok = take(slot);
+                if (!ok) break;
+                wide_issue_pv(tmem + C::kColO, tmem + C::col_s(b) + (uint32_t)(h * 32), v_lo(slot), idO,
+                              j > 0 || h > 0);
+                mma_commit_warp(smem_u32(&bars->ring_empty[slot]));
+            }
             if (!ok) break;
-            tc_fence_after();
-            wide_issue_pv(tmem + C::kColO, tmem + (uint32_t)b * kWN, v_lo(sv), idO, j > 0);
             mma_commit_warp(smem_u32(&bars->pv_done));
-            mma_commit_warp(smem_u32(&bars->v_empty[sv]));
-            ++nv;
             if (j + 2 < n) {
                 ok = issue_s(g + 2, j + 3 == n);
                 if (!ok) break;
@@ -311,23 +354,23 @@ __device__ void wide_mma(uint8_t* smem, WideBars* bars, uint32_t tmem, unsigned 
     __syncwarp();
 }
 
-// One 64-key tile of the online softmax for this thread's row (see the 128-
+// One 128-key tile of the online softmax for this thread's row (see the 128-
 // column forward): mask, tile max, conditional rescale of O (after the
 // previous P.V product has completed), P = 2^(s c - m) to TMEM as bf16 pairs,
 // and the two row sums.
 template <int D, bool MASKED>
-__device__ __forceinline__ void wide_softmax_tile(uint32_t (&sr)[64], int lim, bool first, float c,
+__device__ __forceinline__ void wide_softmax_tile(uint32_t (&sr)[kWN], int lim, bool first, float c,
                                                   uint32_t tP, uint32_t tO, float& m, float& l,
                                                   float& lx, WideBars* bars, long long g,
                                                   const volatile int* abort_flag, bool& ok) {
     if constexpr (MASKED) {
 #pragma unroll
-        for (int cc = 0; cc < 64; ++cc)
+        for (int cc = 0; cc < kWN; ++cc)
             if (cc > lim) sr[cc] = kWNegInf;
     }
     float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
 #pragma unroll
-    for (int cc = 0; cc < 64; cc += 8) {
+    for (int cc = 0; cc < kWN; cc += 8) {
         mx0 = fmax3(mx0, __uint_as_float(sr[cc]), __uint_as_float(sr[cc + 1]));
         mx1 = fmax3(mx1, __uint_as_float(sr[cc + 2]), __uint_as_float(sr[cc + 3]));
         mx2 = fmax3(mx2, __uint_as_float(sr[cc + 4]), __uint_as_float(sr[cc + 5]));
@@ -372,7 +415,7 @@ __device__ __forceinline__ void wide_softmax_tile(uint32_t (&sr)[64], int lim, b
     const uint64_t c2 = f2(c, c), nm2 = f2(-m, -m);
     uint64_t acc0 = 0, acc1 = 0;
 #pragma unroll
-    for (int half = 0; half < 2; ++half) {
+    for (int half = 0; half < kWN / 32; ++half) {
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
@@ -465,14 +508,15 @@ __device__ void wide_softmax(int wq, int lane, uint8_t* smem, WideBars* bars, ui
         float m = -INFINITY, l = 0.f, lx = 0.f;
         for (int j = 0; j < w.n && ok; ++j, ++g) {
             const int b = (int)(g & 1);
-            const uint32_t tS = tmem + (uint32_t)b * kWN + lane_off;
+            const uint32_t tS = tmem + C::col_s(b) + lane_off;
             ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&bars->s_full[b]), (uint32_t)((g >> 1) & 1),
                                                    abort_flag, 32));
             if (!ok) break;
             tc_fence_after();
-            uint32_t sr[64];
-            tmem_ld32(tS, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
-            tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+            uint32_t sr[kWN];
+#pragma unroll
+            for (int cc = 0; cc < kWN; cc += 32)
+                tmem_ld32(tS + cc, *reinterpret_cast<uint32_t(*)[32]>(&sr[cc]));
             tmem_wait_ld();
             const int lim = last_key - j * kWN;
             if (__any_sync(0xFFFFFFFFu, lim < kWN - 1))
@@ -528,11 +572,11 @@ attn_fwd_wide_kernel(const __grid_constant__ CUtensorMap tq, const __grid_consta
     if (threadIdx.x == 0) {
         mbar_init(smem_u32(&bars->q_full), 1);
         mbar_init(smem_u32(&bars->q_empty), 1);
+        for (int i = 0; i < kWSlots; ++i) {
+            mbar_init(smem_u32(&bars->ring_full[i]), 1);
+            mbar_init(smem_u32(&bars->ring_empty[i]), 1);
+        }
         for (int i = 0; i < 2; ++i) {
-            mbar_init(smem_u32(&bars->k_full[i]), 1);
-            mbar_init(smem_u32(&bars->k_empty[i]), 1);
-            mbar_init(smem_u32(&bars->v_full[i]), 1);
-            mbar_init(smem_u32(&bars->v_empty[i]), 1);
             mbar_init(smem_u32(&bars->s_full[i]), 1);
             mbar_init(smem_u32(&bars->p_full[i]), 4);
             mbar_init(smem_u32(&bars->unit_full[i]), 1);
@@ -608,7 +652,7 @@ attn_status_t launch_fwd_wide(const void* q, const void* k, const void* v, void*
     const bool f32 = o_dtype == ATTN_OUT_F32;
     if ((st = encode_tmap_bf16_3d(&tq, q, d, Nq, (long long)B * Hq, kWM)) != ATTN_OK) return st;
     if ((st = encode_tmap_bf16_3d(&tk, k, d, Nk, (long long)B * Hkv, kWN)) != ATTN_OK) return st;
-    if ((st = encode_tmap_bf16_3d(&tv, v, d, Nk, (long long)B * Hkv, kWN)) != ATTN_OK) return st;
+    if ((st = encode_tmap_bf16_3d(&tv, v, d, Nk, (long long)B * Hkv, kWV)) != ATTN_OK) return st;
     if ((st = encode_tmap_out_3d(&to, o, f32, d, Nq, (long long)B * Hq, wide_epi_cols(f32), 32)) != ATTN_OK)
         return st;
     if (d <= 192)

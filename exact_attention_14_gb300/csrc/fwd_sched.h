@@ -117,8 +117,8 @@ GB300_HD void unit_of(const FwdShape& s, uint32_t i, int& bh, int& mb);
 // Makespan, in KV steps, of the greedy list schedule of the units (lecture
 // notes 4.5: each of num_sms workers takes the next unit of the list when it
 // is free), a unit costing its KV steps plus kUnitOverheadSteps: for
-// two-tile units the steps of the longer Q tile (128-key steps), for
-// single-tile units (unit_rows 128) the 64-key steps of the d > 128 kernel.
+// two-tile units the steps of the longer Q tile, for single-tile units
+// (unit_rows 128, the d > 128 kernel) the tile's steps (128 keys each).
 inline double list_makespan(const FwdShape& s, int num_sms, int unit_rows) {
     std::vector<double> load((size_t)num_sms, 0.0);  // a min-heap of worker loads
     for (long long i = 0; i < s.units; ++i) {
@@ -131,7 +131,7 @@ inline double list_makespan(const FwdShape& s, int num_sms, int unit_rows) {
         } else {
             const int r0 = mb * kTileM;
             const int rows = s.Nq - r0 < kTileM ? s.Nq - r0 : kTileM;
-            steps = kv_tiles_for_rows(r0, rows, s.Nq, s.Nk, s.causal, 64);
+            steps = kv_tiles_for_rows(r0, rows, s.Nq, s.Nk, s.causal, kTileN);
         }
         std::pop_heap(load.begin(), load.end(), std::greater<double>());
         load.back() += steps + kUnitOverheadSteps;
