@@ -764,7 +764,7 @@ def run_wide(ea, args, dev, stream, flush, peaks):
     sb_nc, sb_c = stats_ms(tb_nc), stats_ms(tb_c)
     fb = [2.5 * f for f in fw]
     tb = [sb_nc["median_ms"] * 1e-3, sb_c["median_ms"] * 1e-3]
-    return {"kernel": "attn_fwd_wide_kernel<256> (one Q tile per CTA, 64-key tiles, two S buffers)",
+    return {"kernel": "attn_fwd_wide_kernel<256> (one Q tile per CTA, two 128-key S buffers, K/V chunks through one ring)",
             "workload": f"prefill B={cfg.B} H={cfg.Hq} N={cfg.N} d=256",
             "noncausal_tflops": fw[0] / tw[0] / 1e12, "causal_tflops": fw[1] / tw[1] / 1e12,
             "noncausal": s_nc, "causal": s_c,

@@ -90,7 +90,7 @@ typedef enum {
  *
  * Supported: 8 <= d <= 256 with d % 8 == 0: d <= 128 runs on the 64- or
  *            128-column kernel (two 128-row Q tiles per CTA), 128 < d <= 256
- *            on the 192- or 256-column kernel (one Q tile per CTA, 64-key
+ *            on the 192- or 256-column kernel (one Q tile per CTA, 128-key
  *            K/V tiles, no tail split); other d are padded to the next of
  *            these with the columns past d read as zero and never written.
  *            Hq % Hkv == 0; 1 <= Nq, Nk <= 2^24; B*Hq and B*Hkv <= 2^24.
