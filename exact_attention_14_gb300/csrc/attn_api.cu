@@ -377,9 +377,13 @@ attn_status_t attn_fwd_varlen(const void* q, const void* k, const void* v, void*
                                  scale, o_dtype);
     if (st != ATTN_OK) return st;
     if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
-    if (!head_dim_supported(d)) return ATTN_ERR_UNSUPPORTED;
+    if (!fwd_head_dim_supported(d)) return ATTN_ERR_UNSUPPORTED;
     DeviceInfo dev;
     if ((st = current_device_info(&dev)) != ATTN_OK) return st;
+    if (d > 128)
+        return launch_fwd_wide_varlen(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, B, Hq, Hkv,
+                                      total_q, total_k, max_seqlen_q, max_seqlen_k, d, causal,
+                                      scale, o_dtype, static_cast<cudaStream_t>(stream), dev);
     return launch_fwd_varlen(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, B, Hq, Hkv, total_q,
                              total_k, max_seqlen_q, max_seqlen_k, d, causal, scale, o_dtype,
                              static_cast<cudaStream_t>(stream), dev);

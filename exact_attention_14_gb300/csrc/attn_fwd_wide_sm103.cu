@@ -81,7 +81,11 @@ struct WideParams {
     int group, off, d_act;
     float c;          // scale * log2(e)
     uint32_t slot;
-    void* o;          // O: [B, Hq, Nq, d_act]
+    void* o;          // O: [B, Hq, Nq, d_act], or [total_q, Hq, d_act] for packed batches
+    // packed batches: Nq / Nk in shape are the longest sequence's lengths
+    const int* cu_q;  // [B + 1] row offsets in the packed Q / O
+    const int* cu_k;  // [B + 1] row offsets in the packed K / V
+    int total_q, total_k;
 };
 
 constexpr uint32_t kWideQueueSlots = 256;
@@ -89,6 +93,7 @@ __device__ unsigned int g_wide_queue[kWideQueueSlots][2];  // ticket counter, ex
 
 struct WItem {
     int bh, mt, n;
+    int q0, nq, nk;  // packed batches: the sequence's first row and lengths
 };
 
 struct __align__(8) WideBars {
@@ -122,6 +127,9 @@ __device__ __forceinline__ bool take_witem(WideBars* bars, uint32_t k, WItem& w,
     w.bh = src->bh;
     w.mt = src->mt;
     w.n = src->n;
+    w.q0 = src->q0;
+    w.nq = src->nq;
+    w.nk = src->nk;
     __syncwarp();
     if ((threadIdx.x & 31) == 0) mbar_arrive(smem_u32(&bars->unit_empty[i]));
     return true;
@@ -132,7 +140,24 @@ __device__ __forceinline__ void wide_abort(WideBars* bars, unsigned int* err) {
     *((volatile int*)&bars->abort) = 1;
 }
 
-template <int D>
+// Sequence b of a packed batch: its first rows and lengths (the checks of the
+// 128-column forward's packed path).  False, and the error bit from the
+// leader, when its offsets leave the arrays, decrease, or give a length above
+// the launch's maximum, a query row without keys, or, causal, more queries
+// than keys; such a sequence is not computed.
+__device__ __forceinline__ bool wide_varlen_seq(const WideParams& p, int b, bool leader, int& q0,
+                                                int& nq, int& k0, int& nk, unsigned int* err) {
+    const int qs = __ldg(p.cu_q + b), qe = __ldg(p.cu_q + b + 1);
+    const int ks = __ldg(p.cu_k + b), ke = __ldg(p.cu_k + b + 1);
+    const bool good = 0 <= qs && qs <= qe && qe <= p.total_q && qe - qs <= p.shape.Nq &&
+                      0 <= ks && ks <= ke && ke <= p.total_k && ke - ks <= p.shape.Nk &&
+                      (qe == qs || ke > ks) && (!p.shape.causal || qe - qs <= ke - ks);
+    q0 = qs; nq = qe - qs; k0 = ks; nk = ke - ks;
+    if (!good && leader) atomicOr(err, kErrBadSeqlen);
+    return good;
+}
+
+template <int D, bool VARLEN>
 __device__ void wide_producer(const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv,
                               uint8_t* smem, WideBars* bars, const WideParams& p, unsigned int* err) {
     using C = WideCfg<D>;
@@ -141,7 +166,7 @@ __device__ void wide_producer(const CUtensorMap* tq, const CUtensorMap* tk, cons
     const bool leader = elect_one();
     const int leader_lane = __ffs(__ballot_sync(0xFFFFFFFFu, leader)) - 1;
     unsigned int* queue = g_wide_queue[p.slot];
-    int nq = 0;         // Q loads issued
+    int q_loads = 0;    // Q loads issued
     long long L = 0;    // ring entries issued
     bool ok = true;
     for (int local = 0; ok; ++local) {
@@ -150,42 +175,71 @@ __device__ void wide_producer(const CUtensorMap* tq, const CUtensorMap* tk, cons
             ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&bars->unit_empty[hs]),
                                                    (uint32_t)((local >> 1) - 1) & 1u, abort_flag));
         if (!ok) break;
-        uint32_t u = blockIdx.x;
-        if (local > 0) {
-            if (leader) u = gridDim.x + atomicAdd(&queue[0], 1u);
-            u = __shfl_sync(0xFFFFFFFFu, u, leader_lane);
-        }
-        const bool done = u >= (uint32_t)s.units;
+        // A CTA's first unit is its own index, later ones come from the
+        // counter; packed batches skip the units past their sequence's end.
+        bool done = false;
         int bh = -1, mt = 0, n = 0;
-        if (!done) {
+        int q0 = 0, k0 = 0, nq = s.Nq, nk = s.Nk;
+        while (true) {
+            uint32_t u = blockIdx.x;
+            if (local > 0 || (VARLEN && bh >= 0)) {
+                if (leader) u = gridDim.x + atomicAdd(&queue[0], 1u);
+                u = __shfl_sync(0xFFFFFFFFu, u, leader_lane);
+            }
+            done = u >= (uint32_t)s.units;
+            if (done) {
+                bh = -1;
+                break;
+            }
             unit_of(s, u, bh, mt);
-            n = wide_kv_tiles(s, mt);
+            if constexpr (VARLEN) {
+                if (!wide_varlen_seq(p, bh / s.Hq, leader, q0, nq, k0, nk, err)) continue;
+                if (mt * kWM >= nq) continue;
+            }
+            break;
+        }
+        if (!done) {
+            if constexpr (VARLEN) {
+                const int r0 = mt * kWM;
+                n = kv_tiles_for_rows(r0, nq - r0 < kWM ? nq - r0 : kWM, nq, nk, s.causal, kWN);
+            } else {
+                n = wide_kv_tiles(s, mt);
+            }
         }
         if (leader) {
             volatile WItem* dst = &bars->item[hs];
             dst->bh = bh;
             dst->mt = mt;
             dst->n = n;
+            dst->q0 = q0;
+            dst->nq = nq;
+            dst->nk = nk;
             mbar_arrive(smem_u32(&bars->unit_full[hs]));
         }
         __syncwarp();
         if (done) break;
         const int b = bh / s.Hq;
         const int hq = bh - b * s.Hq;
-        const int kvh = b * s.Hkv + hq / p.group;
-        if (nq > 0)
-            ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&bars->q_empty), (uint32_t)(nq - 1) & 1u,
+        // the K/V head: an index into [B * Hkv] dense, into [Hkv] packed
+        const int kvh = VARLEN ? hq / p.group : b * s.Hkv + hq / p.group;
+        if (q_loads > 0)
+            ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&bars->q_empty), (uint32_t)(q_loads - 1) & 1u,
                                                    abort_flag));
         if (!ok) break;
         if (leader) {
             const uint32_t bar = smem_u32(&bars->q_full);
             mbar_arrive_expect_tx(bar, C::kQBytes);
 #pragma unroll
-            for (int c = 0; c < D / 64; ++c)
-                tma_load_3d(smem_u32(smem) + c * (kWM * 128), tq, bar, 64 * c, mt * kWM, bh);
+            for (int c = 0; c < D / 64; ++c) {
+                if constexpr (VARLEN)
+                    tma_load_5d(smem_u32(smem) + c * (kWM * 128), tq, bar, 64 * c, hq,
+                                kRaggedWindow - nq + mt * kWM, q0 + nq, kRaggedWindow);
+                else
+                    tma_load_3d(smem_u32(smem) + c * (kWM * 128), tq, bar, 64 * c, mt * kWM, bh);
+            }
         }
         __syncwarp();
-        ++nq;
+        ++q_loads;
         // ring entries in the MMA warp's order: K_0, K_1, then per tile j
         // V_j and K_{j+2}
         auto emit_k = [&](int j) {
@@ -200,8 +254,13 @@ __device__ void wide_producer(const CUtensorMap* tq, const CUtensorMap* tk, cons
                     mbar_arrive_expect_tx(bar, C::kKChunkBytes(c));
                     const uint32_t dst = smem_u32(smem + C::kRing + slot * kWSlotBytes);
                     const int pieces = C::kKChunkBytes(c) / (kWN * 128);
-                    for (int pc = 0; pc < pieces; ++pc)
-                        tma_load_3d(dst + pc * (kWN * 128), tk, bar, 128 * c + 64 * pc, j * kWN, kvh);
+                    for (int pc = 0; pc < pieces; ++pc) {
+                        if constexpr (VARLEN)
+                            tma_load_5d(dst + pc * (kWN * 128), tk, bar, 128 * c + 64 * pc, kvh,
+                                        kRaggedWindow - nk + j * kWN, k0 + nk, kRaggedWindow);
+                        else
+                            tma_load_3d(dst + pc * (kWN * 128), tk, bar, 128 * c + 64 * pc, j * kWN, kvh);
+                    }
                 }
                 __syncwarp();
                 ++L;
@@ -219,8 +278,13 @@ __device__ void wide_producer(const CUtensorMap* tq, const CUtensorMap* tk, cons
                     mbar_arrive_expect_tx(bar, C::kVHalfBytes);
                     const uint32_t dst = smem_u32(smem + C::kRing + slot * kWSlotBytes);
 #pragma unroll
-                    for (int pc = 0; pc < D / 64; ++pc)
-                        tma_load_3d(dst + pc * (kWV * 128), tv, bar, 64 * pc, j * kWN + kWV * h, kvh);
+                    for (int pc = 0; pc < D / 64; ++pc) {
+                        if constexpr (VARLEN)
+                            tma_load_5d(dst + pc * (kWV * 128), tv, bar, 64 * pc, kvh,
+                                        kRaggedWindow - nk + j * kWN + kWV * h, k0 + nk, kRaggedWindow);
+                        else
+                            tma_load_3d(dst + pc * (kWV * 128), tv, bar, 64 * pc, j * kWN + kWV * h, kvh);
+                    }
                 }
                 __syncwarp();
                 ++L;
@@ -242,7 +306,7 @@ __device__ void wide_producer(const CUtensorMap* tq, const CUtensorMap* tk, cons
         }
     }
     // Drain: every issued copy lands before the CTA may exit.
-    if (nq > 0) mbar_wait(smem_u32(&bars->q_full), (uint32_t)(nq - 1) & 1u, nullptr);
+    if (q_loads > 0) mbar_wait(smem_u32(&bars->q_full), (uint32_t)(q_loads - 1) & 1u, nullptr);
     for (int st = 0; st < kWSlots && st < L; ++st) {
         const long long uses = (L - st + kWSlots - 1) / kWSlots;
         mbar_wait(smem_u32(&bars->ring_full[st]), (uint32_t)((uses - 1) & 1), nullptr);
@@ -484,7 +548,7 @@ __device__ __forceinline__ void wide_store_pairs(const float (&v)[32], int cc, i
     }
 }
 
-template <int D, bool OUT_F32>
+template <int D, bool OUT_F32, bool VARLEN>
 __device__ void wide_softmax(int wq, int lane, uint8_t* smem, WideBars* bars, uint32_t tmem,
                              const WideParams& p, const CUtensorMap* to, float* __restrict__ lse_ptr,
                              unsigned int* err) {
@@ -500,9 +564,11 @@ __device__ void wide_softmax(int wq, int lane, uint8_t* smem, WideBars* bars, ui
         ok = take_witem(bars, k, w, abort_flag);
         if (!ok || w.bh < 0) break;
         const int row = w.mt * kWM + wq * 32 + lane;
-        int last_key = s.Nk - 1;
+        const int nq = VARLEN ? w.nq : s.Nq;
+        const int nk = VARLEN ? w.nk : s.Nk;
+        int last_key = nk - 1;
         if (s.causal) {
-            const int lk = row + p.off;
+            const int lk = row + (VARLEN ? nk - nq : p.off);
             last_key = lk < last_key ? lk : last_key;
         }
         float m = -INFINITY, l = 0.f, lx = 0.f;
@@ -537,7 +603,12 @@ __device__ void wide_softmax(int wq, int lane, uint8_t* smem, WideBars* bars, ui
         const uint64_t il2 = f2(inv_l, inv_l);
         const int row0 = w.mt * kWM + wq * 32;
         constexpr int kEs = OUT_F32 ? 4 : 2;
-        uint8_t* o_warp = static_cast<uint8_t*>(p.o) + ((size_t)w.bh * s.Nq + (size_t)row0) * p.d_act * kEs;
+        const int hq = w.bh - (w.bh / s.Hq) * s.Hq;
+        // this warp's first row of O and the stride between rows
+        const size_t first = VARLEN ? (size_t)(w.q0 + row0) * s.Hq + (size_t)hq
+                                    : (size_t)w.bh * s.Nq + (size_t)row0;
+        const size_t row_stride = (VARLEN ? (size_t)s.Hq : 1u) * (size_t)p.d_act * kEs;
+        uint8_t* o_warp = static_cast<uint8_t*>(p.o) + first * p.d_act * kEs;
 #pragma unroll 1
         for (int cc = 0; cc < D; cc += 32) {
             uint32_t r[32];
@@ -547,17 +618,19 @@ __device__ void wide_softmax(int wq, int lane, uint8_t* smem, WideBars* bars, ui
 #pragma unroll
             for (int i = 0; i < 32; i += 2)
                 f2_split(f2_mul(f2(__uint_as_float(r[i]), __uint_as_float(r[i + 1])), il2), v[i], v[i + 1]);
-            wide_store_pairs<OUT_F32>(v, cc, lane, o_warp, (size_t)p.d_act * kEs, s.Nq - row0, p.d_act);
+            wide_store_pairs<OUT_F32>(v, cc, lane, o_warp, row_stride, nq - row0, p.d_act);
         }
-        if (row < s.Nq && lse_ptr)
-            lse_ptr[(size_t)w.bh * s.Nq + (size_t)row] = (m + log2f(lx)) * kWLn2;
+        // LSE: [B, Hq, Nq], or [Hq, total_q] for packed batches
+        if (row < nq && lse_ptr)
+            lse_ptr[VARLEN ? (size_t)hq * p.total_q + (size_t)(w.q0 + row)
+                           : (size_t)w.bh * s.Nq + (size_t)row] = (m + log2f(lx)) * kWLn2;
         // (the next unit's P.V overwrites O only after this warpgroup's next
         // P is in TMEM, which follows these loads)
     }
     if (!ok) wide_abort(bars, err);
 }
 
-template <int D, bool OUT_F32>
+template <int D, bool OUT_F32, bool VARLEN>
 __global__ void __launch_bounds__(kWThreads, 1)
 attn_fwd_wide_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                      const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap to,
@@ -600,9 +673,10 @@ attn_fwd_wide_kernel(const __grid_constant__ CUtensorMap tq, const __grid_consta
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
-    if (warp == 0) wide_producer<D>(&tq, &tk, &tv, smem, bars, p, err);
+    if (warp == 0) wide_producer<D, VARLEN>(&tq, &tk, &tv, smem, bars, p, err);
     else if (warp == 1) wide_mma<D>(smem, bars, tmem, err);
-    else if (warp >= 4) wide_softmax<D, OUT_F32>(warp & 3, lane, smem, bars, tmem, p, &to, lse_ptr, err);
+    else if (warp >= 4)
+        wide_softmax<D, OUT_F32, VARLEN>(warp & 3, lane, smem, bars, tmem, p, &to, lse_ptr, err);
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
@@ -612,21 +686,26 @@ attn_fwd_wide_kernel(const __grid_constant__ CUtensorMap tq, const __grid_consta
     }
 }
 
-template <int D, bool OUT_F32>
+template <int D, bool OUT_F32, bool VARLEN = false>
 attn_status_t launch_wide_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const CUtensorMap& to, float* lse, const WideParams& p, int grid,
                             cudaStream_t stream, const DeviceInfo& dev) {
     using C = WideCfg<D>;
     static int attr_set[64] = {0};
     if (dev.device < 64 && !attr_set[dev.device]) {
-        if (cudaFuncSetAttribute(attn_fwd_wide_kernel<D, OUT_F32>,
+        if (cudaFuncSetAttribute(attn_fwd_wide_kernel<D, OUT_F32, VARLEN>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) != cudaSuccess)
             return ATTN_ERR_CUDA;
         attr_set[dev.device] = 1;
     }
-    attn_fwd_wide_kernel<D, OUT_F32><<<(unsigned)grid, kWThreads, C::kSmemBytes, stream>>>(
+    attn_fwd_wide_kernel<D, OUT_F32, VARLEN><<<(unsigned)grid, kWThreads, C::kSmemBytes, stream>>>(
         tq, tk, tv, to, lse, p, dev.err_word);
     return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+uint32_t next_wide_queue_slot() {
+    static std::atomic<uint32_t> launches{0};
+    return launches.fetch_add(1u, std::memory_order_relaxed) % kWideQueueSlots;
 }
 
 }  // namespace
@@ -643,8 +722,11 @@ attn_status_t launch_fwd_wide(const void* q, const void* k, const void* v, void*
     p.d_act = d;
     p.c = scale * kWLog2e;
     p.o = o;
-    static std::atomic<uint32_t> launches{0};
-    p.slot = launches.fetch_add(1u, std::memory_order_relaxed) % kWideQueueSlots;
+    p.cu_q = nullptr;
+    p.cu_k = nullptr;
+    p.total_q = 0;
+    p.total_k = 0;
+    p.slot = next_wide_queue_slot();
     const long long units = p.shape.units;
     const int grid = (int)(units < dev.num_sms ? units : dev.num_sms);
     CUtensorMap tq, tk, tv, to;
@@ -660,6 +742,44 @@ attn_status_t launch_fwd_wide(const void* q, const void* k, const void* v, void*
                    : launch_wide_t<192, false>(tq, tk, tv, to, lse, p, grid, stream, dev);
     return f32 ? launch_wide_t<256, true>(tq, tk, tv, to, lse, p, grid, stream, dev)
                : launch_wide_t<256, false>(tq, tk, tv, to, lse, p, grid, stream, dev);
+}
+
+attn_status_t launch_fwd_wide_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                                     const int* cu_q, const int* cu_k, int B, int Hq, int Hkv,
+                                     int total_q, int total_k, int max_q, int max_k, int d,
+                                     int causal, float scale, attn_out_dtype_t o_dtype,
+                                     cudaStream_t stream, const DeviceInfo& dev) {
+    WideParams p;
+    // units cover every sequence at the maximum lengths; the producer skips
+    // the Q tiles past each sequence's own length
+    p.shape = make_fwd_shape(B, Hq, Hkv, max_q, max_k, d, causal, 0, kWM);
+    if (p.shape.units >= (1ll << 31)) return ATTN_ERR_UNSUPPORTED;
+    p.group = Hq / Hkv;
+    p.off = 0;
+    p.d_act = d;
+    p.c = scale * kWLog2e;
+    p.o = o;
+    p.cu_q = cu_q;
+    p.cu_k = cu_k;
+    p.total_q = total_q;
+    p.total_k = total_k;
+    p.slot = next_wide_queue_slot();
+    const long long units = p.shape.units;
+    const int grid = (int)(units < dev.num_sms ? units : dev.num_sms);
+    CUtensorMap tq, tk, tv, to;
+    attn_status_t st;
+    const bool f32 = o_dtype == ATTN_OUT_F32;
+    if ((st = encode_tmap_ragged(&tq, q, false, d, Hq, 64, kWM, true)) != ATTN_OK) return st;
+    if ((st = encode_tmap_ragged(&tk, k, false, d, Hkv, 64, kWN, true)) != ATTN_OK) return st;
+    if ((st = encode_tmap_ragged(&tv, v, false, d, Hkv, 64, kWV, true)) != ATTN_OK) return st;
+    // (O is written from registers, never by this map; it is still encoded,
+    // which checks O's alignment like the other maps)
+    if ((st = encode_tmap_ragged(&to, o, f32, d, Hq, wide_epi_cols(f32), 32, false)) != ATTN_OK) return st;
+    if (d <= 192)
+        return f32 ? launch_wide_t<192, true, true>(tq, tk, tv, to, lse, p, grid, stream, dev)
+                   : launch_wide_t<192, false, true>(tq, tk, tv, to, lse, p, grid, stream, dev);
+    return f32 ? launch_wide_t<256, true, true>(tq, tk, tv, to, lse, p, grid, stream, dev)
+               : launch_wide_t<256, false, true>(tq, tk, tv, to, lse, p, grid, stream, dev);
 }
 
 }  // namespace gb300

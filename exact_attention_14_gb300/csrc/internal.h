@@ -94,6 +94,12 @@ attn_status_t launch_fwd_varlen(const void* q, const void* k, const void* v, voi
                                 int total_q, int total_k, int max_q, int max_k, int d, int causal,
                                 float scale, attn_out_dtype_t o_dtype, cudaStream_t stream,
                                 const DeviceInfo& dev);
+// The same for 128 < d <= 256.
+attn_status_t launch_fwd_wide_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                                     const int* cu_q, const int* cu_k, int B, int Hq, int Hkv,
+                                     int total_q, int total_k, int max_q, int max_k, int d,
+                                     int causal, float scale, attn_out_dtype_t o_dtype,
+                                     cudaStream_t stream, const DeviceInfo& dev);
 
 // Backward: workspace bytes (fp32 dQ accumulator, lse2, D; padded rows).
 size_t bwd_workspace_bytes(int B, int Hq, int Nq, int d);

@@ -142,7 +142,8 @@ size_t attn_fwd_workspace_size(int B, int Hq, int Hkv, int Nq, int Nk, int d, in
  *        neither read nor written)
  *   max_seqlen_q, max_seqlen_k  upper bounds of the lengths (host ints)
  *
- * Supported as attn_fwd but with 8 <= d <= 128 (d % 8 == 0); 1 <= total_q,
+ * Supported as attn_fwd (8 <= d <= 256, d % 8 == 0; d > 128 on the 192- or
+ * 256-column kernel); 1 <= total_q,
  * total_k <= 2^30; max lengths in [1, 2^24].  The lengths live on the device, so their checks run there: a
  * sequence whose offsets leave [0, total], decrease, exceed the maximum
  * length, give query rows without keys, or (causal) more queries than keys

@@ -51,6 +51,74 @@ def test_varlen_parity(d, causal):
     assert_close(o[r], lse[:, r], ro[r], rl[:, r], f"d={d} causal={causal}")
 
 
+@pytest.mark.parametrize("d", [192, 256, 136])
+@pytest.mark.parametrize("causal", [False, True])
+def test_varlen_wide_head_dims(d, causal):
+    """Head dims above 128 (the 192- and 256-column kernels, 128-key tiles):
+    empty, single-row and ragged sequences, GQA, against the oracle."""
+    q, k, v, cu_q, cu_k = make_varlen_inputs(LENS, LENS, 8, 2, d, seed=850 + d)
+    scale = 1 / math.sqrt(d)
+    o, lse = gpu_varlen(q, k, v, cu_q, cu_k, causal, scale)
+    ro, rl = oracle.attention_varlen(q, k, v, cu_q, cu_k, causal=causal, scale=scale)
+    r = _rows(cu_q)
+    assert_close(o[r], lse[:, r], ro[r], rl[:, r], f"d={d} causal={causal}")
+
+
+def test_varlen_wide_cross_lengths_and_neighbours():
+    """d = 256 with queries and keys of different lengths (bottom-right causal),
+    NaN / inf in one sequence's keys, and rows past the last sequence that are
+    never written."""
+    lq = [100, 300, 1, 257]
+    lk = [400, 300, 700, 260]
+    q, k, v, cu_q, cu_k = make_varlen_inputs(lq, lk, 4, 4, 256, seed=852, extra_rows=40)
+    for causal in (False, True):
+        o, lse = gpu_varlen(q, k, v, cu_q, cu_k, causal)
+        ro, rl = oracle.attention_varlen(q, k, v, cu_q, cu_k, causal=causal)
+        n = int(cu_q[-1])
+        assert_close(o[:n], lse[:, :n], ro[:n], rl[:, :n], f"cross lengths causal={causal}")
+        assert np.isnan(o[n:]).all() and np.isnan(lse[:, n:]).all()
+    k2, v2 = k.clone(), v.clone()
+    k2[400:700] = float("nan")
+    v2[400:700] = float("inf")
+    o1, l1 = gpu_varlen(q, k, v, cu_q, cu_k, False)
+    o2, l2 = gpu_varlen(q, k2, v2, cu_q, cu_k, False)
+    for rows in (slice(0, 100), slice(400, 658)):
+        assert np.array_equal(o1[rows], o2[rows]) and np.array_equal(l1[:, rows], l2[:, rows])
+
+
+def test_varlen_wide_equal_lengths_bit_identical_to_dense():
+    """All sequences of one length at d = 256: the dense 256-column kernel's
+    tiles and arithmetic in the packed layout."""
+    B, H, N, d = 2, 4, 500, 256
+    q, k, v, cu_q, cu_k = make_varlen_inputs([N] * B, [N] * B, H, H, d, seed=853)
+    o, lse = gpu_varlen(q, k, v, cu_q, cu_k, True)
+    qd = q.reshape(B, N, H, d).permute(0, 2, 1, 3).contiguous().cuda()
+    kd = k.reshape(B, N, H, d).permute(0, 2, 1, 3).contiguous().cuda()
+    vd = v.reshape(B, N, H, d).permute(0, 2, 1, 3).contiguous().cuda()
+    od, ld = ea.forward(qd, kd, vd, causal=True, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    od = od.permute(0, 2, 1, 3).reshape(B * N, H, d).cpu().double().numpy()
+    ld = ld.permute(1, 0, 2).reshape(H, B * N).cpu().double().numpy()
+    assert np.array_equal(o, od) and np.array_equal(lse, ld)
+
+
+def test_varlen_wide_bad_offsets_reported_and_skipped():
+    """d = 192: a sequence longer than max_seqlen is not computed, the device
+    error word reports it, the other sequences are exact."""
+    lens = [64, 236, 64]
+    q, k, v, cu_q, cu_k = make_varlen_inputs(lens, lens, 2, 2, 192, seed=854)
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    o = torch.full(q.shape, 7.0, dtype=torch.float32).cuda()
+    ea.attn_fwd_varlen(qd, kd, vd, o, cu_q.cuda(), cu_k.cuda(), 200, 236, None, causal=False)
+    torch.cuda.synchronize()
+    assert ea.attn_last_device_error() == ea.ATTN_ERR_INVALID_ARG
+    o = o.cpu().double().numpy()
+    assert (o[64:300] == 7.0).all()
+    ro, rl = oracle.attention_varlen(q, k, v, cu_q, cu_k, causal=False)
+    for rows in (slice(0, 64), slice(300, 364)):
+        assert np.abs(o[rows] - ro[rows]).max() <= 1e-2
+
+
 def test_varlen_keys_differ_from_queries():
     """Cross lengths: non-causal any Nq/Nk; causal needs Nq <= Nk (bottom-right)."""
     lq = [100, 300, 1, 512, 129]
@@ -131,8 +199,9 @@ def test_varlen_bad_offsets_reported_and_skipped():
     assert np.isnan(o2[64:300]).all()
 
 
-def test_varlen_repeatable_and_graph_capture():
-    q, k, v, cu_q, cu_k = make_varlen_inputs(LENS, LENS, 8, 2, 128, seed=818)
+@pytest.mark.parametrize("d", [128, 256])
+def test_varlen_repeatable_and_graph_capture(d):
+    q, k, v, cu_q, cu_k = make_varlen_inputs(LENS, LENS, 8, 2, d, seed=818)
     qd, kd, vd, cq, ck = q.cuda(), k.cuda(), v.cuda(), cu_q.cuda(), cu_k.cuda()
     o = torch.empty(q.shape, dtype=torch.bfloat16, device="cuda")
     lse = torch.empty((8, q.shape[0]), dtype=torch.float32, device="cuda")

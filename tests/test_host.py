@@ -394,7 +394,7 @@ def fwd_varlen(lib, **kw):
     (dict(tq=0), 1), (dict(tk=0), 1), (dict(tq=(1 << 30) + 1), 1), (dict(mq=301), 1),
     (dict(mk=301), 1), (dict(mq=0), 1), (dict(B=0), 1), (dict(Hq=3, Hkv=2), 1),
     (dict(causal=2), 1), (dict(scale=-1.0), 1), (dict(odt=5), 1), (dict(d=100), 2),
-    (dict(d=256), 2),
+    (dict(d=264), 2), (dict(d=252), 2),
 ])
 def test_fwd_varlen_argument_checks(lib, kw, code):
     assert fwd_varlen(lib, **kw) == code
