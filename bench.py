@@ -61,7 +61,7 @@ def read_peaks():
 KERNEL_SOURCES = {
     "attn_fwd_kernel": ["attn_fwd_sm103.cu", "fwd_sched.h", "ptx.cuh", "internal.h"],
     "attn_decode_split_kernel": ["attn_decode_sm103.cu", "ptx.cuh", "internal.h"],
-    "attn_bwd": ["attn_bwd_sm103.cu", "ptx.cuh", "internal.h"],
+    "attn_bwd": ["attn_bwd_sm103.cu", "fwd_sched.h", "ptx.cuh", "internal.h"],
     "attn_fp8": ["attn_fp8_sm103.cu", "fwd_sched.h", "ptx.cuh", "internal.h"],
     "attn_fwd_wide": ["attn_fwd_wide_sm103.cu", "fwd_sched.h", "ptx.cuh", "internal.h"],
 }

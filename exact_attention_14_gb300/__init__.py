@@ -24,7 +24,8 @@ __all__ = [
     "attn_decode_workspace_size", "attn_decode_noalloc", "attn_status_string", "attn_last_device_error",
     "attn_decode_num_splits", "attn_list_schedule", "attn_kv_tiles",
     "attn_fwd_num_units", "attn_fwd_schedule", "attn_fwd_split_plan", "attn_decode_kernel_launches",
-    "attn_bwd", "attn_bwd_workspace_size", "backward", "attn_decode_paged", "decode_paged", "forward", "decode", "library_path", "load",
+    "attn_bwd", "attn_bwd_workspace_size", "backward", "attn_bwd_varlen",
+    "attn_bwd_varlen_workspace_size", "backward_varlen", "attn_decode_paged", "decode_paged", "forward", "decode", "library_path", "load",
 ]
 
 ATTN_OK = 0
@@ -69,6 +70,10 @@ SIGNATURES = {
                                    ctypes.POINTER(ctypes.c_int)]),
     "attn_decode_kernel_launches": (_c_int, [_c_int] * 6),
     "attn_bwd_workspace_size": (ctypes.c_size_t, [_c_int] * 6),
+    "attn_bwd_varlen_workspace_size": (ctypes.c_size_t, [_c_int] * 5),
+    "attn_bwd_varlen": (_c_int, [ctypes.c_void_p] * 11 + [_c_int] * 9 + [ctypes.c_float, _c_int, _c_int,
+                                                                          ctypes.c_void_p, ctypes.c_size_t,
+                                                                          ctypes.c_void_p]),
     "attn_decode_paged": (_c_int, [ctypes.c_void_p] * 7 + [_c_int, _c_int, _c_int, _c_ll, _c_int,
                                                             _c_int, _c_int, ctypes.c_float, _c_int,
                                                             ctypes.c_void_p, ctypes.c_size_t, _c_int,
@@ -421,6 +426,8 @@ def attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, *, causal: bool = False,
     need = attn_bwd_workspace_size(B, Hq, Hkv, Nq, Nk, d)
     if workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+        if isinstance(stream, torch.cuda.Stream):
+            workspace.record_stream(stream)   # freed only after that stream's use
     odt = ATTN_OUT_F32 if o.dtype == torch.float32 else ATTN_OUT_BF16
     g32 = ATTN_OUT_F32 if gdt == torch.float32 else ATTN_OUT_BF16
     with _on(_one_device(q, k, v, o, dout, lse, dq, dk, dv, workspace)):
@@ -442,6 +449,81 @@ def backward(q, k, v, o, dout, lse, *, causal: bool = False, scale: float | None
     dv = torch.empty(v.shape, dtype=grad_dtype, device=q.device)
     return attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, causal=causal, scale=scale,
                     stream=stream)
+
+
+def attn_bwd_varlen_workspace_size(B: int, Hq: int, Hkv: int, total_q: int, d: int) -> int:
+    return int(load().attn_bwd_varlen_workspace_size(B, Hq, Hkv, total_q, d))
+
+
+def attn_bwd_varlen(q, k, v, o, dout, lse, dq, dk, dv, cu_seqlens_q, cu_seqlens_k,
+                    max_seqlen_q: int, max_seqlen_k: int, *, causal: bool = False,
+                    scale: float | None = None, workspace=None, stream=None):
+    """Packed variable-length backward into caller-provided gradients.
+
+    q, dout [total_q,Hq,d] bf16; k, v [total_k,Hkv,d] bf16; o [total_q,Hq,d]
+    bf16 or fp32 and lse [Hq,total_q] fp32 from attn_fwd_varlen; dq
+    [total_q,Hq,d] and dk, dv [total_k,Hkv,d], all bf16 or all fp32;
+    cu_seqlens_q / cu_seqlens_k int32 [B+1] on the device; workspace: uint8 of
+    attn_bwd_varlen_workspace_size bytes.  Asynchronous."""
+    import torch
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (dout, "dout")):
+        _need(t, torch.bfloat16, n)
+    for t, n in ((cu_seqlens_q, "cu_seqlens_q"), (cu_seqlens_k, "cu_seqlens_k")):
+        _need(t, torch.int32, n)
+    if o.dtype not in (torch.bfloat16, torch.float32):
+        raise TypeError("o must be bfloat16 or float32")
+    _need(o, o.dtype, "o")
+    _need(lse, torch.float32, "lse")
+    gdt = dq.dtype
+    if gdt not in (torch.bfloat16, torch.float32) or dk.dtype != gdt or dv.dtype != gdt:
+        raise TypeError("dq, dk, dv must all be bfloat16 or all float32")
+    for t, n in ((dq, "dq"), (dk, "dk"), (dv, "dv")):
+        _need(t, gdt, n)
+    total_q, Hq, d = q.shape
+    total_k, Hkv = k.shape[0], k.shape[1]
+    if (tuple(k.shape) != (total_k, Hkv, d) or tuple(v.shape) != tuple(k.shape)
+            or tuple(dk.shape) != tuple(k.shape) or tuple(dv.shape) != tuple(k.shape)):
+        raise ValueError("k/v/dk/dv shape mismatch")
+    if tuple(o.shape) != tuple(q.shape) or tuple(dout.shape) != tuple(q.shape) \
+            or tuple(dq.shape) != tuple(q.shape):
+        raise ValueError("o/dout/dq shape mismatch")
+    B = cu_seqlens_q.numel() - 1
+    if cu_seqlens_k.numel() != B + 1 or B < 1:
+        raise ValueError("cu_seqlens_q / cu_seqlens_k must both have B + 1 entries")
+    if tuple(lse.shape) != (Hq, total_q):
+        raise ValueError("lse shape mismatch")
+    if scale is None:
+        scale = d ** -0.5
+    dev = _one_device(q, k, v, o, dout, lse, dq, dk, dv, cu_seqlens_q, cu_seqlens_k, workspace)
+    with _on(dev):
+        if workspace is None:
+            workspace = torch.empty(attn_bwd_varlen_workspace_size(B, Hq, Hkv, total_q, d),
+                                    dtype=torch.uint8, device=dev)
+            if isinstance(stream, torch.cuda.Stream):
+                workspace.record_stream(stream)   # freed only after that stream's use
+        ws_ptr, ws_bytes = _workspace(workspace)
+        odt = ATTN_OUT_F32 if o.dtype == torch.float32 else ATTN_OUT_BF16
+        g32 = ATTN_OUT_F32 if gdt == torch.float32 else ATTN_OUT_BF16
+        rc = load().attn_bwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse),
+                                    _ptr(dq), _ptr(dk), _ptr(dv), _ptr(cu_seqlens_q),
+                                    _ptr(cu_seqlens_k), B, Hq, Hkv, total_q, total_k,
+                                    int(max_seqlen_q), int(max_seqlen_k), d, int(bool(causal)),
+                                    float(scale), odt, g32, ws_ptr, ws_bytes, _stream_ptr(stream))
+    _check(rc, "attn_bwd_varlen")
+    return dq, dk, dv
+
+
+def backward_varlen(q, k, v, o, dout, lse, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int,
+                    max_seqlen_k: int, *, causal: bool = False, scale: float | None = None,
+                    grad_dtype=None, stream=None):
+    """Allocate dQ, dK, dV (and the workspace) with torch and run attn_bwd_varlen."""
+    import torch
+    grad_dtype = grad_dtype or torch.bfloat16
+    dq = torch.empty(q.shape, dtype=grad_dtype, device=q.device)
+    dk = torch.empty(k.shape, dtype=grad_dtype, device=q.device)
+    dv = torch.empty(v.shape, dtype=grad_dtype, device=q.device)
+    return attn_bwd_varlen(q, k, v, o, dout, lse, dq, dk, dv, cu_seqlens_q, cu_seqlens_k,
+                           max_seqlen_q, max_seqlen_k, causal=causal, scale=scale, stream=stream)
 
 
 def forward(q, k, v, *, causal: bool = False, scale: float | None = None,

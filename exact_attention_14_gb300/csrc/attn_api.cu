@@ -416,6 +416,43 @@ attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* 
                       o_dtype, grad_dtype, workspace, static_cast<cudaStream_t>(stream), dev);
 }
 
+size_t attn_bwd_varlen_workspace_size(int B, int Hq, int Hkv, int total_q, int d) {
+    if (check_common(B, Hq, Hkv, d, 1.0f, ATTN_OUT_BF16) != ATTN_OK) return 0;
+    if (total_q < 1 || total_q > kMaxPackedRows || !head_dim_supported(d)) return 0;
+    return bwd_varlen_workspace_bytes(B, Hq, total_q);
+}
+
+attn_status_t attn_bwd_varlen(const void* q, const void* k, const void* v, const void* o,
+                              const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                              const int* cu_seqlens_q, const int* cu_seqlens_k, int B, int Hq,
+                              int Hkv, int total_q, int total_k, int max_seqlen_q,
+                              int max_seqlen_k, int d, int causal, float scale,
+                              attn_out_dtype_t o_dtype, attn_out_dtype_t grad_dtype,
+                              void* workspace, size_t workspace_bytes, void* stream) {
+    if (!cu_seqlens_q || !cu_seqlens_k || !aligned4(cu_seqlens_q) || !aligned4(cu_seqlens_k))
+        return ATTN_ERR_INVALID_ARG;
+    if (total_q < 1 || total_k < 1 || total_q > kMaxPackedRows || total_k > kMaxPackedRows)
+        return ATTN_ERR_INVALID_ARG;
+    if (max_seqlen_q > total_q || max_seqlen_k > total_k) return ATTN_ERR_INVALID_ARG;
+    // (the per-sequence causal condition is checked on the device)
+    attn_status_t st = check_fwd(q, k, v, o, lse, B, Hq, Hkv, max_seqlen_q, max_seqlen_k, d, 0,
+                                 scale, o_dtype);
+    if (st != ATTN_OK) return st;
+    if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
+    if (!dout || !lse || !dq || !dk || !dv) return ATTN_ERR_INVALID_ARG;
+    if (!aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+        return ATTN_ERR_INVALID_ARG;
+    if (grad_dtype != ATTN_OUT_BF16 && grad_dtype != ATTN_OUT_F32) return ATTN_ERR_INVALID_ARG;
+    if (!head_dim_supported(d)) return ATTN_ERR_UNSUPPORTED;
+    const size_t need = bwd_varlen_workspace_bytes(B, Hq, total_q);
+    if (!workspace || workspace_bytes < need || !aligned16(workspace)) return ATTN_ERR_WORKSPACE;
+    DeviceInfo dev;
+    if ((st = current_device_info(&dev)) != ATTN_OK) return st;
+    return launch_bwd_varlen(q, k, v, o, dout, lse, dq, dk, dv, cu_seqlens_q, cu_seqlens_k, B, Hq,
+                             Hkv, total_q, total_k, max_seqlen_q, max_seqlen_k, d, causal, scale,
+                             o_dtype, grad_dtype, workspace, static_cast<cudaStream_t>(stream), dev);
+}
+
 size_t attn_decode_workspace_size(int B, int Hq, int Hkv, int Nmax, int d, int num_splits) {
     if (check_decode_shape(B, Hq, Hkv, Nmax, d, num_splits) != ATTN_OK) return 0;
     int sms = 0;

@@ -49,6 +49,7 @@
 #include <cmath>
 #include <cstdint>
 
+#include "fwd_sched.h"
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -81,12 +82,39 @@ struct BwdParams {
     int d_act;          // the tensors' head dim (<= D; the tiles' columns past it are zeros)
     float c;      // scale * log2(e)
     float scale;
-    const float* lse2;  // [B*Hq, Nq_pad]
-    const float* dvec;  // [B*Hq, Nq_pad]
-    void* dq;           // [B, Hq, Nq, d]
-    void* dk;           // [B, Hkv, Nk, d]
+    const float* lse2;  // [B*Hq, Nq_pad]; packed batches [Hq, vstride]
+    const float* dvec;  // [B*Hq, Nq_pad]; packed batches [Hq, vstride]
+    void* dq;           // [B, Hq, Nq, d]; packed batches [total_q, Hq, d]
+    void* dk;           // [B, Hkv, Nk, d]; packed batches [total_k, Hkv, d]
     void* dv;
+    // packed batches (the VARLEN instantiations): Nq and Nk above are the
+    // longest lengths; sequence b holds rows [cu_q[b], cu_q[b+1]) of q / o / dO
+    // / dQ and [cu_k[b], cu_k[b+1]) of k / v / dK / dV; its rows of lse2 / dvec
+    // start at varlen_vbase(cu_q[b], b) of each head's vstride rows.
+    const int* cu_q;
+    const int* cu_k;
+    int total_q, total_k, vstride;
 };
+
+// Row of sequence b's first query in a head's rows of lse2 / dvec for packed
+// batches: the packed row rounded up to 4 floats (16-byte bulk copies), plus
+// 132 rows per earlier sequence, so that each sequence's rows padded to whole
+// 128-row tiles never reach the next sequence's.
+__host__ __device__ inline int varlen_vbase(int q_row0, int b) { return ((q_row0 + 3) & ~3) + 132 * b; }
+
+// Sequence b of a packed batch: first rows and lengths.  False when its
+// offsets leave the arrays, decrease, exceed the longest length, give query
+// rows without keys, or (causal) more queries than keys: the checks of the
+// packed forward.
+__device__ __forceinline__ bool bwd_varlen_seq(const BwdParams& p, int b, int& q0, int& nq,
+                                               int& k0, int& nk) {
+    const int qs = __ldg(p.cu_q + b), qe = __ldg(p.cu_q + b + 1);
+    const int ks = __ldg(p.cu_k + b), ke = __ldg(p.cu_k + b + 1);
+    q0 = qs; nq = qe - qs; k0 = ks; nk = ke - ks;
+    return 0 <= qs && qs <= qe && qe <= p.total_q && qe - qs <= p.Nq && 0 <= ks && ks <= ke &&
+           ke <= p.total_k && ke - ks <= p.Nk && (qe == qs || ke > ks) &&
+           (!p.causal || qe - qs <= ke - ks);
+}
 
 struct __align__(8) BwdBars {
     uint64_t kv_full;
@@ -107,6 +135,9 @@ static_assert(sizeof(BwdBars) <= 256, "barrier block");
 // tiles, first).
 struct BwdWork {
     int b, g, kt, k0, qt_first, n_qt_cta, n_tiles;
+    // the (b, g) problem: lengths, causal offset, and for packed batches the
+    // sequence's first rows (in q and k) and its rows of lse2 / dvec
+    int nq, nk, off, qb, kb, vbase;
 };
 
 __device__ __forceinline__ BwdWork bwd_work(const BwdParams& p) {
@@ -132,6 +163,45 @@ __device__ __forceinline__ BwdWork bwd_work(const BwdParams& p) {
     w.qt_first = first;
     w.n_qt_cta = n_qt - first > 0 ? n_qt - first : 0;
     w.n_tiles = w.n_qt_cta * p.group;
+    w.nq = p.Nq;
+    w.nk = p.Nk;
+    w.off = p.off;
+    w.qb = w.kb = w.vbase = 0;
+    return w;
+}
+
+// The same for packed batches: CTA index = (b * Hkv + g) * n_kt + kt, n_kt
+// for the longest key length.  Key tiles past a sequence's end, and every tile
+// of a sequence whose offsets fail the checks (reported in the error word),
+// have no work and write nothing.
+__device__ __forceinline__ BwdWork bwd_work_varlen(const BwdParams& p, unsigned int* err) {
+    BwdWork w;
+    const int per_b = p.Hkv * p.n_kt;
+    w.b = (int)blockIdx.x / per_b;
+    const int rem = (int)blockIdx.x - w.b * per_b;
+    w.g = rem / p.n_kt;
+    w.kt = rem - w.g * p.n_kt;
+    w.k0 = w.kt * kBT;
+    int q0, nq, k0, nk;
+    if (!bwd_varlen_seq(p, w.b, q0, nq, k0, nk)) {
+        if (threadIdx.x == 0) atomicOr(err, kErrBadSeqlen);
+        q0 = nq = k0 = nk = 0;
+    }
+    w.nq = nq;
+    w.nk = nk;
+    w.off = nk - nq;
+    w.qb = q0;
+    w.kb = k0;
+    w.vbase = varlen_vbase(q0, w.b);
+    const int n_qt = (nq + kBT - 1) / kBT;
+    int first = 0;
+    if (p.causal) {
+        const int lo = w.k0 - w.off;
+        first = lo <= 0 ? 0 : lo / kBT;
+    }
+    w.qt_first = first;
+    w.n_qt_cta = (w.k0 < nk && n_qt - first > 0) ? n_qt - first : 0;
+    w.n_tiles = w.n_qt_cta * p.group;
     return w;
 }
 
@@ -143,21 +213,30 @@ __device__ __forceinline__ void bwd_abort(BwdBars* bars, unsigned int* err) {
 // ---------------------------------------------------------------------------
 // Producer
 // ---------------------------------------------------------------------------
-template <int D>
+template <int D, bool VARLEN>
 __device__ void bwd_producer(const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv,
                              const CUtensorMap* tdo, uint8_t* smem, BwdBars* bars,
                              const BwdParams& p, const BwdWork& w, unsigned int* err) {
     using C = BwdCfg<D>;
     const volatile int* abort_flag = &bars->abort;
     const bool leader = elect_one();
-    const int kvh = w.b * p.Hkv + w.g;
+    // K/V head: an index into [B * Hkv], or into [Hkv] of the packed rows
+    const int kvh = VARLEN ? w.g : w.b * p.Hkv + w.g;
     if (leader) {
         const uint32_t bar = smem_u32(&bars->kv_full);
         mbar_arrive_expect_tx(bar, 2 * C::kTile);
 #pragma unroll
         for (int c = 0; c < D / 64; ++c) {
-            tma_load_3d(smem_u32(smem + C::kK) + c * 16384, tk, bar, 64 * c, w.k0, kvh);
-            tma_load_3d(smem_u32(smem + C::kV) + c * 16384, tv, bar, 64 * c, w.k0, kvh);
+            if constexpr (VARLEN) {
+                const int r = kRaggedWindow - w.nk + w.k0;
+                tma_load_5d(smem_u32(smem + C::kK) + c * 16384, tk, bar, 64 * c, kvh, r, w.kb + w.nk,
+                            kRaggedWindow);
+                tma_load_5d(smem_u32(smem + C::kV) + c * 16384, tv, bar, 64 * c, kvh, r, w.kb + w.nk,
+                            kRaggedWindow);
+            } else {
+                tma_load_3d(smem_u32(smem + C::kK) + c * 16384, tk, bar, 64 * c, w.k0, kvh);
+                tma_load_3d(smem_u32(smem + C::kV) + c * 16384, tv, bar, 64 * c, w.k0, kvh);
+            }
         }
     }
     __syncwarp();
@@ -177,10 +256,19 @@ __device__ void bwd_producer(const CUtensorMap* tq, const CUtensorMap* tk, const
             mbar_arrive_expect_tx(bar, 2 * C::kTile + 1024);
 #pragma unroll
             for (int c = 0; c < D / 64; ++c) {
-                tma_load_3d(smem_u32(smem + C::kQ + st * C::kTile) + c * 16384, tq, bar, 64 * c, q0, bh);
-                tma_load_3d(smem_u32(smem + C::kDO + st * C::kTile) + c * 16384, tdo, bar, 64 * c, q0, bh);
+                if constexpr (VARLEN) {
+                    const int r = kRaggedWindow - w.nq + q0;
+                    tma_load_5d(smem_u32(smem + C::kQ + st * C::kTile) + c * 16384, tq, bar, 64 * c, hq, r,
+                                w.qb + w.nq, kRaggedWindow);
+                    tma_load_5d(smem_u32(smem + C::kDO + st * C::kTile) + c * 16384, tdo, bar, 64 * c, hq, r,
+                                w.qb + w.nq, kRaggedWindow);
+                } else {
+                    tma_load_3d(smem_u32(smem + C::kQ + st * C::kTile) + c * 16384, tq, bar, 64 * c, q0, bh);
+                    tma_load_3d(smem_u32(smem + C::kDO + st * C::kTile) + c * 16384, tdo, bar, 64 * c, q0, bh);
+                }
             }
-            const size_t row = (size_t)bh * p.Nq_pad + q0;
+            const size_t row = VARLEN ? (size_t)hq * p.vstride + (size_t)(w.vbase + q0)
+                                      : (size_t)bh * p.Nq_pad + q0;
             bulk_load(smem_u32(smem + C::kLD + st * 1024), p.lse2 + row, 512, bar);
             bulk_load(smem_u32(smem + C::kLD + st * 1024 + 512), p.dvec + row, 512, bar);
         }
@@ -390,7 +478,7 @@ __device__ __forceinline__ void store_rows32_pairs(void* base, size_t row0, size
     }
 }
 
-template <int D, bool OUT_F32>
+template <int D, bool OUT_F32, bool VARLEN>
 __device__ void bwd_pds(int wq, int lane, uint8_t* smem, BwdBars* bars, uint32_t tmem,
                         const BwdParams& p, const BwdWork& w, unsigned int* err) {
     using C = BwdCfg<D>;
@@ -409,8 +497,8 @@ __device__ void bwd_pds(int wq, int lane, uint8_t* smem, BwdBars* bars, uint32_t
         const uint32_t lse2s = smem_u32(smem + C::kLD + st * 1024);
         const uint32_t ds_vec = lse2s + kBT * 4;
         // causal: query q0 + x sees key jg iff x >= jg - off - q0
-        const int lim = jg - p.off - q0;
-        const bool masked = p.causal && (q0 + p.off < w.k0 + kBT - 1);
+        const int lim = jg - w.off - q0;
+        const bool masked = p.causal && (q0 + w.off < w.k0 + kBT - 1);
         // Phase 1: P^T from S^T, kept in registers and written as bf16 over the
         // S^T columns already read; releases dV(i) and S^T(i+1).
         float pf0[32], pf1[32], pf2[32], pf3[32];
@@ -461,9 +549,15 @@ __device__ void bwd_pds(int wq, int lane, uint8_t* smem, BwdBars* bars, uint32_t
         return;
     }
     // dK = scale * dS^T Q, dV = P^T dO: one key row per thread, written once
-    // this warp's first key row and how many of its rows are inside Nk
-    const size_t wrow0 = ((size_t)w.b * p.Hkv + w.g) * p.Nk + (size_t)(w.k0 + wq * 32);
-    const int rows_live = p.Nk - (w.k0 + wq * 32);
+    // this warp's first key row and how many of its rows are inside Nk (packed
+    // batches: rows of Hkv * d elements, the head's d columns at offset g * d)
+    const size_t wrow0 = VARLEN ? (size_t)(w.kb + w.k0 + wq * 32)
+                                : ((size_t)w.b * p.Hkv + w.g) * p.Nk + (size_t)(w.k0 + wq * 32);
+    const int rows_live = w.nk - (w.k0 + wq * 32);
+    const size_t row_elems = VARLEN ? (size_t)p.Hkv * p.d_act : (size_t)p.d_act;
+    const size_t head_off = VARLEN ? (size_t)w.g * p.d_act * (OUT_F32 ? 4 : 2) : 0;
+    void* dk_base = static_cast<uint8_t*>(p.dk) + head_off;
+    void* dv_base = static_cast<uint8_t*>(p.dv) + head_off;
     if (w.n_tiles == 0) {
         float z[32];
 #pragma unroll
@@ -471,8 +565,8 @@ __device__ void bwd_pds(int wq, int lane, uint8_t* smem, BwdBars* bars, uint32_t
 #pragma unroll 1
         for (int cc = 0; cc < p.d_act; cc += 32) {
             const int nc = p.d_act - cc < 32 ? p.d_act - cc : 32;
-            store_rows32_pairs<OUT_F32>(p.dk, wrow0, p.d_act, cc, z, nc, rows_live, lane);
-            store_rows32_pairs<OUT_F32>(p.dv, wrow0, p.d_act, cc, z, nc, rows_live, lane);
+            store_rows32_pairs<OUT_F32>(dk_base, wrow0, row_elems, cc, z, nc, rows_live, lane);
+            store_rows32_pairs<OUT_F32>(dv_base, wrow0, row_elems, cc, z, nc, rows_live, lane);
         }
         return;
     }
@@ -491,16 +585,16 @@ __device__ void bwd_pds(int wq, int lane, uint8_t* smem, BwdBars* bars, uint32_t
         const int nc = p.d_act - cc < 32 ? p.d_act - cc : 32;  // <= 0: past the head dim
 #pragma unroll
         for (int x = 0; x < 32; ++x) v[x] = __uint_as_float(r[x]);
-        if (nc > 0) store_rows32_pairs<OUT_F32>(p.dv, wrow0, p.d_act, cc, v, nc, rows_live, lane);
+        if (nc > 0) store_rows32_pairs<OUT_F32>(dv_base, wrow0, row_elems, cc, v, nc, rows_live, lane);
         tmem_ld32(tmem + 256 + D + cc + lane_off, r);
         tmem_wait_ld();
 #pragma unroll
         for (int x = 0; x < 32; ++x) v[x] = __uint_as_float(r[x]) * p.scale;
-        if (nc > 0) store_rows32_pairs<OUT_F32>(p.dk, wrow0, p.d_act, cc, v, nc, rows_live, lane);
+        if (nc > 0) store_rows32_pairs<OUT_F32>(dk_base, wrow0, row_elems, cc, v, nc, rows_live, lane);
     }
 }
 
-template <int D, bool OUT_F32>
+template <int D, bool OUT_F32, bool VARLEN>
 __global__ void __launch_bounds__(kBwdThreads, 1)
 attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                      const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
@@ -517,7 +611,7 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tq, const __grid_consta
     BwdBars* bars = reinterpret_cast<BwdBars*>(smem + C::kBar);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const BwdWork w = bwd_work(p);
+    const BwdWork w = VARLEN ? bwd_work_varlen(p, err) : bwd_work(p);
 
     if (threadIdx.x == 0) {
         mbar_init(smem_u32(&bars->kv_full), 1);
@@ -547,9 +641,9 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tq, const __grid_consta
     tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
 
-    if (warp == 0) bwd_producer<D>(&tq, &tk, &tv, &tdo, smem, bars, p, w, err);
+    if (warp == 0) bwd_producer<D, VARLEN>(&tq, &tk, &tv, &tdo, smem, bars, p, w, err);
     else if (warp == 1) bwd_mma<D>(smem, bars, tmem, w, err);
-    else if (warp >= 4) bwd_pds<D, OUT_F32>(warp & 3, lane, smem, bars, tmem, p, w, err);
+    else if (warp >= 4) bwd_pds<D, OUT_F32, VARLEN>(warp & 3, lane, smem, bars, tmem, p, w, err);
 
     tc_fence_before();
     __syncthreads();
@@ -592,6 +686,7 @@ static_assert(sizeof(DqBars) <= 256, "barrier block");
 // query heads, so consecutive CTAs share K and V.
 struct DqWork {
     int b, g, hq, q0, n_kv;
+    int nq, nk, off, qb, kb, vbase;  // as in BwdWork
 };
 
 __device__ __forceinline__ DqWork dq_work(const BwdParams& p) {
@@ -623,10 +718,51 @@ __device__ __forceinline__ DqWork dq_work(const BwdParams& p) {
     } else {
         w.n_kv = p.n_kt;
     }
+    w.nq = p.Nq;
+    w.nk = p.Nk;
+    w.off = p.off;
+    w.qb = w.kb = w.vbase = 0;
     return w;
 }
 
-template <int D>
+// The same for packed batches: CTA index = (b * Hq + hq) * n_qt + qt, n_qt for
+// the longest query length; Q tiles past a sequence's end, and every tile of a
+// sequence whose offsets fail the checks, have no work and write nothing.
+__device__ __forceinline__ DqWork dq_work_varlen(const BwdParams& p, unsigned int* err) {
+    DqWork w;
+    const int n_qt = (p.Nq + kBT - 1) / kBT;
+    const int per_b = p.Hq * n_qt;
+    w.b = (int)blockIdx.x / per_b;
+    const int rem = (int)blockIdx.x - w.b * per_b;
+    w.hq = rem / n_qt;
+    w.g = w.hq / p.group;
+    w.q0 = (rem - w.hq * n_qt) * kBT;
+    int q0, nq, k0, nk;
+    if (!bwd_varlen_seq(p, w.b, q0, nq, k0, nk)) {
+        if (threadIdx.x == 0) atomicOr(err, kErrBadSeqlen);
+        q0 = nq = k0 = nk = 0;
+    }
+    w.nq = nq;
+    w.nk = nk;
+    w.off = nk - nq;
+    w.qb = q0;
+    w.kb = k0;
+    w.vbase = varlen_vbase(q0, w.b);
+    const int n_kt = (nk + kBT - 1) / kBT;
+    if (w.q0 >= nq) {
+        w.n_kv = 0;
+    } else if (p.causal) {
+        const int last_row = (w.q0 + kBT - 1 < nq - 1 ? w.q0 + kBT - 1 : nq - 1);
+        const int last_key = last_row + w.off;
+        const int n = last_key < 0 ? 0 : last_key / kBT + 1;
+        w.n_kv = n < n_kt ? n : n_kt;
+    } else {
+        w.n_kv = n_kt;
+    }
+    return w;
+}
+
+template <int D, bool VARLEN>
 __device__ void dq_producer(const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv,
                             const CUtensorMap* tdo, uint8_t* smem, DqBars* bars, const BwdParams& p,
                             const DqWork& w, unsigned int* err) {
@@ -634,14 +770,23 @@ __device__ void dq_producer(const CUtensorMap* tq, const CUtensorMap* tk, const 
     const volatile int* abort_flag = &bars->abort;
     const bool leader = elect_one();
     const int bh = w.b * p.Hq + w.hq;
-    const int kvh = w.b * p.Hkv + w.g;
+    // K/V head: an index into [B * Hkv], or into [Hkv] of the packed rows
+    const int kvh = VARLEN ? w.g : w.b * p.Hkv + w.g;
     if (leader) {
         const uint32_t bar = smem_u32(&bars->q_full);
         mbar_arrive_expect_tx(bar, 2 * C::kTile);
 #pragma unroll
         for (int c = 0; c < D / 64; ++c) {
-            tma_load_3d(smem_u32(smem + C::kQ) + c * 16384, tq, bar, 64 * c, w.q0, bh);
-            tma_load_3d(smem_u32(smem + C::kDO) + c * 16384, tdo, bar, 64 * c, w.q0, bh);
+            if constexpr (VARLEN) {
+                const int r = kRaggedWindow - w.nq + w.q0;
+                tma_load_5d(smem_u32(smem + C::kQ) + c * 16384, tq, bar, 64 * c, w.hq, r, w.qb + w.nq,
+                            kRaggedWindow);
+                tma_load_5d(smem_u32(smem + C::kDO) + c * 16384, tdo, bar, 64 * c, w.hq, r, w.qb + w.nq,
+                            kRaggedWindow);
+            } else {
+                tma_load_3d(smem_u32(smem + C::kQ) + c * 16384, tq, bar, 64 * c, w.q0, bh);
+                tma_load_3d(smem_u32(smem + C::kDO) + c * 16384, tdo, bar, 64 * c, w.q0, bh);
+            }
         }
     }
     __syncwarp();
@@ -660,7 +805,13 @@ __device__ void dq_producer(const CUtensorMap* tq, const CUtensorMap* tk, const 
             mbar_arrive_expect_tx(bar, C::kTile);
             const uint32_t dst = smem_u32(smem + C::kKRing + sk * C::kTile);
 #pragma unroll
-            for (int c = 0; c < D / 64; ++c) tma_load_3d(dst + c * 16384, tk, bar, 64 * c, j * kBT, kvh);
+            for (int c = 0; c < D / 64; ++c) {
+                if constexpr (VARLEN)
+                    tma_load_5d(dst + c * 16384, tk, bar, 64 * c, kvh, kRaggedWindow - w.nk + j * kBT,
+                                w.kb + w.nk, kRaggedWindow);
+                else
+                    tma_load_3d(dst + c * 16384, tk, bar, 64 * c, j * kBT, kvh);
+            }
         }
         __syncwarp();
         ++nk;
@@ -673,7 +824,13 @@ __device__ void dq_producer(const CUtensorMap* tq, const CUtensorMap* tk, const 
             mbar_arrive_expect_tx(bar, C::kTile);
             const uint32_t dst = smem_u32(smem + C::kVRing + sv * C::kTile);
 #pragma unroll
-            for (int c = 0; c < D / 64; ++c) tma_load_3d(dst + c * 16384, tv, bar, 64 * c, j * kBT, kvh);
+            for (int c = 0; c < D / 64; ++c) {
+                if constexpr (VARLEN)
+                    tma_load_5d(dst + c * 16384, tv, bar, 64 * c, kvh, kRaggedWindow - w.nk + j * kBT,
+                                w.kb + w.nk, kRaggedWindow);
+                else
+                    tma_load_3d(dst + c * 16384, tv, bar, 64 * c, j * kBT, kvh);
+            }
         }
         __syncwarp();
         ++nv;
@@ -785,7 +942,7 @@ __device__ __forceinline__ void ds_row_chunk(const float (&pf)[32], const uint32
     }
 }
 
-template <int D, bool OUT_F32>
+template <int D, bool OUT_F32, bool VARLEN>
 __device__ void dq_ds(int wq, int lane, DqBars* bars, uint32_t tmem, const BwdParams& p,
                       const DqWork& w, unsigned int* err) {
     const volatile int* abort_flag = &bars->abort;
@@ -793,8 +950,10 @@ __device__ void dq_ds(int wq, int lane, DqBars* bars, uint32_t tmem, const BwdPa
     const uint32_t tdP = tmem + 128 + lane_off;
     const int row = w.q0 + wq * 32 + lane;
     const size_t bh = (size_t)w.b * p.Hq + w.hq;
-    const float lse2 = p.lse2[bh * p.Nq_pad + row];  // +inf past Nq: P = 0
-    const float dval = p.dvec[bh * p.Nq_pad + row];
+    const size_t vrow = VARLEN ? (size_t)w.hq * p.vstride + (size_t)(w.vbase + row)
+                               : bh * p.Nq_pad + row;
+    const float lse2 = p.lse2[vrow];  // +inf past the last query: P = 0
+    const float dval = p.dvec[vrow];
     const uint64_t c2 = f2(p.c, p.c), nl2 = f2(-lse2, -lse2), nd2 = f2(-dval, -dval);
     bool ok = true;
     for (int j = 0; j < w.n_kv && ok; ++j) {
@@ -802,7 +961,7 @@ __device__ void dq_ds(int wq, int lane, DqBars* bars, uint32_t tmem, const BwdPa
         ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&bars->s_full[j & 1]), (j >> 1) & 1, abort_flag, 32));
         if (!ok) break;
         tc_fence_after();
-        const int lim = row + p.off - j * kBT;  // causal: key column c allowed iff c <= lim
+        const int lim = row + w.off - j * kBT;  // causal: key column c allowed iff c <= lim
         const bool masked = __any_sync(0xFFFFFFFFu, p.causal && lim < kBT - 1);
         // Phase 1: P from S (needs S_j only; runs while dQ_{j-1} and dP_j compute)
         float pf0[32], pf1[32], pf2[32], pf3[32];
@@ -849,8 +1008,11 @@ __device__ void dq_ds(int wq, int lane, DqBars* bars, uint32_t tmem, const BwdPa
     tc_fence_after();
     // every lane runs the (warp-collective) TMEM loads; rows past Nq store nothing
     // this warp's first query row and how many of its rows are inside Nq
-    const size_t wrow0 = bh * p.Nq + (size_t)(w.q0 + wq * 32);
-    const int rows_live = p.Nq - (w.q0 + wq * 32);
+    // (packed batches: rows of Hq * d elements, the head's d columns at hq * d)
+    const size_t wrow0 = VARLEN ? (size_t)(w.qb + w.q0 + wq * 32) : bh * p.Nq + (size_t)(w.q0 + wq * 32);
+    const int rows_live = w.nq - (w.q0 + wq * 32);
+    const size_t row_elems = VARLEN ? (size_t)p.Hq * p.d_act : (size_t)p.d_act;
+    void* dq_base = static_cast<uint8_t*>(p.dq) + (VARLEN ? (size_t)w.hq * p.d_act * (OUT_F32 ? 4 : 2) : 0);
 #pragma unroll 1
     for (int cc = 0; cc < D; cc += 32) {
         float v[32];
@@ -865,11 +1027,11 @@ __device__ void dq_ds(int wq, int lane, DqBars* bars, uint32_t tmem, const BwdPa
             for (int x = 0; x < 32; ++x) v[x] = 0.f;
         }
         const int nc = p.d_act - cc < 32 ? p.d_act - cc : 32;
-        if (nc > 0) store_rows32_pairs<OUT_F32>(p.dq, wrow0, p.d_act, cc, v, nc, rows_live, lane);
+        if (nc > 0) store_rows32_pairs<OUT_F32>(dq_base, wrow0, row_elems, cc, v, nc, rows_live, lane);
     }
 }
 
-template <int D, bool OUT_F32>
+template <int D, bool OUT_F32, bool VARLEN>
 __global__ void __launch_bounds__(kBwdThreads, 1)
 attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                    const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
@@ -885,7 +1047,7 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
     DqBars* bars = reinterpret_cast<DqBars*>(smem + C::kBar);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const DqWork w = dq_work(p);
+    const DqWork w = VARLEN ? dq_work_varlen(p, err) : dq_work(p);
     if (threadIdx.x == 0) {
         mbar_init(smem_u32(&bars->q_full), 1);
         for (int s = 0; s < 3; ++s) {
@@ -916,9 +1078,9 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
-    if (warp == 0) dq_producer<D>(&tq, &tk, &tv, &tdo, smem, bars, p, w, err);
+    if (warp == 0) dq_producer<D, VARLEN>(&tq, &tk, &tv, &tdo, smem, bars, p, w, err);
     else if (warp == 1) dq_mma<D>(smem, bars, tmem, w, err);
-    else if (warp >= 4) dq_ds<D, OUT_F32>(warp & 3, lane, bars, tmem, p, w, err);
+    else if (warp >= 4) dq_ds<D, OUT_F32, VARLEN>(warp & 3, lane, bars, tmem, p, w, err);
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
@@ -984,6 +1146,89 @@ attn_bwd_prep_kernel(const void* __restrict__ o, int o_f32, const __nv_bfloat16*
     }
 }
 
+// The same for packed batches: block (b, hq, chunk) covers rows
+// [chunk * rows, (chunk + 1) * rows) of sequence b's rows padded to whole
+// 128-row tiles, in the varlen_vbase layout; rows past the sequence's queries
+// get lse2 = +inf, D = 0.  A sequence whose offsets leave the arrays is
+// skipped here (the passes report it and compute nothing for it).
+template <int LPR>
+__global__ void __launch_bounds__(256)
+attn_bwd_prep_varlen_kernel(const void* __restrict__ o, int o_f32, const __nv_bfloat16* __restrict__ dout,
+                            const float* __restrict__ lse, float* __restrict__ lse2,
+                            float* __restrict__ dvec, const int* __restrict__ cu_q, int Hq,
+                            int total_q, int vstride, int chunks, int dh) {
+    constexpr int kRowsPerWarp = 32 / LPR;
+    constexpr int kRowsPerBlock = 8 * kRowsPerWarp;
+    const int lane = threadIdx.x & 31;
+    const int sub = lane % LPR;
+    const int per_b = Hq * chunks;
+    const int b = (int)blockIdx.x / per_b;
+    const int rem = (int)blockIdx.x - b * per_b;
+    const int hq = rem / chunks;
+    const int i = (rem - hq * chunks) * kRowsPerBlock + (threadIdx.x >> 5) * kRowsPerWarp + lane / LPR;
+    const int q0 = __ldg(cu_q + b), qe = __ldg(cu_q + b + 1);
+    const int nq = qe - q0;
+    const bool seq_ok = 0 <= q0 && q0 <= qe && qe <= total_q;
+    const bool live_row = seq_ok && i < (nq + kBT - 1) / kBT * kBT;
+    const bool valid = live_row && i < nq;
+    float sum = 0.f;
+    if (valid) {
+        const size_t base = ((size_t)(q0 + i) * Hq + hq) * dh;
+        for (int c = sub * 8; c < dh; c += LPR * 8) {
+            const uint4 g = *reinterpret_cast<const uint4*>(dout + base + c);
+            const uint32_t gw[4] = {g.x, g.y, g.z, g.w};
+            float ov[8];
+            if (o_f32) {
+                const float4 a = *reinterpret_cast<const float4*>(static_cast<const float*>(o) + base + c);
+                const float4 bb = *reinterpret_cast<const float4*>(static_cast<const float*>(o) + base + c + 4);
+                ov[0] = a.x; ov[1] = a.y; ov[2] = a.z; ov[3] = a.w;
+                ov[4] = bb.x; ov[5] = bb.y; ov[6] = bb.z; ov[7] = bb.w;
+            } else {
+                const uint4 h = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(o) + base + c);
+                const uint32_t hw[4] = {h.x, h.y, h.z, h.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    ov[2 * e] = __uint_as_float(hw[e] << 16);
+                    ov[2 * e + 1] = __uint_as_float(hw[e] & 0xFFFF0000u);
+                }
+            }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                sum = fmaf(__uint_as_float(gw[e] << 16), ov[2 * e], sum);
+                sum = fmaf(__uint_as_float(gw[e] & 0xFFFF0000u), ov[2 * e + 1], sum);
+            }
+        }
+    }
+#pragma unroll
+    for (int s = LPR / 2; s > 0; s >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, s);
+    if (live_row && sub == 0) {
+        const size_t r = (size_t)hq * vstride + (size_t)(varlen_vbase(q0, b) + i);
+        dvec[r] = valid ? sum : 0.f;
+        lse2[r] = valid ? lse[(size_t)hq * total_q + (size_t)(q0 + i)] * kBwdLog2e : INFINITY;
+    }
+}
+
+attn_status_t launch_bwd_prep_varlen(const void* o, int o_f32, const void* dout, const float* lse,
+                                     float* lse2, float* dvec, const BwdParams& p, cudaStream_t stream) {
+    const auto* g = static_cast<const __nv_bfloat16*>(dout);
+    const int dh = p.d_act;
+    const int lpr = dh <= 64 ? 8 : dh <= 128 ? 16 : 32;
+    const int rows_per_block = 8 * (32 / lpr);
+    const int rows_pad = (p.Nq + kBT - 1) / kBT * kBT;
+    const int chunks = (rows_pad + rows_per_block - 1) / rows_per_block;
+    const long long grid = (long long)p.B * p.Hq * chunks;
+    if (grid >= (1ll << 31)) return ATTN_ERR_UNSUPPORTED;
+#define GB300_PREP_VARLEN(L)                                                                       \
+    attn_bwd_prep_varlen_kernel<L><<<(unsigned)grid, 256, 0, stream>>>(o, o_f32, g, lse, lse2, dvec, \
+                                                                       p.cu_q, p.Hq, p.total_q,      \
+                                                                       p.vstride, chunks, dh)
+    if (lpr == 8) GB300_PREP_VARLEN(8);
+    else if (lpr == 16) GB300_PREP_VARLEN(16);
+    else GB300_PREP_VARLEN(32);
+#undef GB300_PREP_VARLEN
+    return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
 // The prep launch for head dim dh (<= 256): 8, 16 or 32 lanes per row.
 attn_status_t launch_bwd_prep(const void* o, int o_f32, const void* dout, const float* lse,
                               float* lse2, float* dvec, long long rows_pad, int Nq, int Nq_pad,
@@ -1001,33 +1246,39 @@ attn_status_t launch_bwd_prep(const void* o, int o_f32, const void* dout, const 
     return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
-template <int D, bool OUT_F32>
+template <int D, bool OUT_F32, bool VARLEN = false>
 attn_status_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                            const CUtensorMap& tdo, const BwdParams& p, const void* o, int o_f32,
                            const void* dout, const float* lse, float* lse2, float* dvec,
                            cudaStream_t stream, const DeviceInfo& dev) {
     static int attr_set[64] = {0};
     if (dev.device < 64 && !attr_set[dev.device]) {
-        if (cudaFuncSetAttribute(attn_bwd_dkdv_kernel<D, OUT_F32>,
+        if (cudaFuncSetAttribute(attn_bwd_dkdv_kernel<D, OUT_F32, VARLEN>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  BwdCfg<D>::kSmemBytes) != cudaSuccess ||
-            cudaFuncSetAttribute(attn_bwd_dq_kernel<D, OUT_F32>,
+            cudaFuncSetAttribute(attn_bwd_dq_kernel<D, OUT_F32, VARLEN>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  DqCfg<D>::kSmemBytes) != cudaSuccess)
             return ATTN_ERR_CUDA;
         attr_set[dev.device] = 1;
     }
-    const long long rows_pad = (long long)p.B * p.Hq * p.Nq_pad;
-    attn_status_t st = launch_bwd_prep(o, o_f32, dout, lse, lse2, dvec, rows_pad, p.Nq, p.Nq_pad,
-                                       p.d_act, stream);
+    attn_status_t st;
+    if constexpr (VARLEN) {
+        st = launch_bwd_prep_varlen(o, o_f32, dout, lse, lse2, dvec, p, stream);
+    } else {
+        const long long rows_pad = (long long)p.B * p.Hq * p.Nq_pad;
+        st = launch_bwd_prep(o, o_f32, dout, lse, lse2, dvec, rows_pad, p.Nq, p.Nq_pad, p.d_act, stream);
+    }
     if (st != ATTN_OK) return st;
+    // (packed batches: units at the longest lengths; the tiles past a
+    // sequence's end have no work)
     const long long kv_ctas = (long long)p.B * p.Hkv * p.n_kt;
-    attn_bwd_dkdv_kernel<D, OUT_F32><<<(unsigned)kv_ctas, kBwdThreads, BwdCfg<D>::kSmemBytes, stream>>>(
-        tq, tk, tv, tdo, p, dev.err_word);
+    attn_bwd_dkdv_kernel<D, OUT_F32, VARLEN><<<(unsigned)kv_ctas, kBwdThreads, BwdCfg<D>::kSmemBytes,
+                                               stream>>>(tq, tk, tv, tdo, p, dev.err_word);
     if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
     const long long q_ctas = (long long)p.B * p.Hq * ((p.Nq + kBT - 1) / kBT);
-    attn_bwd_dq_kernel<D, OUT_F32><<<(unsigned)q_ctas, kBwdThreads, DqCfg<D>::kSmemBytes, stream>>>(
-        tq, tk, tv, tdo, p, dev.err_word);
+    attn_bwd_dq_kernel<D, OUT_F32, VARLEN><<<(unsigned)q_ctas, kBwdThreads, DqCfg<D>::kSmemBytes,
+                                             stream>>>(tq, tk, tv, tdo, p, dev.err_word);
     return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
@@ -1780,6 +2031,63 @@ attn_status_t launch_bwd_wide_t(const CUtensorMap& tq, const CUtensorMap& tk, co
 
 }  // namespace
 
+size_t bwd_varlen_workspace_bytes(int B, int Hq, int total_q) {
+    const size_t vstride = ((size_t)total_q + 132 * (size_t)B + 3) & ~(size_t)3;
+    return 2 * (size_t)Hq * vstride * 4;
+}
+
+attn_status_t launch_bwd_varlen(const void* q, const void* k, const void* v, const void* o,
+                                const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                                const int* cu_q, const int* cu_k, int B, int Hq, int Hkv, int total_q,
+                                int total_k, int max_q, int max_k, int d, int causal, float scale,
+                                attn_out_dtype_t o_dtype, attn_out_dtype_t grad_dtype,
+                                void* workspace, cudaStream_t stream, const DeviceInfo& dev) {
+    if (d > 128) return ATTN_ERR_UNSUPPORTED;
+    BwdParams p;
+    p.B = B;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.Nq = max_q;
+    p.Nk = max_k;
+    p.Nq_pad = (max_q + kBT - 1) / kBT * kBT;
+    p.group = Hq / Hkv;
+    p.off = 0;  // per sequence (nk - nq)
+    p.n_kt = (max_k + kBT - 1) / kBT;
+    p.causal = causal;
+    p.sec_groups = 1;
+    p.c = scale * kBwdLog2e;
+    p.scale = scale;
+    p.d_act = d;
+    p.cu_q = cu_q;
+    p.cu_k = cu_k;
+    p.total_q = total_q;
+    p.total_k = total_k;
+    p.vstride = (int)(((size_t)total_q + 132 * (size_t)B + 3) & ~(size_t)3);
+    float* lse2 = static_cast<float*>(workspace);
+    float* dvec = lse2 + (size_t)Hq * p.vstride;
+    p.lse2 = lse2;
+    p.dvec = dvec;
+    p.dq = dq;
+    p.dk = dk;
+    p.dv = dv;
+    if ((long long)B * Hkv * p.n_kt >= (1ll << 31) || (long long)B * Hq * (p.Nq_pad / kBT) >= (1ll << 31) ||
+        (long long)Hq * p.vstride >= (1ll << 31))
+        return ATTN_ERR_UNSUPPORTED;
+    CUtensorMap tq, tk, tv, tdo;
+    attn_status_t st;
+    if ((st = encode_tmap_ragged(&tq, q, false, d, Hq, 64, kBT, true)) != ATTN_OK) return st;
+    if ((st = encode_tmap_ragged(&tk, k, false, d, Hkv, 64, kBT, true)) != ATTN_OK) return st;
+    if ((st = encode_tmap_ragged(&tv, v, false, d, Hkv, 64, kBT, true)) != ATTN_OK) return st;
+    if ((st = encode_tmap_ragged(&tdo, dout, false, d, Hq, 64, kBT, true)) != ATTN_OK) return st;
+    const int o_f32 = o_dtype == ATTN_OUT_F32;
+    const bool g32 = grad_dtype == ATTN_OUT_F32;
+    if (pad_head_dim(d) == 128)
+        return g32 ? launch_bwd_t<128, true, true>(tq, tk, tv, tdo, p, o, o_f32, dout, lse, lse2, dvec, stream, dev)
+                   : launch_bwd_t<128, false, true>(tq, tk, tv, tdo, p, o, o_f32, dout, lse, lse2, dvec, stream, dev);
+    return g32 ? launch_bwd_t<64, true, true>(tq, tk, tv, tdo, p, o, o_f32, dout, lse, lse2, dvec, stream, dev)
+               : launch_bwd_t<64, false, true>(tq, tk, tv, tdo, p, o, o_f32, dout, lse, lse2, dvec, stream, dev);
+}
+
 size_t bwd_workspace_bytes(int B, int Hq, int Nq, int d) {
     (void)d;
     const size_t nq_pad = (size_t)((Nq + kBT - 1) / kBT) * kBT;
@@ -1821,6 +2129,8 @@ attn_status_t launch_bwd(const void* q, const void* k, const void* v, const void
     p.dq = dq;
     p.dk = dk;
     p.dv = dv;
+    p.cu_q = p.cu_k = nullptr;
+    p.total_q = p.total_k = p.vstride = 0;
     if ((long long)B * Hkv * p.n_kt >= (1ll << 31) ||
         (long long)B * Hq * (p.Nq_pad / kBT) >= (1ll << 31))
         return ATTN_ERR_UNSUPPORTED;

@@ -103,6 +103,14 @@ attn_status_t launch_fwd_wide_varlen(const void* q, const void* k, const void* v
 
 // Backward: workspace bytes (fp32 dQ accumulator, lse2, D; padded rows).
 size_t bwd_workspace_bytes(int B, int Hq, int Nq, int d);
+// Packed backward (d <= 128): workspace bytes, and the launch.
+size_t bwd_varlen_workspace_bytes(int B, int Hq, int total_q);
+attn_status_t launch_bwd_varlen(const void* q, const void* k, const void* v, const void* o,
+                                const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                                const int* cu_q, const int* cu_k, int B, int Hq, int Hkv, int total_q,
+                                int total_k, int max_q, int max_k, int d, int causal, float scale,
+                                attn_out_dtype_t o_dtype, attn_out_dtype_t grad_dtype,
+                                void* workspace, cudaStream_t stream, const DeviceInfo& dev);
 attn_status_t launch_bwd(const void* q, const void* k, const void* v, const void* o,
                          const void* dout, const float* lse, void* dq, void* dk, void* dv, int B,
                          int Hq, int Hkv, int Nq, int Nk, int d, int causal, float scale,

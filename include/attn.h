@@ -262,6 +262,48 @@ attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* 
                        size_t workspace_bytes, void* stream);
 
 /*
+ * attn_bwd_varlen_workspace_size -- bytes of device workspace attn_bwd_varlen
+ * needs: D and the base-2 logsumexp for every query head over each
+ * sequence's rows padded to whole 128-row tiles (8 * Hq * (total_q + 132 B)
+ * bytes, rounded up).  Returns 0 for arguments attn_bwd_varlen would reject.
+ */
+size_t attn_bwd_varlen_workspace_size(int B, int Hq, int Hkv, int total_q, int d);
+
+/*
+ * attn_bwd_varlen -- gradients of attn_fwd_varlen: attn_bwd's computation for
+ * every sequence of a packed batch (each sequence an independent problem,
+ * bottom-right causal alignment per sequence).
+ *
+ *   q, dout  bf16 [total_q, Hq, d]      k, v  bf16 [total_k, Hkv, d]
+ *   o        attn_fwd_varlen's output [total_q, Hq, d], element type per o_dtype
+ *   lse      fp32 [Hq, total_q], attn_fwd_varlen's logsumexp
+ *   dq       [total_q, Hq, d];  dk, dv  [total_k, Hkv, d]; element type per
+ *            grad_dtype
+ *   cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k  as attn_fwd_varlen
+ *   workspace  device memory of at least attn_bwd_varlen_workspace_size bytes,
+ *            16-byte aligned; contents need no initialisation.
+ *
+ * Supported: 8 <= d <= 128 (d % 8 == 0); the other limits of attn_fwd_varlen.
+ * The same three kernels as attn_bwd (D and the base-2 LSE per row, the
+ * K/V-outer pass, the Q-outer pass) read the packed rows through the packed
+ * forward's ragged tensor maps; CTAs cover every sequence at the longest
+ * lengths, and the tiles past a sequence's end have no work.  A sequence whose
+ * offsets fail the checks of attn_fwd_varlen is not computed (its gradient
+ * rows are left as they were) and attn_last_device_error() then reports
+ * ATTN_ERR_INVALID_ARG.  Rows outside every sequence are neither read nor
+ * written.  Gradients are bit-identical from run to run.  Returns ATTN_OK once
+ * the kernels are enqueued; ATTN_ERR_WORKSPACE for a missing or short
+ * workspace; ATTN_ERR_UNSUPPORTED for d > 128.
+ */
+attn_status_t attn_bwd_varlen(const void* q, const void* k, const void* v, const void* o,
+                              const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                              const int* cu_seqlens_q, const int* cu_seqlens_k, int B, int Hq,
+                              int Hkv, int total_q, int total_k, int max_seqlen_q,
+                              int max_seqlen_k, int d, int causal, float scale,
+                              attn_out_dtype_t o_dtype, attn_out_dtype_t grad_dtype,
+                              void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * attn_decode_workspace_size -- bytes of device workspace attn_decode needs
  * for this shape and split request (num_splits as passed to attn_decode).
  * Returns 0 for arguments attn_decode would reject.

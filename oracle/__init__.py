@@ -174,6 +174,34 @@ def attention_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, *, causal: bool = Fals
     return o, lse
 
 
+def attention_bwd_varlen(q, k, v, dout, cu_seqlens_q, cu_seqlens_k, *, causal: bool = False,
+                         scale: float | None = None, n_threads: int = 0):
+    """Gradients for a packed batch (layouts as attention_varlen, dout shaped
+    like q): each sequence is its own problem, so its gradients are
+    attention_bwd() of its rows; key rows of a sequence without queries get
+    zero dK and dV.  Returns (dQ, dK, dV) float64 shaped like q, k, v; rows
+    that belong to no sequence are NaN."""
+    cu_q = [int(x) for x in np.asarray(cu_seqlens_q).reshape(-1)]
+    cu_k = [int(x) for x in np.asarray(cu_seqlens_k).reshape(-1)]
+    dq = np.full(tuple(q.shape), np.nan)
+    dk = np.full(tuple(k.shape), np.nan)
+    dv = np.full(tuple(v.shape), np.nan)
+    for b in range(len(cu_q) - 1):
+        qs, qe, ks, ke = cu_q[b], cu_q[b + 1], cu_k[b], cu_k[b + 1]
+        if qe == qs:
+            dk[ks:ke] = 0.0
+            dv[ks:ke] = 0.0
+            continue
+        seq = lambda t, s0, s1: t[s0:s1].permute(1, 0, 2).unsqueeze(0)  # noqa: E731
+        gq, gk, gv = attention_bwd(seq(q, qs, qe), seq(k, ks, ke), seq(v, ks, ke),
+                                   seq(dout, qs, qe), causal=causal, scale=scale,
+                                   n_threads=n_threads)
+        dq[qs:qe] = gq[0].transpose(1, 0, 2)
+        dk[ks:ke] = gk[0].transpose(1, 0, 2)
+        dv[ks:ke] = gv[0].transpose(1, 0, 2)
+    return dq, dk, dv
+
+
 def decode(q, k_cache, v_cache, seqlens, *, scale: float | None = None,
            n_threads: int = 0):
     """Single-query decode over the valid prefix of each sequence's KV cache.

@@ -1,6 +1,6 @@
 """Seeded random shapes through every entry point against the fp64 oracle:
-forward (both kernels, every supported head dim class), packed batches,
-backward and decode.  Each case is small (the oracle takes
+forward (both kernels, every supported head dim class), packed batches
+(forward and backward), backward and decode.  Each case is small (the oracle takes
 well under a second), and the draws reach the corners the fixed cases leave
 out: head dims from 8 to 256, lengths from 1 up, GQA groups of 1 to 8,
 Nq != Nk (bottom-right causal), and the bf16 output."""
@@ -106,6 +106,29 @@ def test_fuzz_varlen(case):
     n = int(cu_q[-1])
     assert_close(o.cpu().double().numpy()[:n], lse.cpu().double().numpy()[:, :n], ro[:n], rl[:, :n],
                  str(case))
+
+
+@pytest.mark.parametrize("case", [c for c in _varlen_cases(16, 5151) if c[4] <= 128],
+                         ids=lambda c: str(abs(hash(c)) % 10 ** 8))
+def test_fuzz_varlen_backward(case):
+    lq, lk, Hq, Hkv, d, causal = case
+    if sum(lq) == 0 or sum(lk) == 0:
+        pytest.skip("an empty packed batch is rejected by the entry point")
+    q, k, v, cu_q, cu_k = make_varlen_inputs(list(lq), list(lk), Hq, Hkv, d, seed=abs(hash(case)) % (2 ** 31))
+    do = _dout(q.shape, seed=abs(hash(case)) % 1000 + 3)
+    scale = 1 / math.sqrt(d)
+    mq, mk = max(max(lq), 1), max(max(lk), 1)
+    qd, kd, vd, cq, ck = q.cuda(), k.cuda(), v.cuda(), cu_q.cuda(), cu_k.cuda()
+    o = torch.empty(q.shape, dtype=torch.float32, device="cuda")
+    lse = torch.empty((Hq, q.shape[0]), dtype=torch.float32, device="cuda")
+    ea.attn_fwd_varlen(qd, kd, vd, o, cq, ck, mq, mk, lse, causal=causal, scale=scale)
+    dq, dk, dv = ea.backward_varlen(qd, kd, vd, o, do.cuda(), lse, cq, ck, mq, mk, causal=causal,
+                                    scale=scale, grad_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert ea.attn_last_device_error() == 0
+    rq, rk, rv = oracle.attention_bwd_varlen(q, k, v, do, cu_q, cu_k, causal=causal, scale=scale)
+    for got, ref, n in ((dq, rq, "dQ"), (dk, rk, "dK"), (dv, rv, "dV")):
+        bwd_check(got.cpu().double().numpy(), ref, f"{n} {case}")
 
 
 def _decode_cases(n, seed):

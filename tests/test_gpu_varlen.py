@@ -238,3 +238,152 @@ def test_varlen_prefill_workload_sampled():
         vb = v[s:e, 0:2].permute(1, 0, 2).unsqueeze(0)
         ro, rl = oracle.attention(qb, kb, vb, causal=True, scale=cfg.scale)
         assert_close(o[s:e, 0:2], lse[0:2, s:e], ro[0].transpose(1, 0, 2), rl[0], f"seq {b}")
+
+
+# ---------------------------------------------------------------- backward --
+def _dout_packed(shape, seed):
+    g = torch.Generator().manual_seed(seed)
+    return torch.randn(shape, generator=g, dtype=torch.float32).to(torch.bfloat16)
+
+
+def gpu_bwd_varlen(q, k, v, do, cu_q, cu_k, causal, scale=None, grad_dtype=torch.float32,
+                   init=float("nan"), expect_error=0, max_q=None, max_k=None):
+    lq = (cu_q[1:] - cu_q[:-1]).tolist()
+    lk = (cu_k[1:] - cu_k[:-1]).tolist()
+    mq = max_q or max(max(lq), 1)
+    mk = max_k or max(max(lk), 1)
+    qd, kd, vd, dod, cq, ck = q.cuda(), k.cuda(), v.cuda(), do.cuda(), cu_q.cuda(), cu_k.cuda()
+    o = torch.empty(q.shape, dtype=torch.float32, device="cuda")
+    lse = torch.empty((q.shape[1], q.shape[0]), dtype=torch.float32, device="cuda")
+    ea.attn_fwd_varlen(qd, kd, vd, o, cq, ck, mq, mk, lse, causal=causal, scale=scale)
+    dq = torch.full(q.shape, init, dtype=grad_dtype, device="cuda")
+    dk = torch.full(k.shape, init, dtype=grad_dtype, device="cuda")
+    dv = torch.full(v.shape, init, dtype=grad_dtype, device="cuda")
+    ea.attn_bwd_varlen(qd, kd, vd, o, dod, lse, dq, dk, dv, cq, ck, mq, mk, causal=causal,
+                       scale=scale)
+    torch.cuda.synchronize()
+    assert ea.attn_last_device_error() == expect_error
+    return tuple(t.float().cpu().double().numpy() for t in (dq, dk, dv))
+
+
+def _bwd_close(got, ref, rows, what):
+    from test_gpu_bwd import _check
+    _check(got[rows], ref[rows], what)
+
+
+@pytest.mark.parametrize("d", [64, 128, 96])
+@pytest.mark.parametrize("causal", [False, True])
+def test_varlen_bwd_parity(d, causal):
+    """Packed backward against the per-sequence oracle: empty, single-row and
+    ragged sequences, GQA 4:1; rows outside every sequence never written."""
+    q, k, v, cu_q, cu_k = make_varlen_inputs(LENS, LENS, 8, 2, d, seed=870 + d, extra_rows=20)
+    do = _dout_packed(q.shape, 871 + d)
+    scale = 1 / math.sqrt(d)
+    dq, dk, dv = gpu_bwd_varlen(q, k, v, do, cu_q, cu_k, causal, scale)
+    rq, rk, rv = oracle.attention_bwd_varlen(q, k, v, do, cu_q, cu_k, causal=causal, scale=scale)
+    nq, nk = int(cu_q[-1]), int(cu_k[-1])
+    _bwd_close(dq, rq, slice(0, nq), f"dQ d={d} causal={causal}")
+    _bwd_close(dk, rk, slice(0, nk), f"dK d={d} causal={causal}")
+    _bwd_close(dv, rv, slice(0, nk), f"dV d={d} causal={causal}")
+    assert np.isnan(dq[nq:]).all() and np.isnan(dk[nk:]).all() and np.isnan(dv[nk:]).all()
+
+
+def test_varlen_bwd_cross_lengths():
+    """Queries and keys of different lengths per sequence (bottom-right causal),
+    a sequence without queries (its keys get zero gradients), bf16 gradients."""
+    lq = [100, 0, 300, 1, 129]
+    lk = [400, 50, 300, 700, 1000]
+    q, k, v, cu_q, cu_k = make_varlen_inputs(lq, lk, 4, 4, 128, seed=872)
+    do = _dout_packed(q.shape, 873)
+    for causal in (False, True):
+        dq, dk, dv = gpu_bwd_varlen(q, k, v, do, cu_q, cu_k, causal)
+        rq, rk, rv = oracle.attention_bwd_varlen(q, k, v, do, cu_q, cu_k, causal=causal)
+        _bwd_close(dq, rq, slice(None), f"dQ causal={causal}")
+        _bwd_close(dk, rk, slice(None), f"dK causal={causal}")
+        _bwd_close(dv, rv, slice(None), f"dV causal={causal}")
+        assert (dk[400:450] == 0).all() and (dv[400:450] == 0).all()
+    gq, gk, gv = gpu_bwd_varlen(q, k, v, do, cu_q, cu_k, True, grad_dtype=torch.bfloat16)
+    rq, rk, rv = oracle.attention_bwd_varlen(q, k, v, do, cu_q, cu_k, causal=True)
+    from test_gpu_bwd import _check
+    _check(gq, rq, "dQ bf16", bf16=True)
+    _check(gk, rk, "dK bf16", bf16=True)
+    _check(gv, rv, "dV bf16", bf16=True)
+
+
+def test_varlen_bwd_equal_lengths_bit_identical_to_dense():
+    """All sequences of one length: the dense backward's tiles and arithmetic
+    in the packed layout (both fed the same forward outputs)."""
+    B, H, N, d = 3, 4, 700, 128
+    q, k, v, cu_q, cu_k = make_varlen_inputs([N] * B, [N] * B, H, H, d, seed=874)
+    do = _dout_packed(q.shape, 875)
+    dense = lambda t: t.reshape(B, N, H, d).permute(0, 2, 1, 3).contiguous().cuda()  # noqa: E731
+    packed = lambda t: t.permute(0, 2, 1, 3).reshape(B * N, H, d).contiguous()  # noqa: E731
+    for causal in (False, True):
+        od, ld = ea.forward(dense(q), dense(k), dense(v), causal=causal, out_dtype=torch.float32)
+        rq, rk, rv = ea.backward(dense(q), dense(k), dense(v), od, dense(do), ld, causal=causal,
+                                 grad_dtype=torch.float32)
+        grads = [torch.empty(t.shape, dtype=torch.float32, device="cuda") for t in (q, k, v)]
+        ea.attn_bwd_varlen(q.cuda(), k.cuda(), v.cuda(), packed(od), do.cuda(),
+                           ld.permute(1, 0, 2).reshape(H, B * N).contiguous(), *grads,
+                           cu_q.cuda(), cu_k.cuda(), N, N, causal=causal)
+        torch.cuda.synchronize()
+        assert ea.attn_last_device_error() == 0
+        for got, ref in zip(grads, (rq, rk, rv)):
+            assert torch.equal(got, packed(ref)), f"causal={causal}"
+
+
+def test_varlen_bwd_bad_offsets_reported_and_skipped():
+    """A sequence longer than max_seqlen is not computed (its gradient rows are
+    left as they were), the device error word reports it, the other sequences
+    are exact."""
+    lens = [64, 236, 64]
+    q, k, v, cu_q, cu_k = make_varlen_inputs(lens, lens, 2, 2, 64, seed=876)
+    do = _dout_packed(q.shape, 877)
+    qd, kd, vd, dod, cq, ck = q.cuda(), k.cuda(), v.cuda(), do.cuda(), cu_q.cuda(), cu_k.cuda()
+    o = torch.empty(q.shape, dtype=torch.float32, device="cuda")
+    lse = torch.empty((2, q.shape[0]), dtype=torch.float32, device="cuda")
+    ea.attn_fwd_varlen(qd, kd, vd, o, cq, ck, 236, 236, lse)
+    dq = torch.full(q.shape, 7.0, dtype=torch.float32, device="cuda")
+    dk = torch.full(k.shape, 7.0, dtype=torch.float32, device="cuda")
+    dv = torch.full(v.shape, 7.0, dtype=torch.float32, device="cuda")
+    ea.attn_bwd_varlen(qd, kd, vd, o, dod, lse, dq, dk, dv, cq, ck, 200, 236)
+    torch.cuda.synchronize()
+    assert ea.attn_last_device_error() == ea.ATTN_ERR_INVALID_ARG
+    dq, dk, dv = (t.cpu().double().numpy() for t in (dq, dk, dv))
+    assert (dq[64:300] == 7.0).all() and (dk[64:300] == 7.0).all() and (dv[64:300] == 7.0).all()
+    rq, rk, rv = oracle.attention_bwd_varlen(q, k, v, do, cu_q, cu_k)
+    for rows in (slice(0, 64), slice(300, 364)):
+        _bwd_close(dq, rq, rows, "dQ")
+        _bwd_close(dk, rk, rows, "dK")
+        _bwd_close(dv, rv, rows, "dV")
+
+
+def test_varlen_bwd_repeatable_and_graph_capture():
+    q, k, v, cu_q, cu_k = make_varlen_inputs(LENS, LENS, 8, 2, 128, seed=878)
+    do = _dout_packed(q.shape, 879)
+    qd, kd, vd, dod, cq, ck = q.cuda(), k.cuda(), v.cuda(), do.cuda(), cu_q.cuda(), cu_k.cuda()
+    o = torch.empty(q.shape, dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((8, q.shape[0]), dtype=torch.float32, device="cuda")
+    ea.attn_fwd_varlen(qd, kd, vd, o, cq, ck, 600, 600, lse, causal=True)
+    grads = [torch.empty(t.shape, dtype=torch.bfloat16, device="cuda") for t in (q, k, v)]
+    ws = torch.empty(ea.attn_bwd_varlen_workspace_size(len(LENS), 8, 2, q.shape[0], 128),
+                     dtype=torch.uint8, device="cuda")
+    ea.attn_bwd_varlen(qd, kd, vd, o, dod, lse, *grads, cq, ck, 600, 600, causal=True, workspace=ws)
+    torch.cuda.synchronize()
+    ref = [t.clone() for t in grads]
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        for t in grads:
+            t.zero_()
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, stream=s):
+            ea.attn_bwd_varlen(qd, kd, vd, o, dod, lse, *grads, cq, ck, 600, 600, causal=True,
+                               workspace=ws, stream=s)
+    for _ in range(3):
+        for t in grads:
+            t.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert all(torch.equal(a, b) for a, b in zip(grads, ref))
+    assert ea.attn_last_device_error() == 0

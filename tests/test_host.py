@@ -400,6 +400,37 @@ def test_fwd_varlen_argument_checks(lib, kw, code):
     assert fwd_varlen(lib, **kw) == code
 
 
+def bwd_varlen(lib, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, do=FAKE, lse=FAKE, dq=FAKE, dk=FAKE, dv=FAKE,
+             cq=FAKE, ck=FAKE, B=2, Hq=2, Hkv=1, tq=300, tk=300, mq=200, mk=200, d=128, causal=1,
+             scale=0.1, odt=1, gdt=1, ws=FAKE, wsb=1 << 30)
+    a.update(kw)
+    return lib.attn_bwd_varlen(a["q"], a["k"], a["v"], a["o"], a["do"], a["lse"], a["dq"], a["dk"],
+                               a["dv"], a["cq"], a["ck"], a["B"], a["Hq"], a["Hkv"], a["tq"], a["tk"],
+                               a["mq"], a["mk"], a["d"], a["causal"], a["scale"], a["odt"], a["gdt"],
+                               a["ws"], a["wsb"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), 1), (dict(do=None), 1), (dict(lse=None), 1), (dict(dq=None), 1),
+    (dict(cq=None), 1), (dict(ck=FAKE + 2), 1), (dict(dk=FAKE + 4), 1), (dict(tq=0), 1),
+    (dict(mq=301), 1), (dict(B=0), 1), (dict(Hq=3, Hkv=2), 1), (dict(causal=2), 1),
+    (dict(gdt=7), 1), (dict(d=100), 2), (dict(d=136), 2), (dict(d=256), 2),
+    (dict(ws=None), 5), (dict(wsb=16), 5), (dict(ws=FAKE + 4), 5),
+])
+def test_bwd_varlen_argument_checks(lib, kw, code):
+    """Every rejection happens on the host, before a device is touched."""
+    assert bwd_varlen(lib, **kw) == code
+
+
+def test_bwd_varlen_workspace_size():
+    # 2 vectors x Hq x (total_q + 132 B, rounded up to 4) floats
+    assert ea.attn_bwd_varlen_workspace_size(3, 4, 2, 1000, 128) == 2 * 4 * ((1000 + 396 + 3) // 4 * 4) * 4
+    assert ea.attn_bwd_varlen_workspace_size(3, 4, 2, 1000, 256) == 0   # d > 128: not supported
+    assert ea.attn_bwd_varlen_workspace_size(3, 4, 3, 1000, 128) == 0   # Hq % Hkv
+    assert ea.attn_bwd_varlen_workspace_size(0, 4, 2, 1000, 128) == 0
+
+
 def test_fp8_sizes_and_argument_checks(lib):
     assert ea.attn_fp8_codes_bytes(2, 3, 300, 128) == 2 * 3 * 300 * 128
     assert ea.attn_fp8_codes_bytes(2, 3, 300, 128, transpose=True) == 2 * 3 * 128 * 304

@@ -78,3 +78,53 @@ def test_varlen_oracle_empty_sequence_changes_nothing():
     cu2 = torch.tensor([0, 12, 20], dtype=torch.int32)
     o2, l2 = oracle.attention_varlen(q, k, v, cu2, cu2, causal=True)
     assert np.array_equal(o, o2) and np.array_equal(lse, l2)
+
+
+# ---------------------------------------------------------------- backward --
+def _autograd_reference(q, k, v, do, cu_q, cu_k, causal, scale):
+    """float64 autograd of a plain softmax attention, sequence by sequence."""
+    Hq, Hkv = q.shape[1], k.shape[1]
+    grp = Hq // Hkv
+    qf, kf, vf = (t.double().clone().requires_grad_(True) for t in (q, k, v))
+    dof = do.double()
+    for b in range(len(cu_q) - 1):
+        qs, qe, ks, ke = int(cu_q[b]), int(cu_q[b + 1]), int(cu_k[b]), int(cu_k[b + 1])
+        nq, nk = qe - qs, ke - ks
+        if nq == 0:
+            continue
+        for h in range(Hq):
+            s = scale * qf[qs:qe, h] @ kf[ks:ke, h // grp].T
+            if causal:
+                mask = torch.arange(nk)[None, :] > torch.arange(nq)[:, None] + (nk - nq)
+                s = s.masked_fill(mask, float("-inf"))
+            o = torch.softmax(s, dim=1) @ vf[ks:ke, h // grp]
+            (o * dof[qs:qe, h]).sum().backward()
+    return tuple(t.grad.numpy() for t in (qf, kf, vf))
+
+
+def test_varlen_bwd_oracle_matches_autograd_per_sequence():
+    """The packed backward oracle against float64 autograd of plain softmax
+    attention, GQA, causal (bottom-right) and not, with a sequence without
+    queries between two others (its keys get zero gradients)."""
+    for causal in (False, True):
+        lq, lk = [5, 0, 9, 1], [7, 4, 12, 3]
+        q, k, v, cu_q, cu_k = make_varlen_inputs(lq, lk, 4, 2, 16, seed=61)
+        g = torch.Generator().manual_seed(62)
+        do = torch.randn(q.shape, generator=g).to(torch.bfloat16)
+        gq, gk, gv = oracle.attention_bwd_varlen(q, k, v, do, cu_q, cu_k, causal=causal, scale=0.3)
+        rq, rk, rv = _autograd_reference(q, k, v, do, cu_q, cu_k, causal, 0.3)
+        np.testing.assert_allclose(gq, rq, rtol=1e-10, atol=1e-12)
+        np.testing.assert_allclose(gk, rk, rtol=1e-10, atol=1e-12)
+        np.testing.assert_allclose(gv, rv, rtol=1e-10, atol=1e-12)
+        assert (gk[7:11] == 0).all() and (gv[7:11] == 0).all()   # the keys of sequence 1
+
+
+def test_varlen_bwd_oracle_equal_lengths_is_the_dense_oracle():
+    B, H, N, d = 3, 2, 20, 8
+    q, k, v, cu_q, cu_k = make_varlen_inputs([N] * B, [N] * B, H, H, d, seed=63)
+    do = torch.randn(q.shape, generator=torch.Generator().manual_seed(64)).to(torch.bfloat16)
+    gq, gk, gv = oracle.attention_bwd_varlen(q, k, v, do, cu_q, cu_k, causal=True)
+    dense = lambda t: t.reshape(B, N, H, d).permute(0, 2, 1, 3).contiguous()  # noqa: E731
+    rq, rk, rv = oracle.attention_bwd(dense(q), dense(k), dense(v), dense(do), causal=True)
+    back = lambda a: a.transpose(0, 2, 1, 3).reshape(B * N, H, d)  # noqa: E731
+    assert np.array_equal(gq, back(rq)) and np.array_equal(gk, back(rk)) and np.array_equal(gv, back(rv))
