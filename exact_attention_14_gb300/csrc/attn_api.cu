@@ -418,7 +418,7 @@ attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* 
 
 size_t attn_bwd_varlen_workspace_size(int B, int Hq, int Hkv, int total_q, int d) {
     if (check_common(B, Hq, Hkv, d, 1.0f, ATTN_OUT_BF16) != ATTN_OK) return 0;
-    if (total_q < 1 || total_q > kMaxPackedRows || !head_dim_supported(d)) return 0;
+    if (total_q < 1 || total_q > kMaxPackedRows || !fwd_head_dim_supported(d)) return 0;
     return bwd_varlen_workspace_bytes(B, Hq, total_q);
 }
 
@@ -443,7 +443,7 @@ attn_status_t attn_bwd_varlen(const void* q, const void* k, const void* v, const
     if (!aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
         return ATTN_ERR_INVALID_ARG;
     if (grad_dtype != ATTN_OUT_BF16 && grad_dtype != ATTN_OUT_F32) return ATTN_ERR_INVALID_ARG;
-    if (!head_dim_supported(d)) return ATTN_ERR_UNSUPPORTED;
+    if (!fwd_head_dim_supported(d)) return ATTN_ERR_UNSUPPORTED;
     const size_t need = bwd_varlen_workspace_bytes(B, Hq, total_q);
     if (!workspace || workspace_bytes < need || !aligned16(workspace)) return ATTN_ERR_WORKSPACE;
     DeviceInfo dev;

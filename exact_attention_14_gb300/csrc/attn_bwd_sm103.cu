@@ -952,8 +952,10 @@ __device__ void dq_ds(int wq, int lane, DqBars* bars, uint32_t tmem, const BwdPa
     const size_t bh = (size_t)w.b * p.Hq + w.hq;
     const size_t vrow = VARLEN ? (size_t)w.hq * p.vstride + (size_t)(w.vbase + row)
                                : bh * p.Nq_pad + row;
-    const float lse2 = p.lse2[vrow];  // +inf past the last query: P = 0
-    const float dval = p.dvec[vrow];
+    // +inf past the last query: P = 0 (a tile with no work reads nothing: its
+    // rows may lie past the sequence's rows of lse2 / dvec)
+    const float lse2 = w.n_kv > 0 ? p.lse2[vrow] : INFINITY;
+    const float dval = w.n_kv > 0 ? p.dvec[vrow] : 0.f;
     const uint64_t c2 = f2(p.c, p.c), nl2 = f2(-lse2, -lse2), nd2 = f2(-dval, -dval);
     bool ok = true;
     for (int j = 0; j < w.n_kv && ok; ++j) {
@@ -1388,6 +1390,7 @@ __device__ __forceinline__ void wbwd_issue_ta(uint32_t d_tmem, uint32_t a_tmem, 
 
 struct WideDkdvWork {
     int b, g, kt, k0, half, qt_first, n_qt_cta, n_tiles;
+    int nq, nk, off, qb, kb, vbase;  // as in BwdWork
 };
 
 // CTA index -> (column half, then the dkdv pass's section order of key tiles).
@@ -1416,10 +1419,51 @@ __device__ __forceinline__ WideDkdvWork wide_dkdv_work(const BwdParams& p) {
     w.qt_first = first;
     w.n_qt_cta = n_qt - first > 0 ? n_qt - first : 0;
     w.n_tiles = w.n_qt_cta * p.group;
+    w.nq = p.Nq;
+    w.nk = p.Nk;
+    w.off = p.off;
+    w.qb = w.kb = w.vbase = 0;
     return w;
 }
 
-template <bool OUT_F32>
+// The same for packed batches: CTA index = ((b * Hkv + g) * n_kt + kt) * 2 +
+// column half, n_kt for the longest key length; key tiles past a sequence's
+// end, and every tile of a sequence whose offsets fail the checks, have no
+// work and write nothing.
+__device__ __forceinline__ WideDkdvWork wide_dkdv_work_varlen(const BwdParams& p, unsigned int* err) {
+    WideDkdvWork w;
+    const int idx = (int)(blockIdx.x >> 1);
+    w.half = (int)(blockIdx.x & 1u);
+    const int per_b = p.Hkv * p.n_kt;
+    w.b = idx / per_b;
+    const int rem = idx - w.b * per_b;
+    w.g = rem / p.n_kt;
+    w.kt = rem - w.g * p.n_kt;
+    w.k0 = w.kt * kBT;
+    int q0, nq, k0, nk;
+    if (!bwd_varlen_seq(p, w.b, q0, nq, k0, nk)) {
+        if (threadIdx.x == 0) atomicOr(err, kErrBadSeqlen);
+        q0 = nq = k0 = nk = 0;
+    }
+    w.nq = nq;
+    w.nk = nk;
+    w.off = nk - nq;
+    w.qb = q0;
+    w.kb = k0;
+    w.vbase = varlen_vbase(q0, w.b);
+    const int n_qt = (nq + kWQ - 1) / kWQ;
+    int first = 0;
+    if (p.causal) {
+        const int lo = w.k0 - w.off;
+        first = lo <= 0 ? 0 : lo / kWQ;
+    }
+    w.qt_first = first;
+    w.n_qt_cta = (w.k0 < nk && n_qt - first > 0) ? n_qt - first : 0;
+    w.n_tiles = w.n_qt_cta * p.group;
+    return w;
+}
+
+template <bool OUT_F32, bool VARLEN>
 __global__ void __launch_bounds__(kBwdThreads, 1)
 attn_bwd_wide_dkdv_kernel(const __grid_constant__ CUtensorMap tq64, const __grid_constant__ CUtensorMap tdo64,
                           const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
@@ -1436,7 +1480,7 @@ attn_bwd_wide_dkdv_kernel(const __grid_constant__ CUtensorMap tq64, const __grid
     const volatile int* abort_flag = &bars->abort;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const WideDkdvWork w = wide_dkdv_work(p);
+    const WideDkdvWork w = VARLEN ? wide_dkdv_work_varlen(p, err) : wide_dkdv_work(p);
     auto raise_abort = [&]() {
         atomicOr(err, kErrTimeout);
         *((volatile int*)&bars->abort) = 1;
@@ -1477,21 +1521,43 @@ attn_bwd_wide_dkdv_kernel(const __grid_constant__ CUtensorMap tq64, const __grid
         // has read dO_{i-1}, and Q_{i+1} once dK(i-1) and the P/dS warps are done
         // with buffer (i+1) & 1.
         const bool leader = elect_one();
-        const int kvh = w.b * p.Hkv + w.g;
+        const int kvh = VARLEN ? w.g : w.b * p.Hkv + w.g;
         if (leader) {
             const uint32_t bar = smem_u32(&bars->kv_full);
             mbar_arrive_expect_tx(bar, 2 * C::kBig);
 #pragma unroll
             for (int c = 0; c < kWD / 64; ++c) {
-                tma_load_3d(smem_u32(smem + C::kK) + c * 16384, &tk, bar, 64 * c, w.k0, kvh);
-                tma_load_3d(smem_u32(smem + C::kV) + c * 16384, &tv, bar, 64 * c, w.k0, kvh);
+                if constexpr (VARLEN) {
+                    const int r = kRaggedWindow - w.nk + w.k0;
+                    tma_load_5d(smem_u32(smem + C::kK) + c * 16384, &tk, bar, 64 * c, kvh, r, w.kb + w.nk,
+                                kRaggedWindow);
+                    tma_load_5d(smem_u32(smem + C::kV) + c * 16384, &tv, bar, 64 * c, kvh, r, w.kb + w.nk,
+                                kRaggedWindow);
+                } else {
+                    tma_load_3d(smem_u32(smem + C::kK) + c * 16384, &tk, bar, 64 * c, w.k0, kvh);
+                    tma_load_3d(smem_u32(smem + C::kV) + c * 16384, &tv, bar, 64 * c, w.k0, kvh);
+                }
             }
         }
         __syncwarp();
+        // tile i: its first query row, and its head (an index into [B * Hq], or
+        // into [Hq] of the packed rows)
         auto tile_rows = [&](int i, int& q0, int& bh) {
             const int hq = w.g * p.group + i / w.n_qt_cta;
             q0 = (w.qt_first + i % w.n_qt_cta) * kWQ;
-            bh = w.b * p.Hq + hq;
+            bh = VARLEN ? hq : w.b * p.Hq + hq;
+        };
+        // the 64-row tile of Q or dO at q0 (packed: rows past the sequence's
+        // queries read as zeros)
+        auto load_rows = [&](uint32_t dst, const CUtensorMap* map, uint32_t bar, int q0, int bh) {
+#pragma unroll
+            for (int c = 0; c < kWD / 64; ++c) {
+                if constexpr (VARLEN)
+                    tma_load_5d(dst + c * 8192, map, bar, 64 * c, bh, kRaggedWindow - w.nq + q0, w.qb + w.nq,
+                                kRaggedWindow);
+                else
+                    tma_load_3d(dst + c * 8192, map, bar, 64 * c, q0, bh);
+            }
         };
         bool ok = true;
         int nq = 0, ndo = 0;  // Q and dO tiles issued
@@ -1506,10 +1572,9 @@ attn_bwd_wide_dkdv_kernel(const __grid_constant__ CUtensorMap tq64, const __grid
             if (leader) {
                 const uint32_t bar = smem_u32(&bars->q_full[qb]);
                 mbar_arrive_expect_tx(bar, C::kSmall + 2 * kWQ * 4);
-#pragma unroll
-                for (int c = 0; c < kWD / 64; ++c)
-                    tma_load_3d(smem_u32(smem + C::kQ + qb * C::kSmall) + c * 8192, &tq64, bar, 64 * c, q0, bh);
-                const size_t row = (size_t)bh * p.Nq_pad + q0;
+                load_rows(smem_u32(smem + C::kQ + qb * C::kSmall), &tq64, bar, q0, bh);
+                const size_t row = VARLEN ? (size_t)bh * p.vstride + (size_t)(w.vbase + q0)
+                                          : (size_t)bh * p.Nq_pad + q0;
                 const uint32_t ld = smem_u32(smem + C::kLD + qb * 512);
                 bulk_load(ld, p.lse2 + row, kWQ * 4, bar);
                 bulk_load(ld + kWQ * 4, p.dvec + row, kWQ * 4, bar);
@@ -1526,9 +1591,7 @@ attn_bwd_wide_dkdv_kernel(const __grid_constant__ CUtensorMap tq64, const __grid
             if (leader) {
                 const uint32_t bar = smem_u32(&bars->do_full);
                 mbar_arrive_expect_tx(bar, C::kSmall);
-#pragma unroll
-                for (int c = 0; c < kWD / 64; ++c)
-                    tma_load_3d(smem_u32(smem + C::kDO) + c * 8192, &tdo64, bar, 64 * c, q0, bh);
+                load_rows(smem_u32(smem + C::kDO), &tdo64, bar, q0, bh);
             }
             __syncwarp();
             ++ndo;
@@ -1625,8 +1688,8 @@ attn_bwd_wide_dkdv_kernel(const __grid_constant__ CUtensorMap tq64, const __grid
             if (!ok) break;
             tc_fence_after();
             const int q0 = (w.qt_first + i % w.n_qt_cta) * kWQ;
-            const int lim = jg - p.off - q0;  // causal: column x allowed iff x >= lim
-            const bool masked = p.causal && (q0 + p.off < w.k0 + kBT - 1);
+            const int lim = jg - w.off - q0;  // causal: column x allowed iff x >= lim
+            const bool masked = p.causal && (q0 + w.off < w.k0 + kBT - 1);
             const uint32_t lse2s = smem_u32(smem + C::kLD + (i & 1) * 512);
             const uint32_t ds_vec = lse2s + kWQ * 4;
             float pf0[32], pf1[32];
@@ -1673,8 +1736,14 @@ attn_bwd_wide_dkdv_kernel(const __grid_constant__ CUtensorMap tq64, const __grid
             raise_abort();
         } else {
             // dK_h = scale dS^T Q_h, dV_h = P^T dO_h: columns [128h, 128h + 128)
-            const size_t wrow0 = ((size_t)w.b * p.Hkv + w.g) * p.Nk + (size_t)(w.k0 + wq * 32);
-            const int rows_live = p.Nk - (w.k0 + wq * 32);
+            // (packed batches: rows of Hkv * d elements, the head's d columns at g * d)
+            const size_t wrow0 = VARLEN ? (size_t)(w.kb + w.k0 + wq * 32)
+                                        : ((size_t)w.b * p.Hkv + w.g) * p.Nk + (size_t)(w.k0 + wq * 32);
+            const int rows_live = w.nk - (w.k0 + wq * 32);
+            const size_t row_elems = VARLEN ? (size_t)p.Hkv * p.d_act : (size_t)p.d_act;
+            const size_t head_off = VARLEN ? (size_t)w.g * p.d_act * (OUT_F32 ? 4 : 2) : 0;
+            void* dk_base = static_cast<uint8_t*>(p.dk) + head_off;
+            void* dv_base = static_cast<uint8_t*>(p.dv) + head_off;
             const int c0 = w.half * 128;
             const bool have = w.n_tiles > 0;
             if (have) {
@@ -1694,14 +1763,14 @@ attn_bwd_wide_dkdv_kernel(const __grid_constant__ CUtensorMap tq64, const __grid
                     }
 #pragma unroll
                     for (int x = 0; x < 32; ++x) v[x] = have ? __uint_as_float(r[x]) : 0.f;
-                    if (nc > 0) store_rows32_pairs<OUT_F32>(p.dv, wrow0, p.d_act, c0 + cc, v, nc, rows_live, lane);
+                    if (nc > 0) store_rows32_pairs<OUT_F32>(dv_base, wrow0, row_elems, c0 + cc, v, nc, rows_live, lane);
                     if (have) {
                         tmem_ld32(tmem + 256 + cc + lane_off, r);
                         tmem_wait_ld();
                     }
 #pragma unroll
                     for (int x = 0; x < 32; ++x) v[x] = have ? __uint_as_float(r[x]) * p.scale : 0.f;
-                    if (nc > 0) store_rows32_pairs<OUT_F32>(p.dk, wrow0, p.d_act, c0 + cc, v, nc, rows_live, lane);
+                    if (nc > 0) store_rows32_pairs<OUT_F32>(dk_base, wrow0, row_elems, c0 + cc, v, nc, rows_live, lane);
                 }
             }
         }
@@ -1717,21 +1786,32 @@ attn_bwd_wide_dkdv_kernel(const __grid_constant__ CUtensorMap tq64, const __grid
 
 struct WideDqWork {
     int b, g, hq, q0, n_kv;
+    int nq, nk, off, qb, kb, vbase;  // as in BwdWork
 };
 
-// CTA index -> (b, query head, 128-row Q tile) in the dq pass's section order;
-// n_kv counts 64-key tiles.
-__device__ __forceinline__ WideDqWork wide_dq_work(const BwdParams& p) {
-    const DqWork d = dq_work(p);
+// CTA index -> (b, query head, 128-row Q tile) in the dq pass's section order
+// (packed batches: the order of dq_work_varlen); n_kv counts 64-key tiles, 0
+// for a Q tile past the sequence's queries.
+template <bool VARLEN>
+__device__ __forceinline__ WideDqWork wide_dq_work(const BwdParams& p, unsigned int* err) {
+    const DqWork d = VARLEN ? dq_work_varlen(p, err) : dq_work(p);
     WideDqWork w;
     w.b = d.b;
     w.g = d.g;
     w.hq = d.hq;
     w.q0 = d.q0;
-    const int n_t64 = (p.Nk + kWQ - 1) / kWQ;
-    if (p.causal) {
-        const int last_row = (w.q0 + kBT - 1 < p.Nq - 1 ? w.q0 + kBT - 1 : p.Nq - 1);
-        const int last_key = last_row + p.off;
+    w.nq = d.nq;
+    w.nk = d.nk;
+    w.off = d.off;
+    w.qb = d.qb;
+    w.kb = d.kb;
+    w.vbase = d.vbase;
+    const int n_t64 = (w.nk + kWQ - 1) / kWQ;
+    if (w.q0 >= w.nq) {
+        w.n_kv = 0;
+    } else if (p.causal) {
+        const int last_row = (w.q0 + kBT - 1 < w.nq - 1 ? w.q0 + kBT - 1 : w.nq - 1);
+        const int last_key = last_row + w.off;
         const int n = last_key < 0 ? 0 : last_key / kWQ + 1;
         w.n_kv = n < n_t64 ? n : n_t64;
     } else {
@@ -1740,7 +1820,7 @@ __device__ __forceinline__ WideDqWork wide_dq_work(const BwdParams& p) {
     return w;
 }
 
-template <bool OUT_F32>
+template <bool OUT_F32, bool VARLEN>
 __global__ void __launch_bounds__(kBwdThreads, 1)
 attn_bwd_wide_dq_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tdo,
                         const __grid_constant__ CUtensorMap tk64, const __grid_constant__ CUtensorMap tv64,
@@ -1757,7 +1837,7 @@ attn_bwd_wide_dq_kernel(const __grid_constant__ CUtensorMap tq, const __grid_con
     const volatile int* abort_flag = &bars->abort;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const WideDqWork w = wide_dq_work(p);
+    const WideDqWork w = wide_dq_work<VARLEN>(p, err);
     auto raise_abort = [&]() {
         atomicOr(err, kErrTimeout);
         *((volatile int*)&bars->abort) = 1;
@@ -1791,22 +1871,44 @@ attn_bwd_wide_dq_kernel(const __grid_constant__ CUtensorMap tq, const __grid_con
     tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
     const size_t bh = (size_t)w.b * p.Hq + w.hq;
+    // the K/V head and the Q / dO head as the tensor maps index them
+    const int kvh = VARLEN ? w.g : w.b * p.Hkv + w.g;
+    const int qh = VARLEN ? w.hq : (int)bh;
 
     if (warp == 0) {
         // ---- producer: Q, dO once; K_j into buffer j & 1 once dQ(j-2) has read
         // it; V_j into its one buffer once dP(j-1) has read it.
         const bool leader = elect_one();
-        const int kvh = w.b * p.Hkv + w.g;
         if (leader) {
             const uint32_t bar = smem_u32(&bars->res_full);
             mbar_arrive_expect_tx(bar, 2 * C::kBig);
 #pragma unroll
             for (int c = 0; c < kWD / 64; ++c) {
-                tma_load_3d(smem_u32(smem + C::kQ) + c * 16384, &tq, bar, 64 * c, w.q0, (int)bh);
-                tma_load_3d(smem_u32(smem + C::kDO) + c * 16384, &tdo, bar, 64 * c, w.q0, (int)bh);
+                if constexpr (VARLEN) {
+                    const int r = kRaggedWindow - w.nq + w.q0;
+                    tma_load_5d(smem_u32(smem + C::kQ) + c * 16384, &tq, bar, 64 * c, qh, r, w.qb + w.nq,
+                                kRaggedWindow);
+                    tma_load_5d(smem_u32(smem + C::kDO) + c * 16384, &tdo, bar, 64 * c, qh, r, w.qb + w.nq,
+                                kRaggedWindow);
+                } else {
+                    tma_load_3d(smem_u32(smem + C::kQ) + c * 16384, &tq, bar, 64 * c, w.q0, qh);
+                    tma_load_3d(smem_u32(smem + C::kDO) + c * 16384, &tdo, bar, 64 * c, w.q0, qh);
+                }
             }
         }
         __syncwarp();
+        // the 64-key tile j of K or V (packed: rows past the sequence's keys
+        // read as zeros)
+        auto load_keys = [&](uint32_t dst, const CUtensorMap* map, uint32_t bar, int j) {
+#pragma unroll
+            for (int c = 0; c < kWD / 64; ++c) {
+                if constexpr (VARLEN)
+                    tma_load_5d(dst + c * 8192, map, bar, 64 * c, kvh, kRaggedWindow - w.nk + j * kWQ,
+                                w.kb + w.nk, kRaggedWindow);
+                else
+                    tma_load_3d(dst + c * 8192, map, bar, 64 * c, j * kWQ, kvh);
+            }
+        };
         bool ok = true;
         int nk = 0, nv = 0;  // K and V tiles issued
         auto load_k = [&](int j) {
@@ -1818,10 +1920,7 @@ attn_bwd_wide_dq_kernel(const __grid_constant__ CUtensorMap tq, const __grid_con
             if (leader) {
                 const uint32_t bar = smem_u32(&bars->k_full[kb]);
                 mbar_arrive_expect_tx(bar, C::kSmall);
-#pragma unroll
-                for (int c = 0; c < kWD / 64; ++c)
-                    tma_load_3d(smem_u32(smem + C::kK + kb * C::kSmall) + c * 8192, &tk64, bar, 64 * c,
-                                j * kWQ, kvh);
+                load_keys(smem_u32(smem + C::kK + kb * C::kSmall), &tk64, bar, j);
             }
             __syncwarp();
             ++nk;
@@ -1833,9 +1932,7 @@ attn_bwd_wide_dq_kernel(const __grid_constant__ CUtensorMap tq, const __grid_con
             if (leader) {
                 const uint32_t bar = smem_u32(&bars->v_full);
                 mbar_arrive_expect_tx(bar, C::kSmall);
-#pragma unroll
-                for (int c = 0; c < kWD / 64; ++c)
-                    tma_load_3d(smem_u32(smem + C::kV) + c * 8192, &tv64, bar, 64 * c, j * kWQ, kvh);
+                load_keys(smem_u32(smem + C::kV), &tv64, bar, j);
             }
             __syncwarp();
             ++nv;
@@ -1917,8 +2014,11 @@ attn_bwd_wide_dq_kernel(const __grid_constant__ CUtensorMap tq, const __grid_con
         const uint32_t lane_off = uint32_t(wq * 32) << 16;
         const uint32_t tdP = tmem + 128 + lane_off;
         const int row = w.q0 + wq * 32 + lane;
-        const float lse2 = p.lse2[bh * p.Nq_pad + row];  // +inf past Nq: P = 0
-        const float dval = p.dvec[bh * p.Nq_pad + row];
+        const size_t vrow = VARLEN ? (size_t)w.hq * p.vstride + (size_t)(w.vbase + row)
+                                   : bh * p.Nq_pad + row;
+        // +inf past the last query: P = 0 (a tile with no work reads nothing)
+        const float lse2 = w.n_kv > 0 ? p.lse2[vrow] : INFINITY;
+        const float dval = w.n_kv > 0 ? p.dvec[vrow] : 0.f;
         const uint64_t c2 = f2(p.c, p.c), nl2 = f2(-lse2, -lse2), nd2 = f2(-dval, -dval);
         bool ok = true;
         for (int j = 0; j < w.n_kv && ok; ++j) {
@@ -1927,7 +2027,7 @@ attn_bwd_wide_dq_kernel(const __grid_constant__ CUtensorMap tq, const __grid_con
                                                    abort_flag, 32));
             if (!ok) break;
             tc_fence_after();
-            const int lim = row + p.off - j * kWQ;  // causal: key column c allowed iff c <= lim
+            const int lim = row + w.off - j * kWQ;  // causal: key column c allowed iff c <= lim
             const bool masked = __any_sync(0xFFFFFFFFu, p.causal && lim < kWQ - 1);
             float pf0[32], pf1[32];
             {
@@ -1967,9 +2067,13 @@ attn_bwd_wide_dq_kernel(const __grid_constant__ CUtensorMap tq, const __grid_con
         if (!ok) {
             raise_abort();
         } else {
-            // every lane runs the (warp-collective) TMEM loads; rows past Nq store nothing
-            const size_t wrow0 = bh * p.Nq + (size_t)(w.q0 + wq * 32);
-            const int rows_live = p.Nq - (w.q0 + wq * 32);
+            // every lane runs the (warp-collective) TMEM loads; rows past Nq store
+            // nothing (packed batches: rows of Hq * d elements, the head's d
+            // columns at hq * d)
+            const size_t wrow0 = VARLEN ? (size_t)(w.qb + w.q0 + wq * 32) : bh * p.Nq + (size_t)(w.q0 + wq * 32);
+            const int rows_live = w.nq - (w.q0 + wq * 32);
+            const size_t row_elems = VARLEN ? (size_t)p.Hq * p.d_act : (size_t)p.d_act;
+            void* dq_base = static_cast<uint8_t*>(p.dq) + (VARLEN ? (size_t)w.hq * p.d_act * (OUT_F32 ? 4 : 2) : 0);
 #pragma unroll 1
             for (int cc = 0; cc < kWD; cc += 32) {
                 float v[32];
@@ -1984,7 +2088,7 @@ attn_bwd_wide_dq_kernel(const __grid_constant__ CUtensorMap tq, const __grid_con
                     for (int x = 0; x < 32; ++x) v[x] = 0.f;
                 }
                 const int nc = p.d_act - cc < 32 ? p.d_act - cc : 32;
-                if (nc > 0) store_rows32_pairs<OUT_F32>(p.dq, wrow0, p.d_act, cc, v, nc, rows_live, lane);
+                if (nc > 0) store_rows32_pairs<OUT_F32>(dq_base, wrow0, row_elems, cc, v, nc, rows_live, lane);
             }
         }
     }
@@ -1997,7 +2101,7 @@ attn_bwd_wide_dq_kernel(const __grid_constant__ CUtensorMap tq, const __grid_con
     }
 }
 
-template <bool OUT_F32>
+template <bool OUT_F32, bool VARLEN = false>
 attn_status_t launch_bwd_wide_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                 const CUtensorMap& tdo, const CUtensorMap& tq64,
                                 const CUtensorMap& tk64, const CUtensorMap& tv64,
@@ -2006,25 +2110,29 @@ attn_status_t launch_bwd_wide_t(const CUtensorMap& tq, const CUtensorMap& tk, co
                                 float* dvec, cudaStream_t stream, const DeviceInfo& dev) {
     static int attr_set[64] = {0};
     if (dev.device < 64 && !attr_set[dev.device]) {
-        if (cudaFuncSetAttribute(attn_bwd_wide_dkdv_kernel<OUT_F32>,
+        if (cudaFuncSetAttribute(attn_bwd_wide_dkdv_kernel<OUT_F32, VARLEN>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  WideDkdvCfg::kSmemBytes) != cudaSuccess ||
-            cudaFuncSetAttribute(attn_bwd_wide_dq_kernel<OUT_F32>,
+            cudaFuncSetAttribute(attn_bwd_wide_dq_kernel<OUT_F32, VARLEN>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  WideDqCfg::kSmemBytes) != cudaSuccess)
             return ATTN_ERR_CUDA;
         attr_set[dev.device] = 1;
     }
-    const long long rows_pad = (long long)p.B * p.Hq * p.Nq_pad;
-    attn_status_t st = launch_bwd_prep(o, o_f32, dout, lse, lse2, dvec, rows_pad, p.Nq, p.Nq_pad,
-                                       p.d_act, stream);
+    attn_status_t st;
+    if constexpr (VARLEN) {
+        st = launch_bwd_prep_varlen(o, o_f32, dout, lse, lse2, dvec, p, stream);
+    } else {
+        const long long rows_pad = (long long)p.B * p.Hq * p.Nq_pad;
+        st = launch_bwd_prep(o, o_f32, dout, lse, lse2, dvec, rows_pad, p.Nq, p.Nq_pad, p.d_act, stream);
+    }
     if (st != ATTN_OK) return st;
     const long long kv_ctas = 2ll * p.B * p.Hkv * p.n_kt;  // two column halves per key tile
-    attn_bwd_wide_dkdv_kernel<OUT_F32><<<(unsigned)kv_ctas, kBwdThreads, WideDkdvCfg::kSmemBytes, stream>>>(
+    attn_bwd_wide_dkdv_kernel<OUT_F32, VARLEN><<<(unsigned)kv_ctas, kBwdThreads, WideDkdvCfg::kSmemBytes, stream>>>(
         tq64, tdo64, tk, tv, p, dev.err_word);
     if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
     const long long q_ctas = (long long)p.B * p.Hq * ((p.Nq + kBT - 1) / kBT);
-    attn_bwd_wide_dq_kernel<OUT_F32><<<(unsigned)q_ctas, kBwdThreads, WideDqCfg::kSmemBytes, stream>>>(
+    attn_bwd_wide_dq_kernel<OUT_F32, VARLEN><<<(unsigned)q_ctas, kBwdThreads, WideDqCfg::kSmemBytes, stream>>>(
         tq, tdo, tk64, tv64, p, dev.err_word);
     return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
@@ -2042,7 +2150,6 @@ attn_status_t launch_bwd_varlen(const void* q, const void* k, const void* v, con
                                 int total_k, int max_q, int max_k, int d, int causal, float scale,
                                 attn_out_dtype_t o_dtype, attn_out_dtype_t grad_dtype,
                                 void* workspace, cudaStream_t stream, const DeviceInfo& dev) {
-    if (d > 128) return ATTN_ERR_UNSUPPORTED;
     BwdParams p;
     p.B = B;
     p.Hq = Hq;
@@ -2081,6 +2188,19 @@ attn_status_t launch_bwd_varlen(const void* q, const void* k, const void* v, con
     if ((st = encode_tmap_ragged(&tdo, dout, false, d, Hq, 64, kBT, true)) != ATTN_OK) return st;
     const int o_f32 = o_dtype == ATTN_OUT_F32;
     const bool g32 = grad_dtype == ATTN_OUT_F32;
+    if (d > 128) {
+        // 64-row boxes for the streamed tiles of the wide passes
+        if ((long long)B * Hkv * p.n_kt * 2 >= (1ll << 31)) return ATTN_ERR_UNSUPPORTED;
+        CUtensorMap tq64, tk64, tv64, tdo64;
+        if ((st = encode_tmap_ragged(&tq64, q, false, d, Hq, 64, kWQ, true)) != ATTN_OK) return st;
+        if ((st = encode_tmap_ragged(&tk64, k, false, d, Hkv, 64, kWQ, true)) != ATTN_OK) return st;
+        if ((st = encode_tmap_ragged(&tv64, v, false, d, Hkv, 64, kWQ, true)) != ATTN_OK) return st;
+        if ((st = encode_tmap_ragged(&tdo64, dout, false, d, Hq, 64, kWQ, true)) != ATTN_OK) return st;
+        return g32 ? launch_bwd_wide_t<true, true>(tq, tk, tv, tdo, tq64, tk64, tv64, tdo64, p, o, o_f32,
+                                                   dout, lse, lse2, dvec, stream, dev)
+                   : launch_bwd_wide_t<false, true>(tq, tk, tv, tdo, tq64, tk64, tv64, tdo64, p, o, o_f32,
+                                                    dout, lse, lse2, dvec, stream, dev);
+    }
     if (pad_head_dim(d) == 128)
         return g32 ? launch_bwd_t<128, true, true>(tq, tk, tv, tdo, p, o, o_f32, dout, lse, lse2, dvec, stream, dev)
                    : launch_bwd_t<128, false, true>(tq, tk, tv, tdo, p, o, o_f32, dout, lse, lse2, dvec, stream, dev);

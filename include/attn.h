@@ -283,17 +283,18 @@ size_t attn_bwd_varlen_workspace_size(int B, int Hq, int Hkv, int total_q, int d
  *   workspace  device memory of at least attn_bwd_varlen_workspace_size bytes,
  *            16-byte aligned; contents need no initialisation.
  *
- * Supported: 8 <= d <= 128 (d % 8 == 0); the other limits of attn_fwd_varlen.
+ * Supported: 8 <= d <= 256 (d % 8 == 0); the other limits of attn_fwd_varlen.
  * The same three kernels as attn_bwd (D and the base-2 LSE per row, the
- * K/V-outer pass, the Q-outer pass) read the packed rows through the packed
- * forward's ragged tensor maps; CTAs cover every sequence at the longest
- * lengths, and the tiles past a sequence's end have no work.  A sequence whose
+ * K/V-outer pass, the Q-outer pass; for 128 < d <= 256 the 256-column passes)
+ * read the packed rows through the packed forward's ragged tensor maps; CTAs
+ * cover every sequence at the longest lengths, and the tiles past a
+ * sequence's end have no work.  A sequence whose
  * offsets fail the checks of attn_fwd_varlen is not computed (its gradient
  * rows are left as they were) and attn_last_device_error() then reports
  * ATTN_ERR_INVALID_ARG.  Rows outside every sequence are neither read nor
  * written.  Gradients are bit-identical from run to run.  Returns ATTN_OK once
  * the kernels are enqueued; ATTN_ERR_WORKSPACE for a missing or short
- * workspace; ATTN_ERR_UNSUPPORTED for d > 128.
+ * workspace; ATTN_ERR_UNSUPPORTED for d outside the supported range.
  */
 attn_status_t attn_bwd_varlen(const void* q, const void* k, const void* v, const void* o,
                               const void* dout, const float* lse, void* dq, void* dk, void* dv,

@@ -271,7 +271,7 @@ def _bwd_close(got, ref, rows, what):
     _check(got[rows], ref[rows], what)
 
 
-@pytest.mark.parametrize("d", [64, 128, 96])
+@pytest.mark.parametrize("d", [64, 128, 96, 136, 256])
 @pytest.mark.parametrize("causal", [False, True])
 def test_varlen_bwd_parity(d, causal):
     """Packed backward against the per-sequence oracle: empty, single-row and
@@ -288,12 +288,13 @@ def test_varlen_bwd_parity(d, causal):
     assert np.isnan(dq[nq:]).all() and np.isnan(dk[nk:]).all() and np.isnan(dv[nk:]).all()
 
 
-def test_varlen_bwd_cross_lengths():
+@pytest.mark.parametrize("d", [128, 256])
+def test_varlen_bwd_cross_lengths(d):
     """Queries and keys of different lengths per sequence (bottom-right causal),
     a sequence without queries (its keys get zero gradients), bf16 gradients."""
     lq = [100, 0, 300, 1, 129]
     lk = [400, 50, 300, 700, 1000]
-    q, k, v, cu_q, cu_k = make_varlen_inputs(lq, lk, 4, 4, 128, seed=872)
+    q, k, v, cu_q, cu_k = make_varlen_inputs(lq, lk, 4, 4, d, seed=872)
     do = _dout_packed(q.shape, 873)
     for causal in (False, True):
         dq, dk, dv = gpu_bwd_varlen(q, k, v, do, cu_q, cu_k, causal)
@@ -310,10 +311,11 @@ def test_varlen_bwd_cross_lengths():
     _check(gv, rv, "dV bf16", bf16=True)
 
 
-def test_varlen_bwd_equal_lengths_bit_identical_to_dense():
+@pytest.mark.parametrize("d", [128, 256])
+def test_varlen_bwd_equal_lengths_bit_identical_to_dense(d):
     """All sequences of one length: the dense backward's tiles and arithmetic
     in the packed layout (both fed the same forward outputs)."""
-    B, H, N, d = 3, 4, 700, 128
+    B, H, N = 3, 4, 700
     q, k, v, cu_q, cu_k = make_varlen_inputs([N] * B, [N] * B, H, H, d, seed=874)
     do = _dout_packed(q.shape, 875)
     dense = lambda t: t.reshape(B, N, H, d).permute(0, 2, 1, 3).contiguous().cuda()  # noqa: E731

@@ -415,7 +415,7 @@ def bwd_varlen(lib, **kw):
     (dict(q=None), 1), (dict(do=None), 1), (dict(lse=None), 1), (dict(dq=None), 1),
     (dict(cq=None), 1), (dict(ck=FAKE + 2), 1), (dict(dk=FAKE + 4), 1), (dict(tq=0), 1),
     (dict(mq=301), 1), (dict(B=0), 1), (dict(Hq=3, Hkv=2), 1), (dict(causal=2), 1),
-    (dict(gdt=7), 1), (dict(d=100), 2), (dict(d=136), 2), (dict(d=256), 2),
+    (dict(gdt=7), 1), (dict(d=100), 2), (dict(d=264), 2), (dict(d=252), 2),
     (dict(ws=None), 5), (dict(wsb=16), 5), (dict(ws=FAKE + 4), 5),
 ])
 def test_bwd_varlen_argument_checks(lib, kw, code):
@@ -426,7 +426,8 @@ def test_bwd_varlen_argument_checks(lib, kw, code):
 def test_bwd_varlen_workspace_size():
     # 2 vectors x Hq x (total_q + 132 B, rounded up to 4) floats
     assert ea.attn_bwd_varlen_workspace_size(3, 4, 2, 1000, 128) == 2 * 4 * ((1000 + 396 + 3) // 4 * 4) * 4
-    assert ea.attn_bwd_varlen_workspace_size(3, 4, 2, 1000, 256) == 0   # d > 128: not supported
+    assert ea.attn_bwd_varlen_workspace_size(3, 4, 2, 1000, 256) == 2 * 4 * ((1000 + 396 + 3) // 4 * 4) * 4
+    assert ea.attn_bwd_varlen_workspace_size(3, 4, 2, 1000, 264) == 0   # d > 256: not supported
     assert ea.attn_bwd_varlen_workspace_size(3, 4, 3, 1000, 128) == 0   # Hq % Hkv
     assert ea.attn_bwd_varlen_workspace_size(0, 4, 2, 1000, 128) == 0
 
