@@ -56,7 +56,8 @@
 namespace gb300 {
 namespace {
 
-constexpr int kBwdThreads = 256;
+constexpr int kBwdThreads = 256;    // the d > 128 passes: producer, MMA, one P/dS warpgroup
+constexpr int kBwdThreadsEw = 384;  // the d <= 128 passes: producer, MMA, two P/dS warpgroups
 constexpr int kBT = 128;  // keys per K/V tile, query rows per Q tile
 constexpr float kBwdLog2e = 1.44269504088896340736f;
 constexpr int kMaxSmemPerBlock = 232448;
@@ -303,14 +304,19 @@ __device__ __forceinline__ void issue_kmajor(uint32_t d_tmem, uint32_t a_lo, uin
     }
 }
 
-// M=128 x N=d x K=128 with A from TMEM (bf16 pairs, 8 columns per K=16) and B
-// MN-major in smem (16 rows of 128 B per K=16): dV += P^T dO or dK += dS^T Q.
+// M=128 x N=d x K=128 with A from TMEM and B MN-major in smem (16 rows of
+// 128 B per K=16): dV += P^T dO, dK += dS^T Q or dQ += dS K.  A is bf16 pairs,
+// 8 columns per K=16, in two blocks of 32 columns: K [0, 64) at a_tmem and
+// [64, 128) at a_tmem + 64, each written by the warpgroup that owns those
+// f32 columns (a_chunk_col), over columns it has read.
+__device__ __forceinline__ uint32_t a_chunk_col(int cc) { return (uint32_t)((cc >> 1) * 64 + (cc & 1) * 16); }
+
 __device__ __forceinline__ void issue_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo,
                                              uint32_t idesc, bool accumulate) {
 #pragma unroll
     for (int kk = 0; kk < kBT / 16; ++kk)
-        mma_ts_warp(d_tmem, a_tmem + kk * 8, sdesc_join(b_lo + kk * (2048 >> 4), kBwdDescHi), idesc,
-                    (accumulate || kk > 0) ? 1u : 0u);
+        mma_ts_warp(d_tmem, a_tmem + (kk >> 2) * 64 + (kk & 3) * 8,
+                    sdesc_join(b_lo + kk * (2048 >> 4), kBwdDescHi), idesc, (accumulate || kk > 0) ? 1u : 0u);
 }
 
 template <int D>
@@ -479,7 +485,7 @@ __device__ __forceinline__ void store_rows32_pairs(void* base, size_t row0, size
 }
 
 template <int D, bool OUT_F32, bool VARLEN>
-__device__ void bwd_pds(int wq, int lane, uint8_t* smem, BwdBars* bars, uint32_t tmem,
+__device__ void bwd_pds(int wq, int grp, int lane, uint8_t* smem, BwdBars* bars, uint32_t tmem,
                         const BwdParams& p, const BwdWork& w, unsigned int* err) {
     using C = BwdCfg<D>;
     const volatile int* abort_flag = &bars->abort;
@@ -499,9 +505,10 @@ __device__ void bwd_pds(int wq, int lane, uint8_t* smem, BwdBars* bars, uint32_t
         // causal: query q0 + x sees key jg iff x >= jg - off - q0
         const int lim = jg - w.off - q0;
         const bool masked = p.causal && (q0 + w.off < w.k0 + kBT - 1);
-        // Phase 1: P^T from S^T, kept in registers and written as bf16 over the
-        // S^T columns already read; releases dV(i) and S^T(i+1).
-        float pf0[32], pf1[32], pf2[32], pf3[32];
+        // Phase 1: P^T from S^T for this warpgroup's 64 query columns, kept in
+        // registers and written as bf16 over the S^T columns it has read;
+        // with the other warpgroup's, releases dV(i) and S^T(i+1).
+        float pf0[32], pf1[32];
         auto phase1 = [&](int cc, float (&pf)[32]) {
             uint32_t sv[32], pp[16];
             tmem_ld32(tS + cc * 32, sv);
@@ -510,12 +517,10 @@ __device__ void bwd_pds(int wq, int lane, uint8_t* smem, BwdBars* bars, uint32_t
                 p_chunk<true>(sv, lse2s, cc * 32, p.c, lim, pf, pp);
             else
                 p_chunk<false>(sv, lse2s, cc * 32, p.c, lim, pf, pp);
-            tmem_st16(tS + cc * 16, pp);
+            tmem_st16(tS + a_chunk_col(cc), pp);
         };
-        phase1(0, pf0);
-        phase1(1, pf1);
-        phase1(2, pf2);
-        phase1(3, pf3);
+        phase1(2 * grp, pf0);
+        phase1(2 * grp + 1, pf1);
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
@@ -530,12 +535,10 @@ __device__ void bwd_pds(int wq, int lane, uint8_t* smem, BwdBars* bars, uint32_t
             tmem_ld32(tdP + cc * 32, dp);
             tmem_wait_ld();
             ds_chunk_t(pf, dp, ds_vec, cc * 32, dd);
-            tmem_st16(tdP + cc * 16, dd);
+            tmem_st16(tdP + a_chunk_col(cc), dd);
         };
-        phase2(0, pf0);
-        phase2(1, pf1);
-        phase2(2, pf2);
-        phase2(3, pf3);
+        phase2(2 * grp, pf0);
+        phase2(2 * grp + 1, pf1);
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
@@ -558,12 +561,14 @@ __device__ void bwd_pds(int wq, int lane, uint8_t* smem, BwdBars* bars, uint32_t
     const size_t head_off = VARLEN ? (size_t)w.g * p.d_act * (OUT_F32 ? 4 : 2) : 0;
     void* dk_base = static_cast<uint8_t*>(p.dk) + head_off;
     void* dv_base = static_cast<uint8_t*>(p.dv) + head_off;
+    // this warpgroup's half of the columns
+    const int cc_lo = grp * (D / 2), cc_hi = cc_lo + D / 2;
     if (w.n_tiles == 0) {
         float z[32];
 #pragma unroll
         for (int x = 0; x < 32; ++x) z[x] = 0.f;
 #pragma unroll 1
-        for (int cc = 0; cc < p.d_act; cc += 32) {
+        for (int cc = cc_lo; cc < cc_hi && cc < p.d_act; cc += 32) {
             const int nc = p.d_act - cc < 32 ? p.d_act - cc : 32;
             store_rows32_pairs<OUT_F32>(dk_base, wrow0, row_elems, cc, z, nc, rows_live, lane);
             store_rows32_pairs<OUT_F32>(dv_base, wrow0, row_elems, cc, z, nc, rows_live, lane);
@@ -577,7 +582,7 @@ __device__ void bwd_pds(int wq, int lane, uint8_t* smem, BwdBars* bars, uint32_t
     }
     tc_fence_after();
 #pragma unroll 1
-    for (int cc = 0; cc < D; cc += 32) {
+    for (int cc = cc_lo; cc < cc_hi; cc += 32) {
         uint32_t r[32];
         float v[32];
         tmem_ld32(tmem + 256 + cc + lane_off, r);
@@ -595,7 +600,7 @@ __device__ void bwd_pds(int wq, int lane, uint8_t* smem, BwdBars* bars, uint32_t
 }
 
 template <int D, bool OUT_F32, bool VARLEN>
-__global__ void __launch_bounds__(kBwdThreads, 1)
+__global__ void __launch_bounds__(kBwdThreadsEw, 1)
 attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                      const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
                      const BwdParams p, unsigned int* err) {
@@ -617,12 +622,12 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tq, const __grid_consta
         mbar_init(smem_u32(&bars->kv_full), 1);
         for (int s = 0; s < 2; ++s) {
             mbar_init(smem_u32(&bars->qd_full[s]), 1);
-            mbar_init(smem_u32(&bars->qd_empty[s]), 1 + 4);  // dK commit + 4 P/dS warps
+            mbar_init(smem_u32(&bars->qd_empty[s]), 1 + 8);  // dK commit + 8 P/dS warps
         }
         mbar_init(smem_u32(&bars->s_full), 1);
         mbar_init(smem_u32(&bars->dp_full), 1);
-        mbar_init(smem_u32(&bars->p_full), 4);
-        mbar_init(smem_u32(&bars->ds_full), 4);
+        mbar_init(smem_u32(&bars->p_full), 8);
+        mbar_init(smem_u32(&bars->ds_full), 8);
         mbar_init(smem_u32(&bars->acc_full), 1);
         mbar_init(smem_u32(&bars->drain), 1);
         bars->abort = 0;
@@ -643,7 +648,7 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tq, const __grid_consta
 
     if (warp == 0) bwd_producer<D, VARLEN>(&tq, &tk, &tv, &tdo, smem, bars, p, w, err);
     else if (warp == 1) bwd_mma<D>(smem, bars, tmem, w, err);
-    else if (warp >= 4) bwd_pds<D, OUT_F32, VARLEN>(warp & 3, lane, smem, bars, tmem, p, w, err);
+    else if (warp >= 4) bwd_pds<D, OUT_F32, VARLEN>(warp & 3, (warp - 4) >> 2, lane, smem, bars, tmem, p, w, err);
 
     tc_fence_before();
     __syncthreads();
@@ -943,7 +948,7 @@ __device__ __forceinline__ void ds_row_chunk(const float (&pf)[32], const uint32
 }
 
 template <int D, bool OUT_F32, bool VARLEN>
-__device__ void dq_ds(int wq, int lane, DqBars* bars, uint32_t tmem, const BwdParams& p,
+__device__ void dq_ds(int wq, int grp, int lane, DqBars* bars, uint32_t tmem, const BwdParams& p,
                       const DqWork& w, unsigned int* err) {
     const volatile int* abort_flag = &bars->abort;
     const uint32_t lane_off = uint32_t(wq * 32) << 16;
@@ -965,8 +970,9 @@ __device__ void dq_ds(int wq, int lane, DqBars* bars, uint32_t tmem, const BwdPa
         tc_fence_after();
         const int lim = row + w.off - j * kBT;  // causal: key column c allowed iff c <= lim
         const bool masked = __any_sync(0xFFFFFFFFu, p.causal && lim < kBT - 1);
-        // Phase 1: P from S (needs S_j only; runs while dQ_{j-1} and dP_j compute)
-        float pf0[32], pf1[32], pf2[32], pf3[32];
+        // Phase 1: P from S for this warpgroup's 64 key columns (needs S_j only;
+        // runs while dQ_{j-1} and dP_j compute)
+        float pf0[32], pf1[32];
         auto phase1 = [&](int cc, float (&pf)[32]) {
             uint32_t sv[32];
             tmem_ld32(tS + cc * 32, sv);
@@ -976,11 +982,9 @@ __device__ void dq_ds(int wq, int lane, DqBars* bars, uint32_t tmem, const BwdPa
             else
                 p_row_chunk<false>(sv, c2, nl2, cc * 32, kBT, pf);
         };
-        phase1(0, pf0);
-        phase1(1, pf1);
-        phase1(2, pf2);
-        phase1(3, pf3);
-        // Phase 2: dS from P and dP, as bf16 over the S columns (all read)
+        phase1(2 * grp, pf0);
+        phase1(2 * grp + 1, pf1);
+        // Phase 2: dS from P and dP, as bf16 over the S columns this warpgroup read
         ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&bars->dp_full), j & 1, abort_flag, 32));
         if (!ok) break;
         tc_fence_after();
@@ -989,12 +993,10 @@ __device__ void dq_ds(int wq, int lane, DqBars* bars, uint32_t tmem, const BwdPa
             tmem_ld32(tdP + cc * 32, dp);
             tmem_wait_ld();
             ds_row_chunk(pf, dp, nd2, dd);
-            tmem_st16(tS + cc * 16, dd);
+            tmem_st16(tS + a_chunk_col(cc), dd);
         };
-        phase2(0, pf0);
-        phase2(1, pf1);
-        phase2(2, pf2);
-        phase2(3, pf3);
+        phase2(2 * grp, pf0);
+        phase2(2 * grp + 1, pf1);
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
@@ -1016,7 +1018,7 @@ __device__ void dq_ds(int wq, int lane, DqBars* bars, uint32_t tmem, const BwdPa
     const size_t row_elems = VARLEN ? (size_t)p.Hq * p.d_act : (size_t)p.d_act;
     void* dq_base = static_cast<uint8_t*>(p.dq) + (VARLEN ? (size_t)w.hq * p.d_act * (OUT_F32 ? 4 : 2) : 0);
 #pragma unroll 1
-    for (int cc = 0; cc < D; cc += 32) {
+    for (int cc = grp * (D / 2); cc < (grp + 1) * (D / 2); cc += 32) {  // this warpgroup's half
         float v[32];
         if (w.n_kv > 0) {
             uint32_t r[32];
@@ -1034,7 +1036,7 @@ __device__ void dq_ds(int wq, int lane, DqBars* bars, uint32_t tmem, const BwdPa
 }
 
 template <int D, bool OUT_F32, bool VARLEN>
-__global__ void __launch_bounds__(kBwdThreads, 1)
+__global__ void __launch_bounds__(kBwdThreadsEw, 1)
 attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                    const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
                    const BwdParams p, unsigned int* err) {
@@ -1062,7 +1064,7 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
             mbar_init(smem_u32(&bars->s_full[s]), 1);
         }
         mbar_init(smem_u32(&bars->dp_full), 1);
-        mbar_init(smem_u32(&bars->ds_full), 4);
+        mbar_init(smem_u32(&bars->ds_full), 8);
         mbar_init(smem_u32(&bars->dq_full), 1);
         mbar_init(smem_u32(&bars->drain), 1);
         bars->abort = 0;
@@ -1082,7 +1084,7 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
     const uint32_t tmem = bars->tmem_base;
     if (warp == 0) dq_producer<D, VARLEN>(&tq, &tk, &tv, &tdo, smem, bars, p, w, err);
     else if (warp == 1) dq_mma<D>(smem, bars, tmem, w, err);
-    else if (warp >= 4) dq_ds<D, OUT_F32, VARLEN>(warp & 3, lane, bars, tmem, p, w, err);
+    else if (warp >= 4) dq_ds<D, OUT_F32, VARLEN>(warp & 3, (warp - 4) >> 2, lane, bars, tmem, p, w, err);
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
@@ -1275,11 +1277,11 @@ attn_status_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const C
     // (packed batches: units at the longest lengths; the tiles past a
     // sequence's end have no work)
     const long long kv_ctas = (long long)p.B * p.Hkv * p.n_kt;
-    attn_bwd_dkdv_kernel<D, OUT_F32, VARLEN><<<(unsigned)kv_ctas, kBwdThreads, BwdCfg<D>::kSmemBytes,
+    attn_bwd_dkdv_kernel<D, OUT_F32, VARLEN><<<(unsigned)kv_ctas, kBwdThreadsEw, BwdCfg<D>::kSmemBytes,
                                                stream>>>(tq, tk, tv, tdo, p, dev.err_word);
     if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
     const long long q_ctas = (long long)p.B * p.Hq * ((p.Nq + kBT - 1) / kBT);
-    attn_bwd_dq_kernel<D, OUT_F32, VARLEN><<<(unsigned)q_ctas, kBwdThreads, DqCfg<D>::kSmemBytes,
+    attn_bwd_dq_kernel<D, OUT_F32, VARLEN><<<(unsigned)q_ctas, kBwdThreadsEw, DqCfg<D>::kSmemBytes,
                                              stream>>>(tq, tk, tv, tdo, p, dev.err_word);
     return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
