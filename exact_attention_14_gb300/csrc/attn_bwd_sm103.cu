@@ -20,29 +20,36 @@
 //        every 128-row Q tile that can see its keys.  Per Q tile:
 //          S^T  = K Q^T,  dP^T = V dO^T      (tcgen05, operands K-major in smem)
 //          P^T  = 2^(S^T c - lse2),  dS^T = P^T o (dP^T - D)
-//                 (warps 4-7, one key row per thread; P^T and dS^T go to TMEM
-//                 as bf16 pairs)
+//                 (warps 4-11, one key row per thread and half of the
+//                 tile's query columns per warpgroup; P^T and dS^T go to
+//                 TMEM as bf16 pairs)
 //          dV  += P^T dO,  dK += dS^T Q      (A from TMEM, B MN-major in smem)
 //        After the last tile dK (times scale) and dV are written once.
 //  dq    one CTA per (b, query head, 128-row Q tile), K/V tiles streamed
 //        through a ring.  Per K/V tile:
 //          S = Q K^T,  dP = dO V^T,  dS = P o (dP - D)  (one query row per
-//          thread, its lse2 and D in registers; dS to TMEM over S)
+//          thread and half of the tile's keys per warpgroup, its lse2 and D
+//          in registers; dS to TMEM over S)
 //          dQ += dS K                        (A from TMEM, B = K MN-major)
 //        After the last tile dQ (times scale) is written once.
 //
-// Roles (8 warps): warp 0 TMA producer, warp 1 MMA issuer and TMEM owner,
-// warps 2-3 idle, warps 4-7 the elementwise work (one TMEM lane quarter each).
+// Roles (12 warps): warp 0 TMA producer, warp 1 MMA issuer and TMEM owner,
+// warps 2-3 idle, warps 4-7 and 8-11 the elementwise work, two warpgroups
+// (one TMEM lane quarter per warp; warpgroup h takes f32 columns
+// [64h, 64h + 64) of S^T / dP^T / S / dP and writes their bf16 pairs to
+// columns [64h, 64h + 32), over columns it has read itself).  The d > 128
+// passes further down keep 8 warps, one elementwise warpgroup.
 //
-// TMEM, dkdv (512 columns): [0,128) S^T, then P^T in [0,64); [128,256) dP^T,
-// then dS^T in [128,192); dV [256,256+d); dK [256+d,256+2d).  The P^T / dS^T
+// TMEM, dkdv (512 columns): [0,128) S^T, then P^T in [0,32) and [64,96);
+// [128,256) dP^T, then dS^T in [128,160) and [192,224); dV [256,256+d); dK
+// [256+d,256+2d).  The P^T / dS^T
 // warps work in two phases per Q tile (P^T from S^T, then dS^T from dP^T), and
 // the MMAs interleave with them: dV(i) and S^T(i+1) run during phase 2 of tile
 // i, dK(i) and dP^T(i+1) during phase 1 of tile i+1 (each next-tile product is
 // issued after the one that reads its columns: one CTA's MMAs run in issue
 // order).
 // TMEM, dq: S in [0,128) for even K/V tiles and [384,512) for odd ones (dS over
-// its first 64 columns), dP [128,256), dQ [256,256+d).  K streams through a
+// its columns [0,32) and [64,96)), dP [128,256), dQ [256,256+d).  K streams through a
 // 3-stage ring and V through a 2-stage one; S_{j+2} is issued as soon as dQ_j
 // has read tile j's S buffer, so the dS warps' exponentials for tile j+1
 // (phase 1) overlap dQ_j and dP_{j+1}.
@@ -387,7 +394,8 @@ __device__ void bwd_mma(uint8_t* smem, BwdBars* bars, uint32_t tmem, const BwdWo
 }
 
 // ---------------------------------------------------------------------------
-// P / dS warpgroup (one key row per thread) and the dK / dV epilogue
+// P / dS warpgroups (one key row per thread, half the columns each) and the
+// dK / dV epilogue
 // ---------------------------------------------------------------------------
 // P^T = 2^(S^T c - lse2) for 32 query columns [qc, qc + 32) of this thread's
 // key row, kept in fp32 (pf) and packed to bf16 pairs (pp).  lim: query column
