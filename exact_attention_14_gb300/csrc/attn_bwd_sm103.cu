@@ -1302,8 +1302,9 @@ attn_status_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const C
 // each) fill TMEM, and a 128-row Q or dO tile is 64 KiB, so these kernels use
 // other tile shapes, each product a shape the d > 128 forward also runs:
 //  dkdv  one CTA per (b, KV head g, 128-key tile, column half h of d).  K and
-//        V of the tile stay in shared memory (64 KiB each); Q, dO, lse2 and D
-//        stream in 64-row tiles through one stage.  Per Q tile:
+//        V of the tile stay in shared memory (64 KiB each); Q (with its lse2
+//        and D rows) streams in 64-row tiles through two buffers, dO through
+//        one.  Per Q tile:
 //          S^T = K Q^T, dP^T = V dO^T           (M=128, N=64, K=256)
 //          P^T, dS^T as in the d <= 128 pass    (64 query columns per key row)
 //          dV_h += P^T dO_h, dK_h += dS^T Q_h   (M=128, N=128, K=64: columns
@@ -1313,12 +1314,16 @@ attn_status_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const C
 //        TMEM: S^T [0,64) (P^T over [0,32)), dP^T [64,128) (dS^T over
 //        [64,96)), dV_h [128,256), dK_h [256,384).
 //  dq    one CTA per (b, query head, 128-row Q tile).  Q and dO stay in
-//        shared memory; K and V stream in 64-key tiles through one stage.
-//        Per K/V tile: S = Q K^T, dP = dO V^T (M=128, N=64, K=256), dS as in
-//        the d <= 128 pass, dQ += dS K (M=128, N=256, K=64).
-//        TMEM: S [0,64) (dS over [0,32)), dP [64,128), dQ [128,384).
-// Both passes run their steps in order (one stage: the next tile's loads wait
-// for the products that read the current one).
+//        shared memory; K streams in 64-key tiles through two buffers, V
+//        through one.  Per K/V tile: S = Q K^T, dP = dO V^T (M=128, N=64,
+//        K=256), dS as in the d <= 128 pass, dQ += dS K (M=128, N=256, K=64).
+//        TMEM: S in [0,64) for even K/V tiles and [64,128) for odd ones (dS
+//        over its first 32 columns), dP [128,192), dQ [192,448).
+// Both passes issue the next tile's first product while the elementwise warps
+// work on the current tile (the dK/dV pass S^T(i+1) after dV(i), the dQ pass
+// S_{j+2} after dQ_j).  Packed batches (VARLEN) use the d <= 128 passes' work
+// decoding with the Q (dK/dV) and K/V (dQ) tiles read through ragged tensor
+// maps with 64-row boxes.
 // ---------------------------------------------------------------------------
 constexpr int kWD = 256;    // tile columns
 constexpr int kWQ = 64;     // query rows per dkdv Q tile, keys per dq K/V tile
