@@ -15,8 +15,8 @@
 //  prep  per query row: D = sum_c dO_c O_c and lse2 = LSE log2(e), padded to
 //        whole 128-row tiles (lse2 = +inf and D = 0 past Nq, so padded rows
 //        get P = 0 and dS = 0).
-//  dkdv  one CTA per (b, KV head g, 128-key tile).  K and V of the tile stay
-//        in shared memory; the CTA walks every query head of g's group and
+//  dkdv  one item per (b, KV head g, 128-key tile).  K and V of the tile stay
+//        in shared memory; the item walks every query head of g's group and
 //        every 128-row Q tile that can see its keys.  Per Q tile:
 //          S^T  = K Q^T,  dP^T = V dO^T      (tcgen05, operands K-major in smem)
 //          P^T  = 2^(S^T c - lse2),  dS^T = P^T o (dP^T - D)
@@ -25,13 +25,21 @@
 //                 TMEM as bf16 pairs)
 //          dV  += P^T dO,  dK += dS^T Q      (A from TMEM, B MN-major in smem)
 //        After the last tile dK (times scale) and dV are written once.
-//  dq    one CTA per (b, query head, 128-row Q tile), K/V tiles streamed
+//  dq    one item per (b, query head, 128-row Q tile), K/V tiles streamed
 //        through a ring.  Per K/V tile:
 //          S = Q K^T,  dP = dO V^T,  dS = P o (dP - D)  (one query row per
 //          thread and half of the tile's keys per warpgroup, its lse2 and D
 //          in registers; dS to TMEM over S)
 //          dQ += dS K                        (A from TMEM, B = K MN-major)
 //        After the last tile dQ (times scale) is written once.
+//
+// Both passes run persistent grids of at most one CTA per SM; CTA c takes items
+// c, c + gridDim.x, ... and its roles run from one item into the next: the
+// producer loads the next item's K and V (dkdv) or Q and dO (dq) as soon as
+// the current item's last products that read them complete, the rings and
+// the TMEM buffers keep counting across items, and an item's first
+// accumulating product waits only for its first P^T / dS, which the
+// elementwise warps form after reading out the previous item's accumulators.
 //
 // Roles (12 warps): warp 0 TMA producer, warp 1 MMA issuer and TMEM owner,
 // warps 2-3 idle, warps 4-7 and 8-11 the elementwise work, two warpgroups
@@ -125,7 +133,7 @@ __device__ __forceinline__ bool bwd_varlen_seq(const BwdParams& p, int b, int& q
 }
 
 struct __align__(8) BwdBars {
-    uint64_t kv_full;
+    uint64_t kv_full, kv_empty;  // K and V of an item; read by its last S^T and dP^T
     uint64_t qd_full[2], qd_empty[2];
     uint64_t s_full, dp_full, p_full, ds_full, acc_full, drain;
     uint32_t tmem_base;
@@ -148,13 +156,13 @@ struct BwdWork {
     int nq, nk, off, qb, kb, vbase;
 };
 
-__device__ __forceinline__ BwdWork bwd_work(const BwdParams& p) {
+__device__ __forceinline__ BwdWork bwd_work(const BwdParams& p, unsigned idx) {
     BwdWork w;
     const unsigned all = (unsigned)(p.B * p.Hkv);
     const unsigned S = (unsigned)p.sec_groups;
     const unsigned per_sec = S * (unsigned)p.n_kt;
-    const unsigned sec = blockIdx.x / per_sec;
-    const unsigned r = blockIdx.x - sec * per_sec;
+    const unsigned sec = idx / per_sec;
+    const unsigned r = idx - sec * per_sec;
     const unsigned rest = all - sec * S;
     const unsigned gs = rest < S ? rest : S;  // groups in this (possibly partial) section
     w.kt = (int)(r / gs);
@@ -178,15 +186,15 @@ __device__ __forceinline__ BwdWork bwd_work(const BwdParams& p) {
     return w;
 }
 
-// The same for packed batches: CTA index = (b * Hkv + g) * n_kt + kt, n_kt
+// The same for packed batches: item index = (b * Hkv + g) * n_kt + kt, n_kt
 // for the longest key length.  Key tiles past a sequence's end, and every tile
 // of a sequence whose offsets fail the checks (reported in the error word),
 // have no work and write nothing.
-__device__ __forceinline__ BwdWork bwd_work_varlen(const BwdParams& p, unsigned int* err) {
+__device__ __forceinline__ BwdWork bwd_work_varlen(const BwdParams& p, unsigned idx, unsigned int* err) {
     BwdWork w;
     const int per_b = p.Hkv * p.n_kt;
-    w.b = (int)blockIdx.x / per_b;
-    const int rem = (int)blockIdx.x - w.b * per_b;
+    w.b = (int)idx / per_b;
+    const int rem = (int)idx - w.b * per_b;
     w.g = rem / p.n_kt;
     w.kt = rem - w.g * p.n_kt;
     w.k0 = w.kt * kBT;
@@ -213,6 +221,15 @@ __device__ __forceinline__ BwdWork bwd_work_varlen(const BwdParams& p, unsigned 
     return w;
 }
 
+// The dK/dV pass runs a persistent grid (at most one CTA per SM): CTA c takes
+// items c, c + gridDim.x, ... of the order above, each one key tile, and
+// keeps its pipeline running from one item into the next.
+template <bool VARLEN>
+__device__ __forceinline__ BwdWork bwd_item(const BwdParams& p, unsigned idx, unsigned int* err) {
+    if constexpr (VARLEN) return bwd_work_varlen(p, idx, err);
+    else return bwd_work(p, idx);
+}
+
 __device__ __forceinline__ void bwd_abort(BwdBars* bars, unsigned int* err) {
     atomicOr(err, kErrTimeout);
     *((volatile int*)&bars->abort) = 1;
@@ -224,68 +241,81 @@ __device__ __forceinline__ void bwd_abort(BwdBars* bars, unsigned int* err) {
 template <int D, bool VARLEN>
 __device__ void bwd_producer(const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv,
                              const CUtensorMap* tdo, uint8_t* smem, BwdBars* bars,
-                             const BwdParams& p, const BwdWork& w, unsigned int* err) {
+                             const BwdParams& p, unsigned n_items, unsigned int* err) {
     using C = BwdCfg<D>;
     const volatile int* abort_flag = &bars->abort;
     const bool leader = elect_one();
-    // K/V head: an index into [B * Hkv], or into [Hkv] of the packed rows
-    const int kvh = VARLEN ? w.g : w.b * p.Hkv + w.g;
-    if (leader) {
-        const uint32_t bar = smem_u32(&bars->kv_full);
-        mbar_arrive_expect_tx(bar, 2 * C::kTile);
-#pragma unroll
-        for (int c = 0; c < D / 64; ++c) {
-            if constexpr (VARLEN) {
-                const int r = kRaggedWindow - w.nk + w.k0;
-                tma_load_5d(smem_u32(smem + C::kK) + c * 16384, tk, bar, 64 * c, kvh, r, w.kb + w.nk,
-                            kRaggedWindow);
-                tma_load_5d(smem_u32(smem + C::kV) + c * 16384, tv, bar, 64 * c, kvh, r, w.kb + w.nk,
-                            kRaggedWindow);
-            } else {
-                tma_load_3d(smem_u32(smem + C::kK) + c * 16384, tk, bar, 64 * c, w.k0, kvh);
-                tma_load_3d(smem_u32(smem + C::kV) + c * 16384, tv, bar, 64 * c, w.k0, kvh);
-            }
-        }
-    }
-    __syncwarp();
     bool ok = true;
-    int issued = 0;
-    for (int i = 0; i < w.n_tiles && ok; ++i) {
-        const int st = i & 1;
-        if (i >= 2)
-            ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&bars->qd_empty[st]), ((i >> 1) - 1) & 1,
-                                                   abort_flag));
+    int issued = 0;   // Q / dO tiles issued, over the CTA's items
+    int kv_uses = 0;  // K / V loads issued (items with work)
+    for (unsigned idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
+        const BwdWork w = bwd_item<VARLEN>(p, idx, err);
+        if (w.n_tiles == 0) continue;
+        // K and V of the item, once the previous item's last S^T and dP^T have
+        // read theirs
+        if (kv_uses > 0)
+            ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&bars->kv_empty), (kv_uses - 1) & 1, abort_flag));
         if (!ok) break;
-        const int hq = w.g * p.group + i / w.n_qt_cta;
-        const int q0 = (w.qt_first + i % w.n_qt_cta) * kBT;
-        const int bh = w.b * p.Hq + hq;
+        // K/V head: an index into [B * Hkv], or into [Hkv] of the packed rows
+        const int kvh = VARLEN ? w.g : w.b * p.Hkv + w.g;
         if (leader) {
-            const uint32_t bar = smem_u32(&bars->qd_full[st]);
-            mbar_arrive_expect_tx(bar, 2 * C::kTile + 1024);
+            const uint32_t bar = smem_u32(&bars->kv_full);
+            mbar_arrive_expect_tx(bar, 2 * C::kTile);
 #pragma unroll
             for (int c = 0; c < D / 64; ++c) {
                 if constexpr (VARLEN) {
-                    const int r = kRaggedWindow - w.nq + q0;
-                    tma_load_5d(smem_u32(smem + C::kQ + st * C::kTile) + c * 16384, tq, bar, 64 * c, hq, r,
-                                w.qb + w.nq, kRaggedWindow);
-                    tma_load_5d(smem_u32(smem + C::kDO + st * C::kTile) + c * 16384, tdo, bar, 64 * c, hq, r,
-                                w.qb + w.nq, kRaggedWindow);
+                    const int r = kRaggedWindow - w.nk + w.k0;
+                    tma_load_5d(smem_u32(smem + C::kK) + c * 16384, tk, bar, 64 * c, kvh, r, w.kb + w.nk,
+                                kRaggedWindow);
+                    tma_load_5d(smem_u32(smem + C::kV) + c * 16384, tv, bar, 64 * c, kvh, r, w.kb + w.nk,
+                                kRaggedWindow);
                 } else {
-                    tma_load_3d(smem_u32(smem + C::kQ + st * C::kTile) + c * 16384, tq, bar, 64 * c, q0, bh);
-                    tma_load_3d(smem_u32(smem + C::kDO + st * C::kTile) + c * 16384, tdo, bar, 64 * c, q0, bh);
+                    tma_load_3d(smem_u32(smem + C::kK) + c * 16384, tk, bar, 64 * c, w.k0, kvh);
+                    tma_load_3d(smem_u32(smem + C::kV) + c * 16384, tv, bar, 64 * c, w.k0, kvh);
                 }
             }
-            const size_t row = VARLEN ? (size_t)hq * p.vstride + (size_t)(w.vbase + q0)
-                                      : (size_t)bh * p.Nq_pad + q0;
-            bulk_load(smem_u32(smem + C::kLD + st * 1024), p.lse2 + row, 512, bar);
-            bulk_load(smem_u32(smem + C::kLD + st * 1024 + 512), p.dvec + row, 512, bar);
         }
         __syncwarp();
-        ++issued;
+        ++kv_uses;
+        for (int i = 0; i < w.n_tiles && ok; ++i) {
+            const int st = issued & 1;
+            if (issued >= 2)
+                ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&bars->qd_empty[st]), ((issued >> 1) - 1) & 1,
+                                                       abort_flag));
+            if (!ok) break;
+            const int hq = w.g * p.group + i / w.n_qt_cta;
+            const int q0 = (w.qt_first + i % w.n_qt_cta) * kBT;
+            const int bh = w.b * p.Hq + hq;
+            if (leader) {
+                const uint32_t bar = smem_u32(&bars->qd_full[st]);
+                mbar_arrive_expect_tx(bar, 2 * C::kTile + 1024);
+#pragma unroll
+                for (int c = 0; c < D / 64; ++c) {
+                    if constexpr (VARLEN) {
+                        const int r = kRaggedWindow - w.nq + q0;
+                        tma_load_5d(smem_u32(smem + C::kQ + st * C::kTile) + c * 16384, tq, bar, 64 * c, hq, r,
+                                    w.qb + w.nq, kRaggedWindow);
+                        tma_load_5d(smem_u32(smem + C::kDO + st * C::kTile) + c * 16384, tdo, bar, 64 * c, hq,
+                                    r, w.qb + w.nq, kRaggedWindow);
+                    } else {
+                        tma_load_3d(smem_u32(smem + C::kQ + st * C::kTile) + c * 16384, tq, bar, 64 * c, q0,
+                                    bh);
+                        tma_load_3d(smem_u32(smem + C::kDO + st * C::kTile) + c * 16384, tdo, bar, 64 * c, q0,
+                                    bh);
+                    }
+                }
+                const size_t row = VARLEN ? (size_t)hq * p.vstride + (size_t)(w.vbase + q0)
+                                          : (size_t)bh * p.Nq_pad + q0;
+                bulk_load(smem_u32(smem + C::kLD + st * 1024), p.lse2 + row, 512, bar);
+                bulk_load(smem_u32(smem + C::kLD + st * 1024 + 512), p.dvec + row, 512, bar);
+            }
+            __syncwarp();
+            ++issued;
+        }
     }
     if (!ok && leader) bwd_abort(bars, err);
     // Drain: every issued copy lands before the CTA may exit.
-    mbar_wait(smem_u32(&bars->kv_full), 0, nullptr);
+    if (kv_uses > 0) mbar_wait(smem_u32(&bars->kv_full), (kv_uses - 1) & 1, nullptr);
     for (int st = 0; st < 2 && st < issued; ++st) {
         const int uses = (issued - st + 1) / 2;
         mbar_wait(smem_u32(&bars->qd_full[st]), (uses - 1) & 1, nullptr);
@@ -326,9 +356,9 @@ __device__ __forceinline__ void issue_tmem_a(uint32_t d_tmem, uint32_t a_tmem, u
                     sdesc_join(b_lo + kk * (2048 >> 4), kBwdDescHi), idesc, (accumulate || kk > 0) ? 1u : 0u);
 }
 
-template <int D>
-__device__ void bwd_mma(uint8_t* smem, BwdBars* bars, uint32_t tmem, const BwdWork& w,
-                        unsigned int* err) {
+template <int D, bool VARLEN>
+__device__ void bwd_mma(uint8_t* smem, BwdBars* bars, uint32_t tmem, const BwdParams& p,
+                        unsigned n_items, unsigned int* err) {
     using C = BwdCfg<D>;
     const volatile int* abort_flag = &bars->abort;
     const bool leader = elect_one();
@@ -345,36 +375,47 @@ __device__ void bwd_mma(uint8_t* smem, BwdBars* bars, uint32_t tmem, const BwdWo
         return __all_sync(0xFFFFFFFFu, mbar_wait(bar, parity, abort_flag, polls));
     };
     bool ok = true;
-    if (w.n_tiles > 0) {
-        ok = wait_all(smem_u32(&bars->kv_full), 0, 0) && wait_all(smem_u32(&bars->qd_full[0]), 0, 0);
-        if (ok) {
-            tc_fence_after();
-            issue_kmajor<D>(tS, k_kmaj, q_kmaj(0), idS);
-            mma_commit_warp(smem_u32(&bars->s_full));
-            issue_kmajor<D>(tdP, v_kmaj, do_kmaj(0), idS);
-            mma_commit_warp(smem_u32(&bars->dp_full));
-        }
+    int g = 0;  // Q / dO tiles consumed, over the CTA's items
+    int u = 0;  // items with work
+    for (unsigned idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
+        const BwdWork w = bwd_item<VARLEN>(p, idx, err);
+        const int n = w.n_tiles;
+        if (n == 0) continue;
+        ok = wait_all(smem_u32(&bars->kv_full), u & 1, 0) &&
+             wait_all(smem_u32(&bars->qd_full[g & 1]), (g >> 1) & 1, 0);
+        if (!ok) break;
+        // S^T and dP^T of the item's first tile: their columns were last read
+        // by the previous item's dV and dK, issued before (one CTA's MMAs run
+        // in issue order); its dV and dK (accumulate = 0) wait for P^T and
+        // dS^T, which the P/dS warps write after reading out the previous
+        // item's dV and dK.
+        tc_fence_after();
+        issue_kmajor<D>(tS, k_kmaj, q_kmaj(g & 1), idS);
+        mma_commit_warp(smem_u32(&bars->s_full));
+        issue_kmajor<D>(tdP, v_kmaj, do_kmaj(g & 1), idS);
+        mma_commit_warp(smem_u32(&bars->dp_full));
+        if (n == 1) mma_commit_warp(smem_u32(&bars->kv_empty));  // K and V are read
         // Per Q tile i: dV(i) once P^T(i) is in TMEM, then S^T(i+1) into the
         // columns dV(i) has read; dK(i) once dS^T(i) is in TMEM, then dP^T(i+1)
-        // into the columns dK(i) has read (one CTA's MMAs run in issue order).
-        // The P^T / dS^T warps work on tile i while the tensor cores run
-        // dV(i), S^T(i+1) and then dK(i), dP^T(i+1).
-        for (int i = 0; i < w.n_tiles && ok; ++i) {
-            const int st = i & 1;
-            const int st1 = (i + 1) & 1;
-            const bool more = i + 1 < w.n_tiles;
-            ok = wait_all(smem_u32(&bars->p_full), i & 1, 32);
+        // into the columns dK(i) has read.  The P^T / dS^T warps work on tile i
+        // while the tensor cores run dV(i), S^T(i+1) and then dK(i), dP^T(i+1).
+        for (int i = 0; i < n && ok; ++i) {
+            const int gi = g + i;
+            const int st = gi & 1;
+            const int st1 = (gi + 1) & 1;
+            const bool more = i + 1 < n;
+            ok = wait_all(smem_u32(&bars->p_full), gi & 1, 32);
             if (!ok) break;
             tc_fence_after();
             issue_tmem_a(tdV, tS, do_mn(st), idKV, i > 0);          // dV += P^T dO
             if (more) {
-                ok = wait_all(smem_u32(&bars->qd_full[st1]), ((i + 1) >> 1) & 1, 0);
+                ok = wait_all(smem_u32(&bars->qd_full[st1]), ((gi + 1) >> 1) & 1, 0);
                 if (!ok) break;
                 tc_fence_after();
                 issue_kmajor<D>(tS, k_kmaj, q_kmaj(st1), idS);       // S^T(i+1)
                 mma_commit_warp(smem_u32(&bars->s_full));
             }
-            ok = wait_all(smem_u32(&bars->ds_full), i & 1, 32);
+            ok = wait_all(smem_u32(&bars->ds_full), gi & 1, 32);
             if (!ok) break;
             tc_fence_after();
             issue_tmem_a(tdK, tdP, q_mn(st), idKV, i > 0);          // dK += dS^T Q
@@ -382,9 +423,12 @@ __device__ void bwd_mma(uint8_t* smem, BwdBars* bars, uint32_t tmem, const BwdWo
             if (more) {
                 issue_kmajor<D>(tdP, v_kmaj, do_kmaj(st1), idS);     // dP^T(i+1)
                 mma_commit_warp(smem_u32(&bars->dp_full));
+                if (i + 2 == n) mma_commit_warp(smem_u32(&bars->kv_empty));  // the last S^T, dP^T
             }
         }
         if (ok) mma_commit_warp(smem_u32(&bars->acc_full));
+        g += n;
+        ++u;
     }
     if (!ok && leader) bwd_abort(bars, err);
     // Drain: all issued MMAs complete before TMEM is released.
@@ -494,117 +538,124 @@ __device__ __forceinline__ void store_rows32_pairs(void* base, size_t row0, size
 
 template <int D, bool OUT_F32, bool VARLEN>
 __device__ void bwd_pds(int wq, int grp, int lane, uint8_t* smem, BwdBars* bars, uint32_t tmem,
-                        const BwdParams& p, const BwdWork& w, unsigned int* err) {
+                        const BwdParams& p, unsigned n_items, unsigned int* err) {
     using C = BwdCfg<D>;
     const volatile int* abort_flag = &bars->abort;
     const uint32_t lane_off = uint32_t(wq * 32) << 16;
     const uint32_t tS = tmem + lane_off, tdP = tmem + 128 + lane_off;
     const int j = wq * 32 + lane;  // key row of the tile
-    const int jg = w.k0 + j;
-    bool ok = true;
-    for (int i = 0; i < w.n_tiles && ok; ++i) {
-        const int st = i & 1;
-        ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&bars->s_full), i & 1, abort_flag, 32));
-        if (!ok) break;
-        tc_fence_after();
-        const int q0 = (w.qt_first + i % w.n_qt_cta) * kBT;
-        const uint32_t lse2s = smem_u32(smem + C::kLD + st * 1024);
-        const uint32_t ds_vec = lse2s + kBT * 4;
-        // causal: query q0 + x sees key jg iff x >= jg - off - q0
-        const int lim = jg - w.off - q0;
-        const bool masked = p.causal && (q0 + w.off < w.k0 + kBT - 1);
-        // Phase 1: P^T from S^T for this warpgroup's 64 query columns, kept in
-        // registers and written as bf16 over the S^T columns it has read;
-        // with the other warpgroup's, releases dV(i) and S^T(i+1).
-        float pf0[32], pf1[32];
-        auto phase1 = [&](int cc, float (&pf)[32]) {
-            uint32_t sv[32], pp[16];
-            tmem_ld32(tS + cc * 32, sv);
-            tmem_wait_ld();
-            if (masked)
-                p_chunk<true>(sv, lse2s, cc * 32, p.c, lim, pf, pp);
-            else
-                p_chunk<false>(sv, lse2s, cc * 32, p.c, lim, pf, pp);
-            tmem_st16(tS + a_chunk_col(cc), pp);
-        };
-        phase1(2 * grp, pf0);
-        phase1(2 * grp + 1, pf1);
-        tmem_wait_st();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&bars->p_full));
-        // Phase 2: dS^T from P^T and dP^T, written as bf16 over the dP^T
-        // columns already read; releases dK(i) and dP^T(i+1).
-        ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&bars->dp_full), i & 1, abort_flag, 32));
-        if (!ok) break;
-        tc_fence_after();
-        auto phase2 = [&](int cc, const float (&pf)[32]) {
-            uint32_t dp[32], dd[16];
-            tmem_ld32(tdP + cc * 32, dp);
-            tmem_wait_ld();
-            ds_chunk_t(pf, dp, ds_vec, cc * 32, dd);
-            tmem_st16(tdP + a_chunk_col(cc), dd);
-        };
-        phase2(2 * grp, pf0);
-        phase2(2 * grp + 1, pf1);
-        tmem_wait_st();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) {
-            mbar_arrive(smem_u32(&bars->ds_full));
-            mbar_arrive(smem_u32(&bars->qd_empty[st]));
-        }
-    }
-    if (!ok) {
-        bwd_abort(bars, err);
-        return;
-    }
-    // dK = scale * dS^T Q, dV = P^T dO: one key row per thread, written once
-    // this warp's first key row and how many of its rows are inside Nk (packed
-    // batches: rows of Hkv * d elements, the head's d columns at offset g * d)
-    const size_t wrow0 = VARLEN ? (size_t)(w.kb + w.k0 + wq * 32)
-                                : ((size_t)w.b * p.Hkv + w.g) * p.Nk + (size_t)(w.k0 + wq * 32);
-    const int rows_live = w.nk - (w.k0 + wq * 32);
-    const size_t row_elems = VARLEN ? (size_t)p.Hkv * p.d_act : (size_t)p.d_act;
-    const size_t head_off = VARLEN ? (size_t)w.g * p.d_act * (OUT_F32 ? 4 : 2) : 0;
-    void* dk_base = static_cast<uint8_t*>(p.dk) + head_off;
-    void* dv_base = static_cast<uint8_t*>(p.dv) + head_off;
-    // this warpgroup's half of the columns
+    // this warpgroup's half of the output columns
     const int cc_lo = grp * (D / 2), cc_hi = cc_lo + D / 2;
-    if (w.n_tiles == 0) {
-        float z[32];
-#pragma unroll
-        for (int x = 0; x < 32; ++x) z[x] = 0.f;
-#pragma unroll 1
-        for (int cc = cc_lo; cc < cc_hi && cc < p.d_act; cc += 32) {
-            const int nc = p.d_act - cc < 32 ? p.d_act - cc : 32;
-            store_rows32_pairs<OUT_F32>(dk_base, wrow0, row_elems, cc, z, nc, rows_live, lane);
-            store_rows32_pairs<OUT_F32>(dv_base, wrow0, row_elems, cc, z, nc, rows_live, lane);
+    bool ok = true;
+    int g = 0;  // Q tiles done, over the CTA's items
+    int u = 0;  // items with work
+    for (unsigned idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
+        const BwdWork w = bwd_item<VARLEN>(p, idx, err);
+        const int jg = w.k0 + j;
+        for (int i = 0; i < w.n_tiles && ok; ++i) {
+            const int gi = g + i;
+            const int st = gi & 1;
+            ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&bars->s_full), gi & 1, abort_flag, 32));
+            if (!ok) break;
+            tc_fence_after();
+            const int q0 = (w.qt_first + i % w.n_qt_cta) * kBT;
+            const uint32_t lse2s = smem_u32(smem + C::kLD + st * 1024);
+            const uint32_t ds_vec = lse2s + kBT * 4;
+            // causal: query q0 + x sees key jg iff x >= jg - off - q0
+            const int lim = jg - w.off - q0;
+            const bool masked = p.causal && (q0 + w.off < w.k0 + kBT - 1);
+            // Phase 1: P^T from S^T for this warpgroup's 64 query columns, kept
+            // in registers and written as bf16 over the S^T columns it has read;
+            // with the other warpgroup's, releases dV(i) and S^T(i+1).
+            float pf0[32], pf1[32];
+            auto phase1 = [&](int cc, float (&pf)[32]) {
+                uint32_t sv[32], pp[16];
+                tmem_ld32(tS + cc * 32, sv);
+                tmem_wait_ld();
+                if (masked)
+                    p_chunk<true>(sv, lse2s, cc * 32, p.c, lim, pf, pp);
+                else
+                    p_chunk<false>(sv, lse2s, cc * 32, p.c, lim, pf, pp);
+                tmem_st16(tS + a_chunk_col(cc), pp);
+            };
+            phase1(2 * grp, pf0);
+            phase1(2 * grp + 1, pf1);
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&bars->p_full));
+            // Phase 2: dS^T from P^T and dP^T, written as bf16 over the dP^T
+            // columns already read; releases dK(i) and dP^T(i+1).
+            ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&bars->dp_full), gi & 1, abort_flag, 32));
+            if (!ok) break;
+            tc_fence_after();
+            auto phase2 = [&](int cc, const float (&pf)[32]) {
+                uint32_t dp[32], dd[16];
+                tmem_ld32(tdP + cc * 32, dp);
+                tmem_wait_ld();
+                ds_chunk_t(pf, dp, ds_vec, cc * 32, dd);
+                tmem_st16(tdP + a_chunk_col(cc), dd);
+            };
+            phase2(2 * grp, pf0);
+            phase2(2 * grp + 1, pf1);
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(smem_u32(&bars->ds_full));
+                mbar_arrive(smem_u32(&bars->qd_empty[st]));
+            }
         }
-        return;
-    }
-    ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&bars->acc_full), 0, abort_flag));
-    if (!ok) {
-        bwd_abort(bars, err);
-        return;
-    }
-    tc_fence_after();
+        if (!ok) break;
+        // dK = scale * dS^T Q, dV = P^T dO: one key row per thread, written once
+        // this warp's first key row and how many of its rows are inside Nk
+        // (packed batches: rows of Hkv * d elements, the head's d columns at
+        // offset g * d)
+        const size_t wrow0 = VARLEN ? (size_t)(w.kb + w.k0 + wq * 32)
+                                    : ((size_t)w.b * p.Hkv + w.g) * p.Nk + (size_t)(w.k0 + wq * 32);
+        const int rows_live = w.nk - (w.k0 + wq * 32);
+        const size_t row_elems = VARLEN ? (size_t)p.Hkv * p.d_act : (size_t)p.d_act;
+        const size_t head_off = VARLEN ? (size_t)w.g * p.d_act * (OUT_F32 ? 4 : 2) : 0;
+        void* dk_base = static_cast<uint8_t*>(p.dk) + head_off;
+        void* dv_base = static_cast<uint8_t*>(p.dv) + head_off;
+        if (w.n_tiles == 0) {
+            float z[32];
+#pragma unroll
+            for (int x = 0; x < 32; ++x) z[x] = 0.f;
 #pragma unroll 1
-    for (int cc = cc_lo; cc < cc_hi; cc += 32) {
-        uint32_t r[32];
-        float v[32];
-        tmem_ld32(tmem + 256 + cc + lane_off, r);
-        tmem_wait_ld();
-        const int nc = p.d_act - cc < 32 ? p.d_act - cc : 32;  // <= 0: past the head dim
+            for (int cc = cc_lo; cc < cc_hi && cc < p.d_act; cc += 32) {
+                const int nc = p.d_act - cc < 32 ? p.d_act - cc : 32;
+                store_rows32_pairs<OUT_F32>(dk_base, wrow0, row_elems, cc, z, nc, rows_live, lane);
+                store_rows32_pairs<OUT_F32>(dv_base, wrow0, row_elems, cc, z, nc, rows_live, lane);
+            }
+            continue;
+        }
+        ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&bars->acc_full), u & 1, abort_flag));
+        if (!ok) break;
+        tc_fence_after();
+        // The next item's dV and dK (accumulate = 0) are issued only after this
+        // warpgroup's next P^T arrival, which follows these reads.
+#pragma unroll 1
+        for (int cc = cc_lo; cc < cc_hi; cc += 32) {
+            uint32_t r[32];
+            float v[32];
+            tmem_ld32(tmem + 256 + cc + lane_off, r);
+            tmem_wait_ld();
+            const int nc = p.d_act - cc < 32 ? p.d_act - cc : 32;  // <= 0: past the head dim
 #pragma unroll
-        for (int x = 0; x < 32; ++x) v[x] = __uint_as_float(r[x]);
-        if (nc > 0) store_rows32_pairs<OUT_F32>(dv_base, wrow0, row_elems, cc, v, nc, rows_live, lane);
-        tmem_ld32(tmem + 256 + D + cc + lane_off, r);
-        tmem_wait_ld();
+            for (int x = 0; x < 32; ++x) v[x] = __uint_as_float(r[x]);
+            if (nc > 0) store_rows32_pairs<OUT_F32>(dv_base, wrow0, row_elems, cc, v, nc, rows_live, lane);
+            tmem_ld32(tmem + 256 + D + cc + lane_off, r);
+            tmem_wait_ld();
 #pragma unroll
-        for (int x = 0; x < 32; ++x) v[x] = __uint_as_float(r[x]) * p.scale;
-        if (nc > 0) store_rows32_pairs<OUT_F32>(dk_base, wrow0, row_elems, cc, v, nc, rows_live, lane);
+            for (int x = 0; x < 32; ++x) v[x] = __uint_as_float(r[x]) * p.scale;
+            if (nc > 0) store_rows32_pairs<OUT_F32>(dk_base, wrow0, row_elems, cc, v, nc, rows_live, lane);
+        }
+        tc_fence_before();
+        g += w.n_tiles;
+        ++u;
     }
+    if (!ok) bwd_abort(bars, err);
 }
 
 template <int D, bool OUT_F32, bool VARLEN>
@@ -624,10 +675,11 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tq, const __grid_consta
     BwdBars* bars = reinterpret_cast<BwdBars*>(smem + C::kBar);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const BwdWork w = VARLEN ? bwd_work_varlen(p, err) : bwd_work(p);
+    const unsigned n_items = (unsigned)(p.B * p.Hkv * p.n_kt);
 
     if (threadIdx.x == 0) {
         mbar_init(smem_u32(&bars->kv_full), 1);
+        mbar_init(smem_u32(&bars->kv_empty), 1);  // the commit after an item's last S^T and dP^T
         for (int s = 0; s < 2; ++s) {
             mbar_init(smem_u32(&bars->qd_full[s]), 1);
             mbar_init(smem_u32(&bars->qd_empty[s]), 1 + 8);  // dK commit + 8 P/dS warps
@@ -654,9 +706,9 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tq, const __grid_consta
     tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
 
-    if (warp == 0) bwd_producer<D, VARLEN>(&tq, &tk, &tv, &tdo, smem, bars, p, w, err);
-    else if (warp == 1) bwd_mma<D>(smem, bars, tmem, w, err);
-    else if (warp >= 4) bwd_pds<D, OUT_F32, VARLEN>(warp & 3, (warp - 4) >> 2, lane, smem, bars, tmem, p, w, err);
+    if (warp == 0) bwd_producer<D, VARLEN>(&tq, &tk, &tv, &tdo, smem, bars, p, n_items, err);
+    else if (warp == 1) bwd_mma<D, VARLEN>(smem, bars, tmem, p, n_items, err);
+    else if (warp >= 4) bwd_pds<D, OUT_F32, VARLEN>(warp & 3, (warp - 4) >> 2, lane, smem, bars, tmem, p, n_items, err);
 
     tc_fence_before();
     __syncthreads();
@@ -685,7 +737,7 @@ struct DqCfg {
 };
 
 struct __align__(8) DqBars {
-    uint64_t q_full;
+    uint64_t q_full, q_empty;  // Q and dO of an item; read by its last S and dP
     uint64_t k_full[3], k_empty[3], v_full[2], v_empty[2];
     uint64_t s_full[2], dp_full, ds_full, dq_full, drain;  // s_full[b]: the S in buffer b
     uint32_t tmem_base;
@@ -702,14 +754,14 @@ struct DqWork {
     int nq, nk, off, qb, kb, vbase;  // as in BwdWork
 };
 
-__device__ __forceinline__ DqWork dq_work(const BwdParams& p) {
+__device__ __forceinline__ DqWork dq_work(const BwdParams& p, unsigned idx) {
     DqWork w;
     const int n_qt = (p.Nq + kBT - 1) / kBT;
     const unsigned all = (unsigned)(p.B * p.Hkv);
     const unsigned S = (unsigned)p.sec_groups;
     const unsigned per_sec = S * (unsigned)p.group * (unsigned)n_qt;
-    const unsigned sec = blockIdx.x / per_sec;
-    const unsigned r = blockIdx.x - sec * per_sec;
+    const unsigned sec = idx / per_sec;
+    const unsigned r = idx - sec * per_sec;
     const unsigned rest = all - sec * S;
     const unsigned gs = rest < S ? rest : S;
     const unsigned per_rank = gs * (unsigned)p.group;
@@ -738,15 +790,15 @@ __device__ __forceinline__ DqWork dq_work(const BwdParams& p) {
     return w;
 }
 
-// The same for packed batches: CTA index = (b * Hq + hq) * n_qt + qt, n_qt for
-// the longest query length; Q tiles past a sequence's end, and every tile of a
+// The same for packed batches: item index = (b * Hq + hq) * n_qt + qt, n_qt
+// for the longest query length; Q tiles past a sequence's end, and every tile of a
 // sequence whose offsets fail the checks, have no work and write nothing.
-__device__ __forceinline__ DqWork dq_work_varlen(const BwdParams& p, unsigned int* err) {
+__device__ __forceinline__ DqWork dq_work_varlen(const BwdParams& p, unsigned idx, unsigned int* err) {
     DqWork w;
     const int n_qt = (p.Nq + kBT - 1) / kBT;
     const int per_b = p.Hq * n_qt;
-    w.b = (int)blockIdx.x / per_b;
-    const int rem = (int)blockIdx.x - w.b * per_b;
+    w.b = (int)idx / per_b;
+    const int rem = (int)idx - w.b * per_b;
     w.hq = rem / n_qt;
     w.g = w.hq / p.group;
     w.q0 = (rem - w.hq * n_qt) * kBT;
@@ -775,82 +827,102 @@ __device__ __forceinline__ DqWork dq_work_varlen(const BwdParams& p, unsigned in
     return w;
 }
 
+// The dQ pass runs a persistent grid as the dK/dV pass does: CTA c takes items
+// c, c + gridDim.x, ... of the order above, each one Q tile.
+template <bool VARLEN>
+__device__ __forceinline__ DqWork dq_item(const BwdParams& p, unsigned idx, unsigned int* err) {
+    if constexpr (VARLEN) return dq_work_varlen(p, idx, err);
+    else return dq_work(p, idx);
+}
+
 template <int D, bool VARLEN>
 __device__ void dq_producer(const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv,
                             const CUtensorMap* tdo, uint8_t* smem, DqBars* bars, const BwdParams& p,
-                            const DqWork& w, unsigned int* err) {
+                            unsigned n_items, unsigned int* err) {
     using C = DqCfg<D>;
     const volatile int* abort_flag = &bars->abort;
     const bool leader = elect_one();
-    const int bh = w.b * p.Hq + w.hq;
-    // K/V head: an index into [B * Hkv], or into [Hkv] of the packed rows
-    const int kvh = VARLEN ? w.g : w.b * p.Hkv + w.g;
-    if (leader) {
-        const uint32_t bar = smem_u32(&bars->q_full);
-        mbar_arrive_expect_tx(bar, 2 * C::kTile);
-#pragma unroll
-        for (int c = 0; c < D / 64; ++c) {
-            if constexpr (VARLEN) {
-                const int r = kRaggedWindow - w.nq + w.q0;
-                tma_load_5d(smem_u32(smem + C::kQ) + c * 16384, tq, bar, 64 * c, w.hq, r, w.qb + w.nq,
-                            kRaggedWindow);
-                tma_load_5d(smem_u32(smem + C::kDO) + c * 16384, tdo, bar, 64 * c, w.hq, r, w.qb + w.nq,
-                            kRaggedWindow);
-            } else {
-                tma_load_3d(smem_u32(smem + C::kQ) + c * 16384, tq, bar, 64 * c, w.q0, bh);
-                tma_load_3d(smem_u32(smem + C::kDO) + c * 16384, tdo, bar, 64 * c, w.q0, bh);
-            }
-        }
-    }
-    __syncwarp();
-    // K_j into stage j % 3 (free once dQ(j-3) has read it), V_j into stage
-    // j % 2 (free once dP(j-2) has read it).
     bool ok = true;
-    int nk = 0, nv = 0;  // K and V loads issued
-    for (int j = 0; j < w.n_kv && ok; ++j) {
-        const int sk = j % 3, sv = j & 1;
-        if (j >= 3)
-            ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&bars->k_empty[sk]), ((j / 3) - 1) & 1,
-                                                   abort_flag));
+    int q_uses = 0;      // Q / dO loads issued (items with work)
+    int nk = 0, nv = 0;  // K and V loads issued, over the CTA's items
+    for (unsigned idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
+        const DqWork w = dq_item<VARLEN>(p, idx, err);
+        if (w.n_kv == 0) continue;
+        // Q and dO of the item, once the previous item's last S and dP have
+        // read theirs
+        if (q_uses > 0)
+            ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&bars->q_empty), (q_uses - 1) & 1, abort_flag));
         if (!ok) break;
+        const int bh = w.b * p.Hq + w.hq;
+        // K/V head: an index into [B * Hkv], or into [Hkv] of the packed rows
+        const int kvh = VARLEN ? w.g : w.b * p.Hkv + w.g;
         if (leader) {
-            const uint32_t bar = smem_u32(&bars->k_full[sk]);
-            mbar_arrive_expect_tx(bar, C::kTile);
-            const uint32_t dst = smem_u32(smem + C::kKRing + sk * C::kTile);
+            const uint32_t bar = smem_u32(&bars->q_full);
+            mbar_arrive_expect_tx(bar, 2 * C::kTile);
 #pragma unroll
             for (int c = 0; c < D / 64; ++c) {
-                if constexpr (VARLEN)
-                    tma_load_5d(dst + c * 16384, tk, bar, 64 * c, kvh, kRaggedWindow - w.nk + j * kBT,
-                                w.kb + w.nk, kRaggedWindow);
-                else
-                    tma_load_3d(dst + c * 16384, tk, bar, 64 * c, j * kBT, kvh);
+                if constexpr (VARLEN) {
+                    const int r = kRaggedWindow - w.nq + w.q0;
+                    tma_load_5d(smem_u32(smem + C::kQ) + c * 16384, tq, bar, 64 * c, w.hq, r, w.qb + w.nq,
+                                kRaggedWindow);
+                    tma_load_5d(smem_u32(smem + C::kDO) + c * 16384, tdo, bar, 64 * c, w.hq, r, w.qb + w.nq,
+                                kRaggedWindow);
+                } else {
+                    tma_load_3d(smem_u32(smem + C::kQ) + c * 16384, tq, bar, 64 * c, w.q0, bh);
+                    tma_load_3d(smem_u32(smem + C::kDO) + c * 16384, tdo, bar, 64 * c, w.q0, bh);
+                }
             }
         }
         __syncwarp();
-        ++nk;
-        if (j >= 2)
-            ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&bars->v_empty[sv]), ((j >> 1) - 1) & 1,
-                                                   abort_flag));
-        if (!ok) break;
-        if (leader) {
-            const uint32_t bar = smem_u32(&bars->v_full[sv]);
-            mbar_arrive_expect_tx(bar, C::kTile);
-            const uint32_t dst = smem_u32(smem + C::kVRing + sv * C::kTile);
+        ++q_uses;
+        // K_j into stage (K tile count) % 3 (free once the dQ product three K
+        // tiles back has read it), V_j into stage (V tile count) % 2 (free once
+        // the dP product two V tiles back has read it).
+        for (int j = 0; j < w.n_kv && ok; ++j) {
+            const int sk = nk % 3, sv = nv & 1;
+            if (nk >= 3)
+                ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&bars->k_empty[sk]), ((nk / 3) - 1) & 1,
+                                                       abort_flag));
+            if (!ok) break;
+            if (leader) {
+                const uint32_t bar = smem_u32(&bars->k_full[sk]);
+                mbar_arrive_expect_tx(bar, C::kTile);
+                const uint32_t dst = smem_u32(smem + C::kKRing + sk * C::kTile);
 #pragma unroll
-            for (int c = 0; c < D / 64; ++c) {
-                if constexpr (VARLEN)
-                    tma_load_5d(dst + c * 16384, tv, bar, 64 * c, kvh, kRaggedWindow - w.nk + j * kBT,
-                                w.kb + w.nk, kRaggedWindow);
-                else
-                    tma_load_3d(dst + c * 16384, tv, bar, 64 * c, j * kBT, kvh);
+                for (int c = 0; c < D / 64; ++c) {
+                    if constexpr (VARLEN)
+                        tma_load_5d(dst + c * 16384, tk, bar, 64 * c, kvh, kRaggedWindow - w.nk + j * kBT,
+                                    w.kb + w.nk, kRaggedWindow);
+                    else
+                        tma_load_3d(dst + c * 16384, tk, bar, 64 * c, j * kBT, kvh);
+                }
             }
+            __syncwarp();
+            ++nk;
+            if (nv >= 2)
+                ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&bars->v_empty[sv]), ((nv >> 1) - 1) & 1,
+                                                       abort_flag));
+            if (!ok) break;
+            if (leader) {
+                const uint32_t bar = smem_u32(&bars->v_full[sv]);
+                mbar_arrive_expect_tx(bar, C::kTile);
+                const uint32_t dst = smem_u32(smem + C::kVRing + sv * C::kTile);
+#pragma unroll
+                for (int c = 0; c < D / 64; ++c) {
+                    if constexpr (VARLEN)
+                        tma_load_5d(dst + c * 16384, tv, bar, 64 * c, kvh, kRaggedWindow - w.nk + j * kBT,
+                                    w.kb + w.nk, kRaggedWindow);
+                    else
+                        tma_load_3d(dst + c * 16384, tv, bar, 64 * c, j * kBT, kvh);
+                }
+            }
+            __syncwarp();
+            ++nv;
         }
-        __syncwarp();
-        ++nv;
     }
     if (!ok && leader) atomicOr(err, kErrTimeout), *((volatile int*)&bars->abort) = 1;
     // Drain: every issued copy lands before the CTA may exit.
-    mbar_wait(smem_u32(&bars->q_full), 0, nullptr);
+    if (q_uses > 0) mbar_wait(smem_u32(&bars->q_full), (q_uses - 1) & 1, nullptr);
     for (int sk = 0; sk < 3 && sk < nk; ++sk) {
         const int uses = (nk - sk + 2) / 3;
         mbar_wait(smem_u32(&bars->k_full[sk]), (uses - 1) & 1, nullptr);
@@ -862,8 +934,8 @@ __device__ void dq_producer(const CUtensorMap* tq, const CUtensorMap* tk, const 
     __syncwarp();
 }
 
-template <int D>
-__device__ void dq_mma(uint8_t* smem, DqBars* bars, uint32_t tmem, const DqWork& w,
+template <int D, bool VARLEN>
+__device__ void dq_mma(uint8_t* smem, DqBars* bars, uint32_t tmem, const BwdParams& p, unsigned n_items,
                        unsigned int* err) {
     using C = DqCfg<D>;
     const volatile int* abort_flag = &bars->abort;
@@ -871,7 +943,9 @@ __device__ void dq_mma(uint8_t* smem, DqBars* bars, uint32_t tmem, const DqWork&
     const uint32_t idS = make_idesc_bf16(128, 128, 0, 0);
     const uint32_t idQ = make_idesc_bf16(128, D, 0, 1);
     const uint32_t tdP = tmem + 128, tdQ = tmem + 256;
-    auto tS = [&](int j) { return tmem + ((j & 1) ? 384u : 0u); };  // S buffer of tile j
+    // K/V tiles are counted over the CTA's items (t): S buffer t & 1, K stage
+    // t % 3, V stage t % 2
+    auto tS = [&](int t) { return tmem + ((t & 1) ? 384u : 0u); };
     const uint32_t q_k = sdesc_lo(smem_u32(smem + C::kQ), 16);
     const uint32_t do_k = sdesc_lo(smem_u32(smem + C::kDO), 16);
     auto k_k = [&](int sk) { return sdesc_lo(smem_u32(smem + C::kKRing + sk * C::kTile), 16); };
@@ -880,41 +954,56 @@ __device__ void dq_mma(uint8_t* smem, DqBars* bars, uint32_t tmem, const DqWork&
     auto wait_all = [&](uint32_t bar, uint32_t parity, int polls) {
         return __all_sync(0xFFFFFFFFu, mbar_wait(bar, parity, abort_flag, polls));
     };
-    auto issue_s = [&](int j) {  // S_j = Q K_j^T into buffer j & 1
-        if (!wait_all(smem_u32(&bars->k_full[j % 3]), (uint32_t)((j / 3) & 1), 0)) return false;
+    auto issue_s = [&](int t) {  // S = Q K^T of K/V tile t into buffer t & 1
+        if (!wait_all(smem_u32(&bars->k_full[t % 3]), (uint32_t)((t / 3) & 1), 0)) return false;
         tc_fence_after();
-        issue_kmajor<D>(tS(j), q_k, k_k(j % 3), idS);
-        mma_commit_warp(smem_u32(&bars->s_full[j & 1]));
+        issue_kmajor<D>(tS(t), q_k, k_k(t % 3), idS);
+        mma_commit_warp(smem_u32(&bars->s_full[t & 1]));
         return true;
     };
-    auto issue_dp = [&](int j) {  // dP_j = dO V_j^T
-        if (!wait_all(smem_u32(&bars->v_full[j & 1]), (uint32_t)((j >> 1) & 1), 0)) return false;
+    auto issue_dp = [&](int t) {  // dP = dO V^T of K/V tile t
+        if (!wait_all(smem_u32(&bars->v_full[t & 1]), (uint32_t)((t >> 1) & 1), 0)) return false;
         tc_fence_after();
-        issue_kmajor<D>(tdP, do_k, v_k(j & 1), idS);
-        mma_commit_warp(smem_u32(&bars->v_empty[j & 1]));  // V_j is read
+        issue_kmajor<D>(tdP, do_k, v_k(t & 1), idS);
+        mma_commit_warp(smem_u32(&bars->v_empty[t & 1]));  // V of tile t is read
         mma_commit_warp(smem_u32(&bars->dp_full));
         return true;
     };
-    // Order: S_0, dP_0, S_1; then per tile j, once dS_j is in TMEM: dQ += dS_j
-    // K_j, dP_{j+1} (into the dP columns the dS warps have read), S_{j+2} (into
-    // the buffer dQ_j has read; one CTA's MMAs run in issue order).  The dS
-    // warps' exponentials for tile j+1 overlap dQ_j and dP_{j+1}.
+    // Per item: S_0, dP_0, S_1; then per tile j, once dS_j is in TMEM: dQ +=
+    // dS_j K_j, dP_{j+1} (into the dP columns the dS warps have read), S_{j+2}
+    // (into the buffer dQ_j has read; one CTA's MMAs run in issue order).  The
+    // dS warps' exponentials for tile j+1 overlap dQ_j and dP_{j+1}.  An item's
+    // first S and dP use columns the previous item's products have read; its
+    // first dQ (accumulate = 0) waits for its first dS, which the dS warps
+    // write after reading out the previous item's dQ.
     bool ok = true;
-    if (w.n_kv > 0) {
-        ok = wait_all(smem_u32(&bars->q_full), 0, 0);
-        if (ok) ok = issue_s(0);
-        if (ok) ok = issue_dp(0);
-        if (ok && w.n_kv > 1) ok = issue_s(1);
-        for (int j = 0; j < w.n_kv && ok; ++j) {
-            ok = wait_all(smem_u32(&bars->ds_full), j & 1, 32);
+    int t0 = 0;  // K/V tiles before this item
+    int u = 0;   // items with work
+    for (unsigned idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
+        const DqWork w = dq_item<VARLEN>(p, idx, err);
+        const int n = w.n_kv;
+        if (n == 0) continue;
+        ok = wait_all(smem_u32(&bars->q_full), u & 1, 0);
+        if (ok) ok = issue_s(t0);
+        if (ok) ok = issue_dp(t0);
+        if (ok && n == 1) mma_commit_warp(smem_u32(&bars->q_empty));  // Q and dO are read
+        if (ok && n > 1) ok = issue_s(t0 + 1);
+        for (int j = 0; j < n && ok; ++j) {
+            const int t = t0 + j;
+            ok = wait_all(smem_u32(&bars->ds_full), t & 1, 32);
             if (!ok) break;
             tc_fence_after();
-            issue_tmem_a(tdQ, tS(j), k_mn(j % 3), idQ, j > 0);  // dQ += dS_j K_j
-            mma_commit_warp(smem_u32(&bars->k_empty[j % 3]));   // K_j is read (S_j, dQ_j)
-            if (j + 1 < w.n_kv && !(ok = issue_dp(j + 1))) break;
-            if (j + 2 < w.n_kv && !(ok = issue_s(j + 2))) break;
+            issue_tmem_a(tdQ, tS(t), k_mn(t % 3), idQ, j > 0);  // dQ += dS_j K_j
+            mma_commit_warp(smem_u32(&bars->k_empty[t % 3]));   // K_j is read (S_j, dQ_j)
+            if (j + 1 < n) {
+                if (!(ok = issue_dp(t + 1))) break;
+                if (j + 2 == n) mma_commit_warp(smem_u32(&bars->q_empty));  // the last S and dP
+            }
+            if (j + 2 < n && !(ok = issue_s(t + 2))) break;
         }
         if (ok) mma_commit_warp(smem_u32(&bars->dq_full));
+        t0 += n;
+        ++u;
     }
     if (!ok && leader) atomicOr(err, kErrTimeout), *((volatile int*)&bars->abort) = 1;
     mma_commit_warp(smem_u32(&bars->drain));
@@ -957,89 +1046,107 @@ __device__ __forceinline__ void ds_row_chunk(const float (&pf)[32], const uint32
 
 template <int D, bool OUT_F32, bool VARLEN>
 __device__ void dq_ds(int wq, int grp, int lane, DqBars* bars, uint32_t tmem, const BwdParams& p,
-                      const DqWork& w, unsigned int* err) {
+                      unsigned n_items, unsigned int* err) {
     const volatile int* abort_flag = &bars->abort;
     const uint32_t lane_off = uint32_t(wq * 32) << 16;
     const uint32_t tdP = tmem + 128 + lane_off;
-    const int row = w.q0 + wq * 32 + lane;
-    const size_t bh = (size_t)w.b * p.Hq + w.hq;
-    const size_t vrow = VARLEN ? (size_t)w.hq * p.vstride + (size_t)(w.vbase + row)
-                               : bh * p.Nq_pad + row;
-    // +inf past the last query: P = 0 (a tile with no work reads nothing: its
-    // rows may lie past the sequence's rows of lse2 / dvec)
-    const float lse2 = w.n_kv > 0 ? p.lse2[vrow] : INFINITY;
-    const float dval = w.n_kv > 0 ? p.dvec[vrow] : 0.f;
-    const uint64_t c2 = f2(p.c, p.c), nl2 = f2(-lse2, -lse2), nd2 = f2(-dval, -dval);
+    const uint64_t c2 = f2(p.c, p.c);
     bool ok = true;
-    for (int j = 0; j < w.n_kv && ok; ++j) {
-        const uint32_t tS = tmem + ((j & 1) ? 384u : 0u) + lane_off;
-        ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&bars->s_full[j & 1]), (j >> 1) & 1, abort_flag, 32));
+    int t0 = 0;  // K/V tiles before this item, over the CTA's items
+    int u = 0;   // items with work
+    for (unsigned idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
+        const DqWork w = dq_item<VARLEN>(p, idx, err);
+        const int row = w.q0 + wq * 32 + lane;
+        const size_t bh = (size_t)w.b * p.Hq + w.hq;
+        const size_t vrow = VARLEN ? (size_t)w.hq * p.vstride + (size_t)(w.vbase + row)
+                                   : bh * p.Nq_pad + row;
+        // +inf past the last query: P = 0 (a tile with no work reads nothing:
+        // its rows may lie past the sequence's rows of lse2 / dvec)
+        const float lse2 = w.n_kv > 0 ? p.lse2[vrow] : INFINITY;
+        const float dval = w.n_kv > 0 ? p.dvec[vrow] : 0.f;
+        const uint64_t nl2 = f2(-lse2, -lse2), nd2 = f2(-dval, -dval);
+        for (int j = 0; j < w.n_kv && ok; ++j) {
+            const int t = t0 + j;
+            const uint32_t tS = tmem + ((t & 1) ? 384u : 0u) + lane_off;
+            ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&bars->s_full[t & 1]), (t >> 1) & 1, abort_flag, 32));
+            if (!ok) break;
+            tc_fence_after();
+            const int lim = row + w.off - j * kBT;  // causal: key column c allowed iff c <= lim
+            const bool masked = __any_sync(0xFFFFFFFFu, p.causal && lim < kBT - 1);
+            // Phase 1: P from S for this warpgroup's 64 key columns (needs S_j
+            // only; runs while dQ_{j-1} and dP_j compute)
+            float pf0[32], pf1[32];
+            auto phase1 = [&](int cc, float (&pf)[32]) {
+                uint32_t sv[32];
+                tmem_ld32(tS + cc * 32, sv);
+                tmem_wait_ld();
+                if (masked)
+                    p_row_chunk<true>(sv, c2, nl2, cc * 32, p.causal ? lim : kBT, pf);
+                else
+                    p_row_chunk<false>(sv, c2, nl2, cc * 32, kBT, pf);
+            };
+            phase1(2 * grp, pf0);
+            phase1(2 * grp + 1, pf1);
+            // Phase 2: dS from P and dP, as bf16 over the S columns this
+            // warpgroup read
+            ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&bars->dp_full), t & 1, abort_flag, 32));
+            if (!ok) break;
+            tc_fence_after();
+            auto phase2 = [&](int cc, const float (&pf)[32]) {
+                uint32_t dp[32], dd[16];
+                tmem_ld32(tdP + cc * 32, dp);
+                tmem_wait_ld();
+                ds_row_chunk(pf, dp, nd2, dd);
+                tmem_st16(tS + a_chunk_col(cc), dd);
+            };
+            phase2(2 * grp, pf0);
+            phase2(2 * grp + 1, pf1);
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&bars->ds_full));
+        }
         if (!ok) break;
-        tc_fence_after();
-        const int lim = row + w.off - j * kBT;  // causal: key column c allowed iff c <= lim
-        const bool masked = __any_sync(0xFFFFFFFFu, p.causal && lim < kBT - 1);
-        // Phase 1: P from S for this warpgroup's 64 key columns (needs S_j only;
-        // runs while dQ_{j-1} and dP_j compute)
-        float pf0[32], pf1[32];
-        auto phase1 = [&](int cc, float (&pf)[32]) {
-            uint32_t sv[32];
-            tmem_ld32(tS + cc * 32, sv);
-            tmem_wait_ld();
-            if (masked)
-                p_row_chunk<true>(sv, c2, nl2, cc * 32, p.causal ? lim : kBT, pf);
-            else
-                p_row_chunk<false>(sv, c2, nl2, cc * 32, kBT, pf);
-        };
-        phase1(2 * grp, pf0);
-        phase1(2 * grp + 1, pf1);
-        // Phase 2: dS from P and dP, as bf16 over the S columns this warpgroup read
-        ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&bars->dp_full), j & 1, abort_flag, 32));
-        if (!ok) break;
-        tc_fence_after();
-        auto phase2 = [&](int cc, const float (&pf)[32]) {
-            uint32_t dp[32], dd[16];
-            tmem_ld32(tdP + cc * 32, dp);
-            tmem_wait_ld();
-            ds_row_chunk(pf, dp, nd2, dd);
-            tmem_st16(tS + a_chunk_col(cc), dd);
-        };
-        phase2(2 * grp, pf0);
-        phase2(2 * grp + 1, pf1);
-        tmem_wait_st();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&bars->ds_full));
+        if (w.n_kv > 0) {
+            ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&bars->dq_full), u & 1, abort_flag));
+            if (!ok) break;
+            tc_fence_after();
+        }
+        // every lane runs the (warp-collective) TMEM loads; rows past Nq store
+        // nothing.  This warp's first query row and how many of its rows are
+        // inside Nq (packed batches: rows of Hq * d elements, the head's d
+        // columns at hq * d).  The next item's first dQ product (accumulate =
+        // 0) is issued only after this warpgroup's next dS arrival, which
+        // follows these reads.
+        const size_t wrow0 = VARLEN ? (size_t)(w.qb + w.q0 + wq * 32) : bh * p.Nq + (size_t)(w.q0 + wq * 32);
+        const int rows_live = w.nq - (w.q0 + wq * 32);
+        const size_t row_elems = VARLEN ? (size_t)p.Hq * p.d_act : (size_t)p.d_act;
+        void* dq_base = static_cast<uint8_t*>(p.dq) + (VARLEN ? (size_t)w.hq * p.d_act * (OUT_F32 ? 4 : 2) : 0);
+#pragma unroll 1
+        for (int cc = grp * (D / 2); cc < (grp + 1) * (D / 2); cc += 32) {  // this warpgroup's half
+            float v[32];
+            if (w.n_kv > 0) {
+                uint32_t r[32];
+                tmem_ld32(tmem + 256 + cc + lane_off, r);
+                tmem_wait_ld();
+#pragma unroll
+                for (int x = 0; x < 32; ++x) v[x] = __uint_as_float(r[x]) * p.scale;
+            } else {
+#pragma unroll
+                for (int x = 0; x < 32; ++x) v[x] = 0.f;
+            }
+            const int nc = p.d_act - cc < 32 ? p.d_act - cc : 32;
+            if (nc > 0) store_rows32_pairs<OUT_F32>(dq_base, wrow0, row_elems, cc, v, nc, rows_live, lane);
+        }
+        if (w.n_kv > 0) {
+            tc_fence_before();
+            t0 += w.n_kv;
+            ++u;
+        }
     }
-    if (ok && w.n_kv > 0)
-        ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&bars->dq_full), 0, abort_flag));
     if (!ok) {
         atomicOr(err, kErrTimeout);
         *((volatile int*)&bars->abort) = 1;
-        return;
-    }
-    tc_fence_after();
-    // every lane runs the (warp-collective) TMEM loads; rows past Nq store nothing
-    // this warp's first query row and how many of its rows are inside Nq
-    // (packed batches: rows of Hq * d elements, the head's d columns at hq * d)
-    const size_t wrow0 = VARLEN ? (size_t)(w.qb + w.q0 + wq * 32) : bh * p.Nq + (size_t)(w.q0 + wq * 32);
-    const int rows_live = w.nq - (w.q0 + wq * 32);
-    const size_t row_elems = VARLEN ? (size_t)p.Hq * p.d_act : (size_t)p.d_act;
-    void* dq_base = static_cast<uint8_t*>(p.dq) + (VARLEN ? (size_t)w.hq * p.d_act * (OUT_F32 ? 4 : 2) : 0);
-#pragma unroll 1
-    for (int cc = grp * (D / 2); cc < (grp + 1) * (D / 2); cc += 32) {  // this warpgroup's half
-        float v[32];
-        if (w.n_kv > 0) {
-            uint32_t r[32];
-            tmem_ld32(tmem + 256 + cc + lane_off, r);
-            tmem_wait_ld();
-#pragma unroll
-            for (int x = 0; x < 32; ++x) v[x] = __uint_as_float(r[x]) * p.scale;
-        } else {
-#pragma unroll
-            for (int x = 0; x < 32; ++x) v[x] = 0.f;
-        }
-        const int nc = p.d_act - cc < 32 ? p.d_act - cc : 32;
-        if (nc > 0) store_rows32_pairs<OUT_F32>(dq_base, wrow0, row_elems, cc, v, nc, rows_live, lane);
     }
 }
 
@@ -1059,9 +1166,10 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
     DqBars* bars = reinterpret_cast<DqBars*>(smem + C::kBar);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const DqWork w = VARLEN ? dq_work_varlen(p, err) : dq_work(p);
+    const unsigned n_items = (unsigned)(p.B * p.Hq * ((p.Nq + kBT - 1) / kBT));
     if (threadIdx.x == 0) {
         mbar_init(smem_u32(&bars->q_full), 1);
+        mbar_init(smem_u32(&bars->q_empty), 1);  // the commit after an item's last S and dP
         for (int s = 0; s < 3; ++s) {
             mbar_init(smem_u32(&bars->k_full[s]), 1);
             mbar_init(smem_u32(&bars->k_empty[s]), 1);
@@ -1090,9 +1198,9 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
-    if (warp == 0) dq_producer<D, VARLEN>(&tq, &tk, &tv, &tdo, smem, bars, p, w, err);
-    else if (warp == 1) dq_mma<D>(smem, bars, tmem, w, err);
-    else if (warp >= 4) dq_ds<D, OUT_F32, VARLEN>(warp & 3, (warp - 4) >> 2, lane, bars, tmem, p, w, err);
+    if (warp == 0) dq_producer<D, VARLEN>(&tq, &tk, &tv, &tdo, smem, bars, p, n_items, err);
+    else if (warp == 1) dq_mma<D, VARLEN>(smem, bars, tmem, p, n_items, err);
+    else if (warp >= 4) dq_ds<D, OUT_F32, VARLEN>(warp & 3, (warp - 4) >> 2, lane, bars, tmem, p, n_items, err);
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
@@ -1283,12 +1391,15 @@ attn_status_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const C
     }
     if (st != ATTN_OK) return st;
     // (packed batches: units at the longest lengths; the tiles past a
-    // sequence's end have no work)
-    const long long kv_ctas = (long long)p.B * p.Hkv * p.n_kt;
+    // sequence's end have no work).  The dK/dV pass is persistent: at most one
+    // CTA per SM, each taking every gridDim.x-th key tile.
+    const long long kv_items = (long long)p.B * p.Hkv * p.n_kt;
+    const long long kv_ctas = kv_items < dev.num_sms ? kv_items : dev.num_sms;
     attn_bwd_dkdv_kernel<D, OUT_F32, VARLEN><<<(unsigned)kv_ctas, kBwdThreadsEw, BwdCfg<D>::kSmemBytes,
                                                stream>>>(tq, tk, tv, tdo, p, dev.err_word);
     if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
-    const long long q_ctas = (long long)p.B * p.Hq * ((p.Nq + kBT - 1) / kBT);
+    const long long q_items = (long long)p.B * p.Hq * ((p.Nq + kBT - 1) / kBT);
+    const long long q_ctas = q_items < dev.num_sms ? q_items : dev.num_sms;  // persistent, as above
     attn_bwd_dq_kernel<D, OUT_F32, VARLEN><<<(unsigned)q_ctas, kBwdThreadsEw, DqCfg<D>::kSmemBytes,
                                              stream>>>(tq, tk, tv, tdo, p, dev.err_word);
     return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
@@ -1809,7 +1920,7 @@ struct WideDqWork {
 // for a Q tile past the sequence's queries.
 template <bool VARLEN>
 __device__ __forceinline__ WideDqWork wide_dq_work(const BwdParams& p, unsigned int* err) {
-    const DqWork d = VARLEN ? dq_work_varlen(p, err) : dq_work(p);
+    const DqWork d = VARLEN ? dq_work_varlen(p, blockIdx.x, err) : dq_work(p, blockIdx.x);
     WideDqWork w;
     w.b = d.b;
     w.g = d.g;
