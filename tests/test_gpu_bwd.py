@@ -182,3 +182,23 @@ def test_bwd_wide_chained_bf16_and_repeatable():
     rq, rk, rv = oracle.attention_bwd(q, k, v, do, causal=True, scale=1 / 16)
     for got, ref, n in zip(a, (rq, rk, rv), ("dQ", "dK", "dV")):
         _check(got, ref, n, bf16=True)
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,N,d,causal", [
+    (2, 16, 16, 1024, 128, False),
+    (2, 16, 16, 1024, 128, True),
+    (2, 32, 8, 2048, 64, True),   # GQA: four query heads per dK/dV item
+])
+def test_bwd_persistent_many_items(B, Hq, Hkv, N, d, causal):
+    """More dK/dV and dQ items than SMs, so each persistent CTA runs several
+    items back to back (rings, barrier phases and TMEM accumulators carried
+    from one item into the next); every head against the oracle."""
+    q, k, v = make_fwd_inputs(B, Hq, Hkv, N, N, d, seed=950 + N + d)
+    do = _dout(q.shape, seed=951)
+    scale = 1 / math.sqrt(d)
+    dq, dk, dv = _run(q, k, v, do, causal, scale)
+    rq, rk, rv = oracle.attention_bwd(q, k, v, do, causal=causal, scale=scale)
+    what = f"{(B, Hq, Hkv, N, d, causal)}"
+    _check(dq, rq, "dQ " + what)
+    _check(dk, rk, "dK " + what)
+    _check(dv, rv, "dV " + what)

@@ -311,6 +311,23 @@ def test_varlen_bwd_cross_lengths(d):
     _check(gv, rv, "dV bf16", bf16=True)
 
 
+@pytest.mark.parametrize("d,causal", [(128, True), (64, False)])
+def test_varlen_bwd_many_sequences(d, causal):
+    """Sixty sequences of 1..700 tokens: far more items than SMs, most of
+    them past their sequence's end (no work), mixed with short and long ones
+    on the same persistent CTAs."""
+    rng = np.random.default_rng(957)
+    lens = [int(x) for x in rng.integers(1, 701, 60)]
+    q, k, v, cu_q, cu_k = make_varlen_inputs(lens, lens, 4, 2, d, seed=958)
+    do = _dout_packed(q.shape, 959)
+    scale = 1 / math.sqrt(d)
+    dq, dk, dv = gpu_bwd_varlen(q, k, v, do, cu_q, cu_k, causal, scale)
+    rq, rk, rv = oracle.attention_bwd_varlen(q, k, v, do, cu_q, cu_k, causal=causal, scale=scale)
+    _bwd_close(dq, rq, slice(None), f"dQ d={d} causal={causal}")
+    _bwd_close(dk, rk, slice(None), f"dK d={d} causal={causal}")
+    _bwd_close(dv, rv, slice(None), f"dV d={d} causal={causal}")
+
+
 @pytest.mark.parametrize("d", [128, 256])
 def test_varlen_bwd_equal_lengths_bit_identical_to_dense(d):
     """All sequences of one length: the dense backward's tiles and arithmetic
