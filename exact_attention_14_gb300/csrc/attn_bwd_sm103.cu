@@ -84,7 +84,8 @@ struct BwdCfg {
     static constexpr int kV = kTile;
     static constexpr int kQ = 2 * kTile;        // 2 stages
     static constexpr int kDO = 4 * kTile;       // 2 stages
-    static constexpr int kLD = 6 * kTile;       // 2 stages x (lse2[128], D[128])
+    static constexpr int kStg = 6 * kTile;      // 8 P/dS warps x 4 KiB: dK / dV store staging
+    static constexpr int kLD = kStg + 8 * 4096; // 2 stages x (lse2[128], D[128])
     static constexpr int kBar = kLD + 2 * 1024;
     static constexpr int kLayout = kBar + 256;
     static constexpr int kSmemBytes =
@@ -538,7 +539,8 @@ __device__ __forceinline__ void store_rows32_pairs(void* base, size_t row0, size
 
 template <int D, bool OUT_F32, bool VARLEN>
 __device__ void bwd_pds(int wq, int grp, int lane, uint8_t* smem, BwdBars* bars, uint32_t tmem,
-                        const BwdParams& p, unsigned n_items, unsigned int* err) {
+                        const CUtensorMap* tdk, const CUtensorMap* tdv, const BwdParams& p,
+                        unsigned n_items, unsigned int* err) {
     using C = BwdCfg<D>;
     const volatile int* abort_flag = &bars->abort;
     const uint32_t lane_off = uint32_t(wq * 32) << 16;
@@ -635,6 +637,55 @@ __device__ void bwd_pds(int wq, int grp, int lane, uint8_t* smem, BwdBars* bars,
         tc_fence_after();
         // The next item's dV and dK (accumulate = 0) are issued only after this
         // warpgroup's next P^T arrival, which follows these reads.
+        if constexpr (D == 128) {
+            // dV, then dK (x scale): boxes of 32 rows x 128 bytes written into the
+            // warp's 4 KiB of shared memory (128-byte swizzle) and stored by the
+            // tensor-memory accelerator, so the stores drain while the next item
+            // runs; a box waits only until the warp's previous one has been read.
+            constexpr int kBoxCols = OUT_F32 ? 32 : 64;
+            const uint32_t stg = smem_u32(smem + C::kStg + (grp * 4 + wq) * 4096);
+#pragma unroll 1
+            for (int t = 0; t < 2; ++t) {
+                const float sc = t ? p.scale : 1.f;
+#pragma unroll 1
+                for (int c0 = 0; c0 < D / 2; c0 += kBoxCols) {
+                    uint32_t wv[32];
+#pragma unroll
+                    for (int c = 0; c < kBoxCols; c += 32) {
+                        uint32_t r[32];
+                        tmem_ld32(tmem + 256 + t * D + cc_lo + c0 + c + lane_off, r);
+                        tmem_wait_ld();
+                        if constexpr (OUT_F32) {
+#pragma unroll
+                            for (int x = 0; x < 32; ++x) wv[x] = __float_as_uint(__uint_as_float(r[x]) * sc);
+                        } else {
+#pragma unroll
+                            for (int x = 0; x < 16; ++x)
+                                wv[c / 2 + x] = pack_bf16x2(__uint_as_float(r[2 * x]) * sc,
+                                                            __uint_as_float(r[2 * x + 1]) * sc);
+                        }
+                    }
+                    if (lane == 0) bulk_wait_group_read<0>();
+                    __syncwarp();
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        sts128(stg + (uint32_t)(lane * 128 + ((j ^ (lane & 7)) << 4)), wv[4 * j], wv[4 * j + 1],
+                               wv[4 * j + 2], wv[4 * j + 3]);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        const CUtensorMap* map = t ? tdk : tdv;
+                        const int col = cc_lo + c0;
+                        if constexpr (VARLEN)
+                            tma_store_5d(map, stg, col, w.g, kRaggedWindow - w.nk + w.k0 + wq * 32, w.kb + w.nk,
+                                         kRaggedWindow);
+                        else
+                            tma_store_3d(map, stg, col, w.k0 + wq * 32, w.b * p.Hkv + w.g);
+                        bulk_commit_group();
+                    }
+                }
+            }
+        } else {
 #pragma unroll 1
         for (int cc = cc_lo; cc < cc_hi; cc += 32) {
             uint32_t r[32];
@@ -651,17 +702,23 @@ __device__ void bwd_pds(int wq, int grp, int lane, uint8_t* smem, BwdBars* bars,
             for (int x = 0; x < 32; ++x) v[x] = __uint_as_float(r[x]) * p.scale;
             if (nc > 0) store_rows32_pairs<OUT_F32>(dk_base, wrow0, row_elems, cc, v, nc, rows_live, lane);
         }
+        }
         tc_fence_before();
         g += w.n_tiles;
         ++u;
     }
     if (!ok) bwd_abort(bars, err);
+    // every staged store has read shared memory and written global memory
+    // before the CTA may exit
+    if (lane == 0) bulk_wait_group_all();
+    __syncwarp();
 }
 
 template <int D, bool OUT_F32, bool VARLEN>
 __global__ void __launch_bounds__(kBwdThreadsEw, 1)
 attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                      const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
+                     const __grid_constant__ CUtensorMap tdk, const __grid_constant__ CUtensorMap tdv,
                      const BwdParams p, unsigned int* err) {
     using C = BwdCfg<D>;
     extern __shared__ uint8_t smem_raw[];
@@ -708,7 +765,8 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tq, const __grid_consta
 
     if (warp == 0) bwd_producer<D, VARLEN>(&tq, &tk, &tv, &tdo, smem, bars, p, n_items, err);
     else if (warp == 1) bwd_mma<D, VARLEN>(smem, bars, tmem, p, n_items, err);
-    else if (warp >= 4) bwd_pds<D, OUT_F32, VARLEN>(warp & 3, (warp - 4) >> 2, lane, smem, bars, tmem, p, n_items, err);
+    else if (warp >= 4)
+        bwd_pds<D, OUT_F32, VARLEN>(warp & 3, (warp - 4) >> 2, lane, smem, bars, tmem, &tdk, &tdv, p, n_items, err);
 
     tc_fence_before();
     __syncthreads();
@@ -1368,7 +1426,8 @@ attn_status_t launch_bwd_prep(const void* o, int o_f32, const void* dout, const 
 
 template <int D, bool OUT_F32, bool VARLEN = false>
 attn_status_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                           const CUtensorMap& tdo, const BwdParams& p, const void* o, int o_f32,
+                           const CUtensorMap& tdo, const CUtensorMap& tdk, const CUtensorMap& tdv,
+                           const BwdParams& p, const void* o, int o_f32,
                            const void* dout, const float* lse, float* lse2, float* dvec,
                            cudaStream_t stream, const DeviceInfo& dev) {
     static int attr_set[64] = {0};
@@ -1396,7 +1455,7 @@ attn_status_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const C
     const long long kv_items = (long long)p.B * p.Hkv * p.n_kt;
     const long long kv_ctas = kv_items < dev.num_sms ? kv_items : dev.num_sms;
     attn_bwd_dkdv_kernel<D, OUT_F32, VARLEN><<<(unsigned)kv_ctas, kBwdThreadsEw, BwdCfg<D>::kSmemBytes,
-                                               stream>>>(tq, tk, tv, tdo, p, dev.err_word);
+                                               stream>>>(tq, tk, tv, tdo, tdk, tdv, p, dev.err_word);
     if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
     const long long q_items = (long long)p.B * p.Hq * ((p.Nq + kBT - 1) / kBT);
     const long long q_ctas = q_items < dev.num_sms ? q_items : dev.num_sms;  // persistent, as above
@@ -2327,11 +2386,21 @@ attn_status_t launch_bwd_varlen(const void* q, const void* k, const void* v, con
                    : launch_bwd_wide_t<false, true>(tq, tk, tv, tdo, tq64, tk64, tv64, tdo64, p, o, o_f32,
                                                     dout, lse, lse2, dvec, stream, dev);
     }
-    if (pad_head_dim(d) == 128)
-        return g32 ? launch_bwd_t<128, true, true>(tq, tk, tv, tdo, p, o, o_f32, dout, lse, lse2, dvec, stream, dev)
-                   : launch_bwd_t<128, false, true>(tq, tk, tv, tdo, p, o, o_f32, dout, lse, lse2, dvec, stream, dev);
-    return g32 ? launch_bwd_t<64, true, true>(tq, tk, tv, tdo, p, o, o_f32, dout, lse, lse2, dvec, stream, dev)
-               : launch_bwd_t<64, false, true>(tq, tk, tv, tdo, p, o, o_f32, dout, lse, lse2, dvec, stream, dev);
+    // dK / dV output maps for the d = 128 kernel's staged stores: boxes of 32
+    // rows x 128 bytes (64 bf16 or 32 fp32 columns)
+    CUtensorMap tdk = tq, tdv = tq;
+    if (pad_head_dim(d) == 128) {
+        if ((st = encode_tmap_ragged(&tdk, dk, g32, d, Hkv, g32 ? 32 : 64, 32, true)) != ATTN_OK) return st;
+        if ((st = encode_tmap_ragged(&tdv, dv, g32, d, Hkv, g32 ? 32 : 64, 32, true)) != ATTN_OK) return st;
+        return g32 ? launch_bwd_t<128, true, true>(tq, tk, tv, tdo, tdk, tdv, p, o, o_f32, dout, lse, lse2, dvec,
+                                                   stream, dev)
+                   : launch_bwd_t<128, false, true>(tq, tk, tv, tdo, tdk, tdv, p, o, o_f32, dout, lse, lse2, dvec,
+                                                    stream, dev);
+    }
+    return g32 ? launch_bwd_t<64, true, true>(tq, tk, tv, tdo, tdk, tdv, p, o, o_f32, dout, lse, lse2, dvec, stream,
+                                              dev)
+               : launch_bwd_t<64, false, true>(tq, tk, tv, tdo, tdk, tdv, p, o, o_f32, dout, lse, lse2, dvec, stream,
+                                               dev);
 }
 
 size_t bwd_workspace_bytes(int B, int Hq, int Nq, int d) {
@@ -2401,12 +2470,24 @@ attn_status_t launch_bwd(const void* q, const void* k, const void* v, const void
                    : launch_bwd_wide_t<false>(tq, tk, tv, tdo, tq64, tk64, tv64, tdo64, p, o, o_f32,
                                               dout, lse, lse2, dvec, stream, dev);
     }
-    if (pad_head_dim(d) == 128)
-        return g32 ? launch_bwd_t<128, true>(tq, tk, tv, tdo, p, o, o_f32, dout, lse, lse2, dvec, stream, dev)
-                   : launch_bwd_t<128, false>(tq, tk, tv, tdo, p, o, o_f32, dout, lse, lse2, dvec, stream, dev);
+    if (pad_head_dim(d) == 128) {
+        // dK / dV output maps for the staged stores: boxes of 32 rows x 128 bytes
+        CUtensorMap tdk, tdv;
+        if (g32) {
+            if ((st = encode_tmap_f32_sw128_3d(&tdk, dk, d, Nk, (long long)B * Hkv, 32)) != ATTN_OK) return st;
+            if ((st = encode_tmap_f32_sw128_3d(&tdv, dv, d, Nk, (long long)B * Hkv, 32)) != ATTN_OK) return st;
+        } else {
+            if ((st = encode_tmap_bf16_3d(&tdk, dk, d, Nk, (long long)B * Hkv, 32)) != ATTN_OK) return st;
+            if ((st = encode_tmap_bf16_3d(&tdv, dv, d, Nk, (long long)B * Hkv, 32)) != ATTN_OK) return st;
+        }
+        return g32 ? launch_bwd_t<128, true>(tq, tk, tv, tdo, tdk, tdv, p, o, o_f32, dout, lse, lse2, dvec, stream,
+                                             dev)
+                   : launch_bwd_t<128, false>(tq, tk, tv, tdo, tdk, tdv, p, o, o_f32, dout, lse, lse2, dvec, stream,
+                                              dev);
+    }
     if (pad_head_dim(d) == 64)
-        return g32 ? launch_bwd_t<64, true>(tq, tk, tv, tdo, p, o, o_f32, dout, lse, lse2, dvec, stream, dev)
-                   : launch_bwd_t<64, false>(tq, tk, tv, tdo, p, o, o_f32, dout, lse, lse2, dvec, stream, dev);
+        return g32 ? launch_bwd_t<64, true>(tq, tk, tv, tdo, tq, tq, p, o, o_f32, dout, lse, lse2, dvec, stream, dev)
+                   : launch_bwd_t<64, false>(tq, tk, tv, tdo, tq, tq, p, o, o_f32, dout, lse, lse2, dvec, stream, dev);
     return ATTN_ERR_UNSUPPORTED;
 }
 
