@@ -24,7 +24,8 @@
 //                 tile's query columns per warpgroup; P^T and dS^T go to
 //                 TMEM as bf16 pairs)
 //          dV  += P^T dO,  dK += dS^T Q      (A from TMEM, B MN-major in smem)
-//        After the last tile dK (times scale) and dV are written once.
+//        After the last tile dK (times scale) and dV are written once (at
+//        d = 128 through tensor stores from each warp's 4 KiB of staging).
 //  dq    one item per (b, query head, 128-row Q tile), K/V tiles streamed
 //        through a ring.  Per K/V tile:
 //          S = Q K^T,  dP = dO V^T,  dS = P o (dP - D)  (one query row per
