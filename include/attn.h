@@ -242,14 +242,15 @@ size_t attn_bwd_workspace_size(int B, int Hq, int Hkv, int Nq, int Nk, int d);
  * Hq % Hkv == 0, causal needs Nq <= Nk).  d <= 128 runs on the kernels
  * described below; 128 < d <= 256 on kernels built for 256 columns with other
  * tile shapes (the dK/dV pass per 128 keys and per 128-column half of d over
- * 64-row Q tiles, the dQ pass per 128 query rows over 64-key tiles, each with
- * one shared-memory stage).  Pointers 16-byte aligned (lse 4-byte).  The caller owns every
+ * 64-row Q tiles, the dQ pass per 128 query rows over 64-key tiles, one CTA
+ * per item).  Pointers 16-byte aligned (lse 4-byte).  The caller owns every
  * buffer.  Three kernels run in order on `stream`: a per-row pass (D, the LSE
- * in base 2), a K/V-outer pass (one CTA per (b, KV head, 128-key tile): dK
+ * in base 2), a K/V-outer pass (an item per (b, KV head, 128-key tile): dK
  * and dV accumulated in tensor memory over the group's query heads and Q
- * tiles, written once) and a Q-outer pass (one CTA per (b, query head,
+ * tiles, written once) and a Q-outer pass (an item per (b, query head,
  * 128-row Q tile): dQ accumulated in tensor memory over the K/V tiles,
- * written once).  No atomics: every gradient is bit-identical from run to
+ * written once); for d <= 128 both passes run at most one CTA per SM, each
+ * CTA taking every (grid size)-th item.  No atomics: every gradient is bit-identical from run to
  * run.  S and dP are computed in both passes (lecture notes exercise 6).
  * Numerics: scores and all products accumulate in fp32; P and dS are rounded
  * to bf16 before the P.dO, dS.Q and dS.K products.  Returns ATTN_OK once the kernels are enqueued;
